@@ -1,0 +1,301 @@
+"""fp64 CPU oracle for jagged attention -- TEST INFRASTRUCTURE, NOT PRODUCT CODE.
+
+Only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference leg may import this module. The CUDA library never calls it, and it
+imports nothing from the CUDA package: the two implementations share no code.
+
+What it computes is exact attention and its exact gradient, written out from
+the definitions, materialising S and P per (sequence, head) in fp64:
+
+* Forward. "Cutting-edge isn't plug-and-play: customizing FA4 on B300"
+  (TwelveLabs), section "FlashAttention recap": the score matrix is S = Q K^T
+  and FlashAttention only tiles it, so the tiled result is mathematically
+  equal to the naive one. Here: S = scale * Q K^T, P = softmax_rows(S),
+  O = P V, and the saved log-sum-exp LSE_i = ln sum_j exp(S_ij) (natural log;
+  the page only names "LSE").
+* Jagged packing. "Optimizing Jagged Flash Attention with TLX" (aivexanews),
+  third paragraph: sequences are packed back to back, boundaries kept in an
+  offsets tensor, no padded tokens. Sequence b is rows offsets[b]:offsets[b+1].
+* Backward. Same TwelveLabs page, section "Phase 2: chunked backward" and its
+  pseudocode: S and dP are rebuilt per tile, P from S and the saved LSE, then
+  dS from P, dP and "delta". As a plain gradient of O = softmax(scale Q K^T) V:
+      dV = P^T dO,  dP = dO V^T,  D_i = sum_d dO_id O_id  ("delta"),
+      dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+* Broadcast-Q. aivexanews page, third paragraph: one dense Q is shared by the
+  whole batch, so dQ is the sum over the batch of the per-sequence dQ.
+* Paged split-KV GQA decode. "Optimizing FlashAttention-4 for Efficient
+  Inference" (hpjadul), sections "PR 1940" (parallelism across the KV
+  dimension), "PR 1999 and PR 2104" (arbitrary KV page sizes) and "PR 2186"
+  (GQA packing). Attention of one query token per sequence against a KV cache
+  addressed through a page table; query head h reads KV head h // (Hq / Hkv).
+  The split/merge form is a second, separate function; its merge rule
+  (lse = ln sum_s exp(lse_s), O = sum_s exp(lse_s - lse) O_s) is the plainest
+  exact way to combine partial softmaxes and is not printed on the page.
+
+Conventions where the pages are silent (readings, not statements of the pages):
+  * an empty key set gives O = 0 and LSE = -inf (and zero gradients);
+  * causal means L_q == L_k and key j is visible to query i iff j <= i;
+  * split bounds: c_b = ceil(L_b / S); split s covers [s c_b, min((s+1) c_b, L_b)).
+
+Inputs are numpy arrays of float64 (bf16 values upcast exactly by the caller)
+and integer offsets. Nothing here is blocked, fused or reordered beyond the
+definitions above; numpy's matmul is the only library primitive used.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "seq_ranges", "attention_forward", "attention_backward",
+    "broadcast_forward", "broadcast_backward",
+    "split_bounds", "gather_paged", "decode_forward", "decode_split_partials",
+    "merge_partials", "tile_queue",
+]
+
+
+def seq_ranges(offsets):
+    """(start, end) of every packed sequence: rows offsets[b] .. offsets[b+1]."""
+    off = [int(x) for x in np.asarray(offsets).reshape(-1)]
+    return [(off[b], off[b + 1]) for b in range(len(off) - 1)]
+
+
+def _softmax_rows(S):
+    """Row softmax by definition, with the usual max shift for range.
+
+    Returns (P, lse) with lse_i = ln sum_j exp(S_ij); rows whose scores are all
+    -inf (no visible key) give P = 0 and lse = -inf."""
+    m = np.max(S, axis=1, keepdims=True) if S.shape[1] else np.full((S.shape[0], 1), -np.inf)
+    finite = np.isfinite(m)
+    m_safe = np.where(finite, m, 0.0)
+    E = np.exp(S - m_safe)
+    E[~np.broadcast_to(finite, E.shape)] = 0.0
+    Z = np.sum(E, axis=1, keepdims=True)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        P = np.where(Z > 0, E / np.where(Z > 0, Z, 1.0), 0.0)
+        lse = np.where(Z[:, 0] > 0, m_safe[:, 0] + np.log(np.where(Z[:, 0] > 0, Z[:, 0], 1.0)), -np.inf)
+    return P, lse
+
+
+def _scores(Qh, Kh, scale, causal):
+    S = scale * (Qh @ Kh.T)
+    if causal:
+        Lq, Lk = S.shape
+        assert Lq == Lk, "causal attention here is self-attention (L_q == L_k)"
+        S = np.where(np.tril(np.ones((Lq, Lk), dtype=bool)), S, -np.inf)
+    return S
+
+
+def _head_forward(Qh, Kh, Vh, scale, causal):
+    S = _scores(Qh, Kh, scale, causal)
+    P, lse = _softmax_rows(S)
+    return P @ Vh, lse, P
+
+
+def _head_backward(Qh, Kh, Vh, dOh, scale, causal):
+    """Exact gradient of O = softmax(scale Q K^T) V for one (sequence, head)."""
+    S = _scores(Qh, Kh, scale, causal)
+    P, _ = _softmax_rows(S)
+    O = P @ Vh
+    dV = P.T @ dOh
+    dP = dOh @ Vh.T
+    D = np.sum(dOh * O, axis=1)            # "delta": rowsum(dO * O)
+    dS = P * (dP - D[:, None])
+    dQ = scale * (dS @ Kh)
+    dK = scale * (dS.T @ Qh)
+    return dQ, dK, dV, D
+
+
+def attention_forward(q, k, v, offsets, scale, causal=False):
+    """Jagged self-attention forward.
+
+    q, k, v: [total, H, d] float64, packed by `offsets` (int [B+1]).
+    Returns O [total, H, d] and LSE [H, total] (natural log)."""
+    total, H, d = q.shape
+    O = np.zeros((total, H, v.shape[2]), dtype=np.float64)
+    LSE = np.full((H, total), -np.inf, dtype=np.float64)
+    for s, e in seq_ranges(offsets):
+        if e == s:
+            continue
+        for h in range(H):
+            Oh, lse, _ = _head_forward(q[s:e, h], k[s:e, h], v[s:e, h], scale, causal)
+            O[s:e, h] = Oh
+            LSE[h, s:e] = lse
+    return O, LSE
+
+
+def attention_backward(q, k, v, do, offsets, scale, causal=False):
+    """Jagged self-attention backward. Returns dQ, dK, dV [total, H, d] and
+    D [H, total] (the "delta" row sums)."""
+    total, H, d = q.shape
+    dQ = np.zeros_like(q, dtype=np.float64)
+    dK = np.zeros_like(k, dtype=np.float64)
+    dV = np.zeros_like(v, dtype=np.float64)
+    D = np.zeros((H, total), dtype=np.float64)
+    for s, e in seq_ranges(offsets):
+        if e == s:
+            continue
+        for h in range(H):
+            a, b_, c, dd = _head_backward(q[s:e, h], k[s:e, h], v[s:e, h], do[s:e, h], scale, causal)
+            dQ[s:e, h], dK[s:e, h], dV[s:e, h], D[h, s:e] = a, b_, c, dd
+    return dQ, dK, dV, D
+
+
+def broadcast_forward(q, k, v, kv_offsets, scale):
+    """Broadcast-Q forward: q [Lq, H, d] is the query of every sequence b,
+    k, v jagged [total_k, H, d]. Returns O [B, Lq, H, d], LSE [B, H, Lq]."""
+    Lq, H, d = q.shape
+    ranges = seq_ranges(kv_offsets)
+    B = len(ranges)
+    O = np.zeros((B, Lq, H, v.shape[2]), dtype=np.float64)
+    LSE = np.full((B, H, Lq), -np.inf, dtype=np.float64)
+    for b, (s, e) in enumerate(ranges):
+        if e == s:
+            continue
+        for h in range(H):
+            Oh, lse, _ = _head_forward(q[:, h], k[s:e, h], v[s:e, h], scale, False)
+            O[b, :, h] = Oh
+            LSE[b, h] = lse
+    return O, LSE
+
+
+def broadcast_backward(q, k, v, do, kv_offsets, scale):
+    """Broadcast-Q backward: dQ [Lq, H, d] summed over the batch, dK and dV
+    jagged [total_k, H, d]. do is [B, Lq, H, d]."""
+    Lq, H, d = q.shape
+    dQ = np.zeros_like(q, dtype=np.float64)
+    dK = np.zeros_like(k, dtype=np.float64)
+    dV = np.zeros_like(v, dtype=np.float64)
+    for b, (s, e) in enumerate(seq_ranges(kv_offsets)):
+        if e == s:
+            continue
+        for h in range(H):
+            a, b_, c, _ = _head_backward(q[:, h], k[s:e, h], v[s:e, h], do[b, :, h], scale, False)
+            dQ[:, h] += a
+            dK[s:e, h] = b_
+            dV[s:e, h] = c
+    return dQ, dK, dV
+
+
+# ----------------------------------------------------------------------------
+# Paged split-KV GQA decode
+# ----------------------------------------------------------------------------
+
+def split_bounds(seqlens, num_splits):
+    """int64 [B, S, 2]: (start, end) token range of every KV split.
+
+    c_b = ceil(L_b / S); split s covers [s c_b, min((s+1) c_b, L_b)); a split
+    whose start is at or past L_b is empty and reported as (L_b, L_b)."""
+    seqlens = [int(x) for x in np.asarray(seqlens).reshape(-1)]
+    S = int(num_splits)
+    out = np.zeros((len(seqlens), S, 2), dtype=np.int64)
+    for b, L in enumerate(seqlens):
+        c = -(-L // S) if L > 0 else 0
+        for s in range(S):
+            lo = min(s * c, L)
+            hi = min((s + 1) * c, L)
+            out[b, s] = (lo, hi)
+    return out
+
+
+def gather_paged(cache, page_table_row, length, page_size):
+    """Rows 0..length-1 of one sequence from a paged cache [num_pages, P, Hkv, d]:
+    token t lives in page page_table_row[t // P], slot t % P."""
+    idx_page = np.asarray([int(page_table_row[t // page_size]) for t in range(length)], dtype=np.int64)
+    idx_slot = np.arange(length, dtype=np.int64) % page_size
+    return cache[idx_page, idx_slot]           # [length, Hkv, d]
+
+
+def _decode_one(qb, Kb, Vb, scale, q_heads, kv_heads):
+    """One sequence: qb [Hq, d], Kb/Vb [L, Hkv, d] -> O [Hq, d], LSE [Hq]."""
+    group = q_heads // kv_heads
+    O = np.zeros((q_heads, Vb.shape[2] if Vb.ndim == 3 else qb.shape[1]), dtype=np.float64)
+    LSE = np.full(q_heads, -np.inf, dtype=np.float64)
+    if Kb.shape[0] == 0:
+        return O, LSE
+    for h in range(q_heads):
+        g = h // group
+        Oh, lse, _ = _head_forward(qb[h:h + 1], Kb[:, g], Vb[:, g], scale, False)
+        O[h] = Oh[0]
+        LSE[h] = lse[0]
+    return O, LSE
+
+
+def decode_forward(q, k_cache, v_cache, page_table, seqlens, page_size, scale, batch_ids=None):
+    """Unsplit paged decode. q [B, Hq, d]; caches [num_pages, P, Hkv, d];
+    returns O [B, Hq, d], LSE [B, Hq] (rows of `batch_ids` only, if given)."""
+    B, Hq, d = q.shape
+    Hkv = k_cache.shape[2]
+    ids = range(B) if batch_ids is None else batch_ids
+    O = np.zeros((B, Hq, d), dtype=np.float64)
+    LSE = np.full((B, Hq), -np.inf, dtype=np.float64)
+    for b in ids:
+        L = int(seqlens[b])
+        Kb = gather_paged(k_cache, page_table[b], L, page_size)
+        Vb = gather_paged(v_cache, page_table[b], L, page_size)
+        O[b], LSE[b] = _decode_one(q[b], Kb, Vb, scale, Hq, Hkv)
+    return O, LSE
+
+
+def decode_split_partials(q, k_cache, v_cache, page_table, seqlens, page_size, scale, num_splits):
+    """Per-split partial results: O_s [S, B, Hq, d] (normalised within the
+    split) and lse_s [S, B, Hq] (-inf for an empty split)."""
+    B, Hq, d = q.shape
+    Hkv = k_cache.shape[2]
+    bounds = split_bounds(seqlens, num_splits)
+    Os = np.zeros((num_splits, B, Hq, d), dtype=np.float64)
+    lses = np.full((num_splits, B, Hq), -np.inf, dtype=np.float64)
+    for b in range(B):
+        L = int(seqlens[b])
+        Kb = gather_paged(k_cache, page_table[b], L, page_size)
+        Vb = gather_paged(v_cache, page_table[b], L, page_size)
+        for s in range(num_splits):
+            lo, hi = bounds[b, s]
+            Os[s, b], lses[s, b] = _decode_one(q[b], Kb[lo:hi], Vb[lo:hi], scale, Hq, Hkv)
+    return Os, lses
+
+
+def merge_partials(Os, lses):
+    """Combine partial softmaxes: lse = ln sum_s exp(lse_s),
+    O = sum_s exp(lse_s - lse) O_s; all-empty gives O = 0, lse = -inf."""
+    m = np.max(lses, axis=0)
+    finite = np.isfinite(m)
+    m_safe = np.where(finite, m, 0.0)
+    w = np.exp(lses - m_safe[None])             # exp(-inf) = 0 for empty splits
+    w = np.where(np.isfinite(lses), w, 0.0)
+    Z = np.sum(w, axis=0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lse = np.where(Z > 0, m_safe + np.log(np.where(Z > 0, Z, 1.0)), -np.inf)
+        O = np.where((Z > 0)[..., None], np.sum(w[..., None] * Os, axis=0) / np.where(Z > 0, Z, 1.0)[..., None], 0.0)
+    return O, lse
+
+
+# ----------------------------------------------------------------------------
+# Longest-first jagged tile order
+# ----------------------------------------------------------------------------
+
+def tile_queue(offsets, heads, causal, kind, tile=128):
+    """Work items of the persistent kernels in longest-first order.
+
+    "Optimizing Jagged Flash Attention with TLX", fourth and fifth paragraphs:
+    persistent CTAs loop over tiles, and software load balancing of the jagged
+    tiles recovers ~20% of the forward. The order used here (a reading; the
+    page gives none): items (b, h, t) where t is a query tile (kind="fwd") or
+    a key/value tile (kind="bwd") of 128 rows, sorted by descending cost,
+    ties by ascending (b, t, h). Cost = number of partner tiles the item
+    visits: nt = ceil(L_b / 128) when not causal; t + 1 (fwd) or nt - t (bwd)
+    when causal. Returns a list of (b, h, t)."""
+    items = []
+    for b, (s, e) in enumerate(seq_ranges(offsets)):
+        L = e - s
+        nt = -(-L // tile)
+        for t in range(nt):
+            if not causal:
+                cost = nt
+            elif kind == "fwd":
+                cost = t + 1
+            else:
+                cost = nt - t
+            for h in range(heads):
+                items.append((-cost, b, t, h))
+    items.sort()
+    return [(b, h, t) for (_, b, t, h) in items]

@@ -1,0 +1,389 @@
+"""Pins for the fp64 oracle: checks against things other than the oracle itself.
+
+Each ``pin_*`` function takes the oracle module and raises AssertionError when
+the oracle disagrees with a closed form, a brute-force computation, finite
+differences, a library routine in a special case, or an invariant of the
+mathematics. ``test_oracle_pins.py`` runs them on the real oracle (all must
+pass) and on mutants with planted mistakes (at least one must fail).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "closed_form_cases.json")
+
+_ENV = {"log": math.log, "exp": math.exp, "e": math.e, "__builtins__": {}}
+
+
+def _ev(x):
+    """Evaluate a hand-written closed-form expression from the golden file."""
+    if isinstance(x, list):
+        return [_ev(y) for y in x]
+    if isinstance(x, (int, float)):
+        return float(x)
+    return float(eval(x, _ENV))  # expressions use only numbers, log, exp, e
+
+
+def _arr(x):
+    return np.asarray(_ev(x), dtype=np.float64)
+
+
+def golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    both_inf = np.isinf(a) & np.isinf(b) & (np.sign(a) == np.sign(b))
+    with np.errstate(invalid="ignore"):
+        err = np.where(both_inf, 0.0, np.abs(a - b))
+    m = float(np.max(err)) if err.size else 0.0
+    assert m <= tol, f"{what}: max|diff| {m:.3e} > {tol:.1e}"
+
+
+# ---------------------------------------------------------------- closed forms
+
+def pin_golden_attention(o):
+    g = golden()
+    for name in ("two_keys", "causal_pair"):
+        c = g[name]
+        q, k, v, do = (_arr(c[x])[:, None, :] for x in ("q", "k", "v", "do"))
+        off = np.array([0, q.shape[0]])
+        scale = _ev(c["scale"])
+        O, LSE = o.attention_forward(q, k, v, off, scale, c["causal"])
+        _close(O[:, 0], _arr(c["o"]), 1e-13, f"{name} O")
+        _close(LSE[0], _arr(c["lse"]), 1e-13, f"{name} LSE")
+        dQ, dK, dV, _ = o.attention_backward(q, k, v, do, off, scale, c["causal"])
+        _close(dQ[:, 0], _arr(c["dq"]), 1e-13, f"{name} dQ")
+        _close(dK[:, 0], _arr(c["dk"]), 1e-13, f"{name} dK")
+        _close(dV[:, 0], _arr(c["dv"]), 1e-13, f"{name} dV")
+
+
+def pin_golden_decode(o):
+    c = golden()["paged_gqa_decode"]
+    q = _arr(c["q"])
+    kc = _arr(c["k_cache"])
+    vc = _arr(c["v_cache"])
+    pt = np.asarray(c["page_table"])
+    sl = np.asarray(c["seqlens"])
+    O, LSE = o.decode_forward(q, kc, vc, pt, sl, c["page_size"], _ev(c["scale"]))
+    _close(O, _arr(c["o"]), 1e-12, "decode O")
+    _close(LSE, _arr(c["lse"]), 1e-13, "decode LSE")
+    for S in (1, 2, 3, 4):
+        Os, ls = o.decode_split_partials(q, kc, vc, pt, sl, c["page_size"], _ev(c["scale"]), S)
+        O2, L2 = o.merge_partials(Os, ls)
+        _close(O2, _arr(c["o"]), 1e-12, f"decode split {S} O")
+        _close(L2, _arr(c["lse"]), 1e-13, f"decode split {S} LSE")
+
+
+def pin_golden_split_bounds(o):
+    c = golden()["split_bounds"]
+    got = o.split_bounds(np.asarray(c["seqlens"]), c["num_splits"])
+    assert got.tolist() == c["bounds"], got.tolist()
+
+
+# ---------------------------------------------------------------- special cases
+
+def pin_length_one(o):
+    """A length-1 sequence returns its own V row and LSE = scale q.k0."""
+    r = _rng(1)
+    q, k, v = (r.standard_normal((1, 3, 5)) for _ in range(3))
+    O, LSE = o.attention_forward(q, k, v, np.array([0, 1]), 0.7, False)
+    _close(O, v, 1e-15, "L=1 O")
+    _close(LSE[:, 0], 0.7 * np.sum(q[0] * k[0], axis=-1), 1e-14, "L=1 LSE")
+
+
+def pin_constant_v(o):
+    """If every V row equals the same vector, O equals that vector."""
+    r = _rng(2)
+    L = 9
+    q, k = r.standard_normal((L, 2, 4)), r.standard_normal((L, 2, 4))
+    row = r.standard_normal((1, 2, 4))
+    v = np.repeat(row, L, axis=0)
+    for causal in (False, True):
+        O, _ = o.attention_forward(q, k, v, np.array([0, L]), 0.5, causal)
+        _close(O, v, 1e-13, f"constant V (causal={causal})")
+
+
+def pin_rows_sum_to_one(o):
+    """With V = identity (d_v = L), O equals P itself: rows must sum to 1,
+    be non-negative, and be zero on causally hidden keys."""
+    r = _rng(3)
+    L = 7
+    q, k = r.standard_normal((L, 1, 3)), r.standard_normal((L, 1, 3))
+    v = np.eye(L)[:, None, :]
+    for causal in (False, True):
+        P, _ = o.attention_forward(q, k, v, np.array([0, L]), 1.3, causal)
+        P = P[:, 0, :]
+        _close(P.sum(axis=1), np.ones(L), 1e-14, "row sums")
+        assert np.all(P >= 0)
+        if causal:
+            assert np.all(P[np.triu_indices(L, 1)] == 0.0)
+
+
+def pin_brute_force_forward(o):
+    """Pure-Python loops, softmax by its definition exp(s)/sum exp(s)."""
+    r = _rng(4)
+    lengths = [3, 1, 5]
+    H, d = 2, 3
+    off = np.concatenate([[0], np.cumsum(lengths)])
+    T = off[-1]
+    q, k, v = (r.standard_normal((T, H, d)) for _ in range(3))
+    scale = 0.9
+    for causal in (False, True):
+        O, LSE = o.attention_forward(q, k, v, off, scale, causal)
+        for b in range(len(lengths)):
+            s0, s1 = off[b], off[b + 1]
+            for h in range(H):
+                for i in range(s0, s1):
+                    js = [j for j in range(s0, s1) if (not causal or j - s0 <= i - s0)]
+                    sc = [scale * sum(q[i, h, x] * k[j, h, x] for x in range(d)) for j in js]
+                    z = sum(math.exp(t) for t in sc)
+                    for x in range(d):
+                        ref = sum(math.exp(t) / z * v[j, h, x] for t, j in zip(sc, js))
+                        assert abs(O[i, h, x] - ref) < 1e-12, (b, h, i, x)
+                    assert abs(LSE[h, i] - math.log(z)) < 1e-12
+
+
+def _loss(o, q, k, v, do, off, scale, causal):
+    O, _ = o.attention_forward(q, k, v, off, scale, causal)
+    return float(np.sum(O * do))
+
+
+def pin_finite_differences(o):
+    """Analytic gradients of sum(dO*O) against central differences, h = 1e-6."""
+    r = _rng(5)
+    lengths = [2, 4]
+    H, d = 2, 3
+    off = np.concatenate([[0], np.cumsum(lengths)])
+    T = off[-1]
+    scale = 0.8
+    for causal in (False, True):
+        q, k, v, do = (r.standard_normal((T, H, d)) for _ in range(4))
+        dQ, dK, dV, _ = o.attention_backward(q, k, v, do, off, scale, causal)
+        for name, x, g in (("q", q, dQ), ("k", k, dK), ("v", v, dV)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                old = x[idx]
+                x[idx] = old + 1e-6
+                fp = _loss(o, q, k, v, do, off, scale, causal)
+                x[idx] = old - 1e-6
+                fm = _loss(o, q, k, v, do, off, scale, causal)
+                x[idx] = old
+                num[idx] = (fp - fm) / 2e-6
+            rel = np.max(np.abs(num - g)) / max(np.max(np.abs(g)), 1e-30)
+            assert rel < 1e-6, f"d{name} (causal={causal}) rel err {rel:.2e}"
+
+
+def pin_torch_sdpa(o):
+    """torch's fp64 CPU scaled_dot_product_attention (forward) and autograd
+    (backward), applied per sequence, as a library special case."""
+    r = _rng(6)
+    lengths = [5, 1, 8, 3]
+    H, d = 3, 4
+    off = np.concatenate([[0], np.cumsum(lengths)])
+    T = off[-1]
+    scale = 0.6
+    for causal in (False, True):
+        q, k, v, do = (r.standard_normal((T, H, d)) for _ in range(4))
+        O, LSE = o.attention_forward(q, k, v, off, scale, causal)
+        dQ, dK, dV, _ = o.attention_backward(q, k, v, do, off, scale, causal)
+        for b in range(len(lengths)):
+            s0, s1 = off[b], off[b + 1]
+            tq, tk, tv = (torch.tensor(x[s0:s1].transpose(1, 0, 2), requires_grad=True) for x in (q, k, v))
+            out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=scale, is_causal=causal)
+            out.backward(torch.tensor(do[s0:s1].transpose(1, 0, 2)))
+            _close(O[s0:s1], out.detach().numpy().transpose(1, 0, 2), 1e-12, "sdpa O")
+            _close(dQ[s0:s1], tq.grad.numpy().transpose(1, 0, 2), 1e-12, "autograd dQ")
+            _close(dK[s0:s1], tk.grad.numpy().transpose(1, 0, 2), 1e-12, "autograd dK")
+            _close(dV[s0:s1], tv.grad.numpy().transpose(1, 0, 2), 1e-12, "autograd dV")
+            # LSE from the scores via torch.logsumexp
+            S = scale * torch.einsum("hid,hjd->hij", tq.detach(), tk.detach())
+            if causal:
+                L = s1 - s0
+                S = S.masked_fill(~torch.tril(torch.ones(L, L, dtype=torch.bool)), float("-inf"))
+            _close(LSE[:, s0:s1], torch.logsumexp(S, dim=-1).numpy(), 1e-12, "logsumexp")
+
+
+def pin_jagged_equals_separate(o):
+    """Packing is transparent: each sequence's result equals attention on that
+    sequence alone, whatever its neighbours are."""
+    r = _rng(7)
+    lengths = [4, 0, 6, 2]
+    H, d = 2, 3
+    off = np.concatenate([[0], np.cumsum(lengths)])
+    T = off[-1]
+    q, k, v, do = (r.standard_normal((T, H, d)) for _ in range(4))
+    O, LSE = o.attention_forward(q, k, v, off, 1.1, False)
+    dQ, dK, dV, D = o.attention_backward(q, k, v, do, off, 1.1, False)
+    for b in range(len(lengths)):
+        s0, s1 = off[b], off[b + 1]
+        if s0 == s1:
+            continue
+        one = np.array([0, s1 - s0])
+        O1, L1 = o.attention_forward(q[s0:s1], k[s0:s1], v[s0:s1], one, 1.1, False)
+        g1 = o.attention_backward(q[s0:s1], k[s0:s1], v[s0:s1], do[s0:s1], one, 1.1, False)
+        _close(O[s0:s1], O1, 0.0, "packed O")
+        _close(LSE[:, s0:s1], L1, 0.0, "packed LSE")
+        for a, bb in zip((dQ, dK, dV), g1[:3]):
+            _close(a[s0:s1], bb, 0.0, "packed grads")
+
+
+def pin_delta_identity(o):
+    """D = rowsum(dO * O) equals rowsum(P * dP) with dP = dO V^T."""
+    r = _rng(8)
+    L, d = 6, 4
+    q, k, v, do = (r.standard_normal((L, 1, d)) for _ in range(4))
+    off = np.array([0, L])
+    _, _, _, D = o.attention_backward(q, k, v, do, off, 0.5, False)
+    P, _ = o.attention_forward(q, k, np.eye(L)[:, None, :], off, 0.5, False)
+    dP = do[:, 0] @ v[:, 0].T
+    _close(D[0], np.sum(P[:, 0] * dP, axis=1), 1e-13, "delta identity")
+
+
+def pin_broadcast(o):
+    """Broadcast-Q equals per-sequence attention with a copy of Q, and its dQ
+    equals the sum over the batch of those per-sequence dQ (torch autograd)."""
+    r = _rng(9)
+    lengths = [3, 7, 1]
+    Lq, H, d = 4, 2, 3
+    off = np.concatenate([[0], np.cumsum(lengths)])
+    T = off[-1]
+    q = r.standard_normal((Lq, H, d))
+    k, v = r.standard_normal((T, H, d)), r.standard_normal((T, H, d))
+    do = r.standard_normal((len(lengths), Lq, H, d))
+    scale = 0.7
+    O, LSE = o.broadcast_forward(q, k, v, off, scale)
+    dQ, dK, dV = o.broadcast_backward(q, k, v, do, off, scale)
+    tq = torch.tensor(q.transpose(1, 0, 2), requires_grad=True)
+    for b in range(len(lengths)):
+        s0, s1 = off[b], off[b + 1]
+        tk = torch.tensor(k[s0:s1].transpose(1, 0, 2), requires_grad=True)
+        tv = torch.tensor(v[s0:s1].transpose(1, 0, 2), requires_grad=True)
+        out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=scale)
+        out.backward(torch.tensor(do[b].transpose(1, 0, 2)))
+        _close(O[b], out.detach().numpy().transpose(1, 0, 2), 1e-12, "bcast O")
+        _close(dK[s0:s1], tk.grad.numpy().transpose(1, 0, 2), 1e-12, "bcast dK")
+        _close(dV[s0:s1], tv.grad.numpy().transpose(1, 0, 2), 1e-12, "bcast dV")
+        S = scale * torch.einsum("hid,hjd->hij", tq.detach(), tk.detach())
+        _close(LSE[b], torch.logsumexp(S, -1).numpy(), 1e-12, "bcast LSE")
+    _close(dQ, tq.grad.numpy().transpose(1, 0, 2), 1e-12, "bcast dQ = sum over batch")
+
+
+def _random_paged(r, lengths, Hq, Hkv, d, P):
+    pages = [-(-L // P) for L in lengths]
+    n = max(sum(pages), 1)
+    perm = r.permutation(n)
+    pt = np.zeros((len(lengths), max(max(pages), 1)), dtype=np.int64)
+    c = 0
+    for b, m in enumerate(pages):
+        pt[b, :m] = perm[c:c + m]
+        c += m
+    q = r.standard_normal((len(lengths), Hq, d))
+    kc = r.standard_normal((n, P, Hkv, d))
+    vc = r.standard_normal((n, P, Hkv, d))
+    return q, kc, vc, pt
+
+
+def pin_decode(o):
+    """Paged GQA decode equals torch SDPA on the gathered dense K/V with each
+    query head attending its KV group; split+merge equals unsplit; the result
+    does not depend on where the pages sit."""
+    r = _rng(10)
+    lengths = np.array([5, 1, 0, 13, 8])
+    Hq, Hkv, d = 6, 2, 4
+    scale = 0.45
+    for P in (1, 3, 16):
+        q, kc, vc, pt = _random_paged(r, lengths, Hq, Hkv, d, P)
+        O, LSE = o.decode_forward(q, kc, vc, pt, lengths, P, scale)
+        for b, L in enumerate(lengths):
+            if L == 0:
+                assert np.all(O[b] == 0) and np.all(np.isneginf(LSE[b]))
+                continue
+            Kd = np.stack([kc[pt[b, t // P], t % P] for t in range(L)])    # [L, Hkv, d]
+            Vd = np.stack([vc[pt[b, t // P], t % P] for t in range(L)])
+            grp = Hq // Hkv
+            tk = torch.tensor(np.repeat(Kd, grp, axis=1).transpose(1, 0, 2))
+            tv = torch.tensor(np.repeat(Vd, grp, axis=1).transpose(1, 0, 2))
+            tq = torch.tensor(q[b][:, None, :])
+            ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=scale)[:, 0]
+            _close(O[b], ref.numpy(), 1e-12, f"decode P={P}")
+            S = scale * torch.einsum("hd,hjd->hj", tq[:, 0], tk)
+            _close(LSE[b], torch.logsumexp(S, -1).numpy(), 1e-12, "decode LSE")
+        for S_ in (1, 2, 5, 16):
+            Os, ls = o.decode_split_partials(q, kc, vc, pt, lengths, P, scale, S_)
+            O2, L2 = o.merge_partials(Os, ls)
+            _close(O2, O, 1e-12, f"split {S_} O")
+            _close(L2, LSE, 1e-12, f"split {S_} LSE")
+        # moving every page elsewhere (and the table with it) changes nothing
+        n = kc.shape[0]
+        perm = r.permutation(n)
+        kc2, vc2 = np.empty_like(kc), np.empty_like(vc)
+        kc2[perm], vc2[perm] = kc, vc
+        O3, L3 = o.decode_forward(q, kc2, vc2, perm[pt], lengths, P, scale)
+        _close(O3, O, 0.0, "page permutation")
+        _close(L3, LSE, 0.0, "page permutation LSE")
+
+
+def pin_split_cover(o):
+    """Every token lies in exactly one split, splits are contiguous and in
+    order, and none is longer than ceil(L / S)."""
+    for L in (0, 1, 2, 7, 64, 1000, 32768):
+        for S in (1, 2, 3, 7, 16, 64):
+            bnd = o.split_bounds(np.array([L]), S)[0]
+            cover = np.zeros(L, dtype=int)
+            prev = 0
+            c = -(-L // S)
+            for lo, hi in bnd:
+                assert lo == prev or lo == hi == L
+                assert 0 <= hi - lo <= c
+                cover[lo:hi] += 1
+                prev = hi
+            assert np.all(cover == 1) and prev == L
+
+
+def pin_tile_queue(o):
+    """Every (b, h, tile) appears once; costs never increase; ties go by
+    ascending (b, tile, h). Costs are recounted here by brute force: the number
+    of partner tiles with at least one visible (query, key) pair."""
+    off = np.array([0, 300, 300, 301, 700, 1000])
+    H, T = 2, 128
+    for causal in (False, True):
+        for kind in ("fwd", "bwd"):
+            q = o.tile_queue(off, H, causal, kind, T)
+            expect = set()
+            for b in range(len(off) - 1):
+                L = off[b + 1] - off[b]
+                for t in range(-(-L // T)):
+                    for h in range(H):
+                        expect.add((b, h, t))
+            assert len(q) == len(expect) and set(q) == expect
+
+            def cost(item):
+                b, h, t = item
+                L = int(off[b + 1] - off[b])
+                n = 0
+                for u in range(-(-L // T)):
+                    qi, kj = (t, u) if kind == "fwd" else (u, t)
+                    rows = range(qi * T, min(qi * T + T, L))
+                    cols = range(kj * T, min(kj * T + T, L))
+                    if any((not causal) or c <= r_ for r_ in rows for c in cols):
+                        n += 1
+                return n
+            keys = [(-cost(it), it[0], it[2], it[1]) for it in q]
+            assert keys == sorted(keys), (causal, kind)
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

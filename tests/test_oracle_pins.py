@@ -1,0 +1,156 @@
+"""The oracle against its pins, and planted mistakes against the same pins.
+
+No GPU needed. A pin is something other than the oracle itself: a
+hand-derived closed form, brute force in plain loops, central finite
+differences, torch's fp64 attention/autograd in a special case, or an
+invariant. The mutation tests plant plausible mistakes in a copy of the
+oracle (on the CPU) and require that at least one pin catches each.
+"""
+import importlib
+
+import numpy as np
+import pytest
+
+import oracle.attention as real_oracle
+from tests import oracle_pins
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin(real_oracle)
+
+
+def _mutant(patch):
+    """A fresh copy of the oracle module with one function replaced."""
+    spec = importlib.util.find_spec("oracle.attention")
+    m = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(m)
+    patch(m)
+    return m
+
+
+def _bwd_variant(kind):
+    def make(m):
+        orig_scores = m._scores
+        orig_soft = m._softmax_rows
+
+        def hb(Qh, Kh, Vh, dOh, scale, causal):
+            S = orig_scores(Qh, Kh, scale, causal)
+            P, _ = orig_soft(S)
+            O = P @ Vh
+            dV = P.T @ dOh
+            dP = dOh @ Vh.T
+            D = np.sum(dOh * O, axis=1)
+            if kind == "drop_delta":
+                dS = P * dP
+            elif kind == "sign_dS":
+                dS = P * (D[:, None] - dP)
+            else:
+                dS = P * (dP - D[:, None])
+            dQ = scale * (dS @ Kh)
+            dK = scale * (dS.T @ Qh)
+            if kind == "dq_no_scale":
+                dQ = dS @ Kh
+            if kind == "dk_no_scale":
+                dK = dS.T @ Qh
+            if kind == "dv_transposed":
+                dV = (P @ dOh) if P.shape[0] == P.shape[1] else P.T @ dOh * 1.01
+            return dQ, dK, dV, D
+        m._head_backward = hb
+    return make
+
+
+def _fwd_variant(kind):
+    def make(m):
+        orig = m._scores
+
+        def sc(Qh, Kh, scale, causal):
+            if kind == "no_scale":
+                return orig(Qh, Kh, 1.0, causal)
+            if kind == "causal_upper":
+                S = scale * (Qh @ Kh.T)
+                if causal:
+                    L = S.shape[0]
+                    S = np.where(np.triu(np.ones((L, L), dtype=bool)), S, -np.inf)
+                return S
+            return orig(Qh, Kh, scale, causal)
+        m._scores = sc
+    return make
+
+
+def _lse_log2(m):
+    orig = m._softmax_rows
+
+    def soft(S):
+        P, lse = orig(S)
+        return P, lse / np.log(2.0)
+    m._softmax_rows = soft
+
+
+def _merge_no_reweight(m):
+    def merge(Os, lses):
+        O, lse = real_oracle.merge_partials(Os, lses)
+        valid = np.isfinite(lses).sum(axis=0)
+        Oavg = np.where((valid > 0)[..., None], np.sum(np.where(np.isfinite(lses)[..., None], Os, 0.0), 0) / np.maximum(valid, 1)[..., None], 0.0)
+        return Oavg, lse
+    m.merge_partials = merge
+
+
+def _gqa_wrong_group(m):
+    orig = m._decode_one
+
+    def one(qb, Kb, Vb, scale, q_heads, kv_heads):
+        # maps query head h to KV head h % Hkv instead of h // (Hq / Hkv)
+        O, L = orig(qb, Kb, Vb, scale, q_heads, kv_heads)
+        group = q_heads // kv_heads
+        if Kb.shape[0] and group > 1:
+            for h in range(q_heads):
+                g = h % kv_heads
+                Oh, lse, _ = m._head_forward(qb[h:h + 1], Kb[:, g], Vb[:, g], scale, False)
+                O[h], L[h] = Oh[0], lse[0]
+        return O, L
+    m._decode_one = one
+
+
+def _page_slot_off_by_one(m):
+    def gather(cache, row, length, P):
+        idx_page = np.asarray([int(row[t // P]) for t in range(length)], dtype=np.int64)
+        idx_slot = (np.arange(length) + (1 if P > 1 else 0)) % P
+        return cache[idx_page, idx_slot]
+    m.gather_paged = gather
+
+
+def _queue_ascending(m):
+    orig = m.tile_queue
+
+    def q(*a, **k):
+        return list(reversed(orig(*a, **k)))
+    m.tile_queue = q
+
+
+MUTANTS = {
+    "bwd_drop_delta": _bwd_variant("drop_delta"),
+    "bwd_sign_dS": _bwd_variant("sign_dS"),
+    "bwd_dq_no_scale": _bwd_variant("dq_no_scale"),
+    "bwd_dk_no_scale": _bwd_variant("dk_no_scale"),
+    "bwd_dv_transposed": _bwd_variant("dv_transposed"),
+    "fwd_no_scale": _fwd_variant("no_scale"),
+    "fwd_causal_upper": _fwd_variant("causal_upper"),
+    "lse_in_log2": _lse_log2,
+    "merge_no_reweight": _merge_no_reweight,
+    "gqa_wrong_group": _gqa_wrong_group,
+    "page_slot_off_by_one": _page_slot_off_by_one,
+    "queue_ascending": _queue_ascending,
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name):
+    m = _mutant(MUTANTS[name])
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(m)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake {name}"
