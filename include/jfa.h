@@ -1,0 +1,229 @@
+/*
+ * jfa.h -- C ABI of the jagged FlashAttention library for GB300 (sm_103a).
+ *
+ * Exact attention over variable-length ("jagged") sequences packed back to
+ * back with an int32 offsets tensor and no padding tokens, its recompute-based
+ * backward, a broadcast-Q variant whose dQ is summed over the batch, and a
+ * split-KV decode over a paged, grouped-query KV cache.
+ *
+ * Sources of the operations (web pages; cited by title and section):
+ *  [JFA]  "Optimizing Jagged Flash Attention with TLX: The Road Toward SOTA FA4
+ *         on Blackwell" (aivexanews): jagged packing with an offsets tensor,
+ *         broadcast-Q with dQ summed across the batch (third paragraph);
+ *         persistent, warp-specialised CTAs (fourth paragraph); jagged tile
+ *         load balancing, loop peeling, dQ reduce staging (fifth paragraph).
+ *  [B300] "Cutting-edge isn't plug-and-play: customizing FA4 on B300"
+ *         (TwelveLabs): FlashAttention recap (tiling is exact); Phase 1
+ *         (single-buffered TMEM forward); Phase 2 (head-axis chunked backward
+ *         and its pseudocode: S, dP rebuilt per tile, P from the saved LSE,
+ *         "delta", dS); bug hunting (single-stage producer/consumer order).
+ *  [INF]  "Optimizing FlashAttention-4 for Efficient Inference" (hpjadul):
+ *         PR 1940 (parallelism across the KV dimension), PR 1999 / PR 2104
+ *         (KV pages of arbitrary size), PR 2186 (GQA packing), PR 1993 (tiles
+ *         sized to few query rows).
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are dense, row-major, in device memory unless stated otherwise.
+ *    "bf16" is IEEE bfloat16; "[a, b, c]" lists dimensions outermost first.
+ *  - Jagged tensors are [total, heads, head_dim]: sequence b owns rows
+ *    offsets[b] .. offsets[b+1]-1. offsets is int32 [batch+1] on the device
+ *    with offsets[0] = 0, non-decreasing, offsets[batch] = total.
+ *  - LSE is the natural-log log-sum-exp of the scaled scores of each query row.
+ *  - Every pointer must be 16-byte aligned (TMA and 16-byte vector access);
+ *    head_dim must be 64, 128 or 192 unless stated otherwise.
+ *  - The caller owns and allocates every buffer, including the workspace,
+ *    whose size comes from the matching *_workspace_size() call. The library
+ *    allocates no memory, keeps no per-call state between calls, and may be
+ *    called from several host threads on different streams with separate
+ *    workspaces. Concurrent calls that share a workspace race.
+ *  - All work is enqueued on `stream`; no call synchronises the stream except
+ *    jfa_read_device_status(). Host-side argument errors are returned before
+ *    anything is enqueued. Problems only the device can see (malformed
+ *    offsets or page table, a pipeline wait that ran out of time) are written
+ *    to a status word in the workspace, read back by jfa_read_device_status().
+ *  - max_seqlen / total arguments are host copies of facts about the device
+ *    offsets, so that no device-to-host copy is needed; the kernels check
+ *    them against the offsets and report JFA_ERR_BAD_INPUT on a mismatch.
+ *  - main_kernel_events: optional pair of cudaEvent_t (may be NULL). When
+ *    set, event [0] is recorded on `stream` just before the main attention
+ *    kernel and event [1] just after it, so a caller can time that kernel
+ *    alone. The library does not create, own or destroy them.
+ */
+#ifndef JFA_H
+#define JFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define JFA_API __attribute__((visibility("default")))
+#else
+#define JFA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  JFA_OK = 0,
+  JFA_ERR_INVALID_ARG = 1,          /* null/misaligned pointer, bad size, ... */
+  JFA_ERR_UNSUPPORTED = 2,          /* valid request this build does not implement */
+  JFA_ERR_WORKSPACE_TOO_SMALL = 3,
+  JFA_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed */
+  JFA_ERR_TIMEOUT = 5,              /* a device pipeline wait exceeded its time budget */
+  JFA_ERR_BAD_INPUT = 6             /* device data inconsistent (offsets, page table) */
+} jfa_status;
+
+/* ------------------------------------------------------------------ forward
+ * Jagged self-attention forward ([JFA] third paragraph; [B300] FlashAttention
+ * recap). For every sequence b and head h:
+ *   S = scale * Q_b K_b^T (causal: S_ij = -inf for j > i), P = softmax_rows(S),
+ *   O_b = P V_b, LSE_i = ln sum_j exp(S_ij).
+ */
+typedef struct {
+  const void* q;             /* bf16 [total, heads, head_dim] */
+  const void* k;             /* bf16 [total, heads, head_dim] */
+  const void* v;             /* bf16 [total, heads, head_dim] */
+  const int32_t* offsets;    /* int32 [batch+1], device */
+  int32_t batch;             /* >= 0 */
+  int32_t heads;             /* >= 1 */
+  int32_t head_dim;          /* 64, 128 or 192 */
+  int32_t max_seqlen;        /* host: >= every L_b */
+  int32_t total;             /* host: offsets[batch] */
+  float scale;               /* softmax scale, e.g. 1/sqrt(head_dim) */
+  int32_t causal;            /* 0 or 1 (key j visible to query i iff j <= i) */
+  void* o;                   /* out: bf16 [total, heads, head_dim] */
+  float* lse;                /* out: fp32 [heads, total] */
+  void* main_kernel_events;  /* optional cudaEvent_t[2], see above */
+} jfa_fwd_args;
+
+/* ------------------------------------------------------------------ backward
+ * Recompute-based backward ([B300] Phase 2 and its pseudocode): per tile S and
+ * dP are rebuilt from Q, K, V, dO; P from S and the saved LSE; then
+ *   D = rowsum(dO * O) ("delta"), dS = P * (dP - D),
+ *   dV = P^T dO, dQ = scale dS K, dK = scale dS^T Q.
+ * head_dim 192 runs head-axis chunked ([B300] Phase 2): each pass owns a
+ * head_chunk-wide slice of dQ/dK/dV while S and dP are still accumulated over
+ * the whole head dimension.
+ */
+typedef struct {
+  const void* q;             /* bf16 [total, heads, head_dim] */
+  const void* k;             /* bf16 [total, heads, head_dim] */
+  const void* v;             /* bf16 [total, heads, head_dim] */
+  const void* o;             /* bf16 [total, heads, head_dim], forward output */
+  const void* dout;          /* bf16 [total, heads, head_dim], gradient of O */
+  const float* lse;          /* fp32 [heads, total], forward LSE */
+  const int32_t* offsets;    /* int32 [batch+1], device */
+  int32_t batch, heads, head_dim, max_seqlen, total;
+  float scale;
+  int32_t causal;
+  int32_t head_chunk;        /* 0 = automatic (64 for head_dim 192, else head_dim) */
+  void* dq;                  /* out: bf16 [total, heads, head_dim] */
+  void* dk;                  /* out: bf16 [total, heads, head_dim] */
+  void* dv;                  /* out: bf16 [total, heads, head_dim] */
+  void* main_kernel_events;  /* optional cudaEvent_t[2] */
+} jfa_bwd_args;
+
+/* ------------------------------------------------------------------ broadcast-Q
+ * One dense Q [q_len, heads, head_dim] is the query of every sequence of a
+ * jagged K/V batch ([JFA] third paragraph). Not causal.
+ *   O[b] = softmax(scale Q K_b^T) V_b; backward: dQ = sum_b dQ_b (the
+ *   contended cross-CTA reduction), dK_b, dV_b per sequence.
+ */
+typedef struct {
+  const void* q;             /* bf16 [q_len, heads, head_dim] */
+  const void* k;             /* bf16 [total_k, heads, head_dim] */
+  const void* v;             /* bf16 [total_k, heads, head_dim] */
+  const int32_t* kv_offsets; /* int32 [batch+1], device */
+  int32_t batch, q_len, heads, head_dim, max_seqlen_k, total_k;
+  float scale;
+  void* o;                   /* out: bf16 [batch, q_len, heads, head_dim] */
+  float* lse;                /* out: fp32 [batch, heads, q_len] */
+  void* main_kernel_events;
+} jfa_bcast_fwd_args;
+
+typedef struct {
+  const void* q;             /* bf16 [q_len, heads, head_dim] */
+  const void* k;             /* bf16 [total_k, heads, head_dim] */
+  const void* v;             /* bf16 [total_k, heads, head_dim] */
+  const void* o;             /* bf16 [batch, q_len, heads, head_dim] */
+  const void* dout;          /* bf16 [batch, q_len, heads, head_dim] */
+  const float* lse;          /* fp32 [batch, heads, q_len] */
+  const int32_t* kv_offsets;
+  int32_t batch, q_len, heads, head_dim, max_seqlen_k, total_k;
+  float scale;
+  void* dq;                  /* out: bf16 [q_len, heads, head_dim], summed over the batch */
+  void* dk;                  /* out: bf16 [total_k, heads, head_dim] */
+  void* dv;                  /* out: bf16 [total_k, heads, head_dim] */
+  void* main_kernel_events;
+} jfa_bcast_bwd_args;
+
+/* ------------------------------------------------------------------ paged decode
+ * One query token per sequence against a paged KV cache ([INF] PR 1999/2104:
+ * pages of any size >= 1; PR 2186: the q_heads/kv_heads query heads that share
+ * a KV head are processed together; PR 1940: the KV range of each sequence is
+ * split into num_splits parts processed in parallel, then merged).
+ * Token t of sequence b lives in page page_table[b][t / page_size], slot
+ * t % page_size; query head h reads KV head h / (q_heads / kv_heads).
+ * Split s of sequence b covers tokens [s*c, min((s+1)*c, L_b)) with
+ * c = ceil(L_b / num_splits). The merge is
+ *   lse = ln sum_s exp(lse_s), O = sum_s exp(lse_s - lse) O_s.
+ * A sequence with L_b = 0 gets O = 0 and LSE = -inf.
+ * head_dim must be 128; q_heads / kv_heads must be 1, 2, 4, 8 or 16.
+ */
+typedef struct {
+  const void* q;             /* bf16 [batch, q_heads, head_dim] */
+  const void* k_cache;       /* bf16 [num_pages, page_size, kv_heads, head_dim] */
+  const void* v_cache;       /* bf16 [num_pages, page_size, kv_heads, head_dim] */
+  const int32_t* page_table; /* int32 [batch, max_pages]; entries past ceil(L_b/page_size) are not read */
+  const int32_t* seqlens_k;  /* int32 [batch], 0 <= L_b <= max_pages*page_size */
+  int32_t batch, q_heads, kv_heads, head_dim;
+  int32_t page_size;         /* >= 1 */
+  int32_t num_pages;         /* page_table entries must be < num_pages */
+  int32_t max_pages;
+  int32_t num_splits;        /* 1 .. 128 */
+  float scale;
+  void* o;                   /* out: bf16 [batch, q_heads, head_dim] */
+  float* lse;                /* out: fp32 [batch, q_heads] */
+  int32_t* split_bounds_out; /* optional out: int32 [batch, num_splits, 2] (start, end) */
+  void* main_kernel_events;  /* optional cudaEvent_t[2] around the split kernel */
+} jfa_decode_args;
+
+/* Workspace sizes in bytes (0 only when args is NULL). */
+JFA_API size_t jfa_fwd_workspace_size(const jfa_fwd_args* args);
+JFA_API size_t jfa_bwd_workspace_size(const jfa_bwd_args* args);
+JFA_API size_t jfa_bcast_fwd_workspace_size(const jfa_bcast_fwd_args* args);
+JFA_API size_t jfa_bcast_bwd_workspace_size(const jfa_bcast_bwd_args* args);
+JFA_API size_t jfa_decode_workspace_size(const jfa_decode_args* args);
+
+/* Entry points. `workspace` is device memory of at least the size above,
+ * 256-byte aligned; its contents on entry do not matter. */
+JFA_API jfa_status jfa_fwd(const jfa_fwd_args* args, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+JFA_API jfa_status jfa_bwd(const jfa_bwd_args* args, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+JFA_API jfa_status jfa_fwd_broadcast_q(const jfa_bcast_fwd_args* args, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+JFA_API jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* args, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+JFA_API jfa_status jfa_decode_splitkv(const jfa_decode_args* args, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
+/* Synchronises `stream`, then returns the device status word of the last call
+ * that used `workspace` (JFA_OK, JFA_ERR_TIMEOUT or JFA_ERR_BAD_INPUT), or
+ * JFA_ERR_CUDA if the stream reports an error. *detail (optional) receives a
+ * code naming the wait or check that failed. */
+JFA_API jfa_status jfa_read_device_status(const void* workspace, cudaStream_t stream, int32_t* detail);
+
+/* Static string for a status code. */
+JFA_API const char* jfa_status_string(jfa_status status);
+
+/* Library version, as major*10000 + minor*100 + patch. */
+JFA_API int32_t jfa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JFA_H */

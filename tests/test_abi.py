@@ -1,0 +1,145 @@
+"""The C ABI on the CPU: the library loads without a GPU, exports every symbol
+include/jfa.h declares, the ctypes structures match the C layout (checked
+against a C program compiled with the header), and host-side validation
+rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+import varlen_flashattention_gb300 as jfa
+from varlen_flashattention_gb300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "jfa.h")
+CUDA_INC = "/usr/local/cuda/include"
+
+STRUCTS = {
+    "jfa_fwd_args": _abi.FwdArgs,
+    "jfa_bwd_args": _abi.BwdArgs,
+    "jfa_bcast_fwd_args": _abi.BcastFwdArgs,
+    "jfa_bcast_bwd_args": _abi.BcastBwdArgs,
+    "jfa_decode_args": _abi.DecodeArgs,
+}
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"JFA_API\s+[\w\s\*]+?\b(jfa_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from __graft_entry__ import build
+    build()
+    return jfa.library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert len(names) >= 13, names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in jfa.h but not exported"
+    assert {s[0] for s in _abi.SIGNATURES} == set(names)
+
+
+def test_struct_layouts_match_c(tmp_path):
+    gcc = shutil.which("gcc")
+    if gcc is None or not os.path.exists(os.path.join(CUDA_INC, "cuda_runtime_api.h")):
+        pytest.skip("gcc or CUDA headers missing")
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "jfa.h"', "int main(void) {"]
+    for cname, py in STRUCTS.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.check_call([gcc, "-I", os.path.join(ROOT, "include"), "-I", CUDA_INC, str(src), "-o", str(exe)])
+    out = subprocess.check_output([str(exe)], text=True).split("\n")
+    got = {}
+    for line in out:
+        if line:
+            s, f, v = line.split()
+            got[(s, f)] = int(v)
+    for cname, py in STRUCTS.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for f, _ in py._fields_:
+            assert got[(cname, f)] == getattr(py, f).offset, (cname, f)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.jfa_status_string(code)
+    assert lib.jfa_version() >= 100
+
+
+FAKE = 0x10000  # aligned, never dereferenced: every call below returns before any CUDA work
+
+
+def _fwd_args(**kw):
+    a = _abi.FwdArgs(FAKE, FAKE, FAKE, FAKE, 2, 4, 128, 100, 150, 0.1, 0, FAKE, FAKE, None)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_fwd_validation(lib):
+    P = ctypes.byref
+    assert lib.jfa_fwd(None, FAKE, 1 << 30, None) == _abi.JFA_ERR_INVALID_ARG
+    assert lib.jfa_fwd(P(_fwd_args(head_dim=96)), FAKE, 1 << 30, None) == _abi.JFA_ERR_UNSUPPORTED
+    assert lib.jfa_fwd(P(_fwd_args(q=FAKE + 8)), FAKE, 1 << 30, None) == _abi.JFA_ERR_INVALID_ARG
+    assert lib.jfa_fwd(P(_fwd_args(scale=-1.0)), FAKE, 1 << 30, None) == _abi.JFA_ERR_INVALID_ARG
+    assert lib.jfa_fwd(P(_fwd_args(causal=2)), FAKE, 1 << 30, None) == _abi.JFA_ERR_INVALID_ARG
+    assert lib.jfa_fwd(P(_fwd_args(heads=0)), FAKE, 1 << 30, None) == _abi.JFA_ERR_INVALID_ARG
+    assert lib.jfa_fwd(P(_fwd_args()), FAKE + 16, 1 << 30, None) == _abi.JFA_ERR_INVALID_ARG  # ws alignment
+    need = lib.jfa_fwd_workspace_size(P(_fwd_args()))
+    assert need > 256
+    assert lib.jfa_fwd(P(_fwd_args()), FAKE, need - 1, None) == _abi.JFA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_bwd_validation(lib):
+    P = ctypes.byref
+
+    def args(**kw):
+        a = _abi.BwdArgs(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 128, 100, 150, 0.1, 0, 0, FAKE, FAKE, FAKE,
+                         None)
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+    assert lib.jfa_bwd(P(args(head_dim=192, head_chunk=192)), FAKE, 1 << 40, None) == _abi.JFA_ERR_UNSUPPORTED
+    assert lib.jfa_bwd(P(args(head_dim=64, head_chunk=32)), FAKE, 1 << 40, None) == _abi.JFA_ERR_UNSUPPORTED
+    assert lib.jfa_bwd(P(args(dq=FAKE + 4)), FAKE, 1 << 40, None) == _abi.JFA_ERR_INVALID_ARG
+    need = lib.jfa_bwd_workspace_size(P(args()))
+    # the fp32 dQ accumulator dominates: total * heads * head_dim * 4 bytes
+    assert need >= 150 * 4 * 128 * 4
+    assert lib.jfa_bwd(P(args()), FAKE, need - 1, None) == _abi.JFA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_decode_validation(lib):
+    P = ctypes.byref
+
+    def args(**kw):
+        a = _abi.DecodeArgs(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 32, 8, 128, 16, 100, 10, 8, 0.1, FAKE, FAKE, None, None)
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+    for bad in (dict(num_splits=0), dict(num_splits=129), dict(page_size=0), dict(q_heads=30),
+                dict(seqlens_k=FAKE + 2)):
+        assert lib.jfa_decode_splitkv(P(args(**bad)), FAKE, 1 << 30, None) == _abi.JFA_ERR_INVALID_ARG, bad
+    assert lib.jfa_decode_splitkv(P(args(head_dim=64)), FAKE, 1 << 30, None) == _abi.JFA_ERR_UNSUPPORTED
+    assert lib.jfa_decode_splitkv(P(args(kv_heads=1)), FAKE, 1 << 30, None) == _abi.JFA_ERR_UNSUPPORTED  # group 32
+    need = lib.jfa_decode_workspace_size(P(args()))
+    assert need >= 8 * 4 * 32 * 128 * 4
+    assert lib.jfa_decode_splitkv(P(args()), FAKE, need - 1, None) == _abi.JFA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    q = torch.zeros(4, 1, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        jfa.jfa_fwd(q, q, q, torch.zeros(2, dtype=torch.int32), 4)

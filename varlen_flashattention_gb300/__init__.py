@@ -1,0 +1,253 @@
+"""Jagged (varlen) FlashAttention for GB300: Python binding of libjfa.so.
+
+The functions here carry the names of the C entry points and only marshal
+arguments: they check shapes and dtypes, allocate outputs and the workspace
+with PyTorch when the caller does not pass them, and call the library on the
+current CUDA stream. Every step of the computation runs in the sm_103a
+kernels; there is no CPU or PyTorch fallback.
+
+    jfa_fwd               jagged self-attention forward -> (O, LSE)
+    jfa_bwd               its recompute-based backward -> (dQ, dK, dV)
+    jfa_fwd_broadcast_q   one dense Q shared by a jagged K/V batch -> (O, LSE)
+    jfa_bwd_broadcast_q   its backward, dQ summed over the batch -> (dQ, dK, dV)
+    jfa_decode_splitkv    split-KV decode over a paged GQA cache -> (O, LSE)
+    jagged_attention      autograd wrapper of jfa_fwd / jfa_bwd
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _abi
+
+__all__ = [
+    "JfaError", "jfa_fwd", "jfa_bwd", "jfa_fwd_broadcast_q", "jfa_bwd_broadcast_q", "jfa_decode_splitkv",
+    "jfa_read_device_status", "jagged_attention", "library",
+]
+
+
+class JfaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = library().jfa_status_string(status).decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+        self.status = status
+
+
+def library():
+    return _abi.load()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, name, dtype, dims=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dimensions, got {tuple(t.shape)}")
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _events(events):
+    if events is None:
+        return None, None
+    arr = (ctypes.c_void_p * 2)(events[0].cuda_event, events[1].cuda_event)
+    return ctypes.cast(arr, ctypes.c_void_p), arr
+
+
+def _workspace(nbytes, device, workspace):
+    if workspace is None:
+        return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace holds {workspace.numel()} bytes, needs {nbytes}")
+    return workspace
+
+
+def _check(status, where):
+    if status != _abi.JFA_OK:
+        raise JfaError(status, where)
+
+
+def jfa_read_device_status(workspace, stream=None):
+    """Synchronises the stream; returns (status, detail) of the last call that used `workspace`."""
+    d = ctypes.c_int32(0)
+    st = library().jfa_read_device_status(_ptr(workspace), _stream(stream), ctypes.byref(d))
+    return int(st), int(d.value)
+
+
+def _finish(ws, check, stream, where):
+    if check:
+        st, detail = jfa_read_device_status(ws, stream)
+        if st != _abi.JFA_OK:
+            e = JfaError(st, f"{where} (device, detail {detail})")
+            raise e
+
+
+# ---------------------------------------------------------------- forward / backward
+
+def jfa_fwd(q, k, v, offsets, max_seqlen, scale=None, causal=False, o=None, lse=None, workspace=None,
+            stream=None, events=None, check=False):
+    """Jagged self-attention forward. q, k, v: bf16 [total, H, d]; offsets: int32 [B+1] (CUDA).
+    Returns O bf16 [total, H, d] and LSE fp32 [H, total] (natural log)."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, torch.bfloat16, 3)
+    _need(offsets, "offsets", torch.int32, 1)
+    total, H, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "o", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    a = _abi.FwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), offsets.numel() - 1, H, d, int(max_seqlen),
+                     total, scale, int(bool(causal)), _ptr(o), _ptr(lse), None)
+    ev, _keep = _events(events)
+    a.main_kernel_events = ev
+    lib = library()
+    ws = _workspace(lib.jfa_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
+    _check(lib.jfa_fwd(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_fwd")
+    _finish(ws, check, stream, "jfa_fwd")
+    return o, lse
+
+
+def jfa_bwd(q, k, v, o, dout, lse, offsets, max_seqlen, scale=None, causal=False, head_chunk=0,
+            dq=None, dk=None, dv=None, workspace=None, stream=None, events=None, check=False):
+    """Recompute-based backward of jfa_fwd. Returns dQ, dK, dV bf16 [total, H, d]."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _need(t, n, torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    _need(offsets, "offsets", torch.int32, 1)
+    total, H, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    a = _abi.BwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(offsets),
+                     offsets.numel() - 1, H, d, int(max_seqlen), total, scale, int(bool(causal)), int(head_chunk),
+                     _ptr(dq), _ptr(dk), _ptr(dv), None)
+    ev, _keep = _events(events)
+    a.main_kernel_events = ev
+    lib = library()
+    ws = _workspace(lib.jfa_bwd_workspace_size(ctypes.byref(a)), q.device, workspace)
+    _check(lib.jfa_bwd(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_bwd")
+    _finish(ws, check, stream, "jfa_bwd")
+    return dq, dk, dv
+
+
+def jfa_fwd_broadcast_q(q, k, v, kv_offsets, max_seqlen_k, scale=None, o=None, lse=None, workspace=None,
+                        stream=None, events=None, check=False):
+    """Broadcast-Q forward. q: bf16 [Lq, H, d] shared by every sequence; k, v jagged [total_k, H, d].
+    Returns O bf16 [B, Lq, H, d] and LSE fp32 [B, H, Lq]."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, torch.bfloat16, 3)
+    _need(kv_offsets, "kv_offsets", torch.int32, 1)
+    Lq, H, d = q.shape
+    B = kv_offsets.numel() - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty((B, Lq, H, d), dtype=torch.bfloat16, device=q.device) if o is None else o
+    lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device) if lse is None else lse
+    a = _abi.BcastFwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_offsets), B, Lq, H, d, int(max_seqlen_k),
+                          k.shape[0], scale, _ptr(o), _ptr(lse), None)
+    ev, _keep = _events(events)
+    a.main_kernel_events = ev
+    lib = library()
+    ws = _workspace(lib.jfa_bcast_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
+    _check(lib.jfa_fwd_broadcast_q(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_fwd_broadcast_q")
+    _finish(ws, check, stream, "jfa_fwd_broadcast_q")
+    return o, lse
+
+
+def jfa_bwd_broadcast_q(q, k, v, o, dout, lse, kv_offsets, max_seqlen_k, scale=None, dq=None, dk=None, dv=None,
+                        workspace=None, stream=None, events=None, check=False):
+    """Broadcast-Q backward. Returns dQ bf16 [Lq, H, d] summed over the batch, dK, dV [total_k, H, d]."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, torch.bfloat16, 3)
+    _need(o, "o", torch.bfloat16, 4)
+    _need(dout, "dout", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    _need(kv_offsets, "kv_offsets", torch.int32, 1)
+    Lq, H, d = q.shape
+    B = kv_offsets.numel() - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    a = _abi.BcastBwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(kv_offsets),
+                          B, Lq, H, d, int(max_seqlen_k), k.shape[0], scale, _ptr(dq), _ptr(dk), _ptr(dv), None)
+    ev, _keep = _events(events)
+    a.main_kernel_events = ev
+    lib = library()
+    ws = _workspace(lib.jfa_bcast_bwd_workspace_size(ctypes.byref(a)), q.device, workspace)
+    _check(lib.jfa_bwd_broadcast_q(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_bwd_broadcast_q")
+    _finish(ws, check, stream, "jfa_bwd_broadcast_q")
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------- decode
+
+def jfa_decode_splitkv(q, k_cache, v_cache, page_table, seqlens_k, num_splits, scale=None, o=None, lse=None,
+                       split_bounds=None, workspace=None, stream=None, events=None, check=False):
+    """Split-KV decode over a paged GQA cache. q: bf16 [B, Hq, 128]; caches bf16
+    [num_pages, page_size, Hkv, 128]; page_table int32 [B, max_pages]; seqlens_k int32 [B].
+    Returns O bf16 [B, Hq, 128] and LSE fp32 [B, Hq]. If `split_bounds` (int32 [B, S, 2])
+    is given, the kernel writes each split's token range into it."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(seqlens_k, "seqlens_k", torch.int32, 1)
+    B, Hq, d = q.shape
+    num_pages, P, Hkv, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shapes do not match q")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    a = _abi.DecodeArgs(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(seqlens_k),
+                        B, Hq, Hkv, d, P, num_pages, page_table.shape[1], int(num_splits), scale,
+                        _ptr(o), _ptr(lse), _ptr(split_bounds), None)
+    ev, _keep = _events(events)
+    a.main_kernel_events = ev
+    lib = library()
+    ws = _workspace(lib.jfa_decode_workspace_size(ctypes.byref(a)), q.device, workspace)
+    _check(lib.jfa_decode_splitkv(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_decode_splitkv")
+    _finish(ws, check, stream, "jfa_decode_splitkv")
+    return o, lse
+
+
+# ---------------------------------------------------------------- autograd
+
+class _JaggedAttention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, offsets, max_seqlen, scale, causal):
+        o, lse = jfa_fwd(q, k, v, offsets, max_seqlen, scale, causal)
+        ctx.save_for_backward(q, k, v, o, lse, offsets)
+        ctx.max_seqlen, ctx.scale, ctx.causal = max_seqlen, scale, causal
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse, offsets = ctx.saved_tensors
+        dq, dk, dv = jfa_bwd(q, k, v, o, do.contiguous(), lse, offsets, ctx.max_seqlen, ctx.scale, ctx.causal)
+        return dq, dk, dv, None, None, None, None
+
+
+def jagged_attention(q, k, v, offsets, max_seqlen, scale=None, causal=False):
+    """Differentiable jagged attention (bf16 [total, H, d] tensors, int32 offsets)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    return _JaggedAttention.apply(q, k, v, offsets, max_seqlen, scale, causal)

@@ -1,0 +1,521 @@
+// C ABI of the jagged FlashAttention library: argument validation, workspace
+// layout, TMA descriptor encoding and kernel launches. See include/jfa.h for
+// the contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "jfa_internal.h"
+
+namespace jfa {
+
+namespace {
+
+// ------------------------------------------------------------------ helpers
+
+bool aligned(const void* p, size_t a) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+uint64_t wait_budget_ns() {
+  static std::atomic<uint64_t> cached{0};
+  uint64_t v = cached.load(std::memory_order_relaxed);
+  if (v) return v;
+  double ms = 2000.0;
+  if (const char* e = std::getenv("JFA_WAIT_BUDGET_MS")) {
+    const double x = std::atof(e);
+    if (x > 0) ms = x;
+  }
+  v = static_cast<uint64_t>(ms * 1e6);
+  cached.store(v, std::memory_order_relaxed);
+  return v;
+}
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static std::atomic<int> cache[64];
+  if (dev >= 0 && dev < 64) {
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v) return v;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 view [rows, cols] (cols contiguous) read in 128-row x 64-column
+// boxes with the 128-byte swizzle the tcgen05 descriptors expect.
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  if (rows == 0) rows = 1;  // nothing is read from an empty tensor; the map must still be valid
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTile)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool good_dim(int d) { return d == 64 || d == 128 || d == 192; }
+
+jfa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA; }
+
+void record(void* events, int which, cudaStream_t s) {
+  if (events) cudaEventRecord(static_cast<cudaEvent_t*>(events)[which], s);
+}
+
+// ------------------------------------------------------------------ workspace layouts
+
+struct Layout {
+  size_t status = 0, tile_base = 0, items = 0, lse2p = 0, deltap = 0, dq_acc = 0, part_o = 0, part_lse = 0;
+  size_t bytes = 0;
+  int64_t max_items = 0, pad_tiles = 0;
+};
+
+Layout self_layout(int64_t batch, int64_t heads, int64_t total, int64_t head_dim, bool bwd) {
+  Layout L;
+  size_t off = kStatusBytes;
+  L.tile_base = off;
+  off = align_up(off + 4 * (batch + 1), 256);
+  L.pad_tiles = max_tiles(total, batch);
+  L.max_items = heads * L.pad_tiles;
+  L.items = off;
+  off = align_up(off + 16 * L.max_items, 256);
+  if (bwd) {
+    L.lse2p = off;
+    off = align_up(off + 4 * heads * L.pad_tiles * kTile, 256);
+    L.deltap = off;
+    off = align_up(off + 4 * heads * L.pad_tiles * kTile, 256);
+    L.dq_acc = off;
+    off = align_up(off + 4 * total * heads * head_dim, 256);
+  }
+  L.bytes = off;
+  return L;
+}
+
+Layout bcast_layout(int64_t batch, int64_t q_len, int64_t heads, int64_t total_k, int64_t head_dim, bool bwd) {
+  Layout L;
+  size_t off = kStatusBytes;
+  L.tile_base = off;
+  off = align_up(off + 4 * (batch + 1), 256);
+  const int64_t nqt = (q_len + kTile - 1) / kTile;
+  L.max_items = bwd ? heads * max_tiles(total_k, batch) : batch * heads * nqt;
+  L.items = off;
+  off = align_up(off + 16 * L.max_items, 256);
+  if (bwd) {
+    L.pad_tiles = batch * nqt;
+    L.lse2p = off;
+    off = align_up(off + 4 * batch * heads * nqt * kTile, 256);
+    L.deltap = off;
+    off = align_up(off + 4 * batch * heads * nqt * kTile, 256);
+    L.dq_acc = off;
+    off = align_up(off + 4 * q_len * heads * head_dim, 256);
+  }
+  L.bytes = off;
+  return L;
+}
+
+Layout decode_layout(int64_t batch, int64_t q_heads, int64_t splits) {
+  Layout L;
+  size_t off = kStatusBytes;
+  L.part_o = off;
+  off = align_up(off + 4 * splits * batch * q_heads * 128, 256);
+  L.part_lse = off;
+  off = align_up(off + 4 * splits * batch * q_heads, 256);
+  L.bytes = off;
+  return L;
+}
+
+// ------------------------------------------------------------------ validation
+
+jfa_status check_fwd(const jfa_fwd_args* a) {
+  if (!a) return JFA_ERR_INVALID_ARG;
+  if (a->batch < 0 || a->heads < 1 || a->total < 0 || a->max_seqlen < 0) return JFA_ERR_INVALID_ARG;
+  if (!good_dim(a->head_dim)) return JFA_ERR_UNSUPPORTED;
+  if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return JFA_ERR_INVALID_ARG;
+  if (a->causal != 0 && a->causal != 1) return JFA_ERR_INVALID_ARG;
+  if (!aligned(a->offsets, 4)) return JFA_ERR_INVALID_ARG;
+  if (a->total > 0) {
+    if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->o, 16) ||
+        !aligned(a->lse, 4))
+      return JFA_ERR_INVALID_ARG;
+  }
+  if (static_cast<int64_t>(a->total) * a->heads * a->head_dim >= (int64_t(1) << 40)) return JFA_ERR_INVALID_ARG;
+  return JFA_OK;
+}
+
+jfa_status check_bwd(const jfa_bwd_args* a, int* chunk) {
+  if (!a) return JFA_ERR_INVALID_ARG;
+  if (a->batch < 0 || a->heads < 1 || a->total < 0 || a->max_seqlen < 0) return JFA_ERR_INVALID_ARG;
+  if (!good_dim(a->head_dim)) return JFA_ERR_UNSUPPORTED;
+  if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return JFA_ERR_INVALID_ARG;
+  if (a->causal != 0 && a->causal != 1) return JFA_ERR_INVALID_ARG;
+  int c = a->head_chunk;
+  if (c == 0) c = (a->head_dim == 192) ? 64 : a->head_dim;
+  const bool ok_chunk = (c == a->head_dim && a->head_dim != 192) || (c == 64 && a->head_dim >= 128);
+  if (!ok_chunk) return JFA_ERR_UNSUPPORTED;  // head_dim 192 unchunked would overflow TMEM
+  *chunk = c;
+  if (!aligned(a->offsets, 4)) return JFA_ERR_INVALID_ARG;
+  if (a->total > 0) {
+    if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->o, 16) ||
+        !aligned(a->dout, 16) || !aligned(a->lse, 4) || !aligned(a->dq, 16) || !aligned(a->dk, 16) ||
+        !aligned(a->dv, 16))
+      return JFA_ERR_INVALID_ARG;
+  }
+  if (static_cast<int64_t>(a->total) * a->heads * a->head_dim >= (int64_t(1) << 40)) return JFA_ERR_INVALID_ARG;
+  return JFA_OK;
+}
+
+jfa_status check_bcast_common(int batch, int q_len, int heads, int head_dim, int max_seqlen_k, int total_k,
+                              float scale) {
+  if (batch < 0 || q_len < 0 || heads < 1 || max_seqlen_k < 0 || total_k < 0) return JFA_ERR_INVALID_ARG;
+  if (!good_dim(head_dim)) return JFA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(batch) * q_len >= (int64_t(1) << 31)) return JFA_ERR_INVALID_ARG;
+  return JFA_OK;
+}
+
+}  // namespace
+}  // namespace jfa
+
+using namespace jfa;
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+int32_t jfa_version(void) { return 100; }
+
+const char* jfa_status_string(jfa_status s) {
+  switch (s) {
+    case JFA_OK: return "ok";
+    case JFA_ERR_INVALID_ARG: return "invalid argument";
+    case JFA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case JFA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case JFA_ERR_CUDA: return "CUDA error";
+    case JFA_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case JFA_ERR_BAD_INPUT: return "inconsistent device input (offsets or page table)";
+  }
+  return "unknown status";
+}
+
+size_t jfa_fwd_workspace_size(const jfa_fwd_args* a) {
+  if (!a) return 0;
+  return self_layout(a->batch, a->heads, a->total, a->head_dim, false).bytes;
+}
+
+size_t jfa_bwd_workspace_size(const jfa_bwd_args* a) {
+  if (!a) return 0;
+  return self_layout(a->batch, a->heads, a->total, a->head_dim, true).bytes;
+}
+
+size_t jfa_bcast_fwd_workspace_size(const jfa_bcast_fwd_args* a) {
+  if (!a) return 0;
+  return bcast_layout(a->batch, a->q_len, a->heads, a->total_k, a->head_dim, false).bytes;
+}
+
+size_t jfa_bcast_bwd_workspace_size(const jfa_bcast_bwd_args* a) {
+  if (!a) return 0;
+  return bcast_layout(a->batch, a->q_len, a->heads, a->total_k, a->head_dim, true).bytes;
+}
+
+size_t jfa_decode_workspace_size(const jfa_decode_args* a) {
+  if (!a) return 0;
+  return decode_layout(a->batch, a->q_heads, a->num_splits).bytes;
+}
+
+jfa_status jfa_fwd(const jfa_fwd_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  jfa_status st = check_fwd(a);
+  if (st != JFA_OK) return st;
+  const Layout L = self_layout(a->batch, a->heads, a->total, a->head_dim, false);
+  if (!aligned(ws, 256)) return JFA_ERR_INVALID_ARG;
+  if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(w);
+  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (a->batch == 0 || a->total == 0) return JFA_OK;
+  const int sms = sm_count();
+  if (sms <= 0) return JFA_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  const uint64_t cols = static_cast<uint64_t>(a->heads) * a->head_dim;
+  if (!make_tmap_bf16(&tq, a->q, a->total, cols) || !make_tmap_bf16(&tk, a->k, a->total, cols) ||
+      !make_tmap_bf16(&tv, a->v, a->total, cols))
+    return JFA_ERR_CUDA;
+  QueueParams qp;
+  qp.offsets = a->offsets;
+  qp.batch = a->batch;
+  qp.heads = a->heads;
+  qp.total = a->total;
+  qp.max_seqlen = a->max_seqlen;
+  qp.causal = a->causal;
+  qp.mode = kQueueSelfFwd;
+  qp.q_len = 0;
+  qp.status = status;
+  qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
+  qp.items = reinterpret_cast<int4*>(w + L.items);
+  qp.max_items = static_cast<int32_t>(L.max_items);
+  if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
+  record(a->main_kernel_events, 0, stream);
+  cudaError_t e = launch_fwd(a->head_dim, a->causal != 0, tq, tk, tv, a->offsets, qp.items, status, a->o, a->lse,
+                             a->heads, a->total, 0, 0, a->scale, wait_budget_ns(), grid, stream);
+  record(a->main_kernel_events, 1, stream);
+  return cuda_status(e);
+}
+
+jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  int chunk = 0;
+  jfa_status st = check_bwd(a, &chunk);
+  if (st != JFA_OK) return st;
+  const Layout L = self_layout(a->batch, a->heads, a->total, a->head_dim, true);
+  if (!aligned(ws, 256)) return JFA_ERR_INVALID_ARG;
+  if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(w);
+  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (a->batch == 0 || a->total == 0) return JFA_OK;
+  const int sms = sm_count();
+  if (sms <= 0) return JFA_ERR_CUDA;
+  const int64_t n_acc = static_cast<int64_t>(a->total) * a->heads * a->head_dim;
+  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
+  if (cudaMemsetAsync(dq_acc, 0, 4 * n_acc, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  CUtensorMap tq, tk, tv, tdo;
+  const uint64_t cols = static_cast<uint64_t>(a->heads) * a->head_dim;
+  if (!make_tmap_bf16(&tq, a->q, a->total, cols) || !make_tmap_bf16(&tk, a->k, a->total, cols) ||
+      !make_tmap_bf16(&tv, a->v, a->total, cols) || !make_tmap_bf16(&tdo, a->dout, a->total, cols))
+    return JFA_ERR_CUDA;
+  QueueParams qp;
+  qp.offsets = a->offsets;
+  qp.batch = a->batch;
+  qp.heads = a->heads;
+  qp.total = a->total;
+  qp.max_seqlen = a->max_seqlen;
+  qp.causal = a->causal;
+  qp.mode = kQueueSelfBwd;
+  qp.q_len = 0;
+  qp.status = status;
+  qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
+  qp.items = reinterpret_cast<int4*>(w + L.items);
+  qp.max_items = static_cast<int32_t>(L.max_items);
+  if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  float* lse2p = reinterpret_cast<float*>(w + L.lse2p);
+  float* deltap = reinterpret_cast<float*>(w + L.deltap);
+  if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->offsets, qp.tile_base, status, a->batch, a->heads,
+                     a->total, 0, 0, static_cast<int>(L.pad_tiles), static_cast<int>(L.pad_tiles), lse2p, deltap,
+                     stream) != cudaSuccess)
+    return JFA_ERR_CUDA;
+  BwdLaunch bl;
+  bl.head_dim = a->head_dim;
+  bl.head_chunk = chunk;
+  bl.offsets = a->offsets;
+  bl.tile_base = qp.tile_base;
+  bl.items = qp.items;
+  bl.status = status;
+  bl.lse2p = lse2p;
+  bl.deltap = deltap;
+  bl.dq_acc = dq_acc;
+  bl.dk = a->dk;
+  bl.dv = a->dv;
+  bl.heads = a->heads;
+  bl.total = a->total;
+  bl.bcast = 0;
+  bl.q_len = 0;
+  bl.causal = a->causal;
+  bl.pad_tiles = static_cast<int>(L.pad_tiles);
+  bl.scale = a->scale;
+  bl.budget_ns = wait_budget_ns();
+  bl.grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items * (a->head_dim / chunk), 1)));
+  record(a->main_kernel_events, 0, stream);
+  cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, stream);
+  record(a->main_kernel_events, 1, stream);
+  if (e != cudaSuccess) return JFA_ERR_CUDA;
+  return cuda_status(launch_bwd_post(dq_acc, a->dq, n_acc, a->scale, status, sms, stream));
+}
+
+jfa_status jfa_fwd_broadcast_q(const jfa_bcast_fwd_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!a) return JFA_ERR_INVALID_ARG;
+  jfa_status st = check_bcast_common(a->batch, a->q_len, a->heads, a->head_dim, a->max_seqlen_k, a->total_k, a->scale);
+  if (st != JFA_OK) return st;
+  if (!aligned(a->kv_offsets, 4)) return JFA_ERR_INVALID_ARG;
+  if (a->batch > 0 && a->q_len > 0) {
+    if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->o, 16) || !aligned(a->lse, 4))
+      return JFA_ERR_INVALID_ARG;
+  }
+  const Layout L = bcast_layout(a->batch, a->q_len, a->heads, a->total_k, a->head_dim, false);
+  if (!aligned(ws, 256)) return JFA_ERR_INVALID_ARG;
+  if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(w);
+  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (a->batch == 0 || a->q_len == 0) return JFA_OK;
+  const int sms = sm_count();
+  if (sms <= 0) return JFA_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  const uint64_t cols = static_cast<uint64_t>(a->heads) * a->head_dim;
+  if (!make_tmap_bf16(&tq, a->q, a->q_len, cols) || !make_tmap_bf16(&tk, a->k, a->total_k, cols) ||
+      !make_tmap_bf16(&tv, a->v, a->total_k, cols))
+    return JFA_ERR_CUDA;
+  QueueParams qp;
+  qp.offsets = a->kv_offsets;
+  qp.batch = a->batch;
+  qp.heads = a->heads;
+  qp.total = a->total_k;
+  qp.max_seqlen = a->max_seqlen_k;
+  qp.causal = 0;
+  qp.mode = kQueueBcastFwd;
+  qp.q_len = a->q_len;
+  qp.status = status;
+  qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
+  qp.items = reinterpret_cast<int4*>(w + L.items);
+  qp.max_items = static_cast<int32_t>(L.max_items);
+  if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
+  record(a->main_kernel_events, 0, stream);
+  cudaError_t e = launch_fwd(a->head_dim, false, tq, tk, tv, a->kv_offsets, qp.items, status, a->o, a->lse, a->heads,
+                             a->total_k, 1, a->q_len, a->scale, wait_budget_ns(), grid, stream);
+  record(a->main_kernel_events, 1, stream);
+  return cuda_status(e);
+}
+
+jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!a) return JFA_ERR_INVALID_ARG;
+  jfa_status st = check_bcast_common(a->batch, a->q_len, a->heads, a->head_dim, a->max_seqlen_k, a->total_k, a->scale);
+  if (st != JFA_OK) return st;
+  if (a->head_dim == 192) return JFA_ERR_UNSUPPORTED;
+  if (!aligned(a->kv_offsets, 4)) return JFA_ERR_INVALID_ARG;
+  if (a->batch > 0 && a->q_len > 0) {
+    if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->o, 16) ||
+        !aligned(a->dout, 16) || !aligned(a->lse, 4) || !aligned(a->dq, 16) || !aligned(a->dk, 16) ||
+        !aligned(a->dv, 16))
+      return JFA_ERR_INVALID_ARG;
+  }
+  const Layout L = bcast_layout(a->batch, a->q_len, a->heads, a->total_k, a->head_dim, true);
+  if (!aligned(ws, 256)) return JFA_ERR_INVALID_ARG;
+  if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(w);
+  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (a->q_len == 0) return JFA_OK;
+  const int64_t n_acc = static_cast<int64_t>(a->q_len) * a->heads * a->head_dim;
+  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
+  if (cudaMemsetAsync(dq_acc, 0, 4 * n_acc, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  const int sms = sm_count();
+  if (sms <= 0) return JFA_ERR_CUDA;
+  if (a->batch > 0 && a->total_k > 0) {
+    CUtensorMap tq, tk, tv, tdo;
+    const uint64_t cols = static_cast<uint64_t>(a->heads) * a->head_dim;
+    if (!make_tmap_bf16(&tq, a->q, a->q_len, cols) || !make_tmap_bf16(&tk, a->k, a->total_k, cols) ||
+        !make_tmap_bf16(&tv, a->v, a->total_k, cols) ||
+        !make_tmap_bf16(&tdo, a->dout, static_cast<uint64_t>(a->batch) * a->q_len, cols))
+      return JFA_ERR_CUDA;
+    QueueParams qp;
+    qp.offsets = a->kv_offsets;
+    qp.batch = a->batch;
+    qp.heads = a->heads;
+    qp.total = a->total_k;
+    qp.max_seqlen = a->max_seqlen_k;
+    qp.causal = 0;
+    qp.mode = kQueueBcastBwd;
+    qp.q_len = a->q_len;
+    qp.status = status;
+    qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
+    qp.items = reinterpret_cast<int4*>(w + L.items);
+    qp.max_items = static_cast<int32_t>(L.max_items);
+    if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
+    float* lse2p = reinterpret_cast<float*>(w + L.lse2p);
+    float* deltap = reinterpret_cast<float*>(w + L.deltap);
+    if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->kv_offsets, nullptr, status, a->batch, a->heads,
+                       a->total_k, 1, a->q_len, 0, static_cast<int>(L.pad_tiles), lse2p, deltap,
+                       stream) != cudaSuccess)
+      return JFA_ERR_CUDA;
+    BwdLaunch bl;
+    bl.head_dim = a->head_dim;
+    bl.head_chunk = a->head_dim;
+    bl.offsets = a->kv_offsets;
+    bl.tile_base = qp.tile_base;
+    bl.items = qp.items;
+    bl.status = status;
+    bl.lse2p = lse2p;
+    bl.deltap = deltap;
+    bl.dq_acc = dq_acc;
+    bl.dk = a->dk;
+    bl.dv = a->dv;
+    bl.heads = a->heads;
+    bl.total = a->total_k;
+    bl.bcast = 1;
+    bl.q_len = a->q_len;
+    bl.causal = 0;
+    bl.pad_tiles = 0;
+    bl.scale = a->scale;
+    bl.budget_ns = wait_budget_ns();
+    bl.grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
+    record(a->main_kernel_events, 0, stream);
+    cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, stream);
+    record(a->main_kernel_events, 1, stream);
+    if (e != cudaSuccess) return JFA_ERR_CUDA;
+  }
+  return cuda_status(launch_bwd_post(dq_acc, a->dq, n_acc, a->scale, status, sms, stream));
+}
+
+jfa_status jfa_decode_splitkv(const jfa_decode_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!a) return JFA_ERR_INVALID_ARG;
+  if (a->batch < 0 || a->q_heads < 1 || a->kv_heads < 1 || a->page_size < 1 || a->num_pages < 0 ||
+      a->max_pages < 0 || a->num_splits < 1 || a->num_splits > 128)
+    return JFA_ERR_INVALID_ARG;
+  if (a->q_heads % a->kv_heads != 0) return JFA_ERR_INVALID_ARG;
+  const int g = a->q_heads / a->kv_heads;
+  if (a->head_dim != 128 || !(g == 1 || g == 2 || g == 4 || g == 8 || g == 16)) return JFA_ERR_UNSUPPORTED;
+  if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return JFA_ERR_INVALID_ARG;
+  if (a->batch > 0) {
+    if (!aligned(a->q, 16) || !aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->o, 16) ||
+        !aligned(a->lse, 4) || !aligned(a->page_table, 4) || !aligned(a->seqlens_k, 4))
+      return JFA_ERR_INVALID_ARG;
+    if (a->split_bounds_out && !aligned(a->split_bounds_out, 4)) return JFA_ERR_INVALID_ARG;
+  }
+  if (static_cast<int64_t>(a->max_pages) * a->page_size >= (int64_t(1) << 31)) return JFA_ERR_INVALID_ARG;
+  const Layout L = decode_layout(a->batch, a->q_heads, a->num_splits);
+  if (!aligned(ws, 256)) return JFA_ERR_INVALID_ARG;
+  if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (a->batch == 0) return JFA_OK;
+  return cuda_status(launch_decode(*a, reinterpret_cast<float*>(w + L.part_o), reinterpret_cast<float*>(w + L.part_lse),
+                                   reinterpret_cast<int32_t*>(w), stream));
+}
+
+jfa_status jfa_read_device_status(const void* ws, cudaStream_t stream, int32_t* detail) {
+  if (!aligned(ws, 4)) return JFA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return JFA_ERR_CUDA;
+  int32_t h[2] = {0, 0};
+  if (cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return JFA_ERR_CUDA;
+  if (detail) *detail = h[1];
+  return static_cast<jfa_status>(h[0]);
+}
+
+}  // extern "C"

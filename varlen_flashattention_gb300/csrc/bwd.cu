@@ -1,0 +1,649 @@
+// Jagged FlashAttention backward on tcgen05 tensor cores (sm_103a).
+//
+// What it computes ("Cutting-edge isn't plug-and-play: customizing FA4 on
+// B300", Phase 2 and its pseudocode): for each tile pair, S and dP are rebuilt
+// from Q, K, V, dO; P comes from S and the LSE saved by the forward; then
+//   D = rowsum(dO * O) ("delta"), dS = P * (dP - D),
+//   dV += P^T dO, dK += scale dS^T Q, dQ += scale dS K.
+// Broadcast-Q ("Optimizing Jagged Flash Attention with TLX", third
+// paragraph): every sequence reads the same Q, so dQ sums over the batch.
+// Head-axis chunking (TwelveLabs Phase 2): with head_dim 192 one pass owns a
+// 64-wide slice c of dQ/dK/dV, while S and dP are still accumulated over all
+// of the head dimension (three passes rebuild S and dP).
+//
+// Kernel organisation (GB300 design):
+//  * persistent grid; items are (sequence, head, 128-row K/V tile[, slice])
+//    from the longest-first queue; K and V stay in shared memory for the item
+//    while the producer streams the Q, dO tiles (and their LSE/delta rows)
+//    of every query tile that sees this K/V tile;
+//  * scores are computed transposed, S^T = K Q^T, so TMEM lane = key row and
+//    P^T can feed dV += P^T dO straight from TMEM;
+//  * warps 0-3 (one thread per key row) turn S^T into P^T (bf16, written over
+//    S^T in TMEM) and dP^T into dS^T (bf16, written to shared memory in the
+//    128B-swizzled layout the tensor core reads both as dS^T for dK and as
+//    dS for dQ);
+//  * warps 4-7 drain dQ from TMEM into an fp32 accumulator with vector
+//    atomics (the cross-CTA reduction; contended in broadcast-Q) and write dK
+//    and dV at the end of each item;
+//  * warp 8 = TMA producer, warp 9 = MMA issuer.
+//  * Order inside one query tile: S^T, dP^T, dV, dK, dQ. The Q/dO stage is
+//    released only after the last MMA that reads it (dK), so a single-stage
+//    ring cannot deadlock (TwelveLabs, bug hunting).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "jfa_internal.h"
+#include "ptx.cuh"
+
+namespace jfa {
+
+struct BwdParams {
+  const int32_t* offsets;     // self: sequence offsets; broadcast: K/V offsets
+  const int32_t* tile_base;   // self: padded q-tile index of each sequence
+  const int4* items;
+  int32_t* status;
+  const float* lse2p;         // log2-scaled LSE, tile-padded
+  const float* deltap;        // delta, tile-padded
+  float* dq_acc;              // fp32 [rows_q, H, D]
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int32_t heads, total, bcast, q_len, causal, n_chunks;
+  int32_t pad_tiles;          // self: tiles per head in the padded arrays
+  float scale, scale_log2;
+  uint64_t budget_ns;
+};
+
+template <int D, int DC>
+struct BwdLayout {
+  static constexpr int kAtoms = D / 64;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStages = (D == 192) ? 1 : 2;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffQ = 2 * kTileBytes;                       // kStages x Q
+  static constexpr int kOffDO = kOffQ + kStages * kTileBytes;         // kStages x dO
+  static constexpr int kOffDS = kOffDO + kStages * kTileBytes;        // 128 x 128 bf16
+  static constexpr int kOffRow = kOffDS + kTile * kTile * 2;          // kStages x (lse2[128], delta[128])
+  static constexpr int kOffBars = kOffRow + kStages * 1024;
+  // kv_full, kv_empty, q_full[S], q_empty[S], s_full, p_full, dp_full, ds_full, ds_free,
+  // dq_full, dq_free, acc_full, acc_free, drain
+  static constexpr int kNumBars = 2 + 2 * kStages + 10;
+  static constexpr int kOffMisc = kOffBars + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 64;
+  static constexpr int kAlloc = kBytes + 256;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + DC;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kColDK + DC <= kTmemCols, "TMEM budget");
+  static_assert(kAlloc <= 232448, "shared memory budget");
+};
+
+struct BwdItem {
+  int b, h, t, c;  // sequence, head, K/V tile, head-dim slice
+  int kv_row0;     // first K/V row of the tile
+  int Lk, Lq;
+  int i0, nq;      // query tiles i0 .. i0+nq-1
+  int q_row0;      // Q row of query tile 0 (TMA)
+  int do_row0;     // dO row of query tile 0 (TMA)
+  int64_t row_base;  // padded LSE/delta index of query tile 0 (times 128)
+};
+
+__device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
+  const int idx = v / p.n_chunks;
+  BwdItem I;
+  I.c = v - idx * p.n_chunks;
+  const int4 it = p.items[idx];
+  I.b = it.x;
+  I.h = it.y;
+  I.t = it.z;
+  const int s0 = p.offsets[I.b], s1 = p.offsets[I.b + 1];
+  I.Lk = s1 - s0;
+  I.kv_row0 = s0 + kTile * I.t;
+  if (!p.bcast) {
+    I.Lq = I.Lk;
+    I.q_row0 = s0;
+    I.do_row0 = s0;
+    I.row_base = (static_cast<int64_t>(I.h) * p.pad_tiles + p.tile_base[I.b]) * kTile;
+  } else {
+    I.Lq = p.q_len;
+    I.q_row0 = 0;
+    I.do_row0 = I.b * p.q_len;
+    const int nqt = (p.q_len + kTile - 1) / kTile;
+    I.row_base = ((static_cast<int64_t>(I.b) * p.heads + I.h) * nqt) * kTile;
+  }
+  const int nq = (I.Lq + kTile - 1) / kTile;
+  I.i0 = p.causal ? I.t : 0;
+  I.nq = nq - I.i0;
+  return I;
+}
+
+template <int D, int DC>
+__global__ void __launch_bounds__(320, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const BwdParams p) {
+  using Lay = BwdLayout<D, DC>;
+  constexpr int kSt = Lay::kStages;
+  constexpr uint32_t kIdS = ptx::idesc_bf16(128, 128, false, false);   // S^T, dP^T
+  constexpr uint32_t kIdAcc = ptx::idesc_bf16(128, DC, false, true);   // dV, dK
+  constexpr uint32_t kIdDQ = ptx::idesc_bf16(128, DC, true, true);     // dQ (A = dS, M-major)
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the layout needs a 1024-byte aligned base; the launch reserves 256 bytes of slack
+  if (smem + Lay::kBytes > smem_raw + Lay::kAlloc) {
+    if (threadIdx.x == 0) atomicCAS(p.status, JFA_OK, JFA_ERR_UNSUPPORTED);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* kv_empty = bars + 1;
+  uint64_t* q_full = bars + 2;
+  uint64_t* q_empty = bars + 2 + kSt;
+  uint64_t* s_full = bars + 2 + 2 * kSt;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* dp_full = s_full + 2;
+  uint64_t* ds_full = s_full + 3;
+  uint64_t* ds_free = s_full + 4;
+  uint64_t* dq_full = s_full + 5;
+  uint64_t* dq_free = s_full + 6;
+  uint64_t* acc_full = s_full + 7;
+  uint64_t* acc_free = s_full + 8;
+  uint64_t* drain = s_full + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
+  ptx::CtaCtl* ctl = reinterpret_cast<ptx::CtaCtl*>(smem + Lay::kOffMisc + 8);
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(kv_full, 1);
+    ptx::mbar_init(kv_empty, 1);
+    for (int i = 0; i < kSt; ++i) {
+      ptx::mbar_init(q_full + i, 1);
+      ptx::mbar_init(q_empty + i, 1);
+    }
+    ptx::mbar_init(s_full, 1);
+    ptx::mbar_init(p_full, 4);
+    ptx::mbar_init(dp_full, 1);
+    ptx::mbar_init(ds_full, 4);
+    ptx::mbar_init(ds_free, 1);
+    ptx::mbar_init(dq_full, 1);
+    ptx::mbar_init(dq_free, 4);
+    ptx::mbar_init(acc_full, 1);
+    ptx::mbar_init(acc_free, 4);
+    ptx::mbar_init(drain, 1);
+    ctl->abort = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 8 && lane == 0) {
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+    ptx::prefetch_tmap(&tm_do);
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(tmem_slot, Lay::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n_work = p.status[2] * p.n_chunks;
+  int32_t* status = p.status;
+  const uint64_t budget = p.budget_ns;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t pos = 0, kitem = 0;
+      bool ok = true;
+      for (int v = blockIdx.x; ok && v < n_work; v += gridDim.x) {
+        const BwdItem I = bwd_item(p, v);
+        if (I.nq <= 0) continue;
+        if (!(ok = ptx::mbar_wait(kv_empty, (kitem & 1) ^ 1, ctl, status, kSiteBwdProdKV, budget))) break;
+        ptx::mbar_arrive_expect_tx(kv_full, 2 * Lay::kTileBytes);
+#pragma unroll
+        for (int a = 0; a < Lay::kAtoms; ++a) {
+          ptx::tma_load_2d(smem + Lay::kOffK + a * 16384, &tm_k, kv_full, I.h * D + 64 * a, I.kv_row0);
+          ptx::tma_load_2d(smem + Lay::kOffV + a * 16384, &tm_v, kv_full, I.h * D + 64 * a, I.kv_row0);
+        }
+        for (int ii = 0; ii < I.nq; ++ii) {
+          const int i = I.i0 + ii;
+          const uint32_t st = pos % kSt, round = pos / kSt;
+          if (!(ok = ptx::mbar_wait(q_empty + st, (round & 1) ^ 1, ctl, status, kSiteBwdProdQ, budget))) break;
+          ptx::mbar_arrive_expect_tx(q_full + st, 2 * Lay::kTileBytes + 1024);
+          uint8_t* qd = smem + Lay::kOffQ + st * Lay::kTileBytes;
+          uint8_t* dd = smem + Lay::kOffDO + st * Lay::kTileBytes;
+#pragma unroll
+          for (int a = 0; a < Lay::kAtoms; ++a) {
+            ptx::tma_load_2d(qd + a * 16384, &tm_q, q_full + st, I.h * D + 64 * a, I.q_row0 + kTile * i);
+            ptx::tma_load_2d(dd + a * 16384, &tm_do, q_full + st, I.h * D + 64 * a, I.do_row0 + kTile * i);
+          }
+          uint8_t* rows = smem + Lay::kOffRow + st * 1024;
+          ptx::bulk_load(rows, p.lse2p + I.row_base + static_cast<int64_t>(kTile) * i, 512, q_full + st);
+          ptx::bulk_load(rows + 512, p.deltap + I.row_base + static_cast<int64_t>(kTile) * i, 512, q_full + st);
+          ++pos;
+        }
+        ++kitem;
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t pos = 0, x = 0, kitem = 0;
+      bool ok = true;
+      const uint32_t k_addr = ptx::smem_u32(smem + Lay::kOffK);
+      const uint32_t v_addr = ptx::smem_u32(smem + Lay::kOffV);
+      const uint32_t ds_addr = ptx::smem_u32(smem + Lay::kOffDS);
+      for (int v = blockIdx.x; ok && v < n_work; v += gridDim.x) {
+        const BwdItem I = bwd_item(p, v);
+        if (I.nq <= 0) continue;
+        if (!(ok = ptx::mbar_wait(kv_full, kitem & 1, ctl, status, kSiteBwdMmaKV, budget))) break;
+        ptx::tc_fence_after();
+        for (int ii = 0; ii < I.nq; ++ii, ++x) {
+          const uint32_t st = pos % kSt, round = pos / kSt;
+          if (!(ok = ptx::mbar_wait(q_full + st, round & 1, ctl, status, kSiteBwdMmaQ, budget))) break;
+          ptx::tc_fence_after();
+          const uint32_t q_addr = ptx::smem_u32(smem + Lay::kOffQ + st * Lay::kTileBytes);
+          const uint32_t do_addr = ptx::smem_u32(smem + Lay::kOffDO + st * Lay::kTileBytes);
+          // S^T = K Q^T
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            ptx::mma_ss(tmem + Lay::kColS, ptx::sdesc_sw128(k_addr + off, 16, 1024),
+                        ptx::sdesc_sw128(q_addr + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(s_full);
+          // dP^T = V dO^T into the columns dQ of the previous tile used
+          if (x > 0) {
+            if (!(ok = ptx::mbar_wait(dq_free, (x - 1) & 1, ctl, status, kSiteBwdMmaDQFree, budget))) break;
+            ptx::tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            ptx::mma_ss(tmem + Lay::kColDP, ptx::sdesc_sw128(v_addr + off, 16, 1024),
+                        ptx::sdesc_sw128(do_addr + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(dp_full);
+          // dV += P^T dO[:, slice]
+          if (!(ok = ptx::mbar_wait(p_full, x & 1, ctl, status, kSiteBwdMmaP, budget))) break;
+          if (ii == 0 && kitem > 0) {
+            if (!(ok = ptx::mbar_wait(acc_free, (kitem - 1) & 1, ctl, status, kSiteBwdMmaAccFree, budget))) break;
+          }
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            ptx::mma_ts(tmem + Lay::kColDV, tmem + Lay::kColS + kk * 8,
+                        ptx::sdesc_sw128(do_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdAcc,
+                        (ii > 0 || kk > 0) ? 1u : 0u);
+          }
+          // dK += dS^T Q[:, slice]
+          if (!(ok = ptx::mbar_wait(ds_full, x & 1, ctl, status, kSiteBwdMmaDS, budget))) break;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            ptx::mma_ss(tmem + Lay::kColDK, ptx::sdesc_sw128(ds_addr + off, 16, 1024),
+                        ptx::sdesc_sw128(q_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdAcc,
+                        (ii > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(q_empty + st);  // last reader of this Q/dO stage
+          // dQ(tile) = dS K[:, slice] into the dP^T columns
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            ptx::mma_ss(tmem + Lay::kColDP, ptx::sdesc_sw128(ds_addr + kk * 2048, 16384, 1024),
+                        ptx::sdesc_sw128(k_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdDQ,
+                        kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(dq_full);
+          ptx::mma_commit(ds_free);
+          ++pos;
+        }
+        if (!ok) break;
+        ptx::mma_commit(kv_empty);
+        ptx::mma_commit(acc_full);
+        ++kitem;
+      }
+      ptx::mma_commit(drain);
+      ptx::CtaCtl no_abort{0, 0};
+      ptx::mbar_wait(drain, 0, &no_abort, nullptr, kSiteBwdDrain, budget);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ P^T and dS^T (thread = key row)
+    const int r = warp * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl = p.scale_log2;
+    uint32_t pos = 0, x = 0;
+    bool ok = true;
+    uint8_t* ds_row = smem + Lay::kOffDS + r * 128;
+    const int sw = r & 7;
+    for (int v = blockIdx.x; ok && v < n_work; v += gridDim.x) {
+      const BwdItem I = bwd_item(p, v);
+      if (I.nq <= 0) continue;
+      const int rk = I.Lk - kTile * I.t;  // valid key rows of the tile
+      for (int ii = 0; ii < I.nq; ++ii, ++x) {
+        const int i = I.i0 + ii;
+        const uint32_t st = pos % kSt;
+        const float* lse2 = reinterpret_cast<const float*>(smem + Lay::kOffRow + st * 1024);
+        const float* dlt = lse2 + 128;
+        const int rq = I.Lq - kTile * i;  // valid query columns
+        const bool masked = rk < kTile || rq < kTile || (p.causal && i == I.t);
+        const int cmax = (p.causal && i == I.t) ? r : 0;  // causal: query col c visible iff c >= r (same tile)
+        const bool row_ok = r < rk;
+        if (!(ok = ptx::mbar_wait(s_full, x & 1, ctl, status, kSiteBwdSoftS, budget))) break;
+        ptx::tc_fence_after();
+        // P^T = 2^(S^T * scale * log2e - lse2[q])
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t sv[2][32];
+          ptx::tmem_ld32(tmem + lane_base + Lay::kColS + 64 * h2, sv[0]);
+          ptx::tmem_ld32(tmem + lane_base + Lay::kColS + 64 * h2 + 32, sv[1]);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence32(sv[0]);
+          ptx::reg_fence32(sv[1]);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            uint32_t pk[16];
+            const int cb = 64 * h2 + 32 * u;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int c0 = cb + 2 * e;
+              float p0 = ptx::ex2(fmaf(__uint_as_float(sv[u][2 * e]), sl, -lse2[c0]));
+              float p1 = ptx::ex2(fmaf(__uint_as_float(sv[u][2 * e + 1]), sl, -lse2[c0 + 1]));
+              if (masked) {
+                if (!row_ok || c0 >= rq || c0 < cmax) p0 = 0.f;
+                if (!row_ok || c0 + 1 >= rq || c0 + 1 < cmax) p1 = 0.f;
+              }
+              pk[e] = ptx::pack_bf16(p0, p1);
+            }
+            ptx::tmem_st16(tmem + lane_base + Lay::kColS + cb / 2, pk);
+          }
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(p_full);
+        // dS^T = P^T * (dP^T - delta[q])
+        if (!(ok = ptx::mbar_wait(dp_full, x & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
+        ptx::tc_fence_after();
+        if (x > 0) {
+          if (!(ok = ptx::mbar_wait(ds_free, (x - 1) & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
+        }
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t dp[2][32];
+          uint32_t pp[32];
+          ptx::tmem_ld32(tmem + lane_base + Lay::kColDP + 64 * h2, dp[0]);
+          ptx::tmem_ld32(tmem + lane_base + Lay::kColDP + 64 * h2 + 32, dp[1]);
+          ptx::tmem_ld32(tmem + lane_base + Lay::kColS + 32 * h2, pp);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence32(dp[0]);
+          ptx::reg_fence32(dp[1]);
+          ptx::reg_fence32(pp);
+          // 64 query columns = one 128-byte swizzled row of atom h2
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int cl = 8 * ch + 2 * e;  // column within the 64-wide half
+              const uint32_t pw = pp[cl / 2];
+              const float d0 = __uint_as_float(dp[cl >> 5][cl & 31]) - dlt[64 * h2 + cl];
+              const float d1 = __uint_as_float(dp[(cl + 1) >> 5][(cl + 1) & 31]) - dlt[64 * h2 + cl + 1];
+              w[e] = ptx::pack_bf16(ptx::bf16lo(pw) * d0, ptx::bf16hi(pw) * d1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(ds_row + h2 * 16384 + ((ch ^ sw) << 4));
+            *dst = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ds_full);
+        ++pos;
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ dQ drain + dK/dV epilogue
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t x = 0, kitem = 0;
+    bool ok = true;
+    for (int v = blockIdx.x; ok && v < n_work; v += gridDim.x) {
+      const BwdItem I = bwd_item(p, v);
+      if (I.nq <= 0) continue;
+      for (int ii = 0; ii < I.nq; ++ii, ++x) {
+        const int i = I.i0 + ii;
+        if (!(ok = ptx::mbar_wait(dq_full, x & 1, ctl, status, kSiteBwdDQ, budget))) break;
+        ptx::tc_fence_after();
+        const bool q_ok = kTile * i + r < I.Lq;
+        float* dst = p.dq_acc + (static_cast<int64_t>(I.q_row0 + kTile * i + r) * p.heads + I.h) * D + I.c * DC;
+#pragma unroll 1
+        for (int c = 0; c < DC / 32; ++c) {
+          uint32_t dq[32];
+          ptx::tmem_ld32(tmem + lane_base + Lay::kColDP + 32 * c, dq);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence32(dq);
+          if (q_ok) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              float4 val = make_float4(__uint_as_float(dq[4 * e]), __uint_as_float(dq[4 * e + 1]),
+                                       __uint_as_float(dq[4 * e + 2]), __uint_as_float(dq[4 * e + 3]));
+              atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + 4 * e), val);
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(dq_free);
+      }
+      if (!ok) break;
+      if (!(ok = ptx::mbar_wait(acc_full, kitem & 1, ctl, status, kSiteBwdEpi, budget))) break;
+      ptx::tc_fence_after();
+      const bool k_ok = r < I.Lk - kTile * I.t;
+      const int64_t orow = (static_cast<int64_t>(I.kv_row0 + r) * p.heads + I.h) * D + I.c * DC;
+#pragma unroll 1
+      for (int c = 0; c < DC / 32; ++c) {
+        uint32_t a[32], b[32];
+        ptx::tmem_ld32(tmem + lane_base + Lay::kColDV + 32 * c, a);
+        ptx::tmem_ld32(tmem + lane_base + Lay::kColDK + 32 * c, b);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence32(a);
+        ptx::reg_fence32(b);
+        if (k_ok) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t wv[4], wk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              wv[e] = ptx::pack_bf16(__uint_as_float(a[8 * q4 + 2 * e]), __uint_as_float(a[8 * q4 + 2 * e + 1]));
+              wk[e] = ptx::pack_bf16(__uint_as_float(b[8 * q4 + 2 * e]) * p.scale,
+                                     __uint_as_float(b[8 * q4 + 2 * e + 1]) * p.scale);
+            }
+            ptx::st_v4(p.dv + orow + 32 * c + 8 * q4, wv[0], wv[1], wv[2], wv[3]);
+            ptx::st_v4(p.dk + orow + 32 * c + 8 * q4, wk[0], wk[1], wk[2], wk[3]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(acc_free);
+      ++kitem;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, Lay::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ pre / post
+
+// delta = rowsum(dO * O) and lse2 = LSE * log2(e), written in a layout padded
+// to whole 128-row query tiles (zeros past the end of a sequence), so that the
+// backward can fetch one tile's 128 values with a single aligned bulk copy.
+// One CTA per padded query tile (blockIdx.x) and head (blockIdx.y); one warp
+// per row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                      const __nv_bfloat16* __restrict__ dout,
+                                                      const float* __restrict__ lse, const int32_t* offsets,
+                                                      const int32_t* tile_base, const int32_t* status, int batch,
+                                                      int heads, int total, int bcast, int q_len, int pad_tiles,
+                                                      float* __restrict__ lse2p, float* __restrict__ deltap) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  const int gt = blockIdx.x, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (status[0] != JFA_OK) return;
+  // locate the tile: self -> (b, i) by binary search over tile_base; broadcast -> (b, i) directly
+  int b, i, Lq;
+  int64_t qrow0, lse_base, pad_base;
+  if (!bcast) {
+    if (gt >= tile_base[batch]) return;
+    int lo = 0, hi = batch;  // largest b with tile_base[b] <= gt
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tile_base[mid] <= gt) lo = mid; else hi = mid;
+    }
+    b = lo;
+    while (b + 1 < batch && tile_base[b + 1] <= gt) ++b;
+    i = gt - tile_base[b];
+    const int s0 = offsets[b];
+    Lq = offsets[b + 1] - s0;
+    qrow0 = s0 + static_cast<int64_t>(kTile) * i;
+    lse_base = static_cast<int64_t>(h) * total + qrow0;
+    pad_base = (static_cast<int64_t>(h) * pad_tiles + gt) * kTile;
+  } else {
+    const int nqt = (q_len + kTile - 1) / kTile;
+    b = gt / nqt;
+    i = gt - b * nqt;
+    if (b >= batch) return;
+    Lq = q_len;
+    qrow0 = static_cast<int64_t>(b) * q_len + static_cast<int64_t>(kTile) * i;
+    lse_base = (static_cast<int64_t>(b) * heads + h) * q_len + static_cast<int64_t>(kTile) * i;
+    pad_base = ((static_cast<int64_t>(b) * heads + h) * nqt + i) * kTile;
+  }
+  for (int r = warp; r < kTile; r += 8) {
+    const bool ok = kTile * i + r < Lq;
+    float acc = 0.f;
+    if (ok) {
+      const __nv_bfloat16* orow = o + ((qrow0 + r) * heads + h) * D;
+      const __nv_bfloat16* drow = dout + ((qrow0 + r) * heads + h) * D;
+#pragma unroll
+      for (int e = lane * 2; e < D; e += 64) {
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(orow + e);
+        const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(drow + e);
+        acc = fmaf(__bfloat162float(a.x), __bfloat162float(c.x), acc);
+        acc = fmaf(__bfloat162float(a.y), __bfloat162float(c.y), acc);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    }
+    if (lane == 0) {
+      deltap[pad_base + r] = ok ? acc : 0.f;
+      lse2p[pad_base + r] = ok ? lse[lse_base + r] * kLog2e : 0.f;
+    }
+  }
+}
+
+// dQ = scale * dQ_accumulated, fp32 -> bf16, four elements per thread.
+__global__ void bwd_post_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, int64_t n4, float scale,
+                                const int32_t* status) {
+  if (status[0] != JFA_OK) return;
+  for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < n4;
+       k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 v = acc[k];
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x * scale, v.y * scale);
+    __nv_bfloat162 c = __floats2bfloat162_rn(v.z * scale, v.w * scale);
+    uint2 w;
+    w.x = *reinterpret_cast<uint32_t*>(&a);
+    w.y = *reinterpret_cast<uint32_t*>(&c);
+    dq[k] = w;
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+
+template <int D, int DC>
+static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream) {
+  using Lay = BwdLayout<D, DC>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, DC>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  bwd_kernel<D, DC><<<grid, 320, Lay::kAlloc, stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, cudaStream_t stream) {
+  BwdParams p;
+  p.offsets = L.offsets;
+  p.tile_base = L.tile_base;
+  p.items = L.items;
+  p.status = L.status;
+  p.lse2p = L.lse2p;
+  p.deltap = L.deltap;
+  p.dq_acc = L.dq_acc;
+  p.dk = static_cast<__nv_bfloat16*>(L.dk);
+  p.dv = static_cast<__nv_bfloat16*>(L.dv);
+  p.heads = L.heads;
+  p.total = L.total;
+  p.bcast = L.bcast;
+  p.q_len = L.q_len;
+  p.causal = L.causal;
+  p.n_chunks = L.head_dim / L.head_chunk;
+  p.pad_tiles = L.pad_tiles;
+  p.scale = L.scale;
+  p.scale_log2 = L.scale * 1.4426950408889634f;
+  p.budget_ns = L.budget_ns;
+  if (L.head_dim == 64 && L.head_chunk == 64) return launch_bwd_t<64, 64>(tq, tk, tv, tdo, p, L.grid, stream);
+  if (L.head_dim == 128 && L.head_chunk == 128) return launch_bwd_t<128, 128>(tq, tk, tv, tdo, p, L.grid, stream);
+  if (L.head_dim == 128 && L.head_chunk == 64) return launch_bwd_t<128, 64>(tq, tk, tv, tdo, p, L.grid, stream);
+  if (L.head_dim == 192 && L.head_chunk == 64) return launch_bwd_t<192, 64>(tq, tk, tv, tdo, p, L.grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_pre(int head_dim, const void* o, const void* dout, const float* lse, const int32_t* offsets,
+                           const int32_t* tile_base, const int32_t* status, int batch, int heads, int total, int bcast,
+                           int q_len, int pad_tiles, int grid_tiles, float* lse2p, float* deltap,
+                           cudaStream_t stream) {
+  dim3 grid(grid_tiles, heads);
+  auto O = static_cast<const __nv_bfloat16*>(o);
+  auto dO = static_cast<const __nv_bfloat16*>(dout);
+  if (head_dim == 64)
+    bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, status, batch, heads, total, bcast,
+                                                 q_len, pad_tiles, lse2p, deltap);
+  else if (head_dim == 128)
+    bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, status, batch, heads, total, bcast,
+                                                  q_len, pad_tiles, lse2p, deltap);
+  else if (head_dim == 192)
+    bwd_pre_kernel<192><<<grid, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, status, batch, heads, total, bcast,
+                                                  q_len, pad_tiles, lse2p, deltap);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_post(const float* acc, void* dq, int64_t n, float scale, const int32_t* status, int sms,
+                            cudaStream_t stream) {
+  const int64_t n4 = n / 4;
+  int64_t blocks = (n4 + 255) / 256;
+  if (blocks > static_cast<int64_t>(sms) * 16) blocks = static_cast<int64_t>(sms) * 16;
+  if (blocks < 1) blocks = 1;
+  bwd_post_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(reinterpret_cast<const float4*>(acc),
+                                                                 static_cast<uint2*>(dq), n4, scale, status);
+  return cudaGetLastError();
+}
+
+}  // namespace jfa

@@ -1,0 +1,397 @@
+// Split-KV paged GQA decode: one query token per sequence against a KV cache
+// addressed through a page table, the KV range split into parallel parts
+// whose partial softmax results are merged by a second kernel.
+//
+// Sources: "Optimizing FlashAttention-4 for Efficient Inference" (hpjadul),
+// sections PR 1940 (parallelism across the KV dimension), PR 1999 / PR 2104
+// (KV pages of any size), PR 2186 (GQA packing: the query heads that share a
+// KV head are processed in one tile so K/V are read once) and "Key
+// Enhancements" (irregular gathers use per-thread asynchronous loads rather
+// than bulk tensor copies).
+//
+// Design (GB300): the path is bound by HBM reads of K and V (about 0.5 flop
+// per byte), so the kernel is organised around memory-level parallelism:
+// every lane issues 16-byte non-caching loads of whole 256-byte cache rows
+// straight into registers, one 16-token block at a time, while the GQA group
+// of query heads rides along as the rows of an m16n8k16 register MMA. The
+// MMA is used to cut issue slots (no shuffle reductions), not for its FLOPs;
+// tcgen05's 64/128-row tiles would waste more of the tensor core on 1..16
+// real rows than this does.
+//
+// Index mappings used below (each lane: g = lane / 4, q = lane % 4):
+//  * QK^T: head dimension permuted so that each lane's four k-values of
+//    k-steps 2c' and 2c'+1 are the 8 contiguous bf16 at d = 32c' + 8q;
+//    Q is loaded with the same permutation, so dot products are unchanged.
+//  * PV: output column n = g of n-tile j is head-dimension d = 16g + j, so a
+//    lane reads 32 contiguous bytes of each V row it needs; the permutation
+//    is undone when the partial result is written.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "jfa_internal.h"
+#include "ptx.cuh"
+
+namespace jfa {
+
+struct DecodeParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* kc;
+  const __nv_bfloat16* vc;
+  const int32_t* page_table;
+  const int32_t* seqlens;
+  int32_t batch, hq, hkv, page_size, num_pages, max_pages, num_splits;
+  float scale_log2;
+  float* part_o;        // [S, B, Hq, 128], normalised within the split
+  float* part_lse;      // [S, B, Hq], natural log, -inf when empty
+  int32_t* bounds_out;  // optional [B, S, 2]
+  int32_t* status;
+};
+
+constexpr int kDecD = 128;
+constexpr int kDecWarps = 4;
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void flag_bad(int32_t* status, int32_t code) {
+  if (atomicCAS(status, JFA_OK, JFA_ERR_BAD_INPUT) == JFA_OK) status[1] = code;
+}
+
+template <int G>
+__global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecodeParams p) {
+  static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "GQA group");
+  constexpr bool kTwoRowHalves = (G == 16);  // rows g+8 hold real heads only when G == 16
+
+  __shared__ float s_m[kDecWarps][G];
+  __shared__ float s_l[kDecWarps][G];
+  __shared__ __align__(16) float s_o[kDecWarps][G][kDecD];
+
+  const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, qq = lane & 3;
+  const int S = p.num_splits, P = p.page_size;
+
+  int L = p.seqlens[b];
+  const int64_t cap = static_cast<int64_t>(p.max_pages) * P;
+  if (L < 0 || L > cap) {
+    if (threadIdx.x == 0) flag_bad(p.status, kSiteDecodeTable);
+    L = 0;
+  }
+  const int64_t c = (static_cast<int64_t>(L) + S - 1) / S;
+  const int lo = static_cast<int>(min(static_cast<int64_t>(s) * c, static_cast<int64_t>(L)));
+  const int hi = static_cast<int>(min(static_cast<int64_t>(s + 1) * c, static_cast<int64_t>(L)));
+  if (p.bounds_out && kvh == 0 && threadIdx.x == 0) {
+    p.bounds_out[(static_cast<int64_t>(b) * S + s) * 2 + 0] = lo;
+    p.bounds_out[(static_cast<int64_t>(b) * S + s) * 2 + 1] = hi;
+  }
+
+  // Q fragments (A operand, rows = query heads of this KV group).
+  uint32_t qa[8][4];
+  {
+    const __nv_bfloat16* qb = p.q + (static_cast<int64_t>(b) * p.hq + static_cast<int64_t>(kvh) * G) * kDecD;
+#pragma unroll
+    for (int cs = 0; cs < 8; ++cs) {
+      const int d0 = 32 * (cs >> 1) + 8 * qq + 4 * (cs & 1);
+      uint32_t r0a = 0, r0b = 0, r1a = 0, r1b = 0;
+      if (gq < G) {
+        const uint2 v = *reinterpret_cast<const uint2*>(qb + gq * kDecD + d0);
+        r0a = v.x;
+        r0b = v.y;
+      }
+      if (kTwoRowHalves) {
+        const uint2 v = *reinterpret_cast<const uint2*>(qb + (gq + 8) * kDecD + d0);
+        r1a = v.x;
+        r1b = v.y;
+      }
+      qa[cs][0] = r0a;
+      qa[cs][1] = r1a;
+      qa[cs][2] = r0b;
+      qa[cs][3] = r1b;
+    }
+  }
+
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float acc[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+  const int64_t row_stride = static_cast<int64_t>(p.hkv) * kDecD;  // elements between tokens of a page
+  const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+  const int nblk = (hi - lo + 15) >> 4;
+
+  for (int kb = warp; kb < nblk; kb += kDecWarps) {
+    const int t0 = lo + kb * 16;
+    // page of token t0 + (lane % 16), validated
+    int pg = 0;
+    {
+      const int tok = t0 + (lane & 15);
+      if (tok < hi) {
+        pg = pt[tok / P];
+        if (pg < 0 || pg >= p.num_pages) {
+          flag_bad(p.status, kSiteDecodeTable);
+          pg = 0;
+        }
+      }
+    }
+    // K rows of tokens g and g+8 (B operand of QK^T)
+    uint4 kr[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int tk = gq + 8 * u;
+      const int page = __shfl_sync(0xffffffffu, pg, tk);
+      const int tok = t0 + tk;
+      const __nv_bfloat16* row =
+          p.kc + (static_cast<int64_t>(page) * P + (tok % P)) * row_stride + static_cast<int64_t>(kvh) * kDecD;
+#pragma unroll
+      for (int c2 = 0; c2 < 4; ++c2)
+        kr[u][c2] = (tok < hi) ? ptx::ld_nc_v4(row + 32 * c2 + 8 * qq) : make_uint4(0, 0, 0, 0);
+    }
+    // V rows of tokens 2q, 2q+1, 2q+8, 2q+9 (B operand of PV)
+    uint4 vr[4][2];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int tv = 2 * qq + (w & 1) + 8 * (w >> 1);
+      const int page = __shfl_sync(0xffffffffu, pg, tv);
+      const int tok = t0 + tv;
+      const __nv_bfloat16* row =
+          p.vc + (static_cast<int64_t>(page) * P + (tok % P)) * row_stride + static_cast<int64_t>(kvh) * kDecD;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2)
+        vr[w][h2] = (tok < hi) ? ptx::ld_nc_v4(row + 16 * gq + 8 * h2) : make_uint4(0, 0, 0, 0);
+    }
+
+    // S = Q K^T for 16 tokens (two n-tiles of 8)
+    float sc[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      sc[u][0] = sc[u][1] = sc[u][2] = sc[u][3] = 0.f;
+#pragma unroll
+      for (int cs = 0; cs < 8; ++cs) {
+        const uint4 v = kr[u][cs >> 1];
+        const uint32_t b0 = (cs & 1) ? v.z : v.x;
+        const uint32_t b1 = (cs & 1) ? v.w : v.y;
+        mma16816(sc[u], qa[cs], b0, b1);
+      }
+    }
+    // mask tokens past the split end
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        if (t0 + 8 * u + 2 * qq + e >= hi) {
+          sc[u][e] = -INFINITY;
+          sc[u][2 + e] = -INFINITY;
+        }
+
+    // online softmax, row g (and g+8 when G == 16)
+    float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    const float mn0 = fmaxf(m0, mx0 * p.scale_log2);
+    const float al0 = ptx::ex2(m0 - mn0);
+    m0 = mn0;
+    float pr[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      pr[u][0] = ptx::ex2(fmaf(sc[u][0], p.scale_log2, -mn0));
+      pr[u][1] = ptx::ex2(fmaf(sc[u][1], p.scale_log2, -mn0));
+    }
+    l0 = l0 * al0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+    float al1 = 1.f;
+    if (kTwoRowHalves) {
+      float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn1 = fmaxf(m1, mx1 * p.scale_log2);
+      al1 = ptx::ex2(m1 - mn1);
+      m1 = mn1;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        pr[u][2] = ptx::ex2(fmaf(sc[u][2], p.scale_log2, -mn1));
+        pr[u][3] = ptx::ex2(fmaf(sc[u][3], p.scale_log2, -mn1));
+      }
+      l1 = l1 * al1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+    } else {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) pr[u][2] = pr[u][3] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      acc[j][0] *= al0;
+      acc[j][1] *= al0;
+      if (kTwoRowHalves) {
+        acc[j][2] *= al1;
+        acc[j][3] *= al1;
+      }
+    }
+    // P as the A operand (k = 16 tokens)
+    uint32_t pa[4];
+    pa[0] = ptx::pack_bf16(pr[0][0], pr[0][1]);
+    pa[1] = ptx::pack_bf16(pr[0][2], pr[0][3]);
+    pa[2] = ptx::pack_bf16(pr[1][0], pr[1][1]);
+    pa[3] = ptx::pack_bf16(pr[1][2], pr[1][3]);
+    // O += P V over the 16 n-tiles of the (permuted) head dimension
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int wd = j >> 1;  // 32-bit word within the 16-element chunk
+      const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+      auto word = [&](int w) -> uint32_t {
+        const uint4 x = vr[w][wd >> 2];
+        const int k = wd & 3;
+        return k == 0 ? x.x : (k == 1 ? x.y : (k == 2 ? x.z : x.w));
+      };
+      const uint32_t b0 = __byte_perm(word(0), word(1), sel);
+      const uint32_t b1 = __byte_perm(word(2), word(3), sel);
+      mma16816(acc[j], pa, b0, b1);
+    }
+  }
+
+  // row sums across the quad
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+  // per-warp partials to shared memory (un-permuting the head dimension)
+  if (gq < G) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      s_o[warp][gq][16 * (2 * qq) + j] = acc[j][0];
+      s_o[warp][gq][16 * (2 * qq + 1) + j] = acc[j][1];
+    }
+    if (qq == 0) {
+      s_m[warp][gq] = m0;
+      s_l[warp][gq] = l0;
+    }
+  }
+  if (kTwoRowHalves) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      s_o[warp][gq + 8 < G ? gq + 8 : 0][16 * (2 * qq) + j] = acc[j][2];
+      s_o[warp][gq + 8 < G ? gq + 8 : 0][16 * (2 * qq + 1) + j] = acc[j][3];
+    }
+    if (qq == 0) {
+      s_m[warp][gq + 8] = m1;
+      s_l[warp][gq + 8] = l1;
+    }
+  }
+  __syncthreads();
+
+  // merge the four warps; thread -> (head row, 4 columns)
+  constexpr float kLn2 = 0.6931471805599453f;
+  for (int idx = threadIdx.x; idx < G * (kDecD / 4); idx += blockDim.x) {
+    const int r = idx / (kDecD / 4);
+    const int c4 = (idx % (kDecD / 4)) * 4;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, s_m[w][r]);
+    float o4[4] = {0.f, 0.f, 0.f, 0.f};
+    float Lsum = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float f = ptx::ex2(s_m[w][r] - M);
+        Lsum += s_l[w][r] * f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o4[e] += s_o[w][r][c4 + e] * f;
+      }
+    }
+    const int64_t row = (static_cast<int64_t>(s) * p.batch + b) * p.hq + static_cast<int64_t>(kvh) * G + r;
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    float4 out = make_float4(o4[0] * inv, o4[1] * inv, o4[2] * inv, o4[3] * inv);
+    *reinterpret_cast<float4*>(p.part_o + row * kDecD + c4) = out;
+    if (c4 == 0) p.part_lse[row] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+  }
+}
+
+// Merge of the split partials: lse = ln sum_s exp(lse_s), O = sum_s exp(lse_s - lse) O_s.
+__global__ void __launch_bounds__(128) decode_merge_kernel(const float* __restrict__ part_o,
+                                                           const float* __restrict__ part_lse, int S, int B, int Hq,
+                                                           __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + warp;  // (b, h)
+  if (row >= B * Hq) return;
+  constexpr float kLog2e = 1.4426950408889634f;
+  constexpr float kLn2 = 0.6931471805599453f;
+  const int64_t stride = static_cast<int64_t>(B) * Hq;
+  float M = -INFINITY;
+  for (int s = lane; s < S; s += 32) M = fmaxf(M, part_lse[s * stride + row]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float Z = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < S; ++s) {
+      const float ls = part_lse[s * stride + row];
+      if (ls == -INFINITY) continue;
+      const float w = ptx::ex2((ls - M) * kLog2e);
+      Z += w;
+      const float4 v = *reinterpret_cast<const float4*>(part_o + (s * stride + row) * kDecD + 4 * lane);
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+    }
+  }
+  const float inv = Z > 0.f ? 1.f / Z : 0.f;
+  __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  __nv_bfloat162 c = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 packed;
+  packed.x = *reinterpret_cast<uint32_t*>(&a);
+  packed.y = *reinterpret_cast<uint32_t*>(&c);
+  *reinterpret_cast<uint2*>(o + row * kDecD + 4 * lane) = packed;
+  if (lane == 0) lse[row] = Z > 0.f ? M + logf(Z) : -INFINITY;
+  (void)kLn2;
+}
+
+// ------------------------------------------------------------------ launchers
+
+cudaError_t launch_decode(const jfa_decode_args& a, float* part_o, float* part_lse, int32_t* status,
+                          cudaStream_t stream) {
+  DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.kc = static_cast<const __nv_bfloat16*>(a.k_cache);
+  p.vc = static_cast<const __nv_bfloat16*>(a.v_cache);
+  p.page_table = a.page_table;
+  p.seqlens = a.seqlens_k;
+  p.batch = a.batch;
+  p.hq = a.q_heads;
+  p.hkv = a.kv_heads;
+  p.page_size = a.page_size;
+  p.num_pages = a.num_pages;
+  p.max_pages = a.max_pages;
+  p.num_splits = a.num_splits;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.part_o = part_o;
+  p.part_lse = part_lse;
+  p.bounds_out = a.split_bounds_out;
+  p.status = status;
+  const int G = a.q_heads / a.kv_heads;
+  dim3 grid(a.num_splits, a.kv_heads, a.batch);
+  cudaEvent_t* ev = static_cast<cudaEvent_t*>(a.main_kernel_events);
+  if (ev) cudaEventRecord(ev[0], stream);
+  switch (G) {
+    case 1: decode_split_kernel<1><<<grid, 128, 0, stream>>>(p); break;
+    case 2: decode_split_kernel<2><<<grid, 128, 0, stream>>>(p); break;
+    case 4: decode_split_kernel<4><<<grid, 128, 0, stream>>>(p); break;
+    case 8: decode_split_kernel<8><<<grid, 128, 0, stream>>>(p); break;
+    case 16: decode_split_kernel<16><<<grid, 128, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (ev) cudaEventRecord(ev[1], stream);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int rows = a.batch * a.q_heads;
+  decode_merge_kernel<<<(rows + 3) / 4, 128, 0, stream>>>(part_o, part_lse, a.num_splits, a.batch, a.q_heads,
+                                                            static_cast<__nv_bfloat16*>(a.o), a.lse);
+  return cudaGetLastError();
+}
+
+}  // namespace jfa

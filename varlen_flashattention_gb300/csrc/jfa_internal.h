@@ -1,0 +1,105 @@
+// Internal definitions shared by the host layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/jfa.h"
+
+namespace jfa {
+
+constexpr int kTile = 128;  // rows of a Q or K/V tile (tcgen05 M = 128)
+
+// Where a pipeline wait gave up (second word of the device status block).
+enum WaitSite : int32_t {
+  kSiteFwdProdQ = 101,
+  kSiteFwdProdSlot = 102,
+  kSiteFwdMmaQ = 111,
+  kSiteFwdMmaSlot = 112,
+  kSiteFwdMmaP = 113,
+  kSiteFwdMmaOFree = 114,
+  kSiteFwdSoftS = 121,
+  kSiteFwdSoftO = 122,
+  kSiteFwdDrain = 131,
+  kSiteBwdProdKV = 201,
+  kSiteBwdProdQ = 202,
+  kSiteBwdMmaKV = 211,
+  kSiteBwdMmaQ = 212,
+  kSiteBwdMmaP = 213,
+  kSiteBwdMmaDS = 214,
+  kSiteBwdMmaDQFree = 215,
+  kSiteBwdMmaAccFree = 216,
+  kSiteBwdSoftS = 221,
+  kSiteBwdSoftDP = 222,
+  kSiteBwdDQ = 231,
+  kSiteBwdEpi = 241,
+  kSiteBwdDrain = 251,
+  kSiteQueueOffsets = 301,
+  kSiteDecodeTable = 401,
+};
+
+// Device status block at the start of every workspace (256 bytes).
+//   [0] status (jfa_status), [1] detail (WaitSite or check code),
+//   [2] number of queued work items.
+constexpr size_t kStatusBytes = 256;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Queue modes: which tiles are work items and what each costs.
+enum QueueMode : int32_t {
+  kQueueSelfFwd = 0,   // items (b, h, q-tile); cost = kv tiles visited
+  kQueueSelfBwd = 1,   // items (b, h, kv-tile); cost = q tiles visited
+  kQueueBcastFwd = 2,  // items (b, h, q-tile of the shared Q); cost = kv tiles of b
+  kQueueBcastBwd = 3,  // items (b, h, kv-tile of b); cost = q tiles of the shared Q
+};
+
+struct QueueParams {
+  const int32_t* offsets;  // [batch+1]
+  int32_t batch, heads, total, max_seqlen, causal, mode, q_len;
+  int32_t* status;         // status block
+  int32_t* tile_base;      // [batch+1] exclusive prefix of q-tiles (self modes)
+  int4* items;             // (b, h, t, cost)
+  int32_t max_items;
+};
+
+// Work-item bound used to size the queue: sum_b ceil(L_b/128) <= ceil(total/128) + batch.
+inline int64_t max_tiles(int64_t total, int64_t batch) { return (total + kTile - 1) / kTile + batch; }
+
+struct BwdLaunch {
+  int head_dim, head_chunk;
+  const int32_t* offsets;
+  const int32_t* tile_base;
+  const int4* items;
+  int32_t* status;
+  const float* lse2p;
+  const float* deltap;
+  float* dq_acc;
+  void* dk;
+  void* dv;
+  int heads, total, bcast, q_len, causal, pad_tiles;
+  float scale;
+  uint64_t budget_ns;
+  int grid;
+};
+
+// Launchers (defined in the kernel translation units).
+cudaError_t launch_queue(const QueueParams& p, cudaStream_t stream);
+cudaError_t launch_fwd(int head_dim, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const int32_t* offsets, const int4* items, int32_t* status, void* o, float* lse, int heads,
+                       int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
+                       cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, cudaStream_t stream);
+cudaError_t launch_bwd_pre(int head_dim, const void* o, const void* dout, const float* lse, const int32_t* offsets,
+                           const int32_t* tile_base, const int32_t* status, int batch, int heads, int total, int bcast,
+                           int q_len, int pad_tiles, int grid_tiles, float* lse2p, float* deltap,
+                           cudaStream_t stream);
+cudaError_t launch_bwd_post(const float* acc, void* dq, int64_t n, float scale, const int32_t* status, int sms,
+                            cudaStream_t stream);
+cudaError_t launch_decode(const jfa_decode_args& a, float* part_o, float* part_lse, int32_t* status,
+                          cudaStream_t stream);
+
+}  // namespace jfa
