@@ -1,0 +1,545 @@
+#!/usr/bin/env python
+"""Benchmark of the jagged attention hot path on GB300.
+
+One step = jagged FlashAttention forward + backward over the GEM-like
+workload (batch 1024, max_len 1024, sparsity 0.5 -> lengths uniform in
+[1, 1024], 4 heads, head_dim 128, bf16, not causal), through the C ABI.
+
+Printed: one JSON line on rank 0 with
+  value      whole-job TFLOP/s (forward 4 d + backward 10 d FLOPs per visible
+             (query, key) pair per head, real tokens only) / device time,
+  roofline   the dominant kernel's achieved TFLOP/s (CUDA events around that
+             kernel on its stream) against the measured bf16 peak,
+  e2e        the same metric with the inputs copied from pinned host memory
+             and the outputs copied back inside the timed region,
+  cpu_baseline  the fp64 oracle on a bounded sample, on the host cores,
+  decode / detail  split-KV paged decode TB/s and the other workloads.
+
+--impl reference times the fp64 CPU oracle instead (the reference arm).
+Multi-GPU (torchrun): every rank runs its own replica on its own seeded batch
+(weak scaling, no data-path collective); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "jagged attn fwd/bwd bf16 TFLOP/s (% of TC peak); decode HBM TB/s (% of peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------- helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def pair_count(lengths, causal):
+    tot = 0
+    for L in lengths:
+        L = int(L)
+        tot += L * (L + 1) // 2 if causal else L * L
+    return tot
+
+
+def attn_flops(lengths, heads, d, causal, kind):
+    return (4 if kind == "fwd" else 10) * d * heads * pair_count(lengths, causal)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        pg = dist
+    return rank, world, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x, device):
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(pg, x, device):
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- workloads
+
+def gem_workload(seed, device, batch=1024, max_len=1024, sparsity=0.5, heads=4, head_dim=128):
+    import torch
+    from varlen_flashattention_gb300 import inputs
+    g = torch.Generator().manual_seed(seed)
+    lo, hi = inputs.sparsity_range(max_len, sparsity)
+    lengths = inputs.uniform_lengths(batch, lo, hi, g)
+    off = inputs.offsets_from_lengths(lengths)
+    total = int(off[-1])
+    shape = (total, heads, head_dim)
+    w = {"lengths": lengths, "offsets": off.to(device), "max_seqlen": int(lengths.max()), "total": total,
+         "heads": heads, "head_dim": head_dim, "scale": 1.0 / math.sqrt(head_dim)}
+    for i, k in enumerate(("q", "k", "v", "do")):
+        w[k] = inputs.randn_bf16_device(shape, seed * 16 + i + 1, device)
+    return w
+
+
+def run_step(jfa, w, bufs, causal=False, ev_f=None, ev_b=None):
+    jfa.jfa_fwd(w["q"], w["k"], w["v"], w["offsets"], w["max_seqlen"], w["scale"], causal, o=bufs["o"],
+                lse=bufs["lse"], workspace=bufs["ws_f"], events=ev_f)
+    jfa.jfa_bwd(w["q"], w["k"], w["v"], bufs["o"], w["do"], bufs["lse"], w["offsets"], w["max_seqlen"], w["scale"],
+                causal, dq=bufs["dq"], dk=bufs["dk"], dv=bufs["dv"], workspace=bufs["ws_b"], events=ev_b)
+
+
+def alloc_bufs(jfa, w, device):
+    import torch
+    H, D, T = w["heads"], w["head_dim"], w["total"]
+    b = {"o": torch.empty((T, H, D), dtype=torch.bfloat16, device=device),
+         "lse": torch.empty((H, T), dtype=torch.float32, device=device),
+         "dq": torch.empty((T, H, D), dtype=torch.bfloat16, device=device),
+         "dk": torch.empty((T, H, D), dtype=torch.bfloat16, device=device),
+         "dv": torch.empty((T, H, D), dtype=torch.bfloat16, device=device)}
+    # workspaces sized by the library
+    import ctypes
+    from varlen_flashattention_gb300 import _abi
+    lib = jfa.library()
+    fa = _abi.FwdArgs(None, None, None, None, len(w["lengths"]), H, D, w["max_seqlen"], T, w["scale"], 0,
+                      None, None, None)
+    ba = _abi.BwdArgs(None, None, None, None, None, None, None, len(w["lengths"]), H, D, w["max_seqlen"], T,
+                      w["scale"], 0, 0, None, None, None, None)
+    b["ws_f"] = torch.empty(lib.jfa_fwd_workspace_size(ctypes.byref(fa)), dtype=torch.uint8, device=device)
+    b["ws_b"] = torch.empty(lib.jfa_bwd_workspace_size(ctypes.byref(ba)), dtype=torch.uint8, device=device)
+    return b
+
+
+def time_events(fn, iters, warmup):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(iters):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+def measure_decode(jfa, device, peaks, page_size=16, splits=(8, 16, 32, 64), iters=20):
+    """Split-KV paged GQA decode: batch 32, 32/8 heads, d 128, KV lengths in
+    [1024, 32768], random page permutation. Returns the best split count."""
+    import torch
+    from varlen_flashattention_gb300 import inputs
+    g = torch.Generator().manual_seed(0)
+    sl = inputs.uniform_lengths(32, 1024, 32768, g)
+    pages = [(int(L) + page_size - 1) // page_size for L in sl.tolist()]
+    n = sum(pages)
+    perm = torch.randperm(n, generator=g).to(torch.int32)
+    pt = torch.zeros((32, max(pages)), dtype=torch.int32)
+    c = 0
+    for b, m in enumerate(pages):
+        pt[b, :m] = perm[c:c + m]
+        c += m
+    q = inputs.randn_bf16_device((32, 32, 128), 101, device)
+    kc = inputs.randn_bf16_device((n, page_size, 8, 128), 102, device)
+    vc = inputs.randn_bf16_device((n, page_size, 8, 128), 103, device)
+    pt, sl_d = pt.to(device), sl.to(device)
+    o = torch.empty_like(q)
+    lse = torch.empty((32, 32), dtype=torch.float32, device=device)
+    # algorithmic bytes: K + V rows read, Q, O, LSE and the page-table entries used
+    nbytes = int(sl.sum()) * 2 * 8 * 128 * 2 + q.numel() * 2 * 2 + lse.numel() * 4 + sum(pages) * 4
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # 256 MB > L2, cleared between runs
+    best = None
+    for S in splits:
+        ws = torch.empty(1, dtype=torch.uint8, device=device)
+        from varlen_flashattention_gb300 import _abi
+        import ctypes
+        da = _abi.DecodeArgs(None, None, None, None, None, 32, 32, 8, 128, page_size, n, pt.shape[1], S, 0.1,
+                             None, None, None, None)
+        ws = torch.empty(jfa.library().jfa_decode_workspace_size(ctypes.byref(da)), dtype=torch.uint8, device=device)
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        for _ in range(3):
+            jfa.jfa_decode_splitkv(q, kc, vc, pt, sl_d, S, o=o, lse=lse, workspace=ws)
+        times = []
+        for _ in range(iters):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            jfa.jfa_decode_splitkv(q, kc, vc, pt, sl_d, S, o=o, lse=lse, workspace=ws, events=ev)
+            e.record()
+            torch.cuda.synchronize()
+            times.append((s.elapsed_time(e), ev[0].elapsed_time(ev[1])))
+        call_ms = statistics.median(t[0] for t in times)
+        kern_ms = statistics.median(t[1] for t in times)
+        r = {"splits": S, "call_us": call_ms * 1e3, "split_kernel_us": kern_ms * 1e3,
+             "tb_s": nbytes / (call_ms * 1e-3) / 1e12}
+        if best is None or r["tb_s"] > best["tb_s"]:
+            best = r
+    best["frac_of_measured_hbm"] = best["tb_s"] * 1e3 / peaks["hbm_gbs"]
+    best.update({"workload": f"paged GQA decode: batch 32, Hq 32 / Hkv 8, d 128, L_k U[1024,32768], page {page_size}",
+                 "algorithmic_bytes": nbytes, "l2": "256 MB buffer written between runs"})
+    return best
+
+
+def measure_extra(jfa, device, peaks):
+    """Broadcast-Q and dense causal workloads (one timed call each)."""
+    import torch
+    from varlen_flashattention_gb300 import inputs
+    out = {}
+    # broadcast-Q: Q [256, 4, 128] over 512 jagged K/V sequences of length U[16, 2048]
+    g = torch.Generator().manual_seed(0)
+    lk = inputs.uniform_lengths(512, 16, 2048, g)
+    off = inputs.offsets_from_lengths(lk).to(device)
+    T = int(lk.sum())
+    q = inputs.randn_bf16_device((256, 4, 128), 201, device)
+    k = inputs.randn_bf16_device((T, 4, 128), 202, device)
+    v = inputs.randn_bf16_device((T, 4, 128), 203, device)
+    do = inputs.randn_bf16_device((512, 256, 4, 128), 204, device)
+    mx = int(lk.max())
+    sc = 1 / math.sqrt(128)
+    o, lse = jfa.jfa_fwd_broadcast_q(q, k, v, off, mx, sc)
+    tf = time_events(lambda: jfa.jfa_fwd_broadcast_q(q, k, v, off, mx, sc, o=o, lse=lse), 10, 3)
+    tb = time_events(lambda: jfa.jfa_bwd_broadcast_q(q, k, v, o, do, lse, off, mx, sc), 10, 3)
+    pairs = 256 * int(lk.sum())
+    out["broadcast_q"] = {"fwd_tflops": 4 * 128 * 4 * pairs / (tf * 1e-3) / 1e12,
+                          "bwd_tflops": 10 * 128 * 4 * pairs / (tb * 1e-3) / 1e12, "fwd_ms": tf, "bwd_ms": tb}
+    del q, k, v, do, o, lse
+    # dense causal: batch 4 x 8192, 16 heads, d 128 and d 192 (chunked backward)
+    for d in (128, 192):
+        lens = torch.full((4,), 8192, dtype=torch.int32)
+        off = inputs.offsets_from_lengths(lens).to(device)
+        shape = (4 * 8192, 16, d)
+        q, k, v, do = (inputs.randn_bf16_device(shape, 300 + i, device) for i in range(4))
+        sc = 1 / math.sqrt(d)
+        o, lse = jfa.jfa_fwd(q, k, v, off, 8192, sc, True)
+        tf = time_events(lambda: jfa.jfa_fwd(q, k, v, off, 8192, sc, True, o=o, lse=lse), 10, 3)
+        tb = time_events(lambda: jfa.jfa_bwd(q, k, v, o, do, lse, off, 8192, sc, True), 5, 2)
+        pairs = 4 * 8192 * 8193 // 2
+        out[f"dense_causal_d{d}"] = {"fwd_tflops": 4 * d * 16 * pairs / (tf * 1e-3) / 1e12,
+                                     "bwd_tflops": 10 * d * 16 * pairs / (tb * 1e-3) / 1e12,
+                                     "fwd_ms": tf, "bwd_ms": tb}
+        del q, k, v, do, o, lse
+    for sp in (0.1, 0.9):
+        w = gem_workload(0, device, sparsity=sp)
+        bufs = alloc_bufs(jfa, w, device)
+        t = time_events(lambda: run_step(jfa, w, bufs), 10, 3)
+        fl = attn_flops(w["lengths"], 4, 128, False, "fwd") + attn_flops(w["lengths"], 4, 128, False, "bwd")
+        out[f"gem_sparsity_{sp}"] = {"fwd_bwd_tflops": fl / (t * 1e-3) / 1e12, "ms_per_step": t}
+        del w, bufs
+    torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------- CPU oracle legs
+
+def oracle_sample_rate(seed, budget_s, max_seqs=None):
+    """Times the fp64 oracle (forward + backward) on the first sequences of the
+    GEM-like workload until `budget_s` seconds have passed; returns
+    (TFLOP/s, sequences, seconds, cores)."""
+    import numpy as np
+    import torch
+    import oracle.attention as orc
+    from varlen_flashattention_gb300 import inputs
+    g = torch.Generator().manual_seed(seed)
+    lo, hi = inputs.sparsity_range(1024, 0.5)
+    lengths = inputs.uniform_lengths(1024, lo, hi, g)
+    done_flops, t_used, n = 0, 0.0, 0
+    rng = np.random.default_rng(seed)
+    for b, L in enumerate(lengths.tolist()):
+        q, k, v, do = (rng.standard_normal((L, 4, 128)).astype(np.float32).astype(np.float64) for _ in range(4))
+        off = np.array([0, L])
+        t0 = time.perf_counter()
+        orc.attention_forward(q, k, v, off, 1 / math.sqrt(128), False)
+        orc.attention_backward(q, k, v, do, off, 1 / math.sqrt(128), False)
+        t_used += time.perf_counter() - t0
+        done_flops += attn_flops([L], 4, 128, False, "fwd") + attn_flops([L], 4, 128, False, "bwd")
+        n += 1
+        if t_used >= budget_s or (max_seqs and n >= max_seqs):
+            break
+    return done_flops / t_used / 1e12, n, t_used, os.cpu_count()
+
+
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    budget = 4.0
+    for _ in range(args.warmup):
+        oracle_sample_rate(0, budget / 4, max_seqs=2)
+    vals, secs, seqs = [], 0.0, 0
+    for s in range(args.steps):
+        v, n, t, cores = oracle_sample_rate(s, budget)
+        vals.append(v)
+        secs += t
+        seqs += n
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "GEM-like jagged self-attention fwd+bwd, batch 1024, max_len 1024, sparsity 0.5 "
+                                   "(lengths U[1,1024]), 4 heads, head_dim 128, not causal",
+                       "sample": "per step: the workload's first sequences, oracle run until ~4 s of CPU time"},
+            "cpu_baseline": {"kind": "oracle", "cores": os.cpu_count(), "value": value, "unit": "TFLOP/s",
+                             "sample": f"{seqs} sequences over {args.steps} steps (all 4 heads each), numpy fp64"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- main arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip decode / broadcast / causal detail")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import varlen_flashattention_gb300 as jfa
+    from varlen_flashattention_gb300 import build as _build
+    _build.build()
+    rank, world, local, pg = dist_setup(args.gpus)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    peaks, peak_kind = load_peaks()
+
+    w = gem_workload(rank, device)
+    bufs = alloc_bufs(jfa, w, device)
+    flops_f = attn_flops(w["lengths"], w["heads"], w["head_dim"], False, "fwd")
+    flops_b = attn_flops(w["lengths"], w["heads"], w["head_dim"], False, "bwd")
+    flops_step = flops_f + flops_b
+
+    # correctness gate on the device status (cheap, before timing)
+    run_step(jfa, w, bufs)
+    st_f = jfa.jfa_read_device_status(bufs["ws_f"])
+    st_b = jfa.jfa_read_device_status(bufs["ws_b"])
+    if st_f[0] != 0 or st_b[0] != 0:
+        raise SystemExit(f"device status fwd={st_f} bwd={st_b}")
+
+    for _ in range(args.warmup):
+        run_step(jfa, w, bufs)
+    torch.cuda.synchronize()
+
+    evs_f = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs_b = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(pg)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record()
+        for i in range(args.steps):
+            run_step(jfa, w, bufs, ev_f=evs_f[i], ev_b=evs_b[i])
+        stop.record()
+        torch.cuda.synchronize()
+    barrier(pg)
+    ms = start.elapsed_time(stop) / args.steps
+    ms_max = max_over_ranks(pg, ms, device)
+    total_flops = sum_over_ranks(pg, flops_step, device)
+    value = total_flops / (ms_max * 1e-3) / 1e12
+    k_f = statistics.mean(a.elapsed_time(b) for a, b in evs_f)
+    k_b = statistics.mean(a.elapsed_time(b) for a, b in evs_b)
+
+    # dominant kernel and its roofline (kernel timed inside a long step -> sustained peak)
+    if k_b >= k_f:
+        dom, dom_ms, dom_flops = "jfa bwd main kernel (bwd_kernel<128,128>)", k_b, flops_b
+    else:
+        dom, dom_ms, dom_flops = "jfa fwd main kernel (fwd_kernel<128,false>)", k_f, flops_f
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tj = json.load(f)
+        ent = tj.get("bwd" if "bwd" in dom else "fwd")
+        if ent and ent.get("valid", False):
+            traffic = ent.get("dram_bytes_per_launch")
+
+    # end to end: pinned host inputs -> device -> fwd+bwd -> pinned host outputs
+    host_in = {k: w[k].cpu().pin_memory() for k in ("q", "k", "v", "do")}
+    host_off = w["offsets"].cpu().pin_memory()
+    host_out = {k: torch.empty(bufs[k].shape, dtype=bufs[k].dtype).pin_memory()
+                for k in ("o", "lse", "dq", "dk", "dv")}
+    dev_in = {k: torch.empty_like(w[k]) for k in ("q", "k", "v", "do")}
+    dev_off = torch.empty_like(w["offsets"])
+    w2 = dict(w)
+    w2.update(dev_in)
+    w2["offsets"] = dev_off
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + host_off.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for k in dev_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        dev_off.copy_(host_off, non_blocking=True)
+        run_step(jfa, w2, bufs)
+        for k in host_out:
+            host_out[k].copy_(bufs[k], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(pg)
+    t0 = time.perf_counter()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(pg, s2.elapsed_time(e2) / e2e_steps, device)
+    e2e_value = total_flops / (e2e_ms * 1e-3) / 1e12
+    del host_in, host_out, dev_in
+
+    detail = {"fwd_ms": k_f, "bwd_ms": k_b, "fwd_tflops": flops_f / (k_f * 1e-3) / 1e12,
+              "bwd_tflops": flops_b / (k_b * 1e-3) / 1e12, "flops_per_step": flops_step,
+              "tokens_per_rank": w["total"]}
+    decode = None
+    if not args.no_extra and rank == 0:
+        del w, bufs
+        torch.cuda.empty_cache()
+        try:
+            decode = measure_decode(jfa, device, peaks)
+            detail.update(measure_extra(jfa, device, peaks))
+        except Exception as ex:  # report, never hide
+            detail["extra_error"] = repr(ex)
+
+    cpu = None
+    if rank == 0:
+        try:
+            v, n, t, cores = oracle_sample_rate(0, args.cpu_budget)
+            cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                   "sample": f"first {n} sequences of the workload (all 4 heads), fwd+bwd in numpy fp64, {t:.1f} s"}
+        except Exception as ex:
+            cpu = {"value": None, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                   "sample": f"failed: {ex!r}"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "GEM-like jagged self-attention fwd+bwd: batch 1024 per GPU, max_len 1024, "
+                                   "sparsity 0.5 (lengths U[1,1024]), 4 heads, head_dim 128, not causal",
+                       "batch": 1024, "max_len": 1024, "sparsity": 0.5, "heads": 4, "head_dim": 128,
+                       "causal": False, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (4 x 0.54 GB bf16 per step)"},
+            "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_kind} bf16_tflops_sustained (kernel timed inside a long step)"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 6 * args.steps,
+            "clocks": clocks.summary(),
+            "decode": decode,
+            "detail": detail,
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,10 +1,16 @@
 """Shared helpers of the parity tests: tolerances, conversions, comparisons.
 
 Tolerances (stated for bf16 inputs with fp32 accumulation):
-  O      max|gpu - oracle| <= 1e-2
+  O      |gpu - oracle| <= 1e-2 + 2^-7 |oracle|   elementwise
   LSE    max|gpu - oracle| <= 1e-3
   dQ, dK, dV   max|gpu - oracle| <= 2e-2 * max|oracle|
 Integer work (split bounds, tile order) is compared bit for bit.
+
+The 2^-7 |O| term is the bf16 representation allowance derived from the
+arithmetic: O is returned in bf16 (rounding error up to 2^-8 |O|) and the
+probabilities enter P V as bf16 (relative error up to 2^-9 per term, at most
+2^-9 |O| in total), so even an exact kernel exceeds a flat 1e-2 wherever
+|O| > 2.56 -- rows that see one or two keys return nearly a whole V row.
 """
 from __future__ import annotations
 
@@ -34,10 +40,22 @@ def max_err(a, b) -> float:
     return float(d.max())
 
 
+TOL_O_REL = 2.0 ** -7
+
+
 def check_o(gpu, ref, what="O"):
-    e = max_err(gpu, ref)
-    assert e <= TOL_O, f"{what}: max|diff| {e:.3e} > {TOL_O}"
-    return e
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    if ref.size == 0:
+        return 0.0
+    diff = np.abs(gpu - ref)
+    diff = np.where(np.isnan(diff), np.inf, diff)
+    bound = TOL_O + TOL_O_REL * np.abs(ref)
+    worst = int(np.argmax(diff - bound))
+    assert np.all(diff <= bound), (f"{what}: |diff| {diff.flat[worst]:.3e} > {bound.flat[worst]:.3e} "
+                                   f"(= 1e-2 + 2^-7 * |ref| {abs(ref.flat[worst]):.3f}); max|diff| {diff.max():.3e}")
+    return float(diff.max())
 
 
 def check_lse(gpu, ref, what="LSE"):

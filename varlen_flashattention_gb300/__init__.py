@@ -64,6 +64,9 @@ def _stream(stream):
 def _events(events):
     if events is None:
         return None, None
+    for e in events:  # torch creates the CUDA event lazily, on its first record
+        if not e.cuda_event:
+            e.record()
     arr = (ctypes.c_void_p * 2)(events[0].cuda_event, events[1].cuda_event)
     return ctypes.cast(arr, ctypes.c_void_p), arr
 

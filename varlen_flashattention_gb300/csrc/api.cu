@@ -90,6 +90,13 @@ void record(void* events, int which, cudaStream_t s) {
   if (events) cudaEventRecord(static_cast<cudaEvent_t*>(events)[which], s);
 }
 
+// The optional event pair must hold two created events.
+bool events_ok(void* events) {
+  if (!events) return true;
+  const cudaEvent_t* e = static_cast<const cudaEvent_t*>(events);
+  return e[0] != nullptr && e[1] != nullptr;
+}
+
 // ------------------------------------------------------------------ workspace layouts
 
 struct Layout {
@@ -254,7 +261,7 @@ jfa_status jfa_fwd(const jfa_fwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   jfa_status st = check_fwd(a);
   if (st != JFA_OK) return st;
   const Layout L = self_layout(a->batch, a->heads, a->total, a->head_dim, false);
-  if (!aligned(ws, 256)) return JFA_ERR_INVALID_ARG;
+  if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
@@ -294,7 +301,7 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   jfa_status st = check_bwd(a, &chunk);
   if (st != JFA_OK) return st;
   const Layout L = self_layout(a->batch, a->heads, a->total, a->head_dim, true);
-  if (!aligned(ws, 256)) return JFA_ERR_INVALID_ARG;
+  if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
@@ -368,7 +375,7 @@ jfa_status jfa_fwd_broadcast_q(const jfa_bcast_fwd_args* a, void* ws, size_t ws_
       return JFA_ERR_INVALID_ARG;
   }
   const Layout L = bcast_layout(a->batch, a->q_len, a->heads, a->total_k, a->head_dim, false);
-  if (!aligned(ws, 256)) return JFA_ERR_INVALID_ARG;
+  if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
@@ -416,7 +423,7 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
       return JFA_ERR_INVALID_ARG;
   }
   const Layout L = bcast_layout(a->batch, a->q_len, a->heads, a->total_k, a->head_dim, true);
-  if (!aligned(ws, 256)) return JFA_ERR_INVALID_ARG;
+  if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
@@ -500,7 +507,7 @@ jfa_status jfa_decode_splitkv(const jfa_decode_args* a, void* ws, size_t ws_byte
   }
   if (static_cast<int64_t>(a->max_pages) * a->page_size >= (int64_t(1) << 31)) return JFA_ERR_INVALID_ARG;
   const Layout L = decode_layout(a->batch, a->q_heads, a->num_splits);
-  if (!aligned(ws, 256)) return JFA_ERR_INVALID_ARG;
+  if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;

@@ -39,6 +39,15 @@ def _randn_bf16(shape, g: torch.Generator) -> torch.Tensor:
     return torch.randn(*shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
 
 
+def randn_bf16_device(shape, seed: int, device) -> torch.Tensor:
+    """N(0,1) values rounded to bf16, drawn directly on `device` with its own
+    seeded generator. Used where only the shape and distribution matter (the
+    benchmark); parity tests use the CPU draws above."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return torch.randn(*shape, generator=g, dtype=torch.float32, device=device).to(torch.bfloat16)
+
+
 def sparsity_range(max_len: int, sparsity: float) -> tuple[int, int]:
     """Inclusive [lo, hi] of the uniform length draw for a sparsity level."""
     f = 1.0 - float(sparsity)
