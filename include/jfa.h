@@ -210,6 +210,25 @@ JFA_API jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* args, void* wor
 JFA_API jfa_status jfa_decode_splitkv(const jfa_decode_args* args, void* workspace, size_t workspace_bytes,
                               cudaStream_t stream);
 
+/* Paged split-KV decode that allocates nothing. The pages have no
+ * counterpart for this entry point; it exists for callers that cannot
+ * allocate device memory at call time (a plugin handed only its input and
+ * output buffers by a host runtime, or a serving path whose memory is planned
+ * up front and must not allocate or free). Same arguments and results as
+ * jfa_decode_splitkv, but the split partials live in a fixed scratch array
+ * inside the library (about 16.1 MiB per GPU, held until the process exits):
+ *  - num_splits * batch * q_heads must be <= 32768, else the call returns
+ *    JFA_ERR_WORKSPACE_TOO_SMALL before enqueueing anything;
+ *  - the first call on a device looks up the scratch address for that device
+ *    (make that first call before any stream capture on the device);
+ *  - calls no cudaMalloc / cudaFree and no allocating library routine;
+ *  - every call shares the scratch: calls whose work overlaps on the GPU race,
+ *    so serialise them (one stream, or explicit ordering);
+ *  - device-detected input errors (a page entry out of range) are handled in
+ *    the kernel as in jfa_decode_splitkv, but this entry point cannot return
+ *    them: the status word lives in the internal scratch. */
+JFA_API jfa_status jfa_decode_splitkv_noalloc(const jfa_decode_args* args, cudaStream_t stream);
+
 /* Synchronises `stream`, then returns the device status word of the last call
  * that used `workspace` (JFA_OK, JFA_ERR_TIMEOUT or JFA_ERR_BAD_INPUT), or
  * JFA_ERR_CUDA if the stream reports an error. *detail (optional) receives a
