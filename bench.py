@@ -388,11 +388,27 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip decode / broadcast / causal detail")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--profile", action="store_true",
+                    help="profiling run: warmup + steps of the plain fwd+bwd loop only, no JSON line")
+    ap.add_argument("--batch", type=int, default=1024, help="sequences per GPU (profiling runs use fewer)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return reference_arm(args)
+    if args.profile:
+        import torch
+        import varlen_flashattention_gb300 as jfa
+        from varlen_flashattention_gb300 import build as _build
+        _build.build()
+        device = torch.device("cuda", 0)
+        w = gem_workload(0, device, batch=args.batch)
+        bufs = alloc_bufs(jfa, w, device)
+        for _ in range(args.warmup + args.steps):
+            run_step(jfa, w, bufs)
+        torch.cuda.synchronize()
+        print(f"profile run: batch {args.batch}, {w['total']} tokens, {args.warmup + args.steps} steps")
+        return 0
 
     import torch
     import varlen_flashattention_gb300 as jfa
@@ -449,11 +465,17 @@ def main():
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
+        import hashlib
         with open(tpath) as f:
             tj = json.load(f)
         ent = tj.get("bwd" if "bwd" in dom else "fwd")
-        if ent and ent.get("valid", False):
-            traffic = ent.get("dram_bytes_per_launch")
+        if ent:
+            h = hashlib.sha256()
+            for src in ent.get("sources", []):
+                with open(os.path.join(ROOT, src), "rb") as f:
+                    h.update(f.read())
+            if h.hexdigest()[:16] == ent.get("source_sha256"):  # counters still describe this kernel
+                traffic = ent.get("dram_bytes_per_launch")
 
     # end to end: pinned host inputs -> device -> fwd+bwd -> pinned host outputs
     host_in = {k: w[k].cpu().pin_memory() for k in ("q", "k", "v", "do")}
