@@ -160,6 +160,18 @@ def test_tile_queue_order_bit_exact(causal):
     assert got == orc.tile_queue(d["offsets"].numpy(), 3, causal, "fwd")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_stream_queue_order_bit_exact(causal):
+    """head_dim 128 runs the flat-stream forward; its work items are the same
+    longest-first query tiles."""
+    d = _lengths_case([300, 0, 1, 400, 1000, 129, 128, 512], 3, 128, seed=16)
+    q, k, v, off = _gpu(d)
+    a_ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    jfa.jfa_fwd(q, k, v, off, d["max_seqlen"], d["scale"], causal, workspace=a_ws, check=True)
+    got = _queue_from_workspace(a_ws, len(d["lengths"]))
+    assert got == orc.tile_queue(d["offsets"].numpy(), 3, causal, "fwd")
+
+
 def test_bad_offsets_are_reported():
     """Offsets inconsistent with the host's total are rejected on the device
     (JFA_ERR_BAD_INPUT) and no work is queued."""

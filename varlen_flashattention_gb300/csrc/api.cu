@@ -69,13 +69,13 @@ EncodeTiledFn encode_fn() {
 
 // 2-D bf16 view [rows, cols] (cols contiguous) read in 128-row x 64-column
 // boxes with the 128-byte swizzle the tcgen05 descriptors expect.
-bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows = kTile) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   if (rows == 0) rows = 1;  // nothing is read from an empty tensor; the map must still be valid
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTile)};
+  const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -83,6 +83,15 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t co
 }
 
 bool good_dim(int d) { return d == 64 || d == 128 || d == 192; }
+
+// Which forward kernel runs: head_dim 128 takes the flat-stream kernel on
+// single CTAs; 64 and 192 the per-tile kernel. (The CTA-pair form of the
+// stream kernel measured slower: every cross-SM signal in it took about a
+// microsecond to be observed.)
+enum class FwdPath { kTile, kStreamSingle, kStreamPair };
+FwdPath fwd_path(int head_dim, int /*sms*/) {
+  return head_dim == 128 ? FwdPath::kStreamSingle : FwdPath::kTile;
+}
 
 jfa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA; }
 
@@ -281,17 +290,31 @@ jfa_status jfa_fwd(const jfa_fwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   qp.total = a->total;
   qp.max_seqlen = a->max_seqlen;
   qp.causal = a->causal;
-  qp.mode = kQueueSelfFwd;
+  const FwdPath path = fwd_path(a->head_dim, sms);
+  const bool pair = path == FwdPath::kStreamPair;
+  CUtensorMap tk64;
+  if (pair && !make_tmap_bf16(&tk64, a->k, a->total, cols, kTile / 2)) return JFA_ERR_CUDA;
+  qp.mode = pair ? kQueueSelfFwdPair : kQueueSelfFwd;
   qp.q_len = 0;
   qp.status = status;
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
   qp.items = reinterpret_cast<int4*>(w + L.items);
   qp.max_items = static_cast<int32_t>(L.max_items);
+  qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
-  const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
-  record(a->main_kernel_events, 0, stream);
-  cudaError_t e = launch_fwd(a->head_dim, a->causal != 0, tq, tk, tv, a->offsets, qp.items, status, a->o, a->lse,
-                             a->heads, a->total, 0, 0, a->scale, wait_budget_ns(), grid, stream);
+  cudaError_t e;
+  if (path != FwdPath::kTile) {
+    const int grid = pair ? 2 * static_cast<int>(std::min<int64_t>(sms / 2, std::max<int64_t>(L.max_items, 1)))
+                          : static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
+    record(a->main_kernel_events, 0, stream);
+    e = launch_fwd_stream(pair, a->causal != 0, tq, pair ? tk64 : tk, tv, a->offsets, qp.items, status, a->o, a->lse,
+                          a->heads, a->total, 0, 0, a->scale, wait_budget_ns(), grid, stream);
+  } else {
+    const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
+    record(a->main_kernel_events, 0, stream);
+    e = launch_fwd(a->head_dim, a->causal != 0, tq, tk, tv, a->offsets, qp.items, status, a->o, a->lse, a->heads,
+                   a->total, 0, 0, a->scale, wait_budget_ns(), grid, stream);
+  }
   record(a->main_kernel_events, 1, stream);
   return cuda_status(e);
 }
@@ -330,6 +353,7 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
   qp.items = reinterpret_cast<int4*>(w + L.items);
   qp.max_items = static_cast<int32_t>(L.max_items);
+  qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
   float* lse2p = reinterpret_cast<float*>(w + L.lse2p);
   float* deltap = reinterpret_cast<float*>(w + L.deltap);
@@ -395,17 +419,31 @@ jfa_status jfa_fwd_broadcast_q(const jfa_bcast_fwd_args* a, void* ws, size_t ws_
   qp.total = a->total_k;
   qp.max_seqlen = a->max_seqlen_k;
   qp.causal = 0;
-  qp.mode = kQueueBcastFwd;
+  const FwdPath path = fwd_path(a->head_dim, sms);
+  const bool pair = path == FwdPath::kStreamPair;
+  CUtensorMap tk64;
+  if (pair && !make_tmap_bf16(&tk64, a->k, a->total_k, cols, kTile / 2)) return JFA_ERR_CUDA;
+  qp.mode = pair ? kQueueBcastFwdPair : kQueueBcastFwd;
   qp.q_len = a->q_len;
   qp.status = status;
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
   qp.items = reinterpret_cast<int4*>(w + L.items);
   qp.max_items = static_cast<int32_t>(L.max_items);
+  qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
-  const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
-  record(a->main_kernel_events, 0, stream);
-  cudaError_t e = launch_fwd(a->head_dim, false, tq, tk, tv, a->kv_offsets, qp.items, status, a->o, a->lse, a->heads,
-                             a->total_k, 1, a->q_len, a->scale, wait_budget_ns(), grid, stream);
+  cudaError_t e;
+  if (path != FwdPath::kTile) {
+    const int grid = pair ? 2 * static_cast<int>(std::min<int64_t>(sms / 2, std::max<int64_t>(L.max_items, 1)))
+                          : static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
+    record(a->main_kernel_events, 0, stream);
+    e = launch_fwd_stream(pair, false, tq, pair ? tk64 : tk, tv, a->kv_offsets, qp.items, status, a->o, a->lse,
+                          a->heads, a->total_k, 1, a->q_len, a->scale, wait_budget_ns(), grid, stream);
+  } else {
+    const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
+    record(a->main_kernel_events, 0, stream);
+    e = launch_fwd(a->head_dim, false, tq, tk, tv, a->kv_offsets, qp.items, status, a->o, a->lse, a->heads,
+                   a->total_k, 1, a->q_len, a->scale, wait_budget_ns(), grid, stream);
+  }
   record(a->main_kernel_events, 1, stream);
   return cuda_status(e);
 }
@@ -454,6 +492,7 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
     qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
     qp.items = reinterpret_cast<int4*>(w + L.items);
     qp.max_items = static_cast<int32_t>(L.max_items);
+  qp.count_index = 2;
     if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
     float* lse2p = reinterpret_cast<float*>(w + L.lse2p);
     float* deltap = reinterpret_cast<float*>(w + L.deltap);

@@ -23,7 +23,9 @@ enum WaitSite : int32_t {
   kSiteFwdMmaOFree = 114,
   kSiteFwdSoftS = 121,
   kSiteFwdSoftO = 122,
+  kSiteFwdSoftMl = 123,
   kSiteFwdDrain = 131,
+  kSiteFwdEpi = 141,
   kSiteBwdProdKV = 201,
   kSiteBwdProdQ = 202,
   kSiteBwdMmaKV = 211,
@@ -54,6 +56,8 @@ enum QueueMode : int32_t {
   kQueueSelfBwd = 1,   // items (b, h, kv-tile); cost = q tiles visited
   kQueueBcastFwd = 2,  // items (b, h, q-tile of the shared Q); cost = kv tiles of b
   kQueueBcastBwd = 3,  // items (b, h, kv-tile of b); cost = q tiles of the shared Q
+  kQueueSelfFwdPair = 4,   // items (b, h, pair u of q-tiles 2u, 2u+1) for CTA pairs; cost = kv tiles
+  kQueueBcastFwdPair = 5,  // items (b, h, pair u of the shared Q's tiles); cost = kv tiles of b
 };
 
 struct QueueParams {
@@ -63,6 +67,7 @@ struct QueueParams {
   int32_t* tile_base;      // [batch+1] exclusive prefix of q-tiles (self modes)
   int4* items;             // (b, h, t, cost)
   int32_t max_items;
+  int32_t count_index;     // status word that receives the number of items (2 or 3)
 };
 
 // Work-item bound used to size the queue: sum_b ceil(L_b/128) <= ceil(total/128) + batch.
@@ -91,6 +96,14 @@ cudaError_t launch_fwd(int head_dim, bool causal, const CUtensorMap& tq, const C
                        const int32_t* offsets, const int4* items, int32_t* status, void* o, float* lse, int heads,
                        int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
                        cudaStream_t stream);
+// Flat-stream forward (head_dim 128). pair: CTA pairs, items from a pair queue
+// mode, even grid, tk reads K in 64-row boxes (each CTA of a pair loads half
+// of a key tile). Otherwise single CTAs, items from the plain queue mode, tk
+// reads 128-row boxes.
+cudaError_t launch_fwd_stream(bool pair, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, const int32_t* offsets, const int4* items, int32_t* status,
+                              void* o, float* lse, int heads, int total, int bcast, int q_len, float scale,
+                              uint64_t budget_ns, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, cudaStream_t stream);
 cudaError_t launch_bwd_pre(int head_dim, const void* o, const void* dout, const float* lse, const int32_t* offsets,

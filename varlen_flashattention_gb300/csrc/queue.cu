@@ -49,9 +49,30 @@ __device__ int block_exclusive_scan(int v, int* warp_buf, int* total) {
 
 __device__ __forceinline__ int ceil_tiles(int L) { return (L + kTile - 1) / kTile; }
 
-// Number of tiles (work items per head) of sequence b, and the cost of tile t.
+__device__ __forceinline__ bool pair_mode(int mode) { return mode == kQueueSelfFwdPair || mode == kQueueBcastFwdPair; }
+
+// Work items of sequence b (per head): query tiles (forward), query-tile pairs
+// (forward on CTA pairs) or key/value tiles (backward).
 __device__ __forceinline__ int item_tiles(const QueueParams& p, int L) {
-  return p.mode == kQueueBcastFwd ? ceil_tiles(p.q_len) : ceil_tiles(L);
+  switch (p.mode) {
+    case kQueueBcastFwd: return ceil_tiles(p.q_len);
+    case kQueueBcastFwdPair: return (p.q_len + 2 * kTile - 1) / (2 * kTile);
+    case kQueueSelfFwdPair: return (L + 2 * kTile - 1) / (2 * kTile);
+    default: return ceil_tiles(L);
+  }
+}
+
+// Partner tiles an item visits: its cost in the longest-first order.
+__device__ __forceinline__ int item_cost(const QueueParams& p, int L, int t) {
+  const int nk = ceil_tiles(L);
+  switch (p.mode) {
+    case kQueueSelfFwd: return p.causal ? t + 1 : nk;
+    case kQueueSelfBwd: return p.causal ? nk - t : nk;
+    case kQueueSelfFwdPair: return p.causal ? min(2 * t + 2, nk) : nk;
+    case kQueueBcastFwd:
+    case kQueueBcastFwdPair: return nk;
+    default: return ceil_tiles(p.q_len);  // kQueueBcastBwd
+  }
 }
 
 __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParams p) {
@@ -61,8 +82,7 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
   if (tid == 0) s_bad = 0;
   __syncthreads();
 
-  const bool self = (p.mode == kQueueSelfFwd || p.mode == kQueueSelfBwd);
-  // 1. validate offsets, prefix sum of tiles per sequence
+  // 1. validate offsets, prefix sum of 128-row tiles per sequence
   int carry = 0;
   for (int b0 = 0; b0 < p.batch; b0 += kQThreads) {
     const int b = b0 + tid;
@@ -86,18 +106,15 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
   if (s_bad) {
     if (tid == 0) {
       if (atomicCAS(p.status, JFA_OK, JFA_ERR_BAD_INPUT) == JFA_OK) p.status[1] = kSiteQueueOffsets;
-      p.status[2] = 0;
+      p.status[p.count_index] = 0;
     }
     return;
   }
 
-  // 2. bucket sort by descending cost
-  int kmax;
-  if (p.mode == kQueueBcastBwd)
-    kmax = ceil_tiles(p.q_len);
-  else
-    kmax = ceil_tiles(p.max_seqlen);
-  const int kmin = (p.mode == kQueueBcastFwd) ? 0 : 1;  // an empty K/V sequence still owns output rows
+  // 2. bucket sort by descending cost; within a cost, ascending (b, tile, h)
+  const int kmax = (p.mode == kQueueBcastBwd) ? ceil_tiles(p.q_len) : ceil_tiles(p.max_seqlen);
+  const bool keep_empty = (p.mode == kQueueBcastFwd || p.mode == kQueueBcastFwdPair);  // empty K/V still owns output rows
+  const int kmin = keep_empty ? 0 : 1;
   int base = 0;
   for (int k = kmax; k >= kmin; --k) {
     int bucket = 0;
@@ -107,31 +124,18 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
       if (b < p.batch) {
         L = p.offsets[b + 1] - p.offsets[b];
         nt = item_tiles(p, L);
-        if (self && p.causal) {
-          count = (nt >= k) ? 1 : 0;  // fwd: tile k-1; bwd: tile nt-k
-        } else {
-          int cost;
-          if (p.mode == kQueueBcastFwd)
-            cost = ceil_tiles(L);
-          else if (p.mode == kQueueBcastBwd)
-            cost = ceil_tiles(p.q_len);
-          else
-            cost = nt;
-          count = (cost == k) ? nt : 0;
-        }
+        for (int t = 0; t < nt; ++t) count += (item_cost(p, L, t) == k) ? 1 : 0;
       }
       int tot;
       const int pre = block_exclusive_scan(count, warp_buf, &tot);
-      for (int r = 0; r < count; ++r) {
-        int t;
-        if (self && p.causal)
-          t = (p.mode == kQueueSelfFwd) ? k - 1 : nt - k;
-        else
-          t = r;
+      int r = 0;
+      for (int t = 0; t < nt && r < count; ++t) {
+        if (item_cost(p, L, t) != k) continue;
         const int slot = base + (bucket + pre + r) * p.heads;
         for (int h = 0; h < p.heads; ++h) {
           if (slot + h < p.max_items) p.items[slot + h] = make_int4(b, h, t, k);
         }
+        ++r;
       }
       bucket += tot;
     }
@@ -142,7 +146,7 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
       if (atomicCAS(p.status, JFA_OK, JFA_ERR_BAD_INPUT) == JFA_OK) p.status[1] = kSiteQueueOffsets;
       base = 0;
     }
-    p.status[2] = base;
+    p.status[p.count_index] = base;
   }
 }
 
