@@ -82,6 +82,21 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t co
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [rows, cols] accumulator read and reduced in 32-column x 128-row boxes
+// (128 bytes wide) with the 128-byte swizzle.
+bool make_tmap_f32_acc(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  if (rows == 0) rows = 1;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 4};
+  const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kTile)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool good_dim(int d) { return d == 64 || d == 128 || d == 192; }
 
 // Which forward kernel runs: head_dim 128 takes the flat-stream kernel on
@@ -383,7 +398,9 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   bl.budget_ns = wait_budget_ns();
   bl.grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items * (a->head_dim / chunk), 1)));
   record(a->main_kernel_events, 0, stream);
-  cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, stream);
+  CUtensorMap tdq;
+  if (!make_tmap_f32_acc(&tdq, dq_acc, a->total, cols)) return JFA_ERR_CUDA;
+  cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, tdq, stream);
   record(a->main_kernel_events, 1, stream);
   if (e != cudaSuccess) return JFA_ERR_CUDA;
   return cuda_status(launch_bwd_post(dq_acc, a->dq, n_acc, a->scale, status, sms, stream));
@@ -522,7 +539,9 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
     bl.budget_ns = wait_budget_ns();
     bl.grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
     record(a->main_kernel_events, 0, stream);
-    cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, stream);
+    CUtensorMap tdq;
+    if (!make_tmap_f32_acc(&tdq, dq_acc, a->q_len, cols)) return JFA_ERR_CUDA;
+    cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, tdq, stream);
     record(a->main_kernel_events, 1, stream);
     if (e != cudaSuccess) return JFA_ERR_CUDA;
   }

@@ -22,9 +22,14 @@
 //    S^T in TMEM) and dP^T into dS^T (bf16, written to shared memory in the
 //    128B-swizzled layout the tensor core reads both as dS^T for dK and as
 //    dS for dQ);
-//  * warps 4-7 drain dQ from TMEM into an fp32 accumulator with vector
-//    atomics (the cross-CTA reduction; contended in broadcast-Q) and write dK
-//    and dV at the end of each item;
+//  * warps 4-7 drain dQ from TMEM into an fp32 accumulator (the cross-CTA
+//    reduction; contended in broadcast-Q) and write dK and dV at the end of
+//    each item. dQ is staged through the dS buffer (idle between the dQ MMA
+//    and the next dS) in 128B-swizzled boxes and added by TMA reduce-add
+//    ("Optimizing Jagged Flash Attention with TLX", fifth paragraph: staging
+//    of the dQ reduce-add). Per-thread vector atomics measured slower: their
+//    strided requests held the SM's load/store path that the softmax warps
+//    use for TMEM and shared memory;
 //  * warp 8 = TMA producer, warp 9 = MMA issuer.
 //  * Order inside one query tile: S^T, dP^T, dV, dK, dQ. The Q/dO stage is
 //    released only after the last MMA that reads it (dK), so a single-stage
@@ -47,7 +52,6 @@ struct BwdParams {
   int32_t* status;
   const float* lse2p;         // log2-scaled LSE, tile-padded
   const float* deltap;        // delta, tile-padded
-  float* dq_acc;              // fp32 [rows_q, H, D]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int32_t heads, total, bcast, q_len, causal, n_chunks;
@@ -69,8 +73,8 @@ struct BwdLayout {
   static constexpr int kOffRow = kOffDS + kTile * kTile * 2;          // kStages x (lse2[128], delta[128])
   static constexpr int kOffBars = kOffRow + kStages * 1024;
   // kv_full, kv_empty, q_full[S], q_empty[S], s_full, p_full, dp_full, ds_full, ds_free,
-  // dq_full, dq_free, acc_full, acc_free, drain
-  static constexpr int kNumBars = 2 + 2 * kStages + 10;
+  // dq_full, dq_free, acc_full, acc_free, drain, stage_free, staged, stage_read
+  static constexpr int kNumBars = 2 + 2 * kStages + 13;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   static constexpr int kAlloc = kBytes + 256;
@@ -123,7 +127,7 @@ template <int D, int DC>
 __global__ void __launch_bounds__(320, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-               const BwdParams p) {
+               const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using Lay = BwdLayout<D, DC>;
   constexpr int kSt = Lay::kStages;
   constexpr uint32_t kIdS = ptx::idesc_bf16(128, 128, false, false);   // S^T, dP^T
@@ -153,6 +157,9 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* acc_full = s_full + 7;
   uint64_t* acc_free = s_full + 8;
   uint64_t* drain = s_full + 9;
+  uint64_t* stage_free = s_full + 10;  // the dQ staging in the dS buffer has been read by TMA (per tile)
+  uint64_t* staged = s_full + 11;      // the drain threads have written one half of the staging
+  uint64_t* stage_read = s_full + 12;  // TMA has read one half of the staging
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   ptx::CtaCtl* ctl = reinterpret_cast<ptx::CtaCtl*>(smem + Lay::kOffMisc + 8);
 
@@ -173,6 +180,9 @@ __global__ void __launch_bounds__(320, 1)
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(acc_free, 4);
     ptx::mbar_init(drain, 1);
+    ptx::mbar_init(stage_free, 1);
+    ptx::mbar_init(staged, 128);
+    ptx::mbar_init(stage_read, 1);
     ctl->abort = 0;
     ptx::fence_barrier_init();
   }
@@ -181,6 +191,7 @@ __global__ void __launch_bounds__(320, 1)
     ptx::prefetch_tmap(&tm_k);
     ptx::prefetch_tmap(&tm_v);
     ptx::prefetch_tmap(&tm_do);
+    ptx::prefetch_tmap(&tm_dq);
   }
   if (warp == 9) {
     ptx::tmem_alloc(tmem_slot, Lay::kTmemCols);
@@ -331,8 +342,9 @@ __global__ void __launch_bounds__(320, 1)
         const float* dlt = lse2 + 128;
         const int rq = I.Lq - kTile * i;  // valid query columns
         const bool masked = rk < kTile || rq < kTile || (p.causal && i == I.t);
-        const int cmax = (p.causal && i == I.t) ? r : 0;  // causal: query col c visible iff c >= r (same tile)
-        const bool row_ok = r < rk;
+        // visible query columns c of this key row: c_lo <= c < c_hi (causal: c >= r on the diagonal tile)
+        const int c_lo = (p.causal && i == I.t) ? r : 0;
+        const int c_hi = r < rk ? rq : 0;
         if (!(ok = ptx::mbar_wait(s_full, x & 1, ctl, status, kSiteBwdSoftS, budget))) break;
         ptx::tc_fence_after();
         // P^T = 2^(S^T * scale * log2e - lse2[q])
@@ -348,16 +360,28 @@ __global__ void __launch_bounds__(320, 1)
           for (int u = 0; u < 2; ++u) {
             uint32_t pk[16];
             const int cb = 64 * h2 + 32 * u;
+            float lq[32];  // lse2 of the 32 query columns (same for every lane: broadcast reads)
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int c0 = cb + 2 * e;
-              float p0 = ptx::ex2(fmaf(__uint_as_float(sv[u][2 * e]), sl, -lse2[c0]));
-              float p1 = ptx::ex2(fmaf(__uint_as_float(sv[u][2 * e + 1]), sl, -lse2[c0 + 1]));
-              if (masked) {
-                if (!row_ok || c0 >= rq || c0 < cmax) p0 = 0.f;
-                if (!row_ok || c0 + 1 >= rq || c0 + 1 < cmax) p1 = 0.f;
+            for (int e = 0; e < 8; ++e) *reinterpret_cast<float4*>(lq + 4 * e) = reinterpret_cast<const float4*>(lse2 + cb)[e];
+            // branch-free; the masked form only on edge tiles (with the tensor
+            // core reading shared memory, extra instructions here cost a lot)
+            if (!masked) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const float p0 = ptx::ex2(fmaf(__uint_as_float(sv[u][2 * e]), sl, -lq[2 * e]));
+                const float p1 = ptx::ex2(fmaf(__uint_as_float(sv[u][2 * e + 1]), sl, -lq[2 * e + 1]));
+                pk[e] = ptx::pack_bf16(p0, p1);
               }
-              pk[e] = ptx::pack_bf16(p0, p1);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int c0 = cb + 2 * e;
+                float p0 = ptx::ex2(fmaf(__uint_as_float(sv[u][2 * e]), sl, -lq[2 * e]));
+                float p1 = ptx::ex2(fmaf(__uint_as_float(sv[u][2 * e + 1]), sl, -lq[2 * e + 1]));
+                p0 = (c0 >= c_lo && c0 < c_hi) ? p0 : 0.f;
+                p1 = (c0 + 1 >= c_lo && c0 + 1 < c_hi) ? p1 : 0.f;
+                pk[e] = ptx::pack_bf16(p0, p1);
+              }
             }
             ptx::tmem_st16(tmem + lane_base + Lay::kColS + cb / 2, pk);
           }
@@ -369,8 +393,9 @@ __global__ void __launch_bounds__(320, 1)
         // dS^T = P^T * (dP^T - delta[q])
         if (!(ok = ptx::mbar_wait(dp_full, x & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
         ptx::tc_fence_after();
-        if (x > 0) {
+        if (x > 0) {  // the MMAs of the previous tile have read dS, and TMA has read the dQ staged there
           if (!(ok = ptx::mbar_wait(ds_free, (x - 1) & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
+          if (!(ok = ptx::mbar_wait(stage_free, (x - 1) & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
         }
 #pragma unroll 1
         for (int h2 = 0; h2 < 2; ++h2) {
@@ -387,12 +412,15 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             uint32_t w[4];
+            float dq8[8];  // delta of the 8 query columns (broadcast reads)
+            *reinterpret_cast<float4*>(dq8) = reinterpret_cast<const float4*>(dlt + 64 * h2 + 8 * ch)[0];
+            *reinterpret_cast<float4*>(dq8 + 4) = reinterpret_cast<const float4*>(dlt + 64 * h2 + 8 * ch)[1];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int cl = 8 * ch + 2 * e;  // column within the 64-wide half
               const uint32_t pw = pp[cl / 2];
-              const float d0 = __uint_as_float(dp[cl >> 5][cl & 31]) - dlt[64 * h2 + cl];
-              const float d1 = __uint_as_float(dp[(cl + 1) >> 5][(cl + 1) & 31]) - dlt[64 * h2 + cl + 1];
+              const float d0 = __uint_as_float(dp[cl >> 5][cl & 31]) - dq8[2 * e];
+              const float d1 = __uint_as_float(dp[(cl + 1) >> 5][(cl + 1) & 31]) - dq8[2 * e + 1];
               w[e] = ptx::pack_bf16(ptx::bf16lo(pw) * d0, ptx::bf16hi(pw) * d1);
             }
             uint4* dst = reinterpret_cast<uint4*>(ds_row + h2 * 16384 + ((ch ^ sw) << 4));
@@ -411,7 +439,7 @@ __global__ void __launch_bounds__(320, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t x = 0, kitem = 0;
+    uint32_t x = 0, kitem = 0, ns = 0;  // ns: halves of dQ staged so far
     bool ok = true;
     for (int v = blockIdx.x; ok && v < n_work; v += gridDim.x) {
       const BwdItem I = bwd_item(p, v);
@@ -420,26 +448,54 @@ __global__ void __launch_bounds__(320, 1)
         const int i = I.i0 + ii;
         if (!(ok = ptx::mbar_wait(dq_full, x & 1, ctl, status, kSiteBwdDQ, budget))) break;
         ptx::tc_fence_after();
-        const bool q_ok = kTile * i + r < I.Lq;
-        float* dst = p.dq_acc + (static_cast<int64_t>(I.q_row0 + kTile * i + r) * p.heads + I.h) * D + I.c * DC;
-#pragma unroll 1
-        for (int c = 0; c < DC / 32; ++c) {
-          uint32_t dq[32];
-          ptx::tmem_ld32(tmem + lane_base + Lay::kColDP + 32 * c, dq);
-          ptx::tmem_ld_wait();
-          ptx::reg_fence32(dq);
-          if (q_ok) {
+        // The whole dQ row comes out of TMEM first and the columns are released at
+        // once (the next dP^T goes there).
+        uint32_t dq[DC];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              float4 val = make_float4(__uint_as_float(dq[4 * e]), __uint_as_float(dq[4 * e + 1]),
-                                       __uint_as_float(dq[4 * e + 2]), __uint_as_float(dq[4 * e + 3]));
-              atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + 4 * e), val);
-            }
-          }
-        }
+        for (int c = 0; c < DC / 32; ++c)
+          ptx::tmem_ld32(tmem + lane_base + Lay::kColDP + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(dq + 32 * c));
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < DC / 32; ++c) ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(dq + 32 * c));
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(dq_free);
+        // Stage 64 columns at a time (two 32-column fp32 boxes of 16 KB, 128B
+        // swizzle) in the dS buffer, which the dK and dQ MMAs of this tile have
+        // finished reading, and add them into the accumulator with TMA. Rows past
+        // the sequence hold exact zeros (their dS is masked), so whole boxes are
+        // added.
+        uint8_t* stage = smem + Lay::kOffDS;
+        const int qrow = I.q_row0 + kTile * i;
+        const int xcol = I.h * D + I.c * DC;
+        const bool issuer = warp == 4 && lane == 0;
+#pragma unroll
+        for (int hf = 0; hf < DC / 64; ++hf) {
+          // the reduce-adds of the previous half have read the staging
+          if (hf > 0 && !(ok = ptx::mbar_wait(stage_read, (ns - 1) & 1, ctl, status, kSiteBwdDQ, budget))) break;
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            uint8_t* row = stage + b * 16384 + r * 128;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int k = 64 * hf + 32 * b + 4 * e;
+              ptx::st_shared_v4(row + ((e ^ (r & 7)) << 4), dq[k], dq[k + 1], dq[k + 2], dq[k + 3]);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          ptx::mbar_arrive(staged);
+          if (issuer) {
+            if (!(ok = ptx::mbar_wait(staged, ns & 1, ctl, status, kSiteBwdDQ, budget))) break;
+            ptx::tma_reduce_add_2d(&tm_dq, stage, xcol + 64 * hf, qrow);
+            ptx::tma_reduce_add_2d(&tm_dq, stage + 16384, xcol + 64 * hf + 32, qrow);
+            ptx::bulk_commit();
+            ptx::bulk_wait_read0();
+            ptx::mbar_arrive(stage_read);
+          }
+          ++ns;
+        }
+        if (!ok) break;
+        if (issuer) ptx::mbar_arrive(stage_free);
       }
       if (!ok) break;
       if (!(ok = ptx::mbar_wait(acc_full, kitem & 1, ctl, status, kSiteBwdEpi, budget))) break;
@@ -474,6 +530,7 @@ __global__ void __launch_bounds__(320, 1)
       if (lane == 0) ptx::mbar_arrive(acc_free);
       ++kitem;
     }
+    if (warp == 4 && lane == 0) ptx::bulk_wait0();  // every reduce-add has completed
   }
 
   ptx::tc_fence_before();
@@ -573,7 +630,8 @@ __global__ void bwd_post_kernel(const float4* __restrict__ acc, uint2* __restric
 
 template <int D, int DC>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream) {
+                                const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int grid,
+                                cudaStream_t stream) {
   using Lay = BwdLayout<D, DC>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -581,12 +639,12 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  bwd_kernel<D, DC><<<grid, 320, Lay::kAlloc, stream>>>(tq, tk, tv, tdo, p);
+  bwd_kernel<D, DC><<<grid, 320, Lay::kAlloc, stream>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, cudaStream_t stream) {
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, cudaStream_t stream) {
   BwdParams p;
   p.offsets = L.offsets;
   p.tile_base = L.tile_base;
@@ -594,7 +652,6 @@ cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUt
   p.status = L.status;
   p.lse2p = L.lse2p;
   p.deltap = L.deltap;
-  p.dq_acc = L.dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(L.dk);
   p.dv = static_cast<__nv_bfloat16*>(L.dv);
   p.heads = L.heads;
@@ -607,10 +664,10 @@ cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUt
   p.scale = L.scale;
   p.scale_log2 = L.scale * 1.4426950408889634f;
   p.budget_ns = L.budget_ns;
-  if (L.head_dim == 64 && L.head_chunk == 64) return launch_bwd_t<64, 64>(tq, tk, tv, tdo, p, L.grid, stream);
-  if (L.head_dim == 128 && L.head_chunk == 128) return launch_bwd_t<128, 128>(tq, tk, tv, tdo, p, L.grid, stream);
-  if (L.head_dim == 128 && L.head_chunk == 64) return launch_bwd_t<128, 64>(tq, tk, tv, tdo, p, L.grid, stream);
-  if (L.head_dim == 192 && L.head_chunk == 64) return launch_bwd_t<192, 64>(tq, tk, tv, tdo, p, L.grid, stream);
+  if (L.head_dim == 64 && L.head_chunk == 64) return launch_bwd_t<64, 64>(tq, tk, tv, tdo, tdq, p, L.grid, stream);
+  if (L.head_dim == 128 && L.head_chunk == 128) return launch_bwd_t<128, 128>(tq, tk, tv, tdo, tdq, p, L.grid, stream);
+  if (L.head_dim == 128 && L.head_chunk == 64) return launch_bwd_t<128, 64>(tq, tk, tv, tdo, tdq, p, L.grid, stream);
+  if (L.head_dim == 192 && L.head_chunk == 64) return launch_bwd_t<192, 64>(tq, tk, tv, tdo, tdq, p, L.grid, stream);
   return cudaErrorInvalidValue;
 }
 

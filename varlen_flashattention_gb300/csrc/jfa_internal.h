@@ -104,8 +104,9 @@ cudaError_t launch_fwd_stream(bool pair, bool causal, const CUtensorMap& tq, con
                               const CUtensorMap& tv, const int32_t* offsets, const int4* items, int32_t* status,
                               void* o, float* lse, int heads, int total, int bcast, int q_len, float scale,
                               uint64_t budget_ns, int grid, cudaStream_t stream);
+// tdq: the fp32 dQ accumulator [rows, H*D] in 32-column x 128-row boxes, 128B swizzle.
 cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, cudaStream_t stream);
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, cudaStream_t stream);
 cudaError_t launch_bwd_pre(int head_dim, const void* o, const void* dout, const float* lse, const int32_t* offsets,
                            const int32_t* tile_base, const int32_t* status, int batch, int heads, int total, int bcast,
                            int q_len, int pad_tiles, int grid_tiles, float* lse2p, float* deltap,
