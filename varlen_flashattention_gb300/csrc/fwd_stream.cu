@@ -47,7 +47,7 @@ namespace {
 
 constexpr int kD2 = 128;
 
-struct Fwd2Params {
+struct FwdStreamParams {
   const int32_t* offsets;
   const int4* items;  // (b, h, pair u, cost)
   int32_t* status;
@@ -59,7 +59,7 @@ struct Fwd2Params {
 };
 
 template <bool PAIR>
-struct Fwd2Layout {
+struct FwdStreamLayout {
   static constexpr int kQBytes = kTile * kD2 * 2;  // own query tile: 128 rows x 128 d
   // a slot holds half a K tile (64 rows) or half a V tile (64 columns) on a
   // pair, a whole K or V tile on a single CTA
@@ -80,16 +80,16 @@ struct Fwd2Layout {
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
-struct Fwd2Item {
+struct FwdStreamItem {
   int b, h, u, t;  // t = this CTA's query tile (2u + rank)
   int q_tma_row, kv_row0, Lq, Lk, n_kv;
   int64_t o_row, lse0;
 };
 
 template <bool CAUSAL, bool PAIR>
-__device__ __forceinline__ Fwd2Item fwd2_item(const Fwd2Params& p, int idx, uint32_t rank) {
+__device__ __forceinline__ FwdStreamItem stream_item(const FwdStreamParams& p, int idx, uint32_t rank) {
   const int4 it = p.items[idx];
-  Fwd2Item I;
+  FwdStreamItem I;
   I.b = it.x;
   I.h = it.y;
   I.u = it.z;
@@ -117,10 +117,10 @@ __device__ __forceinline__ Fwd2Item fwd2_item(const Fwd2Params& p, int idx, uint
 // The next item of this cluster with at least one key/value tile, starting at
 // index idx. Returns its index (>= n_items when there is none).
 template <bool CAUSAL, bool PAIR>
-__device__ __forceinline__ int next_busy(const Fwd2Params& p, int idx, int stride, int n_items, uint32_t rank,
-                                         Fwd2Item& I) {
+__device__ __forceinline__ int next_busy(const FwdStreamParams& p, int idx, int stride, int n_items, uint32_t rank,
+                                         FwdStreamItem& I) {
   for (; idx < n_items; idx += stride) {
-    I = fwd2_item<CAUSAL, PAIR>(p, idx, rank);
+    I = stream_item<CAUSAL, PAIR>(p, idx, rank);
     if (I.n_kv > 0) break;
   }
   return idx;
@@ -131,9 +131,9 @@ __device__ __forceinline__ int next_busy(const Fwd2Params& p, int idx, int strid
 // item's Q and first K) before V of step j. The producer and the forwarder of
 // CTA 1 both walk it. Each callback returns false to stop the walk.
 template <bool CAUSAL, bool PAIR, class FQ, class FK, class FV>
-__device__ __forceinline__ void walk_loads(const Fwd2Params& p, uint32_t rank, int first, int stride, int n_items,
+__device__ __forceinline__ void walk_loads(const FwdStreamParams& p, uint32_t rank, int first, int stride, int n_items,
                                            FQ on_q, FK on_k, FV on_v) {
-  Fwd2Item cur, nxt;
+  FwdStreamItem cur, nxt;
   int idx = next_busy<CAUSAL, PAIR>(p, first, stride, n_items, rank, cur);
   if (idx >= n_items) return;
   if (!on_q(cur) || !on_k(cur, 0)) return;
@@ -158,9 +158,9 @@ __device__ __forceinline__ void walk_loads(const Fwd2Params& p, uint32_t rank, i
 // (each CTA loads half of a key tile) and 128-row boxes on a single CTA.
 template <bool CAUSAL, bool PAIR>
 __global__ void __launch_bounds__(320, 1)
-    fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const Fwd2Params p) {
-  using Lay = Fwd2Layout<PAIR>;
+    fwd_stream_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const FwdStreamParams p) {
+  using Lay = FwdStreamLayout<PAIR>;
   constexpr int kM = PAIR ? 256 : 128;
   constexpr int kKAtom = PAIR ? 8192 : 16384;  // bytes of one 64-column atom of the K rows a CTA holds
   constexpr uint32_t kPeers = PAIR ? 8 : 4;   // softmax / epilogue warps that signal the issuing CTA
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(320, 1)
         ++pos;
         return true;
       };
-      auto on_q = [&](const Fwd2Item& I) -> bool {
+      auto on_q = [&](const FwdStreamItem& I) -> bool {
         const uint32_t qs = kq % kQS, qround = kq / kQS;
         if (!wait_x(q_empty + qs, (qround & 1) ^ 1, ctl, status, kSiteFwdProdQ, budget)) return false;
         ptx::mbar_arrive_expect_tx(q_full + qs, Lay::kQBytes);
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(320, 1)
         return true;
       };
       // pair: key rows 64 rank .. of tile j, all of d; single: the whole tile
-      auto on_k = [&](const Fwd2Item& I, int j) -> bool {
+      auto on_k = [&](const FwdStreamItem& I, int j) -> bool {
         uint32_t slot;
         if (!next_slot(slot)) return false;
         uint8_t* dst = smem + Lay::kOffSlots + slot * Lay::kHalfBytes;
@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(320, 1)
         return true;
       };
       // pair: all key rows of tile j, head-dim columns 64 rank ..; single: the whole tile
-      auto on_v = [&](const Fwd2Item& I, int j) -> bool {
+      auto on_v = [&](const FwdStreamItem& I, int j) -> bool {
         uint32_t slot;
         if (!next_slot(slot)) return false;
 #pragma unroll
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       return true;
     };
-    Fwd2Item cur, nxt;
+    FwdStreamItem cur, nxt;
     int idx = next_busy<CAUSAL, PAIR>(p, cluster, n_clusters, n_items, rank, cur);
     uint32_t kq = 0, x = 0;  // busy items so far, steps so far
     if (idx < n_items) ok = q_wait(0) && issue_s(0, 0, cur.n_kv == 1);
@@ -416,14 +416,14 @@ __global__ void __launch_bounds__(320, 1)
     // Tells CTA 0 that this CTA's halves of Q and of every K/V tile have landed.
     if (lane == 0) {
       uint32_t pos = 0, kq = 0;
-      auto on_q = [&](const Fwd2Item&) -> bool {
+      auto on_q = [&](const FwdStreamItem&) -> bool {
         const uint32_t qs = kq % kQS, qround = kq / kQS;
         if (!ptx::mbar_wait(q_full + qs, qround & 1, ctl, status, kSiteFwdMmaQ, budget)) return false;
         ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(q_peer + qs), 0));
         ++kq;
         return true;
       };
-      auto on_slot = [&](const Fwd2Item&, int) -> bool {
+      auto on_slot = [&](const FwdStreamItem&, int) -> bool {
         const uint32_t slot = pos % kSlots, round = pos / kSlots;
         if (!ptx::mbar_wait(slot_full + slot, round & 1, ctl, status, kSiteFwdMmaSlot, budget)) return false;
         ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(slot_peer + slot), 0));
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(320, 1)
     uint32_t x = 0, kq = 0;
     bool ok = true;
     for (int idx = cluster; ok && idx < n_items; idx += n_clusters) {
-      const Fwd2Item I = fwd2_item<CAUSAL, PAIR>(p, idx, rank);
+      const FwdStreamItem I = stream_item<CAUSAL, PAIR>(p, idx, rank);
       const int n = I.n_kv;
       if (n == 0) continue;
       const uint32_t ob = kq & 1;
@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(320, 1)
     };
     uint32_t kq = 0;
     for (int idx = cluster; idx < n_items; idx += n_clusters) {
-      const Fwd2Item I = fwd2_item<CAUSAL, PAIR>(p, idx, rank);
+      const FwdStreamItem I = stream_item<CAUSAL, PAIR>(p, idx, rank);
       const int qi = kTile * I.t + r;
       const bool row_ok = qi < I.Lq;
       __nv_bfloat16* orow = p.o + (I.o_row + r) * static_cast<int64_t>(p.heads) * kD2 + static_cast<int64_t>(I.h) * kD2;
@@ -642,12 +642,12 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 template <bool CAUSAL, bool PAIR>
-cudaError_t launch_fwd2_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const Fwd2Params& p,
+cudaError_t launch_fwd_stream_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdStreamParams& p,
                           int grid, cudaStream_t stream) {
-  using Lay = Fwd2Layout<PAIR>;
+  using Lay = FwdStreamLayout<PAIR>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fwd2_kernel<CAUSAL, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fwd_stream_kernel<CAUSAL, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Lay::kAlloc);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -664,7 +664,7 @@ cudaError_t launch_fwd2_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fwd2_kernel<CAUSAL, PAIR>, tq, tk, tv, p);
+  return cudaLaunchKernelEx(&cfg, fwd_stream_kernel<CAUSAL, PAIR>, tq, tk, tv, p);
 }
 
 }  // namespace
@@ -673,7 +673,7 @@ cudaError_t launch_fwd_stream(bool pair, bool causal, const CUtensorMap& tq, con
                               const CUtensorMap& tv, const int32_t* offsets, const int4* items, int32_t* status,
                               void* o, float* lse, int heads, int total, int bcast, int q_len, float scale,
                               uint64_t budget_ns, int grid, cudaStream_t stream) {
-  Fwd2Params p;
+  FwdStreamParams p;
   p.offsets = offsets;
   p.items = items;
   p.status = status;
@@ -686,10 +686,10 @@ cudaError_t launch_fwd_stream(bool pair, bool causal, const CUtensorMap& tq, con
   p.scale_log2 = scale * 1.4426950408889634f;
   p.budget_ns = budget_ns;
   if (pair)
-    return causal ? launch_fwd2_t<true, true>(tq, tk, tv, p, grid, stream)
-                  : launch_fwd2_t<false, true>(tq, tk, tv, p, grid, stream);
-  return causal ? launch_fwd2_t<true, false>(tq, tk, tv, p, grid, stream)
-                : launch_fwd2_t<false, false>(tq, tk, tv, p, grid, stream);
+    return causal ? launch_fwd_stream_t<true, true>(tq, tk, tv, p, grid, stream)
+                  : launch_fwd_stream_t<false, true>(tq, tk, tv, p, grid, stream);
+  return causal ? launch_fwd_stream_t<true, false>(tq, tk, tv, p, grid, stream)
+                : launch_fwd_stream_t<false, false>(tq, tk, tv, p, grid, stream);
 }
 
 }  // namespace jfa
