@@ -50,8 +50,8 @@ struct BwdParams {
   const int32_t* tile_base;   // self: padded q-tile index of each sequence
   const int4* items;
   int32_t* status;
-  const float* lse2p;         // log2-scaled LSE, tile-padded
-  const float* deltap;        // delta, tile-padded
+  const float* lse2p;         // -LSE log2(e), tile-padded (stored negated)
+  const float* deltap;        // -delta, tile-padded (stored negated)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int32_t heads, total, bcast, q_len, causal, n_chunks;
@@ -360,24 +360,30 @@ __global__ void __launch_bounds__(320, 1)
           for (int u = 0; u < 2; ++u) {
             uint32_t pk[16];
             const int cb = 64 * h2 + 32 * u;
-            float lq[32];  // lse2 of the 32 query columns (same for every lane: broadcast reads)
+            float lq[32];  // -lse2 of the 32 query columns (same for every lane: broadcast reads)
 #pragma unroll
             for (int e = 0; e < 8; ++e) *reinterpret_cast<float4*>(lq + 4 * e) = reinterpret_cast<const float4*>(lse2 + cb)[e];
+            const uint64_t sl2 = ptx::f2_packf(sl, sl);
             // branch-free; the masked form only on edge tiles (with the tensor
             // core reading shared memory, extra instructions here cost a lot)
             if (!masked) {
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
-                const float p0 = ptx::ex2(fmaf(__uint_as_float(sv[u][2 * e]), sl, -lq[2 * e]));
-                const float p1 = ptx::ex2(fmaf(__uint_as_float(sv[u][2 * e + 1]), sl, -lq[2 * e + 1]));
-                pk[e] = ptx::pack_bf16(p0, p1);
+                float x0, x1;
+                ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sv[u][2 * e], sv[u][2 * e + 1]), sl2,
+                                           ptx::f2_packf(lq[2 * e], lq[2 * e + 1])),
+                               x0, x1);
+                pk[e] = ptx::pack_bf16(ptx::ex2(x0), ptx::ex2(x1));
               }
             } else {
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
                 const int c0 = cb + 2 * e;
-                float p0 = ptx::ex2(fmaf(__uint_as_float(sv[u][2 * e]), sl, -lq[2 * e]));
-                float p1 = ptx::ex2(fmaf(__uint_as_float(sv[u][2 * e + 1]), sl, -lq[2 * e + 1]));
+                float x0, x1;
+                ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sv[u][2 * e], sv[u][2 * e + 1]), sl2,
+                                           ptx::f2_packf(lq[2 * e], lq[2 * e + 1])),
+                               x0, x1);
+                float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
                 p0 = (c0 >= c_lo && c0 < c_hi) ? p0 : 0.f;
                 p1 = (c0 + 1 >= c_lo && c0 + 1 < c_hi) ? p1 : 0.f;
                 pk[e] = ptx::pack_bf16(p0, p1);
@@ -412,16 +418,19 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             uint32_t w[4];
-            float dq8[8];  // delta of the 8 query columns (broadcast reads)
+            float dq8[8];  // -delta of the 8 query columns (broadcast reads)
             *reinterpret_cast<float4*>(dq8) = reinterpret_cast<const float4*>(dlt + 64 * h2 + 8 * ch)[0];
             *reinterpret_cast<float4*>(dq8 + 4) = reinterpret_cast<const float4*>(dlt + 64 * h2 + 8 * ch)[1];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int cl = 8 * ch + 2 * e;  // column within the 64-wide half
+              const int cl = 8 * ch + 2 * e;  // column within the 64-wide half (even)
               const uint32_t pw = pp[cl / 2];
-              const float d0 = __uint_as_float(dp[cl >> 5][cl & 31]) - dq8[2 * e];
-              const float d1 = __uint_as_float(dp[(cl + 1) >> 5][(cl + 1) & 31]) - dq8[2 * e + 1];
-              w[e] = ptx::pack_bf16(ptx::bf16lo(pw) * d0, ptx::bf16hi(pw) * d1);
+              // (dP - delta) and P (bf16 pair widened) multiplied on fp32 pairs
+              const uint64_t d2 = ptx::f2_add(ptx::f2_pack(dp[cl >> 5][cl & 31], dp[cl >> 5][(cl & 31) + 1]),
+                                              ptx::f2_packf(dq8[2 * e], dq8[2 * e + 1]));
+              float s0, s1;
+              ptx::f2_unpack(ptx::f2_mul(ptx::f2_packf(ptx::bf16lo(pw), ptx::bf16hi(pw)), d2), s0, s1);
+              w[e] = ptx::pack_bf16(s0, s1);
             }
             uint4* dst = reinterpret_cast<uint4*>(ds_row + h2 * 16384 + ((ch ^ sw) << 4));
             *dst = make_uint4(w[0], w[1], w[2], w[3]);
@@ -543,7 +552,8 @@ __global__ void __launch_bounds__(320, 1)
 
 // ------------------------------------------------------------------ pre / post
 
-// delta = rowsum(dO * O) and lse2 = LSE * log2(e), written in a layout padded
+// delta = rowsum(dO * O) and lse2 = LSE * log2(e), both stored negated (the
+// backward adds them with paired fp32 instructions), written in a layout padded
 // to whole 128-row query tiles (zeros past the end of a sequence), so that the
 // backward can fetch one tile's 128 values with a single aligned bulk copy.
 // One CTA per padded query tile (blockIdx.x) and head (blockIdx.y); one warp
@@ -604,8 +614,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
       for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     }
     if (lane == 0) {
-      deltap[pad_base + r] = ok ? acc : 0.f;
-      lse2p[pad_base + r] = ok ? lse[lse_base + r] * kLog2e : 0.f;
+      deltap[pad_base + r] = ok ? -acc : 0.f;
+      lse2p[pad_base + r] = ok ? -lse[lse_base + r] * kLog2e : 0.f;
     }
   }
 }

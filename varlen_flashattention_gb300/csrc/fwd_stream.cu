@@ -481,22 +481,25 @@ __global__ void __launch_bounds__(320, 1)
         mask(sa[0], 0);
         mask(sa[1], 32);
         mask(sb, 64);
-        float mx4[4];
+        // row max: eight independent chains of three-input maxima
+        float mx8[8];
+        auto fold = [&](const uint32_t(&v)[32], int e0) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) mx4[k] = __uint_as_float(sa[0][k]);
+          for (int e = e0; e < 32; e += 2)
+            mx8[(e >> 1) & 7] = ptx::fmax3(mx8[(e >> 1) & 7], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+        };
 #pragma unroll
-        for (int e = 4; e < 32; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(sa[0][e]));
-#pragma unroll
-        for (int e = 0; e < 32; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(sa[1][e]));
-#pragma unroll
-        for (int e = 0; e < 32; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(sb[e]));
+        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(__uint_as_float(sa[0][2 * k]), __uint_as_float(sa[0][2 * k + 1]));
+        fold(sa[0], 16);
+        fold(sa[1], 0);
+        fold(sb, 0);
         ptx::tmem_ld32(s_tmem + 96, sb);
         ptx::tmem_ld_wait();
         ptx::reg_fence32(sb);
         mask(sb, 96);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(sb[e]));
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        fold(sb, 0);
+        const float mx = fmaxf(ptx::fmax3(mx8[0], mx8[1], mx8[2]),
+                               ptx::fmax3(ptx::fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
         const float mnew = mx * sl;
         if (j == 0) {
           m = mnew;
@@ -528,14 +531,17 @@ __global__ void __launch_bounds__(320, 1)
         }
         // a row with every key of this tile masked (possible only above the diagonal) keeps m
         const float mu = (m == -INFINITY) ? 0.f : m;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // P = 2^(S sl - m): scale and shift on fp32 pairs, exp2 per element, sums on pairs
+        const uint64_t sl2 = ptx::f2_packf(sl, sl), nmu2 = ptx::f2_packf(-mu, -mu);
+        uint64_t ls2[2] = {ptx::f2_packf(0.f, 0.f), ptx::f2_packf(0.f, 0.f)};
         auto exp_store = [&](const uint32_t(&v)[32], int c) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ptx::ex2(fmaf(__uint_as_float(v[2 * e]), sl, -mu));
-            const float p1 = ptx::ex2(fmaf(__uint_as_float(v[2 * e + 1]), sl, -mu));
-            ls[e & 3] += p0 + p1;
+            float x0, x1;
+            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(v[2 * e], v[2 * e + 1]), sl2, nmu2), x0, x1);
+            const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+            ls2[e & 1] = ptx::f2_add(ls2[e & 1], ptx::f2_packf(p0, p1));
             pk[e] = ptx::pack_bf16(p0, p1);
           }
           ptx::tmem_st16(s_tmem + 16 * c, pk);
@@ -551,7 +557,12 @@ __global__ void __launch_bounds__(320, 1)
         exp_store(sb, 2);
         mask(sa[0], 96);
         exp_store(sa[0], 3);
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        {
+          float a0, a1, b0, b1;
+          ptx::f2_unpack(ls2[0], a0, a1);
+          ptx::f2_unpack(ls2[1], b0, b1);
+          l += (a0 + a1) + (b0 + b1);
+        }
         if (j + 1 == n) {
           // row statistics of the finished item go to the epilogue
           if (kq >= 2 &&
