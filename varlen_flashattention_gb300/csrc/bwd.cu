@@ -24,16 +24,21 @@
 //    dS for dQ);
 //  * warps 4-7 drain dQ from TMEM into an fp32 accumulator (the cross-CTA
 //    reduction; contended in broadcast-Q) and write dK and dV at the end of
-//    each item. dQ is staged through the dS buffer (idle between the dQ MMA
-//    and the next dS) in 128B-swizzled boxes and added by TMA reduce-add
+//    each item. dQ is staged, in 128B-swizzled fp32 boxes, in the Q/dO stage
+//    buffers of its own query tile (free once the dQ MMA has completed: dK
+//    and dV were their last readers) and added by TMA reduce-add
 //    ("Optimizing Jagged Flash Attention with TLX", fifth paragraph: staging
-//    of the dQ reduce-add). Per-thread vector atomics measured slower: their
+//    of the dQ reduce-add); the drain warps release the stage to the producer
+//    after TMA has read it. Per-thread vector atomics measured slower: their
 //    strided requests held the SM's load/store path that the softmax warps
 //    use for TMEM and shared memory;
 //  * warp 8 = TMA producer, warp 9 = MMA issuer.
-//  * Order inside one query tile: S^T, dP^T, dV, dK, dQ. The Q/dO stage is
-//    released only after the last MMA that reads it (dK), so a single-stage
-//    ring cannot deadlock (TwelveLabs, bug hunting).
+//  * Order inside one query tile: dP^T, dV, [S^T of the next tile], dK, dQ,
+//    so that the softmax of the next tile overlaps the dK / dQ MMAs. With a
+//    single Q/dO stage (head_dim 192) the next tile's Q arrives only after
+//    this tile's dQ has been staged out of the stage, so there S^T is issued
+//    at the start of its own tile (TwelveLabs, bug hunting: the single-stage
+//    deadlock).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -73,8 +78,8 @@ struct BwdLayout {
   static constexpr int kOffRow = kOffDS + kTile * kTile * 2;          // kStages x (lse2[128], delta[128])
   static constexpr int kOffBars = kOffRow + kStages * 1024;
   // kv_full, kv_empty, q_full[S], q_empty[S], s_full, p_full, dp_full, ds_full, ds_free,
-  // dq_full, dq_free, acc_full, acc_free, drain, stage_free, staged, stage_read
-  static constexpr int kNumBars = 2 + 2 * kStages + 13;
+  // dq_full, dq_free, acc_full, acc_free, drain, staged
+  static constexpr int kNumBars = 2 + 2 * kStages + 11;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   static constexpr int kAlloc = kBytes + 256;
@@ -157,9 +162,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* acc_full = s_full + 7;
   uint64_t* acc_free = s_full + 8;
   uint64_t* drain = s_full + 9;
-  uint64_t* stage_free = s_full + 10;  // the dQ staging in the dS buffer has been read by TMA (per tile)
-  uint64_t* staged = s_full + 11;      // the drain threads have written one half of the staging
-  uint64_t* stage_read = s_full + 12;  // TMA has read one half of the staging
+  uint64_t* staged = s_full + 10;  // the drain threads have written the dQ staging of a tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   ptx::CtaCtl* ctl = reinterpret_cast<ptx::CtaCtl*>(smem + Lay::kOffMisc + 8);
 
@@ -180,9 +183,7 @@ __global__ void __launch_bounds__(320, 1)
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(acc_free, 4);
     ptx::mbar_init(drain, 1);
-    ptx::mbar_init(stage_free, 1);
     ptx::mbar_init(staged, 128);
-    ptx::mbar_init(stage_read, 1);
     ctl->abort = 0;
     ptx::fence_barrier_init();
   }
@@ -253,20 +254,33 @@ __global__ void __launch_bounds__(320, 1)
         if (I.nq <= 0) continue;
         if (!(ok = ptx::mbar_wait(kv_full, kitem & 1, ctl, status, kSiteBwdMmaKV, budget))) break;
         ptx::tc_fence_after();
-        for (int ii = 0; ii < I.nq; ++ii, ++x) {
-          const uint32_t st = pos % kSt, round = pos / kSt;
-          if (!(ok = ptx::mbar_wait(q_full + st, round & 1, ctl, status, kSiteBwdMmaQ, budget))) break;
-          ptx::tc_fence_after();
-          const uint32_t q_addr = ptx::smem_u32(smem + Lay::kOffQ + st * Lay::kTileBytes);
-          const uint32_t do_addr = ptx::smem_u32(smem + Lay::kOffDO + st * Lay::kTileBytes);
-          // S^T = K Q^T
+        // S^T(x) = K Q^T. With two Q/dO stages it is issued for the first query
+        // tile of the item here and for every later one right after dS^T of the
+        // previous tile, so the softmax of tile x + 1 overlaps the dK / dQ MMAs
+        // of tile x; with one stage, at the start of its own tile.
+        auto issue_s = [&](uint32_t stage) {
+          const uint32_t qa = ptx::smem_u32(smem + Lay::kOffQ + stage * Lay::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
             ptx::mma_ss(tmem + Lay::kColS, ptx::sdesc_sw128(k_addr + off, 16, 1024),
-                        ptx::sdesc_sw128(q_addr + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                        ptx::sdesc_sw128(qa + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
           }
           ptx::mma_commit(s_full);
+        };
+        auto wait_q = [&](uint32_t ps) -> bool {
+          if (!ptx::mbar_wait(q_full + ps % kSt, (ps / kSt) & 1, ctl, status, kSiteBwdMmaQ, budget)) return false;
+          ptx::tc_fence_after();
+          return true;
+        };
+        for (int ii = 0; ii < I.nq; ++ii, ++x) {
+          const uint32_t st = pos % kSt;
+          if (ii == 0 || kSt == 1) {
+            if (!(ok = wait_q(pos))) break;
+            issue_s(st);
+          }
+          const uint32_t q_addr = ptx::smem_u32(smem + Lay::kOffQ + st * Lay::kTileBytes);
+          const uint32_t do_addr = ptx::smem_u32(smem + Lay::kOffDO + st * Lay::kTileBytes);
           // dP^T = V dO^T into the columns dQ of the previous tile used
           if (x > 0) {
             if (!(ok = ptx::mbar_wait(dq_free, (x - 1) & 1, ctl, status, kSiteBwdMmaDQFree, budget))) break;
@@ -291,9 +305,14 @@ __global__ void __launch_bounds__(320, 1)
                         ptx::sdesc_sw128(do_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdAcc,
                         (ii > 0 || kk > 0) ? 1u : 0u);
           }
-          // dK += dS^T Q[:, slice]
           if (!(ok = ptx::mbar_wait(ds_full, x & 1, ctl, status, kSiteBwdMmaDS, budget))) break;
           ptx::tc_fence_after();
+          // the S^T columns are free: dV has been issued and the softmax has read P^T back
+          if (kSt > 1 && ii + 1 < I.nq) {
+            if (!(ok = wait_q(pos + 1))) break;
+            issue_s((pos + 1) % kSt);
+          }
+          // dK += dS^T Q[:, slice]
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -301,7 +320,6 @@ __global__ void __launch_bounds__(320, 1)
                         ptx::sdesc_sw128(q_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdAcc,
                         (ii > 0 || kk > 0) ? 1u : 0u);
           }
-          ptx::mma_commit(q_empty + st);  // last reader of this Q/dO stage
           // dQ(tile) = dS K[:, slice] into the dP^T columns
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -309,7 +327,7 @@ __global__ void __launch_bounds__(320, 1)
                         ptx::sdesc_sw128(k_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdDQ,
                         kk > 0 ? 1u : 0u);
           }
-          ptx::mma_commit(dq_full);
+          ptx::mma_commit(dq_full);  // the drain stages dQ in this Q/dO stage and then releases it
           ptx::mma_commit(ds_free);
           ++pos;
         }
@@ -399,9 +417,8 @@ __global__ void __launch_bounds__(320, 1)
         // dS^T = P^T * (dP^T - delta[q])
         if (!(ok = ptx::mbar_wait(dp_full, x & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
         ptx::tc_fence_after();
-        if (x > 0) {  // the MMAs of the previous tile have read dS, and TMA has read the dQ staged there
+        if (x > 0) {  // the MMAs of the previous tile have read dS
           if (!(ok = ptx::mbar_wait(ds_free, (x - 1) & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
-          if (!(ok = ptx::mbar_wait(stage_free, (x - 1) & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
         }
 #pragma unroll 1
         for (int h2 = 0; h2 < 2; ++h2) {
@@ -448,7 +465,7 @@ __global__ void __launch_bounds__(320, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t x = 0, kitem = 0, ns = 0;  // ns: halves of dQ staged so far
+    uint32_t x = 0, kitem = 0;
     bool ok = true;
     for (int v = blockIdx.x; ok && v < n_work; v += gridDim.x) {
       const BwdItem I = bwd_item(p, v);
@@ -469,42 +486,39 @@ __global__ void __launch_bounds__(320, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(dq_free);
-        // Stage 64 columns at a time (two 32-column fp32 boxes of 16 KB, 128B
-        // swizzle) in the dS buffer, which the dK and dQ MMAs of this tile have
-        // finished reading, and add them into the accumulator with TMA. Rows past
-        // the sequence hold exact zeros (their dS is masked), so whole boxes are
-        // added.
-        uint8_t* stage = smem + Lay::kOffDS;
+        // Stage the DC columns as 32-column fp32 boxes (16 KB, 128B swizzle) in
+        // this tile's Q and then dO stage buffers, add them into the
+        // accumulator with TMA, and hand the stage back to the producer once
+        // TMA has read it. Rows past the sequence hold exact zeros (their dS is
+        // masked), so whole boxes are added.
+        const uint32_t st = x % kSt;
+        auto box_addr = [&](int bx) -> uint8_t* {
+          const int off = bx * 16384;
+          return off < Lay::kTileBytes ? smem + Lay::kOffQ + st * Lay::kTileBytes + off
+                                       : smem + Lay::kOffDO + st * Lay::kTileBytes + (off - Lay::kTileBytes);
+        };
         const int qrow = I.q_row0 + kTile * i;
         const int xcol = I.h * D + I.c * DC;
         const bool issuer = warp == 4 && lane == 0;
 #pragma unroll
-        for (int hf = 0; hf < DC / 64; ++hf) {
-          // the reduce-adds of the previous half have read the staging
-          if (hf > 0 && !(ok = ptx::mbar_wait(stage_read, (ns - 1) & 1, ctl, status, kSiteBwdDQ, budget))) break;
+        for (int bx = 0; bx < DC / 32; ++bx) {
+          uint8_t* row = box_addr(bx) + r * 128;
 #pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            uint8_t* row = stage + b * 16384 + r * 128;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int k = 64 * hf + 32 * b + 4 * e;
-              ptx::st_shared_v4(row + ((e ^ (r & 7)) << 4), dq[k], dq[k + 1], dq[k + 2], dq[k + 3]);
-            }
+          for (int e = 0; e < 8; ++e) {
+            const int k = 32 * bx + 4 * e;
+            ptx::st_shared_v4(row + ((e ^ (r & 7)) << 4), dq[k], dq[k + 1], dq[k + 2], dq[k + 3]);
           }
-          ptx::fence_proxy_async_smem();
-          ptx::mbar_arrive(staged);
-          if (issuer) {
-            if (!(ok = ptx::mbar_wait(staged, ns & 1, ctl, status, kSiteBwdDQ, budget))) break;
-            ptx::tma_reduce_add_2d(&tm_dq, stage, xcol + 64 * hf, qrow);
-            ptx::tma_reduce_add_2d(&tm_dq, stage + 16384, xcol + 64 * hf + 32, qrow);
-            ptx::bulk_commit();
-            ptx::bulk_wait_read0();
-            ptx::mbar_arrive(stage_read);
-          }
-          ++ns;
         }
-        if (!ok) break;
-        if (issuer) ptx::mbar_arrive(stage_free);
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(staged);
+        if (issuer) {
+          if (!(ok = ptx::mbar_wait(staged, x & 1, ctl, status, kSiteBwdDQ, budget))) break;
+#pragma unroll
+          for (int bx = 0; bx < DC / 32; ++bx) ptx::tma_reduce_add_2d(&tm_dq, box_addr(bx), xcol + 32 * bx, qrow);
+          ptx::bulk_commit();
+          ptx::bulk_wait_read0();
+          ptx::mbar_arrive(q_empty + st);  // the producer may refill this stage
+        }
       }
       if (!ok) break;
       if (!(ok = ptx::mbar_wait(acc_full, kitem & 1, ctl, status, kSiteBwdEpi, budget))) break;
