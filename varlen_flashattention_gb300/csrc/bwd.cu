@@ -26,7 +26,9 @@
 //    reduction; contended in broadcast-Q) and write dK and dV at the end of
 //    each item. dQ is staged, in 128B-swizzled fp32 boxes, in the Q/dO stage
 //    buffers of its own query tile (free once the dQ MMA has completed: dK
-//    and dV were their last readers) and added by TMA reduce-add
+//    and dV were their last readers; with a single stage, head_dim 192, in
+//    the dS buffer instead, so the next tile's Q does not wait for it) and
+//    added by TMA reduce-add
 //    ("Optimizing Jagged Flash Attention with TLX", fifth paragraph: staging
 //    of the dQ reduce-add); the drain warps release the stage to the producer
 //    after TMA has read it. Per-thread vector atomics measured slower: their
@@ -78,8 +80,8 @@ struct BwdLayout {
   static constexpr int kOffRow = kOffDS + kTile * kTile * 2;          // kStages x (lse2[128], delta[128])
   static constexpr int kOffBars = kOffRow + kStages * 1024;
   // kv_full, kv_empty, q_full[S], q_empty[S], s_full, p_full, dp_full, ds_full, ds_free,
-  // dq_full, dq_free, acc_full, acc_free, drain, staged
-  static constexpr int kNumBars = 2 + 2 * kStages + 11;
+  // dq_full, dq_free, acc_full, acc_free, drain, staged, stage_read, stage_free
+  static constexpr int kNumBars = 2 + 2 * kStages + 13;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   static constexpr int kAlloc = kBytes + 256;
@@ -162,7 +164,11 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* acc_full = s_full + 7;
   uint64_t* acc_free = s_full + 8;
   uint64_t* drain = s_full + 9;
-  uint64_t* staged = s_full + 10;  // the drain threads have written the dQ staging of a tile
+  uint64_t* staged = s_full + 10;      // the drain threads have written (part of) the dQ staging
+  uint64_t* stage_read = s_full + 11;  // dS-buffer staging: TMA has read one half
+  uint64_t* stage_free = s_full + 12;  // dS-buffer staging: TMA has read the whole tile
+  // where dQ is staged: the tile's own Q/dO stage (two stages) or the dS buffer (one)
+  constexpr bool kStageInQ = kSt > 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   ptx::CtaCtl* ctl = reinterpret_cast<ptx::CtaCtl*>(smem + Lay::kOffMisc + 8);
 
@@ -184,6 +190,8 @@ __global__ void __launch_bounds__(320, 1)
     ptx::mbar_init(acc_free, 4);
     ptx::mbar_init(drain, 1);
     ptx::mbar_init(staged, 128);
+    ptx::mbar_init(stage_read, 1);
+    ptx::mbar_init(stage_free, 1);
     ctl->abort = 0;
     ptx::fence_barrier_init();
   }
@@ -320,6 +328,7 @@ __global__ void __launch_bounds__(320, 1)
                         ptx::sdesc_sw128(q_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdAcc,
                         (ii > 0 || kk > 0) ? 1u : 0u);
           }
+          if (!kStageInQ) ptx::mma_commit(q_empty + st);  // dK is the last reader of this Q/dO stage
           // dQ(tile) = dS K[:, slice] into the dP^T columns
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -327,7 +336,7 @@ __global__ void __launch_bounds__(320, 1)
                         ptx::sdesc_sw128(k_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdDQ,
                         kk > 0 ? 1u : 0u);
           }
-          ptx::mma_commit(dq_full);  // the drain stages dQ in this Q/dO stage and then releases it
+          ptx::mma_commit(dq_full);  // with two stages the drain stages dQ in this Q/dO stage, then releases it
           ptx::mma_commit(ds_free);
           ++pos;
         }
@@ -417,8 +426,10 @@ __global__ void __launch_bounds__(320, 1)
         // dS^T = P^T * (dP^T - delta[q])
         if (!(ok = ptx::mbar_wait(dp_full, x & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
         ptx::tc_fence_after();
-        if (x > 0) {  // the MMAs of the previous tile have read dS
+        if (x > 0) {  // the MMAs of the previous tile have read dS (and TMA the dQ staged there)
           if (!(ok = ptx::mbar_wait(ds_free, (x - 1) & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
+          if (!kStageInQ && !(ok = ptx::mbar_wait(stage_free, (x - 1) & 1, ctl, status, kSiteBwdSoftDP, budget)))
+            break;
         }
 #pragma unroll 1
         for (int h2 = 0; h2 < 2; ++h2) {
@@ -465,7 +476,7 @@ __global__ void __launch_bounds__(320, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t x = 0, kitem = 0;
+    uint32_t x = 0, kitem = 0, ns = 0;  // ns: rounds of dQ staged so far
     bool ok = true;
     for (int v = blockIdx.x; ok && v < n_work; v += gridDim.x) {
       const BwdItem I = bwd_item(p, v);
@@ -486,38 +497,72 @@ __global__ void __launch_bounds__(320, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(dq_free);
-        // Stage the DC columns as 32-column fp32 boxes (16 KB, 128B swizzle) in
-        // this tile's Q and then dO stage buffers, add them into the
-        // accumulator with TMA, and hand the stage back to the producer once
-        // TMA has read it. Rows past the sequence hold exact zeros (their dS is
-        // masked), so whole boxes are added.
-        const uint32_t st = x % kSt;
-        auto box_addr = [&](int bx) -> uint8_t* {
-          const int off = bx * 16384;
-          return off < Lay::kTileBytes ? smem + Lay::kOffQ + st * Lay::kTileBytes + off
-                                       : smem + Lay::kOffDO + st * Lay::kTileBytes + (off - Lay::kTileBytes);
-        };
         const int qrow = I.q_row0 + kTile * i;
         const int xcol = I.h * D + I.c * DC;
         const bool issuer = warp == 4 && lane == 0;
+        if (kStageInQ) {
+          // Stage the DC columns as 32-column fp32 boxes (16 KB, 128B swizzle) in
+          // this tile's Q and then dO stage buffers, add them into the
+          // accumulator with TMA, and hand the stage back to the producer once
+          // TMA has read it. Rows past the sequence hold exact zeros (their dS
+          // is masked), so whole boxes are added.
+          const uint32_t st = x % kSt;
+          auto box_addr = [&](int bx) -> uint8_t* {
+            const int off = bx * 16384;
+            return off < Lay::kTileBytes ? smem + Lay::kOffQ + st * Lay::kTileBytes + off
+                                         : smem + Lay::kOffDO + st * Lay::kTileBytes + (off - Lay::kTileBytes);
+          };
 #pragma unroll
-        for (int bx = 0; bx < DC / 32; ++bx) {
-          uint8_t* row = box_addr(bx) + r * 128;
+          for (int bx = 0; bx < DC / 32; ++bx) {
+            uint8_t* row = box_addr(bx) + r * 128;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int k = 32 * bx + 4 * e;
-            ptx::st_shared_v4(row + ((e ^ (r & 7)) << 4), dq[k], dq[k + 1], dq[k + 2], dq[k + 3]);
+            for (int e = 0; e < 8; ++e) {
+              const int k = 32 * bx + 4 * e;
+              ptx::st_shared_v4(row + ((e ^ (r & 7)) << 4), dq[k], dq[k + 1], dq[k + 2], dq[k + 3]);
+            }
           }
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(staged);
-        if (issuer) {
-          if (!(ok = ptx::mbar_wait(staged, x & 1, ctl, status, kSiteBwdDQ, budget))) break;
+          ptx::fence_proxy_async_smem();
+          ptx::mbar_arrive(staged);
+          if (issuer) {
+            if (!(ok = ptx::mbar_wait(staged, ns & 1, ctl, status, kSiteBwdDQ, budget))) break;
 #pragma unroll
-          for (int bx = 0; bx < DC / 32; ++bx) ptx::tma_reduce_add_2d(&tm_dq, box_addr(bx), xcol + 32 * bx, qrow);
-          ptx::bulk_commit();
-          ptx::bulk_wait_read0();
-          ptx::mbar_arrive(q_empty + st);  // the producer may refill this stage
+            for (int bx = 0; bx < DC / 32; ++bx) ptx::tma_reduce_add_2d(&tm_dq, box_addr(bx), xcol + 32 * bx, qrow);
+            ptx::bulk_commit();
+            ptx::bulk_wait_read0();
+            ptx::mbar_arrive(q_empty + st);  // the producer may refill this stage
+          }
+          ++ns;
+        } else {
+          // Single stage: stage 64 columns at a time in the dS buffer, which the
+          // dK and dQ MMAs of this tile have finished reading; the softmax waits
+          // for stage_free before writing the next dS there.
+          uint8_t* stage = smem + Lay::kOffDS;
+#pragma unroll
+          for (int hf = 0; hf < DC / 64; ++hf) {
+            if (hf > 0 && !(ok = ptx::mbar_wait(stage_read, (ns - 1) & 1, ctl, status, kSiteBwdDQ, budget))) break;
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+              uint8_t* row = stage + b * 16384 + r * 128;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int k = 64 * hf + 32 * b + 4 * e;
+                ptx::st_shared_v4(row + ((e ^ (r & 7)) << 4), dq[k], dq[k + 1], dq[k + 2], dq[k + 3]);
+              }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(staged);
+            if (issuer) {
+              if (!(ok = ptx::mbar_wait(staged, ns & 1, ctl, status, kSiteBwdDQ, budget))) break;
+              ptx::tma_reduce_add_2d(&tm_dq, stage, xcol + 64 * hf, qrow);
+              ptx::tma_reduce_add_2d(&tm_dq, stage + 16384, xcol + 64 * hf + 32, qrow);
+              ptx::bulk_commit();
+              ptx::bulk_wait_read0();
+              ptx::mbar_arrive(stage_read);
+            }
+            ++ns;
+          }
+          if (!ok) break;
+          if (issuer) ptx::mbar_arrive(stage_free);
         }
       }
       if (!ok) break;

@@ -120,17 +120,29 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
     int bucket = 0;
     for (int b0 = 0; b0 < p.batch; b0 += kQThreads) {
       const int b = b0 + tid;
-      int count = 0, L = 0, nt = 0;
+      // Tiles of sequence b with cost k, in ascending order: t_first and count,
+      // in closed form for the modes whose tiles of one cost are contiguous
+      // (causal: exactly one tile; otherwise all tiles share one cost); the
+      // pair modes scan.
+      int count = 0, L = 0, nt = 0, t_first = 0;
+      const bool scan = pair_mode(p.mode);
       if (b < p.batch) {
         L = p.offsets[b + 1] - p.offsets[b];
         nt = item_tiles(p, L);
-        for (int t = 0; t < nt; ++t) count += (item_cost(p, L, t) == k) ? 1 : 0;
+        if (scan) {
+          for (int t = 0; t < nt; ++t) count += (item_cost(p, L, t) == k) ? 1 : 0;
+        } else if (p.causal && (p.mode == kQueueSelfFwd || p.mode == kQueueSelfBwd)) {
+          count = (k <= nt) ? 1 : 0;
+          t_first = (p.mode == kQueueSelfFwd) ? k - 1 : nt - k;
+        } else {
+          count = (nt > 0 && item_cost(p, L, 0) == k) ? nt : 0;
+        }
       }
       int tot;
       const int pre = block_exclusive_scan(count, warp_buf, &tot);
       int r = 0;
-      for (int t = 0; t < nt && r < count; ++t) {
-        if (item_cost(p, L, t) != k) continue;
+      for (int t = scan ? 0 : t_first; t < nt && r < count; ++t) {
+        if (scan && item_cost(p, L, t) != k) continue;
         const int slot = base + (bucket + pre + r) * p.heads;
         for (int h = 0; h < p.heads; ++h) {
           if (slot + h < p.max_items) p.items[slot + h] = make_int4(b, h, t, k);
