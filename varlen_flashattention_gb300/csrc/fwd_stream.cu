@@ -65,7 +65,7 @@ struct FwdStreamLayout {
   // pair, a whole K or V tile on a single CTA
   static constexpr int kHalfBytes = PAIR ? 16384 : 32768;
   static constexpr int kQSlots = 2;
-  static constexpr int kSlots = PAIR ? 9 : 4;
+  static constexpr int kSlots = PAIR ? 9 : 5;
   static constexpr int kOffQ = 0;
   static constexpr int kOffSlots = kQSlots * kQBytes;
   static constexpr int kOffMl = kOffSlots + kSlots * kHalfBytes;  // float2 (m, l) per row, two buffers
@@ -75,7 +75,10 @@ struct FwdStreamLayout {
   static constexpr int kNumBars = 3 * kQSlots + 3 * kSlots + 7 * 2 + 1;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
-  static constexpr int kAlloc = kBytes + 1024;
+  // Tiles need 1024-byte alignment; the dynamic shared-memory base is 1024-byte
+  // aligned on this part (a kernel that finds it otherwise reports
+  // JFA_ERR_UNSUPPORTED), so no slack is reserved on a single CTA.
+  static constexpr int kAlloc = kBytes + (PAIR ? 1024 : 0);
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384, kTmemCols = 512;
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
@@ -171,6 +174,10 @@ __global__ void __launch_bounds__(320, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (smem + Lay::kBytes > smem_raw + Lay::kAlloc) {  // base not aligned enough for the layout
+    if (threadIdx.x == 0) atomicCAS(p.status, JFA_OK, JFA_ERR_UNSUPPORTED);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
   uint64_t* q_full = bars;
   uint64_t* q_peer = q_full + kQS;
