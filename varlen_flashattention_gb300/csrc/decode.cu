@@ -11,12 +11,16 @@
 //
 // Design (GB300): the path is bound by HBM reads of K and V (about 0.5 flop
 // per byte), so the kernel is organised around memory-level parallelism:
-// every lane issues 16-byte non-caching loads of whole 256-byte cache rows
-// straight into registers, one 16-token block at a time, while the GQA group
-// of query heads rides along as the rows of an m16n8k16 register MMA. The
-// MMA is used to cut issue slots (no shuffle reductions), not for its FLOPs;
-// tcgen05's 64/128-row tiles would waste more of the tensor core on 1..16
-// real rows than this does.
+// every lane copies its 16-byte pieces of whole 256-byte cache rows with
+// cp.async into a private slot of a per-warp ring of kDecStages 16-token
+// blocks, so each warp keeps kDecStages - 1 blocks in flight while it
+// computes one; the GQA group of query heads rides along as the rows of an
+// m16n8k16 register MMA. The MMA is used to cut issue slots (no shuffle
+// reductions), not for its FLOPs; tcgen05's 64/128-row tiles would waste more
+// of the tensor core on 1..16 real rows than this does. A lane only reads
+// back the pieces it copied, so the ring needs no synchronisation beyond the
+// lane's own cp.async groups, and its layout (piece j of lane l at
+// [j][l]) makes every warp-wide copy and read 512 contiguous bytes.
 //
 // Index mappings used below (each lane: g = lane / 4, q = lane % 4):
 //  * QK^T: head dimension permuted so that each lane's four k-values of
@@ -51,6 +55,20 @@ struct DecodeParams {
 
 constexpr int kDecD = 128;
 constexpr int kDecWarps = 4;
+constexpr int kDecStages = 3;                                        // blocks per warp ring
+constexpr int kDecRingBytes = kDecStages * kDecWarps * 16 * 32 * 16;  // 16 pieces x 32 lanes x 16 B
+
+// 16-byte asynchronous global -> shared copy; bytes past src_bytes are zero.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ptx::smem_u32(smem_dst)), "l"(gsrc),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -69,9 +87,11 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecodeParams
   static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "GQA group");
   constexpr bool kTwoRowHalves = (G == 16);  // rows g+8 hold real heads only when G == 16
 
-  __shared__ float s_m[kDecWarps][G];
-  __shared__ float s_l[kDecWarps][G];
-  __shared__ __align__(16) float s_o[kDecWarps][G][kDecD];
+  // the block ring during the loop; afterwards the per-warp partials
+  extern __shared__ __align__(16) uint4 ring[];
+  float(*s_o)[G][kDecD] = reinterpret_cast<float(*)[G][kDecD]>(ring);
+  float(*s_m)[G] = reinterpret_cast<float(*)[G]>(reinterpret_cast<float*>(ring) + kDecWarps * G * kDecD);
+  float(*s_l)[G] = reinterpret_cast<float(*)[G]>(reinterpret_cast<float*>(ring) + kDecWarps * G * (kDecD + 1));
 
   const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -126,11 +146,16 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecodeParams
   const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
   const int nblk = (hi - lo + 15) >> 4;
 
-  for (int kb = warp; kb < nblk; kb += kDecWarps) {
-    const int t0 = lo + kb * 16;
-    // page of token t0 + (lane % 16), validated
-    int pg = 0;
-    {
+  // Copies of block kb (this warp's blocks: warp, warp + 4, ...) into ring slot `slot`:
+  // pieces 0..7 = K rows g and g+8 (B operand of QK^T), 8..15 = V rows 2q, 2q+1,
+  // 2q+8, 2q+9 (B operand of PV). Tokens past the split end are zero-filled
+  // from an in-bounds row.
+  uint4* my_ring = ring + static_cast<size_t>(warp) * kDecStages * 16 * 32;
+  auto issue = [&](int kb, int slot) {
+    uint4* dst = my_ring + slot * 16 * 32 + lane;
+    if (kb < nblk) {
+      const int t0 = lo + kb * 16;
+      int pg = 0;  // page of token t0 + (lane % 16), validated
       const int tok = t0 + (lane & 15);
       if (tok < hi) {
         pg = pt[tok / P];
@@ -139,33 +164,50 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecodeParams
           pg = 0;
         }
       }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int tk = gq + 8 * u;
+        const int page = __shfl_sync(0xffffffffu, pg, tk);
+        const int t = t0 + tk;
+        const __nv_bfloat16* row =
+            p.kc + (static_cast<int64_t>(page) * P + (t % P)) * row_stride + static_cast<int64_t>(kvh) * kDecD;
+#pragma unroll
+        for (int c2 = 0; c2 < 4; ++c2) cp_async16(dst + (4 * u + c2) * 32, row + 32 * c2 + 8 * qq, t < hi ? 16 : 0);
+      }
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int tv = 2 * qq + (w & 1) + 8 * (w >> 1);
+        const int page = __shfl_sync(0xffffffffu, pg, tv);
+        const int t = t0 + tv;
+        const __nv_bfloat16* row =
+            p.vc + (static_cast<int64_t>(page) * P + (t % P)) * row_stride + static_cast<int64_t>(kvh) * kDecD;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) cp_async16(dst + (8 + 2 * w + h2) * 32, row + 16 * gq + 8 * h2, t < hi ? 16 : 0);
+      }
     }
-    // K rows of tokens g and g+8 (B operand of QK^T)
+    cp_async_commit();  // one group per call, empty past the last block
+  };
+  const int nmine = nblk > warp ? (nblk - warp + kDecWarps - 1) / kDecWarps : 0;
+#pragma unroll
+  for (int i = 0; i < kDecStages - 1; ++i) issue(warp + kDecWarps * i, i);
+
+  for (int i = 0; i < nmine; ++i) {
+    const int kb = warp + kDecWarps * i;
+    const int t0 = lo + kb * 16;
+    // keep kDecStages - 1 blocks in flight: the slot refilled held block i - 1
+    issue(warp + kDecWarps * (i + kDecStages - 1), (i + kDecStages - 1) % kDecStages);
+    cp_async_wait<kDecStages - 1>();  // block i has landed
+    const uint4* src = my_ring + (i % kDecStages) * 16 * 32 + lane;
     uint4 kr[2][4];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int tk = gq + 8 * u;
-      const int page = __shfl_sync(0xffffffffu, pg, tk);
-      const int tok = t0 + tk;
-      const __nv_bfloat16* row =
-          p.kc + (static_cast<int64_t>(page) * P + (tok % P)) * row_stride + static_cast<int64_t>(kvh) * kDecD;
+    for (int u = 0; u < 2; ++u)
 #pragma unroll
-      for (int c2 = 0; c2 < 4; ++c2)
-        kr[u][c2] = (tok < hi) ? ptx::ld_nc_v4(row + 32 * c2 + 8 * qq) : make_uint4(0, 0, 0, 0);
-    }
-    // V rows of tokens 2q, 2q+1, 2q+8, 2q+9 (B operand of PV)
+      for (int c2 = 0; c2 < 4; ++c2) kr[u][c2] = src[(4 * u + c2) * 32];
     uint4 vr[4][2];
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const int tv = 2 * qq + (w & 1) + 8 * (w >> 1);
-      const int page = __shfl_sync(0xffffffffu, pg, tv);
-      const int tok = t0 + tv;
-      const __nv_bfloat16* row =
-          p.vc + (static_cast<int64_t>(page) * P + (tok % P)) * row_stride + static_cast<int64_t>(kvh) * kDecD;
+    for (int w = 0; w < 4; ++w)
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2)
-        vr[w][h2] = (tok < hi) ? ptx::ld_nc_v4(row + 16 * gq + 8 * h2) : make_uint4(0, 0, 0, 0);
-    }
+      for (int h2 = 0; h2 < 2; ++h2) vr[w][h2] = src[(8 + 2 * w + h2) * 32];
 
     // S = Q K^T for 16 tokens (two n-tiles of 8)
     float sc[2][4];
@@ -259,6 +301,8 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecodeParams
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
+  cp_async_wait<0>();
+  __syncthreads();  // every warp is done with the ring before it holds the partials
   // per-warp partials to shared memory (un-permuting the head dimension)
   if (gq < G) {
 #pragma unroll
@@ -375,14 +419,23 @@ cudaError_t launch_decode(const jfa_decode_args& a, float* part_o, float* part_l
   p.status = status;
   const int G = a.q_heads / a.kv_heads;
   dim3 grid(a.num_splits, a.kv_heads, a.batch);
+  static bool attr_set = false;
+  if (!attr_set) {
+    for (auto k : {decode_split_kernel<1>, decode_split_kernel<2>, decode_split_kernel<4>, decode_split_kernel<8>,
+                   decode_split_kernel<16>}) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecRingBytes);
+      if (e != cudaSuccess) return e;
+    }
+    attr_set = true;
+  }
   cudaEvent_t* ev = static_cast<cudaEvent_t*>(a.main_kernel_events);
   if (ev) cudaEventRecord(ev[0], stream);
   switch (G) {
-    case 1: decode_split_kernel<1><<<grid, 128, 0, stream>>>(p); break;
-    case 2: decode_split_kernel<2><<<grid, 128, 0, stream>>>(p); break;
-    case 4: decode_split_kernel<4><<<grid, 128, 0, stream>>>(p); break;
-    case 8: decode_split_kernel<8><<<grid, 128, 0, stream>>>(p); break;
-    case 16: decode_split_kernel<16><<<grid, 128, 0, stream>>>(p); break;
+    case 1: decode_split_kernel<1><<<grid, 128, kDecRingBytes, stream>>>(p); break;
+    case 2: decode_split_kernel<2><<<grid, 128, kDecRingBytes, stream>>>(p); break;
+    case 4: decode_split_kernel<4><<<grid, 128, kDecRingBytes, stream>>>(p); break;
+    case 8: decode_split_kernel<8><<<grid, 128, kDecRingBytes, stream>>>(p); break;
+    case 16: decode_split_kernel<16><<<grid, 128, kDecRingBytes, stream>>>(p); break;
     default: return cudaErrorInvalidValue;
   }
   if (ev) cudaEventRecord(ev[1], stream);
