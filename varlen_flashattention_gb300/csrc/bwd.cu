@@ -24,14 +24,14 @@
 //    dS for dQ);
 //  * warps 4-7 drain dQ from TMEM into an fp32 accumulator (the cross-CTA
 //    reduction; contended in broadcast-Q) and write dK and dV at the end of
-//    each item. dQ is staged, in 128B-swizzled fp32 boxes, in the Q/dO stage
-//    buffers of its own query tile (free once the dQ MMA has completed: dK
-//    and dV were their last readers; with a single stage, head_dim 192, in
-//    the dS buffer instead, so the next tile's Q does not wait for it) and
-//    added by TMA reduce-add
+//    each item. dQ is staged, in 128B-swizzled fp32 boxes, in the dO stage
+//    buffer of its own query tile (free once the dQ MMA has completed: dV was
+//    its last reader), a stage-sized part at a time (with a single stage,
+//    head_dim 192, in the dS buffer instead) and added by TMA reduce-add
 //    ("Optimizing Jagged Flash Attention with TLX", fifth paragraph: staging
 //    of the dQ reduce-add); the drain warps release the stage to the producer
-//    after TMA has read it. Per-thread vector atomics measured slower: their
+//    after TMA has read it; the Q half of the stage is released by the MMA
+//    warp right after dK, so the next query tile's Q never waits for dQ. Per-thread vector atomics measured slower: their
 //    strided requests held the SM's load/store path that the softmax warps
 //    use for TMEM and shared memory;
 //  * warp 8 = TMA producer, warp 9 = MMA issuer.
@@ -79,9 +79,9 @@ struct BwdLayout {
   static constexpr int kOffDS = kOffDO + kStages * kTileBytes;        // 128 x 128 bf16
   static constexpr int kOffRow = kOffDS + kTile * kTile * 2;          // kStages x (lse2[128], delta[128])
   static constexpr int kOffBars = kOffRow + kStages * 1024;
-  // kv_full, kv_empty, q_full[S], q_empty[S], s_full, p_full, dp_full, ds_full, ds_free,
-  // dq_full, dq_free, acc_full, acc_free, drain, staged, stage_read, stage_free
-  static constexpr int kNumBars = 2 + 2 * kStages + 13;
+  // kv_full, kv_empty, q_full[S], q_empty[S], do_full[S], do_empty[S], s_full, p_full, dp_full,
+  // ds_full, ds_free, dq_full, dq_free, acc_full, acc_free, drain, staged, stage_read, stage_free
+  static constexpr int kNumBars = 2 + 4 * kStages + 13;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   static constexpr int kAlloc = kBytes + 256;
@@ -152,9 +152,11 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
-  uint64_t* q_full = bars + 2;
+  uint64_t* q_full = bars + 2;            // Q and the LSE / delta rows of a query tile
   uint64_t* q_empty = bars + 2 + kSt;
-  uint64_t* s_full = bars + 2 + 2 * kSt;
+  uint64_t* do_full = bars + 2 + 2 * kSt;  // dO of a query tile
+  uint64_t* do_empty = bars + 2 + 3 * kSt;
+  uint64_t* s_full = bars + 2 + 4 * kSt;
   uint64_t* p_full = s_full + 1;
   uint64_t* dp_full = s_full + 2;
   uint64_t* ds_full = s_full + 3;
@@ -167,8 +169,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* staged = s_full + 10;      // the drain threads have written (part of) the dQ staging
   uint64_t* stage_read = s_full + 11;  // dS-buffer staging: TMA has read one half
   uint64_t* stage_free = s_full + 12;  // dS-buffer staging: TMA has read the whole tile
-  // where dQ is staged: the tile's own Q/dO stage (two stages) or the dS buffer (one)
-  constexpr bool kStageInQ = kSt > 1;
+  // where dQ is staged: the tile's own dO stage buffer (two stages) or the dS buffer (one)
+  constexpr bool kStageInDO = kSt > 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   ptx::CtaCtl* ctl = reinterpret_cast<ptx::CtaCtl*>(smem + Lay::kOffMisc + 8);
 
@@ -178,6 +180,8 @@ __global__ void __launch_bounds__(320, 1)
     for (int i = 0; i < kSt; ++i) {
       ptx::mbar_init(q_full + i, 1);
       ptx::mbar_init(q_empty + i, 1);
+      ptx::mbar_init(do_full + i, 1);
+      ptx::mbar_init(do_empty + i, 1);
     }
     ptx::mbar_init(s_full, 1);
     ptx::mbar_init(p_full, 4);
@@ -233,17 +237,20 @@ __global__ void __launch_bounds__(320, 1)
           const int i = I.i0 + ii;
           const uint32_t st = pos % kSt, round = pos / kSt;
           if (!(ok = ptx::mbar_wait(q_empty + st, (round & 1) ^ 1, ctl, status, kSiteBwdProdQ, budget))) break;
-          ptx::mbar_arrive_expect_tx(q_full + st, 2 * Lay::kTileBytes + 1024);
+          ptx::mbar_arrive_expect_tx(q_full + st, Lay::kTileBytes + 1024);
           uint8_t* qd = smem + Lay::kOffQ + st * Lay::kTileBytes;
-          uint8_t* dd = smem + Lay::kOffDO + st * Lay::kTileBytes;
 #pragma unroll
-          for (int a = 0; a < Lay::kAtoms; ++a) {
+          for (int a = 0; a < Lay::kAtoms; ++a)
             ptx::tma_load_2d(qd + a * 16384, &tm_q, q_full + st, I.h * D + 64 * a, I.q_row0 + kTile * i);
-            ptx::tma_load_2d(dd + a * 16384, &tm_do, q_full + st, I.h * D + 64 * a, I.do_row0 + kTile * i);
-          }
           uint8_t* rows = smem + Lay::kOffRow + st * 1024;
           ptx::bulk_load(rows, p.lse2p + I.row_base + static_cast<int64_t>(kTile) * i, 512, q_full + st);
           ptx::bulk_load(rows + 512, p.deltap + I.row_base + static_cast<int64_t>(kTile) * i, 512, q_full + st);
+          if (!(ok = ptx::mbar_wait(do_empty + st, (round & 1) ^ 1, ctl, status, kSiteBwdProdQ, budget))) break;
+          ptx::mbar_arrive_expect_tx(do_full + st, Lay::kTileBytes);
+          uint8_t* dd = smem + Lay::kOffDO + st * Lay::kTileBytes;
+#pragma unroll
+          for (int a = 0; a < Lay::kAtoms; ++a)
+            ptx::tma_load_2d(dd + a * 16384, &tm_do, do_full + st, I.h * D + 64 * a, I.do_row0 + kTile * i);
           ++pos;
         }
         ++kitem;
@@ -292,8 +299,9 @@ __global__ void __launch_bounds__(320, 1)
           // dP^T = V dO^T into the columns dQ of the previous tile used
           if (x > 0) {
             if (!(ok = ptx::mbar_wait(dq_free, (x - 1) & 1, ctl, status, kSiteBwdMmaDQFree, budget))) break;
-            ptx::tc_fence_after();
           }
+          if (!(ok = ptx::mbar_wait(do_full + st, (pos / kSt) & 1, ctl, status, kSiteBwdMmaQ, budget))) break;
+          ptx::tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -328,7 +336,8 @@ __global__ void __launch_bounds__(320, 1)
                         ptx::sdesc_sw128(q_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdAcc,
                         (ii > 0 || kk > 0) ? 1u : 0u);
           }
-          if (!kStageInQ) ptx::mma_commit(q_empty + st);  // dK is the last reader of this Q/dO stage
+          ptx::mma_commit(q_empty + st);  // dK is the last reader of Q (the softmax read the rows before dS^T)
+          if (!kStageInDO) ptx::mma_commit(do_empty + st);  // single stage: dO is free too (dV read it)
           // dQ(tile) = dS K[:, slice] into the dP^T columns
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -336,7 +345,7 @@ __global__ void __launch_bounds__(320, 1)
                         ptx::sdesc_sw128(k_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdDQ,
                         kk > 0 ? 1u : 0u);
           }
-          ptx::mma_commit(dq_full);  // with two stages the drain stages dQ in this Q/dO stage, then releases it
+          ptx::mma_commit(dq_full);  // with two stages the drain stages dQ in this dO stage, then releases it
           ptx::mma_commit(ds_free);
           ++pos;
         }
@@ -428,7 +437,7 @@ __global__ void __launch_bounds__(320, 1)
         ptx::tc_fence_after();
         if (x > 0) {  // the MMAs of the previous tile have read dS (and TMA the dQ staged there)
           if (!(ok = ptx::mbar_wait(ds_free, (x - 1) & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
-          if (!kStageInQ && !(ok = ptx::mbar_wait(stage_free, (x - 1) & 1, ctl, status, kSiteBwdSoftDP, budget)))
+          if (!kStageInDO && !(ok = ptx::mbar_wait(stage_free, (x - 1) & 1, ctl, status, kSiteBwdSoftDP, budget)))
             break;
         }
 #pragma unroll 1
@@ -500,70 +509,48 @@ __global__ void __launch_bounds__(320, 1)
         const int qrow = I.q_row0 + kTile * i;
         const int xcol = I.h * D + I.c * DC;
         const bool issuer = warp == 4 && lane == 0;
-        if (kStageInQ) {
-          // Stage the DC columns as 32-column fp32 boxes (16 KB, 128B swizzle) in
-          // this tile's Q and then dO stage buffers, add them into the
-          // accumulator with TMA, and hand the stage back to the producer once
-          // TMA has read it. Rows past the sequence hold exact zeros (their dS
-          // is masked), so whole boxes are added.
-          const uint32_t st = x % kSt;
-          auto box_addr = [&](int bx) -> uint8_t* {
-            const int off = bx * 16384;
-            return off < Lay::kTileBytes ? smem + Lay::kOffQ + st * Lay::kTileBytes + off
-                                         : smem + Lay::kOffDO + st * Lay::kTileBytes + (off - Lay::kTileBytes);
-          };
+        // Stage the DC columns as 32-column fp32 boxes (16 KB, 128B swizzle), a
+        // buffer-full at a time: in this tile's dO stage buffer with two stages
+        // (then released to the producer), in the dS buffer with one (then the
+        // softmax may write the next dS). TMA adds each part into the
+        // accumulator. Rows past the sequence hold exact zeros (their dS is
+        // masked), so whole boxes are added.
+        const uint32_t st = x % kSt;
+        uint8_t* stage = kStageInDO ? smem + Lay::kOffDO + st * Lay::kTileBytes : smem + Lay::kOffDS;
+        constexpr int kBoxesPerRound = kStageInDO ? Lay::kTileBytes / 16384 : 2;
+        constexpr int kRounds = (DC / 32) / kBoxesPerRound;
 #pragma unroll
-          for (int bx = 0; bx < DC / 32; ++bx) {
-            uint8_t* row = box_addr(bx) + r * 128;
+        for (int rd = 0; rd < kRounds; ++rd) {
+          // the reduce-adds of the previous part have read the staging
+          if (rd > 0 && !(ok = ptx::mbar_wait(stage_read, (ns - 1) & 1, ctl, status, kSiteBwdDQ, budget))) break;
+#pragma unroll
+          for (int b = 0; b < kBoxesPerRound; ++b) {
+            uint8_t* row = stage + b * 16384 + r * 128;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              const int k = 32 * bx + 4 * e;
+              const int k = 32 * (rd * kBoxesPerRound + b) + 4 * e;
               ptx::st_shared_v4(row + ((e ^ (r & 7)) << 4), dq[k], dq[k + 1], dq[k + 2], dq[k + 3]);
             }
           }
           ptx::fence_proxy_async_smem();
           ptx::mbar_arrive(staged);
+          // Every drain thread waits for the whole round: a thread that ran on to
+          // the next round (or tile) must not arrive again before this phase of
+          // `staged` has completed, or the phase would complete without the
+          // writes of a slower thread.
+          if (!(ok = ptx::mbar_wait(staged, ns & 1, ctl, status, kSiteBwdDQ, budget))) break;
           if (issuer) {
-            if (!(ok = ptx::mbar_wait(staged, ns & 1, ctl, status, kSiteBwdDQ, budget))) break;
 #pragma unroll
-            for (int bx = 0; bx < DC / 32; ++bx) ptx::tma_reduce_add_2d(&tm_dq, box_addr(bx), xcol + 32 * bx, qrow);
+            for (int b = 0; b < kBoxesPerRound; ++b)
+              ptx::tma_reduce_add_2d(&tm_dq, stage + b * 16384, xcol + 32 * (rd * kBoxesPerRound + b), qrow);
             ptx::bulk_commit();
             ptx::bulk_wait_read0();
-            ptx::mbar_arrive(q_empty + st);  // the producer may refill this stage
+            ptx::mbar_arrive(stage_read);
           }
           ++ns;
-        } else {
-          // Single stage: stage 64 columns at a time in the dS buffer, which the
-          // dK and dQ MMAs of this tile have finished reading; the softmax waits
-          // for stage_free before writing the next dS there.
-          uint8_t* stage = smem + Lay::kOffDS;
-#pragma unroll
-          for (int hf = 0; hf < DC / 64; ++hf) {
-            if (hf > 0 && !(ok = ptx::mbar_wait(stage_read, (ns - 1) & 1, ctl, status, kSiteBwdDQ, budget))) break;
-#pragma unroll
-            for (int b = 0; b < 2; ++b) {
-              uint8_t* row = stage + b * 16384 + r * 128;
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int k = 64 * hf + 32 * b + 4 * e;
-                ptx::st_shared_v4(row + ((e ^ (r & 7)) << 4), dq[k], dq[k + 1], dq[k + 2], dq[k + 3]);
-              }
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(staged);
-            if (issuer) {
-              if (!(ok = ptx::mbar_wait(staged, ns & 1, ctl, status, kSiteBwdDQ, budget))) break;
-              ptx::tma_reduce_add_2d(&tm_dq, stage, xcol + 64 * hf, qrow);
-              ptx::tma_reduce_add_2d(&tm_dq, stage + 16384, xcol + 64 * hf + 32, qrow);
-              ptx::bulk_commit();
-              ptx::bulk_wait_read0();
-              ptx::mbar_arrive(stage_read);
-            }
-            ++ns;
-          }
-          if (!ok) break;
-          if (issuer) ptx::mbar_arrive(stage_free);
         }
+        if (!ok) break;
+        if (issuer) ptx::mbar_arrive(kStageInDO ? do_empty + st : stage_free);
       }
       if (!ok) break;
       if (!(ok = ptx::mbar_wait(acc_full, kitem & 1, ctl, status, kSiteBwdEpi, budget))) break;
