@@ -20,8 +20,8 @@
 //    P^T can feed dV += P^T dO straight from TMEM;
 //  * warps 0-3 (one thread per key row) turn S^T into P^T (bf16, written over
 //    S^T in TMEM) and dP^T into dS^T (bf16, written to shared memory in the
-//    128B-swizzled layout the tensor core reads both as dS^T for dK and as
-//    dS for dQ);
+//    128B-swizzled layout the tensor core reads as dS for dQ, and packed
+//    into TMEM over the dP^T columns it has consumed as dS^T for dK);
 //  * warps 4-7 drain dQ from TMEM into an fp32 accumulator (the cross-CTA
 //    reduction; contended in broadcast-Q) and write dK and dV at the end of
 //    each item. dQ is staged, in 128B-swizzled fp32 boxes, in the dO stage
@@ -328,11 +328,10 @@ __global__ void __launch_bounds__(320, 1)
             if (!(ok = wait_q(pos + 1))) break;
             issue_s((pos + 1) % kSt);
           }
-          // dK += dS^T Q[:, slice]
+          // dK += dS^T Q[:, slice], dS^T from TMEM (packed over the dP^T columns)
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            ptx::mma_ss(tmem + Lay::kColDK, ptx::sdesc_sw128(ds_addr + off, 16, 1024),
+            ptx::mma_ts(tmem + Lay::kColDK, tmem + Lay::kColDP + kk * 8,
                         ptx::sdesc_sw128(q_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdAcc,
                         (ii > 0 || kk > 0) ? 1u : 0u);
           }
@@ -444,6 +443,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int h2 = 0; h2 < 2; ++h2) {
           uint32_t dp[2][32];
           uint32_t pp[32];
+          uint32_t dsw[32];
           ptx::tmem_ld32(tmem + lane_base + Lay::kColDP + 64 * h2, dp[0]);
           ptx::tmem_ld32(tmem + lane_base + Lay::kColDP + 64 * h2 + 32, dp[1]);
           ptx::tmem_ld32(tmem + lane_base + Lay::kColS + 32 * h2, pp);
@@ -471,8 +471,15 @@ __global__ void __launch_bounds__(320, 1)
             }
             uint4* dst = reinterpret_cast<uint4*>(ds_row + h2 * 16384 + ((ch ^ sw) << 4));
             *dst = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dsw[4 * ch + e] = w[e];
           }
+          // dS^T of these 64 query columns, two bf16 per column, over dP^T columns
+          // 32 h2 .. 32 h2 + 31, which this thread has already read: the A
+          // operand of dK = dS^T Q straight from TMEM
+          ptx::tmem_st32(tmem + lane_base + Lay::kColDP + 32 * h2, dsw);
         }
+        ptx::tmem_st_wait();
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncwarp();
