@@ -18,11 +18,15 @@
 //    of every query tile that sees this K/V tile;
 //  * scores are computed transposed, S^T = K Q^T, so TMEM lane = key row and
 //    P^T can feed dV += P^T dO straight from TMEM;
-//  * warps 0-3 (one thread per key row) turn S^T into P^T (bf16, written over
-//    S^T in TMEM) and dP^T into dS^T (bf16, written to shared memory in the
-//    128B-swizzled layout the tensor core reads as dS for dQ, and packed
-//    into TMEM over the dP^T columns it has consumed as dS^T for dK);
-//  * warps 4-7 drain dQ from TMEM into an fp32 accumulator (the cross-CTA
+//  * warps 0-7 (one thread per key row; warps w and w + 4 share the TMEM lanes
+//    of their rows, warps 0-3 take query columns 0-63 and warps 4-7 columns
+//    64-127: the exp loops are latency-bound, and two warps per SM
+//    sub-partition run them almost twice as fast while the tensor core is
+//    busy) turn S^T into P^T (bf16, packed over the S^T columns each group has
+//    read) and dP^T into dS^T (bf16, written to shared memory in the
+//    128B-swizzled layout the tensor core reads as dS for dQ, and packed into
+//    TMEM over the dP^T columns each group has read, as dS^T for dK);
+//  * warps 10-13 drain dQ from TMEM into an fp32 accumulator (the cross-CTA
 //    reduction; contended in broadcast-Q) and write dK and dV at the end of
 //    each item. dQ is staged, in 128B-swizzled fp32 boxes, in the dO stage
 //    buffer of its own query tile (free once the dQ MMA has completed: dV was
@@ -34,7 +38,8 @@
 //    warp right after dK, so the next query tile's Q never waits for dQ. Per-thread vector atomics measured slower: their
 //    strided requests held the SM's load/store path that the softmax warps
 //    use for TMEM and shared memory;
-//  * warp 8 = TMA producer, warp 9 = MMA issuer.
+//  * warp 8 = TMA producer, warp 9 = MMA issuer; 448 threads, so a thread has
+//    at most 128 registers.
 //  * Order inside one query tile: dP^T, dV, [S^T of the next tile], dK, dQ,
 //    so that the softmax of the next tile overlaps the dK / dQ MMAs. With a
 //    single Q/dO stage (head_dim 192) the next tile's Q arrives only after
@@ -131,7 +136,7 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
 }
 
 template <int D, int DC>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
@@ -167,8 +172,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* acc_free = s_full + 8;
   uint64_t* drain = s_full + 9;
   uint64_t* staged = s_full + 10;      // the drain threads have written (part of) the dQ staging
-  uint64_t* stage_read = s_full + 11;  // dS-buffer staging: TMA has read one half
-  uint64_t* stage_free = s_full + 12;  // dS-buffer staging: TMA has read the whole tile
+  uint64_t* stage_read = s_full + 11;  // TMA has read a staging round (before the next round is written)
+  uint64_t* stage_free = s_full + 12;  // dS-buffer staging (one stage): TMA has read the whole tile
   // where dQ is staged: the tile's own dO stage buffer (two stages) or the dS buffer (one)
   constexpr bool kStageInDO = kSt > 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
@@ -184,9 +189,9 @@ __global__ void __launch_bounds__(320, 1)
       ptx::mbar_init(do_empty + i, 1);
     }
     ptx::mbar_init(s_full, 1);
-    ptx::mbar_init(p_full, 4);
+    ptx::mbar_init(p_full, 8);
     ptx::mbar_init(dp_full, 1);
-    ptx::mbar_init(ds_full, 4);
+    ptx::mbar_init(ds_full, 8);
     ptx::mbar_init(ds_free, 1);
     ptx::mbar_init(dq_full, 1);
     ptx::mbar_init(dq_free, 4);
@@ -317,7 +322,7 @@ __global__ void __launch_bounds__(320, 1)
           ptx::tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
-            ptx::mma_ts(tmem + Lay::kColDV, tmem + Lay::kColS + kk * 8,
+            ptx::mma_ts(tmem + Lay::kColDV, tmem + Lay::kColS + 64 * (kk >> 2) + 8 * (kk & 3),
                         ptx::sdesc_sw128(do_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdAcc,
                         (ii > 0 || kk > 0) ? 1u : 0u);
           }
@@ -328,10 +333,11 @@ __global__ void __launch_bounds__(320, 1)
             if (!(ok = wait_q(pos + 1))) break;
             issue_s((pos + 1) % kSt);
           }
-          // dK += dS^T Q[:, slice], dS^T from TMEM (packed over the dP^T columns)
+          // dK += dS^T Q[:, slice], dS^T from TMEM (each group's 64 query columns
+          // packed over the first 32 of its dP^T columns)
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
-            ptx::mma_ts(tmem + Lay::kColDK, tmem + Lay::kColDP + kk * 8,
+            ptx::mma_ts(tmem + Lay::kColDK, tmem + Lay::kColDP + 64 * (kk >> 2) + 8 * (kk & 3),
                         ptx::sdesc_sw128(q_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdAcc,
                         (ii > 0 || kk > 0) ? 1u : 0u);
           }
@@ -357,14 +363,19 @@ __global__ void __launch_bounds__(320, 1)
       ptx::CtaCtl no_abort{0, 0};
       ptx::mbar_wait(drain, 0, &no_abort, nullptr, kSiteBwdDrain, budget);
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ P^T and dS^T (thread = key row)
-    const int r = warp * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // group g = warp / 4 takes query columns 64 g .. 64 g + 63
+    const int g = warp >> 2, quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t s_cols = tmem + lane_base + Lay::kColS + 64 * g;    // S^T, then packed P^T
+    const uint32_t dp_cols = tmem + lane_base + Lay::kColDP + 64 * g;  // dP^T, then packed dS^T
     const float sl = p.scale_log2;
+    const uint64_t sl2 = ptx::f2_packf(sl, sl);
     uint32_t pos = 0, x = 0;
     bool ok = true;
-    uint8_t* ds_row = smem + Lay::kOffDS + r * 128;
+    uint8_t* ds_row = smem + Lay::kOffDS + g * 16384 + r * 128;  // this group's atom of dS
     const int sw = r & 7;
     for (int v = blockIdx.x; ok && v < n_work; v += gridDim.x) {
       const BwdItem I = bwd_item(p, v);
@@ -373,7 +384,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int ii = 0; ii < I.nq; ++ii, ++x) {
         const int i = I.i0 + ii;
         const uint32_t st = pos % kSt;
-        const float* lse2 = reinterpret_cast<const float*>(smem + Lay::kOffRow + st * 1024);
+        const float* lse2 = reinterpret_cast<const float*>(smem + Lay::kOffRow + st * 1024) + 64 * g;
         const float* dlt = lse2 + 128;
         const int rq = I.Lq - kTile * i;  // valid query columns
         const bool masked = rk < kTile || rq < kTile || (p.causal && i == I.t);
@@ -382,23 +393,22 @@ __global__ void __launch_bounds__(320, 1)
         const int c_hi = r < rk ? rq : 0;
         if (!(ok = ptx::mbar_wait(s_full, x & 1, ctl, status, kSiteBwdSoftS, budget))) break;
         ptx::tc_fence_after();
-        // P^T = 2^(S^T * scale * log2e - lse2[q])
-#pragma unroll 1
-        for (int h2 = 0; h2 < 2; ++h2) {
+        // P^T = 2^(S^T * scale * log2e - lse2[q]), two chunks of 32 query columns
+        {
           uint32_t sv[2][32];
-          ptx::tmem_ld32(tmem + lane_base + Lay::kColS + 64 * h2, sv[0]);
-          ptx::tmem_ld32(tmem + lane_base + Lay::kColS + 64 * h2 + 32, sv[1]);
+          ptx::tmem_ld32(s_cols, sv[0]);
+          ptx::tmem_ld32(s_cols + 32, sv[1]);
           ptx::tmem_ld_wait();
           ptx::reg_fence32(sv[0]);
           ptx::reg_fence32(sv[1]);
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             uint32_t pk[16];
-            const int cb = 64 * h2 + 32 * u;
+            const int cb = 64 * g + 32 * u;  // first query column of the chunk
             float lq[32];  // -lse2 of the 32 query columns (same for every lane: broadcast reads)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) *reinterpret_cast<float4*>(lq + 4 * e) = reinterpret_cast<const float4*>(lse2 + cb)[e];
-            const uint64_t sl2 = ptx::f2_packf(sl, sl);
+            for (int e = 0; e < 8; ++e)
+              *reinterpret_cast<float4*>(lq + 4 * e) = reinterpret_cast<const float4*>(lse2 + 32 * u)[e];
             // branch-free; the masked form only on edge tiles (with the tensor
             // core reading shared memory, extra instructions here cost a lot)
             if (!masked) {
@@ -424,7 +434,7 @@ __global__ void __launch_bounds__(320, 1)
                 pk[e] = ptx::pack_bf16(p0, p1);
               }
             }
-            ptx::tmem_st16(tmem + lane_base + Lay::kColS + cb / 2, pk);
+            ptx::tmem_st16(s_cols + 16 * u, pk);  // over S^T columns this thread has read
           }
         }
         ptx::tmem_st_wait();
@@ -440,44 +450,41 @@ __global__ void __launch_bounds__(320, 1)
             break;
         }
 #pragma unroll 1
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t dp[2][32];
-          uint32_t pp[32];
-          uint32_t dsw[32];
-          ptx::tmem_ld32(tmem + lane_base + Lay::kColDP + 64 * h2, dp[0]);
-          ptx::tmem_ld32(tmem + lane_base + Lay::kColDP + 64 * h2 + 32, dp[1]);
-          ptx::tmem_ld32(tmem + lane_base + Lay::kColS + 32 * h2, pp);
+        for (int k = 0; k < 2; ++k) {  // two chunks of 32 query columns
+          uint32_t dp[32];
+          uint32_t pp[16];
+          uint32_t dsw[16];
+          ptx::tmem_ld32(dp_cols + 32 * k, dp);
+          ptx::tmem_ld16(s_cols + 16 * k, pp);
           ptx::tmem_ld_wait();
-          ptx::reg_fence32(dp[0]);
-          ptx::reg_fence32(dp[1]);
-          ptx::reg_fence32(pp);
-          // 64 query columns = one 128-byte swizzled row of atom h2
+          ptx::reg_fence32(dp);
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
+          for (int e = 0; e < 16; ++e) asm volatile("" : "+r"(pp[e]));
+          // 32 query columns = half of a 128-byte swizzled row of this group's atom
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int ch = 4 * k + c4;  // 16-byte chunk of the atom row
             uint32_t w[4];
             float dq8[8];  // -delta of the 8 query columns (broadcast reads)
-            *reinterpret_cast<float4*>(dq8) = reinterpret_cast<const float4*>(dlt + 64 * h2 + 8 * ch)[0];
-            *reinterpret_cast<float4*>(dq8 + 4) = reinterpret_cast<const float4*>(dlt + 64 * h2 + 8 * ch)[1];
+            *reinterpret_cast<float4*>(dq8) = reinterpret_cast<const float4*>(dlt + 8 * ch)[0];
+            *reinterpret_cast<float4*>(dq8 + 4) = reinterpret_cast<const float4*>(dlt + 8 * ch)[1];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int cl = 8 * ch + 2 * e;  // column within the 64-wide half (even)
+              const int cl = 8 * c4 + 2 * e;  // column within the 32-wide chunk (even)
               const uint32_t pw = pp[cl / 2];
               // (dP - delta) and P (bf16 pair widened) multiplied on fp32 pairs
-              const uint64_t d2 = ptx::f2_add(ptx::f2_pack(dp[cl >> 5][cl & 31], dp[cl >> 5][(cl & 31) + 1]),
-                                              ptx::f2_packf(dq8[2 * e], dq8[2 * e + 1]));
+              const uint64_t d2 = ptx::f2_add(ptx::f2_pack(dp[cl], dp[cl + 1]), ptx::f2_packf(dq8[2 * e], dq8[2 * e + 1]));
               float s0, s1;
               ptx::f2_unpack(ptx::f2_mul(ptx::f2_packf(ptx::bf16lo(pw), ptx::bf16hi(pw)), d2), s0, s1);
               w[e] = ptx::pack_bf16(s0, s1);
+              dsw[4 * c4 + e] = w[e];
             }
-            uint4* dst = reinterpret_cast<uint4*>(ds_row + h2 * 16384 + ((ch ^ sw) << 4));
+            uint4* dst = reinterpret_cast<uint4*>(ds_row + ((ch ^ sw) << 4));
             *dst = make_uint4(w[0], w[1], w[2], w[3]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) dsw[4 * ch + e] = w[e];
           }
-          // dS^T of these 64 query columns, two bf16 per column, over dP^T columns
-          // 32 h2 .. 32 h2 + 31, which this thread has already read: the A
-          // operand of dK = dS^T Q straight from TMEM
-          ptx::tmem_st32(tmem + lane_base + Lay::kColDP + 32 * h2, dsw);
+          // dS^T of these 32 query columns, two bf16 per column, over dP^T
+          // columns this thread has read: the A operand of dK = dS^T Q
+          ptx::tmem_st16(dp_cols + 16 * k, dsw);
         }
         ptx::tmem_st_wait();
         ptx::fence_proxy_async_smem();
@@ -487,12 +494,12 @@ __global__ void __launch_bounds__(320, 1)
         ++pos;
       }
     }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ dQ drain + dK/dV epilogue
+  } else if (warp >= 10) {
+    // ------------------------------------------------------------ dQ drain + dK/dV epilogue (warps 10-13)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t x = 0, kitem = 0, ns = 0;  // ns: rounds of dQ staged so far
+    uint32_t x = 0, kitem = 0, ns = 0, nr = 0;  // rounds of dQ staged; waits on stage_read
     bool ok = true;
     for (int v = blockIdx.x; ok && v < n_work; v += gridDim.x) {
       const BwdItem I = bwd_item(p, v);
@@ -501,61 +508,83 @@ __global__ void __launch_bounds__(320, 1)
         const int i = I.i0 + ii;
         if (!(ok = ptx::mbar_wait(dq_full, x & 1, ctl, status, kSiteBwdDQ, budget))) break;
         ptx::tc_fence_after();
-        // The whole dQ row comes out of TMEM first and the columns are released at
-        // once (the next dP^T goes there).
-        uint32_t dq[DC];
-#pragma unroll
-        for (int c = 0; c < DC / 32; ++c)
-          ptx::tmem_ld32(tmem + lane_base + Lay::kColDP + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(dq + 32 * c));
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < DC / 32; ++c) ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(dq + 32 * c));
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(dq_free);
+        // dQ leaves TMEM a staging round (a buffer-full of 32-column fp32 boxes,
+        // 16 KB each, 128B swizzle) at a time: in this tile's dO stage buffer
+        // with two stages (then released to the producer), in the dS buffer
+        // with one (then the softmax may write the next dS). The dQ columns are
+        // released as soon as the last round is in registers (the next dP^T
+        // goes there); TMA adds each round into the accumulator. Rows past the
+        // sequence hold exact zeros (their dS is masked), so whole boxes are added.
         const int qrow = I.q_row0 + kTile * i;
         const int xcol = I.h * D + I.c * DC;
-        const bool issuer = warp == 4 && lane == 0;
-        // Stage the DC columns as 32-column fp32 boxes (16 KB, 128B swizzle), a
-        // buffer-full at a time: in this tile's dO stage buffer with two stages
-        // (then released to the producer), in the dS buffer with one (then the
-        // softmax may write the next dS). TMA adds each part into the
-        // accumulator. Rows past the sequence hold exact zeros (their dS is
-        // masked), so whole boxes are added.
+        const bool issuer = warp == 10 && lane == 0;
         const uint32_t st = x % kSt;
         uint8_t* stage = kStageInDO ? smem + Lay::kOffDO + st * Lay::kTileBytes : smem + Lay::kOffDS;
         constexpr int kBoxesPerRound = kStageInDO ? Lay::kTileBytes / 16384 : 2;
         constexpr int kRounds = (DC / 32) / kBoxesPerRound;
+        constexpr int kRoundCols = 32 * kBoxesPerRound;
+        static_assert(kRounds == 1 || kRounds == 2, "dQ staging rounds");
+        uint32_t dq[kRoundCols];
+        auto tmem_read = [&](int rd) {
 #pragma unroll
-        for (int rd = 0; rd < kRounds; ++rd) {
-          // the reduce-adds of the previous part have read the staging
-          if (rd > 0 && !(ok = ptx::mbar_wait(stage_read, (ns - 1) & 1, ctl, status, kSiteBwdDQ, budget))) break;
+          for (int c = 0; c < kRoundCols / 32; ++c)
+            ptx::tmem_ld32(tmem + lane_base + Lay::kColDP + kRoundCols * rd + 32 * c,
+                           *reinterpret_cast<uint32_t(*)[32]>(dq + 32 * c));
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < kRoundCols / 32; ++c) ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(dq + 32 * c));
+        };
+        auto release_dq = [&]() {  // all of dQ is out of TMEM: the next dP^T may go there
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(dq_free);
+        };
+        auto write_round = [&]() {
 #pragma unroll
           for (int b = 0; b < kBoxesPerRound; ++b) {
             uint8_t* row = stage + b * 16384 + r * 128;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              const int k = 32 * (rd * kBoxesPerRound + b) + 4 * e;
+              const int k = 32 * b + 4 * e;
               ptx::st_shared_v4(row + ((e ^ (r & 7)) << 4), dq[k], dq[k + 1], dq[k + 2], dq[k + 3]);
             }
           }
           ptx::fence_proxy_async_smem();
           ptx::mbar_arrive(staged);
-          // Every drain thread waits for the whole round: a thread that ran on to
-          // the next round (or tile) must not arrive again before this phase of
-          // `staged` has completed, or the phase would complete without the
-          // writes of a slower thread.
-          if (!(ok = ptx::mbar_wait(staged, ns & 1, ctl, status, kSiteBwdDQ, budget))) break;
+        };
+        // Every drain thread waits for a whole round before the next: a thread
+        // that ran on must not arrive on `staged` again before this phase has
+        // completed, or the phase would complete without the writes of a slower
+        // thread. The issuer then hands the round to TMA.
+        auto finish_round = [&](int rd) -> bool {
+          if (!ptx::mbar_wait(staged, ns & 1, ctl, status, kSiteBwdDQ, budget)) return false;
           if (issuer) {
 #pragma unroll
             for (int b = 0; b < kBoxesPerRound; ++b)
-              ptx::tma_reduce_add_2d(&tm_dq, stage + b * 16384, xcol + 32 * (rd * kBoxesPerRound + b), qrow);
+              ptx::tma_reduce_add_2d(&tm_dq, stage + b * 16384, xcol + kRoundCols * rd + 32 * b, qrow);
             ptx::bulk_commit();
+          }
+          ++ns;
+          return true;
+        };
+        // round 0 goes to shared memory before round 1 leaves TMEM, so the dQ
+        // columns are released without waiting for any TMA read
+        tmem_read(0);
+        write_round();
+        if (kRounds == 2) tmem_read(1);
+        release_dq();
+        if (!(ok = finish_round(0))) break;
+        if (kRounds == 2) {
+          if (issuer) {  // the reduce-adds of round 0 have read the staging
             ptx::bulk_wait_read0();
             ptx::mbar_arrive(stage_read);
           }
-          ++ns;
+          if (!(ok = ptx::mbar_wait(stage_read, nr & 1, ctl, status, kSiteBwdDQ, budget))) break;
+          ++nr;
+          write_round();
+          if (!(ok = finish_round(1))) break;
         }
+        if (issuer) ptx::bulk_wait_read0();
         if (!ok) break;
         if (issuer) ptx::mbar_arrive(kStageInDO ? do_empty + st : stage_free);
       }
@@ -592,7 +621,7 @@ __global__ void __launch_bounds__(320, 1)
       if (lane == 0) ptx::mbar_arrive(acc_free);
       ++kitem;
     }
-    if (warp == 4 && lane == 0) ptx::bulk_wait0();  // every reduce-add has completed
+    if (warp == 10 && lane == 0) ptx::bulk_wait0();  // every reduce-add has completed
   }
 
   ptx::tc_fence_before();
@@ -702,7 +731,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  bwd_kernel<D, DC><<<grid, 320, Lay::kAlloc, stream>>>(tq, tk, tv, tdo, tdq, p);
+  bwd_kernel<D, DC><<<grid, 448, Lay::kAlloc, stream>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
 
