@@ -299,22 +299,3 @@ def tile_queue(offsets, heads, causal, kind, tile=128):
                 items.append((-cost, b, t, h))
     items.sort()
     return [(b, h, t) for (_, b, t, h) in items]
-
-
-def tile_queue_pairs(offsets, heads, causal, tile=128):
-    """Forward work items when two CTAs share one item ("Optimizing Jagged
-    Flash Attention with TLX", fifth paragraph: the 2-CTA MMA taken from FA4).
-    An item (b, h, u) covers the query tiles 2u and 2u + 1 of sequence b; both
-    visit the same key/value tiles, so its cost is that of the later tile,
-    min(2u + 2, nt) when causal, nt otherwise. Same order as tile_queue:
-    descending cost, ties by ascending (b, u, h). Returns a list of (b, h, u)."""
-    items = []
-    for b, (s, e) in enumerate(seq_ranges(offsets)):
-        L = e - s
-        nt = -(-L // tile)
-        for u in range(-(-nt // 2)):
-            cost = min(2 * u + 2, nt) if causal else nt
-            for h in range(heads):
-                items.append((-cost, b, u, h))
-    items.sort()
-    return [(b, h, u) for (_, b, u, h) in items]

@@ -386,37 +386,4 @@ def pin_tile_queue(o):
             assert keys == sorted(keys), (causal, kind)
 
 
-def pin_tile_queue_pairs(o):
-    """Pair items (b, h, u) cover every (b, h, query tile) exactly once, as
-    tiles 2u and 2u + 1; each costs the number of key tiles that either of its
-    two query tiles sees (recounted by brute force over (query, key) pairs);
-    costs never increase and ties go by ascending (b, u, h)."""
-    off = np.array([0, 300, 300, 301, 700, 1000, 1512])
-    H, T = 2, 128
-    for causal in (False, True):
-        q = o.tile_queue_pairs(off, H, causal, T)
-        covered = []
-        for b, h, u in q:
-            L = int(off[b + 1] - off[b])
-            for t in (2 * u, 2 * u + 1):
-                if t * T < L:
-                    covered.append((b, h, t))
-        expect = [(b, h, t) for b in range(len(off) - 1) for h in range(H)
-                  for t in range(-(-int(off[b + 1] - off[b]) // T))]
-        assert sorted(covered) == sorted(expect) and len(covered) == len(set(covered))
-
-        def cost(item):
-            b, h, u = item
-            L = int(off[b + 1] - off[b])
-            rows = range(2 * u * T, min(2 * u * T + 2 * T, L))
-            n = 0
-            for kj in range(-(-L // T)):
-                cols = range(kj * T, min(kj * T + T, L))
-                if any((not causal) or c <= r_ for r_ in rows for c in cols):
-                    n += 1
-            return n
-        keys = [(-cost(it), it[0], it[2], it[1]) for it in q]
-        assert keys == sorted(keys), causal
-
-
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -128,23 +128,6 @@ def _queue_ascending(m):
     m.tile_queue = q
 
 
-def _pair_cost_lower_tile(m):
-    """The pair's cost taken from its first query tile instead of its second."""
-    seq_ranges = m.seq_ranges
-
-    def q(offsets, heads, causal, tile=128):
-        items = []
-        for b, (s, e) in enumerate(seq_ranges(offsets)):
-            nt = -(-(e - s) // tile)
-            for u in range(-(-nt // 2)):
-                cost = min(2 * u + 1, nt) if causal else nt
-                for h in range(heads):
-                    items.append((-cost, b, u, h))
-        items.sort()
-        return [(b, h, u) for (_, b, u, h) in items]
-    m.tile_queue_pairs = q
-
-
 MUTANTS = {
     "bwd_drop_delta": _bwd_variant("drop_delta"),
     "bwd_sign_dS": _bwd_variant("sign_dS"),
@@ -155,7 +138,6 @@ MUTANTS = {
     "fwd_causal_upper": _fwd_variant("causal_upper"),
     "lse_in_log2": _lse_log2,
     "merge_no_reweight": _merge_no_reweight,
-    "pair_cost_lower_tile": _pair_cost_lower_tile,
     "gqa_wrong_group": _gqa_wrong_group,
     "page_slot_off_by_one": _page_slot_off_by_one,
     "queue_ascending": _queue_ascending,

@@ -99,14 +99,9 @@ bool make_tmap_f32_acc(CUtensorMap* m, const void* base, uint64_t rows, uint64_t
 
 bool good_dim(int d) { return d == 64 || d == 128 || d == 192; }
 
-// Which forward kernel runs: head_dim 128 takes the flat-stream kernel on
-// single CTAs; 64 and 192 the per-tile kernel. (The CTA-pair form of the
-// stream kernel measured slower: every cross-SM signal in it took about a
-// microsecond to be observed.)
-enum class FwdPath { kTile, kStreamSingle, kStreamPair };
-FwdPath fwd_path(int head_dim, int /*sms*/) {
-  return head_dim == 128 ? FwdPath::kStreamSingle : FwdPath::kTile;
-}
+// Which forward kernel runs: head_dim 128 takes the flat-stream kernel, 64
+// and 192 the per-tile kernel.
+bool fwd_stream_path(int head_dim) { return head_dim == 128; }
 
 jfa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA; }
 
@@ -305,11 +300,7 @@ jfa_status jfa_fwd(const jfa_fwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   qp.total = a->total;
   qp.max_seqlen = a->max_seqlen;
   qp.causal = a->causal;
-  const FwdPath path = fwd_path(a->head_dim, sms);
-  const bool pair = path == FwdPath::kStreamPair;
-  CUtensorMap tk64;
-  if (pair && !make_tmap_bf16(&tk64, a->k, a->total, cols, kTile / 2)) return JFA_ERR_CUDA;
-  qp.mode = pair ? kQueueSelfFwdPair : kQueueSelfFwd;
+  qp.mode = kQueueSelfFwd;
   qp.q_len = 0;
   qp.status = status;
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
@@ -318,15 +309,12 @@ jfa_status jfa_fwd(const jfa_fwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
   cudaError_t e;
-  if (path != FwdPath::kTile) {
-    const int grid = pair ? 2 * static_cast<int>(std::min<int64_t>(sms / 2, std::max<int64_t>(L.max_items, 1)))
-                          : static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
-    record(a->main_kernel_events, 0, stream);
-    e = launch_fwd_stream(pair, a->causal != 0, tq, pair ? tk64 : tk, tv, a->offsets, qp.items, status, a->o, a->lse,
-                          a->heads, a->total, 0, 0, a->scale, wait_budget_ns(), grid, stream);
+  const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
+  record(a->main_kernel_events, 0, stream);
+  if (fwd_stream_path(a->head_dim)) {
+    e = launch_fwd_stream(a->causal != 0, tq, tk, tv, a->offsets, qp.items, status, a->o, a->lse, a->heads, a->total,
+                          0, 0, a->scale, wait_budget_ns(), grid, stream);
   } else {
-    const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
-    record(a->main_kernel_events, 0, stream);
     e = launch_fwd(a->head_dim, a->causal != 0, tq, tk, tv, a->offsets, qp.items, status, a->o, a->lse, a->heads,
                    a->total, 0, 0, a->scale, wait_budget_ns(), grid, stream);
   }
@@ -436,11 +424,7 @@ jfa_status jfa_fwd_broadcast_q(const jfa_bcast_fwd_args* a, void* ws, size_t ws_
   qp.total = a->total_k;
   qp.max_seqlen = a->max_seqlen_k;
   qp.causal = 0;
-  const FwdPath path = fwd_path(a->head_dim, sms);
-  const bool pair = path == FwdPath::kStreamPair;
-  CUtensorMap tk64;
-  if (pair && !make_tmap_bf16(&tk64, a->k, a->total_k, cols, kTile / 2)) return JFA_ERR_CUDA;
-  qp.mode = pair ? kQueueBcastFwdPair : kQueueBcastFwd;
+  qp.mode = kQueueBcastFwd;
   qp.q_len = a->q_len;
   qp.status = status;
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
@@ -449,15 +433,12 @@ jfa_status jfa_fwd_broadcast_q(const jfa_bcast_fwd_args* a, void* ws, size_t ws_
   qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
   cudaError_t e;
-  if (path != FwdPath::kTile) {
-    const int grid = pair ? 2 * static_cast<int>(std::min<int64_t>(sms / 2, std::max<int64_t>(L.max_items, 1)))
-                          : static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
-    record(a->main_kernel_events, 0, stream);
-    e = launch_fwd_stream(pair, false, tq, pair ? tk64 : tk, tv, a->kv_offsets, qp.items, status, a->o, a->lse,
-                          a->heads, a->total_k, 1, a->q_len, a->scale, wait_budget_ns(), grid, stream);
+  const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
+  record(a->main_kernel_events, 0, stream);
+  if (fwd_stream_path(a->head_dim)) {
+    e = launch_fwd_stream(false, tq, tk, tv, a->kv_offsets, qp.items, status, a->o, a->lse, a->heads, a->total_k, 1,
+                          a->q_len, a->scale, wait_budget_ns(), grid, stream);
   } else {
-    const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
-    record(a->main_kernel_events, 0, stream);
     e = launch_fwd(a->head_dim, false, tq, tk, tv, a->kv_offsets, qp.items, status, a->o, a->lse, a->heads,
                    a->total_k, 1, a->q_len, a->scale, wait_budget_ns(), grid, stream);
   }

@@ -56,8 +56,6 @@ enum QueueMode : int32_t {
   kQueueSelfBwd = 1,   // items (b, h, kv-tile); cost = q tiles visited
   kQueueBcastFwd = 2,  // items (b, h, q-tile of the shared Q); cost = kv tiles of b
   kQueueBcastBwd = 3,  // items (b, h, kv-tile of b); cost = q tiles of the shared Q
-  kQueueSelfFwdPair = 4,   // items (b, h, pair u of q-tiles 2u, 2u+1) for CTA pairs; cost = kv tiles
-  kQueueBcastFwdPair = 5,  // items (b, h, pair u of the shared Q's tiles); cost = kv tiles of b
 };
 
 struct QueueParams {
@@ -96,14 +94,12 @@ cudaError_t launch_fwd(int head_dim, bool causal, const CUtensorMap& tq, const C
                        const int32_t* offsets, const int4* items, int32_t* status, void* o, float* lse, int heads,
                        int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
                        cudaStream_t stream);
-// Flat-stream forward (head_dim 128). pair: CTA pairs, items from a pair queue
-// mode, even grid, tk reads K in 64-row boxes (each CTA of a pair loads half
-// of a key tile). Otherwise single CTAs, items from the plain queue mode, tk
-// reads 128-row boxes.
-cudaError_t launch_fwd_stream(bool pair, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                              const CUtensorMap& tv, const int32_t* offsets, const int4* items, int32_t* status,
-                              void* o, float* lse, int heads, int total, int bcast, int q_len, float scale,
-                              uint64_t budget_ns, int grid, cudaStream_t stream);
+// Flat-stream forward (head_dim 128); items from the plain forward queue modes,
+// K and V read in 128-row boxes.
+cudaError_t launch_fwd_stream(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const int32_t* offsets, const int4* items, int32_t* status, void* o, float* lse,
+                              int heads, int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
+                              cudaStream_t stream);
 // tdq: the fp32 dQ accumulator [rows, H*D] in 32-column x 128-row boxes, 128B swizzle.
 cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdq, cudaStream_t stream);

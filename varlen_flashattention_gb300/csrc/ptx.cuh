@@ -59,20 +59,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// The same wait with cluster-scope acquire: for barriers that threads or the
-// tensor core of the other CTA of a pair arrive on. A thread suspended in
-// try_wait is not woken promptly by an arrival from another SM (measured: it
-// sleeps for about a microsecond), so the suspension is capped by a short
-// time hint (nanoseconds).
-constexpr uint32_t kRemoteWaitHintNs = 64;
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+// Non-blocking test of the phase with parity `parity` (mbarrier.test_wait):
+// true if it has completed. Issued ahead of the point where the answer is
+// needed, its shared-memory latency overlaps other work.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "n"(kRemoteWaitHintNs)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -90,17 +87,6 @@ __device__ __forceinline__ bool elect_one() {
   return e != 0;
 }
 
-// Warpgroup register reallocation: every warp of the warpgroup executes it.
-// The shares of all warpgroups must add up to the block's launch allocation.
-template <int N>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // Shared control block of a CTA: an abort flag every role polls, so that one
 // role that gives up makes the others leave their loops too.
 struct CtaCtl {
@@ -112,7 +98,6 @@ struct CtaCtl {
 // Returns true when the phase completed. Returns false (after recording
 // JFA_ERR_TIMEOUT and `where` in the device status word and raising the CTA
 // abort flag) when the time budget runs out or another role has aborted.
-template <bool kCluster>
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, CtaCtl* ctl, int32_t* status,
                                                    int where, uint64_t budget_ns);
 
@@ -120,24 +105,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, CtaCtl
                                           uint64_t budget_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
-  return mbar_wait_slow<false>(a, parity, ctl, status, where, budget_ns);
+  return mbar_wait_slow(a, parity, ctl, status, where, budget_ns);
 }
 
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, CtaCtl* ctl, int32_t* status,
-                                                  int where, uint64_t budget_ns) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait_cluster(a, parity)) return true;
-  return mbar_wait_slow<true>(a, parity, ctl, status, where, budget_ns);
-}
-
-template <bool kCluster>
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, CtaCtl* ctl, int32_t* status,
                                                    int where, uint64_t budget_ns) {
   const uint64_t t0 = globaltimer();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait(bar, parity)) return true;
     if (ctl->abort) return false;
     if (globaltimer() - t0 > budget_ns) {
       ctl->abort = 1;
@@ -300,77 +277,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// ---------------------------------------------------------------- CTA pairs (clusters of 2)
-//
-// A pair of CTAs on two SMs runs one tcgen05.mma with M = 256: rows 0..127 of
-// A and of the accumulator live in CTA 0, rows 128..255 in CTA 1; B is split
-// along N (CTA r supplies columns [N/2 r, N/2 (r+1))). CTA 0 issues the MMAs
-// and its commits arrive on the same barrier in both CTAs.
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Every thread of both CTAs must execute it (an unbounded hardware barrier:
-// reached only on paths that every thread takes).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Shared-memory address of the same variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t mapa(uint32_t smem_addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
-  return r;
-}
-
-// Arrive (release, cluster scope) on an mbarrier given by its cluster address.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc2(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish2() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-__device__ __forceinline__ void mma2_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on `bar` in every CTA of `mask` once all prior tcgen05 work of this thread completes.
-__device__ __forceinline__ void mma2_commit(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
 // TMA reduce-add of a shared-memory box into the global tensor of `map` at
 // (x, y) (the box and swizzle of the map). Part of the thread's bulk group.
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* smem_src, int32_t x, int32_t y) {
@@ -386,19 +292,9 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 // Waits until every committed bulk group of this thread has completed.
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// Named barrier `id` (1..15) over `n` threads (a multiple of 32).
-__device__ __forceinline__ void named_bar(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 __device__ __forceinline__ void st_shared_v4(void* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(dst)), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
-}
-
-// Vector reduction (add) of four floats into global memory, performed in L2.
-__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
 // ---------------------------------------------------------------- packed fp32 pairs

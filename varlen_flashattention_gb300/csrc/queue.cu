@@ -49,17 +49,10 @@ __device__ int block_exclusive_scan(int v, int* warp_buf, int* total) {
 
 __device__ __forceinline__ int ceil_tiles(int L) { return (L + kTile - 1) / kTile; }
 
-__device__ __forceinline__ bool pair_mode(int mode) { return mode == kQueueSelfFwdPair || mode == kQueueBcastFwdPair; }
-
-// Work items of sequence b (per head): query tiles (forward), query-tile pairs
-// (forward on CTA pairs) or key/value tiles (backward).
+// Work items of sequence b (per head): query tiles (forward) or key/value
+// tiles (backward).
 __device__ __forceinline__ int item_tiles(const QueueParams& p, int L) {
-  switch (p.mode) {
-    case kQueueBcastFwd: return ceil_tiles(p.q_len);
-    case kQueueBcastFwdPair: return (p.q_len + 2 * kTile - 1) / (2 * kTile);
-    case kQueueSelfFwdPair: return (L + 2 * kTile - 1) / (2 * kTile);
-    default: return ceil_tiles(L);
-  }
+  return p.mode == kQueueBcastFwd ? ceil_tiles(p.q_len) : ceil_tiles(L);
 }
 
 // Partner tiles an item visits: its cost in the longest-first order.
@@ -68,9 +61,7 @@ __device__ __forceinline__ int item_cost(const QueueParams& p, int L, int t) {
   switch (p.mode) {
     case kQueueSelfFwd: return p.causal ? t + 1 : nk;
     case kQueueSelfBwd: return p.causal ? nk - t : nk;
-    case kQueueSelfFwdPair: return p.causal ? min(2 * t + 2, nk) : nk;
-    case kQueueBcastFwd:
-    case kQueueBcastFwdPair: return nk;
+    case kQueueBcastFwd: return nk;
     default: return ceil_tiles(p.q_len);  // kQueueBcastBwd
   }
 }
@@ -113,7 +104,7 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
 
   // 2. bucket sort by descending cost; within a cost, ascending (b, tile, h)
   const int kmax = (p.mode == kQueueBcastBwd) ? ceil_tiles(p.q_len) : ceil_tiles(p.max_seqlen);
-  const bool keep_empty = (p.mode == kQueueBcastFwd || p.mode == kQueueBcastFwdPair);  // empty K/V still owns output rows
+  const bool keep_empty = p.mode == kQueueBcastFwd;  // empty K/V still owns output rows
   const int kmin = keep_empty ? 0 : 1;
   int base = 0;
   for (int k = kmax; k >= kmin; --k) {
@@ -121,17 +112,13 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
     for (int b0 = 0; b0 < p.batch; b0 += kQThreads) {
       const int b = b0 + tid;
       // Tiles of sequence b with cost k, in ascending order: t_first and count,
-      // in closed form for the modes whose tiles of one cost are contiguous
-      // (causal: exactly one tile; otherwise all tiles share one cost); the
-      // pair modes scan.
+      // in closed form (causal: exactly one tile; otherwise all tiles share one
+      // cost).
       int count = 0, L = 0, nt = 0, t_first = 0;
-      const bool scan = pair_mode(p.mode);
       if (b < p.batch) {
         L = p.offsets[b + 1] - p.offsets[b];
         nt = item_tiles(p, L);
-        if (scan) {
-          for (int t = 0; t < nt; ++t) count += (item_cost(p, L, t) == k) ? 1 : 0;
-        } else if (p.causal && (p.mode == kQueueSelfFwd || p.mode == kQueueSelfBwd)) {
+        if (p.causal && (p.mode == kQueueSelfFwd || p.mode == kQueueSelfBwd)) {
           count = (k <= nt) ? 1 : 0;
           t_first = (p.mode == kQueueSelfFwd) ? k - 1 : nt - k;
         } else {
@@ -141,8 +128,7 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
       int tot;
       const int pre = block_exclusive_scan(count, warp_buf, &tot);
       int r = 0;
-      for (int t = scan ? 0 : t_first; t < nt && r < count; ++t) {
-        if (scan && item_cost(p, L, t) != k) continue;
+      for (int t = t_first; t < nt && r < count; ++t) {
         const int slot = base + (bucket + pre + r) * p.heads;
         for (int h = 0; h < p.heads; ++h) {
           if (slot + h < p.max_items) p.items[slot + h] = make_int4(b, h, t, k);
