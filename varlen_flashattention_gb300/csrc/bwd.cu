@@ -263,50 +263,56 @@ __global__ void __launch_bounds__(448, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t pos = 0, x = 0, kitem = 0;
-      bool ok = true;
-      const uint32_t k_addr = ptx::smem_u32(smem + Lay::kOffK);
-      const uint32_t v_addr = ptx::smem_u32(smem + Lay::kOffV);
-      const uint32_t ds_addr = ptx::smem_u32(smem + Lay::kOffDS);
-      for (int v = blockIdx.x; ok && v < n_work; v += gridDim.x) {
-        const BwdItem I = bwd_item(p, v);
-        if (I.nq <= 0) continue;
-        if (!(ok = ptx::mbar_wait(kv_full, kitem & 1, ctl, status, kSiteBwdMmaKV, budget))) break;
-        ptx::tc_fence_after();
-        // S^T(x) = K Q^T. With two Q/dO stages it is issued for the first query
-        // tile of the item here and for every later one right after dS^T of the
-        // previous tile, so the softmax of tile x + 1 overlaps the dK / dQ MMAs
-        // of tile x; with one stage, at the start of its own tile.
-        auto issue_s = [&](uint32_t stage) {
-          const uint32_t qa = ptx::smem_u32(smem + Lay::kOffQ + stage * Lay::kTileBytes);
+    // The whole warp runs the loop (every value it computes is warp-uniform)
+    // and one elected lane issues each group of MMAs and commits: a converged
+    // warp issues at the tensor-core rate, a loop run by one lane does not.
+    // Barriers that are usually complete long before (dO, the next Q, the
+    // accumulators) are waited for ahead of the real dependency, so that their
+    // shared-memory latency overlaps that wait instead of following it.
+    uint32_t pos = 0, x = 0, kitem = 0;
+    bool ok = true;
+    const uint32_t k_addr = ptx::smem_u32(smem + Lay::kOffK);
+    const uint32_t v_addr = ptx::smem_u32(smem + Lay::kOffV);
+    const uint32_t ds_addr = ptx::smem_u32(smem + Lay::kOffDS);
+    auto wait = [&](uint64_t* bar, uint32_t parity, int site) -> bool {
+      return ptx::warp_all(ptx::mbar_wait(bar, parity, ctl, status, site, budget));
+    };
+    for (int v = blockIdx.x; ok && v < n_work; v += gridDim.x) {
+      const BwdItem I = bwd_item(p, v);
+      if (I.nq <= 0) continue;
+      if (!(ok = wait(kv_full, kitem & 1, kSiteBwdMmaKV))) break;
+      ptx::tc_fence_after();
+      // S^T(x) = K Q^T. With two Q/dO stages it is issued for the first query
+      // tile of the item at the start of the tile and for every later one right
+      // after dS^T of the previous tile, so the softmax of tile x + 1 overlaps
+      // the dK / dQ MMAs of tile x; with one stage, at the start of its own tile.
+      // Called by the elected lane.
+      auto issue_s = [&](uint32_t stage) {
+        const uint32_t qa = ptx::smem_u32(smem + Lay::kOffQ + stage * Lay::kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            ptx::mma_ss(tmem + Lay::kColS, ptx::sdesc_sw128(k_addr + off, 16, 1024),
-                        ptx::sdesc_sw128(qa + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
-          }
-          ptx::mma_commit(s_full);
-        };
-        auto wait_q = [&](uint32_t ps) -> bool {
-          if (!ptx::mbar_wait(q_full + ps % kSt, (ps / kSt) & 1, ctl, status, kSiteBwdMmaQ, budget)) return false;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          ptx::mma_ss(tmem + Lay::kColS, ptx::sdesc_sw128(k_addr + off, 16, 1024),
+                      ptx::sdesc_sw128(qa + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(s_full);
+      };
+      auto wait_q = [&](uint32_t ps) -> bool { return wait(q_full + ps % kSt, (ps / kSt) & 1, kSiteBwdMmaQ); };
+      for (int ii = 0; ii < I.nq; ++ii, ++x) {
+        const uint32_t st = pos % kSt;
+        if (ii == 0 || kSt == 1) {
+          if (!(ok = wait_q(pos))) break;
           ptx::tc_fence_after();
-          return true;
-        };
-        for (int ii = 0; ii < I.nq; ++ii, ++x) {
-          const uint32_t st = pos % kSt;
-          if (ii == 0 || kSt == 1) {
-            if (!(ok = wait_q(pos))) break;
-            issue_s(st);
-          }
-          const uint32_t q_addr = ptx::smem_u32(smem + Lay::kOffQ + st * Lay::kTileBytes);
-          const uint32_t do_addr = ptx::smem_u32(smem + Lay::kOffDO + st * Lay::kTileBytes);
-          // dP^T = V dO^T into the columns dQ of the previous tile used
-          if (x > 0) {
-            if (!(ok = ptx::mbar_wait(dq_free, (x - 1) & 1, ctl, status, kSiteBwdMmaDQFree, budget))) break;
-          }
-          if (!(ok = ptx::mbar_wait(do_full + st, (pos / kSt) & 1, ctl, status, kSiteBwdMmaQ, budget))) break;
-          ptx::tc_fence_after();
+          if (ptx::elect_one()) issue_s(st);
+          __syncwarp();
+        }
+        const uint32_t q_addr = ptx::smem_u32(smem + Lay::kOffQ + st * Lay::kTileBytes);
+        const uint32_t do_addr = ptx::smem_u32(smem + Lay::kOffDO + st * Lay::kTileBytes);
+        // dP^T = V dO^T into the columns dQ of the previous tile used
+        if (!(ok = wait(do_full + st, (pos / kSt) & 1, kSiteBwdMmaQ))) break;
+        if (x > 0 && !(ok = wait(dq_free, (x - 1) & 1, kSiteBwdMmaDQFree))) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -314,25 +320,28 @@ __global__ void __launch_bounds__(448, 1)
                         ptx::sdesc_sw128(do_addr + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
           }
           ptx::mma_commit(dp_full);
-          // dV += P^T dO[:, slice]
-          if (!(ok = ptx::mbar_wait(p_full, x & 1, ctl, status, kSiteBwdMmaP, budget))) break;
-          if (ii == 0 && kitem > 0) {
-            if (!(ok = ptx::mbar_wait(acc_free, (kitem - 1) & 1, ctl, status, kSiteBwdMmaAccFree, budget))) break;
-          }
-          ptx::tc_fence_after();
+        }
+        __syncwarp();
+        // dV += P^T dO[:, slice]
+        if (ii == 0 && kitem > 0 && !(ok = wait(acc_free, (kitem - 1) & 1, kSiteBwdMmaAccFree))) break;
+        if (!(ok = wait(p_full, x & 1, kSiteBwdMmaP))) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             ptx::mma_ts(tmem + Lay::kColDV, tmem + Lay::kColS + 64 * (kk >> 2) + 8 * (kk & 3),
                         ptx::sdesc_sw128(do_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdAcc,
                         (ii > 0 || kk > 0) ? 1u : 0u);
           }
-          if (!(ok = ptx::mbar_wait(ds_full, x & 1, ctl, status, kSiteBwdMmaDS, budget))) break;
-          ptx::tc_fence_after();
+        }
+        __syncwarp();
+        const bool next_s = kSt > 1 && ii + 1 < I.nq;
+        if (next_s && !(ok = wait_q(pos + 1))) break;
+        if (!(ok = wait(ds_full, x & 1, kSiteBwdMmaDS))) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) {
           // the S^T columns are free: dV has been issued and the softmax has read P^T back
-          if (kSt > 1 && ii + 1 < I.nq) {
-            if (!(ok = wait_q(pos + 1))) break;
-            issue_s((pos + 1) % kSt);
-          }
+          if (next_s) issue_s((pos + 1) % kSt);
           // dK += dS^T Q[:, slice], dS^T from TMEM (each group's 64 query columns
           // packed over the first 32 of its dP^T columns)
 #pragma unroll
@@ -352,17 +361,23 @@ __global__ void __launch_bounds__(448, 1)
           }
           ptx::mma_commit(dq_full);  // with two stages the drain stages dQ in this dO stage, then releases it
           ptx::mma_commit(ds_free);
-          ++pos;
         }
-        if (!ok) break;
+        __syncwarp();
+        ++pos;
+      }
+      if (!ok) break;
+      if (ptx::elect_one()) {
         ptx::mma_commit(kv_empty);
         ptx::mma_commit(acc_full);
-        ++kitem;
       }
-      ptx::mma_commit(drain);
-      ptx::CtaCtl no_abort{0, 0};
-      ptx::mbar_wait(drain, 0, &no_abort, nullptr, kSiteBwdDrain, budget);
+      __syncwarp();
+      ++kitem;
     }
+    if (ptx::elect_one()) ptx::mma_commit(drain);
+    __syncwarp();
+    ptx::CtaCtl no_abort{0, 0};
+    ptx::mbar_wait(drain, 0, &no_abort, nullptr, kSiteBwdDrain, budget);
+    __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------------------ P^T and dS^T (thread = key row)
     // group g = warp / 4 takes query columns 64 g .. 64 g + 63
@@ -437,15 +452,18 @@ __global__ void __launch_bounds__(448, 1)
             ptx::tmem_st16(s_cols + 16 * u, pk);  // over S^T columns this thread has read
           }
         }
+        // dP^T and the dS buffer, tested while the P^T stores drain
+        const bool dp_ready = ptx::mbar_test(dp_full, x & 1);
+        const bool ds_ready = x == 0 || ptx::mbar_test(ds_free, (x - 1) & 1);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(p_full);
         // dS^T = P^T * (dP^T - delta[q])
-        if (!(ok = ptx::mbar_wait(dp_full, x & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
+        if (!dp_ready && !(ok = ptx::mbar_wait(dp_full, x & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
         ptx::tc_fence_after();
         if (x > 0) {  // the MMAs of the previous tile have read dS (and TMA the dQ staged there)
-          if (!(ok = ptx::mbar_wait(ds_free, (x - 1) & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
+          if (!ds_ready && !(ok = ptx::mbar_wait(ds_free, (x - 1) & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
           if (!kStageInDO && !(ok = ptx::mbar_wait(stage_free, (x - 1) & 1, ctl, status, kSiteBwdSoftDP, budget)))
             break;
         }
