@@ -119,7 +119,8 @@ bool events_ok(void* events) {
 // ------------------------------------------------------------------ workspace layouts
 
 struct Layout {
-  size_t status = 0, tile_base = 0, items = 0, lse2p = 0, deltap = 0, dq_acc = 0, part_o = 0, part_lse = 0;
+  size_t status = 0, tile_base = 0, items = 0, item_seq = 0, lse2p = 0, deltap = 0, dq_acc = 0, part_o = 0,
+         part_lse = 0;
   size_t bytes = 0;
   int64_t max_items = 0, pad_tiles = 0;
 };
@@ -133,6 +134,8 @@ Layout self_layout(int64_t batch, int64_t heads, int64_t total, int64_t head_dim
   L.max_items = heads * L.pad_tiles;
   L.items = off;
   off = align_up(off + 16 * L.max_items, 256);
+  L.item_seq = off;
+  off = align_up(off + 8 * L.max_items, 256);
   if (bwd) {
     L.lse2p = off;
     off = align_up(off + 4 * heads * L.pad_tiles * kTile, 256);
@@ -154,6 +157,8 @@ Layout bcast_layout(int64_t batch, int64_t q_len, int64_t heads, int64_t total_k
   L.max_items = bwd ? heads * max_tiles(total_k, batch) : batch * heads * nqt;
   L.items = off;
   off = align_up(off + 16 * L.max_items, 256);
+  L.item_seq = off;
+  off = align_up(off + 8 * L.max_items, 256);
   if (bwd) {
     L.pad_tiles = batch * nqt;
     L.lse2p = off;
@@ -305,6 +310,7 @@ jfa_status jfa_fwd(const jfa_fwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   qp.status = status;
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
   qp.items = reinterpret_cast<int4*>(w + L.items);
+  qp.item_seq = reinterpret_cast<int2*>(w + L.item_seq);
   qp.max_items = static_cast<int32_t>(L.max_items);
   qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
@@ -312,7 +318,7 @@ jfa_status jfa_fwd(const jfa_fwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
   record(a->main_kernel_events, 0, stream);
   if (fwd_stream_path(a->head_dim)) {
-    e = launch_fwd_stream(a->causal != 0, tq, tk, tv, a->offsets, qp.items, status, a->o, a->lse, a->heads, a->total,
+    e = launch_fwd_stream(a->causal != 0, tq, tk, tv, qp.items, qp.item_seq, status, a->o, a->lse, a->heads, a->total,
                           0, 0, a->scale, wait_budget_ns(), grid, stream);
   } else {
     e = launch_fwd(a->head_dim, a->causal != 0, tq, tk, tv, a->offsets, qp.items, status, a->o, a->lse, a->heads,
@@ -355,6 +361,7 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   qp.status = status;
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
   qp.items = reinterpret_cast<int4*>(w + L.items);
+  qp.item_seq = reinterpret_cast<int2*>(w + L.item_seq);
   qp.max_items = static_cast<int32_t>(L.max_items);
   qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
@@ -429,6 +436,7 @@ jfa_status jfa_fwd_broadcast_q(const jfa_bcast_fwd_args* a, void* ws, size_t ws_
   qp.status = status;
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
   qp.items = reinterpret_cast<int4*>(w + L.items);
+  qp.item_seq = reinterpret_cast<int2*>(w + L.item_seq);
   qp.max_items = static_cast<int32_t>(L.max_items);
   qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
@@ -436,7 +444,7 @@ jfa_status jfa_fwd_broadcast_q(const jfa_bcast_fwd_args* a, void* ws, size_t ws_
   const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
   record(a->main_kernel_events, 0, stream);
   if (fwd_stream_path(a->head_dim)) {
-    e = launch_fwd_stream(false, tq, tk, tv, a->kv_offsets, qp.items, status, a->o, a->lse, a->heads, a->total_k, 1,
+    e = launch_fwd_stream(false, tq, tk, tv, qp.items, qp.item_seq, status, a->o, a->lse, a->heads, a->total_k, 1,
                           a->q_len, a->scale, wait_budget_ns(), grid, stream);
   } else {
     e = launch_fwd(a->head_dim, false, tq, tk, tv, a->kv_offsets, qp.items, status, a->o, a->lse, a->heads,
@@ -489,8 +497,9 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
     qp.status = status;
     qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
     qp.items = reinterpret_cast<int4*>(w + L.items);
+    qp.item_seq = reinterpret_cast<int2*>(w + L.item_seq);
     qp.max_items = static_cast<int32_t>(L.max_items);
-  qp.count_index = 2;
+    qp.count_index = 2;
     if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
     float* lse2p = reinterpret_cast<float*>(w + L.lse2p);
     float* deltap = reinterpret_cast<float*>(w + L.deltap);

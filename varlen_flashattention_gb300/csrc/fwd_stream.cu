@@ -44,8 +44,8 @@ constexpr int kD2 = 128;
 constexpr int kThreads = 448;
 
 struct FwdStreamParams {
-  const int32_t* offsets;
-  const int4* items;  // (b, h, query tile, cost)
+  const int4* items;     // (b, h, query tile, key tiles)
+  const int2* item_seq;  // (first row, length) of the item's key sequence
   int32_t* status;
   __nv_bfloat16* o;
   float* lse;
@@ -82,15 +82,17 @@ struct FwdStreamItem {
   int64_t o_row, lse0;
 };
 
-template <bool CAUSAL>
+// An item's record: two independent loads (the queue stores each item's
+// sequence start and length beside it), so nothing waits on a dependent load.
 __device__ __forceinline__ FwdStreamItem stream_item(const FwdStreamParams& p, int idx) {
   const int4 it = p.items[idx];
+  const int2 sq = p.item_seq[idx];
   FwdStreamItem I;
   I.b = it.x;
   I.h = it.y;
   I.t = it.z;
-  const int s0 = p.offsets[I.b], s1 = p.offsets[I.b + 1];
-  I.Lk = s1 - s0;
+  const int s0 = sq.x;
+  I.Lk = sq.y;
   I.kv_row0 = s0;
   if (!p.bcast) {
     I.Lq = I.Lk;
@@ -103,36 +105,31 @@ __device__ __forceinline__ FwdStreamItem stream_item(const FwdStreamParams& p, i
     I.o_row = static_cast<int64_t>(I.b) * p.q_len + kTile * I.t;
     I.lse0 = (static_cast<int64_t>(I.b) * p.heads + I.h) * p.q_len + kTile * I.t;
   }
-  const int nk = (I.Lk + kTile - 1) / kTile;
-  I.n_kv = CAUSAL ? min(I.t + 1, nk) : nk;
+  I.n_kv = it.w;  // the queue's cost of a forward item is its number of key tiles
   return I;
 }
 
-// The next item of this CTA with at least one key/value tile, starting at
-// index idx. Returns its index (>= n_items when there is none).
-template <bool CAUSAL>
-__device__ __forceinline__ int next_busy(const FwdStreamParams& p, int idx, int stride, int n_items,
-                                         FwdStreamItem& I) {
-  for (; idx < n_items; idx += stride) {
-    I = stream_item<CAUSAL>(p, idx);
-    if (I.n_kv > 0) break;
-  }
+// Items with at least one key tile come first in the queue (descending cost),
+// so a CTA's busy items are its indices below n_busy. Returns idx and loads
+// its record when it is busy; the caller's first use of I is what waits.
+__device__ __forceinline__ int next_busy(const FwdStreamParams& p, int idx, int n_busy, FwdStreamItem& I) {
+  if (idx < n_busy) I = stream_item(p, idx);
   return idx;
 }
 
 // The order in which the loads are issued (and consumed): Q of an item, then
 // K of its first step; for every step j, K of step j + 1 (or the next item's
 // Q and first K) before V of step j. Each callback returns false to stop.
-template <bool CAUSAL, class FQ, class FK, class FV>
-__device__ __forceinline__ void walk_loads(const FwdStreamParams& p, int first, int stride, int n_items, FQ on_q,
+template <class FQ, class FK, class FV>
+__device__ __forceinline__ void walk_loads(const FwdStreamParams& p, int first, int stride, int n_busy, FQ on_q,
                                            FK on_k, FV on_v) {
   FwdStreamItem cur, nxt;
-  int idx = next_busy<CAUSAL>(p, first, stride, n_items, cur);
-  if (idx >= n_items) return;
+  int idx = next_busy(p, first, n_busy, cur);
+  if (idx >= n_busy) return;
   if (!on_q(cur) || !on_k(cur, 0)) return;
   while (true) {
-    const int nidx = next_busy<CAUSAL>(p, idx + stride, stride, n_items, nxt);
-    const bool more = nidx < n_items;
+    const int nidx = next_busy(p, idx + stride, n_busy, nxt);
+    const bool more = nidx < n_busy;
     for (int j = 0; j < cur.n_kv; ++j) {
       if (j + 1 < cur.n_kv) {
         if (!on_k(cur, j + 1)) return;
@@ -223,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int n_items = p.status[2];
+  const int n_busy = p.status[3];  // items with at least one key tile: indices 0 .. n_busy - 1
   int32_t* status = p.status;
   const uint64_t budget = p.budget_ns;
   const int cta = blockIdx.x, n_ctas = gridDim.x;
@@ -261,8 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tma_load_2d(dst + a * 16384, map, slot_full + slot, I.h * kD2 + 64 * a, I.kv_row0 + kTile * j);
         return true;
       };
-      walk_loads<CAUSAL>(
-          p, cta, n_ctas, n_items, on_q, [&](const FwdStreamItem& I, int j) { return on_kv(&tm_k, I, j); },
+      walk_loads(
+          p, cta, n_ctas, n_busy, on_q, [&](const FwdStreamItem& I, int j) { return on_kv(&tm_k, I, j); },
           [&](const FwdStreamItem& I, int j) { return on_kv(&tm_v, I, j); });
       // After an abort some loads may have no consumer: wait (bounded) for the
       // last fill of every slot so that no copy is in flight when the CTA exits.
@@ -317,12 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     FwdStreamItem cur, nxt;
-    int idx = next_busy<CAUSAL>(p, cta, n_ctas, n_items, cur);
+    int idx = next_busy(p, cta, n_busy, cur);
     uint32_t kq = 0, x = 0;  // busy items so far, steps so far
-    if (idx < n_items) ok = q_wait(0) && issue_s(0, 0, cur.n_kv == 1);
-    while (ok && idx < n_items) {
-      const int nidx = next_busy<CAUSAL>(p, idx + n_ctas, n_ctas, n_items, nxt);
-      const bool more = nidx < n_items;
+    if (idx < n_busy) ok = q_wait(0) && issue_s(0, 0, cur.n_kv == 1);
+    while (ok && idx < n_busy) {
+      const int nidx = next_busy(p, idx + n_ctas, n_busy, nxt);
+      const bool more = nidx < n_busy;
       const int n = cur.n_kv;
       const uint32_t ob = kq & 1;
       for (int j = 0; ok && j < n; ++j, ++x) {
@@ -376,10 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl = p.scale_log2;
     uint32_t x = 0, kq = 0;
     bool ok = true, s_ready = false;  // s_ready: S of step x is known to be complete
-    for (int idx = cta; ok && idx < n_items; idx += n_ctas) {
-      const FwdStreamItem I = stream_item<CAUSAL>(p, idx);
+    FwdStreamItem nxt;  // the next item's record, loaded one item ahead
+    if (cta < n_busy) nxt = stream_item(p, cta);
+    for (int idx = cta; ok && idx < n_busy; idx += n_ctas) {
+      const FwdStreamItem I = nxt;
+      if (idx + n_ctas < n_busy) nxt = stream_item(p, idx + n_ctas);
       const int n = I.n_kv;
-      if (n == 0) continue;
       const uint32_t ob = kq & 1;
       const uint32_t o_tmem = tmem + lane_base + (ob ? Lay::kColO1 : Lay::kColO0) + c_own;
       const int qi = kTile * I.t + r;  // query position in its sequence
@@ -473,24 +473,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P = 2^(S sl - m): scale and shift on fp32 pairs, exp2 per element, sums on pairs
         const uint64_t sl2 = ptx::f2_packf(sl, sl), nmu2 = ptx::f2_packf(-mu, -mu);
         uint64_t ls2[2] = {ptx::f2_packf(0.f, 0.f), ptx::f2_packf(0.f, 0.f)};
-        uint32_t pk[2][16];
-        auto exps = [&](const uint32_t(&v)[32], uint32_t(&out)[16]) {
+        // each 32-key chunk of P is stored as soon as it is packed (over S
+        // columns c_own .., once the other group has read them)
+        bool rd_ok = rd_done;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             float x0, x1;
-            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(v[2 * e], v[2 * e + 1]), sl2, nmu2), x0, x1);
+            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sa[u][2 * e], sa[u][2 * e + 1]), sl2, nmu2), x0, x1);
             const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
             ls2[e & 1] = ptx::f2_add(ls2[e & 1], ptx::f2_packf(p0, p1));
-            out[e] = ptx::pack_bf16(p0, p1);
+            pk[e] = ptx::pack_bf16(p0, p1);
           }
-        };
-        exps(sa[0], pk[0]);
-        exps(sa[1], pk[1]);
-        // P goes over S columns c_own .. c_own + 31, once the other group has read them
-        if (!rd_done && !(ok = ptx::mbar_wait(rd, (x >> 1) & 1, ctl, status, kSiteFwdSoftS, budget))) break;
-        ptx::tc_fence_after();
-        ptx::tmem_st16(s_tmem + c_own, pk[0]);
-        ptx::tmem_st16(s_tmem + c_own + 16, pk[1]);
+          if (!rd_ok) {
+            if (!(ok = ptx::mbar_wait(rd, (x >> 1) & 1, ctl, status, kSiteFwdSoftS, budget))) break;
+            rd_ok = true;
+          }
+          ptx::tc_fence_after();
+          ptx::tmem_st16(s_tmem + c_own + 16 * u, pk);
+        }
+        if (!ok) break;
         {
           float a0, a1, b0, b1;
           ptx::f2_unpack(ls2[0], a0, a1);
@@ -528,12 +532,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     constexpr float kLn2 = 0.6931471805599453f;
     uint32_t kq = 0;
+    FwdStreamItem nxt;  // the next item's record, loaded one item ahead
+    if (cta < n_items) nxt = stream_item(p, cta);
     for (int idx = cta; idx < n_items; idx += n_ctas) {
-      const FwdStreamItem I = stream_item<CAUSAL>(p, idx);
+      const FwdStreamItem I = nxt;
+      if (idx + n_ctas < n_items) nxt = stream_item(p, idx + n_ctas);
       const int qi = kTile * I.t + r;
       const bool row_ok = qi < I.Lq;
       __nv_bfloat16* orow = p.o + (I.o_row + r) * static_cast<int64_t>(p.heads) * kD2 + static_cast<int64_t>(I.h) * kD2;
-      if (I.n_kv == 0) {  // no keys: O = 0, LSE = -inf
+      if (idx >= n_busy) {  // no keys: O = 0, LSE = -inf
         if (row_ok) {
           for (int c = 0; c < kD2; c += 8) ptx::st_v4(orow + c, 0, 0, 0, 0);
           p.lse[I.lse0 + r] = -INFINITY;
@@ -601,12 +608,12 @@ cudaError_t launch_fwd_stream_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 }  // namespace
 
 cudaError_t launch_fwd_stream(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const int32_t* offsets, const int4* items, int32_t* status, void* o, float* lse,
+                              const int4* items, const int2* item_seq, int32_t* status, void* o, float* lse,
                               int heads, int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
                               cudaStream_t stream) {
   FwdStreamParams p;
-  p.offsets = offsets;
   p.items = items;
+  p.item_seq = item_seq;
   p.status = status;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;

@@ -64,8 +64,10 @@ struct QueueParams {
   int32_t* status;         // status block
   int32_t* tile_base;      // [batch+1] exclusive prefix of q-tiles (self modes)
   int4* items;             // (b, h, t, cost)
+  int2* item_seq;          // optional: (first row, length) of each item's sequence
   int32_t max_items;
-  int32_t count_index;     // status word that receives the number of items (2 or 3)
+  int32_t count_index;     // status word that receives the number of items; the next word
+                           // receives the number with cost >= 1 (they come first)
 };
 
 // Work-item bound used to size the queue: sum_b ceil(L_b/128) <= ceil(total/128) + batch.
@@ -97,7 +99,7 @@ cudaError_t launch_fwd(int head_dim, bool causal, const CUtensorMap& tq, const C
 // Flat-stream forward (head_dim 128); items from the plain forward queue modes,
 // K and V read in 128-row boxes.
 cudaError_t launch_fwd_stream(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const int32_t* offsets, const int4* items, int32_t* status, void* o, float* lse,
+                              const int4* items, const int2* item_seq, int32_t* status, void* o, float* lse,
                               int heads, int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
                               cudaStream_t stream);
 // tdq: the fp32 dQ accumulator [rows, H*D] in 32-column x 128-row boxes, 128B swizzle.

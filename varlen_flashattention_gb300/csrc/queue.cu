@@ -10,14 +10,24 @@
 // expensive remaining items before any cheaper one.
 //
 // One CTA builds the whole queue with a bucket (counting) sort on the cost, so
-// the order is deterministic and bit-exact. It also checks the offsets.
+// the order is deterministic and bit-exact. It also checks the offsets. The
+// number of tiles a sequence has in a cost bucket has a closed form, and the
+// buckets are dealt to the warps: each warp counts, then places, the tiles of
+// its buckets with warp scans over the sequences, and one block scan over the
+// bucket totals gives every bucket its start. The work grows with
+// buckets x sequences and no step waits on the whole block per bucket.
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "jfa_internal.h"
 
 namespace jfa {
 
 constexpr int kQThreads = 1024;
+// Sequence lengths kept in shared memory for the bucket passes (longer
+// batches read the rest from the offsets).
+constexpr int kQueueLenCache = 8 * 1024;
 
 // Exclusive block-wide scan of one int per thread; returns the prefix and
 // writes the block total to *total. All kQThreads threads must call it.
@@ -66,10 +76,44 @@ __device__ __forceinline__ int item_cost(const QueueParams& p, int L, int t) {
   }
 }
 
-__global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParams p) {
+// Tiles of a sequence of length L with cost k: count, and the first of them
+// (they are consecutive: causal, exactly one tile per cost up to the number of
+// tiles; otherwise all tiles share one cost).
+__device__ __forceinline__ void tiles_with_cost(const QueueParams& p, int L, int k, int& count, int& t_first) {
+  const int nt = item_tiles(p, L);
+  count = 0;
+  t_first = 0;
+  if (p.causal && (p.mode == kQueueSelfFwd || p.mode == kQueueSelfBwd)) {
+    if (k >= 1 && k <= nt) {
+      count = 1;
+      t_first = (p.mode == kQueueSelfFwd) ? k - 1 : nt - k;
+    }
+  } else if (nt > 0 && item_cost(p, L, 0) == k) {
+    count = nt;
+  }
+}
+
+__device__ __forceinline__ int seq_len(const int* s_len, const int32_t* offsets, int b) {
+  return b < kQueueLenCache ? s_len[b] : offsets[b + 1] - offsets[b];
+}
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// kmax: the largest cost. Dynamic shared memory: kmax + 1 bucket starts, then
+// the lengths and the first queue positions of the first min(batch,
+// kQueueLenCache) sequences.
+__global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParams p, int kmax) {
+  extern __shared__ int s_start[];  // [kmax + 1]: tiles (per head) of higher cost than bucket k
+  int* s_len = s_start + kmax + 1;
+  int* s_first = s_len + kQueueLenCache;  // first tile position of sequence b (one-cost modes)
   __shared__ int warp_buf[32];
   __shared__ int s_bad;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kQThreads / 32;
   if (tid == 0) s_bad = 0;
   __syncthreads();
 
@@ -85,6 +129,7 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
       if (b == 0 && lo != 0) bad = true;
       if (b == p.batch - 1 && hi != p.total) bad = true;
       if (bad) s_bad = 1;
+      if (b < kQueueLenCache) s_len[b] = L;
       nt = bad ? 0 : ceil_tiles(L);
     }
     int tot;
@@ -98,58 +143,120 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
     if (tid == 0) {
       if (atomicCAS(p.status, JFA_OK, JFA_ERR_BAD_INPUT) == JFA_OK) p.status[1] = kSiteQueueOffsets;
       p.status[p.count_index] = 0;
+      p.status[p.count_index + 1] = 0;
     }
     return;
   }
 
-  // 2. bucket sort by descending cost; within a cost, ascending (b, tile, h)
-  const int kmax = (p.mode == kQueueBcastBwd) ? ceil_tiles(p.q_len) : ceil_tiles(p.max_seqlen);
+  // 2. tiles per cost bucket; warp w takes the buckets kmin + w + 32 i
   const bool keep_empty = p.mode == kQueueBcastFwd;  // empty K/V still owns output rows
   const int kmin = keep_empty ? 0 : 1;
-  int base = 0;
-  for (int k = kmax; k >= kmin; --k) {
-    int bucket = 0;
-    for (int b0 = 0; b0 < p.batch; b0 += kQThreads) {
-      const int b = b0 + tid;
-      // Tiles of sequence b with cost k, in ascending order: t_first and count,
-      // in closed form (causal: exactly one tile; otherwise all tiles share one
-      // cost).
-      int count = 0, L = 0, nt = 0, t_first = 0;
-      if (b < p.batch) {
-        L = p.offsets[b + 1] - p.offsets[b];
-        nt = item_tiles(p, L);
-        if (p.causal && (p.mode == kQueueSelfFwd || p.mode == kQueueSelfBwd)) {
-          count = (k <= nt) ? 1 : 0;
-          t_first = (p.mode == kQueueSelfFwd) ? k - 1 : nt - k;
-        } else {
-          count = (nt > 0 && item_cost(p, L, 0) == k) ? nt : 0;
-        }
-      }
-      int tot;
-      const int pre = block_exclusive_scan(count, warp_buf, &tot);
-      int r = 0;
-      for (int t = t_first; t < nt && r < count; ++t) {
-        const int slot = base + (bucket + pre + r) * p.heads;
-        for (int h = 0; h < p.heads; ++h) {
-          if (slot + h < p.max_items) p.items[slot + h] = make_int4(b, h, t, k);
-        }
-        ++r;
-      }
-      bucket += tot;
+  for (int k = kmin + warp; k <= kmax; k += kWarps) {
+    int n = 0;
+    for (int b = lane; b < p.batch; b += 32) {
+      int c, tf;
+      tiles_with_cost(p, seq_len(s_len, p.offsets, b), k, c, tf);
+      n += c;
     }
-    base += bucket * p.heads;
+    n = warp_sum(n);
+    if (lane == 0) s_start[k] = n;
+  }
+  __syncthreads();
+
+  // 3. bucket starts in descending cost order
+  int total_tiles = 0;
+  for (int k0 = kmax; k0 >= kmin; k0 -= kQThreads) {
+    const int k = k0 - tid;
+    const int v = k >= kmin ? s_start[k] : 0;
+    int tot;
+    const int pre = block_exclusive_scan(v, warp_buf, &tot);
+    if (k >= kmin) s_start[k] = total_tiles + pre;
+    total_tiles += tot;
+  }
+  __syncthreads();
+  // tiles with cost >= 1 come first
+  const int busy_tiles = kmin == 0 ? s_start[0] : total_tiles;
+
+  // 4. place the items: within a bucket ascending (b, tile, h). When all tiles
+  // of a sequence share one cost, the bucket pass only records where each
+  // sequence starts and every thread then writes its own sequences' items,
+  // so that one large bucket is not written by one warp.
+  const bool one_cost = !(p.causal && (p.mode == kQueueSelfFwd || p.mode == kQueueSelfBwd));
+  auto write_items = [&](int b, int first, int c, int tf, int k, int L) {
+    const int s0 = p.offsets[b];
+    for (int r = 0; r < c; ++r) {
+      const int64_t slot = static_cast<int64_t>(first + r) * p.heads;
+      for (int h = 0; h < p.heads; ++h) {
+        if (slot + h < p.max_items) {
+          p.items[slot + h] = make_int4(b, h, tf + r, k);
+          if (p.item_seq) p.item_seq[slot + h] = make_int2(s0, L);
+        }
+      }
+    }
+  };
+  for (int k = kmin + warp; k <= kmax; k += kWarps) {
+    int run = s_start[k];
+    for (int b0 = 0; b0 < p.batch; b0 += 32) {
+      const int b = b0 + lane;
+      int c = 0, tf = 0, L = 0;
+      if (b < p.batch) {
+        L = seq_len(s_len, p.offsets, b);
+        tiles_with_cost(p, L, k, c, tf);
+      }
+      int incl = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const int first = run + incl - c;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+      if (c > 0) {
+        if (one_cost && b < kQueueLenCache)
+          s_first[b] = first;  // written below by the thread that owns b
+        else
+          write_items(b, first, c, tf, k, L);
+      }
+    }
+  }
+  if (one_cost) {
+    __syncthreads();
+    for (int b = tid; b < min(p.batch, kQueueLenCache); b += kQThreads) {
+      const int L = s_len[b];
+      const int nt = item_tiles(p, L);
+      const int k = nt > 0 ? item_cost(p, L, 0) : 0;
+      if (nt > 0 && k >= kmin) write_items(b, s_first[b], nt, 0, k, L);
+    }
   }
   if (tid == 0) {
-    if (base > p.max_items) {
+    int64_t n_items = static_cast<int64_t>(total_tiles) * p.heads;
+    int64_t n_busy = static_cast<int64_t>(busy_tiles) * p.heads;
+    if (n_items > p.max_items) {
       if (atomicCAS(p.status, JFA_OK, JFA_ERR_BAD_INPUT) == JFA_OK) p.status[1] = kSiteQueueOffsets;
-      base = 0;
+      n_items = 0;
+      n_busy = 0;
     }
-    p.status[p.count_index] = base;
+    p.status[p.count_index] = static_cast<int32_t>(n_items);
+    p.status[p.count_index + 1] = static_cast<int32_t>(n_busy);
   }
 }
 
+// The largest cost bucket the queue handles (its starts live in shared memory).
+constexpr int kQueueMaxCost = 32 * 1024;
+
 cudaError_t launch_queue(const QueueParams& p, cudaStream_t stream) {
-  build_queue_kernel<<<1, kQThreads, 0, stream>>>(p);
+  const int64_t kmax = (p.mode == kQueueBcastBwd) ? (static_cast<int64_t>(p.q_len) + kTile - 1) / kTile
+                                                   : (static_cast<int64_t>(p.max_seqlen) + kTile - 1) / kTile;
+  if (kmax > kQueueMaxCost) return cudaErrorInvalidValue;
+  const size_t smem = static_cast<size_t>(kmax + 1 + kQueueLenCache + std::min(p.batch, kQueueLenCache)) * sizeof(int);
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(build_queue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>((kQueueMaxCost + 1 + 2 * kQueueLenCache) * sizeof(int)));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  build_queue_kernel<<<1, kQThreads, smem, stream>>>(p, static_cast<int>(kmax));
   return cudaGetLastError();
 }
 
