@@ -135,7 +135,7 @@ Layout self_layout(int64_t batch, int64_t heads, int64_t total, int64_t head_dim
   L.items = off;
   off = align_up(off + 16 * L.max_items, 256);
   L.item_seq = off;
-  off = align_up(off + 8 * L.max_items, 256);
+  off = align_up(off + 16 * L.max_items, 256);
   if (bwd) {
     L.lse2p = off;
     off = align_up(off + 4 * heads * L.pad_tiles * kTile, 256);
@@ -158,7 +158,7 @@ Layout bcast_layout(int64_t batch, int64_t q_len, int64_t heads, int64_t total_k
   L.items = off;
   off = align_up(off + 16 * L.max_items, 256);
   L.item_seq = off;
-  off = align_up(off + 8 * L.max_items, 256);
+  off = align_up(off + 16 * L.max_items, 256);
   if (bwd) {
     L.pad_tiles = batch * nqt;
     L.lse2p = off;
@@ -310,7 +310,7 @@ jfa_status jfa_fwd(const jfa_fwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   qp.status = status;
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
   qp.items = reinterpret_cast<int4*>(w + L.items);
-  qp.item_seq = reinterpret_cast<int2*>(w + L.item_seq);
+  qp.item_seq = reinterpret_cast<int4*>(w + L.item_seq);
   qp.max_items = static_cast<int32_t>(L.max_items);
   qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
@@ -361,7 +361,7 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   qp.status = status;
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
   qp.items = reinterpret_cast<int4*>(w + L.items);
-  qp.item_seq = reinterpret_cast<int2*>(w + L.item_seq);
+  qp.item_seq = reinterpret_cast<int4*>(w + L.item_seq);
   qp.max_items = static_cast<int32_t>(L.max_items);
   qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
@@ -377,6 +377,7 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   bl.offsets = a->offsets;
   bl.tile_base = qp.tile_base;
   bl.items = qp.items;
+  bl.item_seq = qp.item_seq;
   bl.status = status;
   bl.lse2p = lse2p;
   bl.deltap = deltap;
@@ -393,9 +394,11 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   bl.budget_ns = wait_budget_ns();
   bl.grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items * (a->head_dim / chunk), 1)));
   record(a->main_kernel_events, 0, stream);
-  CUtensorMap tdq;
-  if (!make_tmap_f32_acc(&tdq, dq_acc, a->total, cols)) return JFA_ERR_CUDA;
-  cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, tdq, stream);
+  CUtensorMap tdq, tdk, tdv;
+  if (!make_tmap_f32_acc(&tdq, dq_acc, a->total, cols) || !make_tmap_bf16(&tdk, a->dk, a->total, cols) ||
+      !make_tmap_bf16(&tdv, a->dv, a->total, cols))
+    return JFA_ERR_CUDA;
+  cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, tdq, tdk, tdv, stream);
   record(a->main_kernel_events, 1, stream);
   if (e != cudaSuccess) return JFA_ERR_CUDA;
   return cuda_status(launch_bwd_post(dq_acc, a->dq, n_acc, a->scale, status, sms, stream));
@@ -436,7 +439,7 @@ jfa_status jfa_fwd_broadcast_q(const jfa_bcast_fwd_args* a, void* ws, size_t ws_
   qp.status = status;
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
   qp.items = reinterpret_cast<int4*>(w + L.items);
-  qp.item_seq = reinterpret_cast<int2*>(w + L.item_seq);
+  qp.item_seq = reinterpret_cast<int4*>(w + L.item_seq);
   qp.max_items = static_cast<int32_t>(L.max_items);
   qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
@@ -497,7 +500,7 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
     qp.status = status;
     qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
     qp.items = reinterpret_cast<int4*>(w + L.items);
-    qp.item_seq = reinterpret_cast<int2*>(w + L.item_seq);
+    qp.item_seq = reinterpret_cast<int4*>(w + L.item_seq);
     qp.max_items = static_cast<int32_t>(L.max_items);
     qp.count_index = 2;
     if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
@@ -513,6 +516,7 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
     bl.offsets = a->kv_offsets;
     bl.tile_base = qp.tile_base;
     bl.items = qp.items;
+    bl.item_seq = qp.item_seq;
     bl.status = status;
     bl.lse2p = lse2p;
     bl.deltap = deltap;
@@ -529,9 +533,11 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
     bl.budget_ns = wait_budget_ns();
     bl.grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
     record(a->main_kernel_events, 0, stream);
-    CUtensorMap tdq;
-    if (!make_tmap_f32_acc(&tdq, dq_acc, a->q_len, cols)) return JFA_ERR_CUDA;
-    cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, tdq, stream);
+    CUtensorMap tdq, tdk, tdv;
+    if (!make_tmap_f32_acc(&tdq, dq_acc, a->q_len, cols) || !make_tmap_bf16(&tdk, a->dk, a->total_k, cols) ||
+        !make_tmap_bf16(&tdv, a->dv, a->total_k, cols))
+      return JFA_ERR_CUDA;
+    cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, tdq, tdk, tdv, stream);
     record(a->main_kernel_events, 1, stream);
     if (e != cudaSuccess) return JFA_ERR_CUDA;
   }

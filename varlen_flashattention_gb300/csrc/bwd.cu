@@ -61,6 +61,7 @@ struct BwdParams {
   const int32_t* offsets;     // self: sequence offsets; broadcast: K/V offsets
   const int32_t* tile_base;   // self: padded q-tile index of each sequence
   const int4* items;
+  const int4* item_seq;       // (first row, length, tile_base) of each item's sequence
   int32_t* status;
   const float* lse2p;         // -LSE log2(e), tile-padded (stored negated)
   const float* deltap;        // -delta, tile-padded (stored negated)
@@ -106,22 +107,25 @@ struct BwdItem {
   int64_t row_base;  // padded LSE/delta index of query tile 0 (times 128)
 };
 
+// An item's record: two independent loads (the queue stores each item's
+// sequence start, length and tile base beside it), no dependent lookup.
 __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
   const int idx = v / p.n_chunks;
   BwdItem I;
   I.c = v - idx * p.n_chunks;
   const int4 it = p.items[idx];
+  const int4 sq = p.item_seq[idx];
   I.b = it.x;
   I.h = it.y;
   I.t = it.z;
-  const int s0 = p.offsets[I.b], s1 = p.offsets[I.b + 1];
-  I.Lk = s1 - s0;
+  const int s0 = sq.x;
+  I.Lk = sq.y;
   I.kv_row0 = s0 + kTile * I.t;
   if (!p.bcast) {
     I.Lq = I.Lk;
     I.q_row0 = s0;
     I.do_row0 = s0;
-    I.row_base = (static_cast<int64_t>(I.h) * p.pad_tiles + p.tile_base[I.b]) * kTile;
+    I.row_base = (static_cast<int64_t>(I.h) * p.pad_tiles + sq.z) * kTile;
   } else {
     I.Lq = p.q_len;
     I.q_row0 = 0;
@@ -139,7 +143,8 @@ template <int D, int DC>
 __global__ void __launch_bounds__(448, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-               const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+               const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+               const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
   using Lay = BwdLayout<D, DC>;
   constexpr int kSt = Lay::kStages;
   constexpr uint32_t kIdS = ptx::idesc_bf16(128, 128, false, false);   // S^T, dP^T
@@ -210,6 +215,8 @@ __global__ void __launch_bounds__(448, 1)
     ptx::prefetch_tmap(&tm_v);
     ptx::prefetch_tmap(&tm_do);
     ptx::prefetch_tmap(&tm_dq);
+    ptx::prefetch_tmap(&tm_dk);
+    ptx::prefetch_tmap(&tm_dv);
   }
   if (warp == 9) {
     ptx::tmem_alloc(tmem_slot, Lay::kTmemCols);
@@ -225,12 +232,44 @@ __global__ void __launch_bounds__(448, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
+    // Order: the first query tile of the next item (its stage frees two tiles
+    // before the end of the current item) before that item's K and V (which
+    // wait for the last MMA of the current item), then its later query tiles.
     if (lane == 0) {
       uint32_t pos = 0, kitem = 0;
       bool ok = true;
-      for (int v = blockIdx.x; ok && v < n_work; v += gridDim.x) {
-        const BwdItem I = bwd_item(p, v);
-        if (I.nq <= 0) continue;
+      auto next_item = [&](int v, BwdItem& I) -> int {  // next item with query tiles, from index v
+        for (; v < n_work; v += gridDim.x) {
+          I = bwd_item(p, v);
+          if (I.nq > 0) break;
+        }
+        return v;
+      };
+      auto load_qdo = [&](const BwdItem& I, int ii) -> bool {
+        const int i = I.i0 + ii;
+        const uint32_t st = pos % kSt, round = pos / kSt;
+        if (!ptx::mbar_wait(q_empty + st, (round & 1) ^ 1, ctl, status, kSiteBwdProdQ, budget)) return false;
+        ptx::mbar_arrive_expect_tx(q_full + st, Lay::kTileBytes + 1024);
+        uint8_t* qd = smem + Lay::kOffQ + st * Lay::kTileBytes;
+#pragma unroll
+        for (int a = 0; a < Lay::kAtoms; ++a)
+          ptx::tma_load_2d(qd + a * 16384, &tm_q, q_full + st, I.h * D + 64 * a, I.q_row0 + kTile * i);
+        uint8_t* rows = smem + Lay::kOffRow + st * 1024;
+        ptx::bulk_load(rows, p.lse2p + I.row_base + static_cast<int64_t>(kTile) * i, 512, q_full + st);
+        ptx::bulk_load(rows + 512, p.deltap + I.row_base + static_cast<int64_t>(kTile) * i, 512, q_full + st);
+        if (!ptx::mbar_wait(do_empty + st, (round & 1) ^ 1, ctl, status, kSiteBwdProdQ, budget)) return false;
+        ptx::mbar_arrive_expect_tx(do_full + st, Lay::kTileBytes);
+        uint8_t* dd = smem + Lay::kOffDO + st * Lay::kTileBytes;
+#pragma unroll
+        for (int a = 0; a < Lay::kAtoms; ++a)
+          ptx::tma_load_2d(dd + a * 16384, &tm_do, do_full + st, I.h * D + 64 * a, I.do_row0 + kTile * i);
+        ++pos;
+        return true;
+      };
+      BwdItem I;
+      int v = next_item(blockIdx.x, I);
+      if (v < n_work) ok = load_qdo(I, 0);
+      while (ok && v < n_work) {
         if (!(ok = ptx::mbar_wait(kv_empty, (kitem & 1) ^ 1, ctl, status, kSiteBwdProdKV, budget))) break;
         ptx::mbar_arrive_expect_tx(kv_full, 2 * Lay::kTileBytes);
 #pragma unroll
@@ -238,28 +277,23 @@ __global__ void __launch_bounds__(448, 1)
           ptx::tma_load_2d(smem + Lay::kOffK + a * 16384, &tm_k, kv_full, I.h * D + 64 * a, I.kv_row0);
           ptx::tma_load_2d(smem + Lay::kOffV + a * 16384, &tm_v, kv_full, I.h * D + 64 * a, I.kv_row0);
         }
-        for (int ii = 0; ii < I.nq; ++ii) {
-          const int i = I.i0 + ii;
-          const uint32_t st = pos % kSt, round = pos / kSt;
-          if (!(ok = ptx::mbar_wait(q_empty + st, (round & 1) ^ 1, ctl, status, kSiteBwdProdQ, budget))) break;
-          ptx::mbar_arrive_expect_tx(q_full + st, Lay::kTileBytes + 1024);
-          uint8_t* qd = smem + Lay::kOffQ + st * Lay::kTileBytes;
-#pragma unroll
-          for (int a = 0; a < Lay::kAtoms; ++a)
-            ptx::tma_load_2d(qd + a * 16384, &tm_q, q_full + st, I.h * D + 64 * a, I.q_row0 + kTile * i);
-          uint8_t* rows = smem + Lay::kOffRow + st * 1024;
-          ptx::bulk_load(rows, p.lse2p + I.row_base + static_cast<int64_t>(kTile) * i, 512, q_full + st);
-          ptx::bulk_load(rows + 512, p.deltap + I.row_base + static_cast<int64_t>(kTile) * i, 512, q_full + st);
-          if (!(ok = ptx::mbar_wait(do_empty + st, (round & 1) ^ 1, ctl, status, kSiteBwdProdQ, budget))) break;
-          ptx::mbar_arrive_expect_tx(do_full + st, Lay::kTileBytes);
-          uint8_t* dd = smem + Lay::kOffDO + st * Lay::kTileBytes;
-#pragma unroll
-          for (int a = 0; a < Lay::kAtoms; ++a)
-            ptx::tma_load_2d(dd + a * 16384, &tm_do, do_full + st, I.h * D + 64 * a, I.do_row0 + kTile * i);
-          ++pos;
-        }
+        for (int ii = 1; ok && ii < I.nq; ++ii) ok = load_qdo(I, ii);
+        if (!ok) break;
+        BwdItem N;
+        v = next_item(v + gridDim.x, N);
+        if (v < n_work) ok = load_qdo(N, 0);
+        I = N;
         ++kitem;
       }
+      // After an abort some loads may have no consumer: wait (bounded) for the
+      // last fill of every stage and of K/V so that no copy is in flight when
+      // the CTA exits.
+      ptx::CtaCtl no_abort{0, 0};
+      for (uint32_t q = pos > kSt ? pos - kSt : 0; q < pos; ++q) {
+        ptx::mbar_wait(q_full + q % kSt, (q / kSt) & 1, &no_abort, nullptr, kSiteBwdDrain, budget);
+        ptx::mbar_wait(do_full + q % kSt, (q / kSt) & 1, &no_abort, nullptr, kSiteBwdDrain, budget);
+      }
+      if (kitem > 0) ptx::mbar_wait(kv_full, (kitem - 1) & 1, &no_abort, nullptr, kSiteBwdDrain, budget);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -350,7 +384,10 @@ __global__ void __launch_bounds__(448, 1)
                         ptx::sdesc_sw128(q_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdAcc,
                         (ii > 0 || kk > 0) ? 1u : 0u);
           }
-          ptx::mma_commit(q_empty + st);  // dK is the last reader of Q (the softmax read the rows before dS^T)
+          // dK is the last reader of Q (the softmax read the rows before dS^T);
+          // the last tile's stage is released by the epilogue, which stages dK
+          // and dV there
+          if (!(kStageInDO && ii + 1 == I.nq)) ptx::mma_commit(q_empty + st);
           if (!kStageInDO) ptx::mma_commit(do_empty + st);  // single stage: dO is free too (dV read it)
           // dQ(tile) = dS K[:, slice] into the dP^T columns
 #pragma unroll
@@ -604,22 +641,42 @@ __global__ void __launch_bounds__(448, 1)
         }
         if (issuer) ptx::bulk_wait_read0();
         if (!ok) break;
-        if (issuer) ptx::mbar_arrive(kStageInDO ? do_empty + st : stage_free);
+        if (issuer && !(kStageInDO && ii + 1 == I.nq)) ptx::mbar_arrive(kStageInDO ? do_empty + st : stage_free);
       }
       if (!ok) break;
       if (!(ok = ptx::mbar_wait(acc_full, kitem & 1, ctl, status, kSiteBwdEpi, budget))) break;
       ptx::tc_fence_after();
-      const bool k_ok = r < I.Lk - kTile * I.t;
-      const int64_t orow = (static_cast<int64_t>(I.kv_row0 + r) * p.heads + I.h) * D + I.c * DC;
+      const bool issuer = warp == 10 && lane == 0;
+      const uint32_t st_last = (x - 1) % kSt;  // stage of the item's last query tile
+      const bool full_tile = I.Lk - kTile * I.t >= kTile;
+      auto release_acc = [&]() {  // dV and dK are out of TMEM: the next item may accumulate
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(acc_free);
+      };
+      if (kStageInDO && full_tile) {
+        // dV and dK go to global memory by TMA: staged as bf16 (128B swizzle,
+        // 64-column atoms) in the Q and dO buffers of the last tile's stage,
+        // which the producer gets back once the stores have read them.
+        uint8_t* sv = smem + Lay::kOffQ + st_last * Lay::kTileBytes;
+        uint8_t* sk = smem + Lay::kOffDO + st_last * Lay::kTileBytes;
+        // the last tile's dQ reduce-adds have read their staging in the dO buffer
+        if (issuer) {
+          ptx::bulk_wait_read0();
+          ptx::mbar_arrive(stage_read);
+        }
+        if (!(ok = ptx::mbar_wait(stage_read, nr & 1, ctl, status, kSiteBwdEpi, budget))) break;
+        ++nr;
 #pragma unroll 1
-      for (int c = 0; c < DC / 32; ++c) {
-        uint32_t a[32], b[32];
-        ptx::tmem_ld32(tmem + lane_base + Lay::kColDV + 32 * c, a);
-        ptx::tmem_ld32(tmem + lane_base + Lay::kColDK + 32 * c, b);
-        ptx::tmem_ld_wait();
-        ptx::reg_fence32(a);
-        ptx::reg_fence32(b);
-        if (k_ok) {
+        for (int c = 0; c < DC / 32; ++c) {
+          uint32_t a[32], b[32];
+          ptx::tmem_ld32(tmem + lane_base + Lay::kColDV + 32 * c, a);
+          ptx::tmem_ld32(tmem + lane_base + Lay::kColDK + 32 * c, b);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence32(a);
+          ptx::reg_fence32(b);
+          if (c == DC / 32 - 1) release_acc();
+          const int off = (c >> 1) * 16384 + r * 128;  // atom of these 32 columns, this row
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t wv[4], wk[4];
@@ -629,14 +686,61 @@ __global__ void __launch_bounds__(448, 1)
               wk[e] = ptx::pack_bf16(__uint_as_float(b[8 * q4 + 2 * e]) * p.scale,
                                      __uint_as_float(b[8 * q4 + 2 * e + 1]) * p.scale);
             }
-            ptx::st_v4(p.dv + orow + 32 * c + 8 * q4, wv[0], wv[1], wv[2], wv[3]);
-            ptx::st_v4(p.dk + orow + 32 * c + 8 * q4, wk[0], wk[1], wk[2], wk[3]);
+            const int chunk = ((((c & 1) << 2) + q4) ^ (r & 7)) << 4;
+            ptx::st_shared_v4(sv + off + chunk, wv[0], wv[1], wv[2], wv[3]);
+            ptx::st_shared_v4(sk + off + chunk, wk[0], wk[1], wk[2], wk[3]);
           }
         }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(staged);
+        if (!(ok = ptx::mbar_wait(staged, ns & 1, ctl, status, kSiteBwdEpi, budget))) break;
+        ++ns;
+        if (issuer) {
+          const int xcol = I.h * D + I.c * DC;
+#pragma unroll
+          for (int at = 0; at < DC / 64; ++at) {
+            ptx::tma_store_2d(&tm_dv, sv + at * 16384, xcol + 64 * at, I.kv_row0);
+            ptx::tma_store_2d(&tm_dk, sk + at * 16384, xcol + 64 * at, I.kv_row0);
+          }
+          ptx::bulk_commit();
+          ptx::bulk_wait_read0();
+          ptx::mbar_arrive(q_empty + st_last);
+          ptx::mbar_arrive(do_empty + st_last);
+        }
+      } else {
+        // a partial key tile (its rows end inside the 128-row box) or a single
+        // stage: every thread stores its own row
+        const bool k_ok = r < I.Lk - kTile * I.t;
+        const int64_t orow = (static_cast<int64_t>(I.kv_row0 + r) * p.heads + I.h) * D + I.c * DC;
+#pragma unroll 1
+        for (int c = 0; c < DC / 32; ++c) {
+          uint32_t a[32], b[32];
+          ptx::tmem_ld32(tmem + lane_base + Lay::kColDV + 32 * c, a);
+          ptx::tmem_ld32(tmem + lane_base + Lay::kColDK + 32 * c, b);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence32(a);
+          ptx::reg_fence32(b);
+          if (c == DC / 32 - 1) release_acc();
+          if (k_ok) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t wv[4], wk[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                wv[e] = ptx::pack_bf16(__uint_as_float(a[8 * q4 + 2 * e]), __uint_as_float(a[8 * q4 + 2 * e + 1]));
+                wk[e] = ptx::pack_bf16(__uint_as_float(b[8 * q4 + 2 * e]) * p.scale,
+                                       __uint_as_float(b[8 * q4 + 2 * e + 1]) * p.scale);
+              }
+              ptx::st_v4(p.dv + orow + 32 * c + 8 * q4, wv[0], wv[1], wv[2], wv[3]);
+              ptx::st_v4(p.dk + orow + 32 * c + 8 * q4, wk[0], wk[1], wk[2], wk[3]);
+            }
+          }
+        }
+        if (kStageInDO && issuer) {  // the last tile's stage: Q was read by dK, dO by dV and the dQ staging
+          ptx::mbar_arrive(q_empty + st_last);
+          ptx::mbar_arrive(do_empty + st_last);
+        }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(acc_free);
       ++kitem;
     }
     if (warp == 10 && lane == 0) ptx::bulk_wait0();  // every reduce-add has completed
@@ -740,7 +844,8 @@ __global__ void bwd_post_kernel(const float4* __restrict__ acc, uint2* __restric
 
 template <int D, int DC>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int grid,
+                                const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                                const CUtensorMap& tdv, const BwdParams& p, int grid,
                                 cudaStream_t stream) {
   using Lay = BwdLayout<D, DC>;
   static bool attr_set = false;
@@ -749,15 +854,17 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  bwd_kernel<D, DC><<<grid, 448, Lay::kAlloc, stream>>>(tq, tk, tv, tdo, tdq, p);
+  bwd_kernel<D, DC><<<grid, 448, Lay::kAlloc, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const CUtensorMap& tdq, cudaStream_t stream) {
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                            const CUtensorMap& tdv, cudaStream_t stream) {
   BwdParams p;
   p.offsets = L.offsets;
   p.tile_base = L.tile_base;
+  p.item_seq = L.item_seq;
   p.items = L.items;
   p.status = L.status;
   p.lse2p = L.lse2p;
@@ -774,10 +881,10 @@ cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUt
   p.scale = L.scale;
   p.scale_log2 = L.scale * 1.4426950408889634f;
   p.budget_ns = L.budget_ns;
-  if (L.head_dim == 64 && L.head_chunk == 64) return launch_bwd_t<64, 64>(tq, tk, tv, tdo, tdq, p, L.grid, stream);
-  if (L.head_dim == 128 && L.head_chunk == 128) return launch_bwd_t<128, 128>(tq, tk, tv, tdo, tdq, p, L.grid, stream);
-  if (L.head_dim == 128 && L.head_chunk == 64) return launch_bwd_t<128, 64>(tq, tk, tv, tdo, tdq, p, L.grid, stream);
-  if (L.head_dim == 192 && L.head_chunk == 64) return launch_bwd_t<192, 64>(tq, tk, tv, tdo, tdq, p, L.grid, stream);
+  if (L.head_dim == 64 && L.head_chunk == 64) return launch_bwd_t<64, 64>(tq, tk, tv, tdo, tdq, tdk, tdv, p, L.grid, stream);
+  if (L.head_dim == 128 && L.head_chunk == 128) return launch_bwd_t<128, 128>(tq, tk, tv, tdo, tdq, tdk, tdv, p, L.grid, stream);
+  if (L.head_dim == 128 && L.head_chunk == 64) return launch_bwd_t<128, 64>(tq, tk, tv, tdo, tdq, tdk, tdv, p, L.grid, stream);
+  if (L.head_dim == 192 && L.head_chunk == 64) return launch_bwd_t<192, 64>(tq, tk, tv, tdo, tdq, tdk, tdv, p, L.grid, stream);
   return cudaErrorInvalidValue;
 }
 

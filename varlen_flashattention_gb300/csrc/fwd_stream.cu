@@ -45,7 +45,7 @@ constexpr int kThreads = 448;
 
 struct FwdStreamParams {
   const int4* items;     // (b, h, query tile, key tiles)
-  const int2* item_seq;  // (first row, length) of the item's key sequence
+  const int4* item_seq;  // (first row, length, tile_base) of the item's key sequence
   int32_t* status;
   __nv_bfloat16* o;
   float* lse;
@@ -86,7 +86,7 @@ struct FwdStreamItem {
 // sequence start and length beside it), so nothing waits on a dependent load.
 __device__ __forceinline__ FwdStreamItem stream_item(const FwdStreamParams& p, int idx) {
   const int4 it = p.items[idx];
-  const int2 sq = p.item_seq[idx];
+  const int4 sq = p.item_seq[idx];
   FwdStreamItem I;
   I.b = it.x;
   I.h = it.y;
@@ -608,7 +608,7 @@ cudaError_t launch_fwd_stream_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 }  // namespace
 
 cudaError_t launch_fwd_stream(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const int4* items, const int2* item_seq, int32_t* status, void* o, float* lse,
+                              const int4* items, const int4* item_seq, int32_t* status, void* o, float* lse,
                               int heads, int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
                               cudaStream_t stream) {
   FwdStreamParams p;

@@ -64,7 +64,7 @@ struct QueueParams {
   int32_t* status;         // status block
   int32_t* tile_base;      // [batch+1] exclusive prefix of q-tiles (self modes)
   int4* items;             // (b, h, t, cost)
-  int2* item_seq;          // optional: (first row, length) of each item's sequence
+  int4* item_seq;          // optional: (first row, length, tile_base) of each item's sequence
   int32_t max_items;
   int32_t count_index;     // status word that receives the number of items; the next word
                            // receives the number with cost >= 1 (they come first)
@@ -78,6 +78,7 @@ struct BwdLaunch {
   const int32_t* offsets;
   const int32_t* tile_base;
   const int4* items;
+  const int4* item_seq;  // (first row, length, tile_base) of each item's sequence
   int32_t* status;
   const float* lse2p;
   const float* deltap;
@@ -99,12 +100,14 @@ cudaError_t launch_fwd(int head_dim, bool causal, const CUtensorMap& tq, const C
 // Flat-stream forward (head_dim 128); items from the plain forward queue modes,
 // K and V read in 128-row boxes.
 cudaError_t launch_fwd_stream(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const int4* items, const int2* item_seq, int32_t* status, void* o, float* lse,
+                              const int4* items, const int4* item_seq, int32_t* status, void* o, float* lse,
                               int heads, int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
                               cudaStream_t stream);
 // tdq: the fp32 dQ accumulator [rows, H*D] in 32-column x 128-row boxes, 128B swizzle.
+// tdk, tdv: dK and dV (bf16 [rows, H*D]) in 64-column x 128-row boxes, 128B swizzle.
 cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const CUtensorMap& tdq, cudaStream_t stream);
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                            const CUtensorMap& tdv, cudaStream_t stream);
 cudaError_t launch_bwd_pre(int head_dim, const void* o, const void* dout, const float* lse, const int32_t* offsets,
                            const int32_t* tile_base, const int32_t* status, int batch, int heads, int total, int bcast,
                            int q_len, int pad_tiles, int grid_tiles, float* lse2p, float* deltap,

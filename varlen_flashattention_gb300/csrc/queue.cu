@@ -184,12 +184,13 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
   const bool one_cost = !(p.causal && (p.mode == kQueueSelfFwd || p.mode == kQueueSelfBwd));
   auto write_items = [&](int b, int first, int c, int tf, int k, int L) {
     const int s0 = p.offsets[b];
+    const int tb = p.tile_base ? p.tile_base[b] : 0;
     for (int r = 0; r < c; ++r) {
       const int64_t slot = static_cast<int64_t>(first + r) * p.heads;
       for (int h = 0; h < p.heads; ++h) {
         if (slot + h < p.max_items) {
           p.items[slot + h] = make_int4(b, h, tf + r, k);
-          if (p.item_seq) p.item_seq[slot + h] = make_int2(s0, L);
+          if (p.item_seq) p.item_seq[slot + h] = make_int4(s0, L, tb, 0);
         }
       }
     }
