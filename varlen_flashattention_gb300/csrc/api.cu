@@ -318,8 +318,10 @@ jfa_status jfa_fwd(const jfa_fwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
   record(a->main_kernel_events, 0, stream);
   if (fwd_stream_path(a->head_dim)) {
-    e = launch_fwd_stream(a->causal != 0, tq, tk, tv, qp.items, qp.item_seq, status, a->o, a->lse, a->heads, a->total,
-                          0, 0, a->scale, wait_budget_ns(), grid, stream);
+    CUtensorMap to;
+    if (!make_tmap_bf16(&to, a->o, a->total, cols)) return JFA_ERR_CUDA;
+    e = launch_fwd_stream(a->causal != 0, tq, tk, tv, to, qp.items, qp.item_seq, status, a->o, a->lse, a->heads,
+                          a->total, 0, 0, a->scale, wait_budget_ns(), grid, stream);
   } else {
     e = launch_fwd(a->head_dim, a->causal != 0, tq, tk, tv, a->offsets, qp.items, status, a->o, a->lse, a->heads,
                    a->total, 0, 0, a->scale, wait_budget_ns(), grid, stream);
@@ -447,8 +449,10 @@ jfa_status jfa_fwd_broadcast_q(const jfa_bcast_fwd_args* a, void* ws, size_t ws_
   const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
   record(a->main_kernel_events, 0, stream);
   if (fwd_stream_path(a->head_dim)) {
-    e = launch_fwd_stream(false, tq, tk, tv, qp.items, qp.item_seq, status, a->o, a->lse, a->heads, a->total_k, 1,
-                          a->q_len, a->scale, wait_budget_ns(), grid, stream);
+    CUtensorMap to;
+    if (!make_tmap_bf16(&to, a->o, static_cast<uint64_t>(a->batch) * a->q_len, cols)) return JFA_ERR_CUDA;
+    e = launch_fwd_stream(false, tq, tk, tv, to, qp.items, qp.item_seq, status, a->o, a->lse, a->heads, a->total_k,
+                          1, a->q_len, a->scale, wait_budget_ns(), grid, stream);
   } else {
     e = launch_fwd(a->head_dim, false, tq, tk, tv, a->kv_offsets, qp.items, status, a->o, a->lse, a->heads,
                    a->total_k, 1, a->q_len, a->scale, wait_budget_ns(), grid, stream);

@@ -58,15 +58,16 @@ struct FwdStreamLayout {
   static constexpr int kQBytes = kTile * kD2 * 2;   // one query tile: 128 rows x 128 d
   static constexpr int kKVBytes = kTile * kD2 * 2;  // one K or V tile
   static constexpr int kQSlots = 2;
-  static constexpr int kSlots = 5;
+  static constexpr int kSlots = 4;
   static constexpr int kOffQ = 0;
   static constexpr int kOffSlots = kQSlots * kQBytes;
-  static constexpr int kOffMl = kOffSlots + kSlots * kKVBytes;  // float2 (m, l) per row, two buffers
+  static constexpr int kOffOStage = kOffSlots + kSlots * kKVBytes;  // O of a finished item (bf16, TMA store)
+  static constexpr int kOffMl = kOffOStage + kTile * kD2 * 2;        // float2 (m, l) per row, two buffers
   static constexpr int kOffBars = kOffMl + 2 * kTile * 8;
   // q_full[2], q_empty[2], slot_full[S], slot_empty[S], s_full[2], p_full[2],
   // o_ready[2], o_final[2], o_free[2], ml_half[2], ml_full[2], ml_empty[2],
   // s_read[2][4], drain
-  static constexpr int kNumBars = 2 * kQSlots + 2 * kSlots + 8 * 2 + 8 + 1;
+  static constexpr int kNumBars = 2 * kQSlots + 2 * kSlots + 8 * 2 + 8 + 1 + 2;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 32;
   // Tiles need 1024-byte alignment; the dynamic shared-memory base is
@@ -147,7 +148,8 @@ __device__ __forceinline__ void walk_loads(const FwdStreamParams& p, int first, 
 template <bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_stream_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const FwdStreamParams p) {
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                      const FwdStreamParams p) {
   using Lay = FwdStreamLayout;
   constexpr int kSlots = Lay::kSlots;
   constexpr int kQS = Lay::kQSlots;
@@ -175,6 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* ml_empty = ml_full + 2;
   uint64_t* s_read = ml_empty + 2;  // [S buffer][warp quarter]
   uint64_t* drain = s_read + 8;
+  uint64_t* o_staged = drain + 1;      // every epilogue thread has written its row of the O staging
+  uint64_t* o_stage_read = drain + 2;  // the TMA store of the previous staged O has read it
   float2* ml = reinterpret_cast<float2*>(smem + Lay::kOffMl);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   ptx::CtaCtl* ctl = reinterpret_cast<ptx::CtaCtl*>(smem + Lay::kOffMisc + 8);
@@ -202,6 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 8; ++i) ptx::mbar_init(s_read + i, 2);  // the two warps on one lane quarter
     ptx::mbar_init(drain, 1);
+    ptx::mbar_init(o_staged, kTile);
+    ptx::mbar_init(o_stage_read, 1);
     ctl->abort = 0;
     ptx::fence_barrier_init();
   }
@@ -209,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tm_q);
     ptx::prefetch_tmap(&tm_k);
     ptx::prefetch_tmap(&tm_v);
+    ptx::prefetch_tmap(&tm_o);
   }
   __syncthreads();
   if (warp == 13) {
@@ -527,12 +534,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 8-11)
+    // O of a whole query tile leaves by TMA store: normalised, packed to bf16
+    // and staged (128B swizzle, two 64-column atoms); a partial tile, whose
+    // 128-row box would reach into the next sequence, is stored row by row.
     const int quarter = warp & 3;  // TMEM lanes 32 (warp % 4) .. are this warp's rows
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     constexpr float kLn2 = 0.6931471805599453f;
-    uint32_t kq = 0;
-    FwdStreamItem nxt;  // the next item's record, loaded one item ahead
+    const bool issuer = warp == 8 && lane == 0;
+    uint8_t* ostage = smem + Lay::kOffOStage;
+    uint32_t kq = 0, n_st = 0;  // busy items; items whose O went through the staging
+    FwdStreamItem nxt;          // the next item's record, loaded one item ahead
     if (cta < n_items) nxt = stream_item(p, cta);
     for (int idx = cta; idx < n_items; idx += n_ctas) {
       const FwdStreamItem I = nxt;
@@ -557,30 +569,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) ptx::mbar_arrive(ml_empty + ob);
       const float inv_l = st.y > 0.f ? 1.0f / st.y : 0.f;
       const uint32_t o_tmem = tmem + lane_base + (ob ? Lay::kColO1 : Lay::kColO0);
+      const bool staged = I.Lq - kTile * I.t >= kTile;
+      if (staged && n_st > 0) {  // the previous TMA store has read the staging
+        if (issuer) {
+          ptx::bulk_wait_read0();
+          ptx::mbar_arrive(o_stage_read);
+        }
+        if (!ptx::mbar_wait(o_stage_read, (n_st - 1) & 1, ctl, status, kSiteFwdEpi, budget)) break;
+      }
 #pragma unroll 1
       for (int c = 0; c < kD2 / 32; ++c) {
         uint32_t ov[32];
         ptx::tmem_ld32(o_tmem + 32 * c, ov);
         ptx::tmem_ld_wait();
         ptx::reg_fence32(ov);
-        if (row_ok) {
+        if (c == kD2 / 32 - 1) {  // all of O is in registers: the next item may use this buffer
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(o_free + ob);
+        }
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t wv[4];
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t wv[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              wv[e] = ptx::pack_bf16(__uint_as_float(ov[8 * q4 + 2 * e]) * inv_l,
-                                     __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv_l);
+          for (int e = 0; e < 4; ++e)
+            wv[e] = ptx::pack_bf16(__uint_as_float(ov[8 * q4 + 2 * e]) * inv_l,
+                                   __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv_l);
+          if (staged)
+            ptx::st_shared_v4(ostage + (c >> 1) * 16384 + r * 128 + (((((c & 1) << 2) + q4) ^ (r & 7)) << 4), wv[0],
+                              wv[1], wv[2], wv[3]);
+          else if (row_ok)
             ptx::st_v4(orow + 32 * c + 8 * q4, wv[0], wv[1], wv[2], wv[3]);
-          }
         }
       }
+      if (staged) {
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(o_staged);
+        if (!ptx::mbar_wait(o_staged, n_st & 1, ctl, status, kSiteFwdEpi, budget)) break;
+        if (issuer) {
+          ptx::tma_store_2d(&tm_o, ostage, I.h * kD2, static_cast<int32_t>(I.o_row));
+          ptx::tma_store_2d(&tm_o, ostage + 16384, I.h * kD2 + 64, static_cast<int32_t>(I.o_row));
+          ptx::bulk_commit();
+        }
+        ++n_st;
+      }
       if (row_ok) p.lse[I.lse0 + r] = (st.x + log2f(st.y)) * kLn2;
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(o_free + ob);
       ++kq;
     }
+    if (issuer) ptx::bulk_wait0();  // every O store has completed
   }
 
   ptx::tc_fence_before();
@@ -593,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <bool CAUSAL>
 cudaError_t launch_fwd_stream_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const FwdStreamParams& p, int grid, cudaStream_t stream) {
+                                const CUtensorMap& to, const FwdStreamParams& p, int grid, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(fwd_stream_kernel<CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -601,14 +637,14 @@ cudaError_t launch_fwd_stream_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  fwd_stream_kernel<CAUSAL><<<grid, kThreads, FwdStreamLayout::kBytes, stream>>>(tq, tk, tv, p);
+  fwd_stream_kernel<CAUSAL><<<grid, kThreads, FwdStreamLayout::kBytes, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_stream(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const int4* items, const int4* item_seq, int32_t* status, void* o, float* lse,
+                              const CUtensorMap& to, const int4* items, const int4* item_seq, int32_t* status, void* o, float* lse,
                               int heads, int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
                               cudaStream_t stream) {
   FwdStreamParams p;
@@ -623,8 +659,8 @@ cudaError_t launch_fwd_stream(bool causal, const CUtensorMap& tq, const CUtensor
   p.q_len = q_len;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.budget_ns = budget_ns;
-  return causal ? launch_fwd_stream_t<true>(tq, tk, tv, p, grid, stream)
-                : launch_fwd_stream_t<false>(tq, tk, tv, p, grid, stream);
+  return causal ? launch_fwd_stream_t<true>(tq, tk, tv, to, p, grid, stream)
+                : launch_fwd_stream_t<false>(tq, tk, tv, to, p, grid, stream);
 }
 
 }  // namespace jfa

@@ -98,9 +98,9 @@ cudaError_t launch_fwd(int head_dim, bool causal, const CUtensorMap& tq, const C
                        int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
                        cudaStream_t stream);
 // Flat-stream forward (head_dim 128); items from the plain forward queue modes,
-// K and V read in 128-row boxes.
+// K and V read in 128-row boxes, O (to) written in 64-column x 128-row boxes.
 cudaError_t launch_fwd_stream(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const int4* items, const int4* item_seq, int32_t* status, void* o, float* lse,
+                              const CUtensorMap& to, const int4* items, const int4* item_seq, int32_t* status, void* o, float* lse,
                               int heads, int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
                               cudaStream_t stream);
 // tdq: the fp32 dQ accumulator [rows, H*D] in 32-column x 128-row boxes, 128B swizzle.
