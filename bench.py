@@ -459,7 +459,7 @@ def main():
     if k_b >= k_f:
         dom, dom_ms, dom_flops = "jfa bwd main kernel (bwd_kernel<128,128>)", k_b, flops_b
     else:
-        dom, dom_ms, dom_flops = "jfa fwd main kernel (fwd_stream_kernel<false,false>)", k_f, flops_f
+        dom, dom_ms, dom_flops = "jfa fwd main kernel (fwd_stream_kernel<false>)", k_f, flops_f
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     traffic = None
