@@ -344,8 +344,7 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   const int sms = sm_count();
   if (sms <= 0) return JFA_ERR_CUDA;
   const int64_t n_acc = static_cast<int64_t>(a->total) * a->heads * a->head_dim;
-  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
-  if (cudaMemsetAsync(dq_acc, 0, 4 * n_acc, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);  // zeroed by the pre-pass
   CUtensorMap tq, tk, tv, tdo;
   const uint64_t cols = static_cast<uint64_t>(a->heads) * a->head_dim;
   if (!make_tmap_bf16(&tq, a->q, a->total, cols) || !make_tmap_bf16(&tk, a->k, a->total, cols) ||
@@ -371,7 +370,7 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   float* deltap = reinterpret_cast<float*>(w + L.deltap);
   if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->offsets, qp.tile_base, status, a->batch, a->heads,
                      a->total, 0, 0, static_cast<int>(L.pad_tiles), static_cast<int>(L.pad_tiles), lse2p, deltap,
-                     stream) != cudaSuccess)
+                     dq_acc, stream) != cudaSuccess)
     return JFA_ERR_CUDA;
   BwdLaunch bl;
   bl.head_dim = a->head_dim;
@@ -481,11 +480,12 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
   if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
   if (a->q_len == 0) return JFA_OK;
   const int64_t n_acc = static_cast<int64_t>(a->q_len) * a->heads * a->head_dim;
-  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
-  if (cudaMemsetAsync(dq_acc, 0, 4 * n_acc, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);  // zeroed by the pre-pass when there are keys
   const int sms = sm_count();
   if (sms <= 0) return JFA_ERR_CUDA;
-  if (a->batch > 0 && a->total_k > 0) {
+  if (!(a->batch > 0 && a->total_k > 0)) {
+    if (cudaMemsetAsync(dq_acc, 0, 4 * n_acc, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  } else {
     CUtensorMap tq, tk, tv, tdo;
     const uint64_t cols = static_cast<uint64_t>(a->heads) * a->head_dim;
     if (!make_tmap_bf16(&tq, a->q, a->q_len, cols) || !make_tmap_bf16(&tk, a->k, a->total_k, cols) ||
@@ -511,7 +511,7 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
     float* lse2p = reinterpret_cast<float*>(w + L.lse2p);
     float* deltap = reinterpret_cast<float*>(w + L.deltap);
     if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->kv_offsets, nullptr, status, a->batch, a->heads,
-                       a->total_k, 1, a->q_len, 0, static_cast<int>(L.pad_tiles), lse2p, deltap,
+                       a->total_k, 1, a->q_len, 0, static_cast<int>(L.pad_tiles), lse2p, deltap, dq_acc,
                        stream) != cudaSuccess)
       return JFA_ERR_CUDA;
     BwdLaunch bl;

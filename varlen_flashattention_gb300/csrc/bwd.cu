@@ -760,22 +760,31 @@ __global__ void __launch_bounds__(448, 1)
 // backward adds them with paired fp32 instructions), written in a layout padded
 // to whole 128-row query tiles (zeros past the end of a sequence), so that the
 // backward can fetch one tile's 128 values with a single aligned bulk copy.
-// One CTA per padded query tile (blockIdx.x) and head (blockIdx.y); one warp
-// per row.
+// The same pass zeroes the tile's rows of the fp32 dQ accumulator (broadcast-Q:
+// the shared Q's rows, once, by the CTAs of sequence 0).
+// One CTA per padded query tile (blockIdx.x) and head (blockIdx.y). A row's
+// d elements are read 16 bytes per lane by a group of kRowLanes lanes, a warp
+// takes 32 / kRowLanes rows at a time, and every load of a warp's 16 rows is
+// issued before the first sum, so that 64 KB of a tile are in flight at once.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dout,
                                                       const float* __restrict__ lse, const int32_t* offsets,
                                                       const int32_t* tile_base, const int32_t* status, int batch,
                                                       int heads, int total, int bcast, int q_len, int pad_tiles,
-                                                      float* __restrict__ lse2p, float* __restrict__ deltap) {
+                                                      float* __restrict__ lse2p, float* __restrict__ deltap,
+                                                      float* __restrict__ dq_acc) {
   constexpr float kLog2e = 1.4426950408889634f;
+  constexpr int kChunks = D / 8;                                             // 16-byte chunks of a row
+  constexpr int kRowLanes = kChunks <= 8 ? 8 : (kChunks <= 16 ? 16 : 32);   // lanes per row (power of two)
+  constexpr int kRowsPerWarp = 32 / kRowLanes;
+  constexpr int kIters = (kTile / 8) / kRowsPerWarp;  // rows of a warp / rows per pass
   const int gt = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (status[0] != JFA_OK) return;
   // locate the tile: self -> (b, i) by binary search over tile_base; broadcast -> (b, i) directly
   int b, i, Lq;
-  int64_t qrow0, lse_base, pad_base;
+  int64_t qrow0, lse_base, pad_base, acc_row0;
   if (!bcast) {
     if (gt >= tile_base[batch]) return;
     int lo = 0, hi = batch;  // largest b with tile_base[b] <= gt
@@ -791,6 +800,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     qrow0 = s0 + static_cast<int64_t>(kTile) * i;
     lse_base = static_cast<int64_t>(h) * total + qrow0;
     pad_base = (static_cast<int64_t>(h) * pad_tiles + gt) * kTile;
+    acc_row0 = qrow0;
   } else {
     const int nqt = (q_len + kTile - 1) / kTile;
     b = gt / nqt;
@@ -800,26 +810,51 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     qrow0 = static_cast<int64_t>(b) * q_len + static_cast<int64_t>(kTile) * i;
     lse_base = (static_cast<int64_t>(b) * heads + h) * q_len + static_cast<int64_t>(kTile) * i;
     pad_base = ((static_cast<int64_t>(b) * heads + h) * nqt + i) * kTile;
+    acc_row0 = b == 0 ? static_cast<int64_t>(kTile) * i : -1;  // the shared Q's rows, zeroed once
   }
-  for (int r = warp; r < kTile; r += 8) {
-    const bool ok = kTile * i + r < Lq;
-    float acc = 0.f;
-    if (ok) {
-      const __nv_bfloat16* orow = o + ((qrow0 + r) * heads + h) * D;
-      const __nv_bfloat16* drow = dout + ((qrow0 + r) * heads + h) * D;
+  const int sub = lane / kRowLanes, cl = lane % kRowLanes;  // row within the pass, chunk lane
+  const int rows_valid = min(kTile, Lq - kTile * i);
+  constexpr int kBatch = kIters > 8 ? 8 : kIters;  // passes whose loads are in flight together
 #pragma unroll
-      for (int e = lane * 2; e < D; e += 64) {
-        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(orow + e);
-        const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(drow + e);
-        acc = fmaf(__bfloat162float(a.x), __bfloat162float(c.x), acc);
-        acc = fmaf(__bfloat162float(a.y), __bfloat162float(c.y), acc);
+  for (int i0 = 0; i0 < kIters; i0 += kBatch) {
+    uint4 a[kBatch], c[kBatch];
+#pragma unroll
+    for (int it = 0; it < kBatch; ++it) {
+      const int r = warp * (kTile / 8) + (i0 + it) * kRowsPerWarp + sub;
+      a[it] = make_uint4(0, 0, 0, 0);
+      c[it] = make_uint4(0, 0, 0, 0);
+      if (r < rows_valid && cl < kChunks) {
+        const int64_t off = ((qrow0 + r) * heads + h) * D + 8 * cl;
+        a[it] = ptx::ld_nc_v4(o + off);
+        c[it] = ptx::ld_nc_v4(dout + off);
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < kBatch; ++it) {
+      const int r = warp * (kTile / 8) + (i0 + it) * kRowsPerWarp + sub;
+      const uint32_t* av = reinterpret_cast<const uint32_t*>(&a[it]);
+      const uint32_t* cv = reinterpret_cast<const uint32_t*>(&c[it]);
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(ptx::bf16lo(av[e]), ptx::bf16lo(cv[e]), acc);
+        acc = fmaf(ptx::bf16hi(av[e]), ptx::bf16hi(cv[e]), acc);
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      for (int off = kRowLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (cl == 0) {
+        const bool ok = r < rows_valid;
+        deltap[pad_base + r] = ok ? -acc : 0.f;
+        lse2p[pad_base + r] = ok ? -lse[lse_base + r] * kLog2e : 0.f;
+      }
     }
-    if (lane == 0) {
-      deltap[pad_base + r] = ok ? -acc : 0.f;
-      lse2p[pad_base + r] = ok ? -lse[lse_base + r] * kLog2e : 0.f;
+  }
+  // zero this tile's rows of the dQ accumulator: one 16-byte store per thread per step
+  if (acc_row0 >= 0) {
+    constexpr int kRowStores = D / 4;  // float4 per row
+    for (int k = threadIdx.x; k < rows_valid * kRowStores; k += blockDim.x) {
+      const int r = k / kRowStores, e = k - r * kRowStores;
+      reinterpret_cast<float4*>(dq_acc + ((acc_row0 + r) * heads + h) * D)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 }
@@ -890,20 +925,20 @@ cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUt
 
 cudaError_t launch_bwd_pre(int head_dim, const void* o, const void* dout, const float* lse, const int32_t* offsets,
                            const int32_t* tile_base, const int32_t* status, int batch, int heads, int total, int bcast,
-                           int q_len, int pad_tiles, int grid_tiles, float* lse2p, float* deltap,
+                           int q_len, int pad_tiles, int grid_tiles, float* lse2p, float* deltap, float* dq_acc,
                            cudaStream_t stream) {
   dim3 grid(grid_tiles, heads);
   auto O = static_cast<const __nv_bfloat16*>(o);
   auto dO = static_cast<const __nv_bfloat16*>(dout);
   if (head_dim == 64)
     bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, status, batch, heads, total, bcast,
-                                                 q_len, pad_tiles, lse2p, deltap);
+                                                 q_len, pad_tiles, lse2p, deltap, dq_acc);
   else if (head_dim == 128)
     bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, status, batch, heads, total, bcast,
-                                                  q_len, pad_tiles, lse2p, deltap);
+                                                  q_len, pad_tiles, lse2p, deltap, dq_acc);
   else if (head_dim == 192)
     bwd_pre_kernel<192><<<grid, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, status, batch, heads, total, bcast,
-                                                  q_len, pad_tiles, lse2p, deltap);
+                                                  q_len, pad_tiles, lse2p, deltap, dq_acc);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

@@ -108,9 +108,11 @@ cudaError_t launch_fwd_stream(bool causal, const CUtensorMap& tq, const CUtensor
 cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                             const CUtensorMap& tdv, cudaStream_t stream);
+// Also zeroes the fp32 dQ accumulator dq_acc ([rows, H*D]: the sequences' rows, or the
+// shared Q's rows for broadcast-Q).
 cudaError_t launch_bwd_pre(int head_dim, const void* o, const void* dout, const float* lse, const int32_t* offsets,
                            const int32_t* tile_base, const int32_t* status, int batch, int heads, int total, int bcast,
-                           int q_len, int pad_tiles, int grid_tiles, float* lse2p, float* deltap,
+                           int q_len, int pad_tiles, int grid_tiles, float* lse2p, float* deltap, float* dq_acc,
                            cudaStream_t stream);
 cudaError_t launch_bwd_post(const float* acc, void* dq, int64_t n, float scale, const int32_t* status, int sms,
                             cudaStream_t stream);
