@@ -182,18 +182,17 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
   // sequence starts and every thread then writes its own sequences' items,
   // so that one large bucket is not written by one warp.
   const bool one_cost = !(p.causal && (p.mode == kQueueSelfFwd || p.mode == kQueueSelfBwd));
+  // The items fit the queue (checked once here; every write below is in range).
+  const bool fits = static_cast<int64_t>(total_tiles) * p.heads <= p.max_items;
   auto write_items = [&](int b, int first, int c, int tf, int k, int L) {
-    const int s0 = p.offsets[b];
-    const int tb = p.tile_base ? p.tile_base[b] : 0;
-    for (int r = 0; r < c; ++r) {
-      const int64_t slot = static_cast<int64_t>(first + r) * p.heads;
-      for (int h = 0; h < p.heads; ++h) {
-        if (slot + h < p.max_items) {
-          p.items[slot + h] = make_int4(b, h, tf + r, k);
-          if (p.item_seq) p.item_seq[slot + h] = make_int4(s0, L, tb, 0);
-        }
-      }
-    }
+    if (!fits) return;
+    const int4 seq = make_int4(p.offsets[b], L, p.tile_base ? p.tile_base[b] : 0, 0);
+    int4* it = p.items + static_cast<int64_t>(first) * p.heads;
+    int4* sq = p.item_seq ? p.item_seq + static_cast<int64_t>(first) * p.heads : nullptr;
+    for (int r = 0; r < c; ++r)
+      for (int h = 0; h < p.heads; ++h) *it++ = make_int4(b, h, tf + r, k);
+    if (sq)
+      for (int e = 0; e < c * p.heads; ++e) *sq++ = seq;
   };
   for (int k = kmin + warp; k <= kmax; k += kWarps) {
     int run = s_start[k];
@@ -232,7 +231,7 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
   if (tid == 0) {
     int64_t n_items = static_cast<int64_t>(total_tiles) * p.heads;
     int64_t n_busy = static_cast<int64_t>(busy_tiles) * p.heads;
-    if (n_items > p.max_items) {
+    if (!fits) {
       if (atomicCAS(p.status, JFA_OK, JFA_ERR_BAD_INPUT) == JFA_OK) p.status[1] = kSiteQueueOffsets;
       n_items = 0;
       n_busy = 0;
