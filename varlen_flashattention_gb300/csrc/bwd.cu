@@ -24,8 +24,9 @@
 //    sub-partition run them almost twice as fast while the tensor core is
 //    busy) turn S^T into P^T (bf16, packed over the S^T columns each group has
 //    read) and dP^T into dS^T (bf16, written to shared memory in the
-//    128B-swizzled layout the tensor core reads as dS for dQ, and packed into
-//    TMEM over the dP^T columns each group has read, as dS^T for dK);
+//    128B-swizzled layout the tensor core reads as dS for dQ and as dS^T for
+//    dK; with a single stage also packed into TMEM over the dP^T columns each
+//    group has read, as dS^T for dK);
 //  * warps 10-13 drain dQ from TMEM into an fp32 accumulator (the cross-CTA
 //    reduction; contended in broadcast-Q) and write dK and dV at the end of
 //    each item. dQ is staged, in 128B-swizzled fp32 boxes, in the dO stage
@@ -40,12 +41,13 @@
 //    use for TMEM and shared memory;
 //  * warp 8 = TMA producer, warp 9 = MMA issuer; 448 threads, so a thread has
 //    at most 128 registers.
-//  * Order inside one query tile: dP^T, dV, [S^T of the next tile], dK, dQ,
-//    so that the softmax of the next tile overlaps the dK / dQ MMAs. With a
-//    single Q/dO stage (head_dim 192) the next tile's Q arrives only after
-//    this tile's dQ has been staged out of the stage, so there S^T is issued
-//    at the start of its own tile (TwelveLabs, bug hunting: the single-stage
-//    deadlock).
+//  * Order inside one query tile: dP^T, dV, dQ, [S^T of the next tile], dK:
+//    dQ goes first so that its drain runs under the S^T and dK MMAs, and the
+//    softmax of the next tile overlaps dK. With a single Q/dO stage (head_dim
+//    192) the next tile's Q arrives only after this tile's dQ has been staged
+//    out of the stage, so there S^T is issued at the start of its own tile
+//    (TwelveLabs, bug hunting: the single-stage deadlock), dK (from TMEM)
+//    precedes dQ, and the stage is released between them.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -374,30 +376,54 @@ __global__ void __launch_bounds__(448, 1)
         if (!(ok = wait(ds_full, x & 1, kSiteBwdMmaDS))) break;
         ptx::tc_fence_after();
         if (ptx::elect_one()) {
-          // the S^T columns are free: dV has been issued and the softmax has read P^T back
-          if (next_s) issue_s((pos + 1) % kSt);
-          // dK += dS^T Q[:, slice], dS^T from TMEM (each group's 64 query columns
-          // packed over the first 32 of its dP^T columns)
+          // dQ(tile) = dS K[:, slice] into the dP^T columns (the softmax has read dP^T)
+          auto mma_dq = [&]() {
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            ptx::mma_ts(tmem + Lay::kColDK, tmem + Lay::kColDP + 64 * (kk >> 2) + 8 * (kk & 3),
-                        ptx::sdesc_sw128(q_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdAcc,
-                        (ii > 0 || kk > 0) ? 1u : 0u);
-          }
-          // dK is the last reader of Q (the softmax read the rows before dS^T);
-          // the last tile's stage is released by the epilogue, which stages dK
-          // and dV there
-          if (!(kStageInDO && ii + 1 == I.nq)) ptx::mma_commit(q_empty + st);
-          if (!kStageInDO) ptx::mma_commit(do_empty + st);  // single stage: dO is free too (dV read it)
-          // dQ(tile) = dS K[:, slice] into the dP^T columns
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+              ptx::mma_ss(tmem + Lay::kColDP, ptx::sdesc_sw128(ds_addr + kk * 2048, 16384, 1024),
+                          ptx::sdesc_sw128(k_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdDQ,
+                          kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(dq_full);
+          };
+          // dK += dS^T Q[:, slice]: dS^T from the swizzled shared-memory copy
+          // (K-major view), or with one stage from its TMEM copy (each group's
+          // 64 query columns packed over the first 32 of its dP^T columns)
+          auto mma_dk = [&]() {
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            ptx::mma_ss(tmem + Lay::kColDP, ptx::sdesc_sw128(ds_addr + kk * 2048, 16384, 1024),
-                        ptx::sdesc_sw128(k_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdDQ,
-                        kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+              const uint64_t q_desc = ptx::sdesc_sw128(q_addr + I.c * 16384 + kk * 2048, 16384, 1024);
+              if (kStageInDO) {
+                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                ptx::mma_ss(tmem + Lay::kColDK, ptx::sdesc_sw128(ds_addr + off, 16, 1024), q_desc, kIdAcc,
+                            (ii > 0 || kk > 0) ? 1u : 0u);
+              } else {
+                ptx::mma_ts(tmem + Lay::kColDK, tmem + Lay::kColDP + 64 * (kk >> 2) + 8 * (kk & 3), q_desc, kIdAcc,
+                            (ii > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+          };
+          if (kStageInDO) {
+            // dQ first, so that its drain (staged in this tile's dO buffer)
+            // overlaps the next S^T and dK; the S^T columns are free once dV has
+            // been issued and the softmax has read P^T back. dK is the last
+            // reader of Q (the softmax read the rows before dS^T); the last
+            // tile's stage is released by the epilogue, which stages dK and dV
+            // there.
+            mma_dq();
+            if (next_s) issue_s((pos + 1) % kSt);
+            mma_dk();
+            if (ii + 1 < I.nq) ptx::mma_commit(q_empty + st);
+          } else {
+            // one stage: dQ is staged in the dS buffer, so dK reads dS first;
+            // the stage (Q read by dK, dO by dV) goes back to the producer
+            // before dQ, as the next tile's S^T waits for it
+            mma_dk();
+            ptx::mma_commit(q_empty + st);
+            ptx::mma_commit(do_empty + st);
+            mma_dq();
           }
-          ptx::mma_commit(dq_full);  // with two stages the drain stages dQ in this dO stage, then releases it
-          ptx::mma_commit(ds_free);
+          ptx::mma_commit(ds_free);  // dQ and dK have read dS
         }
         __syncwarp();
         ++pos;
@@ -508,7 +534,7 @@ __global__ void __launch_bounds__(448, 1)
         for (int k = 0; k < 2; ++k) {  // two chunks of 32 query columns
           uint32_t dp[32];
           uint32_t pp[16];
-          uint32_t dsw[16];
+          uint32_t dsw[16];  // dS^T for the TMEM copy (one stage only)
           ptx::tmem_ld32(dp_cols + 32 * k, dp);
           ptx::tmem_ld16(s_cols + 16 * k, pp);
           ptx::tmem_ld_wait();
@@ -532,16 +558,16 @@ __global__ void __launch_bounds__(448, 1)
               float s0, s1;
               ptx::f2_unpack(ptx::f2_mul(ptx::f2_packf(ptx::bf16lo(pw), ptx::bf16hi(pw)), d2), s0, s1);
               w[e] = ptx::pack_bf16(s0, s1);
-              dsw[4 * c4 + e] = w[e];
+              if constexpr (!kStageInDO) dsw[4 * c4 + e] = w[e];
             }
             uint4* dst = reinterpret_cast<uint4*>(ds_row + ((ch ^ sw) << 4));
             *dst = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          // dS^T of these 32 query columns, two bf16 per column, over dP^T
-          // columns this thread has read: the A operand of dK = dS^T Q
-          ptx::tmem_st16(dp_cols + 16 * k, dsw);
+          // one stage: dS^T of these 32 query columns, two bf16 per column, over
+          // dP^T columns this thread has read (the A operand of dK from TMEM)
+          if constexpr (!kStageInDO) ptx::tmem_st16(dp_cols + 16 * k, dsw);
         }
-        ptx::tmem_st_wait();
+        if constexpr (!kStageInDO) ptx::tmem_st_wait();
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncwarp();
