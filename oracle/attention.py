@@ -23,6 +23,15 @@ the definitions, materialising S and P per (sequence, head) in fp64:
       dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
 * Broadcast-Q. aivexanews page, third paragraph: one dense Q is shared by the
   whole batch, so dQ is the sum over the batch of the per-sequence dQ.
+* Jagged attention with separate query and key lengths and grouped-query
+  heads. "Cutting-edge isn't plug-and-play: customizing FA4 on B300"
+  (TwelveLabs), section on why the development succeeded, second factor: the
+  test suite the kernel had to pass spans MHA / GQA / MQA head layouts,
+  causal and non-causal masks and varlen packing; "Optimizing FlashAttention-4
+  for Efficient Inference" (hpjadul), section "PR 2186": several query heads
+  share one KV head. Sequence b has its query rows at q_offsets[b] .. and its
+  key rows at k_offsets[b] ..; query head h reads KV head h // (Hq / Hkv); dK
+  and dV of a KV head sum over the query heads of its group.
 * Paged split-KV GQA decode. "Optimizing FlashAttention-4 for Efficient
   Inference" (hpjadul), sections "PR 1940" (parallelism across the KV
   dimension), "PR 1999 and PR 2104" (arbitrary KV page sizes) and "PR 2186"
@@ -35,6 +44,9 @@ the definitions, materialising S and P per (sequence, head) in fp64:
 Conventions where the pages are silent (readings, not statements of the pages):
   * an empty key set gives O = 0 and LSE = -inf (and zero gradients);
   * causal means L_q == L_k and key j is visible to query i iff j <= i;
+  * with L_q != L_k (varlen functions), causal aligns the mask to the bottom
+    right: key j is visible to query i iff j <= i + (L_k - L_q), so the last
+    query sees every key; query rows that see no key get O = 0, LSE = -inf;
   * split bounds: c_b = ceil(L_b / S); split s covers [s c_b, min((s+1) c_b, L_b)).
 
 Inputs are numpy arrays of float64 (bf16 values upcast exactly by the caller)
@@ -50,6 +62,7 @@ __all__ = [
     "broadcast_forward", "broadcast_backward",
     "split_bounds", "gather_paged", "decode_forward", "decode_split_partials",
     "merge_partials", "tile_queue",
+    "lower_right_visible", "varlen_forward", "varlen_backward", "varlen_tile_queue",
 ]
 
 
@@ -297,5 +310,115 @@ def tile_queue(offsets, heads, causal, kind, tile=128):
                 cost = nt - t
             for h in range(heads):
                 items.append((-cost, b, t, h))
+    items.sort()
+    return [(b, h, t) for (_, b, t, h) in items]
+
+
+# ----------------------------------------------------------------------------
+# Varlen attention: separate query / key lengths, grouped-query heads
+# ----------------------------------------------------------------------------
+
+def lower_right_visible(Lq, Lk):
+    """bool [Lq, Lk]: key j is visible to query i iff j <= i + (Lk - Lq)
+    (bottom-right aligned causal mask; equal to the lower triangle when
+    Lq == Lk)."""
+    i = np.arange(Lq)[:, None]
+    j = np.arange(Lk)[None, :]
+    return j <= i + (Lk - Lq)
+
+
+def _var_scores(Qh, Kh, scale, causal):
+    S = scale * (Qh @ Kh.T)
+    if causal:
+        S = np.where(lower_right_visible(S.shape[0], S.shape[1]), S, -np.inf)
+    return S
+
+
+def _check_heads(q, k):
+    Hq, Hkv = q.shape[1], k.shape[1]
+    assert Hkv >= 1 and Hq % Hkv == 0, "query heads must be a multiple of KV heads"
+    return Hq // Hkv
+
+
+def varlen_forward(q, k, v, q_offsets, k_offsets, scale, causal=False):
+    """Jagged attention with separate query / key packing and grouped heads.
+
+    q [total_q, Hq, d], k and v [total_k, Hkv, d]; q_offsets and k_offsets are
+    int [B+1]. Query head h of sequence b attends to KV head h // (Hq / Hkv)
+    of the same sequence. Returns O [total_q, Hq, d] and LSE [Hq, total_q];
+    a query row with no visible key has O = 0 and LSE = -inf."""
+    group = _check_heads(q, k)
+    Hq = q.shape[1]
+    qr, kr = seq_ranges(q_offsets), seq_ranges(k_offsets)
+    assert len(qr) == len(kr), "q_offsets and k_offsets must describe the same batch"
+    O = np.zeros((q.shape[0], Hq, v.shape[2]), dtype=np.float64)
+    LSE = np.full((Hq, q.shape[0]), -np.inf, dtype=np.float64)
+    for (qs, qe), (ks, ke) in zip(qr, kr):
+        if qe == qs or ke == ks:
+            continue
+        for h in range(Hq):
+            g = h // group
+            S = _var_scores(q[qs:qe, h], k[ks:ke, g], scale, causal)
+            P, lse = _softmax_rows(S)
+            O[qs:qe, h] = P @ v[ks:ke, g]
+            LSE[h, qs:qe] = lse
+    return O, LSE
+
+
+def varlen_backward(q, k, v, do, q_offsets, k_offsets, scale, causal=False):
+    """Exact gradient of varlen_forward's O against dO: per (sequence, query
+    head) dV = P^T dO, dP = dO V^T, D = rowsum(dO * O), dS = P * (dP - D),
+    dQ = scale dS K, dK = scale dS^T Q; a KV head's dK and dV are the sums
+    over the query heads that read it. Returns dQ [total_q, Hq, d],
+    dK and dV [total_k, Hkv, d]."""
+    group = _check_heads(q, k)
+    Hq = q.shape[1]
+    dQ = np.zeros_like(q, dtype=np.float64)
+    dK = np.zeros_like(k, dtype=np.float64)
+    dV = np.zeros_like(v, dtype=np.float64)
+    for (qs, qe), (ks, ke) in zip(seq_ranges(q_offsets), seq_ranges(k_offsets)):
+        if qe == qs or ke == ks:
+            continue
+        for h in range(Hq):
+            g = h // group
+            Qh, Kh, Vh, dOh = q[qs:qe, h], k[ks:ke, g], v[ks:ke, g], do[qs:qe, h]
+            S = _var_scores(Qh, Kh, scale, causal)
+            P, _ = _softmax_rows(S)
+            O = P @ Vh
+            dP = dOh @ Vh.T
+            D = np.sum(dOh * O, axis=1)
+            dS = P * (dP - D[:, None])
+            dQ[qs:qe, h] = scale * (dS @ Kh)
+            dK[ks:ke, g] += scale * (dS.T @ Qh)
+            dV[ks:ke, g] += P.T @ dOh
+    return dQ, dK, dV
+
+
+def varlen_tile_queue(q_offsets, k_offsets, q_heads, kv_heads, causal, kind, tile=128):
+    """Longest-first work order for varlen attention (same rule as tile_queue).
+
+    kind="fwd": items (b, h, t) for query head h and query tile t; cost = the
+    key tiles holding at least one key visible to a row of the tile.
+    kind="bwd": items (b, g, u) for KV head g and key tile u; cost = (Hq / Hkv)
+    x the query tiles holding at least one query that sees a key of the tile.
+    Items of cost 0 are kept (their outputs are zero). Sorted by descending
+    cost, ties by ascending (b, tile, head). Returns a list of (b, head, tile)."""
+    group = q_heads // kv_heads
+    items = []
+    for b, ((qs, qe), (ks, ke)) in enumerate(zip(seq_ranges(q_offsets), seq_ranges(k_offsets))):
+        Lq, Lk = qe - qs, ke - ks
+        vis = lower_right_visible(Lq, Lk) if causal else np.ones((Lq, Lk), dtype=bool)
+        nq, nk = -(-Lq // tile), -(-Lk // tile)
+        if kind == "fwd":
+            for t in range(nq):
+                cost = sum(bool(vis[t * tile:(t + 1) * tile, u * tile:(u + 1) * tile].any()) for u in range(nk))
+                for h in range(q_heads):
+                    items.append((-cost, b, t, h))
+        else:
+            for u in range(nk):
+                cost = group * sum(bool(vis[t * tile:(t + 1) * tile, u * tile:(u + 1) * tile].any())
+                                   for t in range(nq))
+                for g in range(kv_heads):
+                    items.append((-cost, b, u, g))
     items.sort()
     return [(b, h, t) for (_, b, t, h) in items]

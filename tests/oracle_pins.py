@@ -386,4 +386,161 @@ def pin_tile_queue(o):
             assert keys == sorted(keys), (causal, kind)
 
 
+
+# ---------------------------------------------------------------- varlen / GQA
+
+def _lower_right_library(Lq, Lk):
+    """torch's own bottom-right causal mask (torch.nn.attention.bias)."""
+    import warnings
+
+    from torch.nn.attention.bias import causal_lower_right
+    with warnings.catch_warnings():  # torch warns about SDPA on L_q > L_k; only the mask is used here
+        warnings.simplefilter("ignore")
+        return causal_lower_right(Lq, Lk)._materialize(device=torch.device("cpu"))
+
+
+def pin_varlen_torch_lower_right(o):
+    """torch fp64 SDPA with torch's lower-right causal mask (or no mask), K/V
+    heads expanded by repeat_interleave, and autograd through that expansion
+    (which sums dK/dV over a group): a library special case per sequence.
+    Every query row here sees at least one key."""
+    r = _rng(21)
+    q_lens, k_lens = [3, 5, 1, 8], [7, 5, 4, 9]
+    Hq, Hkv, d = 4, 2, 3
+    qo = np.concatenate([[0], np.cumsum(q_lens)])
+    ko = np.concatenate([[0], np.cumsum(k_lens)])
+    scale = 0.7
+    for causal in (False, True):
+        q, do = r.standard_normal((qo[-1], Hq, d)), r.standard_normal((qo[-1], Hq, d))
+        k, v = r.standard_normal((ko[-1], Hkv, d)), r.standard_normal((ko[-1], Hkv, d))
+        O, LSE = o.varlen_forward(q, k, v, qo, ko, scale, causal)
+        dQ, dK, dV = o.varlen_backward(q, k, v, do, qo, ko, scale, causal)
+        for b in range(len(q_lens)):
+            q0, q1, k0, k1 = qo[b], qo[b + 1], ko[b], ko[b + 1]
+            tq, tk, tv = (torch.tensor(x.transpose(1, 0, 2), requires_grad=True)
+                          for x in (q[q0:q1], k[k0:k1], v[k0:k1]))
+            ek, ev = (t.repeat_interleave(Hq // Hkv, dim=0) for t in (tk, tv))
+            mask = _lower_right_library(q1 - q0, k1 - k0) if causal else None
+            out = torch.nn.functional.scaled_dot_product_attention(tq, ek, ev, attn_mask=mask, scale=scale)
+            out.backward(torch.tensor(do[q0:q1].transpose(1, 0, 2)))
+            _close(O[q0:q1], out.detach().numpy().transpose(1, 0, 2), 1e-12, "varlen sdpa O")
+            _close(dQ[q0:q1], tq.grad.numpy().transpose(1, 0, 2), 1e-12, "varlen autograd dQ")
+            _close(dK[k0:k1], tk.grad.numpy().transpose(1, 0, 2), 1e-12, "varlen autograd dK")
+            _close(dV[k0:k1], tv.grad.numpy().transpose(1, 0, 2), 1e-12, "varlen autograd dV")
+            S = scale * torch.einsum("hid,hjd->hij", tq.detach(), ek.detach())
+            if causal:
+                S = S.masked_fill(~mask, float("-inf"))
+            _close(LSE[:, q0:q1], torch.logsumexp(S, dim=-1).numpy(), 1e-12, "varlen logsumexp")
+
+
+def pin_varlen_brute_force(o):
+    """Pure-Python loops with the visibility rule of a query block that ends
+    where the keys end (query i of L_q sits at key position i + L_k - L_q),
+    including L_q > L_k, where the first L_q - L_k rows see nothing
+    (O = 0, LSE = -inf)."""
+    r = _rng(22)
+    q_lens, k_lens = [5, 2, 3], [2, 6, 0]
+    Hq, Hkv, d = 3, 1, 2
+    qo = np.concatenate([[0], np.cumsum(q_lens)])
+    ko = np.concatenate([[0], np.cumsum(k_lens)])
+    q = r.standard_normal((qo[-1], Hq, d))
+    k, v = r.standard_normal((ko[-1], Hkv, d)), r.standard_normal((ko[-1], Hkv, d))
+    for causal in (False, True):
+        O, LSE = o.varlen_forward(q, k, v, qo, ko, 0.9, causal)
+        for b in range(len(q_lens)):
+            Lq, Lk = q_lens[b], k_lens[b]
+            for h in range(Hq):
+                for i in range(Lq):
+                    pos = i + Lk - Lq  # the query's position on the key axis
+                    keys = [j for j in range(Lk) if (not causal) or j <= pos]
+                    qi = q[qo[b] + i, h]
+                    if not keys:
+                        assert np.all(O[qo[b] + i, h] == 0.0) and LSE[h, qo[b] + i] == -np.inf
+                        continue
+                    s = [0.9 * sum(qi[c] * k[ko[b] + j, 0, c] for c in range(d)) for j in keys]
+                    z = sum(math.exp(x) for x in s)
+                    out = [sum(math.exp(s[n]) / z * v[ko[b] + j, 0, c] for n, j in enumerate(keys))
+                           for c in range(d)]
+                    _close(O[qo[b] + i, h], out, 1e-13, "varlen brute-force O")
+                    _close(LSE[h, qo[b] + i], math.log(z), 1e-13, "varlen brute-force LSE")
+
+
+def pin_varlen_finite_differences(o):
+    """Central differences (h = 1e-6) of sum(O * dO) for a grouped, bottom-right
+    causal case with L_q != L_k: the gradient of a KV head must collect every
+    query head of its group."""
+    r = _rng(23)
+    q_lens, k_lens = [2, 4], [3, 2]
+    Hq, Hkv, d = 4, 2, 2
+    qo = np.concatenate([[0], np.cumsum(q_lens)])
+    ko = np.concatenate([[0], np.cumsum(k_lens)])
+    q, do = r.standard_normal((qo[-1], Hq, d)), r.standard_normal((qo[-1], Hq, d))
+    k, v = r.standard_normal((ko[-1], Hkv, d)), r.standard_normal((ko[-1], Hkv, d))
+
+    def loss():
+        O, _ = o.varlen_forward(q, k, v, qo, ko, 0.8, True)
+        return float(np.sum(O * do))
+    grads = o.varlen_backward(q, k, v, do, qo, ko, 0.8, True)
+    for name, x, g in (("q", q, grads[0]), ("k", k, grads[1]), ("v", v, grads[2])):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + 1e-6
+            fp = loss()
+            x[idx] = old - 1e-6
+            fm = loss()
+            x[idx] = old
+            num[idx] = (fp - fm) / 2e-6
+        rel = np.max(np.abs(num - g)) / max(np.max(np.abs(g)), 1e-30)
+        assert rel < 1e-6, f"varlen d{name} rel err {rel:.2e}"
+
+
+def pin_varlen_reduces_to_self(o):
+    """With q_offsets == k_offsets and Hkv == Hq, varlen attention is jagged
+    self-attention (top-left and bottom-right masks coincide when L_q == L_k)."""
+    r = _rng(24)
+    lengths = [4, 0, 7, 1]
+    off = np.concatenate([[0], np.cumsum(lengths)])
+    q, k, v, do = (r.standard_normal((off[-1], 2, 3)) for _ in range(4))
+    for causal in (False, True):
+        O1, L1 = o.attention_forward(q, k, v, off, 0.6, causal)
+        O2, L2 = o.varlen_forward(q, k, v, off, off, 0.6, causal)
+        _close(O2, O1, 1e-14, "varlen self O")
+        _close(L2, L1, 1e-14, "varlen self LSE")
+        g1 = o.attention_backward(q, k, v, do, off, 0.6, causal)
+        g2 = o.varlen_backward(q, k, v, do, off, off, 0.6, causal)
+        for a, b_ in zip(g2, g1[:3]):
+            _close(a, b_, 1e-14, "varlen self grads")
+
+
+def pin_varlen_tile_queue(o):
+    """Every item appears once; costs never increase; ties go by ascending
+    (b, tile, head); each cost is recounted from torch's lower-right mask,
+    max-pooled over 128 x 128 blocks (a block counts when it holds any
+    visible pair)."""
+    qo = np.array([0, 300, 300, 301, 700, 1000, 1100])
+    ko = np.array([0, 100, 400, 700, 700, 1300, 1350])
+    Hq, Hkv, T = 4, 2, 128
+    for causal in (False, True):
+        for kind in ("fwd", "bwd"):
+            got = o.varlen_tile_queue(qo, ko, Hq, Hkv, causal, kind, T)
+            heads = Hq if kind == "fwd" else Hkv
+            expect_cost = {}
+            for b in range(len(qo) - 1):
+                Lq, Lk = int(qo[b + 1] - qo[b]), int(ko[b + 1] - ko[b])
+                nq, nk = -(-Lq // T), -(-Lk // T)
+                if Lq and Lk:
+                    m = _lower_right_library(Lq, Lk) if causal else torch.ones(Lq, Lk, dtype=torch.bool)
+                    blocks = torch.nn.functional.max_pool2d(m[None, None].double(), T, T, ceil_mode=True)[0, 0] > 0
+                else:
+                    blocks = torch.zeros(nq, nk, dtype=torch.bool)
+                for t in range(nq if kind == "fwd" else nk):
+                    c = int(blocks[t].sum()) if kind == "fwd" else (Hq // Hkv) * int(blocks[:, t].sum())
+                    for h in range(heads):
+                        expect_cost[(b, h, t)] = c
+            assert len(got) == len(expect_cost) and set(got) == set(expect_cost), (causal, kind)
+            keys = [(-expect_cost[it], it[0], it[2], it[1]) for it in got]
+            assert keys == sorted(keys), (causal, kind)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -128,6 +128,37 @@ def _queue_ascending(m):
     m.tile_queue = q
 
 
+def _varlen_top_left(m):
+    # aligns the varlen causal mask to the top left (j <= i) instead of the bottom right
+    def vis(Lq, Lk):
+        return np.arange(Lk)[None, :] <= np.arange(Lq)[:, None]
+    m.lower_right_visible = vis
+
+
+def _varlen_gqa_modulo(m):
+    # query head h reads KV head h % Hkv instead of h // (Hq / Hkv)
+    def fwd(q, k, v, qo, ko, scale, causal=False):
+        Hq, Hkv = q.shape[1], k.shape[1]
+        perm = [h % Hkv for h in range(Hq)]
+        kk = k[:, perm]
+        vv = v[:, perm]
+        return real_oracle.varlen_forward(q, kk, vv, qo, ko, scale, causal)
+    m.varlen_forward = fwd
+
+
+def _varlen_dk_last_head(m):
+    # a KV head's dK keeps only the last query head of its group
+    def bwd(q, k, v, do, qo, ko, scale, causal=False):
+        Hq, Hkv = q.shape[1], k.shape[1]
+        G = Hq // Hkv
+        dQ, dK, dV = real_oracle.varlen_backward(q, k, v, do, qo, ko, scale, causal)
+        kk = np.repeat(k, G, axis=1)
+        vv = np.repeat(v, G, axis=1)
+        _, dK1, _ = real_oracle.varlen_backward(q, kk, vv, do, qo, ko, scale, causal)
+        return dQ, dK1[:, G - 1::G], dV
+    m.varlen_backward = bwd
+
+
 MUTANTS = {
     "bwd_drop_delta": _bwd_variant("drop_delta"),
     "bwd_sign_dS": _bwd_variant("sign_dS"),
@@ -141,6 +172,9 @@ MUTANTS = {
     "gqa_wrong_group": _gqa_wrong_group,
     "page_slot_off_by_one": _page_slot_off_by_one,
     "queue_ascending": _queue_ascending,
+    "varlen_top_left": _varlen_top_left,
+    "varlen_gqa_modulo": _varlen_gqa_modulo,
+    "varlen_dk_last_head": _varlen_dk_last_head,
 }
 
 
