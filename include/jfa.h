@@ -161,6 +161,69 @@ typedef struct {
   void* main_kernel_events;
 } jfa_bcast_bwd_args;
 
+/* ------------------------------------------------------------------ varlen / GQA
+ * Jagged attention whose query and key sequences have their own lengths and
+ * whose query heads share KV heads ([B300] section on why the development
+ * succeeded, second factor: MHA / GQA / MQA head layouts, causal and
+ * non-causal masks and varlen packing are the surface the kernel must cover;
+ * [INF] PR 2186: several query heads are processed against one KV head).
+ * Sequence b has query rows q_offsets[b] .. q_offsets[b+1]-1 and key/value
+ * rows k_offsets[b] .. k_offsets[b+1]-1 (L_q and L_k, either may be 0).
+ * Query head h reads KV head h / (q_heads / kv_heads). For every b and h:
+ *   S = scale * Q_b,h K_b,g^T, P = softmax_rows(S), O = P V_b,g,
+ *   LSE_i = ln sum_j exp(S_ij).
+ * causal = 1 aligns the mask to the bottom right (the pages state no
+ * alignment for L_q != L_k; this is the reading where a query block is the
+ * end of its key sequence): key j is visible to query i iff
+ * j <= i + (L_k - L_q). With L_q == L_k this is the self-attention mask.
+ * A query row that sees no key (L_k = 0, or i < L_q - L_k when causal) gets
+ * O = 0 and LSE = -inf, and contributes no gradient.
+ * head_dim 64, 128 or 192; q_heads must be a multiple of kv_heads. */
+typedef struct {
+  const void* q;              /* bf16 [total_q, q_heads, head_dim] */
+  const void* k;              /* bf16 [total_k, kv_heads, head_dim] */
+  const void* v;              /* bf16 [total_k, kv_heads, head_dim] */
+  const int32_t* q_offsets;   /* int32 [batch+1], device */
+  const int32_t* k_offsets;   /* int32 [batch+1], device */
+  int32_t batch;              /* >= 0 */
+  int32_t q_heads;            /* >= 1 */
+  int32_t kv_heads;           /* >= 1, divides q_heads */
+  int32_t head_dim;           /* 64, 128 or 192 */
+  int32_t max_seqlen_q;       /* host: >= every L_q */
+  int32_t max_seqlen_k;       /* host: >= every L_k */
+  int32_t total_q;            /* host: q_offsets[batch] */
+  int32_t total_k;            /* host: k_offsets[batch] */
+  float scale;
+  int32_t causal;             /* 0, or 1 = bottom-right aligned (see above) */
+  void* o;                    /* out: bf16 [total_q, q_heads, head_dim] */
+  float* lse;                 /* out: fp32 [q_heads, total_q] */
+  void* main_kernel_events;   /* optional cudaEvent_t[2] */
+} jfa_varlen_fwd_args;
+
+/* Backward of jfa_fwd_varlen (same recompute scheme as jfa_bwd). dK and dV of
+ * a KV head are summed over the q_heads / kv_heads query heads that read it
+ * (accumulated on chip, no atomics); dQ as in jfa_bwd. head_dim 192 runs
+ * head-axis chunked (head_chunk 64). */
+typedef struct {
+  const void* q;              /* bf16 [total_q, q_heads, head_dim] */
+  const void* k;              /* bf16 [total_k, kv_heads, head_dim] */
+  const void* v;              /* bf16 [total_k, kv_heads, head_dim] */
+  const void* o;              /* bf16 [total_q, q_heads, head_dim], forward output */
+  const void* dout;           /* bf16 [total_q, q_heads, head_dim] */
+  const float* lse;           /* fp32 [q_heads, total_q], forward LSE */
+  const int32_t* q_offsets;   /* int32 [batch+1], device */
+  const int32_t* k_offsets;   /* int32 [batch+1], device */
+  int32_t batch, q_heads, kv_heads, head_dim;
+  int32_t max_seqlen_q, max_seqlen_k, total_q, total_k;
+  float scale;
+  int32_t causal;
+  int32_t head_chunk;         /* 0 = automatic (64 for head_dim 192, else head_dim) */
+  void* dq;                   /* out: bf16 [total_q, q_heads, head_dim] */
+  void* dk;                   /* out: bf16 [total_k, kv_heads, head_dim] */
+  void* dv;                   /* out: bf16 [total_k, kv_heads, head_dim] */
+  void* main_kernel_events;   /* optional cudaEvent_t[2] */
+} jfa_varlen_bwd_args;
+
 /* ------------------------------------------------------------------ paged decode
  * One query token per sequence against a paged KV cache ([INF] PR 1999/2104:
  * pages of any size >= 1; PR 2186: the q_heads/kv_heads query heads that share
@@ -198,6 +261,8 @@ JFA_API size_t jfa_bwd_workspace_size(const jfa_bwd_args* args);
 JFA_API size_t jfa_bcast_fwd_workspace_size(const jfa_bcast_fwd_args* args);
 JFA_API size_t jfa_bcast_bwd_workspace_size(const jfa_bcast_bwd_args* args);
 JFA_API size_t jfa_decode_workspace_size(const jfa_decode_args* args);
+JFA_API size_t jfa_varlen_fwd_workspace_size(const jfa_varlen_fwd_args* args);
+JFA_API size_t jfa_varlen_bwd_workspace_size(const jfa_varlen_bwd_args* args);
 
 /* Entry points. `workspace` is device memory of at least the size above,
  * 256-byte aligned; its contents on entry do not matter. */
@@ -209,6 +274,10 @@ JFA_API jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* args, void* wor
                                cudaStream_t stream);
 JFA_API jfa_status jfa_decode_splitkv(const jfa_decode_args* args, void* workspace, size_t workspace_bytes,
                               cudaStream_t stream);
+JFA_API jfa_status jfa_fwd_varlen(const jfa_varlen_fwd_args* args, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+JFA_API jfa_status jfa_bwd_varlen(const jfa_varlen_bwd_args* args, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
 
 /* Paged split-KV decode that allocates nothing. The pages have no
  * counterpart for this entry point; it exists for callers that cannot

@@ -23,6 +23,8 @@ STRUCTS = {
     "jfa_bcast_fwd_args": _abi.BcastFwdArgs,
     "jfa_bcast_bwd_args": _abi.BcastBwdArgs,
     "jfa_decode_args": _abi.DecodeArgs,
+    "jfa_varlen_fwd_args": _abi.VarlenFwdArgs,
+    "jfa_varlen_bwd_args": _abi.VarlenBwdArgs,
 }
 
 
@@ -136,6 +138,39 @@ def test_decode_validation(lib):
     need = lib.jfa_decode_workspace_size(P(args()))
     assert need >= 8 * 4 * 32 * 128 * 4
     assert lib.jfa_decode_splitkv(P(args()), FAKE, need - 1, None) == _abi.JFA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_varlen_validation(lib):
+    P = ctypes.byref
+
+    def fargs(**kw):
+        a = _abi.VarlenFwdArgs(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 100, 300, 150, 400, 0.1, 1,
+                               FAKE, FAKE, None)
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+
+    def bargs(**kw):
+        a = _abi.VarlenBwdArgs(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 100, 300, 150, 400,
+                               0.1, 1, 0, FAKE, FAKE, FAKE, None)
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+    for bad in (dict(kv_heads=3), dict(kv_heads=0), dict(k_offsets=FAKE + 2), dict(k=FAKE + 8), dict(causal=2),
+                dict(total_k=-1)):
+        assert lib.jfa_fwd_varlen(P(fargs(**bad)), FAKE, 1 << 30, None) == _abi.JFA_ERR_INVALID_ARG, bad
+        assert lib.jfa_bwd_varlen(P(bargs(**bad)), FAKE, 1 << 40, None) == _abi.JFA_ERR_INVALID_ARG, bad
+    assert lib.jfa_fwd_varlen(P(fargs(head_dim=96)), FAKE, 1 << 30, None) == _abi.JFA_ERR_UNSUPPORTED
+    assert lib.jfa_bwd_varlen(P(bargs(head_dim=192, head_chunk=192)), FAKE, 1 << 40, None) == _abi.JFA_ERR_UNSUPPORTED
+    assert lib.jfa_bwd_varlen(P(bargs(dk=FAKE + 4)), FAKE, 1 << 40, None) == _abi.JFA_ERR_INVALID_ARG
+    # forward items: query tiles of every query head; backward: key tiles of every KV head,
+    # plus the fp32 dQ accumulator over the queries
+    nf = lib.jfa_varlen_fwd_workspace_size(P(fargs()))
+    assert nf >= 256 + 2 * 16 * 8 * (2 + 2)
+    nb = lib.jfa_varlen_bwd_workspace_size(P(bargs()))
+    assert nb >= 150 * 8 * 128 * 4
+    assert lib.jfa_fwd_varlen(P(fargs()), FAKE, nf - 1, None) == _abi.JFA_ERR_WORKSPACE_TOO_SMALL
+    assert lib.jfa_bwd_varlen(P(bargs()), FAKE, nb - 1, None) == _abi.JFA_ERR_WORKSPACE_TOO_SMALL
 
 
 def test_binding_rejects_cpu_tensors():

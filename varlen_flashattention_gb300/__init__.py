@@ -11,7 +11,10 @@ kernels; there is no CPU or PyTorch fallback.
     jfa_fwd_broadcast_q   one dense Q shared by a jagged K/V batch -> (O, LSE)
     jfa_bwd_broadcast_q   its backward, dQ summed over the batch -> (dQ, dK, dV)
     jfa_decode_splitkv    split-KV decode over a paged GQA cache -> (O, LSE)
+    jfa_fwd_varlen        separate query / key lengths, grouped KV heads -> (O, LSE)
+    jfa_bwd_varlen        its backward -> (dQ, dK, dV)
     jagged_attention      autograd wrapper of jfa_fwd / jfa_bwd
+    varlen_attention      autograd wrapper of jfa_fwd_varlen / jfa_bwd_varlen
 """
 from __future__ import annotations
 
@@ -24,7 +27,8 @@ from . import _abi
 
 __all__ = [
     "JfaError", "jfa_fwd", "jfa_bwd", "jfa_fwd_broadcast_q", "jfa_bwd_broadcast_q", "jfa_decode_splitkv",
-    "jfa_read_device_status", "jagged_attention", "library",
+    "jfa_read_device_status", "jagged_attention", "library", "jfa_fwd_varlen", "jfa_bwd_varlen",
+    "varlen_attention",
 ]
 
 
@@ -200,6 +204,70 @@ def jfa_bwd_broadcast_q(q, k, v, o, dout, lse, kv_offsets, max_seqlen_k, scale=N
     return dq, dk, dv
 
 
+# ---------------------------------------------------------------- varlen / GQA
+
+def jfa_fwd_varlen(q, k, v, q_offsets, k_offsets, max_seqlen_q, max_seqlen_k, scale=None, causal=False, o=None,
+                   lse=None, workspace=None, stream=None, events=None, check=False):
+    """Jagged attention with separate query / key packing and grouped KV heads.
+    q: bf16 [total_q, Hq, d]; k, v: bf16 [total_k, Hkv, d] with Hq % Hkv == 0; q_offsets and
+    k_offsets: int32 [B+1] (CUDA). causal aligns the mask to the bottom right (key j visible to
+    query i iff j <= i + L_k - L_q). Returns O bf16 [total_q, Hq, d], LSE fp32 [Hq, total_q]."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, torch.bfloat16, 3)
+    _need(q_offsets, "q_offsets", torch.int32, 1)
+    _need(k_offsets, "k_offsets", torch.int32, 1)
+    total_q, Hq, d = q.shape
+    total_k, Hkv, dk_ = k.shape
+    if v.shape != k.shape or dk_ != d:
+        raise ValueError("k and v must be [total_k, Hkv, d] with the head_dim of q")
+    if q_offsets.numel() != k_offsets.numel():
+        raise ValueError("q_offsets and k_offsets must have the same length")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "o", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    a = _abi.VarlenFwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(q_offsets), _ptr(k_offsets), q_offsets.numel() - 1,
+                           Hq, Hkv, d, int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, scale,
+                           int(bool(causal)), _ptr(o), _ptr(lse), None)
+    ev, _keep = _events(events)
+    a.main_kernel_events = ev
+    lib = library()
+    ws = _workspace(lib.jfa_varlen_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
+    _check(lib.jfa_fwd_varlen(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_fwd_varlen")
+    _finish(ws, check, stream, "jfa_fwd_varlen")
+    return o, lse
+
+
+def jfa_bwd_varlen(q, k, v, o, dout, lse, q_offsets, k_offsets, max_seqlen_q, max_seqlen_k, scale=None,
+                   causal=False, head_chunk=0, dq=None, dk=None, dv=None, workspace=None, stream=None, events=None,
+                   check=False):
+    """Backward of jfa_fwd_varlen. Returns dQ bf16 [total_q, Hq, d] and dK, dV bf16
+    [total_k, Hkv, d] (a KV head's gradient summed over the query heads that read it)."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _need(t, n, torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    _need(q_offsets, "q_offsets", torch.int32, 1)
+    _need(k_offsets, "k_offsets", torch.int32, 1)
+    total_q, Hq, d = q.shape
+    total_k, Hkv, _ = k.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    a = _abi.VarlenBwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(q_offsets),
+                           _ptr(k_offsets), q_offsets.numel() - 1, Hq, Hkv, d, int(max_seqlen_q), int(max_seqlen_k),
+                           total_q, total_k, scale, int(bool(causal)), int(head_chunk), _ptr(dq), _ptr(dk), _ptr(dv),
+                           None)
+    ev, _keep = _events(events)
+    a.main_kernel_events = ev
+    lib = library()
+    ws = _workspace(lib.jfa_varlen_bwd_workspace_size(ctypes.byref(a)), q.device, workspace)
+    _check(lib.jfa_bwd_varlen(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_bwd_varlen")
+    _finish(ws, check, stream, "jfa_bwd_varlen")
+    return dq, dk, dv
+
+
 # ---------------------------------------------------------------- decode
 
 def jfa_decode_splitkv(q, k_cache, v_cache, page_table, seqlens_k, num_splits, scale=None, o=None, lse=None,
@@ -254,3 +322,26 @@ def jagged_attention(q, k, v, offsets, max_seqlen, scale=None, causal=False):
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
     return _JaggedAttention.apply(q, k, v, offsets, max_seqlen, scale, causal)
+
+
+class _VarlenAttention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, q_offsets, k_offsets, max_seqlen_q, max_seqlen_k, scale, causal):
+        o, lse = jfa_fwd_varlen(q, k, v, q_offsets, k_offsets, max_seqlen_q, max_seqlen_k, scale, causal)
+        ctx.save_for_backward(q, k, v, o, lse, q_offsets, k_offsets)
+        ctx.args = (max_seqlen_q, max_seqlen_k, scale, causal)
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse, q_offsets, k_offsets = ctx.saved_tensors
+        mq, mk, scale, causal = ctx.args
+        dq, dk, dv = jfa_bwd_varlen(q, k, v, o, do.contiguous(), lse, q_offsets, k_offsets, mq, mk, scale, causal)
+        return dq, dk, dv, None, None, None, None, None, None
+
+
+def varlen_attention(q, k, v, q_offsets, k_offsets, max_seqlen_q, max_seqlen_k, scale=None, causal=False):
+    """Differentiable varlen / GQA attention (see jfa_fwd_varlen for layouts and the causal alignment)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    return _VarlenAttention.apply(q, k, v, q_offsets, k_offsets, max_seqlen_q, max_seqlen_k, scale, causal)

@@ -65,6 +65,23 @@ class DecodeArgs(ctypes.Structure):
                 ("main_kernel_events", c_void_p)]
 
 
+class VarlenFwdArgs(ctypes.Structure):
+    _fields_ = [("q", c_void_p), ("k", c_void_p), ("v", c_void_p), ("q_offsets", c_void_p), ("k_offsets", c_void_p),
+                ("batch", c_i32), ("q_heads", c_i32), ("kv_heads", c_i32), ("head_dim", c_i32),
+                ("max_seqlen_q", c_i32), ("max_seqlen_k", c_i32), ("total_q", c_i32), ("total_k", c_i32),
+                ("scale", c_f32), ("causal", c_i32),
+                ("o", c_void_p), ("lse", c_void_p), ("main_kernel_events", c_void_p)]
+
+
+class VarlenBwdArgs(ctypes.Structure):
+    _fields_ = [("q", c_void_p), ("k", c_void_p), ("v", c_void_p), ("o", c_void_p), ("dout", c_void_p),
+                ("lse", c_void_p), ("q_offsets", c_void_p), ("k_offsets", c_void_p),
+                ("batch", c_i32), ("q_heads", c_i32), ("kv_heads", c_i32), ("head_dim", c_i32),
+                ("max_seqlen_q", c_i32), ("max_seqlen_k", c_i32), ("total_q", c_i32), ("total_k", c_i32),
+                ("scale", c_f32), ("causal", c_i32), ("head_chunk", c_i32),
+                ("dq", c_void_p), ("dk", c_void_p), ("dv", c_void_p), ("main_kernel_events", c_void_p)]
+
+
 # (name, argtypes, restype) of every exported symbol declared in include/jfa.h
 SIGNATURES = [
     ("jfa_fwd_workspace_size", [ctypes.POINTER(FwdArgs)], ctypes.c_size_t),
@@ -72,11 +89,15 @@ SIGNATURES = [
     ("jfa_bcast_fwd_workspace_size", [ctypes.POINTER(BcastFwdArgs)], ctypes.c_size_t),
     ("jfa_bcast_bwd_workspace_size", [ctypes.POINTER(BcastBwdArgs)], ctypes.c_size_t),
     ("jfa_decode_workspace_size", [ctypes.POINTER(DecodeArgs)], ctypes.c_size_t),
+    ("jfa_varlen_fwd_workspace_size", [ctypes.POINTER(VarlenFwdArgs)], ctypes.c_size_t),
+    ("jfa_varlen_bwd_workspace_size", [ctypes.POINTER(VarlenBwdArgs)], ctypes.c_size_t),
     ("jfa_fwd", [ctypes.POINTER(FwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_bwd", [ctypes.POINTER(BwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_fwd_broadcast_q", [ctypes.POINTER(BcastFwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_bwd_broadcast_q", [ctypes.POINTER(BcastBwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_decode_splitkv", [ctypes.POINTER(DecodeArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
+    ("jfa_fwd_varlen", [ctypes.POINTER(VarlenFwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
+    ("jfa_bwd_varlen", [ctypes.POINTER(VarlenBwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_decode_splitkv_noalloc", [ctypes.POINTER(DecodeArgs), c_void_p], c_i32),
     ("jfa_read_device_status", [c_void_p, c_void_p, ctypes.POINTER(c_i32)], c_i32),
     ("jfa_status_string", [c_i32], ctypes.c_char_p),

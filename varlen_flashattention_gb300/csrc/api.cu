@@ -172,6 +172,33 @@ Layout bcast_layout(int64_t batch, int64_t q_len, int64_t heads, int64_t total_k
   return L;
 }
 
+// Varlen / GQA: items are query tiles of every query head (forward) or key
+// tiles of every KV head (backward); the padded LSE / delta rows and the dQ
+// accumulator follow the queries.
+Layout var_layout(int64_t batch, int64_t q_heads, int64_t kv_heads, int64_t total_q, int64_t total_k,
+                  int64_t head_dim, bool bwd) {
+  Layout L;
+  size_t off = kStatusBytes;
+  L.tile_base = off;
+  off = align_up(off + 4 * (batch + 1), 256);
+  L.pad_tiles = max_tiles(total_q, batch);
+  L.max_items = bwd ? kv_heads * max_tiles(total_k, batch) : q_heads * L.pad_tiles;
+  L.items = off;
+  off = align_up(off + 16 * L.max_items, 256);
+  L.item_seq = off;
+  off = align_up(off + 16 * L.max_items, 256);
+  if (bwd) {
+    L.lse2p = off;
+    off = align_up(off + 4 * q_heads * L.pad_tiles * kTile, 256);
+    L.deltap = off;
+    off = align_up(off + 4 * q_heads * L.pad_tiles * kTile, 256);
+    L.dq_acc = off;
+    off = align_up(off + 4 * total_q * q_heads * head_dim, 256);
+  }
+  L.bytes = off;
+  return L;
+}
+
 Layout decode_layout(int64_t batch, int64_t q_heads, int64_t splits) {
   Layout L;
   size_t off = kStatusBytes;
@@ -220,6 +247,27 @@ jfa_status check_bwd(const jfa_bwd_args* a, int* chunk) {
       return JFA_ERR_INVALID_ARG;
   }
   if (static_cast<int64_t>(a->total) * a->heads * a->head_dim >= (int64_t(1) << 40)) return JFA_ERR_INVALID_ARG;
+  return JFA_OK;
+}
+
+// Shared checks of the varlen entry points (the pointers are checked by the callers).
+jfa_status check_var_common(int batch, int q_heads, int kv_heads, int head_dim, int max_q, int max_k, int total_q,
+                            int total_k, float scale, int causal, const int32_t* q_offsets, const int32_t* k_offsets,
+                            bool bwd) {
+  if (batch < 0 || q_heads < 1 || kv_heads < 1 || max_q < 0 || max_k < 0 || total_q < 0 || total_k < 0)
+    return JFA_ERR_INVALID_ARG;
+  if (q_heads % kv_heads != 0) return JFA_ERR_INVALID_ARG;
+  if (!good_dim(head_dim)) return JFA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return JFA_ERR_INVALID_ARG;
+  if (!aligned(q_offsets, 4) || !aligned(k_offsets, 4)) return JFA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(total_q) * q_heads * head_dim >= (int64_t(1) << 40) ||
+      static_cast<int64_t>(total_k) * kv_heads * head_dim >= (int64_t(1) << 40))
+    return JFA_ERR_INVALID_ARG;
+  // the queue's largest cost bucket: key tiles (forward), group x query tiles (backward)
+  const int64_t kmax = bwd ? static_cast<int64_t>(q_heads / kv_heads) * ((max_q + kTile - 1) / kTile)
+                           : (static_cast<int64_t>(max_k) + kTile - 1) / kTile;
+  if (kmax > 32 * 1024) return JFA_ERR_UNSUPPORTED;
   return JFA_OK;
 }
 
@@ -298,7 +346,7 @@ jfa_status jfa_fwd(const jfa_fwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   if (!make_tmap_bf16(&tq, a->q, a->total, cols) || !make_tmap_bf16(&tk, a->k, a->total, cols) ||
       !make_tmap_bf16(&tv, a->v, a->total, cols))
     return JFA_ERR_CUDA;
-  QueueParams qp;
+  QueueParams qp{};
   qp.offsets = a->offsets;
   qp.batch = a->batch;
   qp.heads = a->heads;
@@ -320,11 +368,11 @@ jfa_status jfa_fwd(const jfa_fwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   if (fwd_stream_path(a->head_dim)) {
     CUtensorMap to;
     if (!make_tmap_bf16(&to, a->o, a->total, cols)) return JFA_ERR_CUDA;
-    e = launch_fwd_stream(a->causal != 0, tq, tk, tv, to, qp.items, qp.item_seq, status, a->o, a->lse, a->heads,
-                          a->total, 0, 0, a->scale, wait_budget_ns(), grid, stream);
+    e = launch_fwd_stream(a->causal != 0, tq, tk, tv, to, qp.items, qp.item_seq, VarInfo{}, status, a->o, a->lse,
+                          a->heads, a->total, 0, 0, a->scale, wait_budget_ns(), grid, stream);
   } else {
-    e = launch_fwd(a->head_dim, a->causal != 0, tq, tk, tv, a->offsets, qp.items, status, a->o, a->lse, a->heads,
-                   a->total, 0, 0, a->scale, wait_budget_ns(), grid, stream);
+    e = launch_fwd(a->head_dim, a->causal != 0, tq, tk, tv, a->offsets, qp.items, qp.item_seq, VarInfo{}, status,
+                   a->o, a->lse, a->heads, a->total, 0, 0, a->scale, wait_budget_ns(), grid, stream);
   }
   record(a->main_kernel_events, 1, stream);
   return cuda_status(e);
@@ -350,7 +398,7 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   if (!make_tmap_bf16(&tq, a->q, a->total, cols) || !make_tmap_bf16(&tk, a->k, a->total, cols) ||
       !make_tmap_bf16(&tv, a->v, a->total, cols) || !make_tmap_bf16(&tdo, a->dout, a->total, cols))
     return JFA_ERR_CUDA;
-  QueueParams qp;
+  QueueParams qp{};
   qp.offsets = a->offsets;
   qp.batch = a->batch;
   qp.heads = a->heads;
@@ -372,7 +420,7 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
                      a->total, 0, 0, static_cast<int>(L.pad_tiles), static_cast<int>(L.pad_tiles), lse2p, deltap,
                      dq_acc, stream) != cudaSuccess)
     return JFA_ERR_CUDA;
-  BwdLaunch bl;
+  BwdLaunch bl{};
   bl.head_dim = a->head_dim;
   bl.head_chunk = chunk;
   bl.offsets = a->offsets;
@@ -428,7 +476,7 @@ jfa_status jfa_fwd_broadcast_q(const jfa_bcast_fwd_args* a, void* ws, size_t ws_
   if (!make_tmap_bf16(&tq, a->q, a->q_len, cols) || !make_tmap_bf16(&tk, a->k, a->total_k, cols) ||
       !make_tmap_bf16(&tv, a->v, a->total_k, cols))
     return JFA_ERR_CUDA;
-  QueueParams qp;
+  QueueParams qp{};
   qp.offsets = a->kv_offsets;
   qp.batch = a->batch;
   qp.heads = a->heads;
@@ -450,11 +498,11 @@ jfa_status jfa_fwd_broadcast_q(const jfa_bcast_fwd_args* a, void* ws, size_t ws_
   if (fwd_stream_path(a->head_dim)) {
     CUtensorMap to;
     if (!make_tmap_bf16(&to, a->o, static_cast<uint64_t>(a->batch) * a->q_len, cols)) return JFA_ERR_CUDA;
-    e = launch_fwd_stream(false, tq, tk, tv, to, qp.items, qp.item_seq, status, a->o, a->lse, a->heads, a->total_k,
-                          1, a->q_len, a->scale, wait_budget_ns(), grid, stream);
+    e = launch_fwd_stream(false, tq, tk, tv, to, qp.items, qp.item_seq, VarInfo{}, status, a->o, a->lse, a->heads,
+                          a->total_k, 1, a->q_len, a->scale, wait_budget_ns(), grid, stream);
   } else {
-    e = launch_fwd(a->head_dim, false, tq, tk, tv, a->kv_offsets, qp.items, status, a->o, a->lse, a->heads,
-                   a->total_k, 1, a->q_len, a->scale, wait_budget_ns(), grid, stream);
+    e = launch_fwd(a->head_dim, false, tq, tk, tv, a->kv_offsets, qp.items, qp.item_seq, VarInfo{}, status, a->o,
+                   a->lse, a->heads, a->total_k, 1, a->q_len, a->scale, wait_budget_ns(), grid, stream);
   }
   record(a->main_kernel_events, 1, stream);
   return cuda_status(e);
@@ -492,7 +540,7 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
         !make_tmap_bf16(&tv, a->v, a->total_k, cols) ||
         !make_tmap_bf16(&tdo, a->dout, static_cast<uint64_t>(a->batch) * a->q_len, cols))
       return JFA_ERR_CUDA;
-    QueueParams qp;
+    QueueParams qp{};
     qp.offsets = a->kv_offsets;
     qp.batch = a->batch;
     qp.heads = a->heads;
@@ -514,7 +562,7 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
                        a->total_k, 1, a->q_len, 0, static_cast<int>(L.pad_tiles), lse2p, deltap, dq_acc,
                        stream) != cudaSuccess)
       return JFA_ERR_CUDA;
-    BwdLaunch bl;
+    BwdLaunch bl{};
     bl.head_dim = a->head_dim;
     bl.head_chunk = a->head_dim;
     bl.offsets = a->kv_offsets;
@@ -572,6 +620,180 @@ jfa_status jfa_decode_splitkv(const jfa_decode_args* a, void* ws, size_t ws_byte
   if (a->batch == 0) return JFA_OK;
   return cuda_status(launch_decode(*a, reinterpret_cast<float*>(w + L.part_o), reinterpret_cast<float*>(w + L.part_lse),
                                    reinterpret_cast<int32_t*>(w), stream));
+}
+
+size_t jfa_varlen_fwd_workspace_size(const jfa_varlen_fwd_args* a) {
+  if (!a) return 0;
+  return var_layout(a->batch, a->q_heads, a->kv_heads, a->total_q, a->total_k, a->head_dim, false).bytes;
+}
+
+size_t jfa_varlen_bwd_workspace_size(const jfa_varlen_bwd_args* a) {
+  if (!a) return 0;
+  return var_layout(a->batch, a->q_heads, a->kv_heads, a->total_q, a->total_k, a->head_dim, true).bytes;
+}
+
+jfa_status jfa_fwd_varlen(const jfa_varlen_fwd_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!a) return JFA_ERR_INVALID_ARG;
+  jfa_status st = check_var_common(a->batch, a->q_heads, a->kv_heads, a->head_dim, a->max_seqlen_q, a->max_seqlen_k,
+                                   a->total_q, a->total_k, a->scale, a->causal, a->q_offsets, a->k_offsets, false);
+  if (st != JFA_OK) return st;
+  if (a->total_q > 0 && (!aligned(a->q, 16) || !aligned(a->o, 16) || !aligned(a->lse, 4))) return JFA_ERR_INVALID_ARG;
+  if (a->total_k > 0 && (!aligned(a->k, 16) || !aligned(a->v, 16))) return JFA_ERR_INVALID_ARG;
+  const Layout L = var_layout(a->batch, a->q_heads, a->kv_heads, a->total_q, a->total_k, a->head_dim, false);
+  if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
+  if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(w);
+  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (a->batch == 0 || a->total_q == 0) return JFA_OK;
+  const int sms = sm_count();
+  if (sms <= 0) return JFA_ERR_CUDA;
+  // with no keys at all the K/V maps are never read; they still need a valid base
+  const void* kb = a->total_k > 0 ? a->k : a->q;
+  const void* vb = a->total_k > 0 ? a->v : a->q;
+  CUtensorMap tq, tk, tv;
+  const uint64_t qcols = static_cast<uint64_t>(a->q_heads) * a->head_dim;
+  const uint64_t kcols = static_cast<uint64_t>(a->kv_heads) * a->head_dim;
+  if (!make_tmap_bf16(&tq, a->q, a->total_q, qcols) || !make_tmap_bf16(&tk, kb, a->total_k, kcols) ||
+      !make_tmap_bf16(&tv, vb, a->total_k, kcols))
+    return JFA_ERR_CUDA;
+  QueueParams qp{};
+  qp.offsets = a->q_offsets;
+  qp.k_offsets = a->k_offsets;
+  qp.batch = a->batch;
+  qp.heads = a->q_heads;
+  qp.total = a->total_q;
+  qp.max_seqlen = a->max_seqlen_q;
+  qp.total_k = a->total_k;
+  qp.max_seqlen_k = a->max_seqlen_k;
+  qp.group = a->q_heads / a->kv_heads;
+  qp.causal = a->causal;
+  qp.mode = kQueueVarFwd;
+  qp.status = status;
+  qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
+  qp.items = reinterpret_cast<int4*>(w + L.items);
+  qp.item_seq = reinterpret_cast<int4*>(w + L.item_seq);
+  qp.max_items = static_cast<int32_t>(L.max_items);
+  qp.count_index = 2;
+  if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  VarInfo vi;
+  vi.var = 1;
+  vi.group = qp.group;
+  cudaError_t e;
+  const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
+  record(a->main_kernel_events, 0, stream);
+  if (fwd_stream_path(a->head_dim)) {
+    CUtensorMap to;
+    if (!make_tmap_bf16(&to, a->o, a->total_q, qcols)) return JFA_ERR_CUDA;
+    e = launch_fwd_stream(a->causal != 0, tq, tk, tv, to, qp.items, qp.item_seq, vi, status, a->o, a->lse,
+                          a->q_heads, a->total_q, 0, 0, a->scale, wait_budget_ns(), grid, stream);
+  } else {
+    e = launch_fwd(a->head_dim, a->causal != 0, tq, tk, tv, a->q_offsets, qp.items, qp.item_seq, vi, status, a->o,
+                   a->lse, a->q_heads, a->total_q, 0, 0, a->scale, wait_budget_ns(), grid, stream);
+  }
+  record(a->main_kernel_events, 1, stream);
+  return cuda_status(e);
+}
+
+jfa_status jfa_bwd_varlen(const jfa_varlen_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!a) return JFA_ERR_INVALID_ARG;
+  jfa_status st = check_var_common(a->batch, a->q_heads, a->kv_heads, a->head_dim, a->max_seqlen_q, a->max_seqlen_k,
+                                   a->total_q, a->total_k, a->scale, a->causal, a->q_offsets, a->k_offsets, true);
+  if (st != JFA_OK) return st;
+  int chunk = a->head_chunk;
+  if (chunk == 0) chunk = (a->head_dim == 192) ? 64 : a->head_dim;
+  if (!((chunk == a->head_dim && a->head_dim != 192) || (chunk == 64 && a->head_dim >= 128)))
+    return JFA_ERR_UNSUPPORTED;  // head_dim 192 unchunked would overflow TMEM
+  if (a->total_q > 0 && (!aligned(a->q, 16) || !aligned(a->o, 16) || !aligned(a->dout, 16) || !aligned(a->lse, 4) ||
+                         !aligned(a->dq, 16)))
+    return JFA_ERR_INVALID_ARG;
+  if (a->total_k > 0 && (!aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->dk, 16) || !aligned(a->dv, 16)))
+    return JFA_ERR_INVALID_ARG;
+  const Layout L = var_layout(a->batch, a->q_heads, a->kv_heads, a->total_q, a->total_k, a->head_dim, true);
+  if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
+  if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(w);
+  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  const size_t kv_bytes = static_cast<size_t>(a->total_k) * a->kv_heads * a->head_dim * 2;
+  if (a->batch == 0 || a->total_k == 0 || a->total_q == 0) {
+    // no (query, key) pair anywhere: every gradient is zero
+    if (kv_bytes && (cudaMemsetAsync(a->dk, 0, kv_bytes, stream) != cudaSuccess ||
+                     cudaMemsetAsync(a->dv, 0, kv_bytes, stream) != cudaSuccess))
+      return JFA_ERR_CUDA;
+    const size_t q_bytes = static_cast<size_t>(a->total_q) * a->q_heads * a->head_dim * 2;
+    if (q_bytes && cudaMemsetAsync(a->dq, 0, q_bytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+    return JFA_OK;
+  }
+  const int sms = sm_count();
+  if (sms <= 0) return JFA_ERR_CUDA;
+  const int64_t n_acc = static_cast<int64_t>(a->total_q) * a->q_heads * a->head_dim;
+  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);  // zeroed by the pre-pass
+  CUtensorMap tq, tk, tv, tdo;
+  const uint64_t qcols = static_cast<uint64_t>(a->q_heads) * a->head_dim;
+  const uint64_t kcols = static_cast<uint64_t>(a->kv_heads) * a->head_dim;
+  if (!make_tmap_bf16(&tq, a->q, a->total_q, qcols) || !make_tmap_bf16(&tk, a->k, a->total_k, kcols) ||
+      !make_tmap_bf16(&tv, a->v, a->total_k, kcols) || !make_tmap_bf16(&tdo, a->dout, a->total_q, qcols))
+    return JFA_ERR_CUDA;
+  QueueParams qp{};
+  qp.offsets = a->q_offsets;
+  qp.k_offsets = a->k_offsets;
+  qp.batch = a->batch;
+  qp.heads = a->kv_heads;
+  qp.total = a->total_q;
+  qp.max_seqlen = a->max_seqlen_q;
+  qp.total_k = a->total_k;
+  qp.max_seqlen_k = a->max_seqlen_k;
+  qp.group = a->q_heads / a->kv_heads;
+  qp.causal = a->causal;
+  qp.mode = kQueueVarBwd;
+  qp.status = status;
+  qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
+  qp.items = reinterpret_cast<int4*>(w + L.items);
+  qp.item_seq = reinterpret_cast<int4*>(w + L.item_seq);
+  qp.max_items = static_cast<int32_t>(L.max_items);
+  qp.count_index = 2;
+  if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  float* lse2p = reinterpret_cast<float*>(w + L.lse2p);
+  float* deltap = reinterpret_cast<float*>(w + L.deltap);
+  if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->q_offsets, qp.tile_base, status, a->batch, a->q_heads,
+                     a->total_q, 0, 0, static_cast<int>(L.pad_tiles), static_cast<int>(L.pad_tiles), lse2p, deltap,
+                     dq_acc, stream) != cudaSuccess)
+    return JFA_ERR_CUDA;
+  BwdLaunch bl{};
+  bl.head_dim = a->head_dim;
+  bl.head_chunk = chunk;
+  bl.offsets = a->q_offsets;
+  bl.tile_base = qp.tile_base;
+  bl.items = qp.items;
+  bl.item_seq = qp.item_seq;
+  bl.status = status;
+  bl.lse2p = lse2p;
+  bl.deltap = deltap;
+  bl.dq_acc = dq_acc;
+  bl.dk = a->dk;
+  bl.dv = a->dv;
+  bl.heads = a->q_heads;
+  bl.total = a->total_q;
+  bl.bcast = 0;
+  bl.q_len = 0;
+  bl.causal = a->causal;
+  bl.pad_tiles = static_cast<int>(L.pad_tiles);
+  bl.var = 1;
+  bl.group = qp.group;
+  bl.kv_heads = a->kv_heads;
+  bl.scale = a->scale;
+  bl.budget_ns = wait_budget_ns();
+  bl.grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items * (a->head_dim / chunk), 1)));
+  CUtensorMap tdq, tdk, tdv;
+  if (!make_tmap_f32_acc(&tdq, dq_acc, a->total_q, qcols) || !make_tmap_bf16(&tdk, a->dk, a->total_k, kcols) ||
+      !make_tmap_bf16(&tdv, a->dv, a->total_k, kcols))
+    return JFA_ERR_CUDA;
+  record(a->main_kernel_events, 0, stream);
+  cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, tdq, tdk, tdv, stream);
+  record(a->main_kernel_events, 1, stream);
+  if (e != cudaSuccess) return JFA_ERR_CUDA;
+  return cuda_status(launch_bwd_post(dq_acc, a->dq, n_acc, a->scale, status, sms, stream));
 }
 
 jfa_status jfa_read_device_status(const void* ws, cudaStream_t stream, int32_t* detail) {

@@ -70,7 +70,9 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int32_t heads, total, bcast, q_len, causal, n_chunks;
-  int32_t pad_tiles;          // self: tiles per head in the padded arrays
+  int32_t pad_tiles;          // self, varlen: query tiles per head in the padded arrays
+  int32_t var, group;         // varlen: items carry query and key bounds; query heads per KV head
+  int32_t kv_heads;           // heads of K, V, dK, dV
   float scale, scale_log2;
   uint64_t budget_ns;
 };
@@ -100,7 +102,10 @@ struct BwdLayout {
 };
 
 struct BwdItem {
-  int b, h, t, c;  // sequence, head, K/V tile, head-dim slice
+  int b, h, t, c;  // sequence, (KV) head, K/V tile, head-dim slice
+  int hq0;         // first query head that reads KV head h (varlen: h * group; else h)
+  int nqt;         // query tiles per query head; the item's steps are nq = group * nqt
+  int delta;       // L_k - L_q: key j is visible to query i iff j <= i + delta (causal)
   int kv_row0;     // first K/V row of the tile
   int Lk, Lq;
   int i0, nq;      // query tiles i0 .. i0+nq-1
@@ -123,6 +128,24 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
   const int s0 = sq.x;
   I.Lk = sq.y;
   I.kv_row0 = s0 + kTile * I.t;
+  I.hq0 = I.h;
+  I.delta = 0;
+  if (p.var) {  // item_seq: (first query row, L_q, first key row, L_k); items.w: query tile base
+    I.Lq = sq.y;
+    I.Lk = sq.w;
+    I.kv_row0 = sq.z + kTile * I.t;
+    I.q_row0 = s0;
+    I.do_row0 = s0;
+    I.hq0 = I.h * p.group;
+    I.delta = I.Lk - I.Lq;
+    I.row_base = (static_cast<int64_t>(I.hq0) * p.pad_tiles + it.w) * kTile;
+    const int nq = (I.Lq + kTile - 1) / kTile;
+    const int i_min = p.causal ? max(0, kTile * I.t - I.delta) : 0;  // first query that sees the tile
+    I.i0 = i_min / kTile;
+    I.nqt = i_min < I.Lq ? nq - I.i0 : 0;
+    I.nq = p.group * I.nqt;
+    return I;
+  }
   if (!p.bcast) {
     I.Lq = I.Lk;
     I.q_row0 = s0;
@@ -138,7 +161,15 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
   const int nq = (I.Lq + kTile - 1) / kTile;
   I.i0 = p.causal ? I.t : 0;
   I.nq = nq - I.i0;
+  I.nqt = I.nq;
   return I;
+}
+
+// Step ii of an item: query head hq0 + g, query tile i. The steps run over the
+// query tiles of each query head of the group in turn.
+__device__ __forceinline__ void bwd_step(const BwdItem& I, int ii, int& g, int& i) {
+  g = (I.nqt == I.nq) ? 0 : ii / I.nqt;
+  i = I.i0 + ii - g * I.nqt;
 }
 
 template <int D, int DC>
@@ -248,23 +279,26 @@ __global__ void __launch_bounds__(448, 1)
         return v;
       };
       auto load_qdo = [&](const BwdItem& I, int ii) -> bool {
-        const int i = I.i0 + ii;
+        int g, i;
+        bwd_step(I, ii, g, i);
+        const int qcol = (I.hq0 + g) * D;
+        const int64_t rbase = I.row_base + static_cast<int64_t>(g) * p.pad_tiles * kTile;
         const uint32_t st = pos % kSt, round = pos / kSt;
         if (!ptx::mbar_wait(q_empty + st, (round & 1) ^ 1, ctl, status, kSiteBwdProdQ, budget)) return false;
         ptx::mbar_arrive_expect_tx(q_full + st, Lay::kTileBytes + 1024);
         uint8_t* qd = smem + Lay::kOffQ + st * Lay::kTileBytes;
 #pragma unroll
         for (int a = 0; a < Lay::kAtoms; ++a)
-          ptx::tma_load_2d(qd + a * 16384, &tm_q, q_full + st, I.h * D + 64 * a, I.q_row0 + kTile * i);
+          ptx::tma_load_2d(qd + a * 16384, &tm_q, q_full + st, qcol + 64 * a, I.q_row0 + kTile * i);
         uint8_t* rows = smem + Lay::kOffRow + st * 1024;
-        ptx::bulk_load(rows, p.lse2p + I.row_base + static_cast<int64_t>(kTile) * i, 512, q_full + st);
-        ptx::bulk_load(rows + 512, p.deltap + I.row_base + static_cast<int64_t>(kTile) * i, 512, q_full + st);
+        ptx::bulk_load(rows, p.lse2p + rbase + static_cast<int64_t>(kTile) * i, 512, q_full + st);
+        ptx::bulk_load(rows + 512, p.deltap + rbase + static_cast<int64_t>(kTile) * i, 512, q_full + st);
         if (!ptx::mbar_wait(do_empty + st, (round & 1) ^ 1, ctl, status, kSiteBwdProdQ, budget)) return false;
         ptx::mbar_arrive_expect_tx(do_full + st, Lay::kTileBytes);
         uint8_t* dd = smem + Lay::kOffDO + st * Lay::kTileBytes;
 #pragma unroll
         for (int a = 0; a < Lay::kAtoms; ++a)
-          ptx::tma_load_2d(dd + a * 16384, &tm_do, do_full + st, I.h * D + 64 * a, I.do_row0 + kTile * i);
+          ptx::tma_load_2d(dd + a * 16384, &tm_do, do_full + st, qcol + 64 * a, I.do_row0 + kTile * i);
         ++pos;
         return true;
       };
@@ -460,14 +494,17 @@ __global__ void __launch_bounds__(448, 1)
       if (I.nq <= 0) continue;
       const int rk = I.Lk - kTile * I.t;  // valid key rows of the tile
       for (int ii = 0; ii < I.nq; ++ii, ++x) {
-        const int i = I.i0 + ii;
+        int g_unused, i;
+        bwd_step(I, ii, g_unused, i);
         const uint32_t st = pos % kSt;
         const float* lse2 = reinterpret_cast<const float*>(smem + Lay::kOffRow + st * 1024) + 64 * g;
         const float* dlt = lse2 + 128;
         const int rq = I.Lq - kTile * i;  // valid query columns
-        const bool masked = rk < kTile || rq < kTile || (p.causal && i == I.t);
-        // visible query columns c of this key row: c_lo <= c < c_hi (causal: c >= r on the diagonal tile)
-        const int c_lo = (p.causal && i == I.t) ? r : 0;
+        // tiles that cross the (bottom-right aligned) diagonal or the end of a sequence
+        const bool masked = rk < kTile || rq < kTile || (p.causal && kTile * I.t + kTile - 1 > kTile * i + I.delta);
+        // visible query columns c of this key row: c_lo <= c < c_hi (causal: query
+        // 128 i + c sees key 128 t + r iff 128 i + c >= 128 t + r - delta)
+        const int c_lo = p.causal ? max(0, kTile * (I.t - i) + r - I.delta) : 0;
         const int c_hi = r < rk ? rq : 0;
         if (!(ok = ptx::mbar_wait(s_full, x & 1, ctl, status, kSiteBwdSoftS, budget))) break;
         ptx::tc_fence_after();
@@ -584,9 +621,21 @@ __global__ void __launch_bounds__(448, 1)
     bool ok = true;
     for (int v = blockIdx.x; ok && v < n_work; v += gridDim.x) {
       const BwdItem I = bwd_item(p, v);
-      if (I.nq <= 0) continue;
+      if (I.nq <= 0) {
+        // a varlen key tile that no query sees: its dK and dV rows are zero
+        if (p.var) {
+          const int64_t orow = (static_cast<int64_t>(I.kv_row0 + r) * p.kv_heads + I.h) * D + I.c * DC;
+          if (r < I.Lk - kTile * I.t)
+            for (int c8 = 0; c8 < DC; c8 += 8) {
+              ptx::st_v4(p.dv + orow + c8, 0, 0, 0, 0);
+              ptx::st_v4(p.dk + orow + c8, 0, 0, 0, 0);
+            }
+        }
+        continue;
+      }
       for (int ii = 0; ii < I.nq; ++ii, ++x) {
-        const int i = I.i0 + ii;
+        int g, i;
+        bwd_step(I, ii, g, i);
         if (!(ok = ptx::mbar_wait(dq_full, x & 1, ctl, status, kSiteBwdDQ, budget))) break;
         ptx::tc_fence_after();
         // dQ leaves TMEM a staging round (a buffer-full of 32-column fp32 boxes,
@@ -597,7 +646,7 @@ __global__ void __launch_bounds__(448, 1)
         // goes there); TMA adds each round into the accumulator. Rows past the
         // sequence hold exact zeros (their dS is masked), so whole boxes are added.
         const int qrow = I.q_row0 + kTile * i;
-        const int xcol = I.h * D + I.c * DC;
+        const int xcol = (I.hq0 + g) * D + I.c * DC;  // dQ of query head hq0 + g
         const bool issuer = warp == 10 && lane == 0;
         const uint32_t st = x % kSt;
         uint8_t* stage = kStageInDO ? smem + Lay::kOffDO + st * Lay::kTileBytes : smem + Lay::kOffDS;
@@ -737,7 +786,7 @@ __global__ void __launch_bounds__(448, 1)
         // a partial key tile (its rows end inside the 128-row box) or a single
         // stage: every thread stores its own row
         const bool k_ok = r < I.Lk - kTile * I.t;
-        const int64_t orow = (static_cast<int64_t>(I.kv_row0 + r) * p.heads + I.h) * D + I.c * DC;
+        const int64_t orow = (static_cast<int64_t>(I.kv_row0 + r) * p.kv_heads + I.h) * D + I.c * DC;
 #pragma unroll 1
         for (int c = 0; c < DC / 32; ++c) {
           uint32_t a[32], b[32];
@@ -933,6 +982,9 @@ cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUt
   p.dk = static_cast<__nv_bfloat16*>(L.dk);
   p.dv = static_cast<__nv_bfloat16*>(L.dv);
   p.heads = L.heads;
+  p.var = L.var;
+  p.group = L.var ? L.group : 1;
+  p.kv_heads = L.var ? L.kv_heads : L.heads;
   p.total = L.total;
   p.bcast = L.bcast;
   p.q_len = L.q_len;

@@ -36,6 +36,7 @@ namespace jfa {
 struct FwdParams {
   const int32_t* offsets;  // self: sequence offsets; broadcast: K/V offsets
   const int4* items;
+  const int4* item_seq;    // varlen: (first query row, L_q, first key row, L_k) of each item
   int32_t* status;         // status block (n_items at [2])
   __nv_bfloat16* o;
   float* lse;
@@ -43,6 +44,7 @@ struct FwdParams {
   int32_t total;           // self: rows of Q/K/V; broadcast: total_k
   int32_t bcast;
   int32_t q_len;           // broadcast only
+  int32_t var, group;      // varlen: bounds from item_seq; query heads per KV head
   float scale_log2;
   uint64_t budget_ns;
 };
@@ -67,6 +69,8 @@ struct FwdLayout {
 
 struct FwdItem {
   int b, h, t;
+  int hk;         // KV head read by query head h
+  int delta;      // L_k - L_q: key j is visible to query i iff j <= i + delta (causal)
   int q_tma_row;  // row of the Q tile in the Q tensor map
   int kv_row0;    // first K/V row of the sequence
   int Lq, Lk;
@@ -82,6 +86,21 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int idx) {
   I.b = it.x;
   I.h = it.y;
   I.t = it.z;
+  if (p.var) {
+    const int4 sq = p.item_seq[idx];
+    I.Lq = sq.y;
+    I.Lk = sq.w;
+    I.kv_row0 = sq.z;
+    I.hk = I.h / p.group;
+    I.delta = I.Lk - I.Lq;
+    I.q_tma_row = sq.x + kTile * I.t;
+    I.o_row = I.q_tma_row;
+    I.lse0 = static_cast<int64_t>(I.h) * p.total + I.q_tma_row;
+    I.n_kv = it.w;  // the queue's cost: key tiles visited
+    return I;
+  }
+  I.hk = I.h;
+  I.delta = 0;
   const int s0 = p.offsets[I.b], s1 = p.offsets[I.b + 1];
   I.Lk = s1 - s0;
   I.kv_row0 = s0;
@@ -184,10 +203,10 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int a = 0; a < Lay::kAtoms; ++a)
           ptx::tma_load_2d(smem + Lay::kOffQ + a * 16384, &tm_q, q_full, I.h * D + 64 * a, I.q_tma_row);
-        ok = load_tile(&tm_k, I.h, I.kv_row0);
+        ok = load_tile(&tm_k, I.hk, I.kv_row0);
         for (int j = 0; ok && j < I.n_kv; ++j) {
-          if (j + 1 < I.n_kv) ok = load_tile(&tm_k, I.h, I.kv_row0 + kTile * (j + 1));
-          if (ok) ok = load_tile(&tm_v, I.h, I.kv_row0 + kTile * j);
+          if (j + 1 < I.n_kv) ok = load_tile(&tm_k, I.hk, I.kv_row0 + kTile * (j + 1));
+          if (ok) ok = load_tile(&tm_v, I.hk, I.kv_row0 + kTile * j);
         }
         ++kq;
       }
@@ -293,10 +312,11 @@ __global__ void __launch_bounds__(192, 1)
         ptx::tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 4; ++c) ptx::reg_fence32(sv[c]);
-        // peeled tail: only the diagonal (causal) or the last partial tile is masked
-        const bool tail = CAUSAL ? (j == I.t) : (j == n - 1 && (I.Lk & (kTile - 1)) != 0);
+        // peeled tail: only tiles that cross the (bottom-right aligned) diagonal
+        // or the end of the keys are masked
+        const bool tail = (CAUSAL && kTile * j + kTile - 1 > kTile * I.t + I.delta) || kTile * (j + 1) > I.Lk;
         if (tail) {
-          const int lim = CAUSAL ? min(r + 1, I.Lk - kTile * j) : I.Lk - kTile * j;
+          const int lim = CAUSAL ? min(r + 1 + kTile * (I.t - j) + I.delta, I.Lk - kTile * j) : I.Lk - kTile * j;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -334,14 +354,16 @@ __global__ void __launch_bounds__(192, 1)
             m = mm;
           }
         }
-        // P = 2^(s*scale*log2e - m), written as bf16 pairs over the scores
+        // P = 2^(s*scale*log2e - m), written as bf16 pairs over the scores; a
+        // row that sees no key so far (m = -inf) shifts by 0 and gets P = 0
+        const float mu = (m == -INFINITY) ? 0.f : m;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ptx::ex2(fmaf(__uint_as_float(sv[c][2 * e]), sl, -m));
-            const float p1 = ptx::ex2(fmaf(__uint_as_float(sv[c][2 * e + 1]), sl, -m));
+            const float p0 = ptx::ex2(fmaf(__uint_as_float(sv[c][2 * e]), sl, -mu));
+            const float p1 = ptx::ex2(fmaf(__uint_as_float(sv[c][2 * e + 1]), sl, -mu));
             l += p0 + p1;
             pk[e] = ptx::pack_bf16(p0, p1);
           }
@@ -357,7 +379,7 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t xl = it + n - 1;
       if (!ptx::mbar_wait(o_ready + (xl & 1), (xl >> 1) & 1, ctl, status, kSiteFwdSoftO, budget)) break;
       ptx::tc_fence_after();
-      const float inv_l = 1.0f / l;
+      const float inv_l = l > 0.f ? 1.0f / l : 0.f;  // a row that sees no key: O = 0
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
@@ -410,7 +432,8 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 }
 
 cudaError_t launch_fwd(int head_dim, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const int32_t* offsets, const int4* items, int32_t* status, void* o, float* lse, int heads,
+                       const int32_t* offsets, const int4* items, const int4* item_seq, const VarInfo& var,
+                       int32_t* status, void* o, float* lse, int heads,
                        int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
                        cudaStream_t stream) {
   FwdParams p;
@@ -423,6 +446,9 @@ cudaError_t launch_fwd(int head_dim, bool causal, const CUtensorMap& tq, const C
   p.total = total;
   p.bcast = bcast;
   p.q_len = q_len;
+  p.item_seq = item_seq;
+  p.var = var.var;
+  p.group = var.group;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.budget_ns = budget_ns;
   if (head_dim == 64) return causal ? launch_fwd_t<64, true>(tq, tk, tv, p, grid, stream)

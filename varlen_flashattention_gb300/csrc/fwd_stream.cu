@@ -50,6 +50,7 @@ struct FwdStreamParams {
   __nv_bfloat16* o;
   float* lse;
   int32_t heads, total, bcast, q_len;
+  int32_t var, group;    // varlen: item_seq holds query and key bounds; query heads per KV head
   float scale_log2;
   uint64_t budget_ns;
 };
@@ -79,6 +80,8 @@ struct FwdStreamLayout {
 
 struct FwdStreamItem {
   int b, h, t;
+  int hk;     // KV head read by query head h
+  int delta;  // L_k - L_q: key j is visible to query i iff j <= i + delta (causal)
   int q_tma_row, kv_row0, Lq, Lk, n_kv;
   int64_t o_row, lse0;
 };
@@ -95,7 +98,18 @@ __device__ __forceinline__ FwdStreamItem stream_item(const FwdStreamParams& p, i
   const int s0 = sq.x;
   I.Lk = sq.y;
   I.kv_row0 = s0;
-  if (!p.bcast) {
+  I.hk = I.h;
+  I.delta = 0;
+  if (p.var) {  // (first query row, L_q, first key row, L_k)
+    I.Lq = sq.y;
+    I.kv_row0 = sq.z;
+    I.Lk = sq.w;
+    I.hk = I.h / p.group;
+    I.delta = I.Lk - I.Lq;
+    I.q_tma_row = s0 + kTile * I.t;
+    I.o_row = I.q_tma_row;
+    I.lse0 = static_cast<int64_t>(I.h) * p.total + s0 + kTile * I.t;
+  } else if (!p.bcast) {
     I.Lq = I.Lk;
     I.q_tma_row = s0 + kTile * I.t;
     I.o_row = I.q_tma_row;
@@ -263,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* dst = smem + Lay::kOffSlots + slot * Lay::kKVBytes;
 #pragma unroll
         for (int a = 0; a < 2; ++a)
-          ptx::tma_load_2d(dst + a * 16384, map, slot_full + slot, I.h * kD2 + 64 * a, I.kv_row0 + kTile * j);
+          ptx::tma_load_2d(dst + a * 16384, map, slot_full + slot, I.hk * kD2 + 64 * a, I.kv_row0 + kTile * j);
         return true;
       };
       walk_loads(
@@ -397,8 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!s_ready && !(ok = ptx::mbar_wait(s_full + (x & 1), (x >> 1) & 1, ctl, status, kSiteFwdSoftS, budget)))
           break;
         ptx::tc_fence_after();
-        // keys j*128 + c with c >= lim are masked (past the sequence, or above the diagonal)
-        const int lim = CAUSAL ? min(qi + 1 - kTile * j, I.Lk - kTile * j) : I.Lk - kTile * j;
+        // keys j*128 + c with c >= lim are masked (past the sequence, or past
+        // the bottom-right aligned diagonal: key j visible iff j <= qi + delta)
+        const int lim = CAUSAL ? min(qi + 1 + I.delta - kTile * j, I.Lk - kTile * j) : I.Lk - kTile * j;
         auto mask = [&](uint32_t(&v)[32], int c0) {
           if (lim < c0 + 32) {
 #pragma unroll
@@ -644,9 +659,9 @@ cudaError_t launch_fwd_stream_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 }  // namespace
 
 cudaError_t launch_fwd_stream(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const CUtensorMap& to, const int4* items, const int4* item_seq, int32_t* status, void* o, float* lse,
-                              int heads, int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
-                              cudaStream_t stream) {
+                              const CUtensorMap& to, const int4* items, const int4* item_seq, const VarInfo& var,
+                              int32_t* status, void* o, float* lse, int heads, int total, int bcast, int q_len,
+                              float scale, uint64_t budget_ns, int grid, cudaStream_t stream) {
   FwdStreamParams p;
   p.items = items;
   p.item_seq = item_seq;
@@ -657,6 +672,8 @@ cudaError_t launch_fwd_stream(bool causal, const CUtensorMap& tq, const CUtensor
   p.total = total;
   p.bcast = bcast;
   p.q_len = q_len;
+  p.var = var.var;
+  p.group = var.group;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.budget_ns = budget_ns;
   return causal ? launch_fwd_stream_t<true>(tq, tk, tv, to, p, grid, stream)

@@ -56,15 +56,24 @@ enum QueueMode : int32_t {
   kQueueSelfBwd = 1,   // items (b, h, kv-tile); cost = q tiles visited
   kQueueBcastFwd = 2,  // items (b, h, q-tile of the shared Q); cost = kv tiles of b
   kQueueBcastBwd = 3,  // items (b, h, kv-tile of b); cost = q tiles of the shared Q
+  // Varlen / GQA: offsets = query offsets, k_offsets = key offsets; causal is
+  // bottom-right aligned. Items of cost 0 are kept (their outputs are zeros).
+  kQueueVarFwd = 4,    // items (b, query head, q-tile); cost = key tiles visited
+  kQueueVarBwd = 5,    // items (b, KV head, kv-tile); cost = group x q tiles visited
 };
 
+__host__ __device__ inline bool queue_var(int mode) { return mode == kQueueVarFwd || mode == kQueueVarBwd; }
+
 struct QueueParams {
-  const int32_t* offsets;  // [batch+1]
+  const int32_t* offsets;  // [batch+1] (varlen: query offsets)
+  const int32_t* k_offsets;  // varlen only: key offsets [batch+1]
   int32_t batch, heads, total, max_seqlen, causal, mode, q_len;
+  int32_t total_k, max_seqlen_k, group;  // varlen only (group = q_heads / kv_heads)
   int32_t* status;         // status block
   int32_t* tile_base;      // [batch+1] exclusive prefix of q-tiles (self modes)
-  int4* items;             // (b, h, t, cost)
-  int4* item_seq;          // optional: (first row, length, tile_base) of each item's sequence
+  int4* items;             // (b, h, t, cost); varlen backward: (b, h, t, query tile_base of b)
+  int4* item_seq;          // optional: (first row, length, tile_base) of each item's sequence;
+                           // varlen: (first query row, L_q, first key row, L_k)
   int32_t max_items;
   int32_t count_index;     // status word that receives the number of items; the next word
                            // receives the number with cost >= 1 (they come first)
@@ -86,23 +95,31 @@ struct BwdLaunch {
   void* dk;
   void* dv;
   int heads, total, bcast, q_len, causal, pad_tiles;
+  int var, group, kv_heads;  // varlen: items carry query and key bounds; q_heads / kv_heads
   float scale;
   uint64_t budget_ns;
   int grid;
 };
 
+// Varlen / GQA description handed to the forward launchers (var = 0: the
+// self-attention or broadcast-Q item records).
+struct VarInfo {
+  int var = 0;
+  int group = 1;
+};
+
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_queue(const QueueParams& p, cudaStream_t stream);
 cudaError_t launch_fwd(int head_dim, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const int32_t* offsets, const int4* items, int32_t* status, void* o, float* lse, int heads,
-                       int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
-                       cudaStream_t stream);
+                       const int32_t* offsets, const int4* items, const int4* item_seq, const VarInfo& var,
+                       int32_t* status, void* o, float* lse, int heads, int total, int bcast, int q_len, float scale,
+                       uint64_t budget_ns, int grid, cudaStream_t stream);
 // Flat-stream forward (head_dim 128); items from the plain forward queue modes,
 // K and V read in 128-row boxes, O (to) written in 64-column x 128-row boxes.
 cudaError_t launch_fwd_stream(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const CUtensorMap& to, const int4* items, const int4* item_seq, int32_t* status, void* o, float* lse,
-                              int heads, int total, int bcast, int q_len, float scale, uint64_t budget_ns, int grid,
-                              cudaStream_t stream);
+                              const CUtensorMap& to, const int4* items, const int4* item_seq, const VarInfo& var,
+                              int32_t* status, void* o, float* lse, int heads, int total, int bcast, int q_len,
+                              float scale, uint64_t budget_ns, int grid, cudaStream_t stream);
 // tdq: the fp32 dQ accumulator [rows, H*D] in 32-column x 128-row boxes, 128B swizzle.
 // tdk, tdv: dK and dV (bf16 [rows, H*D]) in 64-column x 128-row boxes, 128B swizzle.
 cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -60,27 +60,60 @@ __device__ int block_exclusive_scan(int v, int* warp_buf, int* total) {
 __device__ __forceinline__ int ceil_tiles(int L) { return (L + kTile - 1) / kTile; }
 
 // Work items of sequence b (per head): query tiles (forward) or key/value
-// tiles (backward).
-__device__ __forceinline__ int item_tiles(const QueueParams& p, int L) {
-  return p.mode == kQueueBcastFwd ? ceil_tiles(p.q_len) : ceil_tiles(L);
+// tiles (backward). Lq / Lk are the sequence's query and key lengths (equal
+// in the self modes; the broadcast modes pass the key length for both).
+__device__ __forceinline__ int item_tiles(const QueueParams& p, int Lq, int Lk) {
+  switch (p.mode) {
+    case kQueueBcastFwd: return ceil_tiles(p.q_len);
+    case kQueueVarFwd: return ceil_tiles(Lq);
+    default: return ceil_tiles(Lk);
+  }
+}
+
+// Varlen, bottom-right causal: key tiles seen by query tile t (a prefix of
+// the key tiles: the tile's last row sees keys up to row + L_k - L_q).
+__device__ __forceinline__ int var_fwd_tiles(int Lq, int Lk, int t) {
+  const int seen = min(kTile * (t + 1), Lq) + Lk - Lq;  // keys visible to the tile's last row
+  return seen <= 0 ? 0 : min(ceil_tiles(seen), ceil_tiles(Lk));
+}
+
+// Varlen, bottom-right causal: query tiles that see key tile u (a suffix: the
+// first query that sees key 128 u is 128 u - (L_k - L_q)).
+__device__ __forceinline__ int var_bwd_tiles(int Lq, int Lk, int u) {
+  const int i_min = max(0, kTile * u - (Lk - Lq));
+  return i_min >= Lq ? 0 : ceil_tiles(Lq) - i_min / kTile;
 }
 
 // Partner tiles an item visits: its cost in the longest-first order.
-__device__ __forceinline__ int item_cost(const QueueParams& p, int L, int t) {
-  const int nk = ceil_tiles(L);
+__device__ __forceinline__ int item_cost(const QueueParams& p, int Lq, int Lk, int t) {
+  const int nk = ceil_tiles(Lk);
   switch (p.mode) {
     case kQueueSelfFwd: return p.causal ? t + 1 : nk;
     case kQueueSelfBwd: return p.causal ? nk - t : nk;
     case kQueueBcastFwd: return nk;
+    case kQueueVarFwd: return p.causal ? var_fwd_tiles(Lq, Lk, t) : nk;
+    case kQueueVarBwd: return p.group * (p.causal ? var_bwd_tiles(Lq, Lk, t) : ceil_tiles(Lq));
     default: return ceil_tiles(p.q_len);  // kQueueBcastBwd
   }
 }
 
-// Tiles of a sequence of length L with cost k: count, and the first of them
-// (they are consecutive: causal, exactly one tile per cost up to the number of
-// tiles; otherwise all tiles share one cost).
-__device__ __forceinline__ void tiles_with_cost(const QueueParams& p, int L, int k, int& count, int& t_first) {
-  const int nt = item_tiles(p, L);
+// First index in [0, n) at which a monotone (false ... true) predicate holds, or n.
+template <class F>
+__device__ __forceinline__ int first_true(int n, F pred) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (pred(mid)) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
+
+// Tiles of a sequence with cost k: count, and the first of them (they are
+// consecutive: causal self-attention has exactly one tile per cost up to the
+// number of tiles; varlen causal costs are monotone in the tile, found by
+// binary search; otherwise all tiles share one cost).
+__device__ __forceinline__ void tiles_with_cost(const QueueParams& p, int Lq, int Lk, int k, int& count, int& t_first) {
+  const int nt = item_tiles(p, Lq, Lk);
   count = 0;
   t_first = 0;
   if (p.causal && (p.mode == kQueueSelfFwd || p.mode == kQueueSelfBwd)) {
@@ -88,13 +121,28 @@ __device__ __forceinline__ void tiles_with_cost(const QueueParams& p, int L, int
       count = 1;
       t_first = (p.mode == kQueueSelfFwd) ? k - 1 : nt - k;
     }
-  } else if (nt > 0 && item_cost(p, L, 0) == k) {
+  } else if (p.causal && p.mode == kQueueVarFwd) {  // cost non-decreasing in t
+    const int a = first_true(nt, [&](int t) { return item_cost(p, Lq, Lk, t) >= k; });
+    const int b = first_true(nt, [&](int t) { return item_cost(p, Lq, Lk, t) >= k + 1; });
+    count = b - a;
+    t_first = a;
+  } else if (p.causal && p.mode == kQueueVarBwd) {  // cost non-increasing in t
+    const int a = first_true(nt, [&](int t) { return item_cost(p, Lq, Lk, t) <= k; });
+    const int b = first_true(nt, [&](int t) { return item_cost(p, Lq, Lk, t) <= k - 1; });
+    count = b - a;
+    t_first = a;
+  } else if (nt > 0 && item_cost(p, Lq, Lk, 0) == k) {
     count = nt;
   }
 }
 
-__device__ __forceinline__ int seq_len(const int* s_len, const int32_t* offsets, int b) {
-  return b < kQueueLenCache ? s_len[b] : offsets[b + 1] - offsets[b];
+// Query and key lengths of sequence b (cached in shared memory for the first
+// kQueueLenCache sequences).
+__device__ __forceinline__ int2 seq_lens(const QueueParams& p, const int* s_len, const int* s_lenk, int b) {
+  const int L = b < kQueueLenCache ? s_len[b] : p.offsets[b + 1] - p.offsets[b];
+  if (!queue_var(p.mode)) return make_int2(L, L);
+  const int Lk = b < kQueueLenCache ? s_lenk[b] : p.k_offsets[b + 1] - p.k_offsets[b];
+  return make_int2(L, Lk);
 }
 
 __device__ __forceinline__ int warp_sum(int v) {
@@ -104,12 +152,14 @@ __device__ __forceinline__ int warp_sum(int v) {
 }
 
 // kmax: the largest cost. Dynamic shared memory: kmax + 1 bucket starts, then
-// the lengths and the first queue positions of the first min(batch,
-// kQueueLenCache) sequences.
+// the (query) lengths, the first queue positions and (varlen) the key lengths
+// of the first min(batch, kQueueLenCache) sequences.
 __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParams p, int kmax) {
   extern __shared__ int s_start[];  // [kmax + 1]: tiles (per head) of higher cost than bucket k
   int* s_len = s_start + kmax + 1;
   int* s_first = s_len + kQueueLenCache;  // first tile position of sequence b (one-cost modes)
+  int* s_lenk = s_first + min(p.batch, kQueueLenCache);  // varlen: key lengths
+  const bool var = queue_var(p.mode);
   __shared__ int warp_buf[32];
   __shared__ int s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -130,6 +180,15 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
       if (b == p.batch - 1 && hi != p.total) bad = true;
       if (bad) s_bad = 1;
       if (b < kQueueLenCache) s_len[b] = L;
+      if (var) {  // the key offsets obey the same rules
+        const int klo = p.k_offsets[b], khi = p.k_offsets[b + 1];
+        const int Lk = khi - klo;
+        bool kbad = Lk < 0 || Lk > p.max_seqlen_k;
+        if (b == 0 && klo != 0) kbad = true;
+        if (b == p.batch - 1 && khi != p.total_k) kbad = true;
+        if (kbad) s_bad = 1;
+        if (b < kQueueLenCache) s_lenk[b] = Lk;
+      }
       nt = bad ? 0 : ceil_tiles(L);
     }
     int tot;
@@ -149,13 +208,16 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
   }
 
   // 2. tiles per cost bucket; warp w takes the buckets kmin + w + 32 i
-  const bool keep_empty = p.mode == kQueueBcastFwd;  // empty K/V still owns output rows
+  // items of cost 0 still own outputs: query rows with no key (O = 0, LSE = -inf),
+  // varlen key tiles that no query sees (dK = dV = 0)
+  const bool keep_empty = p.mode == kQueueBcastFwd || var;
   const int kmin = keep_empty ? 0 : 1;
   for (int k = kmin + warp; k <= kmax; k += kWarps) {
     int n = 0;
     for (int b = lane; b < p.batch; b += 32) {
       int c, tf;
-      tiles_with_cost(p, seq_len(s_len, p.offsets, b), k, c, tf);
+      const int2 L = seq_lens(p, s_len, s_lenk, b);
+      tiles_with_cost(p, L.x, L.y, k, c, tf);
       n += c;
     }
     n = warp_sum(n);
@@ -181,16 +243,18 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
   // of a sequence share one cost, the bucket pass only records where each
   // sequence starts and every thread then writes its own sequences' items,
   // so that one large bucket is not written by one warp.
-  const bool one_cost = !(p.causal && (p.mode == kQueueSelfFwd || p.mode == kQueueSelfBwd));
+  const bool one_cost = !p.causal;  // the broadcast modes are never causal
   // The items fit the queue (checked once here; every write below is in range).
   const bool fits = static_cast<int64_t>(total_tiles) * p.heads <= p.max_items;
-  auto write_items = [&](int b, int first, int c, int tf, int k, int L) {
+  auto write_items = [&](int b, int first, int c, int tf, int k, int2 L) {
     if (!fits) return;
-    const int4 seq = make_int4(p.offsets[b], L, p.tile_base ? p.tile_base[b] : 0, 0);
+    const int tb = p.tile_base ? p.tile_base[b] : 0;
+    const int4 seq = var ? make_int4(p.offsets[b], L.x, p.k_offsets[b], L.y) : make_int4(p.offsets[b], L.x, tb, 0);
+    const int w = p.mode == kQueueVarBwd ? tb : k;  // the varlen backward carries the query tile base
     int4* it = p.items + static_cast<int64_t>(first) * p.heads;
     int4* sq = p.item_seq ? p.item_seq + static_cast<int64_t>(first) * p.heads : nullptr;
     for (int r = 0; r < c; ++r)
-      for (int h = 0; h < p.heads; ++h) *it++ = make_int4(b, h, tf + r, k);
+      for (int h = 0; h < p.heads; ++h) *it++ = make_int4(b, h, tf + r, w);
     if (sq)
       for (int e = 0; e < c * p.heads; ++e) *sq++ = seq;
   };
@@ -198,10 +262,11 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
     int run = s_start[k];
     for (int b0 = 0; b0 < p.batch; b0 += 32) {
       const int b = b0 + lane;
-      int c = 0, tf = 0, L = 0;
+      int c = 0, tf = 0;
+      int2 L = make_int2(0, 0);
       if (b < p.batch) {
-        L = seq_len(s_len, p.offsets, b);
-        tiles_with_cost(p, L, k, c, tf);
+        L = seq_lens(p, s_len, s_lenk, b);
+        tiles_with_cost(p, L.x, L.y, k, c, tf);
       }
       int incl = c;
 #pragma unroll
@@ -222,9 +287,9 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
   if (one_cost) {
     __syncthreads();
     for (int b = tid; b < min(p.batch, kQueueLenCache); b += kQThreads) {
-      const int L = s_len[b];
-      const int nt = item_tiles(p, L);
-      const int k = nt > 0 ? item_cost(p, L, 0) : 0;
+      const int2 L = seq_lens(p, s_len, s_lenk, b);
+      const int nt = item_tiles(p, L.x, L.y);
+      const int k = nt > 0 ? item_cost(p, L.x, L.y, 0) : 0;
       if (nt > 0 && k >= kmin) write_items(b, s_first[b], nt, 0, k, L);
     }
   }
@@ -245,14 +310,18 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
 constexpr int kQueueMaxCost = 32 * 1024;
 
 cudaError_t launch_queue(const QueueParams& p, cudaStream_t stream) {
-  const int64_t kmax = (p.mode == kQueueBcastBwd) ? (static_cast<int64_t>(p.q_len) + kTile - 1) / kTile
-                                                   : (static_cast<int64_t>(p.max_seqlen) + kTile - 1) / kTile;
+  auto tiles = [](int64_t L) { return (L + kTile - 1) / kTile; };
+  int64_t kmax = tiles(p.max_seqlen);
+  if (p.mode == kQueueBcastBwd) kmax = tiles(p.q_len);
+  if (p.mode == kQueueVarFwd) kmax = tiles(p.max_seqlen_k);
+  if (p.mode == kQueueVarBwd) kmax = static_cast<int64_t>(p.group) * tiles(p.max_seqlen);
   if (kmax > kQueueMaxCost) return cudaErrorInvalidValue;
-  const size_t smem = static_cast<size_t>(kmax + 1 + kQueueLenCache + std::min(p.batch, kQueueLenCache)) * sizeof(int);
+  const int64_t cached = std::min(p.batch, kQueueLenCache);
+  const size_t smem = static_cast<size_t>(kmax + 1 + kQueueLenCache + cached * (queue_var(p.mode) ? 2 : 1)) * sizeof(int);
   static bool attr_set = false;
   if (!attr_set) {
     const cudaError_t e = cudaFuncSetAttribute(build_queue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>((kQueueMaxCost + 1 + 2 * kQueueLenCache) * sizeof(int)));
+                                               static_cast<int>((kQueueMaxCost + 1 + 3 * kQueueLenCache) * sizeof(int)));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }

@@ -9,6 +9,7 @@ the same seed gives the same bf16 tensors on every machine:
 
 * jagged self-attention: lengths -> Q -> K -> V -> dO
 * broadcast-Q:           lengths -> Q -> K -> V -> dO
+* varlen / GQA:          query lengths -> key lengths -> Q -> K -> V -> dO
 * paged decode:          kv lengths -> page permutation -> Q -> K cache -> V cache
 
 Values are ``torch.randn`` in fp32, then rounded to bf16; the identical bf16
@@ -124,6 +125,40 @@ def dense_causal_inputs(batch: int = 4, seqlen: int = 8192, heads: int = 16, hea
     out = jagged_from_lengths(lengths, heads, head_dim, g, True)
     out["causal"] = True
     return out
+
+
+def varlen_from_lengths(q_lengths, k_lengths, q_heads: int, kv_heads: int, head_dim: int,
+                        g: torch.Generator, with_grad: bool = True) -> dict:
+    """Varlen / GQA case from given lengths: Q, dO [total_q, Hq, d]; K, V [total_k, Hkv, d]."""
+    q_lengths = torch.as_tensor(q_lengths, dtype=torch.int32)
+    k_lengths = torch.as_tensor(k_lengths, dtype=torch.int32)
+    assert q_lengths.numel() == k_lengths.numel()
+    qo, ko = offsets_from_lengths(q_lengths), offsets_from_lengths(k_lengths)
+    tq, tk = int(qo[-1]), int(ko[-1])
+    out = {
+        "q_lengths": q_lengths, "k_lengths": k_lengths,
+        "q_offsets": qo, "k_offsets": ko,
+        "total_q": tq, "total_k": tk,
+        "max_seqlen_q": int(q_lengths.max()) if q_lengths.numel() else 0,
+        "max_seqlen_k": int(k_lengths.max()) if k_lengths.numel() else 0,
+        "q_heads": q_heads, "kv_heads": kv_heads, "head_dim": head_dim,
+        "scale": 1.0 / math.sqrt(head_dim),
+        "q": _randn_bf16((tq, q_heads, head_dim), g),
+        "k": _randn_bf16((tk, kv_heads, head_dim), g),
+        "v": _randn_bf16((tk, kv_heads, head_dim), g),
+    }
+    if with_grad:
+        out["do"] = _randn_bf16((tq, q_heads, head_dim), g)
+    return out
+
+
+def varlen_inputs(batch: int, q_lo: int, q_hi: int, k_lo: int, k_hi: int, q_heads: int, kv_heads: int,
+                  head_dim: int, seed: int = 0, with_grad: bool = True) -> dict:
+    """Varlen / GQA case: query lengths U[q_lo, q_hi], key lengths U[k_lo, k_hi] drawn independently."""
+    g = _gen(seed)
+    ql = uniform_lengths(batch, q_lo, q_hi, g)
+    kl = uniform_lengths(batch, k_lo, k_hi, g)
+    return varlen_from_lengths(ql, kl, q_heads, kv_heads, head_dim, g, with_grad)
 
 
 def broadcast_inputs(batch: int = 512, q_len: int = 256, heads: int = 4, head_dim: int = 128,
