@@ -57,6 +57,22 @@ def pair_count(lengths, causal):
     return tot
 
 
+def var_pair_count(q_lengths, k_lengths, causal):
+    """Visible (query, key) pairs of varlen attention; causal is bottom-right
+    aligned (query i sees keys j <= i + L_k - L_q)."""
+    tot = 0
+    for Lq, Lk in zip(q_lengths, k_lengths):
+        Lq, Lk = int(Lq), int(Lk)
+        if not causal:
+            tot += Lq * Lk
+            continue
+        for_all = max(0, Lq - Lk)  # rows that see no key
+        n = Lq - for_all           # rows i = for_all .. Lq-1 see i + Lk - Lq + 1 keys: 1 .. Lk
+        lo = Lk - n + 1
+        tot += (lo + Lk) * n // 2
+    return tot
+
+
 def attn_flops(lengths, heads, d, causal, kind):
     return (4 if kind == "fwd" else 10) * d * heads * pair_count(lengths, causal)
 
@@ -310,6 +326,27 @@ def measure_extra(jfa, device, peaks):
                                      "bwd_tflops": 10 * d * 16 * pairs / (tb * 1e-3) / 1e12,
                                      "fwd_ms": tf, "bwd_ms": tb}
         del q, k, v, do, o, lse
+    # varlen GQA, chunked-prefill shape: 64 sequences, query chunk L_q U[1, 1024] at the
+    # end of L_k = L_q + U[0, 3072] keys, 32 query heads on 8 KV heads, d 128, causal
+    # (bottom-right aligned)
+    g = torch.Generator().manual_seed(0)
+    ql = inputs.uniform_lengths(64, 1, 1024, g)
+    kl = ql + inputs.uniform_lengths(64, 0, 3072, g)
+    qo, ko = inputs.offsets_from_lengths(ql).to(device), inputs.offsets_from_lengths(kl).to(device)
+    tq, tk = int(ql.sum()), int(kl.sum())
+    mq, mk = int(ql.max()), int(kl.max())
+    q, do = (inputs.randn_bf16_device((tq, 32, 128), 401 + i, device) for i in range(2))
+    k, v = (inputs.randn_bf16_device((tk, 8, 128), 403 + i, device) for i in range(2))
+    sc = 1 / math.sqrt(128)
+    o, lse = jfa.jfa_fwd_varlen(q, k, v, qo, ko, mq, mk, sc, True)
+    tf = time_events(lambda: jfa.jfa_fwd_varlen(q, k, v, qo, ko, mq, mk, sc, True, o=o, lse=lse), 10, 3)
+    tb = time_events(lambda: jfa.jfa_bwd_varlen(q, k, v, o, do, lse, qo, ko, mq, mk, sc, True), 10, 3)
+    pairs = var_pair_count(ql.tolist(), kl.tolist(), True)
+    out["varlen_gqa_prefill"] = {"fwd_tflops": 4 * 128 * 32 * pairs / (tf * 1e-3) / 1e12,
+                                 "bwd_tflops": 10 * 128 * 32 * pairs / (tb * 1e-3) / 1e12, "fwd_ms": tf, "bwd_ms": tb,
+                                 "workload": "64 seqs, L_q U[1,1024], L_k = L_q + U[0,3072], Hq 32 / Hkv 8, d 128, "
+                                             "causal bottom-right"}
+    del q, k, v, do, o, lse
     for sp in (0.1, 0.9):
         w = gem_workload(0, device, sparsity=sp)
         bufs = alloc_bufs(jfa, w, device)
