@@ -63,6 +63,7 @@ __all__ = [
     "split_bounds", "gather_paged", "decode_forward", "decode_split_partials",
     "merge_partials", "tile_queue",
     "lower_right_visible", "varlen_forward", "varlen_backward", "varlen_tile_queue",
+    "split_counts", "split_bounds_per_seq", "decode_smallq_forward", "decode_smallq_split_partials",
 ]
 
 
@@ -422,3 +423,102 @@ def varlen_tile_queue(q_offsets, k_offsets, q_heads, kv_heads, causal, kind, til
                     items.append((-cost, b, u, g))
     items.sort()
     return [(b, h, t) for (_, b, t, h) in items]
+
+
+# ----------------------------------------------------------------------------
+# Small-query paged decode: several query tokens per sequence
+# ----------------------------------------------------------------------------
+#
+# "Optimizing FlashAttention-4 for Efficient Inference" (hpjadul), section
+# "PR 1993" (tiles sized to few query rows, e.g. speculative decoding), with
+# the split-KV (PR 1940), paging (PR 1999 / PR 2104) and GQA packing (PR 2186)
+# of the one-token decode. Reading (the page gives no layout): sequence b
+# holds L_b tokens in the cache, the last q_len of them are the new queries;
+# query i sits at key position L_b - q_len + i and sees keys j <= that
+# position (the bottom-right causal reading of varlen_forward).
+
+def split_counts(seqlens, num_splits, min_split_tokens):
+    """Per-sequence split count: num_splits, or with min_split_tokens > 0,
+    clamp(ceil(L_b / min_split_tokens), 1, num_splits)."""
+    out = []
+    for L in (int(x) for x in np.asarray(seqlens).reshape(-1)):
+        if min_split_tokens > 0:
+            out.append(max(1, min(int(num_splits), -(-L // int(min_split_tokens)))))
+        else:
+            out.append(int(num_splits))
+    return np.asarray(out, dtype=np.int64)
+
+
+def split_bounds_per_seq(seqlens, num_splits, counts):
+    """int64 [B, num_splits, 2]: sequence b is split into counts[b] parts with
+    c_b = ceil(L_b / counts[b]), part s covering [s c_b, min((s+1) c_b, L_b));
+    parts s >= counts[b] (and parts starting at or past L_b) are (L_b, L_b)."""
+    seqlens = [int(x) for x in np.asarray(seqlens).reshape(-1)]
+    out = np.zeros((len(seqlens), int(num_splits), 2), dtype=np.int64)
+    for b, L in enumerate(seqlens):
+        Sb = int(counts[b])
+        c = -(-L // Sb) if L > 0 else 0
+        for s in range(int(num_splits)):
+            if s < Sb:
+                out[b, s] = (min(s * c, L), min((s + 1) * c, L))
+            else:
+                out[b, s] = (L, L)
+    return out
+
+
+def _smallq_one(qb, Kb, Vb, scale, causal=True):
+    """qb [q_len, Hq, d] against gathered Kb, Vb [L, Hkv, d] of one sequence."""
+    ql, L = qb.shape[0], Kb.shape[0]
+    return varlen_forward(qb, Kb, Vb, [0, ql], [0, L], scale, causal)
+
+
+def decode_smallq_forward(q, k_cache, v_cache, page_table, seqlens, page_size, scale, batch_ids=None):
+    """Unsplit small-query paged decode. q [B, q_len, Hq, d]; caches
+    [num_pages, P, Hkv, d]. Returns O [B, q_len, Hq, d] and LSE [B, q_len, Hq]
+    (rows of `batch_ids` only, if given)."""
+    B, ql, Hq, d = q.shape
+    ids = range(B) if batch_ids is None else batch_ids
+    O = np.zeros((B, ql, Hq, d), dtype=np.float64)
+    LSE = np.full((B, ql, Hq), -np.inf, dtype=np.float64)
+    for b in ids:
+        L = int(seqlens[b])
+        Kb = gather_paged(k_cache, page_table[b], L, page_size)
+        Vb = gather_paged(v_cache, page_table[b], L, page_size)
+        if L == 0:
+            continue
+        Ob, Lb = _smallq_one(q[b], Kb, Vb, scale)
+        O[b], LSE[b] = Ob, Lb.T
+    return O, LSE
+
+
+def decode_smallq_split_partials(q, k_cache, v_cache, page_table, seqlens, page_size, scale, num_splits,
+                                 min_split_tokens=0):
+    """Per-split partials of the small-query decode: O_s [S, B, q_len, Hq, d]
+    (normalised within the split) and lse_s [S, B, q_len, Hq] (-inf where the
+    split holds no key visible to the row). Keys outside a split are dropped;
+    the causal limit of each query row is the unsplit one."""
+    B, ql, Hq, d = q.shape
+    counts = split_counts(seqlens, num_splits, min_split_tokens)
+    bounds = split_bounds_per_seq(seqlens, num_splits, counts)
+    Os = np.zeros((num_splits, B, ql, Hq, d), dtype=np.float64)
+    lses = np.full((num_splits, B, ql, Hq), -np.inf, dtype=np.float64)
+    for b in range(B):
+        L = int(seqlens[b])
+        Kb = gather_paged(k_cache, page_table[b], L, page_size)
+        Vb = gather_paged(v_cache, page_table[b], L, page_size)
+        group = Hq // Kb.shape[1]
+        for s in range(num_splits):
+            lo, hi = (int(x) for x in bounds[b, s])
+            if hi == lo:
+                continue
+            for i in range(ql):
+                pos = L - ql + i  # key position of query i
+                for h in range(Hq):
+                    keys = [j for j in range(lo, hi) if j <= pos]
+                    if not keys:
+                        continue
+                    Oh, lse, _ = _head_forward(q[b, i, h][None], Kb[keys, h // group], Vb[keys, h // group], scale,
+                                               False)
+                    Os[s, b, i, h] = Oh[0]
+                    lses[s, b, i, h] = lse[0]
+    return Os, lses

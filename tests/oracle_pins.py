@@ -543,4 +543,84 @@ def pin_varlen_tile_queue(o):
             assert keys == sorted(keys), (causal, kind)
 
 
+
+# ---------------------------------------------------------------- small-query paged decode
+
+def pin_golden_smallq_decode(o):
+    c = golden()["smallq_paged_decode"]
+    args = (_arr(c["q"]), _arr(c["k_cache"]), _arr(c["v_cache"]), np.asarray(c["page_table"]),
+            np.asarray(c["seqlens"]), c["page_size"], _ev(c["scale"]))
+    O, LSE = o.decode_smallq_forward(*args)
+    _close(O, _arr(c["o"]), 1e-13, "small-query decode O")
+    _close(LSE, _arr(c["lse"]), 1e-13, "small-query decode LSE")
+    for S in (1, 2, 3):
+        Os, ls = o.decode_smallq_split_partials(*args, S)
+        O2, L2 = o.merge_partials(Os, ls)
+        _close(O2, _arr(c["o"]), 1e-13, f"small-query split {S} O")
+        _close(L2, _arr(c["lse"]), 1e-13, f"small-query split {S} LSE")
+
+
+def pin_golden_dynamic_split_counts(o):
+    c = golden()["dynamic_split_counts"]
+    got = o.split_counts(np.asarray(c["seqlens"]), c["num_splits"], c["min_split_tokens"])
+    assert got.tolist() == c["counts"], got.tolist()
+    b = o.split_bounds_per_seq([1000], 6, [4])[0]
+    assert b.tolist() == c["bounds_1000_of_6"], b.tolist()
+    # without a minimum every sequence takes num_splits parts (the one-token decode rule)
+    assert o.split_counts([5, 0, 99], 7, 0).tolist() == [7, 7, 7]
+    assert (o.split_bounds_per_seq([10, 2, 0], 4, [4, 4, 4]) == o.split_bounds([10, 2, 0], 4)).all()
+
+
+def pin_smallq_brute_force(o):
+    """Pure-Python loops: gather each token through the page table by hand,
+    query i of q_len sits at key position L - q_len + i."""
+    r = _rng(41)
+    lengths, ql, Hq, Hkv, d, P = [5, 2, 7], 3, 4, 2, 2, 3
+    _, kc, vc, pt = _random_paged(r, lengths, Hq, Hkv, d, P)
+    q = r.standard_normal((len(lengths), ql, Hq, d))
+    O, LSE = o.decode_smallq_forward(q, kc, vc, pt, np.array(lengths), P, 0.8)
+    for b, L in enumerate(lengths):
+        for i in range(ql):
+            pos = L - ql + i
+            for h in range(Hq):
+                g = h // (Hq // Hkv)
+                keys = [j for j in range(L) if j <= pos]
+                if not keys:
+                    assert np.all(O[b, i, h] == 0.0) and LSE[b, i, h] == -np.inf
+                    continue
+                rows_k = [kc[int(pt[b][j // P]), j % P, g] for j in keys]
+                rows_v = [vc[int(pt[b][j // P]), j % P, g] for j in keys]
+                sc = [0.8 * sum(q[b, i, h, c] * kr[c] for c in range(d)) for kr in rows_k]
+                z = sum(math.exp(x) for x in sc)
+                out = [sum(math.exp(sc[n]) / z * rows_v[n][c] for n in range(len(keys))) for c in range(d)]
+                _close(O[b, i, h], out, 1e-13, "small-query brute-force O")
+                _close(LSE[b, i, h], math.log(z), 1e-13, "small-query brute-force LSE")
+
+
+def pin_smallq_reduces_to_decode(o):
+    """One query token per sequence is the one-token paged decode."""
+    r = _rng(42)
+    lengths, Hq, Hkv, d, P = [9, 1, 0, 17], 8, 2, 4, 4
+    _, kc, vc, pt = _random_paged(r, lengths, Hq, Hkv, d, P)
+    q = r.standard_normal((len(lengths), 1, Hq, d))
+    O, LSE = o.decode_smallq_forward(q, kc, vc, pt, np.array(lengths), P, 0.5)
+    O1, L1 = o.decode_forward(q[:, 0], kc, vc, pt, np.array(lengths), P, 0.5)
+    _close(O[:, 0], O1, 1e-14, "q_len 1 O")
+    _close(LSE[:, 0], L1, 1e-14, "q_len 1 LSE")
+
+
+def pin_smallq_split_merge(o):
+    """Splits with per-sequence counts, merged, equal the unsplit result."""
+    r = _rng(43)
+    lengths, ql, Hq, Hkv, d, P = [40, 3, 1, 0, 25], 4, 4, 1, 3, 5
+    _, kc, vc, pt = _random_paged(r, lengths, Hq, Hkv, d, P)
+    q = r.standard_normal((len(lengths), ql, Hq, d))
+    O, LSE = o.decode_smallq_forward(q, kc, vc, pt, np.array(lengths), P, 0.7)
+    for S, mn in ((1, 0), (3, 0), (8, 0), (8, 10), (5, 7)):
+        Os, ls = o.decode_smallq_split_partials(q, kc, vc, pt, np.array(lengths), P, 0.7, S, mn)
+        O2, L2 = o.merge_partials(Os, ls)
+        _close(O2, O, 1e-12, f"small-query split {S}/{mn} O")
+        _close(L2, LSE, 1e-12, f"small-query split {S}/{mn} LSE")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

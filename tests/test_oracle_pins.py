@@ -159,6 +159,27 @@ def _varlen_dk_last_head(m):
     m.varlen_backward = bwd
 
 
+def _smallq_top_left(m):
+    # query i of the small-query decode sees keys 0..i (its position counted from the start)
+    def one(qb, Kb, Vb, scale, causal=True):
+        ql, L = qb.shape[0], Kb.shape[0]
+        if ql <= L:
+            O, lse = real_oracle.varlen_forward(qb, Kb[:ql], Vb[:ql], [0, ql], [0, ql], scale, True)
+            return O, lse
+        return real_oracle.varlen_forward(qb, Kb, Vb, [0, ql], [0, L], scale, causal)
+    m._smallq_one = one
+
+
+def _split_counts_floor(m):
+    # floor instead of ceiling in the per-sequence split count
+    def counts(seqlens, num_splits, min_split_tokens):
+        out = []
+        for L in (int(x) for x in np.asarray(seqlens).reshape(-1)):
+            out.append(max(1, min(num_splits, L // min_split_tokens)) if min_split_tokens > 0 else num_splits)
+        return np.asarray(out, dtype=np.int64)
+    m.split_counts = counts
+
+
 MUTANTS = {
     "bwd_drop_delta": _bwd_variant("drop_delta"),
     "bwd_sign_dS": _bwd_variant("sign_dS"),
@@ -175,6 +196,8 @@ MUTANTS = {
     "varlen_top_left": _varlen_top_left,
     "varlen_gqa_modulo": _varlen_gqa_modulo,
     "varlen_dk_last_head": _varlen_dk_last_head,
+    "smallq_top_left": _smallq_top_left,
+    "split_counts_floor": _split_counts_floor,
 }
 
 
