@@ -232,9 +232,10 @@ def time_events(fn, iters, warmup):
     return s.elapsed_time(e) / iters
 
 
-def measure_decode(jfa, device, peaks, page_size=16, splits=(8, 16, 32, 64), iters=20):
+def measure_decode(jfa, device, peaks, page_size=16, splits=(8, 16, 32, 64), iters=20, q_len=1):
     """Split-KV paged GQA decode: batch 32, 32/8 heads, d 128, KV lengths in
-    [1024, 32768], random page permutation. Returns the best split count."""
+    [1024, 32768], random page permutation; q_len > 1 runs the small-query
+    decode (q_len new tokens per sequence). Returns the best split count."""
     import torch
     from varlen_flashattention_gb300 import inputs
     g = torch.Generator().manual_seed(0)
@@ -247,12 +248,12 @@ def measure_decode(jfa, device, peaks, page_size=16, splits=(8, 16, 32, 64), ite
     for b, m in enumerate(pages):
         pt[b, :m] = perm[c:c + m]
         c += m
-    q = inputs.randn_bf16_device((32, 32, 128), 101, device)
+    q = inputs.randn_bf16_device((32, 32, 128) if q_len == 1 else (32, q_len, 32, 128), 101, device)
     kc = inputs.randn_bf16_device((n, page_size, 8, 128), 102, device)
     vc = inputs.randn_bf16_device((n, page_size, 8, 128), 103, device)
     pt, sl_d = pt.to(device), sl.to(device)
     o = torch.empty_like(q)
-    lse = torch.empty((32, 32), dtype=torch.float32, device=device)
+    lse = torch.empty((32, 32) if q_len == 1 else (32, q_len, 32), dtype=torch.float32, device=device)
     # algorithmic bytes: K + V rows read, Q, O, LSE and the page-table entries used
     nbytes = int(sl.sum()) * 2 * 8 * 128 * 2 + q.numel() * 2 * 2 + lse.numel() * 4 + sum(pages) * 4
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # 256 MB > L2, cleared between runs
@@ -261,18 +262,30 @@ def measure_decode(jfa, device, peaks, page_size=16, splits=(8, 16, 32, 64), ite
         ws = torch.empty(1, dtype=torch.uint8, device=device)
         from varlen_flashattention_gb300 import _abi
         import ctypes
-        da = _abi.DecodeArgs(None, None, None, None, None, 32, 32, 8, 128, page_size, n, pt.shape[1], S, 0.1,
-                             None, None, None, None)
-        ws = torch.empty(jfa.library().jfa_decode_workspace_size(ctypes.byref(da)), dtype=torch.uint8, device=device)
+        if q_len == 1:
+            da = _abi.DecodeArgs(None, None, None, None, None, 32, 32, 8, 128, page_size, n, pt.shape[1], S, 0.1,
+                                 None, None, None, None)
+            nbytes_ws = jfa.library().jfa_decode_workspace_size(ctypes.byref(da))
+        else:
+            da = _abi.DecodeSmallqArgs(None, None, None, None, None, 32, q_len, 32, 8, 128, page_size, n,
+                                       pt.shape[1], S, 0, 0.1, None, None, None, None, None)
+            nbytes_ws = jfa.library().jfa_decode_smallq_workspace_size(ctypes.byref(da))
+        ws = torch.empty(nbytes_ws, dtype=torch.uint8, device=device)
         ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+
+        def call(events=None):
+            if q_len == 1:
+                jfa.jfa_decode_splitkv(q, kc, vc, pt, sl_d, S, o=o, lse=lse, workspace=ws, events=events)
+            else:
+                jfa.jfa_decode_smallq(q, kc, vc, pt, sl_d, S, o=o, lse=lse, workspace=ws, events=events)
         for _ in range(3):
-            jfa.jfa_decode_splitkv(q, kc, vc, pt, sl_d, S, o=o, lse=lse, workspace=ws)
+            call()
         times = []
         for _ in range(iters):
             flush.zero_()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record()
-            jfa.jfa_decode_splitkv(q, kc, vc, pt, sl_d, S, o=o, lse=lse, workspace=ws, events=ev)
+            call(ev)
             e.record()
             torch.cuda.synchronize()
             times.append((s.elapsed_time(e), ev[0].elapsed_time(ev[1])))
@@ -283,7 +296,8 @@ def measure_decode(jfa, device, peaks, page_size=16, splits=(8, 16, 32, 64), ite
         if best is None or r["tb_s"] > best["tb_s"]:
             best = r
     best["frac_of_measured_hbm"] = best["tb_s"] * 1e3 / peaks["hbm_gbs"]
-    best.update({"workload": f"paged GQA decode: batch 32, Hq 32 / Hkv 8, d 128, L_k U[1024,32768], page {page_size}",
+    best.update({"workload": f"paged GQA decode: batch 32, {q_len} query token(s) each, Hq 32 / Hkv 8, d 128, "
+                             f"L_k U[1024,32768], page {page_size}",
                  "algorithmic_bytes": nbytes, "l2": "256 MB buffer written between runs"})
     return best
 
@@ -560,6 +574,7 @@ def main():
         torch.cuda.empty_cache()
         try:
             decode = measure_decode(jfa, device, peaks)
+            detail["decode_smallq_q4"] = measure_decode(jfa, device, peaks, splits=(16, 32), q_len=4)
             detail.update(measure_extra(jfa, device, peaks))
         except Exception as ex:  # report, never hide
             detail["extra_error"] = repr(ex)

@@ -255,6 +255,41 @@ typedef struct {
   void* main_kernel_events;  /* optional cudaEvent_t[2] around the split kernel */
 } jfa_decode_args;
 
+/* ------------------------------------------------------------------ small-query paged decode
+ * Paged split-KV GQA decode with q_len >= 1 query tokens per sequence ([INF]
+ * PR 1993: tiles sized to few query rows, e.g. speculative decoding; with the
+ * paging, KV splitting and GQA packing of jfa_decode_splitkv). Reading (the
+ * page gives no layout): the q_len new tokens of sequence b are the last q_len
+ * tokens of its cache (L_b already counts them); query token i sits at key
+ * position L_b - q_len + i and sees keys j <= L_b - q_len + i. A query row
+ * that sees no key (L_b < q_len - i) gets O = 0, LSE = -inf.
+ * The q_len x (q_heads / kv_heads) (token, head) rows of one KV head form one
+ * tile; that product must be <= 16.
+ * Splits: with min_split_tokens = 0 every sequence takes num_splits parts;
+ * with min_split_tokens > 0 sequence b takes
+ *   S_b = clamp(ceil(L_b / min_split_tokens), 1, num_splits)
+ * parts (short sequences are not spread thin); part s < S_b covers
+ * [s c_b, min((s+1) c_b, L_b)) with c_b = ceil(L_b / S_b), parts s >= S_b are
+ * empty, reported as (L_b, L_b). The merge is that of jfa_decode_splitkv.
+ * head_dim must be 128. */
+typedef struct {
+  const void* q;              /* bf16 [batch, q_len, q_heads, head_dim] */
+  const void* k_cache;        /* bf16 [num_pages, page_size, kv_heads, head_dim] */
+  const void* v_cache;        /* bf16 [num_pages, page_size, kv_heads, head_dim] */
+  const int32_t* page_table;  /* int32 [batch, max_pages] */
+  const int32_t* seqlens_k;   /* int32 [batch], 0 <= L_b <= max_pages*page_size, new tokens included */
+  int32_t batch, q_len, q_heads, kv_heads, head_dim;
+  int32_t page_size, num_pages, max_pages;
+  int32_t num_splits;         /* 1 .. 128: split slots (the upper bound of S_b) */
+  int32_t min_split_tokens;   /* 0, or the fewest tokens per part when choosing S_b */
+  float scale;
+  void* o;                    /* out: bf16 [batch, q_len, q_heads, head_dim] */
+  float* lse;                 /* out: fp32 [batch, q_len, q_heads] */
+  int32_t* split_bounds_out;  /* optional out: int32 [batch, num_splits, 2] */
+  int32_t* split_counts_out;  /* optional out: int32 [batch], S_b */
+  void* main_kernel_events;   /* optional cudaEvent_t[2] around the split kernel */
+} jfa_decode_smallq_args;
+
 /* Workspace sizes in bytes (0 only when args is NULL). */
 JFA_API size_t jfa_fwd_workspace_size(const jfa_fwd_args* args);
 JFA_API size_t jfa_bwd_workspace_size(const jfa_bwd_args* args);
@@ -263,6 +298,7 @@ JFA_API size_t jfa_bcast_bwd_workspace_size(const jfa_bcast_bwd_args* args);
 JFA_API size_t jfa_decode_workspace_size(const jfa_decode_args* args);
 JFA_API size_t jfa_varlen_fwd_workspace_size(const jfa_varlen_fwd_args* args);
 JFA_API size_t jfa_varlen_bwd_workspace_size(const jfa_varlen_bwd_args* args);
+JFA_API size_t jfa_decode_smallq_workspace_size(const jfa_decode_smallq_args* args);
 
 /* Entry points. `workspace` is device memory of at least the size above,
  * 256-byte aligned; its contents on entry do not matter. */
@@ -278,6 +314,8 @@ JFA_API jfa_status jfa_fwd_varlen(const jfa_varlen_fwd_args* args, void* workspa
                           cudaStream_t stream);
 JFA_API jfa_status jfa_bwd_varlen(const jfa_varlen_bwd_args* args, void* workspace, size_t workspace_bytes,
                           cudaStream_t stream);
+JFA_API jfa_status jfa_decode_smallq(const jfa_decode_smallq_args* args, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream);
 
 /* Paged split-KV decode that allocates nothing. The pages have no
  * counterpart for this entry point; it exists for callers that cannot

@@ -25,6 +25,7 @@ STRUCTS = {
     "jfa_decode_args": _abi.DecodeArgs,
     "jfa_varlen_fwd_args": _abi.VarlenFwdArgs,
     "jfa_varlen_bwd_args": _abi.VarlenBwdArgs,
+    "jfa_decode_smallq_args": _abi.DecodeSmallqArgs,
 }
 
 
@@ -171,6 +172,26 @@ def test_varlen_validation(lib):
     assert nb >= 150 * 8 * 128 * 4
     assert lib.jfa_fwd_varlen(P(fargs()), FAKE, nf - 1, None) == _abi.JFA_ERR_WORKSPACE_TOO_SMALL
     assert lib.jfa_bwd_varlen(P(bargs()), FAKE, nb - 1, None) == _abi.JFA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_decode_smallq_validation(lib):
+    P = ctypes.byref
+
+    def args(**kw):
+        a = _abi.DecodeSmallqArgs(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 32, 8, 128, 16, 100, 10, 8, 0, 0.1,
+                                  FAKE, FAKE, None, None, None)
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+    for bad in (dict(q_len=0), dict(num_splits=0), dict(min_split_tokens=-1), dict(q_heads=30),
+                dict(split_counts_out=FAKE + 2)):
+        assert lib.jfa_decode_smallq(P(args(**bad)), FAKE, 1 << 30, None) == _abi.JFA_ERR_INVALID_ARG, bad
+    # the (token, head) rows of one KV head must fit one 16-row tile
+    assert lib.jfa_decode_smallq(P(args(q_len=5)), FAKE, 1 << 30, None) == _abi.JFA_ERR_UNSUPPORTED
+    assert lib.jfa_decode_smallq(P(args(head_dim=64)), FAKE, 1 << 30, None) == _abi.JFA_ERR_UNSUPPORTED
+    need = lib.jfa_decode_smallq_workspace_size(P(args()))
+    assert need >= 8 * 4 * 4 * 32 * 128 * 4
+    assert lib.jfa_decode_smallq(P(args()), FAKE, need - 1, None) == _abi.JFA_ERR_WORKSPACE_TOO_SMALL
 
 
 def test_binding_rejects_cpu_tensors():

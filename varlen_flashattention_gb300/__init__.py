@@ -13,6 +13,7 @@ kernels; there is no CPU or PyTorch fallback.
     jfa_decode_splitkv    split-KV decode over a paged GQA cache -> (O, LSE)
     jfa_fwd_varlen        separate query / key lengths, grouped KV heads -> (O, LSE)
     jfa_bwd_varlen        its backward -> (dQ, dK, dV)
+    jfa_decode_smallq     paged split-KV decode of a few query tokens per sequence -> (O, LSE)
     jagged_attention      autograd wrapper of jfa_fwd / jfa_bwd
     varlen_attention      autograd wrapper of jfa_fwd_varlen / jfa_bwd_varlen
 """
@@ -28,7 +29,7 @@ from . import _abi
 __all__ = [
     "JfaError", "jfa_fwd", "jfa_bwd", "jfa_fwd_broadcast_q", "jfa_bwd_broadcast_q", "jfa_decode_splitkv",
     "jfa_read_device_status", "jagged_attention", "library", "jfa_fwd_varlen", "jfa_bwd_varlen",
-    "varlen_attention",
+    "varlen_attention", "jfa_decode_smallq",
 ]
 
 
@@ -297,6 +298,40 @@ def jfa_decode_splitkv(q, k_cache, v_cache, page_table, seqlens_k, num_splits, s
     ws = _workspace(lib.jfa_decode_workspace_size(ctypes.byref(a)), q.device, workspace)
     _check(lib.jfa_decode_splitkv(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_decode_splitkv")
     _finish(ws, check, stream, "jfa_decode_splitkv")
+    return o, lse
+
+
+def jfa_decode_smallq(q, k_cache, v_cache, page_table, seqlens_k, num_splits, min_split_tokens=0, scale=None,
+                      o=None, lse=None, split_bounds=None, split_counts=None, workspace=None, stream=None,
+                      events=None, check=False):
+    """Paged split-KV decode of q_len new tokens per sequence (speculative / chunked decode).
+    q: bf16 [B, q_len, Hq, 128]; caches bf16 [num_pages, page_size, Hkv, 128]; page_table int32
+    [B, max_pages]; seqlens_k int32 [B] (new tokens included: token i of q_len sits at key position
+    L - q_len + i and sees keys up to it). Returns O bf16 [B, q_len, Hq, 128], LSE fp32 [B, q_len, Hq].
+    With min_split_tokens > 0 each sequence uses clamp(ceil(L / min_split_tokens), 1, num_splits)
+    splits; `split_counts` (int32 [B]) and `split_bounds` (int32 [B, S, 2]) receive them if given."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(seqlens_k, "seqlens_k", torch.int32, 1)
+    B, ql, Hq, d = q.shape
+    num_pages, P, Hkv, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shapes do not match q")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, ql, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    a = _abi.DecodeSmallqArgs(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(seqlens_k),
+                              B, ql, Hq, Hkv, d, P, num_pages, page_table.shape[1], int(num_splits),
+                              int(min_split_tokens), scale, _ptr(o), _ptr(lse), _ptr(split_bounds),
+                              _ptr(split_counts), None)
+    ev, _keep = _events(events)
+    a.main_kernel_events = ev
+    lib = library()
+    ws = _workspace(lib.jfa_decode_smallq_workspace_size(ctypes.byref(a)), q.device, workspace)
+    _check(lib.jfa_decode_smallq(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_decode_smallq")
+    _finish(ws, check, stream, "jfa_decode_smallq")
     return o, lse
 
 

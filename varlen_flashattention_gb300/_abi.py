@@ -82,6 +82,16 @@ class VarlenBwdArgs(ctypes.Structure):
                 ("dq", c_void_p), ("dk", c_void_p), ("dv", c_void_p), ("main_kernel_events", c_void_p)]
 
 
+class DecodeSmallqArgs(ctypes.Structure):
+    _fields_ = [("q", c_void_p), ("k_cache", c_void_p), ("v_cache", c_void_p), ("page_table", c_void_p),
+                ("seqlens_k", c_void_p),
+                ("batch", c_i32), ("q_len", c_i32), ("q_heads", c_i32), ("kv_heads", c_i32), ("head_dim", c_i32),
+                ("page_size", c_i32), ("num_pages", c_i32), ("max_pages", c_i32), ("num_splits", c_i32),
+                ("min_split_tokens", c_i32), ("scale", c_f32),
+                ("o", c_void_p), ("lse", c_void_p), ("split_bounds_out", c_void_p), ("split_counts_out", c_void_p),
+                ("main_kernel_events", c_void_p)]
+
+
 # (name, argtypes, restype) of every exported symbol declared in include/jfa.h
 SIGNATURES = [
     ("jfa_fwd_workspace_size", [ctypes.POINTER(FwdArgs)], ctypes.c_size_t),
@@ -91,6 +101,7 @@ SIGNATURES = [
     ("jfa_decode_workspace_size", [ctypes.POINTER(DecodeArgs)], ctypes.c_size_t),
     ("jfa_varlen_fwd_workspace_size", [ctypes.POINTER(VarlenFwdArgs)], ctypes.c_size_t),
     ("jfa_varlen_bwd_workspace_size", [ctypes.POINTER(VarlenBwdArgs)], ctypes.c_size_t),
+    ("jfa_decode_smallq_workspace_size", [ctypes.POINTER(DecodeSmallqArgs)], ctypes.c_size_t),
     ("jfa_fwd", [ctypes.POINTER(FwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_bwd", [ctypes.POINTER(BwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_fwd_broadcast_q", [ctypes.POINTER(BcastFwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
@@ -98,6 +109,7 @@ SIGNATURES = [
     ("jfa_decode_splitkv", [ctypes.POINTER(DecodeArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_fwd_varlen", [ctypes.POINTER(VarlenFwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_bwd_varlen", [ctypes.POINTER(VarlenBwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
+    ("jfa_decode_smallq", [ctypes.POINTER(DecodeSmallqArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_decode_splitkv_noalloc", [ctypes.POINTER(DecodeArgs), c_void_p], c_i32),
     ("jfa_read_device_status", [c_void_p, c_void_p, ctypes.POINTER(c_i32)], c_i32),
     ("jfa_status_string", [c_i32], ctypes.c_char_p),

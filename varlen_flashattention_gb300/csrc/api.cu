@@ -199,6 +199,18 @@ Layout var_layout(int64_t batch, int64_t q_heads, int64_t kv_heads, int64_t tota
   return L;
 }
 
+// Small-query decode: the split partials of every (sequence, token, head) row.
+Layout smallq_layout(int64_t batch, int64_t q_len, int64_t q_heads, int64_t splits) {
+  Layout L;
+  size_t off = kStatusBytes;
+  L.part_o = off;
+  off = align_up(off + 4 * splits * batch * q_len * q_heads * 128, 256);
+  L.part_lse = off;
+  off = align_up(off + 4 * splits * batch * q_len * q_heads, 256);
+  L.bytes = off;
+  return L;
+}
+
 Layout decode_layout(int64_t batch, int64_t q_heads, int64_t splits) {
   Layout L;
   size_t off = kStatusBytes;
@@ -794,6 +806,62 @@ jfa_status jfa_bwd_varlen(const jfa_varlen_bwd_args* a, void* ws, size_t ws_byte
   record(a->main_kernel_events, 1, stream);
   if (e != cudaSuccess) return JFA_ERR_CUDA;
   return cuda_status(launch_bwd_post(dq_acc, a->dq, n_acc, a->scale, status, sms, stream));
+}
+
+size_t jfa_decode_smallq_workspace_size(const jfa_decode_smallq_args* a) {
+  if (!a) return 0;
+  return smallq_layout(a->batch, a->q_len, a->q_heads, a->num_splits).bytes;
+}
+
+jfa_status jfa_decode_smallq(const jfa_decode_smallq_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!a) return JFA_ERR_INVALID_ARG;
+  if (a->batch < 0 || a->q_len < 1 || a->q_heads < 1 || a->kv_heads < 1 || a->page_size < 1 || a->num_pages < 0 ||
+      a->max_pages < 0 || a->num_splits < 1 || a->num_splits > 128 || a->min_split_tokens < 0)
+    return JFA_ERR_INVALID_ARG;
+  if (a->q_heads % a->kv_heads != 0) return JFA_ERR_INVALID_ARG;
+  const int g = a->q_heads / a->kv_heads;
+  if (a->head_dim != 128 || !(g == 1 || g == 2 || g == 4 || g == 8 || g == 16)) return JFA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(g) * a->q_len > 16) return JFA_ERR_UNSUPPORTED;  // rows of one tile
+  if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return JFA_ERR_INVALID_ARG;
+  if (a->batch > 0) {
+    if (!aligned(a->q, 16) || !aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->o, 16) ||
+        !aligned(a->lse, 4) || !aligned(a->page_table, 4) || !aligned(a->seqlens_k, 4))
+      return JFA_ERR_INVALID_ARG;
+    if (a->split_bounds_out && !aligned(a->split_bounds_out, 4)) return JFA_ERR_INVALID_ARG;
+    if (a->split_counts_out && !aligned(a->split_counts_out, 4)) return JFA_ERR_INVALID_ARG;
+  }
+  if (static_cast<int64_t>(a->max_pages) * a->page_size >= (int64_t(1) << 31)) return JFA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(a->batch) * a->q_len * a->q_heads >= (int64_t(1) << 31)) return JFA_ERR_INVALID_ARG;
+  const Layout L = smallq_layout(a->batch, a->q_len, a->q_heads, a->num_splits);
+  if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
+  if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (a->batch == 0) return JFA_OK;
+  DecodeLaunch d;
+  d.q = a->q;
+  d.k_cache = a->k_cache;
+  d.v_cache = a->v_cache;
+  d.page_table = a->page_table;
+  d.seqlens_k = a->seqlens_k;
+  d.batch = a->batch;
+  d.q_len = a->q_len;
+  d.q_heads = a->q_heads;
+  d.kv_heads = a->kv_heads;
+  d.page_size = a->page_size;
+  d.num_pages = a->num_pages;
+  d.max_pages = a->max_pages;
+  d.num_splits = a->num_splits;
+  d.min_split_tokens = a->min_split_tokens;
+  d.scale = a->scale;
+  d.o = a->o;
+  d.lse = a->lse;
+  d.split_bounds_out = a->split_bounds_out;
+  d.split_counts_out = a->split_counts_out;
+  d.main_kernel_events = a->main_kernel_events;
+  return cuda_status(launch_decode_general(d, reinterpret_cast<float*>(w + L.part_o),
+                                           reinterpret_cast<float*>(w + L.part_lse), reinterpret_cast<int32_t*>(w),
+                                           stream));
 }
 
 jfa_status jfa_read_device_status(const void* ws, cudaStream_t stream, int32_t* detail) {

@@ -1,6 +1,6 @@
-// Split-KV paged GQA decode: one query token per sequence against a KV cache
-// addressed through a page table, the KV range split into parallel parts
-// whose partial softmax results are merged by a second kernel.
+// Split-KV paged GQA decode: one or a few query tokens per sequence against a
+// KV cache addressed through a page table, the KV range split into parallel
+// parts whose partial softmax results are merged by a second kernel.
 //
 // Sources: "Optimizing FlashAttention-4 for Efficient Inference" (hpjadul),
 // sections PR 1940 (parallelism across the KV dimension), PR 1999 / PR 2104
@@ -21,6 +21,14 @@
 // back the pieces it copied, so the ring needs no synchronisation beyond the
 // lane's own cp.async groups, and its layout (piece j of lane l at
 // [j][l]) makes every warp-wide copy and read 512 contiguous bytes.
+//
+// Several query tokens ("Optimizing FlashAttention-4 for Efficient
+// Inference", PR 1993: tiles sized to few query rows): the q_len new tokens of
+// a sequence are its last q_len cache positions; query i sits at key position
+// L - q_len + i and sees keys up to it. The rows of the MMA tile are the
+// (token, head) pairs of one KV head, row r = token (r / G), head (r % G), at
+// most 16 rows; each row carries its own causal limit. A split count may be
+// chosen per sequence: S_b = clamp(ceil(L_b / min_split_tokens), 1, S).
 //
 // Index mappings used below (each lane: g = lane / 4, q = lane % 4):
 //  * QK^T: head dimension permuted so that each lane's four k-values of
@@ -46,9 +54,12 @@ struct DecodeParams {
   const int32_t* page_table;
   const int32_t* seqlens;
   int32_t batch, hq, hkv, page_size, num_pages, max_pages, num_splits;
+  int32_t q_len;        // query tokens per sequence (rows of a tile: G * q_len <= 16)
+  int32_t min_split;    // > 0: per-sequence split count clamp(ceil(L / min_split), 1, num_splits)
+  int32_t* counts_out;  // optional [B]: the split count of each sequence
   float scale_log2;
-  float* part_o;        // [S, B, Hq, 128], normalised within the split
-  float* part_lse;      // [S, B, Hq], natural log, -inf when empty
+  float* part_o;        // [S, B, q_len, Hq, 128], normalised within the split
+  float* part_lse;      // [S, B, q_len, Hq], natural log, -inf when empty
   int32_t* bounds_out;  // optional [B, S, 2]
   int32_t* status;
 };
@@ -82,21 +93,26 @@ __device__ __forceinline__ void flag_bad(int32_t* status, int32_t code) {
   if (atomicCAS(status, JFA_OK, JFA_ERR_BAD_INPUT) == JFA_OK) status[1] = code;
 }
 
-template <int G>
+// Rows of a tile: G query heads x q_len tokens. TWO: rows 8..15 are in use.
+template <int G, bool TWO>
 __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecodeParams p) {
   static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "GQA group");
-  constexpr bool kTwoRowHalves = (G == 16);  // rows g+8 hold real heads only when G == 16
+  static_assert(G < 16 || TWO, "a group of 16 fills both row halves");
+  constexpr bool kTwoRowHalves = TWO;
+  constexpr int kRows = TWO ? 16 : 8;
 
   // the block ring during the loop; afterwards the per-warp partials
   extern __shared__ __align__(16) uint4 ring[];
-  float(*s_o)[G][kDecD] = reinterpret_cast<float(*)[G][kDecD]>(ring);
-  float(*s_m)[G] = reinterpret_cast<float(*)[G]>(reinterpret_cast<float*>(ring) + kDecWarps * G * kDecD);
-  float(*s_l)[G] = reinterpret_cast<float(*)[G]>(reinterpret_cast<float*>(ring) + kDecWarps * G * (kDecD + 1));
+  float(*s_o)[kRows][kDecD] = reinterpret_cast<float(*)[kRows][kDecD]>(ring);
+  float(*s_m)[kRows] = reinterpret_cast<float(*)[kRows]>(reinterpret_cast<float*>(ring) + kDecWarps * kRows * kDecD);
+  float(*s_l)[kRows] =
+      reinterpret_cast<float(*)[kRows]>(reinterpret_cast<float*>(ring) + kDecWarps * kRows * (kDecD + 1));
 
   const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, qq = lane & 3;
   const int S = p.num_splits, P = p.page_size;
+  const int QL = p.q_len, nrows = G * QL;
 
   int L = p.seqlens[b];
   const int64_t cap = static_cast<int64_t>(p.max_pages) * P;
@@ -104,29 +120,38 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecodeParams
     if (threadIdx.x == 0) flag_bad(p.status, kSiteDecodeTable);
     L = 0;
   }
-  const int64_t c = (static_cast<int64_t>(L) + S - 1) / S;
-  const int lo = static_cast<int>(min(static_cast<int64_t>(s) * c, static_cast<int64_t>(L)));
-  const int hi = static_cast<int>(min(static_cast<int64_t>(s + 1) * c, static_cast<int64_t>(L)));
+  // this sequence's split count, then split s = [s c, min((s+1) c, L)); splits past it are empty
+  int Sb = S;
+  if (p.min_split > 0) Sb = max(1, min(S, static_cast<int>((static_cast<int64_t>(L) + p.min_split - 1) / p.min_split)));
+  const int64_t c = (static_cast<int64_t>(L) + Sb - 1) / Sb;
+  const int lo = s < Sb ? static_cast<int>(min(static_cast<int64_t>(s) * c, static_cast<int64_t>(L))) : L;
+  const int hi = s < Sb ? static_cast<int>(min(static_cast<int64_t>(s + 1) * c, static_cast<int64_t>(L))) : L;
   if (p.bounds_out && kvh == 0 && threadIdx.x == 0) {
     p.bounds_out[(static_cast<int64_t>(b) * S + s) * 2 + 0] = lo;
     p.bounds_out[(static_cast<int64_t>(b) * S + s) * 2 + 1] = hi;
   }
+  if (p.counts_out && s == 0 && kvh == 0 && threadIdx.x == 0) p.counts_out[b] = Sb;
+  // causal limits (exclusive) of this lane's rows gq and gq + 8: token r / G sees keys < L - q_len + r / G + 1
+  const int lim0 = min(hi, L - QL + gq / G + 1);
+  const int lim1 = min(hi, L - QL + (gq + 8) / G + 1);
 
-  // Q fragments (A operand, rows = query heads of this KV group).
+  // Q fragments (A operand, rows = (token, head) pairs of this KV group).
   uint32_t qa[8][4];
   {
-    const __nv_bfloat16* qb = p.q + (static_cast<int64_t>(b) * p.hq + static_cast<int64_t>(kvh) * G) * kDecD;
+    auto qrow = [&](int r) {  // row r: token r / G, head kvh * G + r % G
+      return p.q + ((static_cast<int64_t>(b) * QL + r / G) * p.hq + static_cast<int64_t>(kvh) * G + r % G) * kDecD;
+    };
 #pragma unroll
     for (int cs = 0; cs < 8; ++cs) {
       const int d0 = 32 * (cs >> 1) + 8 * qq + 4 * (cs & 1);
       uint32_t r0a = 0, r0b = 0, r1a = 0, r1b = 0;
-      if (gq < G) {
-        const uint2 v = *reinterpret_cast<const uint2*>(qb + gq * kDecD + d0);
+      if (gq < nrows) {
+        const uint2 v = *reinterpret_cast<const uint2*>(qrow(gq) + d0);
         r0a = v.x;
         r0b = v.y;
       }
-      if (kTwoRowHalves) {
-        const uint2 v = *reinterpret_cast<const uint2*>(qb + (gq + 8) * kDecD + d0);
+      if (kTwoRowHalves && gq + 8 < nrows) {
+        const uint2 v = *reinterpret_cast<const uint2*>(qrow(gq + 8) + d0);
         r1a = v.x;
         r1b = v.y;
       }
@@ -222,28 +247,30 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecodeParams
         mma16816(sc[u], qa[cs], b0, b1);
       }
     }
-    // mask tokens past the split end
+    // mask tokens past the split end, and past each row's causal limit
 #pragma unroll
     for (int u = 0; u < 2; ++u)
 #pragma unroll
-      for (int e = 0; e < 2; ++e)
-        if (t0 + 8 * u + 2 * qq + e >= hi) {
-          sc[u][e] = -INFINITY;
-          sc[u][2 + e] = -INFINITY;
-        }
+      for (int e = 0; e < 2; ++e) {
+        const int t = t0 + 8 * u + 2 * qq + e;
+        if (t >= lim0) sc[u][e] = -INFINITY;
+        if (t >= lim1) sc[u][2 + e] = -INFINITY;
+      }
 
-    // online softmax, row g (and g+8 when G == 16)
+    // online softmax, row g (and g+8 when both halves are in use); a row that
+    // has seen no visible key yet (max -inf) shifts by 0 and keeps P = 0
     float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     const float mn0 = fmaxf(m0, mx0 * p.scale_log2);
-    const float al0 = ptx::ex2(m0 - mn0);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float al0 = ptx::ex2(m0 - mu0);
     m0 = mn0;
     float pr[2][4];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      pr[u][0] = ptx::ex2(fmaf(sc[u][0], p.scale_log2, -mn0));
-      pr[u][1] = ptx::ex2(fmaf(sc[u][1], p.scale_log2, -mn0));
+      pr[u][0] = ptx::ex2(fmaf(sc[u][0], p.scale_log2, -mu0));
+      pr[u][1] = ptx::ex2(fmaf(sc[u][1], p.scale_log2, -mu0));
     }
     l0 = l0 * al0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
     float al1 = 1.f;
@@ -252,12 +279,13 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecodeParams
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
       const float mn1 = fmaxf(m1, mx1 * p.scale_log2);
-      al1 = ptx::ex2(m1 - mn1);
+      const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+      al1 = ptx::ex2(m1 - mu1);
       m1 = mn1;
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        pr[u][2] = ptx::ex2(fmaf(sc[u][2], p.scale_log2, -mn1));
-        pr[u][3] = ptx::ex2(fmaf(sc[u][3], p.scale_log2, -mn1));
+        pr[u][2] = ptx::ex2(fmaf(sc[u][2], p.scale_log2, -mu1));
+        pr[u][3] = ptx::ex2(fmaf(sc[u][3], p.scale_log2, -mu1));
       }
       l1 = l1 * al1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
     } else {
@@ -304,7 +332,7 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecodeParams
   cp_async_wait<0>();
   __syncthreads();  // every warp is done with the ring before it holds the partials
   // per-warp partials to shared memory (un-permuting the head dimension)
-  if (gq < G) {
+  if (gq < nrows) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       s_o[warp][gq][16 * (2 * qq) + j] = acc[j][0];
@@ -315,11 +343,11 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecodeParams
       s_l[warp][gq] = l0;
     }
   }
-  if (kTwoRowHalves) {
+  if (kTwoRowHalves && gq + 8 < nrows) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      s_o[warp][gq + 8 < G ? gq + 8 : 0][16 * (2 * qq) + j] = acc[j][2];
-      s_o[warp][gq + 8 < G ? gq + 8 : 0][16 * (2 * qq + 1) + j] = acc[j][3];
+      s_o[warp][gq + 8][16 * (2 * qq) + j] = acc[j][2];
+      s_o[warp][gq + 8][16 * (2 * qq + 1) + j] = acc[j][3];
     }
     if (qq == 0) {
       s_m[warp][gq + 8] = m1;
@@ -328,9 +356,9 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecodeParams
   }
   __syncthreads();
 
-  // merge the four warps; thread -> (head row, 4 columns)
+  // merge the four warps; thread -> (row, 4 columns)
   constexpr float kLn2 = 0.6931471805599453f;
-  for (int idx = threadIdx.x; idx < G * (kDecD / 4); idx += blockDim.x) {
+  for (int idx = threadIdx.x; idx < nrows * (kDecD / 4); idx += blockDim.x) {
     const int r = idx / (kDecD / 4);
     const int c4 = (idx % (kDecD / 4)) * 4;
     float M = -INFINITY;
@@ -347,7 +375,9 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecodeParams
         for (int e = 0; e < 4; ++e) o4[e] += s_o[w][r][c4 + e] * f;
       }
     }
-    const int64_t row = (static_cast<int64_t>(s) * p.batch + b) * p.hq + static_cast<int64_t>(kvh) * G + r;
+    // partial row (s, b, token r / G, head kvh * G + r % G)
+    const int64_t row = ((static_cast<int64_t>(s) * p.batch + b) * QL + r / G) * p.hq + static_cast<int64_t>(kvh) * G +
+                        r % G;
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
     float4 out = make_float4(o4[0] * inv, o4[1] * inv, o4[2] * inv, o4[3] * inv);
     *reinterpret_cast<float4*>(p.part_o + row * kDecD + c4) = out;
@@ -397,8 +427,20 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const float* __restri
 
 // ------------------------------------------------------------------ launchers
 
-cudaError_t launch_decode(const jfa_decode_args& a, float* part_o, float* part_lse, int32_t* status,
-                          cudaStream_t stream) {
+template <int G>
+static cudaError_t launch_split(bool two, dim3 grid, const DecodeParams& p, cudaStream_t stream) {
+  if constexpr (G == 16) {
+    decode_split_kernel<16, true><<<grid, 128, kDecRingBytes, stream>>>(p);
+  } else if (two) {
+    decode_split_kernel<G, true><<<grid, 128, kDecRingBytes, stream>>>(p);
+  } else {
+    decode_split_kernel<G, false><<<grid, 128, kDecRingBytes, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_general(const DecodeLaunch& a, float* part_o, float* part_lse, int32_t* status,
+                                  cudaStream_t stream) {
   DecodeParams p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.kc = static_cast<const __nv_bfloat16*>(a.k_cache);
@@ -412,17 +454,22 @@ cudaError_t launch_decode(const jfa_decode_args& a, float* part_o, float* part_l
   p.num_pages = a.num_pages;
   p.max_pages = a.max_pages;
   p.num_splits = a.num_splits;
+  p.q_len = a.q_len;
+  p.min_split = a.min_split_tokens;
+  p.counts_out = a.split_counts_out;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.part_o = part_o;
   p.part_lse = part_lse;
   p.bounds_out = a.split_bounds_out;
   p.status = status;
   const int G = a.q_heads / a.kv_heads;
+  const bool two = G * a.q_len > 8;
   dim3 grid(a.num_splits, a.kv_heads, a.batch);
   static bool attr_set = false;
   if (!attr_set) {
-    for (auto k : {decode_split_kernel<1>, decode_split_kernel<2>, decode_split_kernel<4>, decode_split_kernel<8>,
-                   decode_split_kernel<16>}) {
+    for (auto k : {decode_split_kernel<1, false>, decode_split_kernel<2, false>, decode_split_kernel<4, false>,
+                   decode_split_kernel<8, false>, decode_split_kernel<1, true>, decode_split_kernel<2, true>,
+                   decode_split_kernel<4, true>, decode_split_kernel<8, true>, decode_split_kernel<16, true>}) {
       cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecRingBytes);
       if (e != cudaSuccess) return e;
     }
@@ -430,21 +477,47 @@ cudaError_t launch_decode(const jfa_decode_args& a, float* part_o, float* part_l
   }
   cudaEvent_t* ev = static_cast<cudaEvent_t*>(a.main_kernel_events);
   if (ev) cudaEventRecord(ev[0], stream);
+  cudaError_t e;
   switch (G) {
-    case 1: decode_split_kernel<1><<<grid, 128, kDecRingBytes, stream>>>(p); break;
-    case 2: decode_split_kernel<2><<<grid, 128, kDecRingBytes, stream>>>(p); break;
-    case 4: decode_split_kernel<4><<<grid, 128, kDecRingBytes, stream>>>(p); break;
-    case 8: decode_split_kernel<8><<<grid, 128, kDecRingBytes, stream>>>(p); break;
-    case 16: decode_split_kernel<16><<<grid, 128, kDecRingBytes, stream>>>(p); break;
+    case 1: e = launch_split<1>(two, grid, p, stream); break;
+    case 2: e = launch_split<2>(two, grid, p, stream); break;
+    case 4: e = launch_split<4>(two, grid, p, stream); break;
+    case 8: e = launch_split<8>(two, grid, p, stream); break;
+    case 16: e = launch_split<16>(two, grid, p, stream); break;
     default: return cudaErrorInvalidValue;
   }
   if (ev) cudaEventRecord(ev[1], stream);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int rows = a.batch * a.q_heads;
-  decode_merge_kernel<<<(rows + 3) / 4, 128, 0, stream>>>(part_o, part_lse, a.num_splits, a.batch, a.q_heads,
-                                                            static_cast<__nv_bfloat16*>(a.o), a.lse);
+  const int rows = a.batch * a.q_len * a.q_heads;  // (b, token, head) rows of O
+  decode_merge_kernel<<<(rows + 3) / 4, 128, 0, stream>>>(part_o, part_lse, a.num_splits, a.batch * a.q_len,
+                                                            a.q_heads, static_cast<__nv_bfloat16*>(a.o), a.lse);
   return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const jfa_decode_args& a, float* part_o, float* part_lse, int32_t* status,
+                          cudaStream_t stream) {
+  DecodeLaunch d;
+  d.q = a.q;
+  d.k_cache = a.k_cache;
+  d.v_cache = a.v_cache;
+  d.page_table = a.page_table;
+  d.seqlens_k = a.seqlens_k;
+  d.batch = a.batch;
+  d.q_len = 1;
+  d.q_heads = a.q_heads;
+  d.kv_heads = a.kv_heads;
+  d.page_size = a.page_size;
+  d.num_pages = a.num_pages;
+  d.max_pages = a.max_pages;
+  d.num_splits = a.num_splits;
+  d.min_split_tokens = 0;
+  d.scale = a.scale;
+  d.o = a.o;
+  d.lse = a.lse;
+  d.split_bounds_out = a.split_bounds_out;
+  d.split_counts_out = nullptr;
+  d.main_kernel_events = a.main_kernel_events;
+  return launch_decode_general(d, part_o, part_lse, status, stream);
 }
 
 }  // namespace jfa

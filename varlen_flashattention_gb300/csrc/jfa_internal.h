@@ -135,5 +135,24 @@ cudaError_t launch_bwd_post(const float* acc, void* dq, int64_t n, float scale, 
                             cudaStream_t stream);
 cudaError_t launch_decode(const jfa_decode_args& a, float* part_o, float* part_lse, int32_t* status,
                           cudaStream_t stream);
+// The split-KV decode with q_len query tokens per sequence and optional
+// per-sequence split counts (min_split_tokens > 0); launch_decode is q_len 1,
+// min_split_tokens 0. Partials: part_o [S, B, q_len, Hq, 128], part_lse [S, B, q_len, Hq].
+struct DecodeLaunch {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* page_table;
+  const int32_t* seqlens_k;
+  int32_t batch, q_len, q_heads, kv_heads, page_size, num_pages, max_pages, num_splits, min_split_tokens;
+  float scale;
+  void* o;
+  float* lse;
+  int32_t* split_bounds_out;
+  int32_t* split_counts_out;
+  void* main_kernel_events;
+};
+cudaError_t launch_decode_general(const DecodeLaunch& a, float* part_o, float* part_lse, int32_t* status,
+                                  cudaStream_t stream);
 
 }  // namespace jfa

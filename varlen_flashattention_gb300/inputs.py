@@ -187,7 +187,7 @@ def broadcast_inputs(batch: int = 512, q_len: int = 256, heads: int = 4, head_di
 
 def decode_inputs(batch: int = 32, q_heads: int = 32, kv_heads: int = 8, head_dim: int = 128,
                   lk_lo: int = 1024, lk_hi: int = 32768, page_size: int = 16, seed: int = 0,
-                  seqlens=None) -> dict:
+                  seqlens=None, q_len=None) -> dict:
     """Paged GQA decode: one query token per sequence, KV cache in pages of
     `page_size` tokens, pages handed out by a random permutation.
 
@@ -210,7 +210,8 @@ def decode_inputs(batch: int = 32, q_heads: int = 32, kv_heads: int = 8, head_di
     for b, n in enumerate(pages_per_seq):
         page_table[b, :n] = perm[cursor:cursor + n]
         cursor += n
-    q = _randn_bf16((batch, q_heads, head_dim), g)
+    # one query token per sequence ([B, Hq, d]), or q_len new tokens ([B, q_len, Hq, d])
+    q = _randn_bf16((batch, q_heads, head_dim) if q_len is None else (batch, q_len, q_heads, head_dim), g)
     k_cache = _randn_bf16((num_pages, page_size, kv_heads, head_dim), g)
     v_cache = _randn_bf16((num_pages, page_size, kv_heads, head_dim), g)
     return {
@@ -227,4 +228,5 @@ def decode_inputs(batch: int = 32, q_heads: int = 32, kv_heads: int = 8, head_di
         "q": q,
         "k_cache": k_cache,
         "v_cache": v_cache,
+        "q_len": 1 if q_len is None else q_len,
     }
