@@ -3,8 +3,10 @@
  *
  * Exact attention over variable-length ("jagged") sequences packed back to
  * back with an int32 offsets tensor and no padding tokens, its recompute-based
- * backward, a broadcast-Q variant whose dQ is summed over the batch, and a
- * split-KV decode over a paged, grouped-query KV cache.
+ * backward, a broadcast-Q variant whose dQ is summed over the batch, a varlen
+ * form with separate query / key lengths and grouped KV heads, and a split-KV
+ * decode (one or a few query tokens per sequence) over a paged, grouped-query
+ * KV cache.
  *
  * Sources of the operations (web pages; cited by title and section):
  *  [JFA]  "Optimizing Jagged Flash Attention with TLX: The Road Toward SOTA FA4
