@@ -340,6 +340,17 @@ def measure_extra(jfa, device, peaks):
                                      "bwd_tflops": 10 * d * 16 * pairs / (tb * 1e-3) / 1e12,
                                      "fwd_ms": tf, "bwd_ms": tb}
         del q, k, v, do, o, lse
+    # the tiny config (batch 4, L U[1,64], 2 heads, d 64): per-call overhead, reported apart
+    d = inputs.tiny_inputs(0)
+    q, k, v, do = (d[x].to(device) for x in ("q", "k", "v", "do"))
+    off = d["offsets"].to(device)
+    o, lse = jfa.jfa_fwd(q, k, v, off, d["max_seqlen"], d["scale"])
+    tt = time_events(lambda: (jfa.jfa_fwd(q, k, v, off, d["max_seqlen"], d["scale"], o=o, lse=lse),
+                              jfa.jfa_bwd(q, k, v, o, do, lse, off, d["max_seqlen"], d["scale"])), 20, 3)
+    fl = attn_flops(d["lengths"].tolist(), 2, 64, False, "fwd") + attn_flops(d["lengths"].tolist(), 2, 64, False, "bwd")
+    out["tiny"] = {"fwd_bwd_us": tt * 1e3, "fwd_bwd_tflops": fl / (tt * 1e-3) / 1e12,
+                   "workload": "batch 4, L U[1,64], 2 heads, d 64 (launch- and queue-bound)"}
+    del q, k, v, do, o, lse
     # varlen GQA, chunked-prefill shape: 64 sequences, query chunk L_q U[1, 1024] at the
     # end of L_k = L_q + U[0, 3072] keys, 32 query heads on 8 KV heads, d 128, causal
     # (bottom-right aligned)

@@ -338,6 +338,21 @@ JFA_API jfa_status jfa_decode_smallq(const jfa_decode_smallq_args* args, void* w
  *    them: the status word lives in the internal scratch. */
 JFA_API jfa_status jfa_decode_splitkv_noalloc(const jfa_decode_args* args, cudaStream_t stream);
 
+/* Failure-detection self-test ([B300] bug hunting: a producer/consumer
+ * pipeline that deadlocked). Every pipeline wait in this library is bounded in
+ * time; when one runs out, the kernel records JFA_ERR_TIMEOUT and the waiting
+ * site in the workspace status word, raises its CTA's abort flag so that every
+ * other role leaves as well, and returns, leaving the CUDA context usable.
+ * This entry point runs that path on purpose: a one-CTA kernel whose first
+ * stage waits budget_us microseconds (1 .. 10^7) for an input that never
+ * arrives, while its second stage waits for the first with an 8x longer
+ * budget. Afterwards jfa_read_device_status(workspace) returns
+ * JFA_ERR_TIMEOUT with detail 901 (the first stage's wait), and the 32-bit
+ * word at byte offset 16 of the workspace is 1 when the second stage left
+ * through the abort flag before its own budget. workspace: >= 256 bytes of
+ * device memory, 256-byte aligned. */
+JFA_API jfa_status jfa_selftest_wait_timeout(int32_t budget_us, void* workspace, cudaStream_t stream);
+
 /* Synchronises `stream`, then returns the device status word of the last call
  * that used `workspace` (JFA_OK, JFA_ERR_TIMEOUT or JFA_ERR_BAD_INPUT), or
  * JFA_ERR_CUDA if the stream reports an error. *detail (optional) receives a

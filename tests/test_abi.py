@@ -194,6 +194,12 @@ def test_decode_smallq_validation(lib):
     assert lib.jfa_decode_smallq(P(args()), FAKE, need - 1, None) == _abi.JFA_ERR_WORKSPACE_TOO_SMALL
 
 
+def test_selftest_validation(lib):
+    assert lib.jfa_selftest_wait_timeout(0, FAKE, None) == _abi.JFA_ERR_INVALID_ARG
+    assert lib.jfa_selftest_wait_timeout(10 ** 8, FAKE, None) == _abi.JFA_ERR_INVALID_ARG
+    assert lib.jfa_selftest_wait_timeout(1000, FAKE + 16, None) == _abi.JFA_ERR_INVALID_ARG
+
+
 def test_binding_rejects_cpu_tensors():
     import torch
     q = torch.zeros(4, 1, 64, dtype=torch.bfloat16)

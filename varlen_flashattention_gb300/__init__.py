@@ -29,7 +29,7 @@ from . import _abi
 __all__ = [
     "JfaError", "jfa_fwd", "jfa_bwd", "jfa_fwd_broadcast_q", "jfa_bwd_broadcast_q", "jfa_decode_splitkv",
     "jfa_read_device_status", "jagged_attention", "library", "jfa_fwd_varlen", "jfa_bwd_varlen",
-    "varlen_attention", "jfa_decode_smallq",
+    "varlen_attention", "jfa_decode_smallq", "jfa_selftest_wait_timeout",
 ]
 
 
@@ -94,6 +94,16 @@ def jfa_read_device_status(workspace, stream=None):
     d = ctypes.c_int32(0)
     st = library().jfa_read_device_status(_ptr(workspace), _stream(stream), ctypes.byref(d))
     return int(st), int(d.value)
+
+
+def jfa_selftest_wait_timeout(budget_us=20000, workspace=None, stream=None):
+    """Runs the failure-detection self-test (a pipeline wait whose input never
+    arrives, bounded to budget_us). Returns (status, detail, second_stage_aborted)."""
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda") if workspace is None else workspace
+    _check(library().jfa_selftest_wait_timeout(int(budget_us), _ptr(ws), _stream(stream)), "jfa_selftest_wait_timeout")
+    st, detail = jfa_read_device_status(ws, stream)
+    aborted = int(ws[16:20].view(torch.int32).item())
+    return st, detail, aborted
 
 
 def _finish(ws, check, stream, where):

@@ -864,6 +864,12 @@ jfa_status jfa_decode_smallq(const jfa_decode_smallq_args* a, void* ws, size_t w
                                            stream));
 }
 
+jfa_status jfa_selftest_wait_timeout(int32_t budget_us, void* ws, cudaStream_t stream) {
+  if (budget_us < 1 || budget_us > 10 * 1000 * 1000 || !aligned(ws, 256)) return JFA_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(ws, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  return cuda_status(launch_selftest_wait(static_cast<int32_t*>(ws), static_cast<uint64_t>(budget_us) * 1000, stream));
+}
+
 jfa_status jfa_read_device_status(const void* ws, cudaStream_t stream, int32_t* detail) {
   if (!aligned(ws, 4)) return JFA_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return JFA_ERR_CUDA;

@@ -41,6 +41,8 @@ enum WaitSite : int32_t {
   kSiteBwdDrain = 251,
   kSiteQueueOffsets = 301,
   kSiteDecodeTable = 401,
+  kSiteSelftestInput = 901,  // the self-test's first stage (its input never arrives)
+  kSiteSelftestChain = 902,  // the self-test's second stage (should leave through the abort flag)
 };
 
 // Device status block at the start of every workspace (256 bytes).
@@ -133,6 +135,10 @@ cudaError_t launch_bwd_pre(int head_dim, const void* o, const void* dout, const 
                            cudaStream_t stream);
 cudaError_t launch_bwd_post(const float* acc, void* dq, int64_t n, float scale, const int32_t* status, int sms,
                             cudaStream_t stream);
+// Failure-detection self-test: one CTA whose first pipeline stage waits for an
+// input that never arrives; status[4] = 1 when the second stage left through
+// the abort flag.
+cudaError_t launch_selftest_wait(int32_t* status, uint64_t budget_ns, cudaStream_t stream);
 cudaError_t launch_decode(const jfa_decode_args& a, float* part_o, float* part_lse, int32_t* status,
                           cudaStream_t stream);
 // The split-KV decode with q_len query tokens per sequence and optional
