@@ -108,8 +108,10 @@ typedef struct {
  *   D = rowsum(dO * O) ("delta"), dS = P * (dP - D),
  *   dV = P^T dO, dQ = scale dS K, dK = scale dS^T Q.
  * head_dim 192 runs head-axis chunked ([B300] Phase 2): each pass owns a
- * head_chunk-wide slice of dQ/dK/dV while S and dP are still accumulated over
- * the whole head dimension.
+ * slice of dQ/dK/dV while S and dP are still accumulated over the whole head
+ * dimension. By default (head_chunk 0) the slices are columns 0-127 and
+ * 128-191 (two passes: TMEM holds dV and dK slices of at most 128 columns next
+ * to S and dP); head_chunk 64 runs three 64-column passes.
  */
 typedef struct {
   const void* q;             /* bf16 [total, heads, head_dim] */
@@ -122,7 +124,7 @@ typedef struct {
   int32_t batch, heads, head_dim, max_seqlen, total;
   float scale;
   int32_t causal;
-  int32_t head_chunk;        /* 0 = automatic (64 for head_dim 192, else head_dim) */
+  int32_t head_chunk;        /* 0 = automatic (head_dim 192: slices of 128 and 64; else head_dim), or 64 */
   void* dq;                  /* out: bf16 [total, heads, head_dim] */
   void* dk;                  /* out: bf16 [total, heads, head_dim] */
   void* dv;                  /* out: bf16 [total, heads, head_dim] */
@@ -205,7 +207,7 @@ typedef struct {
 /* Backward of jfa_fwd_varlen (same recompute scheme as jfa_bwd). dK and dV of
  * a KV head are summed over the q_heads / kv_heads query heads that read it
  * (accumulated on chip, no atomics); dQ as in jfa_bwd. head_dim 192 runs
- * head-axis chunked (head_chunk 64). */
+ * head-axis chunked as in jfa_bwd. */
 typedef struct {
   const void* q;              /* bf16 [total_q, q_heads, head_dim] */
   const void* k;              /* bf16 [total_k, kv_heads, head_dim] */
@@ -219,7 +221,7 @@ typedef struct {
   int32_t max_seqlen_q, max_seqlen_k, total_q, total_k;
   float scale;
   int32_t causal;
-  int32_t head_chunk;         /* 0 = automatic (64 for head_dim 192, else head_dim) */
+  int32_t head_chunk;         /* 0 = automatic (as in jfa_bwd_args), or 64 */
   void* dq;                   /* out: bf16 [total_q, q_heads, head_dim] */
   void* dk;                   /* out: bf16 [total_k, kv_heads, head_dim] */
   void* dv;                   /* out: bf16 [total_k, kv_heads, head_dim] */

@@ -98,6 +98,14 @@ def test_head_chunk_128_by_64():
     _check_all(d, False, head_chunk=64, tag="d=128 chunk 64")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dim_192_three_passes(causal):
+    """head_dim 192 with head_chunk 64 (three 64-column passes) instead of the default two
+    passes (128 + 64 columns): both must match the oracle."""
+    d = _lengths_case([300, 129, 1, 640], 2, 192, seed=18)
+    _check_all(d, causal, head_chunk=64, tag=f"d=192 chunk 64 causal={causal}")
+
+
 @pytest.mark.parametrize("sparsity", [0.1, 0.5, 0.9])
 def test_gem_like_reduced_batch(sparsity):
     """GEM-like lengths (max_len 1024, H=4, d=128) on a batch of 24 sequences, full compare."""

@@ -247,8 +247,9 @@ jfa_status check_bwd(const jfa_bwd_args* a, int* chunk) {
   if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return JFA_ERR_INVALID_ARG;
   if (a->causal != 0 && a->causal != 1) return JFA_ERR_INVALID_ARG;
   int c = a->head_chunk;
-  if (c == 0) c = (a->head_dim == 192) ? 64 : a->head_dim;
-  const bool ok_chunk = (c == a->head_dim && a->head_dim != 192) || (c == 64 && a->head_dim >= 128);
+  if (c == 0 && a->head_dim != 192) c = a->head_dim;  // head_dim 192: 0 stays "two passes"
+  const bool ok_chunk =
+      (c == 0) || (c == a->head_dim && a->head_dim != 192) || (c == 64 && a->head_dim >= 128);
   if (!ok_chunk) return JFA_ERR_UNSUPPORTED;  // head_dim 192 unchunked would overflow TMEM
   *chunk = c;
   if (!aligned(a->offsets, 4)) return JFA_ERR_INVALID_ARG;
@@ -290,6 +291,33 @@ jfa_status check_bcast_common(int batch, int q_len, int heads, int head_dim, int
   if (!(scale > 0.f) || !std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(batch) * q_len >= (int64_t(1) << 31)) return JFA_ERR_INVALID_ARG;
   return JFA_OK;
+}
+
+// The main backward launch(es). chunk 0 (head_dim 192 only) runs two passes
+// over the head dimension, columns 0-127 and then 128-191: TMEM holds S^T and
+// dP^T (256 columns) plus dV and dK slices of at most 128 columns each, and
+// every pass rebuilds S^T and dP^T, so two passes do less work than three
+// 64-wide ones. Otherwise each item is split into head_dim / chunk slices.
+cudaError_t run_bwd_main(BwdLaunch bl, int chunk, int sms, int64_t max_items, const CUtensorMap& tq,
+                         const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                         const CUtensorMap& tdk, const CUtensorMap& tdv, cudaStream_t stream) {
+  const int64_t items = std::max<int64_t>(max_items, 1);
+  if (chunk == 0) {
+    bl.n_chunks = 1;
+    bl.grid = static_cast<int>(std::min<int64_t>(sms, items));
+    bl.head_chunk = 128;
+    bl.col0 = 0;
+    const cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, tdq, tdk, tdv, stream);
+    if (e != cudaSuccess) return e;
+    bl.head_chunk = 64;
+    bl.col0 = 128;
+    return launch_bwd_main(bl, tq, tk, tv, tdo, tdq, tdk, tdv, stream);
+  }
+  bl.head_chunk = chunk;
+  bl.col0 = 0;
+  bl.n_chunks = bl.head_dim / chunk;
+  bl.grid = static_cast<int>(std::min<int64_t>(sms, items * bl.n_chunks));
+  return launch_bwd_main(bl, tq, tk, tv, tdo, tdq, tdk, tdv, stream);
 }
 
 }  // namespace
@@ -453,13 +481,12 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   bl.pad_tiles = static_cast<int>(L.pad_tiles);
   bl.scale = a->scale;
   bl.budget_ns = wait_budget_ns();
-  bl.grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items * (a->head_dim / chunk), 1)));
   record(a->main_kernel_events, 0, stream);
   CUtensorMap tdq, tdk, tdv;
   if (!make_tmap_f32_acc(&tdq, dq_acc, a->total, cols) || !make_tmap_bf16(&tdk, a->dk, a->total, cols) ||
       !make_tmap_bf16(&tdv, a->dv, a->total, cols))
     return JFA_ERR_CUDA;
-  cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, tdq, tdk, tdv, stream);
+  cudaError_t e = run_bwd_main(bl, chunk, sms, L.max_items, tq, tk, tv, tdo, tdq, tdk, tdv, stream);
   record(a->main_kernel_events, 1, stream);
   if (e != cudaSuccess) return JFA_ERR_CUDA;
   return cuda_status(launch_bwd_post(dq_acc, a->dq, n_acc, a->scale, status, sms, stream));
@@ -713,8 +740,8 @@ jfa_status jfa_bwd_varlen(const jfa_varlen_bwd_args* a, void* ws, size_t ws_byte
                                    a->total_q, a->total_k, a->scale, a->causal, a->q_offsets, a->k_offsets, true);
   if (st != JFA_OK) return st;
   int chunk = a->head_chunk;
-  if (chunk == 0) chunk = (a->head_dim == 192) ? 64 : a->head_dim;
-  if (!((chunk == a->head_dim && a->head_dim != 192) || (chunk == 64 && a->head_dim >= 128)))
+  if (chunk == 0 && a->head_dim != 192) chunk = a->head_dim;  // head_dim 192: 0 stays "two passes"
+  if (!(chunk == 0 || (chunk == a->head_dim && a->head_dim != 192) || (chunk == 64 && a->head_dim >= 128)))
     return JFA_ERR_UNSUPPORTED;  // head_dim 192 unchunked would overflow TMEM
   if (a->total_q > 0 && (!aligned(a->q, 16) || !aligned(a->o, 16) || !aligned(a->dout, 16) || !aligned(a->lse, 4) ||
                          !aligned(a->dq, 16)))
@@ -796,13 +823,12 @@ jfa_status jfa_bwd_varlen(const jfa_varlen_bwd_args* a, void* ws, size_t ws_byte
   bl.kv_heads = a->kv_heads;
   bl.scale = a->scale;
   bl.budget_ns = wait_budget_ns();
-  bl.grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items * (a->head_dim / chunk), 1)));
   CUtensorMap tdq, tdk, tdv;
   if (!make_tmap_f32_acc(&tdq, dq_acc, a->total_q, qcols) || !make_tmap_bf16(&tdk, a->dk, a->total_k, kcols) ||
       !make_tmap_bf16(&tdv, a->dv, a->total_k, kcols))
     return JFA_ERR_CUDA;
   record(a->main_kernel_events, 0, stream);
-  cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, tdq, tdk, tdv, stream);
+  cudaError_t e = run_bwd_main(bl, chunk, sms, L.max_items, tq, tk, tv, tdo, tdq, tdk, tdv, stream);
   record(a->main_kernel_events, 1, stream);
   if (e != cudaSuccess) return JFA_ERR_CUDA;
   return cuda_status(launch_bwd_post(dq_acc, a->dq, n_acc, a->scale, status, sms, stream));

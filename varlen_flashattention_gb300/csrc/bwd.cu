@@ -72,6 +72,8 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int32_t heads, total, bcast, q_len, causal, n_chunks;
+  int32_t col0;               // first head-dim column of this launch's slices (slice c: col0 + c DC ..)
+  int32_t chunk;              // DC, the slice width
   int32_t pad_tiles;          // self, varlen: query tiles per head in the padded arrays
   int32_t var, group;         // varlen: items carry query and key bounds; query heads per KV head
   int32_t kv_heads;           // heads of K, V, dK, dV
@@ -177,11 +179,21 @@ __device__ __forceinline__ void bwd_step(const BwdItem& I, int ii, int& g, int& 
   i = I.i0 + ii - g * I.nqt;
 }
 
+// First head-dim column of an item's slice (0 when one slice covers the head).
+template <int D, int DC>
+__device__ __forceinline__ int slice_col(const BwdParams& p, const BwdItem& I) {
+  if constexpr (DC == D) return 0;
+  else return p.col0 + I.c * DC;
+}
+
 // One-stage pipeline: the n-th 64-column atom of Q (or dO) in load and MMA
-// order for a pass over slice c: the atoms other than c in ascending order,
-// then c. S^T (dP^T) reads every atom but only dK (dV) reads atom c again, so
-// the others are refilled for the next query tile while this one finishes.
-__device__ __forceinline__ int atom_at(int n, int c, int atoms) { return n == atoms - 1 ? c : n + (n >= c ? 1 : 0); }
+// order for a pass over the slice of `sa` atoms starting at atom ca: the atoms
+// outside the slice in ascending order, then the slice's. S^T (dP^T) reads
+// every atom but only dK (dV) reads the slice again, so the others are refilled
+// for the next query tile while this one finishes.
+__device__ __forceinline__ int atom_at(int n, int ca, int sa, int atoms) {
+  return n < atoms - sa ? (n < ca ? n : n + sa) : ca + (n - (atoms - sa));
+}
 
 template <int D, int DC>
 __global__ void __launch_bounds__(448, 1)
@@ -191,6 +203,7 @@ __global__ void __launch_bounds__(448, 1)
                const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
   using Lay = BwdLayout<D, DC>;
   constexpr int kSt = Lay::kStages;
+  constexpr int kSliceAtoms = DC / 64;  // 64-column atoms of one head-dim slice
   constexpr uint32_t kIdS = ptx::idesc_bf16(128, 128, false, false);   // S^T, dP^T
   constexpr uint32_t kIdAcc = ptx::idesc_bf16(128, DC, false, true);   // dV, dK
   constexpr uint32_t kIdDQ = ptx::idesc_bf16(128, DC, true, true);     // dQ (A = dS, M-major)
@@ -296,6 +309,7 @@ __global__ void __launch_bounds__(448, 1)
         int g, i;
         bwd_step(I, ii, g, i);
         const int qcol = (I.hq0 + g) * D;
+        const int ca = slice_col<D, DC>(p, I) >> 6;  // first atom of the item's slice
         const int64_t rbase = I.row_base + static_cast<int64_t>(g) * p.pad_tiles * kTile;
         if constexpr (kSt == 1) {
           // per atom, in the order the MMAs release them: Q and dO atoms outside
@@ -311,19 +325,28 @@ __global__ void __launch_bounds__(448, 1)
             ++count[a];
             return true;
           };
+          constexpr int kOut = Lay::kAtoms - kSliceAtoms;  // atoms outside the slice
 #pragma unroll 1
-          for (int n = 0; n + 1 < Lay::kAtoms; ++n)
-            if (!load_atom(q_full, q_empty, nq_loads, &tm_q, Lay::kOffQ, atom_at(n, I.c, Lay::kAtoms), qrow, 0))
+          for (int n = 0; n < kOut; ++n)
+            if (!load_atom(q_full, q_empty, nq_loads, &tm_q, Lay::kOffQ, atom_at(n, ca, kSliceAtoms, Lay::kAtoms),
+                           qrow, 0))
               return false;
 #pragma unroll 1
-          for (int n = 0; n + 1 < Lay::kAtoms; ++n)
-            if (!load_atom(do_full, do_empty, ndo_loads, &tm_do, Lay::kOffDO, atom_at(n, I.c, Lay::kAtoms), drow, 0))
+          for (int n = 0; n < kOut; ++n)
+            if (!load_atom(do_full, do_empty, ndo_loads, &tm_do, Lay::kOffDO,
+                           atom_at(n, ca, kSliceAtoms, Lay::kAtoms), drow, 0))
               return false;
-          if (!load_atom(do_full, do_empty, ndo_loads, &tm_do, Lay::kOffDO, I.c, drow, 0)) return false;
-          if (!load_atom(q_full, q_empty, nq_loads, &tm_q, Lay::kOffQ, I.c, qrow, 1024)) return false;
+#pragma unroll 1
+          for (int k = 0; k < kSliceAtoms; ++k)
+            if (!load_atom(do_full, do_empty, ndo_loads, &tm_do, Lay::kOffDO, ca + k, drow, 0)) return false;
+          const int last = ca + kSliceAtoms - 1;  // the last Q atom carries the LSE / delta rows
+#pragma unroll 1
+          for (int k = 0; k < kSliceAtoms; ++k)
+            if (!load_atom(q_full, q_empty, nq_loads, &tm_q, Lay::kOffQ, ca + k, qrow, ca + k == last ? 1024 : 0))
+              return false;
           uint8_t* rows = smem + Lay::kOffRow;
-          ptx::bulk_load(rows, p.lse2p + rbase + static_cast<int64_t>(kTile) * i, 512, q_full + I.c);
-          ptx::bulk_load(rows + 512, p.deltap + rbase + static_cast<int64_t>(kTile) * i, 512, q_full + I.c);
+          ptx::bulk_load(rows, p.lse2p + rbase + static_cast<int64_t>(kTile) * i, 512, q_full + last);
+          ptx::bulk_load(rows + 512, p.deltap + rbase + static_cast<int64_t>(kTile) * i, 512, q_full + last);
           ++pos;
           return true;
         }
@@ -402,6 +425,7 @@ __global__ void __launch_bounds__(448, 1)
     for (int v = blockIdx.x; ok && v < n_work; v += gridDim.x) {
       const BwdItem I = bwd_item(p, v);
       if (I.nq <= 0) continue;
+      const int ca = slice_col<D, DC>(p, I) >> 6;  // first atom of the item's slice
       if (!(ok = wait(kv_full, kitem & 1, kSiteBwdMmaKV))) break;
       ptx::tc_fence_after();
       // S^T(x) = K Q^T. With two Q/dO stages it is issued for the first query
@@ -426,7 +450,7 @@ __global__ void __launch_bounds__(448, 1)
       auto atoms_mma = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr, uint64_t* full, uint64_t* empty,
                            uint64_t* done) -> bool {
         for (int n = 0; n < Lay::kAtoms; ++n) {
-          const int a = atom_at(n, I.c, Lay::kAtoms);
+          const int a = atom_at(n, ca, kSliceAtoms, Lay::kAtoms);
           if (!wait(full + a, x & 1, kSiteBwdMmaQ)) return false;
           ptx::tc_fence_after();
           if (ptx::elect_one()) {
@@ -438,7 +462,8 @@ __global__ void __launch_bounds__(448, 1)
             }
             if (n + 1 == Lay::kAtoms) {
               ptx::mma_commit(done);
-              for (int m = 0; m + 1 < Lay::kAtoms; ++m) ptx::mma_commit(empty + atom_at(m, I.c, Lay::kAtoms));
+              for (int m = 0; m < Lay::kAtoms - kSliceAtoms; ++m)
+                ptx::mma_commit(empty + atom_at(m, ca, kSliceAtoms, Lay::kAtoms));
             }
           }
           __syncwarp();
@@ -484,10 +509,11 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             ptx::mma_ts(tmem + Lay::kColDV, tmem + Lay::kColS + 64 * (kk >> 2) + 8 * (kk & 3),
-                        ptx::sdesc_sw128(do_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdAcc,
+                        ptx::sdesc_sw128(do_addr + ca * 16384 + kk * 2048, 16384, 1024), kIdAcc,
                         (ii > 0 || kk > 0) ? 1u : 0u);
           }
-          if constexpr (kSt == 1) ptx::mma_commit(do_empty + I.c);  // dV was the last reader of dO
+          if constexpr (kSt == 1)  // dV was the last reader of the slice's dO atoms
+            for (int k = 0; k < kSliceAtoms; ++k) ptx::mma_commit(do_empty + ca + k);
         }
         __syncwarp();
         const bool next_s = kSt > 1 && ii + 1 < I.nq;
@@ -500,7 +526,7 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
               ptx::mma_ss(tmem + Lay::kColDP, ptx::sdesc_sw128(ds_addr + kk * 2048, 16384, 1024),
-                          ptx::sdesc_sw128(k_addr + I.c * 16384 + kk * 2048, 16384, 1024), kIdDQ,
+                          ptx::sdesc_sw128(k_addr + ca * 16384 + kk * 2048, 16384, 1024), kIdDQ,
                           kk > 0 ? 1u : 0u);
             }
             ptx::mma_commit(dq_full);
@@ -511,7 +537,7 @@ __global__ void __launch_bounds__(448, 1)
           auto mma_dk = [&]() {
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
-              const uint64_t q_desc = ptx::sdesc_sw128(q_addr + I.c * 16384 + kk * 2048, 16384, 1024);
+              const uint64_t q_desc = ptx::sdesc_sw128(q_addr + ca * 16384 + kk * 2048, 16384, 1024);
               if (kStageInDO) {
                 const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
                 ptx::mma_ss(tmem + Lay::kColDK, ptx::sdesc_sw128(ds_addr + off, 16, 1024), q_desc, kIdAcc,
@@ -538,7 +564,7 @@ __global__ void __launch_bounds__(448, 1)
             // Q atom c (read by dK) and the LSE / delta rows go back to the
             // producer before dQ, as the next tile's S^T waits for them
             mma_dk();
-            ptx::mma_commit(q_empty + I.c);
+            for (int k = 0; k < kSliceAtoms; ++k) ptx::mma_commit(q_empty + ca + k);
             mma_dq();
           }
           ptx::mma_commit(ds_free);  // dQ and dK have read dS
@@ -708,7 +734,7 @@ __global__ void __launch_bounds__(448, 1)
       if (I.nq <= 0) {
         // a varlen key tile that no query sees: its dK and dV rows are zero
         if (p.var) {
-          const int64_t orow = (static_cast<int64_t>(I.kv_row0 + r) * p.kv_heads + I.h) * D + I.c * DC;
+          const int64_t orow = (static_cast<int64_t>(I.kv_row0 + r) * p.kv_heads + I.h) * D + slice_col<D, DC>(p, I);
           if (r < I.Lk - kTile * I.t)
             for (int c8 = 0; c8 < DC; c8 += 8) {
               ptx::st_v4(p.dv + orow + c8, 0, 0, 0, 0);
@@ -730,7 +756,7 @@ __global__ void __launch_bounds__(448, 1)
         // goes there); TMA adds each round into the accumulator. Rows past the
         // sequence hold exact zeros (their dS is masked), so whole boxes are added.
         const int qrow = I.q_row0 + kTile * i;
-        const int xcol = (I.hq0 + g) * D + I.c * DC;  // dQ of query head hq0 + g
+        const int xcol = (I.hq0 + g) * D + slice_col<D, DC>(p, I);  // dQ of query head hq0 + g
         const bool issuer = warp == 10 && lane == 0;
         const uint32_t st = x % kSt;
         uint8_t* stage = kStageInDO ? smem + Lay::kOffDO + st * Lay::kTileBytes : smem + Lay::kOffDS;
@@ -855,7 +881,7 @@ __global__ void __launch_bounds__(448, 1)
         if (!(ok = ptx::mbar_wait(staged, ns & 1, ctl, status, kSiteBwdEpi, budget))) break;
         ++ns;
         if (issuer) {
-          const int xcol = I.h * D + I.c * DC;
+          const int xcol = I.h * D + slice_col<D, DC>(p, I);
 #pragma unroll
           for (int at = 0; at < DC / 64; ++at) {
             ptx::tma_store_2d(&tm_dv, sv + at * 16384, xcol + 64 * at, I.kv_row0);
@@ -870,7 +896,7 @@ __global__ void __launch_bounds__(448, 1)
         // a partial key tile (its rows end inside the 128-row box) or a single
         // stage: every thread stores its own row
         const bool k_ok = r < I.Lk - kTile * I.t;
-        const int64_t orow = (static_cast<int64_t>(I.kv_row0 + r) * p.kv_heads + I.h) * D + I.c * DC;
+        const int64_t orow = (static_cast<int64_t>(I.kv_row0 + r) * p.kv_heads + I.h) * D + slice_col<D, DC>(p, I);
 #pragma unroll 1
         for (int c = 0; c < DC / 32; ++c) {
           uint32_t a[32], b[32];
@@ -1073,7 +1099,9 @@ cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUt
   p.bcast = L.bcast;
   p.q_len = L.q_len;
   p.causal = L.causal;
-  p.n_chunks = L.head_dim / L.head_chunk;
+  p.n_chunks = L.n_chunks > 0 ? L.n_chunks : L.head_dim / L.head_chunk;
+  p.col0 = L.col0;
+  p.chunk = L.head_chunk;
   p.pad_tiles = L.pad_tiles;
   p.scale = L.scale;
   p.scale_log2 = L.scale * 1.4426950408889634f;
@@ -1082,6 +1110,7 @@ cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUt
   if (L.head_dim == 128 && L.head_chunk == 128) return launch_bwd_t<128, 128>(tq, tk, tv, tdo, tdq, tdk, tdv, p, L.grid, stream);
   if (L.head_dim == 128 && L.head_chunk == 64) return launch_bwd_t<128, 64>(tq, tk, tv, tdo, tdq, tdk, tdv, p, L.grid, stream);
   if (L.head_dim == 192 && L.head_chunk == 64) return launch_bwd_t<192, 64>(tq, tk, tv, tdo, tdq, tdk, tdv, p, L.grid, stream);
+  if (L.head_dim == 192 && L.head_chunk == 128) return launch_bwd_t<192, 128>(tq, tk, tv, tdo, tdq, tdk, tdv, p, L.grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -98,6 +98,8 @@ struct BwdLaunch {
   void* dv;
   int heads, total, bcast, q_len, causal, pad_tiles;
   int var, group, kv_heads;  // varlen: items carry query and key bounds; q_heads / kv_heads
+  int col0;      // first head-dim column of this launch's slices (0 unless a pass covers part of d)
+  int n_chunks;  // slices per item in this launch (0: head_dim / head_chunk)
   float scale;
   uint64_t budget_ns;
   int grid;
