@@ -96,9 +96,9 @@ struct BwdLayout {
   // With one stage, Q and dO are tracked per 64-column atom (barrier i = atom i), so the atoms
   // outside the pass's slice can be refilled as soon as S^T / dP^T have read them.
   static constexpr int kQBars = (kStages == 1) ? kAtoms : kStages;
-  // kv_full, kv_empty, q_full[B], q_empty[B], do_full[B], do_empty[B], s_full, p_full, dp_full,
-  // ds_full, ds_free, dq_full, dq_free, acc_full, acc_free, drain, staged, stage_read, stage_free
-  static constexpr int kNumBars = 2 + 4 * kQBars + 13;
+  // k_full, k_empty, v_full, v_empty, q_full[B], q_empty[B], do_full[B], do_empty[B], s_full, p_full,
+  // dp_full, ds_full, ds_free, dq_full, dq_free, acc_full, acc_free, drain, staged, stage_read, stage_free
+  static constexpr int kNumBars = 4 + 4 * kQBars + 13;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   static constexpr int kAlloc = kBytes + 256;
@@ -217,15 +217,20 @@ __global__ void __launch_bounds__(448, 1)
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
-  uint64_t* kv_full = bars + 0;
-  uint64_t* kv_empty = bars + 1;
+  // K and V of an item are released separately: V after the item's last dP^T,
+  // K after its last dQ, so the next item's V (and most of its K) load while
+  // the last tile of this one is still computing
+  uint64_t* k_full = bars + 0;
+  uint64_t* k_empty = bars + 1;
+  uint64_t* v_full = bars + 2;
+  uint64_t* v_empty = bars + 3;
   // per stage (two stages) or per 64-column atom (one stage)
   constexpr int kQB = Lay::kQBars;
-  uint64_t* q_full = bars + 2;            // Q and the LSE / delta rows of a query tile
-  uint64_t* q_empty = bars + 2 + kQB;
-  uint64_t* do_full = bars + 2 + 2 * kQB;  // dO of a query tile
-  uint64_t* do_empty = bars + 2 + 3 * kQB;
-  uint64_t* s_full = bars + 2 + 4 * kQB;
+  uint64_t* q_full = bars + 4;            // Q and the LSE / delta rows of a query tile
+  uint64_t* q_empty = bars + 4 + kQB;
+  uint64_t* do_full = bars + 4 + 2 * kQB;  // dO of a query tile
+  uint64_t* do_empty = bars + 4 + 3 * kQB;
+  uint64_t* s_full = bars + 4 + 4 * kQB;
   uint64_t* p_full = s_full + 1;
   uint64_t* dp_full = s_full + 2;
   uint64_t* ds_full = s_full + 3;
@@ -244,8 +249,10 @@ __global__ void __launch_bounds__(448, 1)
   ptx::CtaCtl* ctl = reinterpret_cast<ptx::CtaCtl*>(smem + Lay::kOffMisc + 8);
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(kv_full, 1);
-    ptx::mbar_init(kv_empty, 1);
+    ptx::mbar_init(k_full, 1);
+    ptx::mbar_init(k_empty, 1);
+    ptx::mbar_init(v_full, 1);
+    ptx::mbar_init(v_empty, 1);
     for (int i = 0; i < kQB; ++i) {
       ptx::mbar_init(q_full + i, 1);
       ptx::mbar_init(q_empty + i, 1);
@@ -373,13 +380,17 @@ __global__ void __launch_bounds__(448, 1)
       int v = next_item(blockIdx.x, I);
       if (v < n_work) ok = load_qdo(I, 0);
       while (ok && v < n_work) {
-        if (!(ok = ptx::mbar_wait(kv_empty, (kitem & 1) ^ 1, ctl, status, kSiteBwdProdKV, budget))) break;
-        ptx::mbar_arrive_expect_tx(kv_full, 2 * Lay::kTileBytes);
+        // V first: the previous item's last dP^T released it before its last dQ released K
+        if (!(ok = ptx::mbar_wait(v_empty, (kitem & 1) ^ 1, ctl, status, kSiteBwdProdKV, budget))) break;
+        ptx::mbar_arrive_expect_tx(v_full, Lay::kTileBytes);
 #pragma unroll
-        for (int a = 0; a < Lay::kAtoms; ++a) {
-          ptx::tma_load_2d(smem + Lay::kOffK + a * 16384, &tm_k, kv_full, I.h * D + 64 * a, I.kv_row0);
-          ptx::tma_load_2d(smem + Lay::kOffV + a * 16384, &tm_v, kv_full, I.h * D + 64 * a, I.kv_row0);
-        }
+        for (int a = 0; a < Lay::kAtoms; ++a)
+          ptx::tma_load_2d(smem + Lay::kOffV + a * 16384, &tm_v, v_full, I.h * D + 64 * a, I.kv_row0);
+        if (!(ok = ptx::mbar_wait(k_empty, (kitem & 1) ^ 1, ctl, status, kSiteBwdProdKV, budget))) break;
+        ptx::mbar_arrive_expect_tx(k_full, Lay::kTileBytes);
+#pragma unroll
+        for (int a = 0; a < Lay::kAtoms; ++a)
+          ptx::tma_load_2d(smem + Lay::kOffK + a * 16384, &tm_k, k_full, I.h * D + 64 * a, I.kv_row0);
         for (int ii = 1; ok && ii < I.nq; ++ii) ok = load_qdo(I, ii);
         if (!ok) break;
         BwdItem N;
@@ -404,7 +415,10 @@ __global__ void __launch_bounds__(448, 1)
           ptx::mbar_wait(do_full + q % kSt, (q / kSt) & 1, &no_abort, nullptr, kSiteBwdDrain, budget);
         }
       }
-      if (kitem > 0) ptx::mbar_wait(kv_full, (kitem - 1) & 1, &no_abort, nullptr, kSiteBwdDrain, budget);
+      if (kitem > 0) {  // the last fills of V and (if its wait was reached) K
+        ptx::mbar_wait(v_full, (kitem - 1) & 1, &no_abort, nullptr, kSiteBwdDrain, budget);
+        ptx::mbar_wait(k_full, (kitem - 1) & 1, &no_abort, nullptr, kSiteBwdDrain, budget);
+      }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -426,7 +440,7 @@ __global__ void __launch_bounds__(448, 1)
       const BwdItem I = bwd_item(p, v);
       if (I.nq <= 0) continue;
       const int ca = slice_col<D, DC>(p, I) >> 6;  // first atom of the item's slice
-      if (!(ok = wait(kv_full, kitem & 1, kSiteBwdMmaKV))) break;
+      if (!(ok = wait(k_full, kitem & 1, kSiteBwdMmaKV))) break;
       ptx::tc_fence_after();
       // S^T(x) = K Q^T. With two Q/dO stages it is issued for the first query
       // tile of the item at the start of the tile and for every later one right
@@ -478,7 +492,12 @@ __global__ void __launch_bounds__(448, 1)
           if (!(ok = atoms_mma(Lay::kColS, k_addr, q_addr, q_full, q_empty, s_full))) break;
           // dP^T = V dO^T into the columns dQ of the previous tile used
           if (x > 0 && !(ok = wait(dq_free, (x - 1) & 1, kSiteBwdMmaDQFree))) break;
+          if (ii == 0 && !(ok = wait(v_full, kitem & 1, kSiteBwdMmaKV))) break;
           if (!(ok = atoms_mma(Lay::kColDP, v_addr, do_addr, do_full, do_empty, dp_full))) break;
+          if (ii + 1 == I.nq) {  // the item's last dP^T was V's last reader
+            if (ptx::elect_one()) ptx::mma_commit(v_empty);
+            __syncwarp();
+          }
         } else {
           if (ii == 0) {
             if (!(ok = wait_q(pos))) break;
@@ -489,6 +508,7 @@ __global__ void __launch_bounds__(448, 1)
           // dP^T = V dO^T into the columns dQ of the previous tile used
           if (!(ok = wait(do_full + st, (pos / kSt) & 1, kSiteBwdMmaQ))) break;
           if (x > 0 && !(ok = wait(dq_free, (x - 1) & 1, kSiteBwdMmaDQFree))) break;
+          if (ii == 0 && !(ok = wait(v_full, kitem & 1, kSiteBwdMmaKV))) break;
           ptx::tc_fence_after();
           if (ptx::elect_one()) {
 #pragma unroll
@@ -498,6 +518,7 @@ __global__ void __launch_bounds__(448, 1)
                           ptx::sdesc_sw128(do_addr + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
             }
             ptx::mma_commit(dp_full);
+            if (ii + 1 == I.nq) ptx::mma_commit(v_empty);  // the item's last dP^T was V's last reader
           }
           __syncwarp();
         }
@@ -556,6 +577,7 @@ __global__ void __launch_bounds__(448, 1)
             // tile's stage is released by the epilogue, which stages dK and dV
             // there.
             mma_dq();
+            if (ii + 1 == I.nq) ptx::mma_commit(k_empty);  // the item's last dQ was K's last reader
             if (next_s) issue_s((pos + 1) % kSt);
             mma_dk();
             if (ii + 1 < I.nq) ptx::mma_commit(q_empty + st);
@@ -566,6 +588,7 @@ __global__ void __launch_bounds__(448, 1)
             mma_dk();
             for (int k = 0; k < kSliceAtoms; ++k) ptx::mma_commit(q_empty + ca + k);
             mma_dq();
+            if (ii + 1 == I.nq) ptx::mma_commit(k_empty);  // the item's last dQ was K's last reader
           }
           ptx::mma_commit(ds_free);  // dQ and dK have read dS
         }
@@ -573,10 +596,7 @@ __global__ void __launch_bounds__(448, 1)
         ++pos;
       }
       if (!ok) break;
-      if (ptx::elect_one()) {
-        ptx::mma_commit(kv_empty);
-        ptx::mma_commit(acc_full);
-      }
+      if (ptx::elect_one()) ptx::mma_commit(acc_full);
       __syncwarp();
       ++kitem;
     }
