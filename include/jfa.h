@@ -135,7 +135,8 @@ typedef struct {
  * One dense Q [q_len, heads, head_dim] is the query of every sequence of a
  * jagged K/V batch ([JFA] third paragraph). Not causal.
  *   O[b] = softmax(scale Q K_b^T) V_b; backward: dQ = sum_b dQ_b (the
- *   contended cross-CTA reduction), dK_b, dV_b per sequence.
+ *   contended cross-CTA reduction), dK_b, dV_b per sequence. The backward at
+ *   head_dim 192 runs the two head-axis passes of jfa_bwd.
  */
 typedef struct {
   const void* q;             /* bf16 [q_len, heads, head_dim] */

@@ -21,6 +21,21 @@ def _run(d):
     return o, lse, dq, dk, dv
 
 
+@pytest.mark.parametrize("head_dim", [64, 192])
+def test_broadcast_head_dims(head_dim):
+    """Broadcast-Q at head_dim 64 and 192 (the backward in two head-axis passes)."""
+    d = inputs.broadcast_inputs(batch=4, q_len=130, head_dim=head_dim, lk_lo=1, lk_hi=300, seed=2)
+    o, lse, dq, dk, dv = _run(d)
+    off = d["kv_offsets"].numpy()
+    O_ref, L_ref = orc.broadcast_forward(np64(d["q"]), np64(d["k"]), np64(d["v"]), off, d["scale"])
+    dQ, dK, dV = orc.broadcast_backward(np64(d["q"]), np64(d["k"]), np64(d["v"]), np64(d["do"]), off, d["scale"])
+    check_o(np64(o), O_ref, f"O d={head_dim}")
+    check_lse(np64(lse), L_ref, f"LSE d={head_dim}")
+    check_grad(np64(dq), dQ, f"dQ d={head_dim}")
+    check_grad(np64(dk), dK, f"dK d={head_dim}")
+    check_grad(np64(dv), dV, f"dV d={head_dim}")
+
+
 @pytest.mark.parametrize("q_len,batch,lo,hi", [(256, 6, 16, 2048), (100, 5, 1, 300), (300, 4, 120, 140)])
 def test_broadcast_small(q_len, batch, lo, hi):
     d = inputs.broadcast_inputs(batch=batch, q_len=q_len, lk_lo=lo, lk_hi=hi, seed=1)

@@ -551,7 +551,6 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
   if (!a) return JFA_ERR_INVALID_ARG;
   jfa_status st = check_bcast_common(a->batch, a->q_len, a->heads, a->head_dim, a->max_seqlen_k, a->total_k, a->scale);
   if (st != JFA_OK) return st;
-  if (a->head_dim == 192) return JFA_ERR_UNSUPPORTED;
   if (!aligned(a->kv_offsets, 4)) return JFA_ERR_INVALID_ARG;
   if (a->batch > 0 && a->q_len > 0) {
     if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->o, 16) ||
@@ -603,7 +602,6 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
       return JFA_ERR_CUDA;
     BwdLaunch bl{};
     bl.head_dim = a->head_dim;
-    bl.head_chunk = a->head_dim;
     bl.offsets = a->kv_offsets;
     bl.tile_base = qp.tile_base;
     bl.items = qp.items;
@@ -622,13 +620,14 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
     bl.pad_tiles = 0;
     bl.scale = a->scale;
     bl.budget_ns = wait_budget_ns();
-    bl.grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
     record(a->main_kernel_events, 0, stream);
     CUtensorMap tdq, tdk, tdv;
     if (!make_tmap_f32_acc(&tdq, dq_acc, a->q_len, cols) || !make_tmap_bf16(&tdk, a->dk, a->total_k, cols) ||
         !make_tmap_bf16(&tdv, a->dv, a->total_k, cols))
       return JFA_ERR_CUDA;
-    cudaError_t e = launch_bwd_main(bl, tq, tk, tv, tdo, tdq, tdk, tdv, stream);
+    // head_dim 192: the two head-axis passes of jfa_bwd; otherwise one slice
+    const int chunk = a->head_dim == 192 ? 0 : a->head_dim;
+    cudaError_t e = run_bwd_main(bl, chunk, sms, L.max_items, tq, tk, tv, tdo, tdq, tdk, tdv, stream);
     record(a->main_kernel_events, 1, stream);
     if (e != cudaSuccess) return JFA_ERR_CUDA;
   }
