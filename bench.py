@@ -616,7 +616,18 @@ def main():
         try:
             decode = measure_decode(jfa, device, peaks)
             detail["decode_smallq_q4"] = measure_decode(jfa, device, peaks, splits=(16, 32), q_len=4)
+            for P in (1, 128):  # the other page sizes of the decode workload
+                detail[f"decode_page{P}"] = measure_decode(jfa, device, peaks, page_size=P, splits=(16, 32))
             detail.update(measure_extra(jfa, device, peaks))
+            # every row against the measured peaks: attention against the sustained bf16 rate
+            # (each kernel runs inside a longer job), decode against the copy rate
+            tc = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+            for row in detail.values():
+                if not isinstance(row, dict):
+                    continue
+                for key in ("fwd_tflops", "bwd_tflops", "fwd_bwd_tflops"):
+                    if row.get(key) is not None:
+                        row[key.replace("tflops", "frac_of_measured_tc")] = row[key] / tc
         except Exception as ex:  # report, never hide
             detail["extra_error"] = repr(ex)
 

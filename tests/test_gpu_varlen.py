@@ -133,3 +133,26 @@ def test_varlen_autograd_wrapper():
     check_grad(np64(q.grad), dQ, "autograd dQ")
     check_grad(np64(k.grad), dK, "autograd dK")
     check_grad(np64(v.grad), dV, "autograd dV")
+
+
+def test_varlen_prefill_full_size_sampled():
+    """The chunked-prefill workload the bench times (64 sequences, L_q U[1, 1024] at the end of
+    L_k = L_q + U[0, 3072] keys, 32 query heads on 8 KV heads, d 128, causal) at full size; the
+    oracle checks forward and backward of three sampled sequences."""
+    g = torch.Generator().manual_seed(38)
+    ql = inputs.uniform_lengths(64, 1, 1024, g)
+    kl = ql + inputs.uniform_lengths(64, 0, 3072, g)
+    d = inputs.varlen_from_lengths(ql, kl, 32, 8, 128, g)
+    o, lse, dq, dk, dv = _run(d, True)
+    qo, ko = d["q_offsets"].numpy(), d["k_offsets"].numpy()
+    for b in (0, 31, 63):
+        q0, q1, k0, k1 = int(qo[b]), int(qo[b + 1]), int(ko[b]), int(ko[b + 1])
+        one_q, one_k = np.array([0, q1 - q0]), np.array([0, k1 - k0])
+        args = (np64(d["q"][q0:q1]), np64(d["k"][k0:k1]), np64(d["v"][k0:k1]))
+        O_ref, L_ref = orc.varlen_forward(*args, one_q, one_k, d["scale"], True)
+        check_o(np64(o[q0:q1]), O_ref, f"O seq {b}")
+        check_lse(np64(lse[:, q0:q1]), L_ref, f"LSE seq {b}")
+        dQ, dK, dV = orc.varlen_backward(*args, np64(d["do"][q0:q1]), one_q, one_k, d["scale"], True)
+        check_grad(np64(dq[q0:q1]), dQ, f"dQ seq {b}")
+        check_grad(np64(dk[k0:k1]), dK, f"dK seq {b}")
+        check_grad(np64(dv[k0:k1]), dV, f"dV seq {b}")
