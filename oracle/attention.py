@@ -64,6 +64,7 @@ __all__ = [
     "merge_partials", "tile_queue",
     "lower_right_visible", "varlen_forward", "varlen_backward", "varlen_tile_queue",
     "split_counts", "split_bounds_per_seq", "decode_smallq_forward", "decode_smallq_split_partials",
+    "e4m3_decode", "attention_forward_fp8",
 ]
 
 
@@ -522,3 +523,41 @@ def decode_smallq_split_partials(q, k_cache, v_cache, page_table, seqlens, page_
                     Os[s, b, i, h] = Oh[0]
                     lses[s, b, i, h] = lse[0]
     return Os, lses
+
+
+# ----------------------------------------------------------------------------
+# FP8 (e4m3) inputs
+# ----------------------------------------------------------------------------
+#
+# "Optimizing FlashAttention-4 for Efficient Inference" (hpjadul), section
+# "PR 2109: Support FP8 Inputs": the forward takes FP8 inputs for inference.
+# The page gives neither the FP8 format nor a scale convention. Reading: e4m3
+# (the 8-bit format with 4 exponent and 3 mantissa bits, the one with the range
+# for activations) with one descale factor per tensor, so an input byte x of
+# tensor T stands for e4m3(x) * T_descale. What the forward computes is then
+# exact attention over those real values, and the output is bf16.
+
+def e4m3_decode(codes):
+    """float64 values of e4m3 byte codes (uint8 array), from the format's
+    definition: bit 7 sign, bits 6-3 exponent with bias 7, bits 2-0 mantissa;
+    exponent field 0 is subnormal (mantissa / 8 * 2^-6); exponent 15 with
+    mantissa 7 is NaN; there are no infinities, so the largest value is 448."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    normal = (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0)
+    sub = (m / 8.0) * 2.0 ** -6
+    val = sign * np.where(e == 0, sub, normal)
+    return np.where((e == 15) & ((c & 0x7) == 7), np.nan, val)
+
+
+def attention_forward_fp8(q8, k8, v8, offsets, scale, causal, q_descale, k_descale, v_descale):
+    """Jagged attention over FP8 inputs: q8, k8, v8 are uint8 e4m3 codes
+    [total, H, d]; each stands for its decoded value times the tensor's
+    descale. Returns O [total, H, d] and LSE [H, total] of exact attention
+    over those values (attention_forward on the dequantized tensors)."""
+    q = e4m3_decode(q8) * float(q_descale)
+    k = e4m3_decode(k8) * float(k_descale)
+    v = e4m3_decode(v8) * float(v_descale)
+    return attention_forward(q, k, v, offsets, scale, causal)

@@ -623,4 +623,46 @@ def pin_smallq_split_merge(o):
         _close(L2, LSE, 1e-12, f"small-query split {S}/{mn} LSE")
 
 
+
+# ---------------------------------------------------------------- FP8 inputs
+
+def pin_e4m3_decode(o):
+    """The e4m3 decoder against hand-derived codes and against torch's own
+    float8_e4m3fn type for all 256 codes (NaN where torch has NaN)."""
+    hand = {0x00: 0.0, 0x80: -0.0, 0x38: 1.0, 0x40: 2.0, 0x3C: 1.5, 0x7E: 448.0, 0xFE: -448.0,
+            0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x30: 0.5}
+    for code, val in hand.items():
+        got = float(o.e4m3_decode(np.array([code], dtype=np.uint8))[0])
+        assert got == val, (hex(code), got, val)
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.tensor(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = o.e4m3_decode(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+def pin_fp8_attention(o):
+    """FP8 attention is attention over the dequantized inputs; with unit
+    descales and inputs that are already e4m3 values it equals torch fp64 SDPA."""
+    r = _rng(51)
+    lengths = [5, 1, 9]
+    off = np.concatenate([[0], np.cumsum(lengths)])
+    T, H, d = off[-1], 2, 4
+    x = [torch.tensor(r.standard_normal((T, H, d))).to(torch.float8_e4m3fn) for _ in range(3)]
+    codes = [t.view(torch.uint8).numpy() for t in x]
+    for causal in (False, True):
+        O, LSE = o.attention_forward_fp8(*codes, off, 0.5, causal, 1.0, 1.0, 1.0)
+        for b in range(len(lengths)):
+            s0, s1 = off[b], off[b + 1]
+            tq, tk, tv = (t[s0:s1].to(torch.float64).transpose(0, 1) for t in x)
+            ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=0.5, is_causal=causal)
+            _close(O[s0:s1], ref.numpy().transpose(1, 0, 2), 1e-12, "fp8 attention vs sdpa")
+    # descales: scaling K by c is scaling the softmax scale by c; scaling V scales O
+    O1, L1 = o.attention_forward_fp8(*codes, off, 0.5, False, 1.0, 2.0, 3.0)
+    O2, L2 = o.attention_forward_fp8(*codes, off, 1.0, False, 1.0, 1.0, 1.0)
+    _close(O1, 3.0 * O2, 1e-12, "fp8 descales O")
+    _close(L1, L2, 1e-12, "fp8 descales LSE")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -180,6 +180,21 @@ def _split_counts_floor(m):
     m.split_counts = counts
 
 
+def _e4m3_bias_8(m):
+    # exponent bias 8 instead of 7
+    orig = m.e4m3_decode
+
+    def dec(codes):
+        return orig(codes) * 0.5
+    m.e4m3_decode = dec
+
+
+def _fp8_no_v_descale(m):
+    def fwd(q8, k8, v8, offsets, scale, causal, qd, kd, vd):
+        return real_oracle.attention_forward_fp8(q8, k8, v8, offsets, scale, causal, qd, kd, 1.0)
+    m.attention_forward_fp8 = fwd
+
+
 MUTANTS = {
     "bwd_drop_delta": _bwd_variant("drop_delta"),
     "bwd_sign_dS": _bwd_variant("sign_dS"),
@@ -198,6 +213,8 @@ MUTANTS = {
     "varlen_dk_last_head": _varlen_dk_last_head,
     "smallq_top_left": _smallq_top_left,
     "split_counts_floor": _split_counts_floor,
+    "e4m3_bias_8": _e4m3_bias_8,
+    "fp8_no_v_descale": _fp8_no_v_descale,
 }
 
 
