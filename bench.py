@@ -372,6 +372,17 @@ def measure_extra(jfa, device, peaks):
                                  "workload": "64 seqs, L_q U[1,1024], L_k = L_q + U[0,3072], Hq 32 / Hkv 8, d 128, "
                                              "causal bottom-right"}
     del q, k, v, do, o, lse
+    # FP8 (e4m3) inputs, GEM-like s=0.5 forward (batch 1024, H 4, d 128), per-tensor descales
+    w = gem_workload(0, device)
+    T = w["total"]
+    q8, k8, v8 = (inputs.fp8_quantize(w[x].float())[0] for x in ("q", "k", "v"))
+    o8, l8 = jfa.jfa_fwd_fp8(q8, k8, v8, w["offsets"], w["max_seqlen"], 0.01, 0.01, 0.01)
+    t8 = time_events(lambda: jfa.jfa_fwd_fp8(q8, k8, v8, w["offsets"], w["max_seqlen"], 0.01, 0.01, 0.01, o=o8,
+                                             lse=l8), 10, 3)
+    out["fp8_fwd_gem"] = {"fwd_tflops": attn_flops(w["lengths"], 4, 128, False, "fwd") / (t8 * 1e-3) / 1e12,
+                          "fwd_ms": t8, "workload": "GEM-like s=0.5 forward, e4m3 Q/K/V (V transposed per tile in "
+                                                    "the call), bf16 O"}
+    del w, q8, k8, v8, o8, l8
     for sp in (0.1, 0.9):
         w = gem_workload(0, device, sparsity=sp)
         bufs = alloc_bufs(jfa, w, device)

@@ -260,6 +260,29 @@ typedef struct {
   void* main_kernel_events;  /* optional cudaEvent_t[2] around the split kernel */
 } jfa_decode_args;
 
+/* ------------------------------------------------------------------ FP8 forward
+ * Jagged self-attention forward with FP8 inputs ([INF] PR 2109: FP8 inputs for
+ * inference). The page gives no format or scale convention; reading: e4m3
+ * bytes (sign, 4 exponent bits with bias 7, 3 mantissa bits) with one descale
+ * factor per tensor, so byte x of Q stands for e4m3(x) * q_descale (likewise
+ * K, V), and the forward computes jfa_fwd's attention over those values:
+ *   S = scale * Q_b K_b^T (causal: j <= i), P = softmax_rows(S), O = P V_b.
+ * P enters P V as e4m3 (relative rounding error up to 2^-4); O is bf16, LSE
+ * fp32 natural log. head_dim must be 128. */
+typedef struct {
+  const void* q;             /* e4m3 bytes [total, heads, 128] */
+  const void* k;             /* e4m3 bytes [total, heads, 128] */
+  const void* v;             /* e4m3 bytes [total, heads, 128] */
+  const int32_t* offsets;    /* int32 [batch+1], device */
+  int32_t batch, heads, head_dim, max_seqlen, total;
+  float scale;
+  int32_t causal;
+  float q_descale, k_descale, v_descale;  /* > 0 */
+  void* o;                   /* out: bf16 [total, heads, 128] */
+  float* lse;                /* out: fp32 [heads, total] */
+  void* main_kernel_events;  /* optional cudaEvent_t[2] */
+} jfa_fwd_fp8_args;
+
 /* ------------------------------------------------------------------ small-query paged decode
  * Paged split-KV GQA decode with q_len >= 1 query tokens per sequence ([INF]
  * PR 1993: tiles sized to few query rows, e.g. speculative decoding; with the
@@ -304,6 +327,7 @@ JFA_API size_t jfa_decode_workspace_size(const jfa_decode_args* args);
 JFA_API size_t jfa_varlen_fwd_workspace_size(const jfa_varlen_fwd_args* args);
 JFA_API size_t jfa_varlen_bwd_workspace_size(const jfa_varlen_bwd_args* args);
 JFA_API size_t jfa_decode_smallq_workspace_size(const jfa_decode_smallq_args* args);
+JFA_API size_t jfa_fwd_fp8_workspace_size(const jfa_fwd_fp8_args* args);
 
 /* Entry points. `workspace` is device memory of at least the size above,
  * 256-byte aligned; its contents on entry do not matter. */
@@ -321,6 +345,8 @@ JFA_API jfa_status jfa_bwd_varlen(const jfa_varlen_bwd_args* args, void* workspa
                           cudaStream_t stream);
 JFA_API jfa_status jfa_decode_smallq(const jfa_decode_smallq_args* args, void* workspace, size_t workspace_bytes,
                              cudaStream_t stream);
+JFA_API jfa_status jfa_fwd_fp8(const jfa_fwd_fp8_args* args, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
 
 /* Paged split-KV decode that allocates nothing. The pages have no
  * counterpart for this entry point; it exists for callers that cannot

@@ -26,6 +26,7 @@ STRUCTS = {
     "jfa_varlen_fwd_args": _abi.VarlenFwdArgs,
     "jfa_varlen_bwd_args": _abi.VarlenBwdArgs,
     "jfa_decode_smallq_args": _abi.DecodeSmallqArgs,
+    "jfa_fwd_fp8_args": _abi.FwdFp8Args,
 }
 
 

@@ -14,6 +14,7 @@ kernels; there is no CPU or PyTorch fallback.
     jfa_fwd_varlen        separate query / key lengths, grouped KV heads -> (O, LSE)
     jfa_bwd_varlen        its backward -> (dQ, dK, dV)
     jfa_decode_smallq     paged split-KV decode of a few query tokens per sequence -> (O, LSE)
+    jfa_fwd_fp8           jagged forward over FP8 (e4m3) inputs with per-tensor descales -> (O, LSE)
     jagged_attention      autograd wrapper of jfa_fwd / jfa_bwd
     varlen_attention      autograd wrapper of jfa_fwd_varlen / jfa_bwd_varlen
 """
@@ -29,7 +30,7 @@ from . import _abi
 __all__ = [
     "JfaError", "jfa_fwd", "jfa_bwd", "jfa_fwd_broadcast_q", "jfa_bwd_broadcast_q", "jfa_decode_splitkv",
     "jfa_read_device_status", "jagged_attention", "library", "jfa_fwd_varlen", "jfa_bwd_varlen",
-    "varlen_attention", "jfa_decode_smallq", "jfa_selftest_wait_timeout",
+    "varlen_attention", "jfa_decode_smallq", "jfa_selftest_wait_timeout", "jfa_fwd_fp8",
 ]
 
 
@@ -213,6 +214,39 @@ def jfa_bwd_broadcast_q(q, k, v, o, dout, lse, kv_offsets, max_seqlen_k, scale=N
     _check(lib.jfa_bwd_broadcast_q(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_bwd_broadcast_q")
     _finish(ws, check, stream, "jfa_bwd_broadcast_q")
     return dq, dk, dv
+
+
+def jfa_fwd_fp8(q, k, v, offsets, max_seqlen, q_descale, k_descale, v_descale, scale=None, causal=False, o=None,
+                lse=None, workspace=None, stream=None, events=None, check=False):
+    """Jagged forward over FP8 inputs. q, k, v: e4m3 codes [total, H, 128] (torch.uint8 or
+    torch.float8_e4m3fn); byte x of q stands for e4m3(x) * q_descale (likewise k, v).
+    Returns O bf16 [total, H, 128] and LSE fp32 [H, total]."""
+    qkv = []
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        if isinstance(t, torch.Tensor) and t.dtype == torch.float8_e4m3fn:
+            t = t.view(torch.uint8)
+        _need(t, n, torch.uint8, 3)
+        qkv.append(t)
+    q, k, v = qkv
+    _need(offsets, "offsets", torch.int32, 1)
+    total, H, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty((total, H, d), dtype=torch.bfloat16, device=q.device) if o is None else o
+    lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "o", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    a = _abi.FwdFp8Args(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), offsets.numel() - 1, H, d, int(max_seqlen), total,
+                        scale, int(bool(causal)), float(q_descale), float(k_descale), float(v_descale), _ptr(o),
+                        _ptr(lse), None)
+    ev, _keep = _events(events)
+    a.main_kernel_events = ev
+    lib = library()
+    ws = _workspace(lib.jfa_fwd_fp8_workspace_size(ctypes.byref(a)), q.device, workspace)
+    _check(lib.jfa_fwd_fp8(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_fwd_fp8")
+    _finish(ws, check, stream, "jfa_fwd_fp8")
+    return o, lse
 
 
 # ---------------------------------------------------------------- varlen / GQA

@@ -67,6 +67,21 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// 2-D byte view [rows, cols] (e4m3 tiles) read in 128-row x 128-byte boxes
+// with the 128-byte swizzle.
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  if (rows == 0) rows = 1;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(kTile)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D bf16 view [rows, cols] (cols contiguous) read in 128-row x 64-column
 // boxes with the 128-byte swizzle the tcgen05 descriptors expect.
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows = kTile) {
@@ -196,6 +211,15 @@ Layout var_layout(int64_t batch, int64_t q_heads, int64_t kv_heads, int64_t tota
     off = align_up(off + 4 * total_q * q_heads * head_dim, 256);
   }
   L.bytes = off;
+  return L;
+}
+
+// FP8 forward: the self-attention forward layout plus the transposed V blocks
+// (one [128 x 128] byte block per key tile and head).
+Layout fp8_layout(int64_t batch, int64_t heads, int64_t total, size_t* vt_off) {
+  Layout L = self_layout(batch, heads, total, 128, false);
+  *vt_off = L.bytes;
+  L.bytes = align_up(L.bytes + static_cast<size_t>(L.pad_tiles) * heads * 128 * 128, 256);
   return L;
 }
 
@@ -893,6 +917,67 @@ jfa_status jfa_selftest_wait_timeout(int32_t budget_us, void* ws, cudaStream_t s
   if (budget_us < 1 || budget_us > 10 * 1000 * 1000 || !aligned(ws, 256)) return JFA_ERR_INVALID_ARG;
   if (cudaMemsetAsync(ws, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
   return cuda_status(launch_selftest_wait(static_cast<int32_t*>(ws), static_cast<uint64_t>(budget_us) * 1000, stream));
+}
+
+size_t jfa_fwd_fp8_workspace_size(const jfa_fwd_fp8_args* a) {
+  if (!a) return 0;
+  size_t vt_off = 0;
+  return fp8_layout(a->batch, a->heads, a->total, &vt_off).bytes;
+}
+
+jfa_status jfa_fwd_fp8(const jfa_fwd_fp8_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!a) return JFA_ERR_INVALID_ARG;
+  if (a->batch < 0 || a->heads < 1 || a->total < 0 || a->max_seqlen < 0) return JFA_ERR_INVALID_ARG;
+  if (a->head_dim != 128) return JFA_ERR_UNSUPPORTED;
+  if (!(a->scale > 0.f) || !std::isfinite(a->scale) || a->causal < 0 || a->causal > 1) return JFA_ERR_INVALID_ARG;
+  for (float f : {a->q_descale, a->k_descale, a->v_descale})
+    if (!(f > 0.f) || !std::isfinite(f)) return JFA_ERR_INVALID_ARG;
+  if (!aligned(a->offsets, 4)) return JFA_ERR_INVALID_ARG;
+  if (a->total > 0 && (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->o, 16) ||
+                       !aligned(a->lse, 4)))
+    return JFA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(a->total) * a->heads * 128 >= (int64_t(1) << 40)) return JFA_ERR_INVALID_ARG;
+  size_t vt_off = 0;
+  const Layout L = fp8_layout(a->batch, a->heads, a->total, &vt_off);
+  if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
+  if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(w);
+  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (a->batch == 0 || a->total == 0) return JFA_OK;
+  const int sms = sm_count();
+  if (sms <= 0) return JFA_ERR_CUDA;
+  QueueParams qp{};
+  qp.offsets = a->offsets;
+  qp.batch = a->batch;
+  qp.heads = a->heads;
+  qp.total = a->total;
+  qp.max_seqlen = a->max_seqlen;
+  qp.causal = a->causal;
+  qp.mode = kQueueSelfFwd;
+  qp.status = status;
+  qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
+  qp.items = reinterpret_cast<int4*>(w + L.items);
+  qp.item_seq = reinterpret_cast<int4*>(w + L.item_seq);
+  qp.max_items = static_cast<int32_t>(L.max_items);
+  qp.count_index = 2;
+  if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  uint8_t* vt = w + vt_off;
+  if (launch_vt_transpose(a->v, a->offsets, qp.tile_base, status, a->batch, a->heads, static_cast<int>(L.pad_tiles),
+                          vt, stream) != cudaSuccess)
+    return JFA_ERR_CUDA;
+  CUtensorMap tq, tk, tvt;
+  const uint64_t cols = static_cast<uint64_t>(a->heads) * 128;
+  if (!make_tmap_u8(&tq, a->q, a->total, cols) || !make_tmap_u8(&tk, a->k, a->total, cols) ||
+      !make_tmap_u8(&tvt, vt, static_cast<uint64_t>(L.pad_tiles) * a->heads * 128, 128))
+    return JFA_ERR_CUDA;
+  const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
+  const float s_log2 = a->scale * a->q_descale * a->k_descale * 1.4426950408889634f;
+  record(a->main_kernel_events, 0, stream);
+  const cudaError_t e = launch_fwd_fp8(a->causal != 0, tq, tk, tvt, qp.items, qp.item_seq, status, a->o, a->lse,
+                                       a->heads, a->total, s_log2, a->v_descale, wait_budget_ns(), grid, stream);
+  record(a->main_kernel_events, 1, stream);
+  return cuda_status(e);
 }
 
 jfa_status jfa_read_device_status(const void* ws, cudaStream_t stream, int32_t* detail) {

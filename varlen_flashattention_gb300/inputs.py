@@ -161,6 +161,31 @@ def varlen_inputs(batch: int, q_lo: int, q_hi: int, k_lo: int, k_hi: int, q_head
     return varlen_from_lengths(ql, kl, q_heads, kv_heads, head_dim, g, with_grad)
 
 
+def fp8_quantize(x: torch.Tensor):
+    """Per-tensor e4m3 quantization of fp32 values: descale = amax / 448 (the largest e4m3
+    value), codes = e4m3(x / descale) as uint8. Returns (codes, descale)."""
+    amax = float(x.abs().max()) if x.numel() else 1.0
+    descale = max(amax, 1e-30) / 448.0
+    codes = (x / descale).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, descale
+
+
+def fp8_from_lengths(lengths, heads: int, seed: int, head_dim: int = 128) -> dict:
+    """FP8 jagged inputs: lengths -> Q -> K -> V drawn N(0,1) in fp32, each quantized to e4m3
+    with its own descale."""
+    g = _gen(seed)
+    lengths = torch.as_tensor(lengths, dtype=torch.int32)
+    offsets = offsets_from_lengths(lengths)
+    total = int(offsets[-1])
+    out = {"lengths": lengths, "offsets": offsets, "total": total,
+           "max_seqlen": int(lengths.max()) if lengths.numel() else 0, "heads": heads, "head_dim": head_dim,
+           "scale": 1.0 / math.sqrt(head_dim)}
+    for name in ("q", "k", "v"):
+        x = torch.randn(total, heads, head_dim, generator=g, dtype=torch.float32)
+        out[name], out[name + "_descale"] = fp8_quantize(x)
+    return out
+
+
 def broadcast_inputs(batch: int = 512, q_len: int = 256, heads: int = 4, head_dim: int = 128,
                      lk_lo: int = 16, lk_hi: int = 2048, seed: int = 0) -> dict:
     """Broadcast-Q: one dense Q [q_len, H, d] shared by `batch` jagged K/V sequences."""
