@@ -37,6 +37,23 @@ namespace jfa {
 
 namespace {
 
+// Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format code 0 in
+// bits 7-9 and 10-12), fp32 accumulation, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem], 8-bit inputs (K = 32 per instruction)
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 constexpr int kF8D = 128;                 // head_dim
 constexpr int kF8TileBytes = kTile * kF8D;  // one 128 x 128 e4m3 tile
 
@@ -92,7 +109,7 @@ __global__ void __launch_bounds__(192, 1)
                    const __grid_constant__ CUtensorMap tm_vt, const Fp8Params p) {
   using Lay = Fp8Layout;
   constexpr int kSlots = Lay::kSlots;
-  constexpr uint32_t kIdesc = ptx::idesc_e4m3(128, 128);
+  constexpr uint32_t kIdesc = idesc_e4m3(128, 128);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -195,7 +212,7 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t d_tmem = tmem + ((x & 1) ? Lay::kColS1 : Lay::kColS0);
 #pragma unroll
         for (int kk = 0; kk < kF8D / 32; ++kk)
-          ptx::mma_ss_f8(d_tmem, ptx::sdesc_sw128(q_addr + kk * 32, 16, 1024),
+          mma_ss_f8(d_tmem, ptx::sdesc_sw128(q_addr + kk * 32, 16, 1024),
                          ptx::sdesc_sw128(k_addr + kk * 32, 16, 1024), kIdesc, kk > 0 ? 1u : 0u);
         ptx::mma_commit(s_full + (x & 1));
         ptx::mma_commit(slot_empty + slot);
@@ -229,7 +246,7 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t p_addr = ptx::smem_u32(smem + Lay::kOffP + (x & 1) * kF8TileBytes);
 #pragma unroll
           for (int kk = 0; kk < kTile / 32; ++kk)
-            ptx::mma_ss_f8(tmem + Lay::kColO, ptx::sdesc_sw128(p_addr + kk * 32, 16, 1024),
+            mma_ss_f8(tmem + Lay::kColO, ptx::sdesc_sw128(p_addr + kk * 32, 16, 1024),
                            ptx::sdesc_sw128(vt_addr + kk * 32, 16, 1024), kIdesc, (j > 0 || kk > 0) ? 1u : 0u);
           ptx::mma_commit(o_ready + (x & 1));
           ptx::mma_commit(slot_empty + slot);
