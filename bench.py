@@ -633,12 +633,14 @@ def main():
             # every row against the measured peaks: attention against the sustained bf16 rate
             # (each kernel runs inside a longer job), decode against the copy rate
             tc = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-            for row in detail.values():
+            for name, row in detail.items():
                 if not isinstance(row, dict):
                     continue
+                # an FP8 contraction against the fp8 rate: the measured bf16 rate x the nominal 2x
+                peak_row = tc * 2 if name.startswith("fp8") else tc
                 for key in ("fwd_tflops", "bwd_tflops", "fwd_bwd_tflops"):
                     if row.get(key) is not None:
-                        row[key.replace("tflops", "frac_of_measured_tc")] = row[key] / tc
+                        row[key.replace("tflops", "frac_of_measured_tc")] = row[key] / peak_row
         except Exception as ex:  # report, never hide
             detail["extra_error"] = repr(ex)
 
