@@ -963,8 +963,8 @@ jfa_status jfa_fwd_fp8(const jfa_fwd_fp8_args* a, void* ws, size_t ws_bytes, cud
   qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
   uint8_t* vt = w + vt_off;
-  if (launch_vt_transpose(a->v, a->offsets, qp.tile_base, status, a->batch, a->heads, static_cast<int>(L.pad_tiles),
-                          vt, stream) != cudaSuccess)
+  if (launch_vt_transpose(a->v, qp.items, qp.item_seq, status, a->heads, static_cast<int>(L.max_items), vt,
+                          stream) != cudaSuccess)
     return JFA_ERR_CUDA;
   CUtensorMap tq, tk, tvt;
   const uint64_t cols = static_cast<uint64_t>(a->heads) * 128;
@@ -973,8 +973,10 @@ jfa_status jfa_fwd_fp8(const jfa_fwd_fp8_args* a, void* ws, size_t ws_bytes, cud
     return JFA_ERR_CUDA;
   const int grid = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(L.max_items, 1)));
   const float s_log2 = a->scale * a->q_descale * a->k_descale * 1.4426950408889634f;
+  CUtensorMap to;
+  if (!make_tmap_bf16(&to, a->o, a->total, cols)) return JFA_ERR_CUDA;
   record(a->main_kernel_events, 0, stream);
-  const cudaError_t e = launch_fwd_fp8(a->causal != 0, tq, tk, tvt, qp.items, qp.item_seq, status, a->o, a->lse,
+  const cudaError_t e = launch_fwd_fp8(a->causal != 0, tq, tk, tvt, to, qp.items, qp.item_seq, status, a->o, a->lse,
                                        a->heads, a->total, s_log2, a->v_descale, wait_budget_ns(), grid, stream);
   record(a->main_kernel_events, 1, stream);
   return cuda_status(e);

@@ -139,11 +139,12 @@ cudaError_t launch_bwd_post(const float* acc, void* dq, int64_t n, float scale, 
                             cudaStream_t stream);
 // FP8 (e4m3) input forward, head_dim 128: V transposed per 128-key tile into
 // [128 head-dim rows x 128 keys] blocks (block g * H + h = key tile g, head h;
-// tiles numbered by tile_base), then the forward over the self-attention queue.
-cudaError_t launch_vt_transpose(const void* v, const int32_t* offsets, const int32_t* tile_base, const int32_t* status,
-                                int batch, int heads, int pad_tiles, void* vt, cudaStream_t stream);
+// tiles numbered by tile_base), one CTA per item of the self-attention forward
+// queue, then the forward over that queue.
+cudaError_t launch_vt_transpose(const void* v, const int4* items, const int4* item_seq, const int32_t* status,
+                                int heads, int max_items, void* vt, cudaStream_t stream);
 cudaError_t launch_fwd_fp8(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
-                           const int4* items, const int4* item_seq, int32_t* status, void* o, float* lse, int heads,
+                           const CUtensorMap& to, const int4* items, const int4* item_seq, int32_t* status, void* o, float* lse, int heads,
                            int total, float s_log2, float v_descale, uint64_t budget_ns, int grid,
                            cudaStream_t stream);
 // Failure-detection self-test: one CTA whose first pipeline stage waits for an
