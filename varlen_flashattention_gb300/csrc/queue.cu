@@ -285,12 +285,24 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
     }
   }
   if (one_cost) {
+    // every warp writes whole sequences, one record per lane, so each store
+    // instruction covers 32 consecutive records
     __syncthreads();
-    for (int b = tid; b < min(p.batch, kQueueLenCache); b += kQThreads) {
+    for (int b = warp; b < min(p.batch, kQueueLenCache); b += kWarps) {
       const int2 L = seq_lens(p, s_len, s_lenk, b);
       const int nt = item_tiles(p, L.x, L.y);
       const int k = nt > 0 ? item_cost(p, L.x, L.y, 0) : 0;
-      if (nt > 0 && k >= kmin) write_items(b, s_first[b], nt, 0, k, L);
+      if (!(fits && nt > 0 && k >= kmin)) continue;
+      const int tb = p.tile_base ? p.tile_base[b] : 0;
+      const int4 seq = var ? make_int4(p.offsets[b], L.x, p.k_offsets[b], L.y) : make_int4(p.offsets[b], L.x, tb, 0);
+      const int w = p.mode == kQueueVarBwd ? tb : k;
+      const int64_t first = static_cast<int64_t>(s_first[b]) * p.heads;
+      const int n = nt * p.heads;  // records tile-major, heads inner: record e = (tile e / H, head e % H)
+      for (int e = lane; e < n; e += 32) {
+        const int t = e / p.heads;
+        p.items[first + e] = make_int4(b, e - t * p.heads, t, w);
+        if (p.item_seq) p.item_seq[first + e] = seq;
+      }
     }
   }
   if (tid == 0) {
