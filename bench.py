@@ -348,9 +348,25 @@ def measure_extra(jfa, device, peaks):
     tt = time_events(lambda: (jfa.jfa_fwd(q, k, v, off, d["max_seqlen"], d["scale"], o=o, lse=lse),
                               jfa.jfa_bwd(q, k, v, o, do, lse, off, d["max_seqlen"], d["scale"])), 20, 3)
     fl = attn_flops(d["lengths"].tolist(), 2, 64, False, "fwd") + attn_flops(d["lengths"].tolist(), 2, 64, False, "bwd")
+    # the same step captured once in a CUDA graph and replayed (one launch per step)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws_f = torch.empty(1 << 20, dtype=torch.uint8, device=device)
+    ws_b = torch.empty(8 << 20, dtype=torch.uint8, device=device)
+
+    def tiny_step():
+        jfa.jfa_fwd(q, k, v, off, d["max_seqlen"], d["scale"], o=o, lse=lse, workspace=ws_f)
+        jfa.jfa_bwd(q, k, v, o, do, lse, off, d["max_seqlen"], d["scale"], dq=dq, dk=dk, dv=dv, workspace=ws_b)
+    tiny_step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        tiny_step()
+    tg = time_events(graph.replay, 50, 5)
     out["tiny"] = {"fwd_bwd_us": tt * 1e3, "fwd_bwd_tflops": fl / (tt * 1e-3) / 1e12,
-                   "workload": "batch 4, L U[1,64], 2 heads, d 64 (launch- and queue-bound)"}
-    del q, k, v, do, o, lse
+                   "graph_replay_us": tg * 1e3,
+                   "workload": "batch 4, L U[1,64], 2 heads, d 64 (launch- and queue-bound); graph_replay_us: the "
+                               "same fwd+bwd captured in a CUDA graph"}
+    del q, k, v, do, o, lse, dq, dk, dv, graph
     # varlen GQA, chunked-prefill shape: 64 sequences, query chunk L_q U[1, 1024] at the
     # end of L_k = L_q + U[0, 3072] keys, 32 query heads on 8 KV heads, d 128, causal
     # (bottom-right aligned)
