@@ -49,17 +49,44 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _need(t, name, dtype, dims=None):
+def _need(t, name, dtype, shape):
+    """Type, dtype, shape (a tuple, or an int: the number of dimensions) and
+    layout of one argument. The kernels address every tensor from the shapes
+    of q (and k), so each buffer is checked against them here; the device is
+    checked by _device once every tensor of the call is known."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be on a CUDA device")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if isinstance(shape, int):
+        if t.dim() != shape:
+            raise ValueError(f"{name} must have {shape} dimensions, got {tuple(t.shape)}")
+    elif tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if dims is not None and t.dim() != dims:
-        raise ValueError(f"{name} must have {dims} dimensions, got {tuple(t.shape)}")
+
+
+def _need_offsets(t, name):
+    _need(t, name, torch.int32, 1)
+    if t.numel() < 1:
+        raise ValueError(f"{name} must hold batch + 1 >= 1 entries")
+
+
+def _device(**tensors):
+    """The one CUDA device that holds every given tensor (None entries are
+    skipped); the call runs there, on that device's stream."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be on a CUDA device")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the other tensors on {dev}")
+    return dev
 
 
 def _stream(stream):
@@ -80,9 +107,29 @@ def _events(events):
 def _workspace(nbytes, device, workspace):
     if workspace is None:
         return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
-    if workspace.numel() * workspace.element_size() < nbytes:
-        raise ValueError(f"workspace holds {workspace.numel()} bytes, needs {nbytes}")
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor")
+    if workspace.device != device:
+        raise ValueError(f"workspace is on {workspace.device}, the call runs on {device}")
+    if _nbytes(workspace) < nbytes:
+        raise ValueError(f"workspace holds {_nbytes(workspace)} bytes, needs {nbytes}")
     return workspace
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def _run(entry, size_entry, a, device, workspace, stream, check):
+    """Sizes the workspace, calls the entry point on `device` and its stream,
+    and with check=True reads the device status back (a stream sync)."""
+    lib = library()
+    with torch.cuda.device(device):
+        if stream is not None and stream.device != device:
+            raise ValueError(f"stream belongs to {stream.device}, the call runs on {device}")
+        ws = _workspace(getattr(lib, size_entry)(ctypes.byref(a)), device, workspace)
+        _check(getattr(lib, entry)(ctypes.byref(a), _ptr(ws), _nbytes(ws), _stream(stream)), entry)
+        _finish(ws, check, stream, entry)
 
 
 def _check(status, where):
@@ -121,36 +168,40 @@ def jfa_fwd(q, k, v, offsets, max_seqlen, scale=None, causal=False, o=None, lse=
             stream=None, events=None, check=False):
     """Jagged self-attention forward. q, k, v: bf16 [total, H, d]; offsets: int32 [B+1] (CUDA).
     Returns O bf16 [total, H, d] and LSE fp32 [H, total] (natural log)."""
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _need(t, n, torch.bfloat16, 3)
-    _need(offsets, "offsets", torch.int32, 1)
+    _need(q, "q", torch.bfloat16, 3)
     total, H, d = q.shape
-    if k.shape != q.shape or v.shape != q.shape:
-        raise ValueError("q, k, v must have the same shape")
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need_offsets(offsets, "offsets")
+    if o is not None:
+        _need(o, "o", torch.bfloat16, q.shape)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (H, total))
+    dev = _device(q=q, k=k, v=v, offsets=offsets, o=o, lse=lse)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
-    _need(o, "o", torch.bfloat16, 3)
-    _need(lse, "lse", torch.float32, 2)
+    lse = torch.empty((H, total), dtype=torch.float32, device=dev) if lse is None else lse
     a = _abi.FwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), offsets.numel() - 1, H, d, int(max_seqlen),
                      total, scale, int(bool(causal)), _ptr(o), _ptr(lse), None)
     ev, _keep = _events(events)
     a.main_kernel_events = ev
-    lib = library()
-    ws = _workspace(lib.jfa_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
-    _check(lib.jfa_fwd(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_fwd")
-    _finish(ws, check, stream, "jfa_fwd")
+    _run("jfa_fwd", "jfa_fwd_workspace_size", a, dev, workspace, stream, check)
     return o, lse
 
 
 def jfa_bwd(q, k, v, o, dout, lse, offsets, max_seqlen, scale=None, causal=False, head_chunk=0,
             dq=None, dk=None, dv=None, workspace=None, stream=None, events=None, check=False):
     """Recompute-based backward of jfa_fwd. Returns dQ, dK, dV bf16 [total, H, d]."""
-    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
-        _need(t, n, torch.bfloat16, 3)
-    _need(lse, "lse", torch.float32, 2)
-    _need(offsets, "offsets", torch.int32, 1)
+    _need(q, "q", torch.bfloat16, 3)
     total, H, d = q.shape
+    for n, t in (("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _need(t, n, torch.bfloat16, q.shape)
+    _need(lse, "lse", torch.float32, (H, total))
+    _need_offsets(offsets, "offsets")
+    for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        if t is not None:
+            _need(t, n, torch.bfloat16, q.shape)
+    dev = _device(q=q, k=k, v=v, o=o, dout=dout, lse=lse, offsets=offsets, dq=dq, dk=dk, dv=dv)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -160,10 +211,7 @@ def jfa_bwd(q, k, v, o, dout, lse, offsets, max_seqlen, scale=None, causal=False
                      _ptr(dq), _ptr(dk), _ptr(dv), None)
     ev, _keep = _events(events)
     a.main_kernel_events = ev
-    lib = library()
-    ws = _workspace(lib.jfa_bwd_workspace_size(ctypes.byref(a)), q.device, workspace)
-    _check(lib.jfa_bwd(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_bwd")
-    _finish(ws, check, stream, "jfa_bwd")
+    _run("jfa_bwd", "jfa_bwd_workspace_size", a, dev, workspace, stream, check)
     return dq, dk, dv
 
 
@@ -171,36 +219,49 @@ def jfa_fwd_broadcast_q(q, k, v, kv_offsets, max_seqlen_k, scale=None, o=None, l
                         stream=None, events=None, check=False):
     """Broadcast-Q forward. q: bf16 [Lq, H, d] shared by every sequence; k, v jagged [total_k, H, d].
     Returns O bf16 [B, Lq, H, d] and LSE fp32 [B, H, Lq]."""
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _need(t, n, torch.bfloat16, 3)
-    _need(kv_offsets, "kv_offsets", torch.int32, 1)
+    _need(q, "q", torch.bfloat16, 3)
     Lq, H, d = q.shape
+    _need(k, "k", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, (k.shape[0], H, d))
+    _need(v, "v", torch.bfloat16, k.shape)
+    _need_offsets(kv_offsets, "kv_offsets")
     B = kv_offsets.numel() - 1
+    if o is not None:
+        _need(o, "o", torch.bfloat16, (B, Lq, H, d))
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, H, Lq))
+    dev = _device(q=q, k=k, v=v, kv_offsets=kv_offsets, o=o, lse=lse)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    o = torch.empty((B, Lq, H, d), dtype=torch.bfloat16, device=q.device) if o is None else o
-    lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device) if lse is None else lse
+    o = torch.empty((B, Lq, H, d), dtype=torch.bfloat16, device=dev) if o is None else o
+    lse = torch.empty((B, H, Lq), dtype=torch.float32, device=dev) if lse is None else lse
     a = _abi.BcastFwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_offsets), B, Lq, H, d, int(max_seqlen_k),
                           k.shape[0], scale, _ptr(o), _ptr(lse), None)
     ev, _keep = _events(events)
     a.main_kernel_events = ev
-    lib = library()
-    ws = _workspace(lib.jfa_bcast_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
-    _check(lib.jfa_fwd_broadcast_q(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_fwd_broadcast_q")
-    _finish(ws, check, stream, "jfa_fwd_broadcast_q")
+    _run("jfa_fwd_broadcast_q", "jfa_bcast_fwd_workspace_size", a, dev, workspace, stream, check)
     return o, lse
 
 
 def jfa_bwd_broadcast_q(q, k, v, o, dout, lse, kv_offsets, max_seqlen_k, scale=None, dq=None, dk=None, dv=None,
                         workspace=None, stream=None, events=None, check=False):
     """Broadcast-Q backward. Returns dQ bf16 [Lq, H, d] summed over the batch, dK, dV [total_k, H, d]."""
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _need(t, n, torch.bfloat16, 3)
-    _need(o, "o", torch.bfloat16, 4)
-    _need(dout, "dout", torch.bfloat16, 4)
-    _need(lse, "lse", torch.float32, 3)
-    _need(kv_offsets, "kv_offsets", torch.int32, 1)
+    _need(q, "q", torch.bfloat16, 3)
     Lq, H, d = q.shape
+    _need(k, "k", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, (k.shape[0], H, d))
+    _need(v, "v", torch.bfloat16, k.shape)
+    _need_offsets(kv_offsets, "kv_offsets")
     B = kv_offsets.numel() - 1
+    _need(o, "o", torch.bfloat16, (B, Lq, H, d))
+    _need(dout, "dout", torch.bfloat16, (B, Lq, H, d))
+    _need(lse, "lse", torch.float32, (B, H, Lq))
+    if dq is not None:
+        _need(dq, "dq", torch.bfloat16, q.shape)
+    if dk is not None:
+        _need(dk, "dk", torch.bfloat16, k.shape)
+    if dv is not None:
+        _need(dv, "dv", torch.bfloat16, k.shape)
+    dev = _device(q=q, k=k, v=v, o=o, dout=dout, lse=lse, kv_offsets=kv_offsets, dq=dq, dk=dk, dv=dv)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -209,10 +270,7 @@ def jfa_bwd_broadcast_q(q, k, v, o, dout, lse, kv_offsets, max_seqlen_k, scale=N
                           B, Lq, H, d, int(max_seqlen_k), k.shape[0], scale, _ptr(dq), _ptr(dk), _ptr(dv), None)
     ev, _keep = _events(events)
     a.main_kernel_events = ev
-    lib = library()
-    ws = _workspace(lib.jfa_bcast_bwd_workspace_size(ctypes.byref(a)), q.device, workspace)
-    _check(lib.jfa_bwd_broadcast_q(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_bwd_broadcast_q")
-    _finish(ws, check, stream, "jfa_bwd_broadcast_q")
+    _run("jfa_bwd_broadcast_q", "jfa_bcast_bwd_workspace_size", a, dev, workspace, stream, check)
     return dq, dk, dv
 
 
@@ -228,28 +286,42 @@ def jfa_fwd_fp8(q, k, v, offsets, max_seqlen, q_descale, k_descale, v_descale, s
         _need(t, n, torch.uint8, 3)
         qkv.append(t)
     q, k, v = qkv
-    _need(offsets, "offsets", torch.int32, 1)
     total, H, d = q.shape
-    if k.shape != q.shape or v.shape != q.shape:
-        raise ValueError("q, k, v must have the same shape")
+    _need(k, "k", torch.uint8, q.shape)
+    _need(v, "v", torch.uint8, q.shape)
+    _need_offsets(offsets, "offsets")
+    if o is not None:
+        _need(o, "o", torch.bfloat16, q.shape)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (H, total))
+    dev = _device(q=q, k=k, v=v, offsets=offsets, o=o, lse=lse)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    o = torch.empty((total, H, d), dtype=torch.bfloat16, device=q.device) if o is None else o
-    lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
-    _need(o, "o", torch.bfloat16, 3)
-    _need(lse, "lse", torch.float32, 2)
+    o = torch.empty((total, H, d), dtype=torch.bfloat16, device=dev) if o is None else o
+    lse = torch.empty((H, total), dtype=torch.float32, device=dev) if lse is None else lse
     a = _abi.FwdFp8Args(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), offsets.numel() - 1, H, d, int(max_seqlen), total,
                         scale, int(bool(causal)), float(q_descale), float(k_descale), float(v_descale), _ptr(o),
                         _ptr(lse), None)
     ev, _keep = _events(events)
     a.main_kernel_events = ev
-    lib = library()
-    ws = _workspace(lib.jfa_fwd_fp8_workspace_size(ctypes.byref(a)), q.device, workspace)
-    _check(lib.jfa_fwd_fp8(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_fwd_fp8")
-    _finish(ws, check, stream, "jfa_fwd_fp8")
+    _run("jfa_fwd_fp8", "jfa_fwd_fp8_workspace_size", a, dev, workspace, stream, check)
     return o, lse
 
 
 # ---------------------------------------------------------------- varlen / GQA
+
+def _var_inputs(q, k, v, q_offsets, k_offsets):
+    _need(q, "q", torch.bfloat16, 3)
+    total_q, Hq, d = q.shape
+    _need(k, "k", torch.bfloat16, 3)
+    total_k, Hkv, _ = k.shape
+    _need(k, "k", torch.bfloat16, (total_k, Hkv, d))
+    _need(v, "v", torch.bfloat16, k.shape)
+    _need_offsets(q_offsets, "q_offsets")
+    _need_offsets(k_offsets, "k_offsets")
+    if q_offsets.numel() != k_offsets.numel():
+        raise ValueError("q_offsets and k_offsets must have the same length")
+    return total_q, Hq, d, total_k, Hkv
+
 
 def jfa_fwd_varlen(q, k, v, q_offsets, k_offsets, max_seqlen_q, max_seqlen_k, scale=None, causal=False, o=None,
                    lse=None, workspace=None, stream=None, events=None, check=False):
@@ -257,30 +329,21 @@ def jfa_fwd_varlen(q, k, v, q_offsets, k_offsets, max_seqlen_q, max_seqlen_k, sc
     q: bf16 [total_q, Hq, d]; k, v: bf16 [total_k, Hkv, d] with Hq % Hkv == 0; q_offsets and
     k_offsets: int32 [B+1] (CUDA). causal aligns the mask to the bottom right (key j visible to
     query i iff j <= i + L_k - L_q). Returns O bf16 [total_q, Hq, d], LSE fp32 [Hq, total_q]."""
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _need(t, n, torch.bfloat16, 3)
-    _need(q_offsets, "q_offsets", torch.int32, 1)
-    _need(k_offsets, "k_offsets", torch.int32, 1)
-    total_q, Hq, d = q.shape
-    total_k, Hkv, dk_ = k.shape
-    if v.shape != k.shape or dk_ != d:
-        raise ValueError("k and v must be [total_k, Hkv, d] with the head_dim of q")
-    if q_offsets.numel() != k_offsets.numel():
-        raise ValueError("q_offsets and k_offsets must have the same length")
+    total_q, Hq, d, total_k, Hkv = _var_inputs(q, k, v, q_offsets, k_offsets)
+    if o is not None:
+        _need(o, "o", torch.bfloat16, q.shape)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (Hq, total_q))
+    dev = _device(q=q, k=k, v=v, q_offsets=q_offsets, k_offsets=k_offsets, o=o, lse=lse)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device) if lse is None else lse
-    _need(o, "o", torch.bfloat16, 3)
-    _need(lse, "lse", torch.float32, 2)
+    lse = torch.empty((Hq, total_q), dtype=torch.float32, device=dev) if lse is None else lse
     a = _abi.VarlenFwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(q_offsets), _ptr(k_offsets), q_offsets.numel() - 1,
                            Hq, Hkv, d, int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, scale,
                            int(bool(causal)), _ptr(o), _ptr(lse), None)
     ev, _keep = _events(events)
     a.main_kernel_events = ev
-    lib = library()
-    ws = _workspace(lib.jfa_varlen_fwd_workspace_size(ctypes.byref(a)), q.device, workspace)
-    _check(lib.jfa_fwd_varlen(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_fwd_varlen")
-    _finish(ws, check, stream, "jfa_fwd_varlen")
+    _run("jfa_fwd_varlen", "jfa_varlen_fwd_workspace_size", a, dev, workspace, stream, check)
     return o, lse
 
 
@@ -289,13 +352,18 @@ def jfa_bwd_varlen(q, k, v, o, dout, lse, q_offsets, k_offsets, max_seqlen_q, ma
                    check=False):
     """Backward of jfa_fwd_varlen. Returns dQ bf16 [total_q, Hq, d] and dK, dV bf16
     [total_k, Hkv, d] (a KV head's gradient summed over the query heads that read it)."""
-    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
-        _need(t, n, torch.bfloat16, 3)
-    _need(lse, "lse", torch.float32, 2)
-    _need(q_offsets, "q_offsets", torch.int32, 1)
-    _need(k_offsets, "k_offsets", torch.int32, 1)
-    total_q, Hq, d = q.shape
-    total_k, Hkv, _ = k.shape
+    total_q, Hq, d, total_k, Hkv = _var_inputs(q, k, v, q_offsets, k_offsets)
+    _need(o, "o", torch.bfloat16, q.shape)
+    _need(dout, "dout", torch.bfloat16, q.shape)
+    _need(lse, "lse", torch.float32, (Hq, total_q))
+    if dq is not None:
+        _need(dq, "dq", torch.bfloat16, q.shape)
+    if dk is not None:
+        _need(dk, "dk", torch.bfloat16, k.shape)
+    if dv is not None:
+        _need(dv, "dv", torch.bfloat16, k.shape)
+    dev = _device(q=q, k=k, v=v, o=o, dout=dout, lse=lse, q_offsets=q_offsets, k_offsets=k_offsets, dq=dq, dk=dk,
+                  dv=dv)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -306,14 +374,22 @@ def jfa_bwd_varlen(q, k, v, o, dout, lse, q_offsets, k_offsets, max_seqlen_q, ma
                            None)
     ev, _keep = _events(events)
     a.main_kernel_events = ev
-    lib = library()
-    ws = _workspace(lib.jfa_varlen_bwd_workspace_size(ctypes.byref(a)), q.device, workspace)
-    _check(lib.jfa_bwd_varlen(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_bwd_varlen")
-    _finish(ws, check, stream, "jfa_bwd_varlen")
+    _run("jfa_bwd_varlen", "jfa_varlen_bwd_workspace_size", a, dev, workspace, stream, check)
     return dq, dk, dv
 
 
 # ---------------------------------------------------------------- decode
+
+def _cache_inputs(k_cache, v_cache, page_table, seqlens_k, B, d):
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    num_pages, P, Hkv, _ = k_cache.shape
+    _need(k_cache, "k_cache", torch.bfloat16, (num_pages, P, Hkv, d))
+    _need(v_cache, "v_cache", torch.bfloat16, k_cache.shape)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(page_table, "page_table", torch.int32, (B, page_table.shape[1]))
+    _need(seqlens_k, "seqlens_k", torch.int32, (B,))
+    return num_pages, P, Hkv
+
 
 def jfa_decode_splitkv(q, k_cache, v_cache, page_table, seqlens_k, num_splits, scale=None, o=None, lse=None,
                        split_bounds=None, workspace=None, stream=None, events=None, check=False):
@@ -322,26 +398,25 @@ def jfa_decode_splitkv(q, k_cache, v_cache, page_table, seqlens_k, num_splits, s
     Returns O bf16 [B, Hq, 128] and LSE fp32 [B, Hq]. If `split_bounds` (int32 [B, S, 2])
     is given, the kernel writes each split's token range into it."""
     _need(q, "q", torch.bfloat16, 3)
-    _need(k_cache, "k_cache", torch.bfloat16, 4)
-    _need(v_cache, "v_cache", torch.bfloat16, 4)
-    _need(page_table, "page_table", torch.int32, 2)
-    _need(seqlens_k, "seqlens_k", torch.int32, 1)
     B, Hq, d = q.shape
-    num_pages, P, Hkv, d2 = k_cache.shape
-    if d2 != d or v_cache.shape != k_cache.shape:
-        raise ValueError("cache shapes do not match q")
+    num_pages, P, Hkv = _cache_inputs(k_cache, v_cache, page_table, seqlens_k, B, d)
+    if split_bounds is not None:
+        _need(split_bounds, "split_bounds", torch.int32, (B, int(num_splits), 2))
+    if o is not None:
+        _need(o, "o", torch.bfloat16, q.shape)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, Hq))
+    dev = _device(q=q, k_cache=k_cache, v_cache=v_cache, page_table=page_table, seqlens_k=seqlens_k, o=o, lse=lse,
+                  split_bounds=split_bounds)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev) if lse is None else lse
     a = _abi.DecodeArgs(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(seqlens_k),
                         B, Hq, Hkv, d, P, num_pages, page_table.shape[1], int(num_splits), scale,
                         _ptr(o), _ptr(lse), _ptr(split_bounds), None)
     ev, _keep = _events(events)
     a.main_kernel_events = ev
-    lib = library()
-    ws = _workspace(lib.jfa_decode_workspace_size(ctypes.byref(a)), q.device, workspace)
-    _check(lib.jfa_decode_splitkv(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_decode_splitkv")
-    _finish(ws, check, stream, "jfa_decode_splitkv")
+    _run("jfa_decode_splitkv", "jfa_decode_workspace_size", a, dev, workspace, stream, check)
     return o, lse
 
 
@@ -355,27 +430,28 @@ def jfa_decode_smallq(q, k_cache, v_cache, page_table, seqlens_k, num_splits, mi
     With min_split_tokens > 0 each sequence uses clamp(ceil(L / min_split_tokens), 1, num_splits)
     splits; `split_counts` (int32 [B]) and `split_bounds` (int32 [B, S, 2]) receive them if given."""
     _need(q, "q", torch.bfloat16, 4)
-    _need(k_cache, "k_cache", torch.bfloat16, 4)
-    _need(v_cache, "v_cache", torch.bfloat16, 4)
-    _need(page_table, "page_table", torch.int32, 2)
-    _need(seqlens_k, "seqlens_k", torch.int32, 1)
     B, ql, Hq, d = q.shape
-    num_pages, P, Hkv, d2 = k_cache.shape
-    if d2 != d or v_cache.shape != k_cache.shape:
-        raise ValueError("cache shapes do not match q")
+    num_pages, P, Hkv = _cache_inputs(k_cache, v_cache, page_table, seqlens_k, B, d)
+    if split_bounds is not None:
+        _need(split_bounds, "split_bounds", torch.int32, (B, int(num_splits), 2))
+    if split_counts is not None:
+        _need(split_counts, "split_counts", torch.int32, (B,))
+    if o is not None:
+        _need(o, "o", torch.bfloat16, q.shape)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, ql, Hq))
+    dev = _device(q=q, k_cache=k_cache, v_cache=v_cache, page_table=page_table, seqlens_k=seqlens_k, o=o, lse=lse,
+                  split_bounds=split_bounds, split_counts=split_counts)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((B, ql, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    lse = torch.empty((B, ql, Hq), dtype=torch.float32, device=dev) if lse is None else lse
     a = _abi.DecodeSmallqArgs(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(seqlens_k),
                               B, ql, Hq, Hkv, d, P, num_pages, page_table.shape[1], int(num_splits),
                               int(min_split_tokens), scale, _ptr(o), _ptr(lse), _ptr(split_bounds),
                               _ptr(split_counts), None)
     ev, _keep = _events(events)
     a.main_kernel_events = ev
-    lib = library()
-    ws = _workspace(lib.jfa_decode_smallq_workspace_size(ctypes.byref(a)), q.device, workspace)
-    _check(lib.jfa_decode_smallq(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "jfa_decode_smallq")
-    _finish(ws, check, stream, "jfa_decode_smallq")
+    _run("jfa_decode_smallq", "jfa_decode_smallq_workspace_size", a, dev, workspace, stream, check)
     return o, lse
 
 

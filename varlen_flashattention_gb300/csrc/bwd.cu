@@ -1088,12 +1088,11 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
                                 const CUtensorMap& tdv, const BwdParams& p, int grid,
                                 cudaStream_t stream) {
   using Lay = BwdLayout<D, DC>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, DC>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t e = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(bwd_kernel<D, DC>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
+  });
+  if (e != cudaSuccess) return e;
   bwd_kernel<D, DC><<<grid, 448, Lay::kAlloc, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
   return cudaGetLastError();
 }

@@ -465,16 +465,17 @@ cudaError_t launch_decode_general(const DecodeLaunch& a, float* part_o, float* p
   const int G = a.q_heads / a.kv_heads;
   const bool two = G * a.q_len > 8;
   dim3 grid(a.num_splits, a.kv_heads, a.batch);
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t ea = once_per_device(attr_done, [] {
     for (auto k : {decode_split_kernel<1, false>, decode_split_kernel<2, false>, decode_split_kernel<4, false>,
                    decode_split_kernel<8, false>, decode_split_kernel<1, true>, decode_split_kernel<2, true>,
                    decode_split_kernel<4, true>, decode_split_kernel<8, true>, decode_split_kernel<16, true>}) {
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecRingBytes);
+      const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecRingBytes);
       if (e != cudaSuccess) return e;
     }
-    attr_set = true;
-  }
+    return cudaSuccess;
+  });
+  if (ea != cudaSuccess) return ea;
   cudaEvent_t* ev = static_cast<cudaEvent_t*>(a.main_kernel_events);
   if (ev) cudaEventRecord(ev[0], stream);
   cudaError_t e;

@@ -421,12 +421,11 @@ template <int D, bool CAUSAL>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const FwdParams& p, int grid, cudaStream_t stream) {
   using Lay = FwdLayout<D>;
-  static bool attr_set = false;  // idempotent; a race only repeats the call
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t e = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(fwd_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
+  });
+  if (e != cudaSuccess) return e;
   fwd_kernel<D, CAUSAL><<<grid, 192, Lay::kAlloc, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

@@ -616,13 +616,12 @@ __global__ void __launch_bounds__(256) vt_transpose_kernel(const uint8_t* __rest
 template <bool CAUSAL>
 cudaError_t launch_fp8_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt, const CUtensorMap& to,
                          const Fp8Params& p, int grid, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(fwd_fp8_kernel<CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, Fp8Layout::kAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t e = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(fwd_fp8_kernel<CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Fp8Layout::kAlloc);
+  });
+  if (e != cudaSuccess) return e;
   fwd_fp8_kernel<CAUSAL><<<grid, kF8Threads, Fp8Layout::kAlloc, stream>>>(tq, tk, tvt, to, p);
   return cudaGetLastError();
 }

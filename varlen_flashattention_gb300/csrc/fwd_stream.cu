@@ -645,13 +645,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool CAUSAL>
 cudaError_t launch_fwd_stream_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& to, const FwdStreamParams& p, int grid, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_stream_kernel<CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         FwdStreamLayout::kBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t e = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(fwd_stream_kernel<CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FwdStreamLayout::kBytes);
+  });
+  if (e != cudaSuccess) return e;
   fwd_stream_kernel<CAUSAL><<<grid, kThreads, FwdStreamLayout::kBytes, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }

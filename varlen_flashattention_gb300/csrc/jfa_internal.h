@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -12,6 +13,21 @@
 namespace jfa {
 
 constexpr int kTile = 128;  // rows of a Q or K/V tile (tcgen05 M = 128)
+
+// Runs `set` (a kernel attribute call, idempotent) once per device: `done`
+// holds one bit per device already set, so launches from several threads or
+// on several devices stay correct. Devices past 63 run it on every launch.
+template <class F>
+inline cudaError_t once_per_device(std::atomic<uint64_t>& done, F&& set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? uint64_t(1) << dev : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Where a pipeline wait gave up (second word of the device status block).
 enum WaitSite : int32_t {

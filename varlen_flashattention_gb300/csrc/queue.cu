@@ -330,13 +330,12 @@ cudaError_t launch_queue(const QueueParams& p, cudaStream_t stream) {
   if (kmax > kQueueMaxCost) return cudaErrorInvalidValue;
   const int64_t cached = std::min(p.batch, kQueueLenCache);
   const size_t smem = static_cast<size_t>(kmax + 1 + kQueueLenCache + cached * (queue_var(p.mode) ? 2 : 1)) * sizeof(int);
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(build_queue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>((kQueueMaxCost + 1 + 3 * kQueueLenCache) * sizeof(int)));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t e = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(build_queue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>((kQueueMaxCost + 1 + 3 * kQueueLenCache) * sizeof(int)));
+  });
+  if (e != cudaSuccess) return e;
   build_queue_kernel<<<1, kQThreads, smem, stream>>>(p, static_cast<int>(kmax));
   return cudaGetLastError();
 }
