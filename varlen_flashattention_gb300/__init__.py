@@ -20,6 +20,7 @@ kernels; there is no CPU or PyTorch fallback.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 
@@ -61,7 +62,7 @@ def _need(t, name, dtype, shape):
     if isinstance(shape, int):
         if t.dim() != shape:
             raise ValueError(f"{name} must have {shape} dimensions, got {tuple(t.shape)}")
-    elif tuple(t.shape) != tuple(shape):
+    elif t.shape != shape:
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
@@ -76,17 +77,18 @@ def _need_offsets(t, name):
 def _device(**tensors):
     """The one CUDA device that holds every given tensor (None entries are
     skipped); the call runs there, on that device's stream."""
-    dev = None
+    idx = None
     for name, t in tensors.items():
         if t is None:
             continue
-        if not t.is_cuda:
+        i = t.get_device()  # -1 on the host
+        if i < 0:
             raise ValueError(f"{name} must be on a CUDA device")
-        if dev is None:
-            dev = t.device
-        elif t.device != dev:
-            raise ValueError(f"{name} is on {t.device}, the other tensors on {dev}")
-    return dev
+        if idx is None:
+            idx = i
+        elif i != idx:
+            raise ValueError(f"{name} is on cuda:{i}, the other tensors on cuda:{idx}")
+    return torch.device("cuda", idx)
 
 
 def _stream(stream):
@@ -109,7 +111,7 @@ def _workspace(nbytes, device, workspace):
         return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
     if not isinstance(workspace, torch.Tensor) or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous tensor")
-    if workspace.device != device:
+    if workspace.get_device() != device.index:
         raise ValueError(f"workspace is on {workspace.device}, the call runs on {device}")
     if _nbytes(workspace) < nbytes:
         raise ValueError(f"workspace holds {_nbytes(workspace)} bytes, needs {nbytes}")
@@ -124,8 +126,9 @@ def _run(entry, size_entry, a, device, workspace, stream, check):
     """Sizes the workspace, calls the entry point on `device` and its stream,
     and with check=True reads the device status back (a stream sync)."""
     lib = library()
-    with torch.cuda.device(device):
-        if stream is not None and stream.device != device:
+    here = device.index == torch.cuda.current_device()
+    with contextlib.nullcontext() if here else torch.cuda.device(device):
+        if stream is not None and stream.device_index != device.index:
             raise ValueError(f"stream belongs to {stream.device}, the call runs on {device}")
         ws = _workspace(getattr(lib, size_entry)(ctypes.byref(a)), device, workspace)
         _check(getattr(lib, entry)(ctypes.byref(a), _ptr(ws), _nbytes(ws), _stream(stream)), entry)
