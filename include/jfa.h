@@ -33,11 +33,18 @@
  *  - LSE is the natural-log log-sum-exp of the scaled scores of each query row.
  *  - Every pointer must be 16-byte aligned (TMA and 16-byte vector access);
  *    head_dim must be 64, 128 or 192 unless stated otherwise.
+ *  - Every pointer is device memory of the current device (cudaGetDevice()
+ *    when the call is made), and each buffer spans at least the extent its
+ *    field comment gives for the sizes in the argument struct. The library
+ *    checks null pointers, alignment and the sizes themselves, but cannot see
+ *    an allocation's extent: a shorter buffer is read or written out of bounds.
  *  - The caller owns and allocates every buffer, including the workspace,
  *    whose size comes from the matching *_workspace_size() call. The library
  *    allocates no memory, keeps no per-call state between calls, and may be
  *    called from several host threads on different streams with separate
- *    workspaces. Concurrent calls that share a workspace race.
+ *    workspaces. Concurrent calls that share a workspace race. (Its only
+ *    process-wide state is set-once: each kernel's shared-memory limit, raised
+ *    once per device, and cached device properties.)
  *  - All work is enqueued on `stream`; no call synchronises the stream except
  *    jfa_read_device_status(). Host-side argument errors are returned before
  *    anything is enqueued. Problems only the device can see (malformed
