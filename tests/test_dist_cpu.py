@@ -81,3 +81,68 @@ def test_two_rank_partition_and_reductions():
     for rank, err, mx, sm in results:
         assert err < 1e-13, (rank, err)
         assert mx == 3.0 and sm == 3.0
+
+
+def _bcast_worker(rank, world, port, out_q):
+    """Broadcast-Q backward with the batch sharded: each rank takes whole
+    sequences (longest-first greedy on the key lengths, as a balanced shard
+    would), computes its partial dQ, and one all-reduce (sum) gives the dQ of
+    the whole batch; dK / dV rows belong to one rank each."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import sys
+        root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+        sys.path.insert(0, root)
+        import oracle.attention as orc
+
+        rng = np.random.default_rng(1)
+        k_lengths = [7, 0, 23, 3, 12, 1, 18]
+        Lq, H, d = 5, 2, 8
+        off = np.concatenate([[0], np.cumsum(k_lengths)])
+        T = int(off[-1])
+        q = rng.standard_normal((Lq, H, d))
+        k, v = (rng.standard_normal((T, H, d)) for _ in range(2))
+        do = rng.standard_normal((len(k_lengths), Lq, H, d))
+        load = [0] * world
+        owner = {}
+        for b in sorted(range(len(k_lengths)), key=lambda b: (-k_lengths[b], b)):
+            r = min(range(world), key=lambda r: (load[r], r))
+            owner[b] = r
+            load[r] += k_lengths[b]
+        mine = [b for b in range(len(k_lengths)) if owner[b] == rank]
+        dq = np.zeros((Lq, H, d))
+        dk = np.zeros((T, H, d))
+        dv = np.zeros((T, H, d))
+        for b in mine:
+            s0, s1 = int(off[b]), int(off[b + 1])
+            one = np.array([0, s1 - s0])
+            a, kk, vv = orc.broadcast_backward(q, k[s0:s1], v[s0:s1], do[b:b + 1], one, 0.35)
+            dq += a
+            dk[s0:s1] = kk
+            dv[s0:s1] = vv
+        t = [torch.from_numpy(x) for x in (dq, dk, dv)]
+        for x in t:
+            dist.all_reduce(x)
+        ref = orc.broadcast_backward(q, k, v, do, off, 0.35)
+        err = max(float(np.max(np.abs(x.numpy() - r))) for x, r in zip(t, ref))
+        out_q.put((rank, err, len(mine)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_broadcast_dq_all_reduce():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_bcast_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = [q.get(timeout=240) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert sum(n for _, _, n in results) == 7
+    for rank, err, _ in results:
+        assert err < 1e-12, (rank, err)
