@@ -25,9 +25,10 @@
 namespace jfa {
 
 constexpr int kQThreads = 1024;
-// Sequence lengths kept in shared memory for the bucket passes (longer
-// batches read the rest from the offsets).
-constexpr int kQueueLenCache = 8 * 1024;
+// Per-sequence values (lengths, first rows, tile bases) kept in shared memory
+// for the bucket and record passes, for the first kQueueLenCache sequences
+// (longer batches read the rest from global memory).
+constexpr int kQueueLenCache = 4 * 1024;
 
 // Exclusive block-wide scan of one int per thread; returns the prefix and
 // writes the block total to *total. All kQThreads threads must call it.
@@ -151,14 +152,21 @@ __device__ __forceinline__ int warp_sum(int v) {
   return v;
 }
 
-// kmax: the largest cost. Dynamic shared memory: kmax + 1 bucket starts, then
-// the (query) lengths, the first queue positions and (varlen) the key lengths
-// of the first min(batch, kQueueLenCache) sequences.
+// kmax: the largest cost. Dynamic shared memory: kmax + 1 bucket starts, then,
+// for the first C = min(batch, kQueueLenCache) sequences, the (query) lengths,
+// the first queue positions, the first rows and the tile bases, and (varlen)
+// the key lengths and first key rows: the record passes then read no global
+// memory per sequence (a dependent global load per sequence and warp had
+// dominated the kernel).
 __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParams p, int kmax) {
   extern __shared__ int s_start[];  // [kmax + 1]: tiles (per head) of higher cost than bucket k
+  const int n_cached = min(p.batch, kQueueLenCache);
   int* s_len = s_start + kmax + 1;
-  int* s_first = s_len + kQueueLenCache;  // first tile position of sequence b (one-cost modes)
-  int* s_lenk = s_first + min(p.batch, kQueueLenCache);  // varlen: key lengths
+  int* s_first = s_len + n_cached;  // first tile position of sequence b (one-cost modes)
+  int* s_off = s_first + n_cached;  // first (query) row of sequence b
+  int* s_tb = s_off + n_cached;     // tile base of sequence b
+  int* s_lenk = s_tb + n_cached;    // varlen: key lengths
+  int* s_koff = s_lenk + n_cached;  // varlen: first key row
   const bool var = queue_var(p.mode);
   __shared__ int warp_buf[32];
   __shared__ int s_bad;
@@ -179,7 +187,10 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
       if (b == 0 && lo != 0) bad = true;
       if (b == p.batch - 1 && hi != p.total) bad = true;
       if (bad) s_bad = 1;
-      if (b < kQueueLenCache) s_len[b] = L;
+      if (b < kQueueLenCache) {
+        s_len[b] = L;
+        s_off[b] = lo;
+      }
       if (var) {  // the key offsets obey the same rules
         const int klo = p.k_offsets[b], khi = p.k_offsets[b + 1];
         const int Lk = khi - klo;
@@ -187,13 +198,17 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
         if (b == 0 && klo != 0) kbad = true;
         if (b == p.batch - 1 && khi != p.total_k) kbad = true;
         if (kbad) s_bad = 1;
-        if (b < kQueueLenCache) s_lenk[b] = Lk;
+        if (b < kQueueLenCache) {
+          s_lenk[b] = Lk;
+          s_koff[b] = klo;
+        }
       }
       nt = bad ? 0 : ceil_tiles(L);
     }
     int tot;
     const int pre = block_exclusive_scan(nt, warp_buf, &tot);
     if (b < p.batch && p.tile_base) p.tile_base[b] = carry + pre;
+    if (b < p.batch && b < kQueueLenCache) s_tb[b] = carry + pre;
     carry += tot;
   }
   if (tid == 0 && p.tile_base) p.tile_base[p.batch] = carry;
@@ -246,10 +261,14 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
   const bool one_cost = !p.causal;  // the broadcast modes are never causal
   // The items fit the queue (checked once here; every write below is in range).
   const bool fits = static_cast<int64_t>(total_tiles) * p.heads <= p.max_items;
+  // a sequence's first row, first key row and tile base, from shared memory when cached
+  auto row0 = [&](int b) { return b < kQueueLenCache ? s_off[b] : p.offsets[b]; };
+  auto krow0 = [&](int b) { return b < kQueueLenCache ? s_koff[b] : p.k_offsets[b]; };
+  auto tbase = [&](int b) { return p.tile_base ? (b < kQueueLenCache ? s_tb[b] : p.tile_base[b]) : 0; };
   auto write_items = [&](int b, int first, int c, int tf, int k, int2 L) {
     if (!fits) return;
-    const int tb = p.tile_base ? p.tile_base[b] : 0;
-    const int4 seq = var ? make_int4(p.offsets[b], L.x, p.k_offsets[b], L.y) : make_int4(p.offsets[b], L.x, tb, 0);
+    const int tb = tbase(b);
+    const int4 seq = var ? make_int4(row0(b), L.x, krow0(b), L.y) : make_int4(row0(b), L.x, tb, 0);
     const int w = p.mode == kQueueVarBwd ? tb : k;  // the varlen backward carries the query tile base
     int4* it = p.items + static_cast<int64_t>(first) * p.heads;
     int4* sq = p.item_seq ? p.item_seq + static_cast<int64_t>(first) * p.heads : nullptr;
@@ -293,8 +312,8 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
       const int nt = item_tiles(p, L.x, L.y);
       const int k = nt > 0 ? item_cost(p, L.x, L.y, 0) : 0;
       if (!(fits && nt > 0 && k >= kmin)) continue;
-      const int tb = p.tile_base ? p.tile_base[b] : 0;
-      const int4 seq = var ? make_int4(p.offsets[b], L.x, p.k_offsets[b], L.y) : make_int4(p.offsets[b], L.x, tb, 0);
+      const int tb = tbase(b);
+      const int4 seq = var ? make_int4(row0(b), L.x, krow0(b), L.y) : make_int4(row0(b), L.x, tb, 0);
       const int w = p.mode == kQueueVarBwd ? tb : k;
       const int64_t first = static_cast<int64_t>(s_first[b]) * p.heads;
       const int n = nt * p.heads;  // records tile-major, heads inner: record e = (tile e / H, head e % H)
@@ -329,11 +348,11 @@ cudaError_t launch_queue(const QueueParams& p, cudaStream_t stream) {
   if (p.mode == kQueueVarBwd) kmax = static_cast<int64_t>(p.group) * tiles(p.max_seqlen);
   if (kmax > kQueueMaxCost) return cudaErrorInvalidValue;
   const int64_t cached = std::min(p.batch, kQueueLenCache);
-  const size_t smem = static_cast<size_t>(kmax + 1 + kQueueLenCache + cached * (queue_var(p.mode) ? 2 : 1)) * sizeof(int);
+  const size_t smem = static_cast<size_t>(kmax + 1 + cached * (queue_var(p.mode) ? 6 : 4)) * sizeof(int);
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t e = once_per_device(attr_done, [] {
     return cudaFuncSetAttribute(build_queue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>((kQueueMaxCost + 1 + 3 * kQueueLenCache) * sizeof(int)));
+                                static_cast<int>((kQueueMaxCost + 1 + 6 * kQueueLenCache) * sizeof(int)));
   });
   if (e != cudaSuccess) return e;
   build_queue_kernel<<<1, kQThreads, smem, stream>>>(p, static_cast<int>(kmax));
