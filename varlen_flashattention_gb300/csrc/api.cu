@@ -134,8 +134,8 @@ bool events_ok(void* events) {
 // ------------------------------------------------------------------ workspace layouts
 
 struct Layout {
-  size_t status = 0, tile_base = 0, items = 0, item_seq = 0, lse2p = 0, deltap = 0, dq_acc = 0, part_o = 0,
-         part_lse = 0;
+  size_t status = 0, tile_base = 0, items = 0, item_seq = 0, tile_seq = 0, lse2p = 0, deltap = 0, dq_acc = 0,
+         part_o = 0, part_lse = 0;
   size_t bytes = 0;
   int64_t max_items = 0, pad_tiles = 0;
 };
@@ -152,6 +152,8 @@ Layout self_layout(int64_t batch, int64_t heads, int64_t total, int64_t head_dim
   L.item_seq = off;
   off = align_up(off + 16 * L.max_items, 256);
   if (bwd) {
+    L.tile_seq = off;
+    off = align_up(off + 4 * L.pad_tiles, 256);
     L.lse2p = off;
     off = align_up(off + 4 * heads * L.pad_tiles * kTile, 256);
     L.deltap = off;
@@ -203,6 +205,8 @@ Layout var_layout(int64_t batch, int64_t q_heads, int64_t kv_heads, int64_t tota
   L.item_seq = off;
   off = align_up(off + 16 * L.max_items, 256);
   if (bwd) {
+    L.tile_seq = off;
+    off = align_up(off + 4 * L.pad_tiles, 256);
     L.lse2p = off;
     off = align_up(off + 4 * q_heads * L.pad_tiles * kTile, 256);
     L.deltap = off;
@@ -345,6 +349,28 @@ cudaError_t run_bwd_main(BwdLaunch bl, int chunk, int sms, int64_t max_items, co
 }
 
 }  // namespace
+
+// Scalar and pointer checks of the one-token paged decode (shared with the
+// allocation-free entry point, which runs them before its scratch-size check).
+jfa_status check_decode_args(const jfa_decode_args* a) {
+  if (!a) return JFA_ERR_INVALID_ARG;
+  if (a->batch < 0 || a->q_heads < 1 || a->kv_heads < 1 || a->page_size < 1 || a->num_pages < 0 ||
+      a->max_pages < 0 || a->num_splits < 1 || a->num_splits > 128)
+    return JFA_ERR_INVALID_ARG;
+  if (a->q_heads % a->kv_heads != 0) return JFA_ERR_INVALID_ARG;
+  const int g = a->q_heads / a->kv_heads;
+  if (a->head_dim != 128 || !(g == 1 || g == 2 || g == 4 || g == 8 || g == 16)) return JFA_ERR_UNSUPPORTED;
+  if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return JFA_ERR_INVALID_ARG;
+  if (a->batch > 0) {
+    if (!aligned(a->q, 16) || !aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->o, 16) ||
+        !aligned(a->lse, 4) || !aligned(a->page_table, 4) || !aligned(a->seqlens_k, 4))
+      return JFA_ERR_INVALID_ARG;
+    if (a->split_bounds_out && !aligned(a->split_bounds_out, 4)) return JFA_ERR_INVALID_ARG;
+  }
+  if (static_cast<int64_t>(a->max_pages) * a->page_size >= (int64_t(1) << 31)) return JFA_ERR_INVALID_ARG;
+  return JFA_OK;
+}
+
 }  // namespace jfa
 
 using namespace jfa;
@@ -456,7 +482,8 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   const int sms = sm_count();
   if (sms <= 0) return JFA_ERR_CUDA;
   const int64_t n_acc = static_cast<int64_t>(a->total) * a->heads * a->head_dim;
-  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);  // zeroed by the pre-pass
+  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
+  if (cudaMemsetAsync(dq_acc, 0, 4 * n_acc, stream) != cudaSuccess) return JFA_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo;
   const uint64_t cols = static_cast<uint64_t>(a->heads) * a->head_dim;
   if (!make_tmap_bf16(&tq, a->q, a->total, cols) || !make_tmap_bf16(&tk, a->k, a->total, cols) ||
@@ -475,14 +502,15 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
   qp.items = reinterpret_cast<int4*>(w + L.items);
   qp.item_seq = reinterpret_cast<int4*>(w + L.item_seq);
+  qp.tile_seq = reinterpret_cast<int32_t*>(w + L.tile_seq);
   qp.max_items = static_cast<int32_t>(L.max_items);
   qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
   float* lse2p = reinterpret_cast<float*>(w + L.lse2p);
   float* deltap = reinterpret_cast<float*>(w + L.deltap);
-  if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->offsets, qp.tile_base, status, a->batch, a->heads,
-                     a->total, 0, 0, static_cast<int>(L.pad_tiles), static_cast<int>(L.pad_tiles), lse2p, deltap,
-                     dq_acc, stream) != cudaSuccess)
+  if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->offsets, qp.tile_base, qp.tile_seq, status, a->batch,
+                     a->heads, a->total, 0, 0, static_cast<int>(L.pad_tiles), static_cast<int>(L.pad_tiles), lse2p,
+                     deltap, stream) != cudaSuccess)
     return JFA_ERR_CUDA;
   BwdLaunch bl{};
   bl.head_dim = a->head_dim;
@@ -590,12 +618,11 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
   if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
   if (a->q_len == 0) return JFA_OK;
   const int64_t n_acc = static_cast<int64_t>(a->q_len) * a->heads * a->head_dim;
-  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);  // zeroed by the pre-pass when there are keys
+  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
   const int sms = sm_count();
   if (sms <= 0) return JFA_ERR_CUDA;
-  if (!(a->batch > 0 && a->total_k > 0)) {
-    if (cudaMemsetAsync(dq_acc, 0, 4 * n_acc, stream) != cudaSuccess) return JFA_ERR_CUDA;
-  } else {
+  if (cudaMemsetAsync(dq_acc, 0, 4 * n_acc, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (a->batch > 0 && a->total_k > 0) {
     CUtensorMap tq, tk, tv, tdo;
     const uint64_t cols = static_cast<uint64_t>(a->heads) * a->head_dim;
     if (!make_tmap_bf16(&tq, a->q, a->q_len, cols) || !make_tmap_bf16(&tk, a->k, a->total_k, cols) ||
@@ -620,8 +647,8 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
     if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
     float* lse2p = reinterpret_cast<float*>(w + L.lse2p);
     float* deltap = reinterpret_cast<float*>(w + L.deltap);
-    if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->kv_offsets, nullptr, status, a->batch, a->heads,
-                       a->total_k, 1, a->q_len, 0, static_cast<int>(L.pad_tiles), lse2p, deltap, dq_acc,
+    if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->kv_offsets, nullptr, nullptr, status, a->batch,
+                       a->heads, a->total_k, 1, a->q_len, 0, static_cast<int>(L.pad_tiles), lse2p, deltap,
                        stream) != cudaSuccess)
       return JFA_ERR_CUDA;
     BwdLaunch bl{};
@@ -659,21 +686,8 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
 }
 
 jfa_status jfa_decode_splitkv(const jfa_decode_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  if (!a) return JFA_ERR_INVALID_ARG;
-  if (a->batch < 0 || a->q_heads < 1 || a->kv_heads < 1 || a->page_size < 1 || a->num_pages < 0 ||
-      a->max_pages < 0 || a->num_splits < 1 || a->num_splits > 128)
-    return JFA_ERR_INVALID_ARG;
-  if (a->q_heads % a->kv_heads != 0) return JFA_ERR_INVALID_ARG;
-  const int g = a->q_heads / a->kv_heads;
-  if (a->head_dim != 128 || !(g == 1 || g == 2 || g == 4 || g == 8 || g == 16)) return JFA_ERR_UNSUPPORTED;
-  if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return JFA_ERR_INVALID_ARG;
-  if (a->batch > 0) {
-    if (!aligned(a->q, 16) || !aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->o, 16) ||
-        !aligned(a->lse, 4) || !aligned(a->page_table, 4) || !aligned(a->seqlens_k, 4))
-      return JFA_ERR_INVALID_ARG;
-    if (a->split_bounds_out && !aligned(a->split_bounds_out, 4)) return JFA_ERR_INVALID_ARG;
-  }
-  if (static_cast<int64_t>(a->max_pages) * a->page_size >= (int64_t(1) << 31)) return JFA_ERR_INVALID_ARG;
+  const jfa_status st = check_decode_args(a);
+  if (st != JFA_OK) return st;
   const Layout L = decode_layout(a->batch, a->q_heads, a->num_splits);
   if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
@@ -790,7 +804,8 @@ jfa_status jfa_bwd_varlen(const jfa_varlen_bwd_args* a, void* ws, size_t ws_byte
   const int sms = sm_count();
   if (sms <= 0) return JFA_ERR_CUDA;
   const int64_t n_acc = static_cast<int64_t>(a->total_q) * a->q_heads * a->head_dim;
-  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);  // zeroed by the pre-pass
+  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
+  if (cudaMemsetAsync(dq_acc, 0, 4 * n_acc, stream) != cudaSuccess) return JFA_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo;
   const uint64_t qcols = static_cast<uint64_t>(a->q_heads) * a->head_dim;
   const uint64_t kcols = static_cast<uint64_t>(a->kv_heads) * a->head_dim;
@@ -813,14 +828,15 @@ jfa_status jfa_bwd_varlen(const jfa_varlen_bwd_args* a, void* ws, size_t ws_byte
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
   qp.items = reinterpret_cast<int4*>(w + L.items);
   qp.item_seq = reinterpret_cast<int4*>(w + L.item_seq);
+  qp.tile_seq = reinterpret_cast<int32_t*>(w + L.tile_seq);
   qp.max_items = static_cast<int32_t>(L.max_items);
   qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
   float* lse2p = reinterpret_cast<float*>(w + L.lse2p);
   float* deltap = reinterpret_cast<float*>(w + L.deltap);
-  if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->q_offsets, qp.tile_base, status, a->batch, a->q_heads,
-                     a->total_q, 0, 0, static_cast<int>(L.pad_tiles), static_cast<int>(L.pad_tiles), lse2p, deltap,
-                     dq_acc, stream) != cudaSuccess)
+  if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->q_offsets, qp.tile_base, qp.tile_seq, status, a->batch,
+                     a->q_heads, a->total_q, 0, 0, static_cast<int>(L.pad_tiles), static_cast<int>(L.pad_tiles), lse2p,
+                     deltap, stream) != cudaSuccess)
     return JFA_ERR_CUDA;
   BwdLaunch bl{};
   bl.head_dim = a->head_dim;
