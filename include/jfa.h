@@ -369,10 +369,22 @@ JFA_API jfa_status jfa_fwd_fp8(const jfa_fwd_fp8_args* args, void* workspace, si
  *  - calls no cudaMalloc / cudaFree and no allocating library routine;
  *  - every call shares the scratch: calls whose work overlaps on the GPU race,
  *    so serialise them (one stream, or explicit ordering);
+ *  - the scratch address is looked up once per CUDA context (a context
+ *    recreated after cudaDeviceReset, or a second context on the device, gets
+ *    its own lookup);
+ *  - arguments are checked as in jfa_decode_splitkv before the size limit, so
+ *    a malformed request returns JFA_ERR_INVALID_ARG / JFA_ERR_UNSUPPORTED;
  *  - device-detected input errors (a page entry out of range) are handled in
- *    the kernel as in jfa_decode_splitkv, but this entry point cannot return
- *    them: the status word lives in the internal scratch. */
+ *    the kernel as in jfa_decode_splitkv and recorded in the status word of
+ *    the internal scratch: read them with jfa_decode_noalloc_status. */
 JFA_API jfa_status jfa_decode_splitkv_noalloc(const jfa_decode_args* args, cudaStream_t stream);
+
+/* Device status of the last jfa_decode_splitkv_noalloc call on the current
+ * context, as jfa_read_device_status returns it for a workspace: synchronises
+ * `stream`, then returns JFA_OK, JFA_ERR_TIMEOUT or JFA_ERR_BAD_INPUT (with a
+ * check code in *detail, optional), or JFA_ERR_CUDA. Allocates nothing. No
+ * counterpart on the pages either. */
+JFA_API jfa_status jfa_decode_noalloc_status(cudaStream_t stream, int32_t* detail);
 
 /* Failure-detection self-test ([B300] bug hunting: a producer/consumer
  * pipeline that deadlocked). Every pipeline wait in this library is bounded in

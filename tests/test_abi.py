@@ -142,6 +142,27 @@ def test_decode_validation(lib):
     assert lib.jfa_decode_splitkv(P(args()), FAKE, need - 1, None) == _abi.JFA_ERR_WORKSPACE_TOO_SMALL
 
 
+def test_decode_noalloc_validation_precedes_the_size_limit(lib):
+    """A malformed request to the allocation-free decode is refused as such,
+    not as one too large for its scratch (the checks run before the limit)."""
+    P = ctypes.byref
+
+    def args(**kw):
+        a = _abi.DecodeArgs(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 32, 8, 128, 16, 100, 10, 8, 0.1, FAKE, FAKE, None, None)
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+    assert lib.jfa_decode_splitkv_noalloc(None, None) == _abi.JFA_ERR_INVALID_ARG
+    # num_splits 129 with a batch that would also overflow the 32768-row scratch
+    for bad in (dict(batch=-1), dict(num_splits=129), dict(num_splits=129, batch=64), dict(num_splits=0),
+                dict(page_size=0), dict(q=FAKE + 8)):
+        assert lib.jfa_decode_splitkv_noalloc(P(args(**bad)), None) == _abi.JFA_ERR_INVALID_ARG, bad
+    assert lib.jfa_decode_splitkv_noalloc(P(args(head_dim=64)), None) == _abi.JFA_ERR_UNSUPPORTED
+    # a well-formed request above the limit: 32 splits x 64 sequences x 32 heads = 65536 rows
+    assert lib.jfa_decode_splitkv_noalloc(P(args(batch=64, num_splits=32)), None) == \
+        _abi.JFA_ERR_WORKSPACE_TOO_SMALL
+
+
 def test_varlen_validation(lib):
     P = ctypes.byref
 

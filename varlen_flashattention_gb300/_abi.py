@@ -120,6 +120,7 @@ SIGNATURES = [
     ("jfa_decode_smallq", [ctypes.POINTER(DecodeSmallqArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_fwd_fp8", [ctypes.POINTER(FwdFp8Args), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_decode_splitkv_noalloc", [ctypes.POINTER(DecodeArgs), c_void_p], c_i32),
+    ("jfa_decode_noalloc_status", [c_void_p, ctypes.POINTER(c_i32)], c_i32),
     ("jfa_read_device_status", [c_void_p, c_void_p, ctypes.POINTER(c_i32)], c_i32),
     ("jfa_selftest_wait_timeout", [c_i32, c_void_p, c_void_p], c_i32),
     ("jfa_status_string", [c_i32], ctypes.c_char_p),

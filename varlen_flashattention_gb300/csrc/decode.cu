@@ -393,7 +393,6 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const float* __restri
   const int row = blockIdx.x * 4 + warp;  // (b, h)
   if (row >= B * Hq) return;
   constexpr float kLog2e = 1.4426950408889634f;
-  constexpr float kLn2 = 0.6931471805599453f;
   const int64_t stride = static_cast<int64_t>(B) * Hq;
   float M = -INFINITY;
   for (int s = lane; s < S; s += 32) M = fmaxf(M, part_lse[s * stride + row]);
@@ -422,7 +421,6 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const float* __restri
   packed.y = *reinterpret_cast<uint32_t*>(&c);
   *reinterpret_cast<uint2*>(o + row * kDecD + 4 * lane) = packed;
   if (lane == 0) lse[row] = Z > 0.f ? M + logf(Z) : -INFINITY;
-  (void)kLn2;
 }
 
 // ------------------------------------------------------------------ launchers

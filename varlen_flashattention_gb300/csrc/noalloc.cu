@@ -13,6 +13,7 @@
 // the library holds it until the process exits. All calls share it, so calls
 // whose work overlaps on the GPU (different streams, or different host
 // threads on the same device) race on it; serialise them.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -27,22 +28,59 @@ constexpr size_t kDecodeScratchBytes = kStatusBytes + kMaxPartialRows * 128 * 4 
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kDecodeScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_addr[kMaxDevices] = {};
+// cuCtxGetCurrent, taken from the driver through the runtime (the library
+// does not link libcuda directly).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
 
-// Device address of g_decode_scratch on the current device, looked up once
-// per device (host code cannot use the array's name as a device address).
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<CtxGetCurrentFn>(nullptr);
+    return reinterpret_cast<CtxGetCurrentFn>(f);
+  }();
+  return fn;
+}
+
+// Scratch addresses already looked up, keyed by CUDA context: the array is
+// allocated once per context that loads the library's module, so a context
+// recreated after cudaDeviceReset, or a second (non-primary) context on the
+// same device, gets its own entry.
+constexpr int kMaxContexts = 64;
+std::mutex g_mu;
+CUcontext g_ctx[kMaxContexts] = {};
+void* g_addr[kMaxContexts] = {};
+int g_used = 0;
+
+// Device address of g_decode_scratch in the current context (host code cannot
+// use the array's name as a device address).
 jfa_status scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return JFA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_addr[dev] == nullptr) {
+  CtxGetCurrentFn get = ctx_get_current();
+  CUcontext ctx = nullptr;
+  if (get == nullptr || get(&ctx) != CUDA_SUCCESS) return JFA_ERR_CUDA;
+  if (ctx == nullptr) {
+    // no context is current yet: the runtime call makes the current device's
+    // primary context current
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return JFA_ERR_CUDA;
-    g_addr[dev] = p;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return JFA_ERR_CUDA;
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return JFA_ERR_CUDA;
   }
-  *out = g_addr[dev];
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (int i = 0; i < g_used; ++i)
+    if (g_ctx[i] == ctx) {
+      *out = g_addr[i];
+      return JFA_OK;
+    }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return JFA_ERR_CUDA;
+  if (g_used < kMaxContexts) {
+    g_ctx[g_used] = ctx;
+    g_addr[g_used] = p;
+    ++g_used;
+  }
+  *out = p;
   return JFA_OK;
 }
 
@@ -50,7 +88,10 @@ jfa_status scratch_address(void** out) {
 }  // namespace jfa
 
 extern "C" jfa_status jfa_decode_splitkv_noalloc(const jfa_decode_args* args, cudaStream_t stream) {
-  if (!args) return JFA_ERR_INVALID_ARG;
+  // the ordinary argument checks first, so that a bad request reads as such
+  // and not as one that is too large
+  const jfa_status chk = jfa::check_decode_args(args);
+  if (chk != JFA_OK) return chk;
   if (jfa_decode_workspace_size(args) > jfa::kDecodeScratchBytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   const jfa_status st = jfa::scratch_address(&scratch);
@@ -58,4 +99,11 @@ extern "C" jfa_status jfa_decode_splitkv_noalloc(const jfa_decode_args* args, cu
   // the decode clears the status block at the start of the call; every
   // partial row it reads is written by the same call first
   return jfa_decode_splitkv(args, scratch, jfa::kDecodeScratchBytes, stream);
+}
+
+extern "C" jfa_status jfa_decode_noalloc_status(cudaStream_t stream, int32_t* detail) {
+  void* scratch = nullptr;
+  const jfa_status st = jfa::scratch_address(&scratch);
+  if (st != JFA_OK) return st;
+  return jfa_read_device_status(scratch, stream, detail);
 }
