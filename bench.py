@@ -77,6 +77,37 @@ def attn_flops(lengths, heads, d, causal, kind):
     return (4 if kind == "fwd" else 10) * d * heads * pair_count(lengths, causal)
 
 
+def attn_bytes(lengths, heads, d, kind):
+    """Algorithmic HBM bytes of jagged self-attention: the forward reads Q, K, V
+    and writes O (8 L d bytes per sequence and head, bf16); the backward reads
+    Q, K, V, O, dO and writes dQ, dK, dV (16 L d). LSE and delta are left out."""
+    per = {"fwd": 8, "bwd": 16, "fwd_bwd": 24}[kind]
+    return per * d * heads * sum(int(L) for L in lengths)
+
+
+def choose_tc_peak(peaks, clocks):
+    """The bf16 tensor peak a kernel is held to: the burst figure (a cuBLAS GEMM
+    timed alone) unless the run's own clock record shows the sustained regime
+    (power-cap samples, or a median SM clock more than 3% below the maximum).
+    Returns (peak TFLOP/s, which, why)."""
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    sm, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    reasons = clocks.get("reasons", [])
+    if "sw_power_cap" in reasons:
+        return sustained, "bf16_tflops_sustained", "power-cap samples in the timed region"
+    if sm is not None and mx and sm < 0.97 * mx:
+        return sustained, "bf16_tflops_sustained", f"median SM clock {sm:.0f} of {mx:.0f} MHz"
+    if sm is None:
+        return burst, "bf16_tflops", "no clock record; burst figure"
+    return burst, "bf16_tflops", f"median SM clock {sm:.0f} of {mx:.0f} MHz, no power cap: burst regime"
+
+
+def attainable(flops, nbytes, tc_peak_tflops, hbm_gbs):
+    """min(tensor peak, arithmetic intensity x HBM bandwidth) in TFLOP/s."""
+    return min(tc_peak_tflops, flops / nbytes * hbm_gbs / 1e3)
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
 
@@ -139,6 +170,9 @@ def dist_setup(n_gpus):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if n_gpus != world:
+        raise SystemExit(f"--gpus {n_gpus} but {world} rank(s) were launched: run N > 1 under torchrun "
+                         f"(--nproc-per-node N), one rank per GPU")
     pg = None
     if world > 1:
         import torch.distributed as dist
@@ -232,10 +266,11 @@ def time_events(fn, iters, warmup):
     return s.elapsed_time(e) / iters
 
 
-def measure_decode(jfa, device, peaks, page_size=16, splits=(8, 16, 32, 64), iters=20, q_len=1):
+def measure_decode(jfa, device, peaks, page_size=16, splits=(1, 2, 4, 8, 16, 32, 64), iters=20, q_len=1):
     """Split-KV paged GQA decode: batch 32, 32/8 heads, d 128, KV lengths in
     [1024, 32768], random page permutation; q_len > 1 runs the small-query
-    decode (q_len new tokens per sequence). Returns the best split count."""
+    decode (q_len new tokens per sequence). Times every split count given and
+    returns the best one, with the whole curve under "curve"."""
     import torch
     from varlen_flashattention_gb300 import inputs
     g = torch.Generator().manual_seed(0)
@@ -258,10 +293,10 @@ def measure_decode(jfa, device, peaks, page_size=16, splits=(8, 16, 32, 64), ite
     nbytes = int(sl.sum()) * 2 * 8 * 128 * 2 + q.numel() * 2 * 2 + lse.numel() * 4 + sum(pages) * 4
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # 256 MB > L2, cleared between runs
     best = None
+    curve = []
+    from varlen_flashattention_gb300 import _abi
+    import ctypes
     for S in splits:
-        ws = torch.empty(1, dtype=torch.uint8, device=device)
-        from varlen_flashattention_gb300 import _abi
-        import ctypes
         if q_len == 1:
             da = _abi.DecodeArgs(None, None, None, None, None, 32, 32, 8, 128, page_size, n, pt.shape[1], S, 0.1,
                                  None, None, None, None)
@@ -293,16 +328,17 @@ def measure_decode(jfa, device, peaks, page_size=16, splits=(8, 16, 32, 64), ite
         kern_ms = statistics.median(t[1] for t in times)
         r = {"splits": S, "call_us": call_ms * 1e3, "split_kernel_us": kern_ms * 1e3,
              "tb_s": nbytes / (call_ms * 1e-3) / 1e12}
+        curve.append({"splits": S, "call_us": round(r["call_us"], 2), "tb_s": round(r["tb_s"], 3)})
         if best is None or r["tb_s"] > best["tb_s"]:
-            best = r
+            best = dict(r)
     best["frac_of_measured_hbm"] = best["tb_s"] * 1e3 / peaks["hbm_gbs"]
     best.update({"workload": f"paged GQA decode: batch 32, {q_len} query token(s) each, Hq 32 / Hkv 8, d 128, "
                              f"L_k U[1024,32768], page {page_size}",
-                 "algorithmic_bytes": nbytes, "l2": "256 MB buffer written between runs"})
+                 "algorithmic_bytes": nbytes, "l2": "256 MB buffer written between runs", "curve": curve})
     return best
 
 
-def measure_extra(jfa, device, peaks):
+def measure_extra(jfa, device, peaks, tc_peak):
     """Broadcast-Q and dense causal workloads (one timed call each)."""
     import torch
     from varlen_flashattention_gb300 import inputs
@@ -404,7 +440,9 @@ def measure_extra(jfa, device, peaks):
         bufs = alloc_bufs(jfa, w, device)
         t = time_events(lambda: run_step(jfa, w, bufs), 10, 3)
         fl = attn_flops(w["lengths"], 4, 128, False, "fwd") + attn_flops(w["lengths"], 4, 128, False, "bwd")
-        out[f"gem_sparsity_{sp}"] = {"fwd_bwd_tflops": fl / (t * 1e-3) / 1e12, "ms_per_step": t}
+        att = attainable(fl, attn_bytes(w["lengths"], 4, 128, "fwd_bwd"), tc_peak, peaks["hbm_gbs"])
+        out[f"gem_sparsity_{sp}"] = {"fwd_bwd_tflops": fl / (t * 1e-3) / 1e12, "ms_per_step": t,
+                                     "attainable_tflops": att, "frac_of_attainable": fl / (t * 1e-3) / 1e12 / att}
         del w, bufs
     torch.cuda.empty_cache()
     return out
@@ -544,13 +582,16 @@ def main():
     k_f = statistics.mean(a.elapsed_time(b) for a, b in evs_f)
     k_b = statistics.mean(a.elapsed_time(b) for a, b in evs_b)
 
-    # dominant kernel and its roofline (kernel timed inside a long step -> sustained peak)
+    # dominant kernel and its roofline: the peak follows the run's own clock record
+    # (burst unless it shows power capping or lowered clocks)
+    clk = clocks.summary()
+    tc_peak, peak_key, peak_why = choose_tc_peak(peaks, clk)
     if k_b >= k_f:
         dom, dom_ms, dom_flops = "jfa bwd main kernel (bwd_kernel<128,128>)", k_b, flops_b
     else:
         dom, dom_ms, dom_flops = "jfa fwd main kernel (fwd_stream_kernel<false>)", k_f, flops_f
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    peak = tc_peak
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
@@ -633,27 +674,33 @@ def main():
     e2e_value = total_flops / (e2e_ms * 1e-3) / 1e12
     del host_in, host_out, sets
 
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    step_att = attainable(flops_step, attn_bytes(w["lengths"], w["heads"], w["head_dim"], "fwd_bwd"), tc_peak, hbm)
     detail = {"fwd_ms": k_f, "bwd_ms": k_b, "fwd_tflops": flops_f / (k_f * 1e-3) / 1e12,
               "bwd_tflops": flops_b / (k_b * 1e-3) / 1e12, "flops_per_step": flops_step,
-              "tokens_per_rank": w["total"]}
+              "tokens_per_rank": w["total"],
+              "tc_peak": {"tflops": tc_peak, "which": f"{peak_kind} {peak_key}", "why": peak_why},
+              "step_frac_of_measured_tc": value / world / tc_peak,
+              "step_attainable_tflops": step_att, "step_frac_of_attainable": value / world / step_att}
+    detail["fwd_frac_of_measured_tc"] = detail["fwd_tflops"] / tc_peak
+    detail["bwd_frac_of_measured_tc"] = detail["bwd_tflops"] / tc_peak
     decode = None
     if not args.no_extra and rank == 0:
         del w, bufs
         torch.cuda.empty_cache()
         try:
             decode = measure_decode(jfa, device, peaks)
-            detail["decode_smallq_q4"] = measure_decode(jfa, device, peaks, splits=(16, 32), q_len=4)
+            detail["decode_smallq_q4"] = measure_decode(jfa, device, peaks, splits=(4, 8, 16, 32, 64), q_len=4)
             for P in (1, 128):  # the other page sizes of the decode workload
-                detail[f"decode_page{P}"] = measure_decode(jfa, device, peaks, page_size=P, splits=(16, 32))
-            detail.update(measure_extra(jfa, device, peaks))
-            # every row against the measured peaks: attention against the sustained bf16 rate
-            # (each kernel runs inside a longer job), decode against the copy rate
-            tc = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+                detail[f"decode_page{P}"] = measure_decode(jfa, device, peaks, page_size=P)
+            detail.update(measure_extra(jfa, device, peaks, tc_peak))
+            # every attention row against the bf16 tensor peak chosen above (an FP8
+            # contraction against the measured bf16 rate x the nominal 2x); decode
+            # rows carry their fraction of the copy rate
             for name, row in detail.items():
-                if not isinstance(row, dict):
+                if not isinstance(row, dict) or name == "tc_peak":
                     continue
-                # an FP8 contraction against the fp8 rate: the measured bf16 rate x the nominal 2x
-                peak_row = tc * 2 if name.startswith("fp8") else tc
+                peak_row = tc_peak * 2 if name.startswith("fp8") else tc_peak
                 for key in ("fwd_tflops", "bwd_tflops", "fwd_bwd_tflops"):
                     if row.get(key) is not None:
                         row[key.replace("tflops", "frac_of_measured_tc")] = row[key] / peak_row
@@ -682,14 +729,14 @@ def main():
                        "l2": "inputs larger than L2 (4 x 0.54 GB bf16 per step)"},
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{peak_kind} bf16_tflops_sustained (kernel timed inside a long step)"},
+                         "peak_source": f"{peak_kind} {peak_key}: {peak_why}"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms,
                     "how": "public API; pinned host inputs copied in and all outputs copied out every step; "
                            "copies of neighbouring steps overlap compute (3 streams, 2 buffer sets)"},
             "gpu_launches": 6 * args.steps,
-            "clocks": clocks.summary(),
+            "clocks": clk,
             "decode": decode,
             "detail": detail,
         }

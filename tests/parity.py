@@ -78,3 +78,26 @@ def to_cuda(d: dict, keys) -> dict:
     for k in keys:
         out[k] = d[k].cuda()
     return out
+
+
+def fp8_error_bound(q, k, v, offsets, scale, causal, O_ref):
+    """Per-element bound on |O_gpu - O_ref| for the FP8 (e4m3) forward, from the
+    dequantized fp64 inputs q, k, v ([total, H, d]):
+      2^-4 sum_j P_ij |V_jd| + 2^-10 sum_j |V_jd| / l_true_i + 2^-8 |O_ref| + 1e-3.
+    P is rounded to e4m3 before P V (2^-4 relative at or above 2^-6, 2^-10
+    absolute below), the kernel's row sum is never below the true one, O is
+    returned in bf16 (2^-8) and the fp32 arithmetic adds 1e-3."""
+    import oracle.attention as orc
+    PabsV, _ = orc.attention_forward(q, k, np.abs(v), offsets, scale, causal)  # sum_j P_ij |V_jd|
+    sub = np.zeros_like(O_ref)  # sum_j |V_jd| / l_true_i over the keys row i sees
+    for s0, s1 in orc.seq_ranges(offsets):
+        if s1 == s0:
+            continue
+        for h in range(q.shape[1]):
+            S = scale * (q[s0:s1, h] @ k[s0:s1, h].T)
+            vis = np.tril(np.ones(S.shape, dtype=bool)) if causal else np.ones(S.shape, dtype=bool)
+            S = np.where(vis, S, -np.inf)
+            mx = S.max(axis=1)
+            l_true = np.exp(S - mx[:, None]).sum(axis=1)
+            sub[s0:s1, h] = (vis.astype(np.float64) @ np.abs(v[s0:s1, h])) / l_true[:, None]
+    return 2.0 ** -4 * PabsV + 2.0 ** -10 * sub + 2.0 ** -8 * np.abs(O_ref) + 1e-3

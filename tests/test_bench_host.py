@@ -73,3 +73,37 @@ def test_clock_summary_flags_throttle_reasons():
     assert out["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
     empty = bench.ClockSampler(0)
     assert empty.summary()["reasons"] == ["unsampled"]
+
+
+def test_tc_peak_follows_the_clock_record():
+    peaks = {"bf16_tflops": 1971.6, "bf16_tflops_sustained": 1718.0, "hbm_gbs": 6790.3}
+    burst = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 4}
+    capped = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 4}
+    low = {"sm_mhz": 1455.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 40}
+    assert bench.choose_tc_peak(peaks, burst)[:2] == (1971.6, "bf16_tflops")
+    assert bench.choose_tc_peak(peaks, capped)[:2] == (1718.0, "bf16_tflops_sustained")
+    assert bench.choose_tc_peak(peaks, low)[:2] == (1718.0, "bf16_tflops_sustained")
+    # the headline kernel of the first bench line, recomputed: 864.1 TFLOP/s at burst clocks
+    peak, _, _ = bench.choose_tc_peak(peaks, burst)
+    assert abs(864.118 / peak - 0.438) < 1e-3
+
+
+def test_attainable_roofline_of_the_sparse_gem_step():
+    # GEM-like s=0.9 (105,061 tokens, 4 heads, d 128): 24 L d bytes per sequence and head
+    lengths = [105061]
+    nbytes = bench.attn_bytes(lengths, 4, 128, "fwd_bwd")
+    assert nbytes == 24 * 128 * 4 * 105061
+    assert bench.attn_bytes([3, 5], 2, 64, "fwd") + bench.attn_bytes([3, 5], 2, 64, "bwd") == \
+        bench.attn_bytes([3, 5], 2, 64, "fwd_bwd")
+    # HBM-bound: AI x bandwidth below the tensor peak
+    att = bench.attainable(1.0e11, nbytes, 1971.6, 6790.3)
+    assert abs(att - 1.0e11 / nbytes * 6790.3 / 1e3) < 1e-9 and att < 1971.6
+    # compute-bound: capped at the tensor peak
+    assert bench.attainable(1.0e15, 1.0e9, 1971.6, 6790.3) == 1971.6
+
+
+def test_gpus_flag_must_match_the_launched_ranks(monkeypatch):
+    import pytest
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    with pytest.raises(SystemExit):
+        bench.dist_setup(2)

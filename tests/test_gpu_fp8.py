@@ -19,7 +19,7 @@ import torch
 import oracle.attention as orc
 import varlen_flashattention_gb300 as jfa
 from varlen_flashattention_gb300 import inputs
-from tests.parity import check_lse, np64
+from tests.parity import check_lse, fp8_error_bound, np64
 
 pytestmark = pytest.mark.gpu
 
@@ -41,19 +41,7 @@ def _check(d, causal, tag):
     check_lse(lse, L_ref, f"LSE {tag}")
     # the bound's terms, from the dequantized inputs
     q, k, v = orc.e4m3_decode(q8) * qd, orc.e4m3_decode(k8) * kd, orc.e4m3_decode(v8) * vd
-    PabsV, _ = orc.attention_forward(q, k, np.abs(v), off, d["scale"], causal)  # sum_j P_ij |V_jd|
-    sub = np.zeros_like(O_ref)  # sum_j |V_jd| / l_true_i over the keys row i sees
-    for s0, s1 in orc.seq_ranges(off):
-        if s1 == s0:
-            continue
-        for h in range(q.shape[1]):
-            S = d["scale"] * (q[s0:s1, h] @ k[s0:s1, h].T)
-            vis = np.tril(np.ones(S.shape, dtype=bool)) if causal else np.ones(S.shape, dtype=bool)
-            S = np.where(vis, S, -np.inf)
-            mx = S.max(axis=1)
-            l_true = np.exp(S - mx[:, None]).sum(axis=1)
-            sub[s0:s1, h] = (vis.astype(np.float64) @ np.abs(v[s0:s1, h])) / l_true[:, None]
-    bound = 2.0 ** -4 * PabsV + 2.0 ** -10 * sub + 2.0 ** -8 * np.abs(O_ref) + 1e-3
+    bound = fp8_error_bound(q, k, v, off, d["scale"], causal, O_ref)
     err = np.abs(o - O_ref)
     worst = np.unravel_index(np.argmax(err - bound), err.shape)
     assert np.all(err <= bound), f"O {tag}: |diff| {err[worst]:.3e} > bound {bound[worst]:.3e}"
