@@ -3,8 +3,9 @@
 Element-by-element comparison on seeded inputs that span several 128-row
 tiles with ragged tails (lengths 1, 127, 128, 129, ...), empty sequences,
 causal and non-causal masks, head dims 64 / 128 / 192 (192 with the
-head-axis chunked backward), the tiny and GEM-like workloads (three sparsity
-levels), and the dense causal workload at full size on sampled (sequence,
+head-axis chunked backward), the tiny workload, the GEM-like workload at full
+size on every sequence (three sparsity levels; the oracle fans out over the
+host cores), and the dense causal workload at full size on 8 seeded (sequence,
 head) pairs. The longest-first work order is compared bit for bit.
 """
 import numpy as np
@@ -113,48 +114,36 @@ def test_gem_like_reduced_batch(sparsity):
     _check_all(d, False, tag=f"GEM s={sparsity}")
 
 
+@pytest.fixture(scope="module")
+def oracle_workers():
+    """Spawned oracle workers for the full-size checks (one core each)."""
+    from tests import oracle_pool
+    ex = oracle_pool.pool(mem_per_worker_gb=4.0)
+    yield ex
+    ex.shutdown()
+
+
 @pytest.mark.parametrize("sparsity", [0.1, 0.5, 0.9])
-def test_gem_like_full_size_sampled(sparsity):
-    """The full GEM-like workload (batch 1024) on the GPU; the oracle checks a
-    seeded sample of 12 sequences (all heads) element by element."""
+def test_gem_like_full_size(sparsity, oracle_workers):
+    """The full GEM-like workload (batch 1024, max_len 1024, H 4, d 128) on the
+    GPU, every sequence compared with the oracle element by element."""
+    from tests import oracle_pool
     d = inputs.jagged_inputs(1024, 1024, sparsity, 4, 128, seed=0)
-    o, lse, dq, dk, dv = _fwd_bwd(d, False)
-    o, lse, dq, dk, dv = (np64(t) for t in (o, lse, dq, dk, dv))
-    rng = np.random.default_rng(123)
-    off = d["offsets"].numpy()
-    for b in sorted(rng.choice(1024, 12, replace=False).tolist()):
-        s0, s1 = int(off[b]), int(off[b + 1])
-        sub = {k: d[k][s0:s1] for k in ("q", "k", "v", "do")}
-        one = np.array([0, s1 - s0])
-        O_ref, L_ref = orc.attention_forward(np64(sub["q"]), np64(sub["k"]), np64(sub["v"]), one, d["scale"])
-        dQ, dK, dV, _ = orc.attention_backward(np64(sub["q"]), np64(sub["k"]), np64(sub["v"]), np64(sub["do"]),
-                                               one, d["scale"])
-        check_o(o[s0:s1], O_ref, f"O b={b}")
-        check_lse(lse[:, s0:s1], L_ref, f"LSE b={b}")
-        check_grad(dq[s0:s1], dQ, f"dQ b={b}")
-        check_grad(dk[s0:s1], dK, f"dK b={b}")
-        check_grad(dv[s0:s1], dV, f"dV b={b}")
+    gpu = _fwd_bwd(d, False)
+    oracle_pool.check_self_full(oracle_workers, d, gpu, False, f"GEM s={sparsity} full")
 
 
 @pytest.mark.parametrize("head_dim", [128, 192])
-def test_dense_causal_full_size_sampled(head_dim):
+def test_dense_causal_full_size_sampled(head_dim, oracle_workers):
     """Batch 4 x 8192 tokens, 16 heads, causal (d=192 with the chunked backward);
-    the oracle checks two (sequence, head) pairs in full."""
+    the oracle checks 8 of the 64 (sequence, head) pairs in full, drawn from a
+    seeded generator."""
+    from tests import oracle_pool
     d = inputs.dense_causal_inputs(4, 8192, 16, head_dim, seed=0)
-    o, lse, dq, dk, dv = _fwd_bwd(d, True)
-    o, lse, dq, dk, dv = (np64(t) for t in (o, lse, dq, dk, dv))
-    L = 8192
-    for b, h in ((0, 0), (3, 11)):
-        s0, s1 = b * L, (b + 1) * L
-        q, k, v, do = (np64(d[x][s0:s1, h:h + 1]) for x in ("q", "k", "v", "do"))
-        one = np.array([0, L])
-        O_ref, L_ref = orc.attention_forward(q, k, v, one, d["scale"], True)
-        dQ, dK, dV, _ = orc.attention_backward(q, k, v, do, one, d["scale"], True)
-        check_o(o[s0:s1, h:h + 1], O_ref, f"O b={b} h={h}")
-        check_lse(lse[h:h + 1, s0:s1], L_ref, f"LSE b={b} h={h}")
-        check_grad(dq[s0:s1, h:h + 1], dQ, f"dQ b={b} h={h}")
-        check_grad(dk[s0:s1, h:h + 1], dK, f"dK b={b} h={h}")
-        check_grad(dv[s0:s1, h:h + 1], dV, f"dV b={b} h={h}")
+    gpu = _fwd_bwd(d, True)
+    rng = np.random.default_rng(1234 + head_dim)
+    pairs = [(int(x) // 16, int(x) % 16) for x in sorted(rng.choice(64, 8, replace=False))]
+    oracle_pool.check_self_pairs(oracle_workers, d, gpu, pairs, True, f"dense causal d={head_dim} {pairs}")
 
 
 def _queue_from_workspace(ws, batch):

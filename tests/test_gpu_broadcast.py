@@ -51,23 +51,17 @@ def test_broadcast_small(q_len, batch, lo, hi):
 
 
 def test_broadcast_full_size():
-    """Q [256, 4, 128] shared by 512 jagged K/V sequences (lengths in [16, 2048]).
-    Forward, dK and dV are checked on 8 sampled sequences; dQ (a sum over all
-    512) is checked against the oracle's full sum."""
+    """Q [256, 4, 128] shared by 512 jagged K/V sequences (lengths in [16, 2048]):
+    O, LSE, dK and dV of every sequence and dQ (the sum over all 512) compared
+    with the oracle, which runs in spawned workers over chunks of sequences."""
+    from tests import oracle_pool
     d = inputs.broadcast_inputs(seed=0)
-    o, lse, dq, dk, dv = _run(d)
-    off = d["kv_offsets"].numpy()
-    dQ, dK, dV = orc.broadcast_backward(np64(d["q"]), np64(d["k"]), np64(d["v"]), np64(d["do"]), off, d["scale"])
-    check_grad(np64(dq), dQ, "dQ (sum over 512 sequences)")
-    O_ref, L_ref = orc.broadcast_forward(np64(d["q"]), np64(d["k"]), np64(d["v"]), off, d["scale"])
-    o, lse, dk, dv = np64(o), np64(lse), np64(dk), np64(dv)
-    rng = np.random.default_rng(7)
-    for b in sorted(rng.choice(512, 8, replace=False).tolist()):
-        s0, s1 = int(off[b]), int(off[b + 1])
-        check_o(o[b], O_ref[b], f"O b={b}")
-        check_lse(lse[b], L_ref[b], f"LSE b={b}")
-        check_grad(dk[s0:s1], dK[s0:s1], f"dK b={b}")
-        check_grad(dv[s0:s1], dV[s0:s1], f"dV b={b}")
+    gpu = _run(d)
+    ex = oracle_pool.pool(mem_per_worker_gb=2.0)
+    try:
+        oracle_pool.check_bcast_full(ex, d, gpu, "broadcast-Q full")
+    finally:
+        ex.shutdown()
 
 
 def test_broadcast_empty_sequence():
