@@ -134,8 +134,8 @@ bool events_ok(void* events) {
 // ------------------------------------------------------------------ workspace layouts
 
 struct Layout {
-  size_t status = 0, tile_base = 0, items = 0, item_seq = 0, tile_seq = 0, lse2p = 0, deltap = 0, dq_acc = 0,
-         part_o = 0, part_lse = 0;
+  size_t status = 0, tile_base = 0, items = 0, item_seq = 0, lse2p = 0, deltap = 0, dq_acc = 0, part_o = 0,
+         part_lse = 0;
   size_t bytes = 0;
   int64_t max_items = 0, pad_tiles = 0;
 };
@@ -152,8 +152,6 @@ Layout self_layout(int64_t batch, int64_t heads, int64_t total, int64_t head_dim
   L.item_seq = off;
   off = align_up(off + 16 * L.max_items, 256);
   if (bwd) {
-    L.tile_seq = off;
-    off = align_up(off + 4 * L.pad_tiles, 256);
     L.lse2p = off;
     off = align_up(off + 4 * heads * L.pad_tiles * kTile, 256);
     L.deltap = off;
@@ -205,8 +203,6 @@ Layout var_layout(int64_t batch, int64_t q_heads, int64_t kv_heads, int64_t tota
   L.item_seq = off;
   off = align_up(off + 16 * L.max_items, 256);
   if (bwd) {
-    L.tile_seq = off;
-    off = align_up(off + 4 * L.pad_tiles, 256);
     L.lse2p = off;
     off = align_up(off + 4 * q_heads * L.pad_tiles * kTile, 256);
     L.deltap = off;
@@ -482,8 +478,7 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   const int sms = sm_count();
   if (sms <= 0) return JFA_ERR_CUDA;
   const int64_t n_acc = static_cast<int64_t>(a->total) * a->heads * a->head_dim;
-  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
-  if (cudaMemsetAsync(dq_acc, 0, 4 * n_acc, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);  // zeroed by the pre-pass
   CUtensorMap tq, tk, tv, tdo;
   const uint64_t cols = static_cast<uint64_t>(a->heads) * a->head_dim;
   if (!make_tmap_bf16(&tq, a->q, a->total, cols) || !make_tmap_bf16(&tk, a->k, a->total, cols) ||
@@ -502,15 +497,14 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
   qp.items = reinterpret_cast<int4*>(w + L.items);
   qp.item_seq = reinterpret_cast<int4*>(w + L.item_seq);
-  qp.tile_seq = reinterpret_cast<int32_t*>(w + L.tile_seq);
   qp.max_items = static_cast<int32_t>(L.max_items);
   qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
   float* lse2p = reinterpret_cast<float*>(w + L.lse2p);
   float* deltap = reinterpret_cast<float*>(w + L.deltap);
-  if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->offsets, qp.tile_base, qp.tile_seq, status, a->batch,
-                     a->heads, a->total, 0, 0, static_cast<int>(L.pad_tiles), static_cast<int>(L.pad_tiles), lse2p,
-                     deltap, stream) != cudaSuccess)
+  if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->offsets, qp.tile_base, status, a->batch, a->heads,
+                     a->total, 0, 0, static_cast<int>(L.pad_tiles), static_cast<int>(L.pad_tiles), lse2p, deltap,
+                     dq_acc, stream) != cudaSuccess)
     return JFA_ERR_CUDA;
   BwdLaunch bl{};
   bl.head_dim = a->head_dim;
@@ -618,11 +612,12 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
   if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
   if (a->q_len == 0) return JFA_OK;
   const int64_t n_acc = static_cast<int64_t>(a->q_len) * a->heads * a->head_dim;
-  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
+  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);  // zeroed by the pre-pass when there are keys
   const int sms = sm_count();
   if (sms <= 0) return JFA_ERR_CUDA;
-  if (cudaMemsetAsync(dq_acc, 0, 4 * n_acc, stream) != cudaSuccess) return JFA_ERR_CUDA;
-  if (a->batch > 0 && a->total_k > 0) {
+  if (!(a->batch > 0 && a->total_k > 0)) {
+    if (cudaMemsetAsync(dq_acc, 0, 4 * n_acc, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  } else {
     CUtensorMap tq, tk, tv, tdo;
     const uint64_t cols = static_cast<uint64_t>(a->heads) * a->head_dim;
     if (!make_tmap_bf16(&tq, a->q, a->q_len, cols) || !make_tmap_bf16(&tk, a->k, a->total_k, cols) ||
@@ -647,8 +642,8 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
     if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
     float* lse2p = reinterpret_cast<float*>(w + L.lse2p);
     float* deltap = reinterpret_cast<float*>(w + L.deltap);
-    if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->kv_offsets, nullptr, nullptr, status, a->batch,
-                       a->heads, a->total_k, 1, a->q_len, 0, static_cast<int>(L.pad_tiles), lse2p, deltap,
+    if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->kv_offsets, nullptr, status, a->batch, a->heads,
+                       a->total_k, 1, a->q_len, 0, static_cast<int>(L.pad_tiles), lse2p, deltap, dq_acc,
                        stream) != cudaSuccess)
       return JFA_ERR_CUDA;
     BwdLaunch bl{};
@@ -804,8 +799,7 @@ jfa_status jfa_bwd_varlen(const jfa_varlen_bwd_args* a, void* ws, size_t ws_byte
   const int sms = sm_count();
   if (sms <= 0) return JFA_ERR_CUDA;
   const int64_t n_acc = static_cast<int64_t>(a->total_q) * a->q_heads * a->head_dim;
-  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
-  if (cudaMemsetAsync(dq_acc, 0, 4 * n_acc, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);  // zeroed by the pre-pass
   CUtensorMap tq, tk, tv, tdo;
   const uint64_t qcols = static_cast<uint64_t>(a->q_heads) * a->head_dim;
   const uint64_t kcols = static_cast<uint64_t>(a->kv_heads) * a->head_dim;
@@ -828,15 +822,14 @@ jfa_status jfa_bwd_varlen(const jfa_varlen_bwd_args* a, void* ws, size_t ws_byte
   qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
   qp.items = reinterpret_cast<int4*>(w + L.items);
   qp.item_seq = reinterpret_cast<int4*>(w + L.item_seq);
-  qp.tile_seq = reinterpret_cast<int32_t*>(w + L.tile_seq);
   qp.max_items = static_cast<int32_t>(L.max_items);
   qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
   float* lse2p = reinterpret_cast<float*>(w + L.lse2p);
   float* deltap = reinterpret_cast<float*>(w + L.deltap);
-  if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->q_offsets, qp.tile_base, qp.tile_seq, status, a->batch,
-                     a->q_heads, a->total_q, 0, 0, static_cast<int>(L.pad_tiles), static_cast<int>(L.pad_tiles), lse2p,
-                     deltap, stream) != cudaSuccess)
+  if (launch_bwd_pre(a->head_dim, a->o, a->dout, a->lse, a->q_offsets, qp.tile_base, status, a->batch, a->q_heads,
+                     a->total_q, 0, 0, static_cast<int>(L.pad_tiles), static_cast<int>(L.pad_tiles), lse2p, deltap,
+                     dq_acc, stream) != cudaSuccess)
     return JFA_ERR_CUDA;
   BwdLaunch bl{};
   bl.head_dim = a->head_dim;

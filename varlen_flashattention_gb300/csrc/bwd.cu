@@ -116,7 +116,6 @@ struct BwdItem {
   int kv_row0;     // first K/V row of the tile
   int Lk, Lq;
   int i0, nq;      // query tiles i0 .. i0+nq-1
-  int rot;         // the item's walk over its nqt query tiles starts at i0 + rot
   int q_row0;      // Q row of query tile 0 (TMA)
   int do_row0;     // dO row of query tile 0 (TMA)
   int64_t row_base;  // padded LSE/delta index of query tile 0 (times 128)
@@ -152,7 +151,6 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
     I.i0 = i_min / kTile;
     I.nqt = i_min < I.Lq ? nq - I.i0 : 0;
     I.nq = p.group * I.nqt;
-    I.rot = I.nqt > 0 ? I.t % I.nqt : 0;
     return I;
   }
   if (!p.bcast) {
@@ -171,21 +169,14 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
   I.i0 = p.causal ? I.t : 0;
   I.nq = nq - I.i0;
   I.nqt = I.nq;
-  I.rot = I.nqt > 0 ? I.t % I.nqt : 0;
   return I;
 }
 
 // Step ii of an item: query head hq0 + g, query tile i. The steps run over the
-// query tiles of each query head of the group in turn, starting at tile
-// i0 + rot and wrapping around: the key tiles of one (sequence, head) sit next
-// to each other in the queue and run at the same time on neighbouring CTAs, and
-// the rotation (rot = key tile mod nqt) keeps their dQ reduce-adds on different
-// query tiles instead of the same accumulator rows at once.
+// query tiles of each query head of the group in turn.
 __device__ __forceinline__ void bwd_step(const BwdItem& I, int ii, int& g, int& i) {
   g = (I.nqt == I.nq) ? 0 : ii / I.nqt;
-  int j = ii - g * I.nqt + I.rot;
-  if (j >= I.nqt) j -= I.nqt;
-  i = I.i0 + j;
+  i = I.i0 + ii - g * I.nqt;
 }
 
 // First head-dim column of an item's slice (0 when one slice covers the head).
@@ -974,73 +965,78 @@ __global__ void __launch_bounds__(448, 1)
 // backward adds them with paired fp32 instructions), written in a layout padded
 // to whole 128-row query tiles (zeros past the end of a sequence), so that the
 // backward can fetch one tile's 128 values with a single aligned bulk copy.
-// One CTA per padded query tile, all heads: the tile's rows of O and dO are one
-// contiguous block of 128 x H x d bf16 (token-major), read as (row, head) units
-// of d elements, kRowLanes lanes and 16 bytes per lane each; every load of
-// kBatch passes is issued before the first sum. Self and varlen: the tile's
-// sequence comes from tile_seq (written by the queue builder); broadcast-Q:
-// tile gt is query tile gt % nqt of sequence gt / nqt.
+// The same pass zeroes the tile's rows of the fp32 dQ accumulator (broadcast-Q:
+// the shared Q's rows, once, by the CTAs of sequence 0).
+// One CTA per padded query tile (blockIdx.x) and head (blockIdx.y). A row's
+// d elements are read 16 bytes per lane by a group of kRowLanes lanes, a warp
+// takes 32 / kRowLanes rows at a time, and every load of a warp's 16 rows is
+// issued before the first sum, so that 64 KB of a tile are in flight at once.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dout,
                                                       const float* __restrict__ lse, const int32_t* offsets,
-                                                      const int32_t* tile_base, const int32_t* tile_seq,
-                                                      const int32_t* status, int batch, int heads, int total, int bcast,
-                                                      int q_len, int pad_tiles, float* __restrict__ lse2p,
-                                                      float* __restrict__ deltap) {
+                                                      const int32_t* tile_base, const int32_t* status, int batch,
+                                                      int heads, int total, int bcast, int q_len, int pad_tiles,
+                                                      float* __restrict__ lse2p, float* __restrict__ deltap,
+                                                      float* __restrict__ dq_acc) {
   constexpr float kLog2e = 1.4426950408889634f;
   constexpr int kChunks = D / 8;                                             // 16-byte chunks of a row
-  constexpr int kRowLanes = kChunks <= 8 ? 8 : (kChunks <= 16 ? 16 : 32);   // lanes per unit (power of two)
-  constexpr int kUnitsPerPass = 256 / kRowLanes;                             // units of the CTA per pass
-  constexpr int kBatch = 8;                                                  // passes with loads in flight
-  const int gt = blockIdx.x;
-  const int lane = threadIdx.x & 31;
+  constexpr int kRowLanes = kChunks <= 8 ? 8 : (kChunks <= 16 ? 16 : 32);   // lanes per row (power of two)
+  constexpr int kRowsPerWarp = 32 / kRowLanes;
+  constexpr int kIters = (kTile / 8) / kRowsPerWarp;  // rows of a warp / rows per pass
+  const int gt = blockIdx.x, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (status[0] != JFA_OK) return;
-  int Lq, i;
-  int64_t qrow0, lse_base, lse_head_stride, pad_base, pad_head_stride;
+  // locate the tile: self -> (b, i) by binary search over tile_base; broadcast -> (b, i) directly
+  int b, i, Lq;
+  int64_t qrow0, lse_base, pad_base, acc_row0;
   if (!bcast) {
     if (gt >= tile_base[batch]) return;
-    const int b = tile_seq[gt];
+    int lo = 0, hi = batch;  // largest b with tile_base[b] <= gt
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tile_base[mid] <= gt) lo = mid; else hi = mid;
+    }
+    b = lo;
+    while (b + 1 < batch && tile_base[b + 1] <= gt) ++b;
     i = gt - tile_base[b];
     const int s0 = offsets[b];
     Lq = offsets[b + 1] - s0;
     qrow0 = s0 + static_cast<int64_t>(kTile) * i;
-    lse_base = qrow0;                        // LSE [H, total]
-    lse_head_stride = total;
-    pad_base = static_cast<int64_t>(gt) * kTile;  // padded rows [H, pad_tiles, 128]
-    pad_head_stride = static_cast<int64_t>(pad_tiles) * kTile;
+    lse_base = static_cast<int64_t>(h) * total + qrow0;
+    pad_base = (static_cast<int64_t>(h) * pad_tiles + gt) * kTile;
+    acc_row0 = qrow0;
   } else {
     const int nqt = (q_len + kTile - 1) / kTile;
-    const int b = gt / nqt;
+    b = gt / nqt;
     i = gt - b * nqt;
     if (b >= batch) return;
     Lq = q_len;
     qrow0 = static_cast<int64_t>(b) * q_len + static_cast<int64_t>(kTile) * i;
-    lse_base = static_cast<int64_t>(b) * heads * q_len + static_cast<int64_t>(kTile) * i;  // LSE [B, H, Lq]
-    lse_head_stride = q_len;
-    pad_base = (static_cast<int64_t>(b) * heads * nqt + i) * kTile;  // padded rows [B, H, nqt, 128]
-    pad_head_stride = static_cast<int64_t>(nqt) * kTile;
+    lse_base = (static_cast<int64_t>(b) * heads + h) * q_len + static_cast<int64_t>(kTile) * i;
+    pad_base = ((static_cast<int64_t>(b) * heads + h) * nqt + i) * kTile;
+    acc_row0 = b == 0 ? static_cast<int64_t>(kTile) * i : -1;  // the shared Q's rows, zeroed once
   }
+  const int sub = lane / kRowLanes, cl = lane % kRowLanes;  // row within the pass, chunk lane
   const int rows_valid = min(kTile, Lq - kTile * i);
-  const int n_units = kTile * heads;  // unit u = (row u / H, head u % H); invalid rows write zeros
-  const int sub = threadIdx.x / kRowLanes, cl = lane % kRowLanes;
-  const int64_t elem0 = qrow0 * heads * D;  // first element of the tile's block
-  for (int u0 = 0; u0 < n_units; u0 += kUnitsPerPass * kBatch) {
+  constexpr int kBatch = kIters > 8 ? 8 : kIters;  // passes whose loads are in flight together
+#pragma unroll
+  for (int i0 = 0; i0 < kIters; i0 += kBatch) {
     uint4 a[kBatch], c[kBatch];
 #pragma unroll
     for (int it = 0; it < kBatch; ++it) {
-      const int u = u0 + it * kUnitsPerPass + sub;
+      const int r = warp * (kTile / 8) + (i0 + it) * kRowsPerWarp + sub;
       a[it] = make_uint4(0, 0, 0, 0);
       c[it] = make_uint4(0, 0, 0, 0);
-      if (u < n_units && u / heads < rows_valid && cl < kChunks) {
-        const int64_t off = elem0 + static_cast<int64_t>(u) * D + 8 * cl;
+      if (r < rows_valid && cl < kChunks) {
+        const int64_t off = ((qrow0 + r) * heads + h) * D + 8 * cl;
         a[it] = ptx::ld_nc_v4(o + off);
         c[it] = ptx::ld_nc_v4(dout + off);
       }
     }
 #pragma unroll
     for (int it = 0; it < kBatch; ++it) {
-      const int u = u0 + it * kUnitsPerPass + sub;
+      const int r = warp * (kTile / 8) + (i0 + it) * kRowsPerWarp + sub;
       const uint32_t* av = reinterpret_cast<const uint32_t*>(&a[it]);
       const uint32_t* cv = reinterpret_cast<const uint32_t*>(&c[it]);
       float acc = 0.f;
@@ -1051,40 +1047,36 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
       }
 #pragma unroll
       for (int off = kRowLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (cl == 0 && u < n_units) {
-        const int r = u / heads, h = u - r * heads;
+      if (cl == 0) {
         const bool ok = r < rows_valid;
-        deltap[h * pad_head_stride + pad_base + r] = ok ? -acc : 0.f;
-        lse2p[h * pad_head_stride + pad_base + r] = ok ? -lse[h * lse_head_stride + lse_base + r] * kLog2e : 0.f;
+        deltap[pad_base + r] = ok ? -acc : 0.f;
+        lse2p[pad_base + r] = ok ? -lse[lse_base + r] * kLog2e : 0.f;
       }
+    }
+  }
+  // zero this tile's rows of the dQ accumulator: one 16-byte store per thread per step
+  if (acc_row0 >= 0) {
+    constexpr int kRowStores = D / 4;  // float4 per row
+    for (int k = threadIdx.x; k < rows_valid * kRowStores; k += blockDim.x) {
+      const int r = k / kRowStores, e = k - r * kRowStores;
+      reinterpret_cast<float4*>(dq_acc + ((acc_row0 + r) * heads + h) * D)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 }
 
-// dQ = scale * dQ_accumulated, fp32 -> bf16: four 16-byte loads of every
-// thread in flight together, then their four 8-byte stores.
-__global__ void __launch_bounds__(256) bwd_post_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq,
-                                                       int64_t n4, float scale, const int32_t* status) {
-  constexpr int kUnroll = 4;
+// dQ = scale * dQ_accumulated, fp32 -> bf16, four elements per thread.
+__global__ void bwd_post_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, int64_t n4, float scale,
+                                const int32_t* status) {
   if (status[0] != JFA_OK) return;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t k0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k0 < n4; k0 += kUnroll * stride) {
-    float4 v[kUnroll];
-#pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      const int64_t k = k0 + j * stride;
-      if (k < n4) v[j] = acc[k];
-    }
-#pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      const int64_t k = k0 + j * stride;
-      if (k < n4) {
-        uint2 w;
-        w.x = ptx::pack_bf16(v[j].x * scale, v[j].y * scale);
-        w.y = ptx::pack_bf16(v[j].z * scale, v[j].w * scale);
-        dq[k] = w;
-      }
-    }
+  for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < n4;
+       k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 v = acc[k];
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x * scale, v.y * scale);
+    __nv_bfloat162 c = __floats2bfloat162_rn(v.z * scale, v.w * scale);
+    uint2 w;
+    w.x = *reinterpret_cast<uint32_t*>(&a);
+    w.y = *reinterpret_cast<uint32_t*>(&c);
+    dq[k] = w;
   }
 }
 
@@ -1142,21 +1134,21 @@ cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUt
 }
 
 cudaError_t launch_bwd_pre(int head_dim, const void* o, const void* dout, const float* lse, const int32_t* offsets,
-                           const int32_t* tile_base, const int32_t* tile_seq, const int32_t* status, int batch,
-                           int heads, int total, int bcast, int q_len, int pad_tiles, int grid_tiles, float* lse2p,
-                           float* deltap, cudaStream_t stream) {
-  if (grid_tiles <= 0) return cudaSuccess;
+                           const int32_t* tile_base, const int32_t* status, int batch, int heads, int total, int bcast,
+                           int q_len, int pad_tiles, int grid_tiles, float* lse2p, float* deltap, float* dq_acc,
+                           cudaStream_t stream) {
+  dim3 grid(grid_tiles, heads);
   auto O = static_cast<const __nv_bfloat16*>(o);
   auto dO = static_cast<const __nv_bfloat16*>(dout);
   if (head_dim == 64)
-    bwd_pre_kernel<64><<<grid_tiles, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, tile_seq, status, batch, heads,
-                                                       total, bcast, q_len, pad_tiles, lse2p, deltap);
+    bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, status, batch, heads, total, bcast,
+                                                 q_len, pad_tiles, lse2p, deltap, dq_acc);
   else if (head_dim == 128)
-    bwd_pre_kernel<128><<<grid_tiles, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, tile_seq, status, batch,
-                                                        heads, total, bcast, q_len, pad_tiles, lse2p, deltap);
+    bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, status, batch, heads, total, bcast,
+                                                  q_len, pad_tiles, lse2p, deltap, dq_acc);
   else if (head_dim == 192)
-    bwd_pre_kernel<192><<<grid_tiles, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, tile_seq, status, batch,
-                                                        heads, total, bcast, q_len, pad_tiles, lse2p, deltap);
+    bwd_pre_kernel<192><<<grid, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, status, batch, heads, total, bcast,
+                                                  q_len, pad_tiles, lse2p, deltap, dq_acc);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
@@ -1165,8 +1157,8 @@ cudaError_t launch_bwd_pre(int head_dim, const void* o, const void* dout, const 
 cudaError_t launch_bwd_post(const float* acc, void* dq, int64_t n, float scale, const int32_t* status, int sms,
                             cudaStream_t stream) {
   const int64_t n4 = n / 4;
-  int64_t blocks = (n4 + 4 * 256 - 1) / (4 * 256);
-  if (blocks > static_cast<int64_t>(sms) * 8) blocks = static_cast<int64_t>(sms) * 8;
+  int64_t blocks = (n4 + 255) / 256;
+  if (blocks > static_cast<int64_t>(sms) * 16) blocks = static_cast<int64_t>(sms) * 16;
   if (blocks < 1) blocks = 1;
   bwd_post_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(reinterpret_cast<const float4*>(acc),
                                                                  static_cast<uint2*>(dq), n4, scale, status);

@@ -92,7 +92,6 @@ struct QueueParams {
   int4* items;             // (b, h, t, cost); varlen backward: (b, h, t, query tile_base of b)
   int4* item_seq;          // optional: (first row, length, tile_base) of each item's sequence;
                            // varlen: (first query row, L_q, first key row, L_k)
-  int32_t* tile_seq;       // optional: the sequence of every (query) tile, [tile_base[batch]]
   int32_t max_items;
   int32_t count_index;     // status word that receives the number of items; the next word
                            // receives the number with cost >= 1 (they come first)
@@ -146,12 +145,12 @@ cudaError_t launch_fwd_stream(bool causal, const CUtensorMap& tq, const CUtensor
 cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                             const CUtensorMap& tdv, cudaStream_t stream);
-// delta and the log2-scaled LSE, tile-padded; one CTA per padded query tile
-// (grid_tiles of them; self and varlen: tile_seq maps a tile to its sequence).
+// Also zeroes the fp32 dQ accumulator dq_acc ([rows, H*D]: the sequences' rows, or the
+// shared Q's rows for broadcast-Q).
 cudaError_t launch_bwd_pre(int head_dim, const void* o, const void* dout, const float* lse, const int32_t* offsets,
-                           const int32_t* tile_base, const int32_t* tile_seq, const int32_t* status, int batch,
-                           int heads, int total, int bcast, int q_len, int pad_tiles, int grid_tiles, float* lse2p,
-                           float* deltap, cudaStream_t stream);
+                           const int32_t* tile_base, const int32_t* status, int batch, int heads, int total, int bcast,
+                           int q_len, int pad_tiles, int grid_tiles, float* lse2p, float* deltap, float* dq_acc,
+                           cudaStream_t stream);
 cudaError_t launch_bwd_post(const float* acc, void* dq, int64_t n, float scale, const int32_t* status, int sms,
                             cudaStream_t stream);
 // FP8 (e4m3) input forward, head_dim 128: V transposed per 128-key tile into

@@ -324,15 +324,6 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
       }
     }
   }
-  if (p.tile_seq) {
-    // the sequence of every (query) tile, for the backward pre-pass: one warp per
-    // sequence, 32 consecutive tiles per store instruction
-    for (int b = warp; b < p.batch; b += kWarps) {
-      const int nt = ceil_tiles(seq_lens(p, s_len, s_lenk, b).x);
-      const int tb = tbase(b);
-      for (int i = lane; i < nt; i += 32) p.tile_seq[tb + i] = b;
-    }
-  }
   if (tid == 0) {
     int64_t n_items = static_cast<int64_t>(total_tiles) * p.heads;
     int64_t n_busy = static_cast<int64_t>(busy_tiles) * p.heads;
