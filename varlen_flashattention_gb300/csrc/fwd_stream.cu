@@ -53,6 +53,7 @@ struct FwdStreamParams {
   int32_t var, group;    // varlen: item_seq holds query and key bounds; query heads per KV head
   float scale_log2;
   uint64_t budget_ns;
+  int32_t* counter;      // items handed out so far (zero at launch): the producers claim items from it
 };
 
 struct FwdStreamLayout {
@@ -64,11 +65,13 @@ struct FwdStreamLayout {
   static constexpr int kOffSlots = kQSlots * kQBytes;
   static constexpr int kOffOStage = kOffSlots + kSlots * kKVBytes;  // O of a finished item (bf16, TMA store)
   static constexpr int kOffMl = kOffOStage + kTile * kD2 * 2;        // float2 (m, l) per row, two buffers
-  static constexpr int kOffBars = kOffMl + 2 * kTile * 8;
+  static constexpr int kRing = 8;                                    // claimed items in flight
+  static constexpr int kOffRing = kOffMl + 2 * kTile * 8;            // int4 pairs (item, item_seq) per entry
+  static constexpr int kOffBars = kOffRing + kRing * 32;
   // q_full[2], q_empty[2], slot_full[S], slot_empty[S], s_full[2], p_full[2],
   // o_ready[2], o_final[2], o_free[2], ml_half[2], ml_full[2], ml_empty[2],
-  // s_read[2][4], drain
-  static constexpr int kNumBars = 2 * kQSlots + 2 * kSlots + 8 * 2 + 8 + 1 + 2;
+  // s_read[2][4], drain, o_staged, o_stage_read, ring_full[R], ring_empty[R]
+  static constexpr int kNumBars = 2 * kQSlots + 2 * kSlots + 8 * 2 + 8 + 1 + 2 + 2 * kRing;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 32;
   // Tiles need 1024-byte alignment; the dynamic shared-memory base is
@@ -76,6 +79,7 @@ struct FwdStreamLayout {
   // JFA_ERR_UNSUPPORTED), so no slack is reserved.
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384, kTmemCols = 512;
   static_assert(kBytes <= 232448, "shared memory budget");
+  static_assert(kOffRing % 16 == 0 && kOffBars % 8 == 0, "ring and barrier alignment");
 };
 
 struct FwdStreamItem {
@@ -86,11 +90,9 @@ struct FwdStreamItem {
   int64_t o_row, lse0;
 };
 
-// An item's record: two independent loads (the queue stores each item's
-// sequence start and length beside it), so nothing waits on a dependent load.
-__device__ __forceinline__ FwdStreamItem stream_item(const FwdStreamParams& p, int idx) {
-  const int4 it = p.items[idx];
-  const int4 sq = p.item_seq[idx];
+// An item's record: the queue's (b, h, tile, key tiles) and the item's
+// sequence bounds, stored side by side, so nothing waits on a dependent load.
+__device__ __forceinline__ FwdStreamItem item_from(const FwdStreamParams& p, int4 it, int4 sq) {
   FwdStreamItem I;
   I.b = it.x;
   I.h = it.y;
@@ -124,27 +126,38 @@ __device__ __forceinline__ FwdStreamItem stream_item(const FwdStreamParams& p, i
   return I;
 }
 
-// Items with at least one key tile come first in the queue (descending cost),
-// so a CTA's busy items are its indices below n_busy. Returns idx and loads
-// its record when it is busy; the caller's first use of I is what waits.
-__device__ __forceinline__ int next_busy(const FwdStreamParams& p, int idx, int n_busy, FwdStreamItem& I) {
-  if (idx < n_busy) I = stream_item(p, idx);
-  return idx;
+__device__ __forceinline__ FwdStreamItem stream_item(const FwdStreamParams& p, int idx) {
+  return item_from(p, p.items[idx], p.item_seq[idx]);
 }
+
+// Causal items cost 1 .. n key tiles, very unequal even in longest-first
+// order, so they are handed out on demand: the producer warp claims the next
+// item with an atomic counter (two items ahead of its loads) and passes each
+// record to the other roles through a ring of kRing entries in shared memory;
+// an entry with b = -1 ends the stream. A CTA whose items turn out short
+// simply claims more, so no CTA idles while another still has items left.
+// Non-causal items of one sequence all cost the same and are dealt
+// round-robin (CTA c takes c, c + grid, ..), each role reading the records
+// itself one item ahead: the ring's hand-offs cost more there than the
+// balance gains.
+struct ItemRing {
+  int4* rec;         // [kRing][2]
+  uint64_t* full;    // [kRing], one arrive (the producer)
+  uint64_t* empty;   // [kRing], one arrive per consumer warp
+};
+constexpr int kRingConsumers = 13;  // the MMA warp, eight softmax warps, four epilogue warps
 
 // The order in which the loads are issued (and consumed): Q of an item, then
 // K of its first step; for every step j, K of step j + 1 (or the next item's
-// Q and first K) before V of step j. Each callback returns false to stop.
-template <class FQ, class FK, class FV>
-__device__ __forceinline__ void walk_loads(const FwdStreamParams& p, int first, int stride, int n_busy, FQ on_q,
-                                           FK on_k, FV on_v) {
+// Q and first K) before V of step j. claim(I) takes the next item (false at
+// the end of the queue); each callback returns false to stop.
+template <class FC, class FQ, class FK, class FV>
+__device__ __forceinline__ void walk_loads(FC claim, FQ on_q, FK on_k, FV on_v) {
   FwdStreamItem cur, nxt;
-  int idx = next_busy(p, first, n_busy, cur);
-  if (idx >= n_busy) return;
+  if (!claim(cur)) return;
+  bool more = claim(nxt);
   if (!on_q(cur) || !on_k(cur, 0)) return;
   while (true) {
-    const int nidx = next_busy(p, idx + stride, n_busy, nxt);
-    const bool more = nidx < n_busy;
     for (int j = 0; j < cur.n_kv; ++j) {
       if (j + 1 < cur.n_kv) {
         if (!on_k(cur, j + 1)) return;
@@ -155,7 +168,7 @@ __device__ __forceinline__ void walk_loads(const FwdStreamParams& p, int first, 
     }
     if (!more) return;
     cur = nxt;
-    idx = nidx;
+    more = claim(nxt);
   }
 }
 
@@ -193,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = s_read + 8;
   uint64_t* o_staged = drain + 1;      // every epilogue thread has written its row of the O staging
   uint64_t* o_stage_read = drain + 2;  // the TMA store of the previous staged O has read it
+  const ItemRing ring{reinterpret_cast<int4*>(smem + Lay::kOffRing), drain + 3, drain + 3 + Lay::kRing};
   float2* ml = reinterpret_cast<float2*>(smem + Lay::kOffMl);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   ptx::CtaCtl* ctl = reinterpret_cast<ptx::CtaCtl*>(smem + Lay::kOffMisc + 8);
@@ -222,6 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(drain, 1);
     ptx::mbar_init(o_staged, kTile);
     ptx::mbar_init(o_stage_read, 1);
+    for (int i = 0; i < Lay::kRing; ++i) {
+      ptx::mbar_init(ring.full + i, 1);
+      ptx::mbar_init(ring.empty + i, kRingConsumers);
+    }
     ctl->abort = 0;
     ptx::fence_barrier_init();
   }
@@ -245,6 +263,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* status = p.status;
   const uint64_t budget = p.budget_ns;
   const int cta = blockIdx.x, n_ctas = gridDim.x;
+  // The next item of a consumer role. Causal: entry k of the item ring (every
+  // lane of the warp reads it, lane 0 gives the entry back). Otherwise the
+  // role's own round-robin share: st_idx / st_pre hold the next index and its
+  // record, read one item ahead. Returns false at the end of the stream or
+  // when a wait gave up (ok then turns false as well).
+  auto take = [&](uint32_t k, FwdStreamItem& I, bool& ok, int& st_idx, FwdStreamItem& st_pre) -> bool {
+    if constexpr (!CAUSAL) {
+      (void)k;
+      if (st_idx >= n_busy) return false;
+      I = st_pre;
+      st_idx += n_ctas;
+      if (st_idx < n_busy) st_pre = stream_item(p, st_idx);
+      return true;
+    }
+    const uint32_t e = k % Lay::kRing;
+    ok = ptx::warp_all(ptx::mbar_wait(ring.full + e, (k / Lay::kRing) & 1, ctl, status, kSiteFwdMmaQ, budget));
+    if (!ok) return false;
+    const int4 it = ring.rec[2 * e], sq = ring.rec[2 * e + 1];
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ring.empty + e);
+    if (it.x < 0) return false;
+    I = item_from(p, it, sq);
+    return true;
+  };
 
   if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
@@ -280,8 +322,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tma_load_2d(dst + a * 16384, map, slot_full + slot, I.hk * kD2 + 64 * a, I.kv_row0 + kTile * j);
         return true;
       };
+      uint32_t kc = 0;  // items claimed (ring entries written)
+      auto claim = [&](FwdStreamItem& I) -> bool {
+        if constexpr (!CAUSAL) {  // round-robin share, read directly
+          const int idx = cta + static_cast<int>(kc++) * n_ctas;
+          if (idx >= n_busy) return false;
+          I = stream_item(p, idx);
+          return true;
+        }
+        const uint32_t e = kc % Lay::kRing;
+        if (!ptx::mbar_wait(ring.empty + e, ((kc / Lay::kRing) & 1) ^ 1, ctl, status, kSiteFwdProdQ, budget))
+          return false;
+        const int idx = atomicAdd(p.counter, 1);
+        int4 it = make_int4(-1, 0, 0, 0), sq = make_int4(0, 0, 0, 0);
+        if (idx < n_busy) {
+          it = p.items[idx];
+          sq = p.item_seq[idx];
+        }
+        ring.rec[2 * e] = it;
+        ring.rec[2 * e + 1] = sq;
+        ptx::mbar_arrive(ring.full + e);  // release: the record is visible to the entry's waiters
+        ++kc;
+        if (it.x < 0) return false;
+        I = item_from(p, it, sq);
+        return true;
+      };
+      // the walk stops at the first claim past the queue, which wrote the end entry
+      // (or at an abort, which the consumers' waits see as well)
       walk_loads(
-          p, cta, n_ctas, n_busy, on_q, [&](const FwdStreamItem& I, int j) { return on_kv(&tm_k, I, j); },
+          claim, on_q, [&](const FwdStreamItem& I, int j) { return on_kv(&tm_k, I, j); },
           [&](const FwdStreamItem& I, int j) { return on_kv(&tm_v, I, j); });
       // After an abort some loads may have no consumer: wait (bounded) for the
       // last fill of every slot so that no copy is in flight when the CTA exits.
@@ -335,13 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
-    FwdStreamItem cur, nxt;
-    int idx = next_busy(p, cta, n_busy, cur);
+    FwdStreamItem cur, nxt, st_pre;
+    int st_idx = cta;  // round-robin share (non-causal)
+    if (!CAUSAL && st_idx < n_busy) st_pre = stream_item(p, st_idx);
+    uint32_t kr = 0;  // ring entries taken
+    bool have = take(kr++, cur, ok, st_idx, st_pre);
     uint32_t kq = 0, x = 0;  // busy items so far, steps so far
-    if (idx < n_busy) ok = q_wait(0) && issue_s(0, 0, cur.n_kv == 1);
-    while (ok && idx < n_busy) {
-      const int nidx = next_busy(p, idx + n_ctas, n_busy, nxt);
-      const bool more = nidx < n_busy;
+    if (have) ok = q_wait(0) && issue_s(0, 0, cur.n_kv == 1);
+    while (ok && have) {
+      const bool more = take(kr++, nxt, ok, st_idx, st_pre);
+      if (!ok) break;
       const int n = cur.n_kv;
       const uint32_t ob = kq & 1;
       for (int j = 0; ok && j < n; ++j, ++x) {
@@ -379,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++kq;
       cur = nxt;
-      idx = nidx;
+      have = more;
     }
     if (ptx::elect_one()) ptx::mma_commit(drain);
     __syncwarp();
@@ -395,11 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl = p.scale_log2;
     uint32_t x = 0, kq = 0;
     bool ok = true, s_ready = false;  // s_ready: S of step x is known to be complete
-    FwdStreamItem nxt;  // the next item's record, loaded one item ahead
-    if (cta < n_busy) nxt = stream_item(p, cta);
-    for (int idx = cta; ok && idx < n_busy; idx += n_ctas) {
-      const FwdStreamItem I = nxt;
-      if (idx + n_ctas < n_busy) nxt = stream_item(p, idx + n_ctas);
+    uint32_t kr = 0;  // ring entries taken
+    FwdStreamItem I, st_pre;
+    int st_idx = cta;  // round-robin share (non-causal)
+    if (!CAUSAL && st_idx < n_busy) st_pre = stream_item(p, st_idx);
+    while (ok && take(kr++, I, ok, st_idx, st_pre)) {
       const int n = I.n_kv;
       const uint32_t ob = kq & 1;
       const uint32_t o_tmem = tmem + lane_base + (ob ? Lay::kColO1 : Lay::kColO0) + c_own;
@@ -559,21 +631,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool issuer = warp == 8 && lane == 0;
     uint8_t* ostage = smem + Lay::kOffOStage;
     uint32_t kq = 0, n_st = 0;  // busy items; items whose O went through the staging
-    FwdStreamItem nxt;          // the next item's record, loaded one item ahead
-    if (cta < n_items) nxt = stream_item(p, cta);
-    for (int idx = cta; idx < n_items; idx += n_ctas) {
-      const FwdStreamItem I = nxt;
-      if (idx + n_ctas < n_items) nxt = stream_item(p, idx + n_ctas);
+    // items with no key (they follow the busy ones): O = 0, LSE = -inf, dealt statically
+    for (int idx = n_busy + cta; idx < n_items; idx += n_ctas) {
+      const FwdStreamItem I = stream_item(p, idx);
+      const int qi = kTile * I.t + r;
+      __nv_bfloat16* orow = p.o + (I.o_row + r) * static_cast<int64_t>(p.heads) * kD2 + static_cast<int64_t>(I.h) * kD2;
+      if (qi < I.Lq) {
+        for (int c = 0; c < kD2; c += 8) ptx::st_v4(orow + c, 0, 0, 0, 0);
+        p.lse[I.lse0 + r] = -INFINITY;
+      }
+    }
+    uint32_t kr = 0;  // ring entries taken
+    bool ok = true;
+    FwdStreamItem I, st_pre;
+    int st_idx = cta;  // round-robin share (non-causal)
+    if (!CAUSAL && st_idx < n_busy) st_pre = stream_item(p, st_idx);
+    while (ok && take(kr++, I, ok, st_idx, st_pre)) {
       const int qi = kTile * I.t + r;
       const bool row_ok = qi < I.Lq;
       __nv_bfloat16* orow = p.o + (I.o_row + r) * static_cast<int64_t>(p.heads) * kD2 + static_cast<int64_t>(I.h) * kD2;
-      if (idx >= n_busy) {  // no keys: O = 0, LSE = -inf
-        if (row_ok) {
-          for (int c = 0; c < kD2; c += 8) ptx::st_v4(orow + c, 0, 0, 0, 0);
-          p.lse[I.lse0 + r] = -INFINITY;
-        }
-        continue;
-      }
       const uint32_t ob = kq & 1;
       bool w = ptx::mbar_wait(o_final + ob, (kq >> 1) & 1, ctl, status, kSiteFwdEpi, budget);
       w = w && ptx::mbar_wait(ml_full + ob, (kq >> 1) & 1, ctl, status, kSiteFwdEpi, budget);
@@ -675,6 +751,7 @@ cudaError_t launch_fwd_stream(bool causal, const CUtensorMap& tq, const CUtensor
   p.group = var.group;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.budget_ns = budget_ns;
+  p.counter = status + kStatusItemCounter;
   return causal ? launch_fwd_stream_t<true>(tq, tk, tv, to, p, grid, stream)
                 : launch_fwd_stream_t<false>(tq, tk, tv, to, p, grid, stream);
 }

@@ -65,6 +65,8 @@ enum WaitSite : int32_t {
 //   [0] status (jfa_status), [1] detail (WaitSite or check code),
 //   [2] number of queued work items.
 constexpr size_t kStatusBytes = 256;
+// Status word counting the work items handed out on demand (zeroed with the block).
+constexpr int kStatusItemCounter = 8;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
