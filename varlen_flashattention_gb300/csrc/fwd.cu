@@ -47,6 +47,7 @@ struct FwdParams {
   int32_t var, group;      // varlen: bounds from item_seq; query heads per KV head
   float scale_log2;
   uint64_t budget_ns;
+  int32_t* counter;        // items handed out so far (zero at launch; causal items are claimed from it)
 };
 
 template <int D>
@@ -57,10 +58,13 @@ struct FwdLayout {
   static constexpr int kOffQ = 0;
   static constexpr int kOffSlots = kTileBytes;
   static constexpr int kOffBars = kTileBytes * (1 + kSlots);
-  // q_full, q_empty, slot_full[S], slot_empty[S], s_full[2], p_full[2], o_ready[2], o_free, drain
-  static constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 1 + 1;
+  static constexpr int kRing = 8;  // claimed items in flight (causal)
+  // q_full, q_empty, slot_full[S], slot_empty[S], s_full[2], p_full[2], o_ready[2], o_free, drain,
+  // ring_full[R], ring_empty[R]
+  static constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 1 + 1 + 2 * kRing;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 64;
+  static constexpr int kOffRing = kOffMisc + 64;  // item index of each ring entry
+  static constexpr int kBytes = kOffRing + kRing * 4;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
   static constexpr uint32_t kTmemCols = 512;
@@ -141,6 +145,13 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* o_ready = p_full + 2;
   uint64_t* o_free = o_ready + 2;
   uint64_t* drain = o_free + 1;
+  // Causal items cost 1 .. n key tiles, very unequal even in longest-first
+  // order: the producer claims them on demand from an atomic counter and
+  // passes each index to the MMA thread and the softmax warps through a ring
+  // (an index of -1 ends the stream). Other items are dealt round-robin.
+  uint64_t* ring_full = drain + 1;
+  uint64_t* ring_empty = ring_full + Lay::kRing;
+  int32_t* ring_idx = reinterpret_cast<int32_t*>(smem + Lay::kOffRing);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   ptx::CtaCtl* ctl = reinterpret_cast<ptx::CtaCtl*>(smem + Lay::kOffMisc + 8);
 
@@ -160,6 +171,10 @@ __global__ void __launch_bounds__(192, 1)
     }
     ptx::mbar_init(o_free, 4);
     ptx::mbar_init(drain, 1);
+    for (int i = 0; i < Lay::kRing; ++i) {
+      ptx::mbar_init(ring_full + i, 1);
+      ptx::mbar_init(ring_empty + i, 5);  // the MMA thread and the four softmax warps
+    }
     ctl->abort = 0;
     ptx::fence_barrier_init();
   }
@@ -179,6 +194,29 @@ __global__ void __launch_bounds__(192, 1)
   const int n_items = p.status[2];
   int32_t* status = p.status;
   const uint64_t budget = p.budget_ns;
+  // The next item index of a consumer (the MMA thread, or a whole softmax
+  // warp whose lane 0 gives the entry back): from the ring when causal,
+  // else the round-robin share st. -1 at the end of the stream, -2 when the
+  // wait gave up.
+  auto take_idx = [&](uint32_t k, int& st, bool warp_wide) -> int {
+    if constexpr (!CAUSAL) {
+      const int v = st;
+      st += gridDim.x;
+      return v < n_items ? v : -1;
+    }
+    const uint32_t e = k % Lay::kRing;
+    bool w = ptx::mbar_wait(ring_full + e, (k / Lay::kRing) & 1, ctl, status, kSiteFwdMmaQ, budget);
+    if (warp_wide) w = ptx::warp_all(w);
+    if (!w) return -2;
+    const int v = ring_idx[e];
+    if (warp_wide) {
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ring_empty + e);
+    } else {
+      ptx::mbar_arrive(ring_empty + e);
+    }
+    return v;
+  };
 
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
@@ -195,7 +233,23 @@ __global__ void __launch_bounds__(192, 1)
         ++pos;
         return true;
       };
-      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+      uint32_t kc = 0;  // items claimed
+      auto claim = [&]() -> int {  // next item index, -1 at the end, -2 when a wait gave up
+        if constexpr (!CAUSAL) {
+          const int v = static_cast<int>(blockIdx.x + kc++ * gridDim.x);
+          return v < n_items ? v : -1;
+        }
+        const uint32_t e = kc % Lay::kRing;
+        if (!ptx::mbar_wait(ring_empty + e, ((kc / Lay::kRing) & 1) ^ 1, ctl, status, kSiteFwdProdQ, budget))
+          return -2;
+        int v = atomicAdd(p.counter, 1);
+        if (v >= n_items) v = -1;
+        ring_idx[e] = v;
+        ptx::mbar_arrive(ring_full + e);  // release: the index is visible to the entry's waiters
+        ++kc;
+        return v;
+      };
+      for (int idx = claim(); ok && idx >= 0; idx = claim()) {
         const FwdItem I = fwd_item<CAUSAL>(p, idx);
         if (I.n_kv == 0) continue;
         if (!ptx::mbar_wait(q_empty, (kq & 1) ^ 1, ctl, status, kSiteFwdProdQ, budget)) break;
@@ -237,7 +291,9 @@ __global__ void __launch_bounds__(192, 1)
         ptx::mma_commit(slot_empty + slot);
         ++pos;
       };
-      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+      uint32_t kr = 0;
+      int st = blockIdx.x;
+      for (int idx = take_idx(kr++, st, false); ok && idx >= 0; idx = take_idx(kr++, st, false)) {
         const FwdItem I = fwd_item<CAUSAL>(p, idx);
         const int n = I.n_kv;
         if (n == 0) continue;
@@ -286,8 +342,9 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float sl = p.scale_log2;
     constexpr float kLn2 = 0.6931471805599453f;
-    uint32_t it = 0, kq = 0;
-    for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
+    uint32_t it = 0, kq = 0, kr = 0;
+    int st = blockIdx.x;
+    for (int idx = take_idx(kr++, st, true); idx >= 0; idx = take_idx(kr++, st, true)) {
       const FwdItem I = fwd_item<CAUSAL>(p, idx);
       const int n = I.n_kv;
       const bool row_ok = kTile * I.t + r < I.Lq;
@@ -450,6 +507,7 @@ cudaError_t launch_fwd(int head_dim, bool causal, const CUtensorMap& tq, const C
   p.group = var.group;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.budget_ns = budget_ns;
+  p.counter = status + kStatusItemCounter;
   if (head_dim == 64) return causal ? launch_fwd_t<64, true>(tq, tk, tv, p, grid, stream)
                                     : launch_fwd_t<64, false>(tq, tk, tv, p, grid, stream);
   if (head_dim == 128) return causal ? launch_fwd_t<128, true>(tq, tk, tv, p, grid, stream)
