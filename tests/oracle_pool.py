@@ -60,12 +60,13 @@ def bf16_words_to_f64(w: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------- worker side
 
 def _o_stats(gpu, ref):
-    """(max over elements of |diff| - bound, max |diff|)."""
+    """(max over elements of |diff| - bound, max |diff|, elements above the plain 1e-2, elements)."""
     if ref.size == 0:
-        return -np.inf, 0.0
+        return -np.inf, 0.0, 0, 0
     diff = np.abs(gpu - ref)
     diff = np.where(np.isnan(diff), np.inf, diff)
-    return float(np.max(diff - (TOL_O + TOL_O_REL * np.abs(ref)))), float(diff.max())
+    return (float(np.max(diff - (TOL_O + TOL_O_REL * np.abs(ref)))), float(diff.max()),
+            int(np.count_nonzero(diff > TOL_O)), int(diff.size))
 
 
 def _max_err(a, b):
@@ -121,8 +122,11 @@ def _chunks(offsets, max_rows):
 
 
 def _assert_stats(stats, what, grads):
+    from tests.parity import report_plain_o
     viol = max(s["o"][0] for s in stats)
     assert viol <= 0.0, f"{what}: O exceeds 1e-2 + 2^-7|O| by {viol:.3e} (max|diff| {max(s['o'][1] for s in stats):.3e})"
+    report_plain_o(f"{what} O", sum(s["o"][2] for s in stats), sum(s["o"][3] for s in stats),
+                   max(s["o"][1] for s in stats))
     e = max(s["lse"] for s in stats)
     assert e <= TOL_LSE, f"{what}: LSE max|diff| {e:.3e} > {TOL_LSE}"
     for g in grads:

@@ -4,7 +4,9 @@ Tolerances (stated for bf16 inputs with fp32 accumulation):
   O      |gpu - oracle| <= 1e-2 + 2^-7 |oracle|   elementwise
   LSE    max|gpu - oracle| <= 1e-3
   dQ, dK, dV   max|gpu - oracle| <= 2e-2 * max|oracle|
-Integer work (split bounds, tile order) is compared bit for bit.
+Integer work (split bounds, tile order) is compared bit for bit. Elements of O
+above the plain 1e-2 (within the allowance) are reported as pytest warnings
+with their count and the largest error.
 
 The 2^-7 |O| term is the bf16 representation allowance derived from the
 arithmetic: O is returned in bf16 (rounding error up to 2^-8 |O|) and the
@@ -43,6 +45,15 @@ def max_err(a, b) -> float:
 TOL_O_REL = 2.0 ** -7
 
 
+def report_plain_o(what, n_over, n, worst):
+    """Records elements whose O error exceeds the plain 1e-2 while staying within
+    the bf16 allowance: a pytest warning with the count and the largest error."""
+    if n_over:
+        import warnings
+        warnings.warn(f"{what}: {n_over} of {n} elements above the plain 1e-2 (largest {worst:.4e}), "
+                      f"all within 1e-2 + 2^-7 |O|", stacklevel=3)
+
+
 def check_o(gpu, ref, what="O"):
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
@@ -55,6 +66,7 @@ def check_o(gpu, ref, what="O"):
     worst = int(np.argmax(diff - bound))
     assert np.all(diff <= bound), (f"{what}: |diff| {diff.flat[worst]:.3e} > {bound.flat[worst]:.3e} "
                                    f"(= 1e-2 + 2^-7 * |ref| {abs(ref.flat[worst]):.3f}); max|diff| {diff.max():.3e}")
+    report_plain_o(what, int(np.count_nonzero(diff > TOL_O)), diff.size, float(diff.max()))
     return float(diff.max())
 
 
