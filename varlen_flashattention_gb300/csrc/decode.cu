@@ -66,7 +66,11 @@ struct DecodeParams {
 
 constexpr int kDecD = 128;
 constexpr int kDecWarps = 4;
-constexpr int kDecStages = 3;                                        // blocks per warp ring
+// Blocks per warp ring: two (one in flight while one is computed) at three
+// CTAs per SM measured faster than three at two CTAs per SM (4.61 against
+// 4.43 TB/s at page 16, 16 splits): more CTAs per SM overlap one CTA's start
+// and final merge with the others' loops, which deeper rings did not make up.
+constexpr int kDecStages = 2;
 constexpr int kDecRingBytes = kDecStages * kDecWarps * 16 * 32 * 16;  // 16 pieces x 32 lanes x 16 B
 
 // 16-byte asynchronous global -> shared copy; bytes past src_bytes are zero.
@@ -95,7 +99,7 @@ __device__ __forceinline__ void flag_bad(int32_t* status, int32_t code) {
 
 // Rows of a tile: G query heads x q_len tokens. TWO: rows 8..15 are in use.
 template <int G, bool TWO>
-__global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(128, 3) decode_split_kernel(const DecodeParams p) {
   static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "GQA group");
   static_assert(G < 16 || TWO, "a group of 16 fills both row halves");
   constexpr bool kTwoRowHalves = TWO;

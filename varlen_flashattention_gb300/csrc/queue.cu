@@ -158,10 +158,21 @@ __device__ __forceinline__ int warp_sum(int v) {
 // the key lengths and first key rows: the record passes then read no global
 // memory per sequence (a dependent global load per sequence and warp had
 // dominated the kernel).
+// The one-pass counting sort (fast path) applies when every tile of a sequence
+// has the same cost (not causal), the batch has one sequence per thread and
+// the costs fit 32 buckets; it needs a [32 buckets][32 warps] table.
+__host__ __device__ inline bool queue_fast_path(const QueueParams& p, int kmax) {
+  return !p.causal && p.batch <= 1024 && kmax < 32;
+}
+constexpr int kQueueFastTable = 32 * 32;
+
 __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParams p, int kmax) {
   extern __shared__ int s_start[];  // [kmax + 1]: tiles (per head) of higher cost than bucket k
   const int n_cached = min(p.batch, kQueueLenCache);
-  int* s_len = s_start + kmax + 1;
+  const bool fast = queue_fast_path(p, kmax);
+  // fast path: [bucket][warp] tiles, then their exclusive prefix over warps
+  int (*s_wtot)[32] = reinterpret_cast<int (*)[32]>(s_start + kmax + 1);
+  int* s_len = s_start + kmax + 1 + (fast ? kQueueFastTable : 0);
   int* s_first = s_len + n_cached;  // first tile position of sequence b (one-cost modes)
   int* s_off = s_first + n_cached;  // first (query) row of sequence b
   int* s_tb = s_off + n_cached;     // tile base of sequence b
@@ -227,16 +238,40 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
   // varlen key tiles that no query sees (dK = dV = 0)
   const bool keep_empty = p.mode == kQueueBcastFwd || var;
   const int kmin = keep_empty ? 0 : 1;
-  for (int k = kmin + warp; k <= kmax; k += kWarps) {
-    int n = 0;
-    for (int b = lane; b < p.batch; b += 32) {
-      int c, tf;
-      const int2 L = seq_lens(p, s_len, s_lenk, b);
-      tiles_with_cost(p, L.x, L.y, k, c, tf);
-      n += c;
+  // Fast path (counting sort in one pass, queue_fast_path): each sequence's
+  // bucket and tile count are found once, and the per-bucket totals and
+  // positions come from shared-memory sums and warp scans, instead of one pass
+  // over all sequences per bucket.
+  int f_k = -1, f_c = 0;          // fast path: this thread's sequence's bucket and tiles (0: none queued)
+  if (fast) {
+    s_wtot[warp][lane] = 0;
+    if (tid <= kmax) s_start[tid] = 0;
+    if (tid < p.batch) {
+      const int2 L = seq_lens(p, s_len, s_lenk, tid);
+      const int nt = item_tiles(p, L.x, L.y);
+      const int k = nt > 0 ? item_cost(p, L.x, L.y, 0) : -1;
+      if (nt > 0 && k >= kmin) {
+        f_k = k;
+        f_c = nt;
+      }
     }
-    n = warp_sum(n);
-    if (lane == 0) s_start[k] = n;
+    __syncthreads();
+    if (f_c > 0) {
+      atomicAdd(&s_start[f_k], f_c);
+      atomicAdd(&s_wtot[f_k][warp], f_c);
+    }
+  } else {
+    for (int k = kmin + warp; k <= kmax; k += kWarps) {
+      int n = 0;
+      for (int b = lane; b < p.batch; b += 32) {
+        int c, tf;
+        const int2 L = seq_lens(p, s_len, s_lenk, b);
+        tiles_with_cost(p, L.x, L.y, k, c, tf);
+        n += c;
+      }
+      n = warp_sum(n);
+      if (lane == 0) s_start[k] = n;
+    }
   }
   __syncthreads();
 
@@ -277,7 +312,29 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
     if (sq)
       for (int e = 0; e < c * p.heads; ++e) *sq++ = seq;
   };
-  for (int k = kmin + warp; k <= kmax; k += kWarps) {
+  if (fast) {
+    // the tiles of earlier warps in each bucket (warp k scans bucket k over the
+    // warps), then of earlier lanes with the same bucket in this warp
+    if (warp <= kmax) {
+      const int v = s_wtot[warp][lane];
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      s_wtot[warp][lane] = incl - v;
+    }
+    int pre = 0;
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) {
+      const int kj = __shfl_sync(0xffffffffu, f_k, j), cj = __shfl_sync(0xffffffffu, f_c, j);
+      if (j < lane && kj == f_k) pre += cj;
+    }
+    __syncthreads();
+    if (f_c > 0) s_first[tid] = s_start[f_k] + s_wtot[f_k][warp] + pre;
+  }
+  for (int k = kmin + warp; !fast && k <= kmax; k += kWarps) {
     int run = s_start[k];
     for (int b0 = 0; b0 < p.batch; b0 += 32) {
       const int b = b0 + lane;
@@ -348,7 +405,8 @@ cudaError_t launch_queue(const QueueParams& p, cudaStream_t stream) {
   if (p.mode == kQueueVarBwd) kmax = static_cast<int64_t>(p.group) * tiles(p.max_seqlen);
   if (kmax > kQueueMaxCost) return cudaErrorInvalidValue;
   const int64_t cached = std::min(p.batch, kQueueLenCache);
-  const size_t smem = static_cast<size_t>(kmax + 1 + cached * (queue_var(p.mode) ? 6 : 4)) * sizeof(int);
+  const int64_t table = queue_fast_path(p, static_cast<int>(kmax)) ? kQueueFastTable : 0;
+  const size_t smem = static_cast<size_t>(kmax + 1 + table + cached * (queue_var(p.mode) ? 6 : 4)) * sizeof(int);
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t e = once_per_device(attr_done, [] {
     return cudaFuncSetAttribute(build_queue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
