@@ -315,17 +315,22 @@ def measure_decode(jfa, device, peaks, page_size=16, splits=(1, 2, 4, 8, 16, 32,
                 jfa.jfa_decode_smallq(q, kc, vc, pt, sl_d, S, o=o, lse=lse, workspace=ws, events=events)
         for _ in range(3):
             call()
-        times = []
-        for _ in range(iters):
+        # the whole call (no events inside it: an event between the split and
+        # merge launches would hold the merge back), then the split kernel alone
+        times, kern = [], []
+        for k in range(2 * iters):
             flush.zero_()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record()
-            call(ev)
+            call(ev if k >= iters else None)
             e.record()
             torch.cuda.synchronize()
-            times.append((s.elapsed_time(e), ev[0].elapsed_time(ev[1])))
-        call_ms = statistics.median(t[0] for t in times)
-        kern_ms = statistics.median(t[1] for t in times)
+            if k < iters:
+                times.append(s.elapsed_time(e))
+            else:
+                kern.append(ev[0].elapsed_time(ev[1]))
+        call_ms = statistics.median(times)
+        kern_ms = statistics.median(kern)
         r = {"splits": S, "call_us": call_ms * 1e3, "split_kernel_us": kern_ms * 1e3,
              "tb_s": nbytes / (call_ms * 1e-3) / 1e12}
         curve.append({"splits": S, "call_us": round(r["call_us"], 2), "tb_s": round(r["tb_s"], 3)})
@@ -518,11 +523,23 @@ def main():
     ap.add_argument("--profile", action="store_true",
                     help="profiling run: warmup + steps of the plain fwd+bwd loop only, no JSON line")
     ap.add_argument("--batch", type=int, default=1024, help="sequences per GPU (profiling runs use fewer)")
+    ap.add_argument("--profile-decode", type=int, default=0, metavar="PAGE",
+                    help="profiling run: the paged decode workload at this page size, 32 splits, a few calls")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return reference_arm(args)
+    if args.profile_decode:
+        import torch
+        import varlen_flashattention_gb300 as jfa
+        from varlen_flashattention_gb300 import build as _build
+        _build.build()
+        peaks, _ = load_peaks()
+        r = measure_decode(jfa, torch.device("cuda", 0), peaks, page_size=args.profile_decode, splits=(32,), iters=2)
+        print(f"profile run: decode page {args.profile_decode}, 32 splits: {r['tb_s']:.3f} TB/s "
+              f"(3 warm-up calls, then 4 timed; not a bench value)")
+        return 0
     if args.profile:
         import torch
         import varlen_flashattention_gb300 as jfa

@@ -687,7 +687,7 @@ jfa_status jfa_decode_splitkv(const jfa_decode_args* a, void* ws, size_t ws_byte
   if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (launch_decode_status_clear(reinterpret_cast<int32_t*>(w), stream) != cudaSuccess) return JFA_ERR_CUDA;
   if (a->batch == 0) return JFA_OK;
   return cuda_status(launch_decode(*a, reinterpret_cast<float*>(w + L.part_o), reinterpret_cast<float*>(w + L.part_lse),
                                    reinterpret_cast<int32_t*>(w), stream));
@@ -894,7 +894,7 @@ jfa_status jfa_decode_smallq(const jfa_decode_smallq_args* a, void* ws, size_t w
   if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (launch_decode_status_clear(reinterpret_cast<int32_t*>(w), stream) != cudaSuccess) return JFA_ERR_CUDA;
   if (a->batch == 0) return JFA_OK;
   DecodeLaunch d;
   d.q = a->q;

@@ -97,6 +97,77 @@ __device__ __forceinline__ void flag_bad(int32_t* status, int32_t code) {
   if (atomicCAS(status, JFA_OK, JFA_ERR_BAD_INPUT) == JFA_OK) status[1] = code;
 }
 
+constexpr int kDecMaxSplits = 128;  // the entry points accept at most 128 splits
+
+// Merge of the S split partials of one output row (one warp):
+// lse = ln sum_s exp(lse_s), O = sum_s exp(lse_s - lse) O_s. The split
+// weights go through shared memory (0 for an empty split, whose partial O is
+// zero); each lane sums four output columns over the splits in order, with
+// the loads of sixteen splits in flight at a time. Partials are read with
+// L2-only loads (other SMs wrote them).
+__device__ __forceinline__ void merge_row(const float* part_o, const float* part_lse, int S, int64_t stride,
+                                          int64_t row, int lane, float* s_w, __nv_bfloat16* o, float* lse) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  float ls[kDecMaxSplits / 32];
+  float M = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kDecMaxSplits / 32; ++k) {
+    const int s = lane + 32 * k;
+    ls[k] = s < S ? __ldcg(part_lse + s * stride + row) : -INFINITY;
+    M = fmaxf(M, ls[k]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+#pragma unroll
+  for (int k = 0; k < kDecMaxSplits / 32; ++k) {
+    const int s = lane + 32 * k;
+    if (s < S) s_w[s] = (M == -INFINITY || ls[k] == -INFINITY) ? 0.f : ptx::ex2((ls[k] - M) * kLog2e);
+  }
+  __syncwarp();
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float Z = 0.f;
+  for (int s0 = 0; s0 < S; s0 += 16) {
+    float4 v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      v[j] = s0 + j < S ? __ldcg(reinterpret_cast<const float4*>(part_o + ((s0 + j) * stride + row) * kDecD) + lane)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (s0 + j >= S) break;
+      const float w = s_w[s0 + j];
+      Z += w;
+      acc.x += w * v[j].x;
+      acc.y += w * v[j].y;
+      acc.z += w * v[j].z;
+      acc.w += w * v[j].w;
+    }
+  }
+  __syncwarp();  // s_w is rewritten for the warp's next row
+  const float inv = Z > 0.f ? 1.f / Z : 0.f;
+  __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  __nv_bfloat162 c = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 packed;
+  packed.x = *reinterpret_cast<uint32_t*>(&a);
+  packed.y = *reinterpret_cast<uint32_t*>(&c);
+  *reinterpret_cast<uint2*>(o + row * kDecD + 4 * lane) = packed;
+  if (lane == 0) lse[row] = Z > 0.f ? M + logf(Z) : -INFINITY;
+}
+
+// Launched as a programmatic dependent of the split kernel: its blocks may be
+// scheduled while the split kernel's last blocks run, and wait here until that
+// grid has completed and its partials are visible.
+__global__ void __launch_bounds__(128) decode_merge_kernel(const float* __restrict__ part_o,
+                                                           const float* __restrict__ part_lse, int S, int rows,
+                                                           __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+  __shared__ float s_w[4][kDecMaxSplits];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + warp;  // (b, token, head)
+  if (row >= rows) return;
+  merge_row(part_o, part_lse, S, rows, row, lane, s_w[warp], o, lse);
+}
+
 // Rows of a tile: G query heads x q_len tokens. TWO: rows 8..15 are in use.
 template <int G, bool TWO>
 __global__ void __launch_bounds__(128, 3) decode_split_kernel(const DecodeParams p) {
@@ -112,6 +183,10 @@ __global__ void __launch_bounds__(128, 3) decode_split_kernel(const DecodeParams
   float(*s_l)[kRows] =
       reinterpret_cast<float(*)[kRows]>(reinterpret_cast<float*>(ring) + kDecWarps * kRows * (kDecD + 1));
 
+  // the status block is cleared by the kernel before this one (launched as its dependent)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // every block has started: the merge kernel may be scheduled (it waits for this grid to finish)
+  asm volatile("griddepcontrol.launch_dependents;");
   const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, qq = lane & 3;
@@ -180,18 +255,19 @@ __global__ void __launch_bounds__(128, 3) decode_split_kernel(const DecodeParams
   // 2q+8, 2q+9 (B operand of PV). Tokens past the split end are zero-filled
   // from an in-bounds row.
   uint4* my_ring = ring + static_cast<size_t>(warp) * kDecStages * 16 * 32;
-  auto issue = [&](int kb, int slot) {
+  // Page-table entry of token lo + 16 kb + (lane % 16), read one block ahead
+  // of its copies so that its latency is not in front of every block.
+  auto page_entry = [&](int kb) -> int {
+    const int tok = lo + kb * 16 + (lane & 15);
+    return (kb < nblk && tok < hi) ? pt[tok / P] : 0;
+  };
+  auto issue = [&](int kb, int slot, int pg) {
     uint4* dst = my_ring + slot * 16 * 32 + lane;
     if (kb < nblk) {
       const int t0 = lo + kb * 16;
-      int pg = 0;  // page of token t0 + (lane % 16), validated
-      const int tok = t0 + (lane & 15);
-      if (tok < hi) {
-        pg = pt[tok / P];
-        if (pg < 0 || pg >= p.num_pages) {
-          flag_bad(p.status, kSiteDecodeTable);
-          pg = 0;
-        }
+      if (pg < 0 || pg >= p.num_pages) {  // page of token t0 + (lane % 16), validated
+        flag_bad(p.status, kSiteDecodeTable);
+        pg = 0;
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
@@ -218,13 +294,15 @@ __global__ void __launch_bounds__(128, 3) decode_split_kernel(const DecodeParams
   };
   const int nmine = nblk > warp ? (nblk - warp + kDecWarps - 1) / kDecWarps : 0;
 #pragma unroll
-  for (int i = 0; i < kDecStages - 1; ++i) issue(warp + kDecWarps * i, i);
+  for (int i = 0; i < kDecStages - 1; ++i) issue(warp + kDecWarps * i, i, page_entry(warp + kDecWarps * i));
+  int pg_next = page_entry(warp + kDecWarps * (kDecStages - 1));
 
   for (int i = 0; i < nmine; ++i) {
     const int kb = warp + kDecWarps * i;
     const int t0 = lo + kb * 16;
     // keep kDecStages - 1 blocks in flight: the slot refilled held block i - 1
-    issue(warp + kDecWarps * (i + kDecStages - 1), (i + kDecStages - 1) % kDecStages);
+    issue(warp + kDecWarps * (i + kDecStages - 1), (i + kDecStages - 1) % kDecStages, pg_next);
+    pg_next = page_entry(warp + kDecWarps * (i + kDecStages));
     cp_async_wait<kDecStages - 1>();  // block i has landed
     const uint4* src = my_ring + (i % kDecStages) * 16 * 32 + lane;
     uint4 kr[2][4];
@@ -389,55 +467,43 @@ __global__ void __launch_bounds__(128, 3) decode_split_kernel(const DecodeParams
   }
 }
 
-// Merge of the split partials: lse = ln sum_s exp(lse_s), O = sum_s exp(lse_s - lse) O_s.
-__global__ void __launch_bounds__(128) decode_merge_kernel(const float* __restrict__ part_o,
-                                                           const float* __restrict__ part_lse, int S, int B, int Hq,
-                                                           __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + warp;  // (b, h)
-  if (row >= B * Hq) return;
-  constexpr float kLog2e = 1.4426950408889634f;
-  const int64_t stride = static_cast<int64_t>(B) * Hq;
-  float M = -INFINITY;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, part_lse[s * stride + row]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float Z = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      const float ls = part_lse[s * stride + row];
-      if (ls == -INFINITY) continue;
-      const float w = ptx::ex2((ls - M) * kLog2e);
-      Z += w;
-      const float4 v = *reinterpret_cast<const float4*>(part_o + (s * stride + row) * kDecD + 4 * lane);
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
-    }
-  }
-  const float inv = Z > 0.f ? 1.f / Z : 0.f;
-  __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-  __nv_bfloat162 c = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-  uint2 packed;
-  packed.x = *reinterpret_cast<uint32_t*>(&a);
-  packed.y = *reinterpret_cast<uint32_t*>(&c);
-  *reinterpret_cast<uint2*>(o + row * kDecD + 4 * lane) = packed;
-  if (lane == 0) lse[row] = Z > 0.f ? M + logf(Z) : -INFINITY;
-}
-
 // ------------------------------------------------------------------ launchers
+
+// A launch that may begin while the previous kernel on the stream finishes
+// (programmatic dependent launch): the kernel waits for that grid with
+// griddepcontrol.wait before touching anything it wrote.
+template <class... KArgs, class... Args>
+static cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, int threads, size_t smem,
+                                    cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 template <int G>
 static cudaError_t launch_split(bool two, dim3 grid, const DecodeParams& p, cudaStream_t stream) {
   if constexpr (G == 16) {
-    decode_split_kernel<16, true><<<grid, 128, kDecRingBytes, stream>>>(p);
-  } else if (two) {
-    decode_split_kernel<G, true><<<grid, 128, kDecRingBytes, stream>>>(p);
+    return launch_dependent(decode_split_kernel<16, true>, grid, 128, kDecRingBytes, stream, p);
   } else {
-    decode_split_kernel<G, false><<<grid, 128, kDecRingBytes, stream>>>(p);
+    if (two) return launch_dependent(decode_split_kernel<G, true>, grid, 128, kDecRingBytes, stream, p);
+    return launch_dependent(decode_split_kernel<G, false>, grid, 128, kDecRingBytes, stream, p);
   }
+}
+
+// The status block of a decode call, cleared by a kernel (not a memset) so that
+// the split kernel can be launched as its programmatic dependent.
+__global__ void decode_status_clear_kernel(int32_t* status) { status[threadIdx.x] = 0; }
+
+cudaError_t launch_decode_status_clear(int32_t* status, cudaStream_t stream) {
+  decode_status_clear_kernel<<<1, kStatusBytes / 4, 0, stream>>>(status);
   return cudaGetLastError();
 }
 
@@ -492,9 +558,9 @@ cudaError_t launch_decode_general(const DecodeLaunch& a, float* part_o, float* p
   if (ev) cudaEventRecord(ev[1], stream);
   if (e != cudaSuccess) return e;
   const int rows = a.batch * a.q_len * a.q_heads;  // (b, token, head) rows of O
-  decode_merge_kernel<<<(rows + 3) / 4, 128, 0, stream>>>(part_o, part_lse, a.num_splits, a.batch * a.q_len,
-                                                            a.q_heads, static_cast<__nv_bfloat16*>(a.o), a.lse);
-  return cudaGetLastError();
+  return launch_dependent(decode_merge_kernel, dim3((rows + 3) / 4), 128, 0, stream, static_cast<const float*>(part_o),
+                          static_cast<const float*>(part_lse), a.num_splits, rows, static_cast<__nv_bfloat16*>(a.o),
+                          a.lse);
 }
 
 cudaError_t launch_decode(const jfa_decode_args& a, float* part_o, float* part_lse, int32_t* status,

@@ -190,6 +190,9 @@ struct DecodeLaunch {
 };
 cudaError_t launch_decode_general(const DecodeLaunch& a, float* part_o, float* part_lse, int32_t* status,
                                   cudaStream_t stream);
+// Clears a decode call's status block (a kernel, so that the split kernel can
+// start as its programmatic dependent).
+cudaError_t launch_decode_status_clear(int32_t* status, cudaStream_t stream);
 // Argument checks of jfa_decode_splitkv (scalars, alignment), without the workspace.
 jfa_status check_decode_args(const jfa_decode_args* a);
 
