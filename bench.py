@@ -585,11 +585,17 @@ def main():
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(pg)
     torch.cuda.synchronize()
+    # the timed steps carry no events inside them (an event between two kernels of
+    # a call holds back the programmatic launch of the second); the main kernels
+    # are timed on the same number of steps right after, with events around them
     with ClockSampler(local) as clocks:
         start.record()
         for i in range(args.steps):
-            run_step(jfa, w, bufs, ev_f=evs_f[i], ev_b=evs_b[i])
+            run_step(jfa, w, bufs)
         stop.record()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            run_step(jfa, w, bufs, ev_f=evs_f[i], ev_b=evs_b[i])
         torch.cuda.synchronize()
     barrier(pg)
     ms = start.elapsed_time(stop) / args.steps
@@ -752,7 +758,9 @@ def main():
                     "ms_per_step": e2e_ms,
                     "how": "public API; pinned host inputs copied in and all outputs copied out every step; "
                            "copies of neighbouring steps overlap compute (3 streams, 2 buffer sets)"},
-            "gpu_launches": 6 * args.steps,
+            # per step: status clear, queue and forward kernel; status clear, queue,
+            # pre-pass, backward kernel and post-pass
+            "gpu_launches": 8 * args.steps,
             "clocks": clk,
             "decode": decode,
             "detail": detail,

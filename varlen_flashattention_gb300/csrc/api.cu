@@ -423,7 +423,7 @@ jfa_status jfa_fwd(const jfa_fwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
-  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (launch_status_clear(reinterpret_cast<int32_t*>(w), stream) != cudaSuccess) return JFA_ERR_CUDA;
   if (a->batch == 0 || a->total == 0) return JFA_OK;
   const int sms = sm_count();
   if (sms <= 0) return JFA_ERR_CUDA;
@@ -473,7 +473,7 @@ jfa_status jfa_bwd(const jfa_bwd_args* a, void* ws, size_t ws_bytes, cudaStream_
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
-  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (launch_status_clear(reinterpret_cast<int32_t*>(w), stream) != cudaSuccess) return JFA_ERR_CUDA;
   if (a->batch == 0 || a->total == 0) return JFA_OK;
   const int sms = sm_count();
   if (sms <= 0) return JFA_ERR_CUDA;
@@ -552,7 +552,7 @@ jfa_status jfa_fwd_broadcast_q(const jfa_bcast_fwd_args* a, void* ws, size_t ws_
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
-  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (launch_status_clear(reinterpret_cast<int32_t*>(w), stream) != cudaSuccess) return JFA_ERR_CUDA;
   if (a->batch == 0 || a->q_len == 0) return JFA_OK;
   const int sms = sm_count();
   if (sms <= 0) return JFA_ERR_CUDA;
@@ -609,7 +609,7 @@ jfa_status jfa_bwd_broadcast_q(const jfa_bcast_bwd_args* a, void* ws, size_t ws_
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
-  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (launch_status_clear(reinterpret_cast<int32_t*>(w), stream) != cudaSuccess) return JFA_ERR_CUDA;
   if (a->q_len == 0) return JFA_OK;
   const int64_t n_acc = static_cast<int64_t>(a->q_len) * a->heads * a->head_dim;
   float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);  // zeroed by the pre-pass when there are keys
@@ -687,7 +687,7 @@ jfa_status jfa_decode_splitkv(const jfa_decode_args* a, void* ws, size_t ws_byte
   if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  if (launch_decode_status_clear(reinterpret_cast<int32_t*>(w), stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (launch_status_clear(reinterpret_cast<int32_t*>(w), stream) != cudaSuccess) return JFA_ERR_CUDA;
   if (a->batch == 0) return JFA_OK;
   return cuda_status(launch_decode(*a, reinterpret_cast<float*>(w + L.part_o), reinterpret_cast<float*>(w + L.part_lse),
                                    reinterpret_cast<int32_t*>(w), stream));
@@ -715,7 +715,7 @@ jfa_status jfa_fwd_varlen(const jfa_varlen_fwd_args* a, void* ws, size_t ws_byte
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
-  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (launch_status_clear(reinterpret_cast<int32_t*>(w), stream) != cudaSuccess) return JFA_ERR_CUDA;
   if (a->batch == 0 || a->total_q == 0) return JFA_OK;
   const int sms = sm_count();
   if (sms <= 0) return JFA_ERR_CUDA;
@@ -785,7 +785,7 @@ jfa_status jfa_bwd_varlen(const jfa_varlen_bwd_args* a, void* ws, size_t ws_byte
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
-  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (launch_status_clear(reinterpret_cast<int32_t*>(w), stream) != cudaSuccess) return JFA_ERR_CUDA;
   const size_t kv_bytes = static_cast<size_t>(a->total_k) * a->kv_heads * a->head_dim * 2;
   if (a->batch == 0 || a->total_k == 0 || a->total_q == 0) {
     // no (query, key) pair anywhere: every gradient is zero
@@ -894,7 +894,7 @@ jfa_status jfa_decode_smallq(const jfa_decode_smallq_args* a, void* ws, size_t w
   if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  if (launch_decode_status_clear(reinterpret_cast<int32_t*>(w), stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (launch_status_clear(reinterpret_cast<int32_t*>(w), stream) != cudaSuccess) return JFA_ERR_CUDA;
   if (a->batch == 0) return JFA_OK;
   DecodeLaunch d;
   d.q = a->q;
@@ -952,7 +952,7 @@ jfa_status jfa_fwd_fp8(const jfa_fwd_fp8_args* a, void* ws, size_t ws_bytes, cud
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
-  if (cudaMemsetAsync(w, 0, kStatusBytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (launch_status_clear(reinterpret_cast<int32_t*>(w), stream) != cudaSuccess) return JFA_ERR_CUDA;
   if (a->batch == 0 || a->total == 0) return JFA_OK;
   const int sms = sm_count();
   if (sms <= 0) return JFA_ERR_CUDA;

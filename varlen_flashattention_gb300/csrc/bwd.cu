@@ -213,6 +213,7 @@ __global__ void __launch_bounds__(448, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the layout needs a 1024-byte aligned base; the launch reserves 256 bytes of slack
   if (smem + Lay::kBytes > smem_raw + Lay::kAlloc) {
+    wait_prior_grid();  // the status block was cleared before this kernel
     if (threadIdx.x == 0) atomicCAS(p.status, JFA_OK, JFA_ERR_UNSUPPORTED);
     return;
   }
@@ -291,6 +292,10 @@ __global__ void __launch_bounds__(448, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // everything above is local set-up; the queue and the pre-pass are read below.
+  // The post-pass is not let in early: its blocks would wait on these SMs
+  // through the whole kernel.
+  wait_prior_grid();
   const uint32_t tmem = *tmem_slot;
   const int n_work = p.status[2] * p.n_chunks;
   int32_t* status = p.status;
@@ -984,6 +989,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   constexpr int kRowLanes = kChunks <= 8 ? 8 : (kChunks <= 16 ? 16 : 32);   // lanes per row (power of two)
   constexpr int kRowsPerWarp = 32 / kRowLanes;
   constexpr int kIters = (kTile / 8) / kRowsPerWarp;  // rows of a warp / rows per pass
+  wait_prior_grid();
+  allow_next_grid();
   const int gt = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (status[0] != JFA_OK) return;
@@ -1067,6 +1074,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 // dQ = scale * dQ_accumulated, fp32 -> bf16, four elements per thread.
 __global__ void bwd_post_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, int64_t n4, float scale,
                                 const int32_t* status) {
+  wait_prior_grid();
   if (status[0] != JFA_OK) return;
   for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < n4;
        k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -1093,8 +1101,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     return cudaFuncSetAttribute(bwd_kernel<D, DC>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
   });
   if (e != cudaSuccess) return e;
-  bwd_kernel<D, DC><<<grid, 448, Lay::kAlloc, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
-  return cudaGetLastError();
+  return launch_after(bwd_kernel<D, DC>, dim3(grid), dim3(448), Lay::kAlloc, stream, tq, tk, tv, tdo, tdq, tdk, tdv, p);
 }
 
 cudaError_t launch_bwd_main(const BwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -1140,18 +1147,19 @@ cudaError_t launch_bwd_pre(int head_dim, const void* o, const void* dout, const 
   dim3 grid(grid_tiles, heads);
   auto O = static_cast<const __nv_bfloat16*>(o);
   auto dO = static_cast<const __nv_bfloat16*>(dout);
+  cudaError_t e;
   if (head_dim == 64)
-    bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, status, batch, heads, total, bcast,
-                                                 q_len, pad_tiles, lse2p, deltap, dq_acc);
+    e = launch_after(bwd_pre_kernel<64>, grid, dim3(256), 0, stream, O, dO, lse, offsets, tile_base, status, batch,
+                     heads, total, bcast, q_len, pad_tiles, lse2p, deltap, dq_acc);
   else if (head_dim == 128)
-    bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, status, batch, heads, total, bcast,
-                                                  q_len, pad_tiles, lse2p, deltap, dq_acc);
+    e = launch_after(bwd_pre_kernel<128>, grid, dim3(256), 0, stream, O, dO, lse, offsets, tile_base, status, batch,
+                     heads, total, bcast, q_len, pad_tiles, lse2p, deltap, dq_acc);
   else if (head_dim == 192)
-    bwd_pre_kernel<192><<<grid, 256, 0, stream>>>(O, dO, lse, offsets, tile_base, status, batch, heads, total, bcast,
-                                                  q_len, pad_tiles, lse2p, deltap, dq_acc);
+    e = launch_after(bwd_pre_kernel<192>, grid, dim3(256), 0, stream, O, dO, lse, offsets, tile_base, status, batch,
+                     heads, total, bcast, q_len, pad_tiles, lse2p, deltap, dq_acc);
   else
     return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_bwd_post(const float* acc, void* dq, int64_t n, float scale, const int32_t* status, int sms,
@@ -1160,9 +1168,8 @@ cudaError_t launch_bwd_post(const float* acc, void* dq, int64_t n, float scale, 
   int64_t blocks = (n4 + 255) / 256;
   if (blocks > static_cast<int64_t>(sms) * 16) blocks = static_cast<int64_t>(sms) * 16;
   if (blocks < 1) blocks = 1;
-  bwd_post_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(reinterpret_cast<const float4*>(acc),
-                                                                 static_cast<uint2*>(dq), n4, scale, status);
-  return cudaGetLastError();
+  return launch_after(bwd_post_kernel, dim3(static_cast<int>(blocks)), dim3(256), 0, stream,
+                      reinterpret_cast<const float4*>(acc), static_cast<uint2*>(dq), n4, scale, status);
 }
 
 }  // namespace jfa

@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const float* __restri
                                                            const float* __restrict__ part_lse, int S, int rows,
                                                            __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
   __shared__ float s_w[4][kDecMaxSplits];
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  wait_prior_grid();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + warp;  // (b, token, head)
   if (row >= rows) return;
@@ -184,9 +184,8 @@ __global__ void __launch_bounds__(128, 3) decode_split_kernel(const DecodeParams
       reinterpret_cast<float(*)[kRows]>(reinterpret_cast<float*>(ring) + kDecWarps * kRows * (kDecD + 1));
 
   // the status block is cleared by the kernel before this one (launched as its dependent)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // every block has started: the merge kernel may be scheduled (it waits for this grid to finish)
-  asm volatile("griddepcontrol.launch_dependents;");
+  wait_prior_grid();
+  allow_next_grid();  // every block has started: the merge kernel may be scheduled (it waits for this grid)
   const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, qq = lane & 3;
@@ -469,42 +468,14 @@ __global__ void __launch_bounds__(128, 3) decode_split_kernel(const DecodeParams
 
 // ------------------------------------------------------------------ launchers
 
-// A launch that may begin while the previous kernel on the stream finishes
-// (programmatic dependent launch): the kernel waits for that grid with
-// griddepcontrol.wait before touching anything it wrote.
-template <class... KArgs, class... Args>
-static cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, int threads, size_t smem,
-                                    cudaStream_t stream, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
 template <int G>
 static cudaError_t launch_split(bool two, dim3 grid, const DecodeParams& p, cudaStream_t stream) {
   if constexpr (G == 16) {
-    return launch_dependent(decode_split_kernel<16, true>, grid, 128, kDecRingBytes, stream, p);
+    return launch_after(decode_split_kernel<16, true>, grid, dim3(128), kDecRingBytes, stream, p);
   } else {
-    if (two) return launch_dependent(decode_split_kernel<G, true>, grid, 128, kDecRingBytes, stream, p);
-    return launch_dependent(decode_split_kernel<G, false>, grid, 128, kDecRingBytes, stream, p);
+    if (two) return launch_after(decode_split_kernel<G, true>, grid, dim3(128), kDecRingBytes, stream, p);
+    return launch_after(decode_split_kernel<G, false>, grid, dim3(128), kDecRingBytes, stream, p);
   }
-}
-
-// The status block of a decode call, cleared by a kernel (not a memset) so that
-// the split kernel can be launched as its programmatic dependent.
-__global__ void decode_status_clear_kernel(int32_t* status) { status[threadIdx.x] = 0; }
-
-cudaError_t launch_decode_status_clear(int32_t* status, cudaStream_t stream) {
-  decode_status_clear_kernel<<<1, kStatusBytes / 4, 0, stream>>>(status);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_general(const DecodeLaunch& a, float* part_o, float* part_lse, int32_t* status,
@@ -558,7 +529,7 @@ cudaError_t launch_decode_general(const DecodeLaunch& a, float* part_o, float* p
   if (ev) cudaEventRecord(ev[1], stream);
   if (e != cudaSuccess) return e;
   const int rows = a.batch * a.q_len * a.q_heads;  // (b, token, head) rows of O
-  return launch_dependent(decode_merge_kernel, dim3((rows + 3) / 4), 128, 0, stream, static_cast<const float*>(part_o),
+  return launch_after(decode_merge_kernel, dim3((rows + 3) / 4), dim3(128), 0, stream, static_cast<const float*>(part_o),
                           static_cast<const float*>(part_lse), a.num_splits, rows, static_cast<__nv_bfloat16*>(a.o),
                           a.lse);
 }

@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(192, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  wait_prior_grid();  // the set-up above is local; the queue's items are read below
   const uint32_t tmem = *tmem_slot;
   const int n_items = p.status[2];
   int32_t* status = p.status;
@@ -483,8 +484,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     return cudaFuncSetAttribute(fwd_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
   });
   if (e != cudaSuccess) return e;
-  fwd_kernel<D, CAUSAL><<<grid, 192, Lay::kAlloc, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  return launch_after(fwd_kernel<D, CAUSAL>, dim3(grid), dim3(192), Lay::kAlloc, stream, tq, tk, tv, p);
 }
 
 cudaError_t launch_fwd(int head_dim, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  wait_prior_grid();  // the set-up above is local; the queue's items are read below
   const uint32_t tmem = *tmem_slot;
   const int n_items = p.status[2];
   int32_t* status = p.status;
@@ -587,6 +588,8 @@ __device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t c,
 __global__ void __launch_bounds__(256) vt_transpose_kernel(const uint8_t* __restrict__ v, const int4* items,
                                                            const int4* item_seq, const int32_t* status, int heads,
                                                            uint8_t* __restrict__ vt) {
+  wait_prior_grid();
+  allow_next_grid();
   const int idx = blockIdx.x;
   if (status[0] != JFA_OK || idx >= status[2]) return;
   const int4 it = items[idx], sq = item_seq[idx];
@@ -622,17 +625,16 @@ cudaError_t launch_fp8_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                                 Fp8Layout::kAlloc);
   });
   if (e != cudaSuccess) return e;
-  fwd_fp8_kernel<CAUSAL><<<grid, kF8Threads, Fp8Layout::kAlloc, stream>>>(tq, tk, tvt, to, p);
-  return cudaGetLastError();
+  return launch_after(fwd_fp8_kernel<CAUSAL>, dim3(grid), dim3(kF8Threads), Fp8Layout::kAlloc, stream, tq, tk, tvt, to,
+                      p);
 }
 
 }  // namespace
 
 cudaError_t launch_vt_transpose(const void* v, const int4* items, const int4* item_seq, const int32_t* status,
                                 int heads, int max_items, void* vt, cudaStream_t stream) {
-  vt_transpose_kernel<<<max_items, 256, 0, stream>>>(static_cast<const uint8_t*>(v), items, item_seq, status, heads,
-                                                     static_cast<uint8_t*>(vt));
-  return cudaGetLastError();
+  return launch_after(vt_transpose_kernel, dim3(max_items), dim3(256), 0, stream, static_cast<const uint8_t*>(v), items,
+                      item_seq, static_cast<const int32_t*>(status), heads, static_cast<uint8_t*>(vt));
 }
 
 cudaError_t launch_fwd_fp8(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,

@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   if (smem != smem_raw) {  // base not aligned enough for the layout
+    wait_prior_grid();  // the status block was cleared before this kernel
     if (threadIdx.x == 0) atomicCAS(p.status, JFA_OK, JFA_ERR_UNSUPPORTED);
     return;
   }
@@ -257,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  wait_prior_grid();  // the set-up above is local; the queue's items are read below
   const uint32_t tmem = *tmem_slot;
   const int n_items = p.status[2];
   const int n_busy = p.status[3];  // items with at least one key tile: indices 0 .. n_busy - 1
@@ -727,8 +729,8 @@ cudaError_t launch_fwd_stream_t(const CUtensorMap& tq, const CUtensorMap& tk, co
                                 FwdStreamLayout::kBytes);
   });
   if (e != cudaSuccess) return e;
-  fwd_stream_kernel<CAUSAL><<<grid, kThreads, FwdStreamLayout::kBytes, stream>>>(tq, tk, tv, to, p);
-  return cudaGetLastError();
+  return launch_after(fwd_stream_kernel<CAUSAL>, dim3(grid), dim3(kThreads), FwdStreamLayout::kBytes, stream, tq, tk, tv,
+                      to, p);
 }
 
 }  // namespace

@@ -14,6 +14,35 @@ namespace jfa {
 
 constexpr int kTile = 128;  // rows of a Q or K/V tile (tcgen05 M = 128)
 
+// Programmatic dependent launch. The kernels of one entry point run as a chain
+// on the caller's stream (status clear, queue, pre-pass, main kernel,
+// post-pass); each later kernel is launched so that it may be scheduled while
+// the one before it finishes, and it calls wait_prior_grid() before it touches
+// anything that kernel wrote (the wait returns once the prior grid has
+// completed and its writes are visible). A kernel calls allow_next_grid()
+// once every block of it has started, which lets the next one be scheduled.
+// Every kernel launched this way waits before it exits, so completion is
+// ordered along the chain.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+#ifdef __CUDACC__
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#endif
+
 // Runs `set` (a kernel attribute call, idempotent) once per device: `done`
 // holds one bit per device already set, so launches from several threads or
 // on several devices stay correct. Devices past 63 run it on every launch.
@@ -190,9 +219,9 @@ struct DecodeLaunch {
 };
 cudaError_t launch_decode_general(const DecodeLaunch& a, float* part_o, float* part_lse, int32_t* status,
                                   cudaStream_t stream);
-// Clears a decode call's status block (a kernel, so that the split kernel can
-// start as its programmatic dependent).
-cudaError_t launch_decode_status_clear(int32_t* status, cudaStream_t stream);
+// Clears a call's status block (a kernel, not a memset, so that the call's next
+// kernel can start as its programmatic dependent).
+cudaError_t launch_status_clear(int32_t* status, cudaStream_t stream);
 // Argument checks of jfa_decode_splitkv (scalars, alignment), without the workspace.
 jfa_status check_decode_args(const jfa_decode_args* a);
 

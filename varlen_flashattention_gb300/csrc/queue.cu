@@ -167,6 +167,8 @@ __host__ __device__ inline bool queue_fast_path(const QueueParams& p, int kmax) 
 constexpr int kQueueFastTable = 32 * 32;
 
 __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParams p, int kmax) {
+  wait_prior_grid();  // the status block is cleared by the kernel before this one
+  allow_next_grid();
   extern __shared__ int s_start[];  // [kmax + 1]: tiles (per head) of higher cost than bucket k
   const int n_cached = min(p.batch, kQueueLenCache);
   const bool fast = queue_fast_path(p, kmax);
@@ -413,7 +415,18 @@ cudaError_t launch_queue(const QueueParams& p, cudaStream_t stream) {
                                 static_cast<int>((kQueueMaxCost + 1 + 6 * kQueueLenCache) * sizeof(int)));
   });
   if (e != cudaSuccess) return e;
-  build_queue_kernel<<<1, kQThreads, smem, stream>>>(p, static_cast<int>(kmax));
+  return launch_after(build_queue_kernel, dim3(1), dim3(kQThreads), smem, stream, p, static_cast<int>(kmax));
+}
+
+// A call's status block cleared by one small block; the call's next kernel may
+// be scheduled at once (it waits for this one before reading the block).
+__global__ void status_clear_kernel(int32_t* status) {
+  allow_next_grid();
+  status[threadIdx.x] = 0;
+}
+
+cudaError_t launch_status_clear(int32_t* status, cudaStream_t stream) {
+  status_clear_kernel<<<1, kStatusBytes / 4, 0, stream>>>(status);
   return cudaGetLastError();
 }
 
