@@ -53,10 +53,17 @@
  *  - max_seqlen / total arguments are host copies of facts about the device
  *    offsets, so that no device-to-host copy is needed; the kernels check
  *    them against the offsets and report JFA_ERR_BAD_INPUT on a mismatch.
+ *  - A call enqueues a short chain of kernels (a status clear, the work
+ *    queue, the pass's kernels). Every kernel after the first is launched with
+ *    programmatic stream serialization: it may be scheduled while the one
+ *    before it finishes and waits for it on the device before reading its
+ *    results, so the chain keeps stream order and can be captured in a graph.
  *  - main_kernel_events: optional pair of cudaEvent_t (may be NULL). When
  *    set, event [0] is recorded on `stream` just before the main attention
  *    kernel and event [1] just after it, so a caller can time that kernel
- *    alone. The library does not create, own or destroy them.
+ *    alone (the recorded events keep the main kernel from starting before
+ *    the kernel in front of it has finished). The library does not create,
+ *    own or destroy them.
  */
 #ifndef JFA_H
 #define JFA_H
