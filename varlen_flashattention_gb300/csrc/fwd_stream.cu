@@ -70,8 +70,8 @@ struct FwdStreamLayout {
   static constexpr int kOffBars = kOffRing + kRing * 32;
   // q_full[2], q_empty[2], slot_full[S], slot_empty[S], s_full[2], p_full[2],
   // o_ready[2], o_final[2], o_free[2], ml_half[2], ml_full[2], ml_empty[2],
-  // s_read[2][4], drain, o_staged, o_stage_read, ring_full[R], ring_empty[R]
-  static constexpr int kNumBars = 2 * kQSlots + 2 * kSlots + 8 * 2 + 8 + 1 + 2 + 2 * kRing;
+  // half_max[2][2][4], drain, o_staged, o_stage_read, ring_full[R], ring_empty[R]
+  static constexpr int kNumBars = 2 * kQSlots + 2 * kSlots + 8 * 2 + 16 + 1 + 2 + 2 * kRing;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 32;
   // Tiles need 1024-byte alignment; the dynamic shared-memory base is
@@ -81,6 +81,16 @@ struct FwdStreamLayout {
   static_assert(kBytes <= 232448, "shared memory budget");
   static_assert(kOffRing % 16 == 0 && kOffBars % 8 == 0, "ring and barrier alignment");
 };
+
+// One 32-bit TMEM column of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t v;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
+  return v;
+}
 
 struct FwdStreamItem {
   int b, h, t;
@@ -203,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* ml_half = o_free + 2;
   uint64_t* ml_full = ml_half + 2;
   uint64_t* ml_empty = ml_full + 2;
-  uint64_t* s_read = ml_empty + 2;  // [S buffer][warp quarter]
-  uint64_t* drain = s_read + 8;
+  uint64_t* half_max = ml_empty + 2;  // [S buffer][group][warp quarter]: the group's row maxima are published
+  uint64_t* drain = half_max + 16;
   uint64_t* o_staged = drain + 1;      // every epilogue thread has written its row of the O staging
   uint64_t* o_stage_read = drain + 2;  // the TMA store of the previous staged O has read it
   const ItemRing ring{reinterpret_cast<int4*>(smem + Lay::kOffRing), drain + 3, drain + 3 + Lay::kRing};
@@ -233,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(ml_full + i, kTile);  // every group-1 softmax thread
       ptx::mbar_init(ml_empty + i, 4);     // the four epilogue warps
     }
-    for (int i = 0; i < 8; ++i) ptx::mbar_init(s_read + i, 2);  // the two warps on one lane quarter
+    for (int i = 0; i < 16; ++i) ptx::mbar_init(half_max + i, 1);  // one softmax warp each
     ptx::mbar_init(drain, 1);
     ptx::mbar_init(o_staged, kTile);
     ptx::mbar_init(o_stage_read, 1);
@@ -481,7 +491,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j, ++x) {
         const uint32_t s_tmem = tmem + lane_base + ((x & 1) ? Lay::kColS1 : Lay::kColS0);
-        uint64_t* rd = s_read + (x & 1) * 4 + quarter;
         if (!s_ready && !(ok = ptx::mbar_wait(s_full + (x & 1), (x >> 1) & 1, ctl, status, kSiteFwdSoftS, budget)))
           break;
         ptx::tc_fence_after();
@@ -495,31 +504,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (c0 + e >= lim) v[e] = __float_as_uint(-INFINITY);
           }
         };
-        // row max over all 128 columns: eight independent chains of three-input maxima
-        float mx8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
-        auto fold = [&](const uint32_t(&v)[32]) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            mx8[(e >> 1) & 7] = ptx::fmax3(mx8[(e >> 1) & 7], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-        };
-        // The other group's half first (only its maximum is needed), so that
-        // the other group may start overwriting it with P early; then the own
-        // half, which stays in registers.
+        // this group's half of the row (it stays in registers) and its maximum,
+        // folded in eight independent chains of three-input maxima
         uint32_t sa[2][32];
-        ptx::tmem_ld32(s_tmem + c_other, sa[0]);
-        ptx::tmem_ld32(s_tmem + c_other + 32, sa[1]);
-        ptx::tmem_ld_wait();
-        ptx::reg_fence32(sa[0]);
-        ptx::reg_fence32(sa[1]);
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(rd);
-        mask(sa[0], c_other);
-        mask(sa[1], c_other + 32);
-        fold(sa[0]);
-        fold(sa[1]);
         ptx::tmem_ld32(s_tmem + c_own, sa[0]);
         ptx::tmem_ld32(s_tmem + c_own + 32, sa[1]);
         ptx::tmem_ld_wait();
@@ -527,20 +514,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::reg_fence32(sa[1]);
         mask(sa[0], c_own);
         mask(sa[1], c_own + 32);
-        fold(sa[0]);
-        fold(sa[1]);
-        // the other group's read of this group's half, tested now and waited
-        // for (if still needed) after the exponentials
-        const bool rd_done = ptx::mbar_test(rd, (x >> 1) & 1);
-        const float mx = fmaxf(ptx::fmax3(mx8[0], mx8[1], mx8[2]),
-                               ptx::fmax3(ptx::fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-        const float mnew = mx * sl;
+        float mx8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            mx8[(e >> 1) & 7] = ptx::fmax3(mx8[(e >> 1) & 7], __uint_as_float(sa[u][e]), __uint_as_float(sa[u][e + 1]));
+        const float hmax = fmaxf(ptx::fmax3(mx8[0], mx8[1], mx8[2]),
+                                 ptx::fmax3(ptx::fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+        // The two groups exchange their halves' maxima (neither reads the
+        // other's scores): each writes its maximum into the last column of its
+        // own half of S, which it no longer needs (P goes over the first 32).
+        // After the first step of an item the exponentials are taken against
+        // the running max at once, and taken again only if the row max turns
+        // out to have grown by more than 2^8 (both groups see the same two
+        // maxima, so they decide alike).
+        tmem_st1(s_tmem + c_own + 63, __float_as_uint(hmax));
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(half_max + ((x & 1) * 2 + g) * 4 + quarter);
+        uint64_t* other = half_max + ((x & 1) * 2 + (1 - g)) * 4 + quarter;
+        auto other_max = [&]() -> float {  // after `other` has completed
+          ptx::tc_fence_after();
+          const uint32_t v = tmem_ld1(s_tmem + c_other + 63);
+          ptx::tmem_ld_wait();
+          return __uint_as_float(v);
+        };
+        // P = 2^(S sl - m) over this group's half, stored over its S columns; returns the half-row sum
+        const uint64_t sl2 = ptx::f2_packf(sl, sl);
+        auto exps = [&](float mref) -> float {
+          const float mu = (mref == -INFINITY) ? 0.f : mref;  // a row with no visible key yet keeps P = 0
+          const uint64_t nmu2 = ptx::f2_packf(-mu, -mu);
+          uint64_t ls2[2] = {ptx::f2_packf(0.f, 0.f), ptx::f2_packf(0.f, 0.f)};
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              float x0, x1;
+              ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sa[u][2 * e], sa[u][2 * e + 1]), sl2, nmu2), x0, x1);
+              const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+              ls2[e & 1] = ptx::f2_add(ls2[e & 1], ptx::f2_packf(p0, p1));
+              pk[e] = ptx::pack_bf16(p0, p1);
+            }
+            ptx::tmem_st16(s_tmem + c_own + 16 * u, pk);
+          }
+          float a0, a1, b0, b1;
+          ptx::f2_unpack(ls2[0], a0, a1);
+          ptx::f2_unpack(ls2[1], b0, b1);
+          return (a0 + a1) + (b0 + b1);
+        };
+        float lsum = 0.f;
         if (j == 0) {
-          m = mnew;
+          if (!(ok = ptx::mbar_wait(other, (x >> 1) & 1, ctl, status, kSiteFwdSoftS, budget))) break;
+          m = fmaxf(hmax, other_max()) * sl;
+          lsum = exps(m);
         } else {
+          lsum = exps(m);
+          if (!(ok = ptx::mbar_wait(other, (x >> 1) & 1, ctl, status, kSiteFwdSoftS, budget))) break;
+          const float mnew = fmaxf(hmax, other_max()) * sl;
           // O is rescaled only when the running max grows by more than 2^8;
           // otherwise the old max stays the reference and P stays below 2^8.
-          // Both groups see the same maximum, so they decide alike.
           const bool need = mnew > m + 8.0f;
           if (__any_sync(0xffffffffu, need)) {
             const float mm = need ? mnew : m;
@@ -559,44 +596,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
               ptx::tmem_st16(o_tmem + 16 * c, ov);
             }
-            ptx::tmem_st_wait();
             l *= f;
             m = mm;
+            lsum = exps(m);  // again, against the new reference (over the first try's P)
           }
         }
-        // a row with every key of this tile masked (possible only above the diagonal) keeps m
-        const float mu = (m == -INFINITY) ? 0.f : m;
-        // P = 2^(S sl - m): scale and shift on fp32 pairs, exp2 per element, sums on pairs
-        const uint64_t sl2 = ptx::f2_packf(sl, sl), nmu2 = ptx::f2_packf(-mu, -mu);
-        uint64_t ls2[2] = {ptx::f2_packf(0.f, 0.f), ptx::f2_packf(0.f, 0.f)};
-        // each 32-key chunk of P is stored as soon as it is packed (over S
-        // columns c_own .., once the other group has read them)
-        bool rd_ok = rd_done;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float x0, x1;
-            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sa[u][2 * e], sa[u][2 * e + 1]), sl2, nmu2), x0, x1);
-            const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-            ls2[e & 1] = ptx::f2_add(ls2[e & 1], ptx::f2_packf(p0, p1));
-            pk[e] = ptx::pack_bf16(p0, p1);
-          }
-          if (!rd_ok) {
-            if (!(ok = ptx::mbar_wait(rd, (x >> 1) & 1, ctl, status, kSiteFwdSoftS, budget))) break;
-            rd_ok = true;
-          }
-          ptx::tc_fence_after();
-          ptx::tmem_st16(s_tmem + c_own + 16 * u, pk);
-        }
-        if (!ok) break;
-        {
-          float a0, a1, b0, b1;
-          ptx::f2_unpack(ls2[0], a0, a1);
-          ptx::f2_unpack(ls2[1], b0, b1);
-          l += (a0 + a1) + (b0 + b1);
-        }
+        l += lsum;
         if (j + 1 == n) {
           // Row statistics of the finished item go to the epilogue: group 0
           // stores (m, its sum), group 1 adds its sum to that.
