@@ -84,13 +84,23 @@ struct Fp8Layout {
   static constexpr int kOffBars = kOffMl + 2 * kTile * 8;
   // q_full[2], q_empty[2], slot_full[S], slot_empty[S], s_full[2], p_full[2], o_ready[2], o_final[2],
   // o_free[2], ml_half[2], ml_full[2], ml_empty[2], drain, o_staged, o_stage_read
-  static constexpr int kNumBars = 2 * kQSlots + 2 * kSlots + 9 * 2 + 3;
+  static constexpr int kNumBars = 2 * kQSlots + 2 * kSlots + 9 * 2 + 3 + 16;  // + half_max[2][2][4]
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   static constexpr int kAlloc = kBytes + 1024;  // slack for the 1024-byte alignment of the tiles
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384, kTmemCols = 512;
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
+
+// One 32-bit TMEM column of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t v;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
+  return v;
+}
 
 struct Fp8Item {
   int h, t;
@@ -164,7 +174,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   uint64_t* ml_half = o_free + 2;
   uint64_t* ml_full = ml_half + 2;
   uint64_t* ml_empty = ml_full + 2;
-  uint64_t* drain = ml_empty + 2;
+  uint64_t* half_max = ml_empty + 2;  // [S buffer][group][warp quarter]: the group's row maxima are published
+  uint64_t* drain = half_max + 16;
   uint64_t* o_staged = drain + 1;      // every epilogue thread has written its row of the O staging
   uint64_t* o_stage_read = drain + 2;  // the TMA store of the previous staged O has read it
   float2* ml = reinterpret_cast<float2*>(smem + Lay::kOffMl);
@@ -191,6 +202,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       ptx::mbar_init(ml_full + i, kTile);  // every group-1 softmax thread
       ptx::mbar_init(ml_empty + i, 4);     // the four epilogue warps
     }
+    for (int i = 0; i < 16; ++i) ptx::mbar_init(half_max + i, 1);  // one softmax warp each
     ptx::mbar_init(drain, 1);
     ptx::mbar_init(o_staged, kTile);
     ptx::mbar_init(o_stage_read, 1);
@@ -372,24 +384,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
               if (c0 + e >= lim) v[e] = __float_as_uint(-INFINITY);
           }
         };
-        float mx8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
-        auto fold = [&](const uint32_t(&v)[32]) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            mx8[(e >> 1) & 7] = ptx::fmax3(mx8[(e >> 1) & 7], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-        };
+        // this group's half of the row (it stays in registers) and its maximum
         uint32_t sa[2][32];
-        ptx::tmem_ld32(s_tmem + c_other, sa[0]);
-        ptx::tmem_ld32(s_tmem + c_other + 32, sa[1]);
-        ptx::tmem_ld_wait();
-        ptx::reg_fence32(sa[0]);
-        ptx::reg_fence32(sa[1]);
-        mask(sa[0], c_other);
-        mask(sa[1], c_other + 32);
-        fold(sa[0]);
-        fold(sa[1]);
         ptx::tmem_ld32(s_tmem + c_own, sa[0]);
         ptx::tmem_ld32(s_tmem + c_own + 32, sa[1]);
         ptx::tmem_ld_wait();
@@ -397,14 +393,72 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         ptx::reg_fence32(sa[1]);
         mask(sa[0], c_own);
         mask(sa[1], c_own + 32);
-        fold(sa[0]);
-        fold(sa[1]);
-        const float mx = fmaxf(ptx::fmax3(mx8[0], mx8[1], mx8[2]),
-                               ptx::fmax3(ptx::fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-        const float mnew = mx * sl;
+        float mx8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            mx8[(e >> 1) & 7] = ptx::fmax3(mx8[(e >> 1) & 7], __uint_as_float(sa[u][e]), __uint_as_float(sa[u][e + 1]));
+        const float hmax = fmaxf(ptx::fmax3(mx8[0], mx8[1], mx8[2]),
+                                 ptx::fmax3(ptx::fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+        // The halves' maxima are exchanged through the last TMEM column of each
+        // half (read into registers already; P goes to shared memory); after an
+        // item's first step the exponentials run against the running max before
+        // the other half's maximum is known, and again only if it grew by > 2^8.
+        tmem_st1(s_tmem + c_own + 63, __float_as_uint(hmax));
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(half_max + ((x & 1) * 2 + g) * 4 + quarter);
+        uint64_t* other = half_max + ((x & 1) * 2 + (1 - g)) * 4 + quarter;
+        auto other_max = [&]() -> float {  // after `other` has completed
+          ptx::tc_fence_after();
+          const uint32_t v = tmem_ld1(s_tmem + c_other + 63);
+          ptx::tmem_ld_wait();
+          return __uint_as_float(v);
+        };
+        // P = 2^(S sl - m) as e4m3: this group's 64 keys, 16 per 16-byte chunk of
+        // the swizzled row; returns the half-row sum
+        uint8_t* prow = p_row + (x & 1) * kF8TileBytes;
+        const uint64_t sl2 = ptx::f2_packf(sl, sl);
+        auto exps = [&](float mref) -> float {
+          const float mu = (mref == -INFINITY) ? 0.f : mref;
+          const uint64_t nmu2 = ptx::f2_packf(-mu, -mu);
+          uint64_t ls2[2] = {ptx::f2_packf(0.f, 0.f), ptx::f2_packf(0.f, 0.f)};
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {  // keys 4 e .. 4 e + 3 of this 32-key half
+              float q0, q1, q2, q3;
+              ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sa[u][4 * e], sa[u][4 * e + 1]), sl2, nmu2), q0, q1);
+              ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sa[u][4 * e + 2], sa[u][4 * e + 3]), sl2, nmu2), q2, q3);
+              const float p0 = ptx::ex2(q0), p1 = ptx::ex2(q1), p2 = ptx::ex2(q2), p3 = ptx::ex2(q3);
+              ls2[e & 1] = ptx::f2_add(ls2[e & 1], ptx::f2_add(ptx::f2_packf(p0, p1), ptx::f2_packf(p2, p3)));
+              const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
+              const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p2, p3), __NV_SATFINITE, __NV_E4M3);
+              w[e] = lo | (hi << 16);
+            }
+            const int ch = (c_own >> 4) + 2 * u;  // 16-byte chunks ch, ch + 1 of the 128-byte row
+            ptx::st_shared_v4(prow + ((ch ^ sw) << 4), w[0], w[1], w[2], w[3]);
+            ptx::st_shared_v4(prow + (((ch + 1) ^ sw) << 4), w[4], w[5], w[6], w[7]);
+          }
+          float a0, a1, b0, b1;
+          ptx::f2_unpack(ls2[0], a0, a1);
+          ptx::f2_unpack(ls2[1], b0, b1);
+          return (a0 + a1) + (b0 + b1);
+        };
+        float lsum = 0.f;
         if (j == 0) {
-          m = mnew;
+          if (!(ok = ptx::mbar_wait(other, (x >> 1) & 1, ctl, status, kSiteFwdSoftS, budget))) break;
+          m = fmaxf(hmax, other_max()) * sl;
+          lsum = exps(m);
         } else {
+          lsum = exps(m);
+          if (!(ok = ptx::mbar_wait(other, (x >> 1) & 1, ctl, status, kSiteFwdSoftS, budget))) break;
+          const float mnew = fmaxf(hmax, other_max()) * sl;
           // rescale O only when the row max grows by more than 2^8 (P stays below 2^8 < 448)
           const bool need = mnew > m + 8.0f;
           if (__any_sync(0xffffffffu, need)) {
@@ -427,37 +481,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             ptx::tmem_st_wait();
             l *= f;
             m = mm;
+            lsum = exps(m);  // again, against the new reference (over the first try's P)
           }
         }
-        // P = 2^(S sl - m) as e4m3: this group's 64 keys, 16 per 16-byte chunk of the swizzled row
-        const float mu = (m == -INFINITY) ? 0.f : m;
-        const uint64_t sl2 = ptx::f2_packf(sl, sl), nmu2 = ptx::f2_packf(-mu, -mu);
-        uint64_t ls2[2] = {ptx::f2_packf(0.f, 0.f), ptx::f2_packf(0.f, 0.f)};
-        uint8_t* prow = p_row + (x & 1) * kF8TileBytes;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          uint32_t w[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {  // keys 4 e .. 4 e + 3 of this 32-key half
-            float q0, q1, q2, q3;
-            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sa[u][4 * e], sa[u][4 * e + 1]), sl2, nmu2), q0, q1);
-            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sa[u][4 * e + 2], sa[u][4 * e + 3]), sl2, nmu2), q2, q3);
-            const float p0 = ptx::ex2(q0), p1 = ptx::ex2(q1), p2 = ptx::ex2(q2), p3 = ptx::ex2(q3);
-            ls2[e & 1] = ptx::f2_add(ls2[e & 1], ptx::f2_add(ptx::f2_packf(p0, p1), ptx::f2_packf(p2, p3)));
-            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
-            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p2, p3), __NV_SATFINITE, __NV_E4M3);
-            w[e] = lo | (hi << 16);
-          }
-          const int ch = (c_own >> 4) + 2 * u;  // 16-byte chunks ch, ch + 1 of the 128-byte row
-          ptx::st_shared_v4(prow + ((ch ^ sw) << 4), w[0], w[1], w[2], w[3]);
-          ptx::st_shared_v4(prow + (((ch + 1) ^ sw) << 4), w[4], w[5], w[6], w[7]);
-        }
-        {
-          float a0, a1, b0, b1;
-          ptx::f2_unpack(ls2[0], a0, a1);
-          ptx::f2_unpack(ls2[1], b0, b1);
-          l += (a0 + a1) + (b0 + b1);
-        }
+        l += lsum;
         if (j + 1 == n) {
           // row statistics of the finished item: group 0 stores (m, its sum), group 1 adds its sum
           if (g == 0) {
