@@ -30,6 +30,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "jfa_internal.h"
@@ -606,40 +607,62 @@ __device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t c,
 // V (e4m3 [total, H, 128]) -> one [128 head-dim rows x 128 keys] block per key
 // tile and head: block (g * H + h) holds key tile g (tile_base numbering) of
 // head h, keys past the end of the sequence zero. In self-attention every
-// query tile is also a key tile, so one CTA per item of the forward queue
-// (its record names the head, the tile, the sequence start and tile base):
-// lane l takes keys 4 l .. 4 l + 3, warp w head-dim columns 16 w .. 16 w + 15;
-// each thread loads its four 16-byte key rows, transposes 4 x 4 byte blocks
-// in registers and writes 4 keys of 16 head-dim rows, so every warp store is
-// one contiguous 128-byte row of the block.
-__global__ void __launch_bounds__(256) vt_transpose_kernel(const uint8_t* __restrict__ v, const int4* items,
-                                                           const int4* item_seq, const int32_t* status, int heads,
-                                                           uint8_t* __restrict__ vt) {
+// query tile is also a key tile, so the forward queue's items (head, tile,
+// sequence start and tile base) name the blocks; a few CTAs per SM walk them.
+// Per item: the 16 KB tile is read from global memory whole rows at a time
+// (lane l of a warp reads 16-byte chunk l % 8 of row l / 8 + 4 w + 32 m) into
+// shared memory, chunk c of key row k at position c ^ (k / 4 % 8); then lane l
+// of warp w takes keys 4 l .. 4 l + 3 at head-dim columns 16 w .. 16 w + 15
+// (one 16-byte read per key, conflict-free under that swizzle), transposes
+// 4 x 4 byte blocks in registers and writes 4 keys of 16 head-dim rows, so
+// every warp store is one contiguous 128-byte row of the block.
+constexpr int kVtThreads = 256;
+__global__ void __launch_bounds__(kVtThreads) vt_transpose_kernel(const uint8_t* __restrict__ v, const int4* items,
+                                                                  const int4* item_seq, const int32_t* status,
+                                                                  int heads, uint8_t* __restrict__ vt) {
+  __shared__ __align__(16) uint8_t tile[kTile * kF8D];
   wait_prior_grid();
   allow_next_grid();
-  const int idx = blockIdx.x;
-  if (status[0] != JFA_OK || idx >= status[2]) return;
-  const int4 it = items[idx], sq = item_seq[idx];
-  const int h = it.y, j = it.z;        // head, tile of the sequence
-  const int s0 = sq.x, gt = sq.z + j;  // sequence start; tile index in tile_base numbering
-  const int rows = min(kTile, sq.y - kTile * j);  // valid keys of the tile
+  if (status[0] != JFA_OK) return;
+  const int n_items = status[2];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int k0 = 4 * lane, d0 = 16 * w;
-  uint4 r[4];
+  for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
+    const int4 it = items[idx], sq = item_seq[idx];
+    const int h = it.y, j = it.z;        // head, tile of the sequence
+    const int s0 = sq.x, gt = sq.z + j;  // sequence start; tile index in tile_base numbering
+    const int rows = min(kTile, sq.y - kTile * j);  // valid keys of the tile
+    const int c = lane & 7;
+    uint4 g[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    r[i] = make_uint4(0, 0, 0, 0);
-    if (k0 + i < rows)
-      r[i] = ptx::ld_nc_v4(v + ((static_cast<int64_t>(s0) + kTile * j + k0 + i) * heads + h) * kF8D + d0);
-  }
-  uint8_t* out = vt + (static_cast<int64_t>(gt) * heads + h) * kF8D * kTile + k0;
-  auto word = [](const uint4& x, int q) { return q == 0 ? x.x : (q == 1 ? x.y : (q == 2 ? x.z : x.w)); };
+    for (int m = 0; m < 4; ++m) {
+      const int k = (lane >> 3) + 4 * w + 32 * m;
+      g[m] = make_uint4(0, 0, 0, 0);
+      if (k < rows) g[m] = ptx::ld_nc_v4(v + ((static_cast<int64_t>(s0) + kTile * j + k) * heads + h) * kF8D + 16 * c);
+    }
+    __syncthreads();  // the previous item's reads of the tile are done
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {  // head-dim columns d0 + 4 q .. d0 + 4 q + 3
-    uint32_t t[4];
-    transpose4x4(word(r[0], q), word(r[1], q), word(r[2], q), word(r[3], q), t);
+    for (int m = 0; m < 4; ++m) {
+      const int k = (lane >> 3) + 4 * w + 32 * m;
+      *reinterpret_cast<uint4*>(tile + k * kF8D + ((c ^ ((k >> 2) & 7)) << 4)) = g[m];
+    }
+    __syncthreads();
+    const int k0 = 4 * lane, d0 = 16 * w;
+    uint4 r[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(d0 + 4 * q + e) * kTile) = t[e];
+    for (int i = 0; i < 4; ++i) {
+      const int k = k0 + i;
+      r[i] = *reinterpret_cast<const uint4*>(tile + k * kF8D + ((w ^ ((k >> 2) & 7)) << 4));
+    }
+    uint8_t* out = vt + (static_cast<int64_t>(gt) * heads + h) * kF8D * kTile + k0;
+    auto word = [](const uint4& x, int q) { return q == 0 ? x.x : (q == 1 ? x.y : (q == 2 ? x.z : x.w)); };
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // head-dim columns d0 + 4 q .. d0 + 4 q + 3
+      uint32_t t[4];
+      transpose4x4(word(r[0], q), word(r[1], q), word(r[2], q), word(r[3], q), t);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(d0 + 4 * q + e) * kTile) = t[e];
+    }
   }
 }
 
@@ -660,8 +683,12 @@ cudaError_t launch_fp8_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 cudaError_t launch_vt_transpose(const void* v, const int4* items, const int4* item_seq, const int32_t* status,
                                 int heads, int max_items, void* vt, cudaStream_t stream) {
-  return launch_after(vt_transpose_kernel, dim3(max_items), dim3(256), 0, stream, static_cast<const uint8_t*>(v), items,
-                      item_seq, static_cast<const int32_t*>(status), heads, static_cast<uint8_t*>(vt));
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  const int grid = std::max(1, std::min(max_items, 8 * sms));  // a few blocks per SM walk the items
+  return launch_after(vt_transpose_kernel, dim3(grid), dim3(kVtThreads), 0, stream, static_cast<const uint8_t*>(v),
+                      items, item_seq, static_cast<const int32_t*>(status), heads, static_cast<uint8_t*>(vt));
 }
 
 cudaError_t launch_fwd_fp8(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
