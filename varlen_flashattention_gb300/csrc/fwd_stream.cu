@@ -16,13 +16,13 @@
 // 16 MMAs of 128x128x16), so two warps share every row: warps 0-3 (group 0)
 // exponentiate key columns 0-63 of the score tile and warps 4-7 (group 1)
 // columns 64-127, each on its own TMEM lanes' quarter (warp w reads lanes
-// 32 (w % 4) ..). Both groups read the whole score row for the row maximum,
-// so they reach the same maximum and the same rescaling decision without
-// exchanging it. Each writes its half of P (bf16 pairs) over the first 32
-// TMEM columns of its own half of S, so a group writes P only after the other
-// group has read that half of the row (one mbarrier per warp quarter and S
-// buffer). Each group keeps the sum of its own half of the row; the two sums
-// meet in shared memory at the end of an item.
+// 32 (w % 4) ..). Each group reads only its own half of the score row and
+// publishes that half's maximum in the half's last TMEM column (one mbarrier
+// per warp quarter, group and S buffer); the other group reads it there, so
+// both reach the same row maximum and the same rescaling decision. Each
+// writes its half of P (bf16 pairs) over the first 32 TMEM columns of its own
+// half of S. Each group keeps the sum of its own half of the row; the two
+// sums meet in shared memory at the end of an item.
 //
 // Roles (448 threads): warps 0-7 softmax, warps 8-11 epilogue, warp 12 TMA
 // producer, warp 13 MMA issuer (the whole warp runs the loop, one elected
