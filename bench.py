@@ -510,6 +510,56 @@ def reference_arm(args):
     return 0
 
 
+# ---------------------------------------------------------------- per-role timeline
+
+def trace_timeline(args):
+    """One GEM-like step (causal off, sparsity 0.5, H 4, d 128) through the trace build: the
+    forward and the backward each recorded into a zeroed buffer after the warm-up steps, then
+    summarised per role in SM cycles (with the cycles-per-ns ratio the records themselves give)."""
+    os.environ["JFA_LIBRARY_VARIANT"] = "trace"  # before the package loads a library
+    import numpy as np
+    import torch
+    import varlen_flashattention_gb300 as jfa
+    from varlen_flashattention_gb300 import build as _build, trace
+    _build.build(variant="trace")
+    assert jfa.jfa_trace_compiled() == 1
+    device = torch.device("cuda", 0)
+    w = gem_workload(0, device, batch=args.batch)
+    bufs = alloc_bufs(jfa, w, device)
+    for _ in range(args.warmup):
+        run_step(jfa, w, bufs)
+    cap = 4096
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    buf = torch.zeros(trace.buffer_bytes(sms, cap), dtype=torch.uint8, device=device)
+    out = {}
+    for tag in ("fwd", "bwd"):
+        buf.zero_()
+        torch.cuda.synchronize()
+        jfa.jfa_trace_enable(buf, cap)
+        if tag == "fwd":
+            jfa.jfa_fwd(w["q"], w["k"], w["v"], w["offsets"], w["max_seqlen"], w["scale"], False, o=bufs["o"],
+                        lse=bufs["lse"], workspace=bufs["ws_f"])
+        else:
+            jfa.jfa_bwd(w["q"], w["k"], w["v"], bufs["o"], w["do"], bufs["lse"], w["offsets"], w["max_seqlen"],
+                        w["scale"], False, dq=bufs["dq"], dk=bufs["dk"], dv=bufs["dv"], workspace=bufs["ws_b"])
+        torch.cuda.synchronize()
+        jfa.jfa_trace_enable(None)
+        recs = trace.decode(buf.cpu().numpy(), cap)
+        full = int((recs["seq"] == cap - 1).sum())
+        mma = recs[recs["warp"] == (13 if tag == "fwd" else 9)]
+        rates = []  # SM cycles per ns over each CTA's MMA-warp records (clock64 is per SM)
+        for cta in np.unique(mma["cta"]):
+            m = mma[mma["cta"] == cta]
+            dt = float(m["gtime"].max() - m["gtime"].min())
+            if dt > 1e4:
+                rates.append(float(m["clock"].max() - m["clock"].min()) / dt)
+        out[tag] = {"summary": trace.summary_fwd(recs) if tag == "fwd" else trace.summary_bwd(recs),
+                    "counts": trace.counts(recs), "slots_full": full,
+                    "cycles_per_ns": float(np.median(rates)) if rates else None}
+    print(json.dumps({"trace_timeline": {"batch": args.batch, "tokens": w["total"], **out}}, indent=1), flush=True)
+    return 0
+
+
 # ---------------------------------------------------------------- main arm
 
 def main():
@@ -525,11 +575,16 @@ def main():
     ap.add_argument("--batch", type=int, default=1024, help="sequences per GPU (profiling runs use fewer)")
     ap.add_argument("--profile-decode", type=int, default=0, metavar="PAGE",
                     help="profiling run: the paged decode workload at this page size, 32 splits, a few calls")
+    ap.add_argument("--trace-timeline", action="store_true",
+                    help="per-role event trace of one GEM-like fwd+bwd step (--batch sequences) with the "
+                         "JFA_TRACE build of the library; prints per-role cycle statistics, no bench line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return reference_arm(args)
+    if args.trace_timeline:
+        return trace_timeline(args)
     if args.profile_decode:
         import torch
         import varlen_flashattention_gb300 as jfa

@@ -414,6 +414,30 @@ JFA_API jfa_status jfa_selftest_wait_timeout(int32_t budget_us, void* workspace,
  * code naming the wait or check that failed. */
 JFA_API jfa_status jfa_read_device_status(const void* workspace, cudaStream_t stream, int32_t* detail);
 
+/* Per-role event trace of the persistent kernels (the head_dim 128 forward
+ * of jfa_fwd / jfa_fwd_broadcast_q / jfa_fwd_varlen and every backward), for
+ * looking into the warp-specialised pipelines ("Cutting-edge isn't
+ * plug-and-play: customizing FA4 on B300", bug hunting: a producer/consumer
+ * deadlock). Only a library built with JFA_TRACE records; jfa_trace_compiled()
+ * returns 1 there and 0 otherwise, where jfa_trace_enable returns
+ * JFA_ERR_UNSUPPORTED and the kernels hold no trace code.
+ *  - buffer: device memory, 16-byte aligned, owned by the caller, of at least
+ *    SMs x 16 x records_per_warp x 32 bytes (SMs of the current device; else
+ *    JFA_ERR_INVALID_ARG); zero it before each call to be recorded.
+ *  - Layout: [CTA][warp slot 0..15][records_per_warp] records of 32 bytes:
+ *    uint64 clock64 (SM cycles), uint64 globaltimer (ns), uint32 event
+ *    (kernel << 16 | code: kernel 1 = forward, 2 = backward; the codes are
+ *    listed in varlen_flashattention_gb300/trace.py), uint32 argument (step or
+ *    item counter of the CTA), uint32 SM id, uint32 0. A warp's records are in
+ *    program order; the first all-zero record ends them; records past
+ *    records_per_warp are dropped.
+ *  - Each traced kernel launch writes from the start of every slot, so the
+ *    buffer holds the last one (for head_dim 192, the second head-axis pass).
+ *  - The setting is process-wide and applies to calls enqueued after it;
+ *    jfa_trace_enable(NULL, 0, 0) turns recording off. */
+JFA_API jfa_status jfa_trace_enable(void* buffer, size_t bytes, int32_t records_per_warp);
+JFA_API int32_t jfa_trace_compiled(void);
+
 /* Static string for a status code. */
 JFA_API const char* jfa_status_string(jfa_status status);
 

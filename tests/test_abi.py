@@ -227,3 +227,39 @@ def test_binding_rejects_cpu_tensors():
     q = torch.zeros(4, 1, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         jfa.jfa_fwd(q, q, q, torch.zeros(2, dtype=torch.int32), 4)
+
+
+def test_trace_entry_points_of_the_default_build(lib):
+    assert lib.jfa_trace_compiled() == 0
+    assert lib.jfa_trace_enable(None, 0, 0) == _abi.JFA_ERR_UNSUPPORTED
+    with pytest.raises(jfa.JfaError):
+        jfa.jfa_trace_enable(None)
+
+
+_VARIANT_PROBE = r"""
+import ctypes, sys
+from varlen_flashattention_gb300 import _abi
+lib = _abi.load()
+assert lib._name.endswith("libjfa_%s.so" % sys.argv[1]), lib._name
+print(lib.jfa_trace_compiled(), lib.jfa_trace_enable(None, 0, 0), lib.jfa_trace_enable(ctypes.c_void_p(4096), 16, 0))
+"""
+
+
+@pytest.mark.parametrize("variant", ["trace", "debug"])
+def test_debugging_builds_compile_and_export_the_abi(variant):
+    """Each debugging build compiles, loads in place of libjfa.so when JFA_LIBRARY_VARIANT names
+    it, exports every declared symbol, and answers the trace entry points for its build."""
+    from varlen_flashattention_gb300 import build
+    path = build.build(variant=variant)
+    vlib = ctypes.CDLL(path)
+    for n in _declared_functions():
+        assert hasattr(vlib, n), f"{n} not exported by {os.path.basename(path)}"
+    env = dict(os.environ, JFA_LIBRARY_VARIANT=variant)
+    r = subprocess.run(["python", "-c", _VARIANT_PROBE, variant], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    compiled, off, bad = (int(x) for x in r.stdout.split())
+    if variant == "trace":
+        assert (compiled, off, bad) == (1, _abi.JFA_OK, _abi.JFA_ERR_INVALID_ARG)
+    else:
+        assert (compiled, off, bad) == (0, _abi.JFA_ERR_UNSUPPORTED, _abi.JFA_ERR_UNSUPPORTED)

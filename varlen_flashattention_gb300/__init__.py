@@ -15,6 +15,8 @@ kernels; there is no CPU or PyTorch fallback.
     jfa_bwd_varlen        its backward -> (dQ, dK, dV)
     jfa_decode_smallq     paged split-KV decode of a few query tokens per sequence -> (O, LSE)
     jfa_fwd_fp8           jagged forward over FP8 (e4m3) inputs with per-tensor descales -> (O, LSE)
+    jfa_trace_enable      registers a per-role event trace buffer (JFA_TRACE builds; see trace.py)
+    jfa_trace_compiled    1 if the loaded library records traces
     jagged_attention      autograd wrapper of jfa_fwd / jfa_bwd
     varlen_attention      autograd wrapper of jfa_fwd_varlen / jfa_bwd_varlen
 """
@@ -32,6 +34,7 @@ __all__ = [
     "JfaError", "jfa_fwd", "jfa_bwd", "jfa_fwd_broadcast_q", "jfa_bwd_broadcast_q", "jfa_decode_splitkv",
     "jfa_read_device_status", "jagged_attention", "library", "jfa_fwd_varlen", "jfa_bwd_varlen",
     "varlen_attention", "jfa_decode_smallq", "jfa_selftest_wait_timeout", "jfa_fwd_fp8",
+    "jfa_trace_enable", "jfa_trace_compiled",
 ]
 
 
@@ -155,6 +158,24 @@ def jfa_selftest_wait_timeout(budget_us=20000, workspace=None, stream=None):
     st, detail = jfa_read_device_status(ws, stream)
     aborted = int(ws[16:20].view(torch.int32).item())
     return st, detail, aborted
+
+
+def jfa_trace_compiled():
+    """1 if the loaded library was built with JFA_TRACE (it records traces), else 0."""
+    return int(library().jfa_trace_compiled())
+
+
+def jfa_trace_enable(buffer, records_per_warp=1024):
+    """Registers `buffer` (a zeroed uint8 CUDA tensor of at least
+    trace.buffer_bytes(SMs, records_per_warp) bytes) for the per-role event
+    records of later calls; None turns recording off. Raises JfaError
+    (unsupported) unless the library was built with JFA_TRACE."""
+    if buffer is not None:
+        if not isinstance(buffer, torch.Tensor) or not buffer.is_cuda or not buffer.is_contiguous():
+            raise TypeError("buffer must be a contiguous CUDA tensor")
+        _check(library().jfa_trace_enable(_ptr(buffer), _nbytes(buffer), int(records_per_warp)), "jfa_trace_enable")
+    else:
+        _check(library().jfa_trace_enable(None, 0, 0), "jfa_trace_enable")
 
 
 def _finish(ws, check, stream, where):

@@ -11,6 +11,9 @@ import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libjfa.so")
+# A debugging build of the same sources to load instead ("trace" or "debug",
+# made by build.build(variant=...)); read once, at the first load.
+VARIANT_ENV = "JFA_LIBRARY_VARIANT"
 
 c_void_p = ctypes.c_void_p
 c_i32 = ctypes.c_int32
@@ -123,6 +126,8 @@ SIGNATURES = [
     ("jfa_decode_noalloc_status", [c_void_p, ctypes.POINTER(c_i32)], c_i32),
     ("jfa_read_device_status", [c_void_p, c_void_p, ctypes.POINTER(c_i32)], c_i32),
     ("jfa_selftest_wait_timeout", [c_i32, c_void_p, c_void_p], c_i32),
+    ("jfa_trace_enable", [c_void_p, ctypes.c_size_t, c_i32], c_i32),
+    ("jfa_trace_compiled", [], c_i32),
     ("jfa_status_string", [c_i32], ctypes.c_char_p),
     ("jfa_version", [], c_i32),
 ]
@@ -131,14 +136,20 @@ _lib = None
 
 
 def load() -> ctypes.CDLL:
-    """The loaded libjfa.so with typed entry points. Raises if it is missing."""
+    """The loaded libjfa.so (or the variant JFA_LIBRARY_VARIANT names) with
+    typed entry points. Raises if it is missing."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
+        variant = os.environ.get(VARIANT_ENV, "")
+        if variant and variant not in ("trace", "debug"):
+            raise RuntimeError(f"{VARIANT_ENV}={variant!r}: expected 'trace' or 'debug'")
+        path = os.path.join(_PKG, f"libjfa_{variant}.so") if variant else LIB_PATH
+        if not os.path.exists(path):
             raise RuntimeError(
-                f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
-                "(the CUDA library is required; there is no CPU fallback)")
-        lib = ctypes.CDLL(LIB_PATH)
+                f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+                "(or build.build(variant=...) for a debugging build; the CUDA library is required, "
+                "there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
         for name, argtypes, restype in SIGNATURES:
             fn = getattr(lib, name)
             fn.argtypes = argtypes

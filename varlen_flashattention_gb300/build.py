@@ -3,6 +3,12 @@
 Every translation unit under ``csrc/`` is compiled in parallel into
 ``_build/`` and linked into ``varlen_flashattention_gb300/libjfa.so``. A unit
 is recompiled only when it or a header is newer than its object file.
+
+Two variants of the same sources serve debugging (``build(variant=...)``):
+``trace`` (-DJFA_TRACE: per-role event records, libjfa_trace.so) and
+``debug`` (-DJFA_DEBUG: bounds checks of every tile load, libjfa_debug.so).
+They build into ``_build/<variant>/``; the package loads one of them instead
+of libjfa.so when JFA_LIBRARY_VARIANT names it.
 """
 from __future__ import annotations
 
@@ -18,6 +24,11 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libjfa.so")
+VARIANTS = {"trace": ["-DJFA_TRACE"], "debug": ["-DJFA_DEBUG"]}
+
+
+def lib_path(variant=None) -> str:
+    return LIB if not variant else os.path.join(PKG, f"libjfa_{variant}.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]
@@ -42,15 +53,19 @@ def _stale(src: str, obj: str, newest_header: float) -> bool:
     return os.path.getmtime(src) > t or newest_header > t
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
+def build(verbose: bool = False, force: bool = False, extra_flags=None, variant=None) -> str:
     """Compile and link; returns the path of the shared library."""
-    os.makedirs(BUILD, exist_ok=True)
+    if variant is not None and variant not in VARIANTS:
+        raise ValueError(f"unknown variant {variant!r} (known: {sorted(VARIANTS)})")
+    bdir = BUILD if variant is None else os.path.join(BUILD, variant)
+    lib = lib_path(variant)
+    os.makedirs(bdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     newest = max([os.path.getmtime(h) for h in _headers()] + [0.0])
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    flags = NVCC_FLAGS + VARIANTS.get(variant, []) + list(extra_flags or [])
     jobs = []
     for s in srcs:
-        obj = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(s)[:-3] + ".o")
         if force or _stale(s, obj, newest):
             jobs.append((s, obj))
 
@@ -69,17 +84,17 @@ def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
             list(ex.map(compile_one, jobs))
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
-    if jobs or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        cmd = [nvcc()] + ARCH + ["-shared", "-o", LIB] + objs
+    objs = [os.path.join(bdir, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    if jobs or not os.path.exists(lib) or any(os.path.getmtime(o) > os.path.getmtime(lib) for o in objs):
+        cmd = [nvcc()] + ARCH + ["-shared", "-o", lib] + objs
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    build(verbose="-v" in sys.argv, force="-f" in sys.argv)
-    print(LIB)
+    v = next((a for a in sys.argv[1:] if a in VARIANTS), None)
+    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv, variant=v))

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "jfa_internal.h"
+#include "trace.cuh"
 
 namespace jfa {
 
@@ -989,6 +990,37 @@ jfa_status jfa_fwd_fp8(const jfa_fwd_fp8_args* a, void* ws, size_t ws_bytes, cud
                                        a->heads, a->total, s_log2, a->v_descale, wait_budget_ns(), grid, stream);
   record(a->main_kernel_events, 1, stream);
   return cuda_status(e);
+}
+
+int32_t jfa_trace_compiled(void) {
+#ifdef JFA_TRACE
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+jfa_status jfa_trace_enable(void* buffer, size_t bytes, int32_t records_per_warp) {
+#ifdef JFA_TRACE
+  if (buffer == nullptr) {
+    jfa::set_trace_buffer(nullptr, 0, 0);
+    return JFA_OK;
+  }
+  if (records_per_warp < 1 || !aligned(buffer, 16)) return JFA_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return JFA_ERR_CUDA;
+  const size_t need = static_cast<size_t>(sms) * jfa::trace::kWarpSlots * static_cast<size_t>(records_per_warp) *
+                      jfa::trace::kRecordBytes;
+  if (bytes < need) return JFA_ERR_INVALID_ARG;
+  jfa::set_trace_buffer(buffer, records_per_warp, sms);
+  return JFA_OK;
+#else
+  (void)buffer;
+  (void)bytes;
+  (void)records_per_warp;
+  return JFA_ERR_UNSUPPORTED;
+#endif
 }
 
 jfa_status jfa_read_device_status(const void* ws, cudaStream_t stream, int32_t* detail) {

@@ -58,6 +58,7 @@
 
 #include "jfa_internal.h"
 #include "ptx.cuh"
+#include "trace.cuh"
 
 namespace jfa {
 
@@ -300,6 +301,8 @@ __global__ void __launch_bounds__(448, 1)
   const int n_work = p.status[2] * p.n_chunks;
   int32_t* status = p.status;
   const uint64_t budget = p.budget_ns;
+  trace::Writer tw;  // records only in a JFA_TRACE build
+  tw.open(status, warp);
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
@@ -320,6 +323,10 @@ __global__ void __launch_bounds__(448, 1)
       auto load_qdo = [&](const BwdItem& I, int ii) -> bool {
         int g, i;
         bwd_step(I, ii, g, i);
+        if (!JFA_TILE_OK(i >= I.i0 && kTile * i < I.Lq && g >= 0 && I.hq0 + g < p.heads, ctl, status,
+                         kSiteCheckBwdQ))
+          return false;
+        tw.rec(trace::kBwd, trace::kBwdQLoad, pos);
         const int qcol = (I.hq0 + g) * D;
         const int ca = slice_col<D, DC>(p, I) >> 6;  // first atom of the item's slice
         const int64_t rbase = I.row_base + static_cast<int64_t>(g) * p.pad_tiles * kTile;
@@ -385,6 +392,9 @@ __global__ void __launch_bounds__(448, 1)
       int v = next_item(blockIdx.x, I);
       if (v < n_work) ok = load_qdo(I, 0);
       while (ok && v < n_work) {
+        if (!(ok = JFA_TILE_OK(I.t >= 0 && kTile * I.t < I.Lk && I.h >= 0 && I.h < p.kv_heads, ctl, status,
+                               kSiteCheckBwdKV)))
+          break;
         // V first: the previous item's last dP^T released it before its last dQ released K
         if (!(ok = ptx::mbar_wait(v_empty, (kitem & 1) ^ 1, ctl, status, kSiteBwdProdKV, budget))) break;
         ptx::mbar_arrive_expect_tx(v_full, Lay::kTileBytes);
@@ -396,6 +406,7 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int a = 0; a < Lay::kAtoms; ++a)
           ptx::tma_load_2d(smem + Lay::kOffK + a * 16384, &tm_k, k_full, I.h * D + 64 * a, I.kv_row0);
+        tw.rec(trace::kBwd, trace::kBwdKVLoad, kitem);
         for (int ii = 1; ok && ii < I.nq; ++ii) ok = load_qdo(I, ii);
         if (!ok) break;
         BwdItem N;
@@ -447,6 +458,7 @@ __global__ void __launch_bounds__(448, 1)
       const int ca = slice_col<D, DC>(p, I) >> 6;  // first atom of the item's slice
       if (!(ok = wait(k_full, kitem & 1, kSiteBwdMmaKV))) break;
       ptx::tc_fence_after();
+      if (lane == 0) tw.rec(trace::kBwd, trace::kBwdItem, kitem);
       // S^T(x) = K Q^T. With two Q/dO stages it is issued for the first query
       // tile of the item at the start of the tile and for every later one right
       // after dS^T of the previous tile, so the softmax of tile x + 1 overlaps
@@ -494,10 +506,12 @@ __global__ void __launch_bounds__(448, 1)
         const uint32_t q_addr = ptx::smem_u32(smem + Lay::kOffQ + st * Lay::kTileBytes);
         const uint32_t do_addr = ptx::smem_u32(smem + Lay::kOffDO + st * Lay::kTileBytes);
         if constexpr (kSt == 1) {
+          if (lane == 0) tw.rec(trace::kBwd, trace::kBwdSIssue, x);
           if (!(ok = atoms_mma(Lay::kColS, k_addr, q_addr, q_full, q_empty, s_full))) break;
           // dP^T = V dO^T into the columns dQ of the previous tile used
           if (x > 0 && !(ok = wait(dq_free, (x - 1) & 1, kSiteBwdMmaDQFree))) break;
           if (ii == 0 && !(ok = wait(v_full, kitem & 1, kSiteBwdMmaKV))) break;
+          if (lane == 0) tw.rec(trace::kBwd, trace::kBwdDPIssue, x);
           if (!(ok = atoms_mma(Lay::kColDP, v_addr, do_addr, do_full, do_empty, dp_full))) break;
           if (ii + 1 == I.nq) {  // the item's last dP^T was V's last reader
             if (ptx::elect_one()) ptx::mma_commit(v_empty);
@@ -507,6 +521,7 @@ __global__ void __launch_bounds__(448, 1)
           if (ii == 0) {
             if (!(ok = wait_q(pos))) break;
             ptx::tc_fence_after();
+            if (lane == 0) tw.rec(trace::kBwd, trace::kBwdSIssue, x);
             if (ptx::elect_one()) issue_s(st);
             __syncwarp();
           }
@@ -515,6 +530,7 @@ __global__ void __launch_bounds__(448, 1)
           if (x > 0 && !(ok = wait(dq_free, (x - 1) & 1, kSiteBwdMmaDQFree))) break;
           if (ii == 0 && !(ok = wait(v_full, kitem & 1, kSiteBwdMmaKV))) break;
           ptx::tc_fence_after();
+          if (lane == 0) tw.rec(trace::kBwd, trace::kBwdDPIssue, x);
           if (ptx::elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -531,6 +547,7 @@ __global__ void __launch_bounds__(448, 1)
         if (ii == 0 && kitem > 0 && !(ok = wait(acc_free, (kitem - 1) & 1, kSiteBwdMmaAccFree))) break;
         if (!(ok = wait(p_full, x & 1, kSiteBwdMmaP))) break;
         ptx::tc_fence_after();
+        if (lane == 0) tw.rec(trace::kBwd, trace::kBwdDVIssue, x);
         if (ptx::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -546,6 +563,10 @@ __global__ void __launch_bounds__(448, 1)
         if (next_s && !(ok = wait_q(pos + 1))) break;
         if (!(ok = wait(ds_full, x & 1, kSiteBwdMmaDS))) break;
         ptx::tc_fence_after();
+        if (lane == 0) {
+          tw.rec(trace::kBwd, trace::kBwdDQDKIssue, x);
+          if (next_s && kStageInDO) tw.rec(trace::kBwd, trace::kBwdSIssue, x + 1);  // issued between dQ and dK
+        }
         if (ptx::elect_one()) {
           // dQ(tile) = dS K[:, slice] into the dP^T columns (the softmax has read dP^T)
           auto mma_dq = [&]() {
@@ -643,6 +664,7 @@ __global__ void __launch_bounds__(448, 1)
         const int c_hi = r < rk ? rq : 0;
         if (!(ok = ptx::mbar_wait(s_full, x & 1, ctl, status, kSiteBwdSoftS, budget))) break;
         ptx::tc_fence_after();
+        if (lane == 0) tw.rec(trace::kBwd, trace::kBwdPBegin, x);
         // P^T = 2^(S^T * scale * log2e - lse2[q]), two chunks of 32 query columns
         {
           uint32_t sv[2][32];
@@ -694,6 +716,7 @@ __global__ void __launch_bounds__(448, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(p_full);
+        if (lane == 0) tw.rec(trace::kBwd, trace::kBwdPEnd, x);
         // dS^T = P^T * (dP^T - delta[q])
         if (!dp_ready && !(ok = ptx::mbar_wait(dp_full, x & 1, ctl, status, kSiteBwdSoftDP, budget))) break;
         ptx::tc_fence_after();
@@ -702,6 +725,7 @@ __global__ void __launch_bounds__(448, 1)
           if (!kStageInDO && !(ok = ptx::mbar_wait(stage_free, (x - 1) & 1, ctl, status, kSiteBwdSoftDP, budget)))
             break;
         }
+        if (lane == 0) tw.rec(trace::kBwd, trace::kBwdDSBegin, x);
 #pragma unroll 1
         for (int k = 0; k < 2; ++k) {  // two chunks of 32 query columns
           uint32_t dp[32];
@@ -744,6 +768,7 @@ __global__ void __launch_bounds__(448, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ds_full);
+        if (lane == 0) tw.rec(trace::kBwd, trace::kBwdDSEnd, x);
         ++pos;
       }
     }
@@ -773,6 +798,7 @@ __global__ void __launch_bounds__(448, 1)
         bwd_step(I, ii, g, i);
         if (!(ok = ptx::mbar_wait(dq_full, x & 1, ctl, status, kSiteBwdDQ, budget))) break;
         ptx::tc_fence_after();
+        if (lane == 0) tw.rec(trace::kBwd, trace::kBwdDQBegin, x);
         // dQ leaves TMEM a staging round (a buffer-full of 32-column fp32 boxes,
         // 16 KB each, 128B swizzle) at a time: in this tile's dO stage buffer
         // with two stages (then released to the producer), in the dS buffer
@@ -851,11 +877,13 @@ __global__ void __launch_bounds__(448, 1)
         }
         if (issuer) ptx::bulk_wait_read0();
         if (!ok) break;
+        if (lane == 0) tw.rec(trace::kBwd, trace::kBwdDQEnd, x);
         if (issuer && !(kStageInDO && ii + 1 == I.nq)) ptx::mbar_arrive(kStageInDO ? do_empty + st : stage_free);
       }
       if (!ok) break;
       if (!(ok = ptx::mbar_wait(acc_full, kitem & 1, ctl, status, kSiteBwdEpi, budget))) break;
       ptx::tc_fence_after();
+      if (lane == 0) tw.rec(trace::kBwd, trace::kBwdAccBegin, kitem);
       const bool issuer = warp == 10 && lane == 0;
       const uint32_t st_last = (x - 1) % kSt;  // stage of the item's last query tile
       const bool full_tile = I.Lk - kTile * I.t >= kTile;
@@ -951,6 +979,7 @@ __global__ void __launch_bounds__(448, 1)
           ptx::mbar_arrive(do_empty + st_last);
         }
       }
+      if (lane == 0) tw.rec(trace::kBwd, trace::kBwdAccEnd, kitem);
       ++kitem;
     }
     if (warp == 10 && lane == 0) ptx::bulk_wait0();  // every reduce-add has completed

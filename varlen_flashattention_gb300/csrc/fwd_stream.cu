@@ -35,6 +35,7 @@
 
 #include "jfa_internal.h"
 #include "ptx.cuh"
+#include "trace.cuh"
 
 namespace jfa {
 
@@ -275,6 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* status = p.status;
   const uint64_t budget = p.budget_ns;
   const int cta = blockIdx.x, n_ctas = gridDim.x;
+  trace::Writer tw;  // records only in a JFA_TRACE build
+  tw.open(status, warp);
   // The next item of a consumer role. Causal: entry k of the item ring (every
   // lane of the warp reads it, lane 0 gives the entry back). Otherwise the
   // role's own round-robin share: st_idx / st_pre hold the next index and its
@@ -314,6 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto on_q = [&](const FwdStreamItem& I) -> bool {
+        if (!JFA_TILE_OK(I.t >= 0 && kTile * I.t < I.Lq && I.h >= 0 && I.h < p.heads, ctl, status, kSiteCheckFwdQ))
+          return false;
+        tw.rec(trace::kFwdStream, trace::kFwdQLoad, kq);
         const uint32_t qs = kq % kQS, qround = kq / kQS;
         if (!ptx::mbar_wait(q_empty + qs, (qround & 1) ^ 1, ctl, status, kSiteFwdProdQ, budget)) return false;
         ptx::mbar_arrive_expect_tx(q_full + qs, Lay::kQBytes);
@@ -326,6 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // K and V tiles: two 64-column atoms of 128 rows each
       auto on_kv = [&](const CUtensorMap* map, const FwdStreamItem& I, int j) -> bool {
+        if (!JFA_TILE_OK(j >= 0 && kTile * j < I.Lk && I.hk >= 0, ctl, status, kSiteCheckFwdKV)) return false;
+        tw.rec(trace::kFwdStream, trace::kFwdKVLoad, pos);
         uint32_t slot;
         if (!next_slot(slot)) return false;
         uint8_t* dst = smem + Lay::kOffSlots + slot * Lay::kKVBytes;
@@ -403,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t k_desc =
           ptx::sdesc_sw128(ptx::smem_u32(smem + Lay::kOffSlots + slot * Lay::kKVBytes), 16, 1024);
       const uint32_t d_tmem = tmem + ((x & 1) ? Lay::kColS1 : Lay::kColS0);
+      if (lane == 0) tw.rec(trace::kFwdStream, trace::kFwdSIssue, x);
       if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < kD2 / 16; ++kk) {
@@ -448,6 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::sdesc_sw128(ptx::smem_u32(smem + Lay::kOffSlots + slot * Lay::kKVBytes), 16384, 1024);
         const uint32_t p_tmem = tmem + ((x & 1) ? Lay::kColS1 : Lay::kColS0);
         const uint32_t o_tmem = tmem + (ob ? Lay::kColO1 : Lay::kColO0);
+        if (lane == 0) tw.rec(trace::kFwdStream, trace::kFwdPVIssue, x);
         if (ptx::elect_one()) {
           // keys 16 kk ..: group 0's P (keys 0-63) at S columns 0-31, group 1's
           // (keys 64-127) at S columns 64-95
@@ -494,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!s_ready && !(ok = ptx::mbar_wait(s_full + (x & 1), (x >> 1) & 1, ctl, status, kSiteFwdSoftS, budget)))
           break;
         ptx::tc_fence_after();
+        if (lane == 0) tw.rec(trace::kFwdStream, trace::kFwdSoftBegin, x);
         // keys j*128 + c with c >= lim are masked (past the sequence, or past
         // the bottom-right aligned diagonal: key j visible iff j <= qi + delta)
         const int lim = CAUSAL ? min(qi + 1 + I.delta - kTile * j, I.Lk - kTile * j) : I.Lk - kTile * j;
@@ -623,6 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(p_full + (x & 1));
+        if (lane == 0) tw.rec(trace::kFwdStream, trace::kFwdSoftEnd, x);
       }
       ++kq;
     }
@@ -662,6 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       w = w && ptx::mbar_wait(ml_full + ob, (kq >> 1) & 1, ctl, status, kSiteFwdEpi, budget);
       if (!w) break;
       ptx::tc_fence_after();
+      if (lane == 0) tw.rec(trace::kFwdStream, trace::kFwdEpiBegin, kq);
       const float2 st = ml[ob * kTile + r];
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ml_empty + ob);
@@ -712,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++n_st;
       }
       if (row_ok) p.lse[I.lse0 + r] = (st.x + log2f(st.y)) * kLn2;
+      if (lane == 0) tw.rec(trace::kFwdStream, trace::kFwdEpiEnd, kq);
       ++kq;
     }
     if (issuer) ptx::bulk_wait0();  // every O store has completed

@@ -84,6 +84,11 @@ enum WaitSite : int32_t {
   kSiteBwdDQ = 231,
   kSiteBwdEpi = 241,
   kSiteBwdDrain = 251,
+  // checks of a debug build (JFA_ERR_BAD_INPUT): a tile outside its sequence or head
+  kSiteCheckFwdQ = 161,
+  kSiteCheckFwdKV = 162,
+  kSiteCheckBwdKV = 261,
+  kSiteCheckBwdQ = 262,
   kSiteQueueOffsets = 301,
   kSiteDecodeTable = 401,
   kSiteSelftestInput = 901,  // the self-test's first stage (its input never arrives)
@@ -222,6 +227,11 @@ cudaError_t launch_decode_general(const DecodeLaunch& a, float* part_o, float* p
 // Clears a call's status block (a kernel, not a memset, so that the call's next
 // kernel can start as its programmatic dependent).
 cudaError_t launch_status_clear(int32_t* status, cudaStream_t stream);
+#ifdef JFA_TRACE
+// Registers the trace buffer that later calls' status blocks carry (nullptr: off):
+// `ctas` CTA slots of 16 warp slots of `records_per_warp` records.
+void set_trace_buffer(void* buffer, int32_t records_per_warp, int32_t ctas);
+#endif
 // Argument checks of jfa_decode_splitkv (scalars, alignment), without the workspace.
 jfa_status check_decode_args(const jfa_decode_args* a);
 

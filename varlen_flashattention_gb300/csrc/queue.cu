@@ -420,6 +420,37 @@ cudaError_t launch_queue(const QueueParams& p, cudaStream_t stream) {
 
 // A call's status block cleared by one small block; the call's next kernel may
 // be scheduled at once (it waits for this one before reading the block).
+#ifdef JFA_TRACE
+namespace {
+std::atomic<uint64_t> g_trace_addr{0};
+std::atomic<int32_t> g_trace_cap{0};
+std::atomic<int32_t> g_trace_ctas{0};
+}  // namespace
+
+void set_trace_buffer(void* buffer, int32_t records_per_warp, int32_t ctas) {
+  g_trace_cap.store(buffer ? records_per_warp : 0);
+  g_trace_ctas.store(buffer ? ctas : 0);
+  g_trace_addr.store(reinterpret_cast<uint64_t>(buffer));
+}
+
+// Also writes the registered trace buffer into status words 16-19, where the
+// persistent kernels of the call read it.
+__global__ void status_clear_kernel(int32_t* status, uint64_t trace_addr, int32_t trace_cap, int32_t trace_ctas) {
+  allow_next_grid();
+  int32_t w = 0;
+  if (threadIdx.x == 16) w = static_cast<int32_t>(static_cast<uint32_t>(trace_addr));
+  if (threadIdx.x == 17) w = static_cast<int32_t>(static_cast<uint32_t>(trace_addr >> 32));
+  if (threadIdx.x == 18) w = trace_cap;
+  if (threadIdx.x == 19) w = trace_ctas;
+  status[threadIdx.x] = w;
+}
+
+cudaError_t launch_status_clear(int32_t* status, cudaStream_t stream) {
+  status_clear_kernel<<<1, kStatusBytes / 4, 0, stream>>>(status, g_trace_addr.load(), g_trace_cap.load(),
+                                                        g_trace_ctas.load());
+  return cudaGetLastError();
+}
+#else
 __global__ void status_clear_kernel(int32_t* status) {
   allow_next_grid();
   status[threadIdx.x] = 0;
@@ -429,5 +460,6 @@ cudaError_t launch_status_clear(int32_t* status, cudaStream_t stream) {
   status_clear_kernel<<<1, kStatusBytes / 4, 0, stream>>>(status);
   return cudaGetLastError();
 }
+#endif
 
 }  // namespace jfa
