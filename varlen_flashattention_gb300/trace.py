@@ -104,28 +104,32 @@ def _paired(g, begin, end):
 def summary_bwd(recs: np.ndarray) -> dict:
     """Per-role cycle statistics of the backward kernel over all CTAs:
     step: cycles between consecutive dQ/dK issues of the MMA warp within an item;
-    item_gap: from the last dQ/dK issue of an item to the next item's first S^T issue;
-    k_wait: from the last dQ/dK issue of an item to the next item's K arrival;
+    item_gap: from the last dQ/dK issue of an item to the next item's first S^T issue
+    (0 when that S^T was issued right after the last dQ);
+    k_wait: from the last dQ/dK issue of an item to the MMA warp's start of the next item
+    (its K has arrived);
     p_pass, ds_pass: softmax warps' P^T and dS passes; p_to_ds: from P^T stored to
     the start of the dS pass (waiting for dP^T or the dS buffer);
     dq_drain, acc_drain: epilogue's dQ and dK / dV drains."""
     step, gap, kwait, pp, dsp, p2d, dqd, accd = [], [], [], [], [], [], [], []
     for (cta, warp), g in _groups(recs[recs["kernel"] == 2]).items():
         if warp == 9:  # the MMA warp in program order: item (K arrived), S^T, dP^T, dV, dQ/dK issues
-            item, last_item, last_dqdk, gap_open = -1, -1, None, False
+            item, last_item, last_dqdk, last_x = -1, -1, None, None
+            s_at, bounds = {}, []
             for code, clk, arg in zip(g["code"].tolist(), g["clock"].tolist(), g["arg"].tolist()):
                 if code == 3:
                     item = arg
                     if last_dqdk is not None:
                         kwait.append(clk - last_dqdk)
-                        gap_open = True
-                elif code == 4 and gap_open:
-                    gap.append(clk - last_dqdk)
-                    gap_open = False
+                        bounds.append((last_dqdk, last_x + 1))
+                elif code == 4:
+                    s_at.setdefault(arg, clk)
                 elif code == 7:
                     if last_dqdk is not None and last_item == item:
                         step.append(clk - last_dqdk)
-                    last_dqdk, last_item = clk, item
+                    last_dqdk, last_item, last_x = clk, item, arg
+            # the next item's first S^T may be recorded before its item event (issued early)
+            gap += [s_at[x1] - c for c, x1 in bounds if x1 in s_at]
         elif warp < 8:
             pp += _paired(g, 8, 9)
             dsp += _paired(g, 10, 11)
