@@ -392,9 +392,8 @@ __global__ void __launch_bounds__(448, 1)
       int v = next_item(blockIdx.x, I);
       if (v < n_work) ok = load_qdo(I, 0);
       while (ok && v < n_work) {
-        if (!(ok = JFA_TILE_OK(I.t >= 0 && kTile * I.t < I.Lk && I.h >= 0 && I.h < p.kv_heads, ctl, status,
-                               kSiteCheckBwdKV)))
-          break;
+        ok = JFA_TILE_OK(I.t >= 0 && kTile * I.t < I.Lk && I.h >= 0 && I.h < p.kv_heads, ctl, status, kSiteCheckBwdKV);
+        if (!ok) break;
         // V first: the previous item's last dP^T released it before its last dQ released K
         if (!(ok = ptx::mbar_wait(v_empty, (kitem & 1) ^ 1, ctl, status, kSiteBwdProdKV, budget))) break;
         ptx::mbar_arrive_expect_tx(v_full, Lay::kTileBytes);
