@@ -4,9 +4,9 @@ with JFA_LIBRARY_VARIANT set, so that the package loads libjfa_trace.so / libjfa
 trace: forward and backward of a jagged batch with tracing on; every role records one event
        per step or item (counts derived from the lengths), each warp's cycle stamps never
        decrease, and the results still match the fp64 oracle.
-debug: the parity cases of the persistent kernels (self-attention at head_dim 128 and 192,
-       causal and not; varlen GQA; broadcast-Q) with every tile load checked; the status is OK
-       and the results match the oracle.
+debug: the parity cases of the persistent kernels (self-attention at head_dim 64, 128 and 192,
+       causal and not; varlen GQA; broadcast-Q; the FP8 forward) with every tile load checked;
+       the status is OK and the results match the oracle.
 Exits non-zero on the first failure.
 """
 from __future__ import annotations
@@ -21,7 +21,7 @@ import torch
 import oracle.attention as orc
 import varlen_flashattention_gb300 as jfa
 from varlen_flashattention_gb300 import inputs, trace
-from tests.parity import check_grad, check_lse, check_o, np64
+from tests.parity import check_grad, check_lse, check_o, fp8_error_bound, np64
 
 LENGTHS = [300, 128, 1, 513, 77, 256, 0, 129]
 
@@ -105,7 +105,7 @@ def run_trace():
 
 def run_debug():
     assert jfa.jfa_trace_compiled() == 0
-    for head_dim, causal, chunk in ((128, False, 0), (128, True, 0), (192, False, 0), (192, True, 64)):
+    for head_dim, causal, chunk in ((128, False, 0), (128, True, 0), (64, True, 0), (192, False, 0), (192, True, 64)):
         d = _case(LENGTHS, 2, head_dim, seed=head_dim + causal)
         _check_self(d, causal, _self(d, causal, chunk), f"debug build d={head_dim} causal={causal} chunk={chunk}")
     # varlen GQA, bottom-right causal
@@ -138,6 +138,19 @@ def run_debug():
     check_grad(np64(dq), dQ, "dQ broadcast debug build")
     check_grad(np64(dk), dK, "dK broadcast debug build")
     check_grad(np64(dv), dV, "dV broadcast debug build")
+    # FP8 forward (its own kernel and V transpose pass), within the derived bound
+    for causal in (False, True):
+        d8 = inputs.fp8_from_lengths(LENGTHS, 2, seed=17)
+        q, k, v, off = (d8[x].cuda() for x in ("q", "k", "v", "offsets"))
+        o, lse = jfa.jfa_fwd_fp8(q, k, v, off, d8["max_seqlen"], d8["q_descale"], d8["k_descale"], d8["v_descale"],
+                                 d8["scale"], causal, check=True)
+        q8, k8, v8 = (d8[x].numpy() for x in ("q", "k", "v"))
+        qd, kd, vd = d8["q_descale"], d8["k_descale"], d8["v_descale"]
+        O, L = orc.attention_forward_fp8(q8, k8, v8, d8["offsets"].numpy(), d8["scale"], causal, qd, kd, vd)
+        check_lse(np64(lse), L, f"LSE fp8 debug build causal={causal}")
+        bound = fp8_error_bound(orc.e4m3_decode(q8) * qd, orc.e4m3_decode(k8) * kd, orc.e4m3_decode(v8) * vd,
+                                d8["offsets"].numpy(), d8["scale"], causal, O)
+        assert np.all(np.abs(np64(o) - O) <= bound), f"O fp8 debug build causal={causal} outside the bound"
     print("debug ok")
 
 

@@ -30,6 +30,7 @@
 
 #include "jfa_internal.h"
 #include "ptx.cuh"
+#include "trace.cuh"
 
 namespace jfa {
 
@@ -253,6 +254,10 @@ __global__ void __launch_bounds__(192, 1)
       for (int idx = claim(); ok && idx >= 0; idx = claim()) {
         const FwdItem I = fwd_item<CAUSAL>(p, idx);
         if (I.n_kv == 0) continue;
+        // debug builds: the Q tile and every K/V tile start inside their sequences and heads
+        if (!JFA_TILE_OK(I.t >= 0 && kTile * I.t < I.Lq && I.h >= 0 && I.h < p.heads, ctl, status, kSiteCheckFwdQ))
+          break;
+        if (!JFA_TILE_OK(I.n_kv > 0 && kTile * (I.n_kv - 1) < I.Lk && I.hk >= 0, ctl, status, kSiteCheckFwdKV)) break;
         if (!ptx::mbar_wait(q_empty, (kq & 1) ^ 1, ctl, status, kSiteFwdProdQ, budget)) break;
         ptx::mbar_arrive_expect_tx(q_full, Lay::kTileBytes);
 #pragma unroll

@@ -35,6 +35,7 @@
 
 #include "jfa_internal.h"
 #include "ptx.cuh"
+#include "trace.cuh"
 
 namespace jfa {
 
@@ -244,6 +245,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         return true;
       };
       auto on_q = [&](const Fp8Item& I) -> bool {
+        // debug builds: the Q tile and every K/V tile start inside their sequences and heads
+        if (!JFA_TILE_OK(I.t >= 0 && kTile * I.t < I.L && I.h >= 0 && I.h < p.heads, ctl, status, kSiteCheckFwdQ))
+          return false;
+        if (!JFA_TILE_OK(I.n_kv > 0 && kTile * (I.n_kv - 1) < I.L && I.vt0 >= 0, ctl, status, kSiteCheckFwdKV))
+          return false;
         const uint32_t qs = kq % kQS, qround = kq / kQS;
         if (!ptx::mbar_wait(q_empty + qs, (qround & 1) ^ 1, ctl, status, kSiteFwdProdQ, budget)) return false;
         ptx::mbar_arrive_expect_tx(q_full + qs, kF8TileBytes);
