@@ -363,23 +363,49 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
     }
   }
   if (one_cost) {
-    // every warp writes whole sequences, one record per lane, so each store
-    // instruction covers 32 consecutive records
+    // Each thread works out its own sequence's records once (first position,
+    // count, cost word, bounds); then every warp writes the records of its 32
+    // sequences one sequence at a time, the values broadcast from the owning
+    // lane and one record per lane, so each store instruction covers up to 32
+    // consecutive records and no lane repeats the per-sequence arithmetic (a
+    // warp per sequence with every lane recomputing it made this loop
+    // instruction-bound, ~3/4 of the kernel).
     __syncthreads();
-    for (int b = warp; b < min(p.batch, kQueueLenCache); b += kWarps) {
-      const int2 L = seq_lens(p, s_len, s_lenk, b);
-      const int nt = item_tiles(p, L.x, L.y);
-      const int k = nt > 0 ? item_cost(p, L.x, L.y, 0) : 0;
-      if (!(fits && nt > 0 && k >= kmin)) continue;
-      const int tb = tbase(b);
-      const int4 seq = var ? make_int4(row0(b), L.x, krow0(b), L.y) : make_int4(row0(b), L.x, tb, 0);
-      const int w = p.mode == kQueueVarBwd ? tb : k;
-      const int64_t first = static_cast<int64_t>(s_first[b]) * p.heads;
-      const int n = nt * p.heads;  // records tile-major, heads inner: record e = (tile e / H, head e % H)
-      for (int e = lane; e < n; e += 32) {
-        const int t = e / p.heads;
-        p.items[first + e] = make_int4(b, e - t * p.heads, t, w);
-        if (p.item_seq) p.item_seq[first + e] = seq;
+    const int n_seq = min(p.batch, kQueueLenCache);
+    const int t_lane = lane / p.heads, h_lane = lane - t_lane * p.heads;  // record `lane` of a sequence
+    for (int b0 = 0; b0 < n_seq; b0 += kQThreads) {
+      const int b = b0 + tid;
+      int first = 0, n = 0, w = 0;
+      int4 seq = make_int4(0, 0, 0, 0);
+      if (b < n_seq) {
+        const int2 L = seq_lens(p, s_len, s_lenk, b);
+        const int nt = item_tiles(p, L.x, L.y);
+        const int k = nt > 0 ? item_cost(p, L.x, L.y, 0) : 0;
+        if (fits && nt > 0 && k >= kmin) {
+          const int tb = tbase(b);
+          seq = var ? make_int4(row0(b), L.x, krow0(b), L.y) : make_int4(row0(b), L.x, tb, 0);
+          w = p.mode == kQueueVarBwd ? tb : k;
+          first = s_first[b];
+          n = nt * p.heads;  // records tile-major, heads inner: record e = (tile e / H, head e % H)
+        }
+      }
+      for (int j = 0; j < 32; ++j) {
+        const int nj = __shfl_sync(0xffffffffu, n, j);
+        if (nj == 0) continue;
+        const int bj = b0 + 32 * warp + j;
+        const int64_t fj = static_cast<int64_t>(__shfl_sync(0xffffffffu, first, j)) * p.heads;
+        const int wj = __shfl_sync(0xffffffffu, w, j);
+        const int4 sj = make_int4(__shfl_sync(0xffffffffu, seq.x, j), __shfl_sync(0xffffffffu, seq.y, j),
+                                  __shfl_sync(0xffffffffu, seq.z, j), __shfl_sync(0xffffffffu, seq.w, j));
+        for (int e = lane; e < nj; e += 32) {
+          int t = t_lane, h = h_lane;
+          if (e != lane) {
+            t = e / p.heads;
+            h = e - t * p.heads;
+          }
+          p.items[fj + e] = make_int4(bj, h, t, wj);
+          if (p.item_seq) p.item_seq[fj + e] = sj;
+        }
       }
     }
   }
