@@ -510,6 +510,50 @@ def reference_arm(args):
     return 0
 
 
+# ---------------------------------------------------------------- profiling runs of the other workloads
+
+def profile_config(args):
+    """warmup + steps calls of one reduced workload, for ncu captures (inputs still larger than L2)."""
+    import torch
+    import varlen_flashattention_gb300 as jfa
+    from varlen_flashattention_gb300 import build as _build, inputs
+    _build.build()
+    dev = torch.device("cuda", 0)
+    n = args.warmup + args.steps
+    if args.profile_config == "causal192":
+        lens = torch.full((1,), 8192, dtype=torch.int32)
+        off = inputs.offsets_from_lengths(lens).to(dev)
+        q, k, v, do = (inputs.randn_bf16_device((8192, 16, 192), 300 + i, dev) for i in range(4))
+        sc = 1 / math.sqrt(192)
+        for _ in range(n):
+            o, lse = jfa.jfa_fwd(q, k, v, off, 8192, sc, True)
+            jfa.jfa_bwd(q, k, v, o, do, lse, off, 8192, sc, True)
+        what = "dense causal d=192, 1 x 8192, 16 heads"
+    elif args.profile_config == "bcast":
+        g = torch.Generator().manual_seed(0)
+        lk = inputs.uniform_lengths(128, 16, 2048, g)
+        off = inputs.offsets_from_lengths(lk).to(dev)
+        T = int(lk.sum())
+        q = inputs.randn_bf16_device((256, 4, 128), 201, dev)
+        k = inputs.randn_bf16_device((T, 4, 128), 202, dev)
+        v = inputs.randn_bf16_device((T, 4, 128), 203, dev)
+        do = inputs.randn_bf16_device((128, 256, 4, 128), 204, dev)
+        mx, sc = int(lk.max()), 1 / math.sqrt(128)
+        for _ in range(n):
+            o, lse = jfa.jfa_fwd_broadcast_q(q, k, v, off, mx, sc)
+            jfa.jfa_bwd_broadcast_q(q, k, v, o, do, lse, off, mx, sc)
+        what = f"broadcast-Q, 128 sequences, {T} keys"
+    else:
+        w = gem_workload(0, dev, batch=256)
+        q8, k8, v8 = (inputs.fp8_quantize(w[x].float())[0] for x in ("q", "k", "v"))
+        for _ in range(n):
+            jfa.jfa_fwd_fp8(q8, k8, v8, w["offsets"], w["max_seqlen"], 0.01, 0.01, 0.01)
+        what = f"FP8 GEM-like forward, batch 256, {w['total']} tokens"
+    torch.cuda.synchronize()
+    print(f"profile run: {what}, {n} calls")
+    return 0
+
+
 # ---------------------------------------------------------------- per-role timeline
 
 def trace_timeline(args):
@@ -575,6 +619,10 @@ def main():
     ap.add_argument("--batch", type=int, default=1024, help="sequences per GPU (profiling runs use fewer)")
     ap.add_argument("--profile-decode", type=int, default=0, metavar="PAGE",
                     help="profiling run: the paged decode workload at this page size, 32 splits, a few calls")
+    ap.add_argument("--profile-config", default="", choices=["", "causal192", "bcast", "fp8"],
+                    help="profiling run of one more workload, reduced to a few GB: dense causal d=192 (1 x 8192, "
+                         "16 heads) fwd+bwd, broadcast-Q (Q 256 x 4 x 128 over 128 sequences) fwd+bwd, or the "
+                         "FP8 GEM-like forward (batch 256); warmup + steps calls, no JSON line")
     ap.add_argument("--trace-timeline", action="store_true",
                     help="per-role event trace of one GEM-like fwd+bwd step (--batch sequences) with the "
                          "JFA_TRACE build of the library; prints per-role cycle statistics, no bench line")
@@ -585,6 +633,8 @@ def main():
         return reference_arm(args)
     if args.trace_timeline:
         return trace_timeline(args)
+    if args.profile_config:
+        return profile_config(args)
     if args.profile_decode:
         import torch
         import varlen_flashattention_gb300 as jfa
