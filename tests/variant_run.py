@@ -79,7 +79,9 @@ def run_trace():
     f = trace.counts(recs["fwd"])
     want_f = {"fwd_stream.q_load": items, "fwd_stream.kv_load": 2 * steps, "fwd_stream.s_issue": steps,
               "fwd_stream.pv_issue": steps, "fwd_stream.soft_begin": 8 * steps, "fwd_stream.soft_end": 8 * steps,
-              "fwd_stream.epi_begin": 4 * items, "fwd_stream.epi_end": 4 * items}
+              "fwd_stream.epi_begin": 4 * items, "fwd_stream.epi_end": 4 * items,
+              "fwd_stream.soft_loaded": 8 * steps, "fwd_stream.soft_pub": 8 * steps, "fwd_stream.soft_exp": 8 * steps,
+              "fwd_stream.soft_max": 8 * steps}
     assert f == want_f, f"forward event counts {f} != {want_f}"
     b = trace.counts(recs["bwd"])
     want_b = {"bwd.kv_load": items, "bwd.q_load": steps, "bwd.item": items, "bwd.s_issue": steps,

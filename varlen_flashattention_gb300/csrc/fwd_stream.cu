@@ -525,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::reg_fence32(sa[1]);
         mask(sa[0], c_own);
         mask(sa[1], c_own + 32);
+        if (lane == 0) tw.rec(trace::kFwdStream, trace::kFwdSoftLoaded, x);
         float mx8[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
@@ -547,6 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(half_max + ((x & 1) * 2 + g) * 4 + quarter);
+        if (lane == 0) tw.rec(trace::kFwdStream, trace::kFwdSoftPub, x);
         uint64_t* other = half_max + ((x & 1) * 2 + (1 - g)) * 4 + quarter;
         auto other_max = [&]() -> float {  // after `other` has completed
           ptx::tc_fence_after();
@@ -582,11 +584,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j == 0) {
           if (!(ok = ptx::mbar_wait(other, (x >> 1) & 1, ctl, status, kSiteFwdSoftS, budget))) break;
           m = fmaxf(hmax, other_max()) * sl;
+          if (lane == 0) tw.rec(trace::kFwdStream, trace::kFwdSoftMax, x);
           lsum = exps(m);
+          if (lane == 0) tw.rec(trace::kFwdStream, trace::kFwdSoftExp, x);
         } else {
           lsum = exps(m);
+          if (lane == 0) tw.rec(trace::kFwdStream, trace::kFwdSoftExp, x);
           if (!(ok = ptx::mbar_wait(other, (x >> 1) & 1, ctl, status, kSiteFwdSoftS, budget))) break;
           const float mnew = fmaxf(hmax, other_max()) * sl;
+          if (lane == 0) tw.rec(trace::kFwdStream, trace::kFwdSoftMax, x);
           // O is rescaled only when the running max grows by more than 2^8;
           // otherwise the old max stays the reference and P stays below 2^8.
           const bool need = mnew > m + 8.0f;

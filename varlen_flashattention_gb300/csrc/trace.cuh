@@ -51,6 +51,10 @@ enum FwdEvent : uint32_t {
   kFwdSoftEnd = 6,     // softmax: P of the step stored (x)
   kFwdEpiBegin = 7,    // epilogue: O of an item complete (item)
   kFwdEpiEnd = 8,      // epilogue: O and LSE of the item written (item)
+  kFwdSoftLoaded = 9,  // softmax: the group's half of S in registers (x)
+  kFwdSoftPub = 10,    // softmax: the half's maximum published (x)
+  kFwdSoftExp = 11,    // softmax: exponentials taken (the first time) (x)
+  kFwdSoftMax = 12,    // softmax: the other half's maximum read (x)
 };
 enum BwdEvent : uint32_t {
   kBwdKVLoad = 1,      // producer: K and V of an item issued (item)

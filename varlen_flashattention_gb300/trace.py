@@ -20,7 +20,7 @@ RECORD_BYTES = 32
 KERNELS = {1: "fwd_stream", 2: "bwd"}
 EVENTS = {
     1: {1: "q_load", 2: "kv_load", 3: "s_issue", 4: "pv_issue", 5: "soft_begin", 6: "soft_end",
-        7: "epi_begin", 8: "epi_end"},
+        7: "epi_begin", 8: "epi_end", 9: "soft_loaded", 10: "soft_pub", 11: "soft_exp", 12: "soft_max"},
     2: {1: "kv_load", 2: "q_load", 3: "item", 4: "s_issue", 5: "dp_issue", 6: "dv_issue", 7: "dqdk_issue",
         8: "p_begin", 9: "p_end", 10: "ds_begin", 11: "ds_end", 12: "dq_begin", 13: "dq_end",
         14: "acc_begin", 15: "acc_end"},
@@ -101,6 +101,14 @@ def _paired(g, begin, end):
     return [ends[a] - c for a, c in zip(a_b.tolist(), c_b.tolist()) if a in ends]
 
 
+def _paired_next(g, end, begin):
+    """Gaps from an event `end` of step x to the event `begin` of step x + 1 of one warp."""
+    a_e, c_e = _code(g, end)
+    a_b, c_b = _code(g, begin)
+    starts = dict(zip(a_b.tolist(), c_b.tolist()))
+    return [starts[a + 1] - c for a, c in zip(a_e.tolist(), c_e.tolist()) if a + 1 in starts]
+
+
 def summary_bwd(recs: np.ndarray) -> dict:
     """Per-role cycle statistics of the backward kernel over all CTAs:
     step: cycles between consecutive dQ/dK issues of the MMA warp within an item;
@@ -146,8 +154,13 @@ def summary_fwd(recs: np.ndarray) -> dict:
     step: cycles between consecutive P V issues of the MMA warp;
     soft: softmax warps from S complete to P stored; s_to_soft: from the S
     issue to the start of that step's softmax (S in flight or queued);
-    epi: epilogue from O complete to O and LSE written."""
+    epi: epilogue from O complete to O and LSE written;
+    soft_load / soft_max_pub / soft_exp / soft_other_max / soft_tail: the softmax step's phases
+    (S read into registers; this half's maximum folded and published; the exponentials; waiting
+    for and reading the other half's maximum; the rest up to P stored), soft_idle: from P stored
+    to the next step's S complete."""
     step, soft, s2s, epi = [], [], [], []
+    phases = {k: [] for k in ("load", "max_pub", "exp", "other_max", "tail", "idle")}
     groups = _groups(recs[recs["kernel"] == 1])
     s_issue = {}
     for (cta, warp), g in groups.items():
@@ -159,9 +172,30 @@ def summary_fwd(recs: np.ndarray) -> dict:
     for (cta, warp), g in groups.items():
         if warp < 8:
             soft += _paired(g, 5, 6)
+            phases["load"] += _paired(g, 5, 9)
+            phases["max_pub"] += _paired(g, 9, 10)
+            phases["idle"] += _paired_next(g, 6, 5)
+            a_e, c_e = _code(g, 11)
+            a_m, c_m = _code(g, 12)
+            a_p, c_p = _code(g, 10)
+            a_z, c_z = _code(g, 6)
+            e_at, m_at, p_at, z_at = (dict(zip(a.tolist(), c.tolist())) for a, c in
+                                      ((a_e, c_e), (a_m, c_m), (a_p, c_p), (a_z, c_z)))
+            for x_, ce in e_at.items():
+                if x_ in m_at and x_ in p_at and x_ in z_at:
+                    if ce <= m_at[x_]:  # exponentials first (speculative), then the other maximum
+                        phases["exp"].append(ce - p_at[x_])
+                        phases["other_max"].append(m_at[x_] - ce)
+                        phases["tail"].append(z_at[x_] - m_at[x_])
+                    else:               # first step of an item: the other maximum first
+                        phases["other_max"].append(m_at[x_] - p_at[x_])
+                        phases["exp"].append(ce - m_at[x_])
+                        phases["tail"].append(z_at[x_] - ce)
             s_at = s_issue.get(cta, {})
             a_b, c_b = _code(g, 5)
             s2s += [c - s_at[a] for a, c in zip(a_b.tolist(), c_b.tolist()) if a in s_at]
         elif 8 <= warp < 12:
             epi += _paired(g, 7, 8)
-    return {"step": _stats(step), "soft": _stats(soft), "s_to_soft": _stats(s2s), "epi": _stats(epi)}
+    out = {"step": _stats(step), "soft": _stats(soft), "s_to_soft": _stats(s2s), "epi": _stats(epi)}
+    out.update({f"soft_{k}": _stats(v) for k, v in phases.items()})
+    return out
