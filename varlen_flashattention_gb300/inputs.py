@@ -43,7 +43,9 @@ def _randn_bf16(shape, g: torch.Generator) -> torch.Tensor:
 def randn_bf16_device(shape, seed: int, device) -> torch.Tensor:
     """N(0,1) values rounded to bf16, drawn directly on `device` with its own
     seeded generator. Used where only the shape and distribution matter (the
-    benchmark); parity tests use the CPU draws above."""
+    benchmark) and where a CPU draw would be too large (the test past 2^31
+    elements, which copies its sampled sequences back for the oracle); other
+    parity tests use the CPU draws above."""
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
     return torch.randn(*shape, generator=g, dtype=torch.float32, device=device).to(torch.bfloat16)
