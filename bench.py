@@ -436,10 +436,19 @@ def measure_extra(jfa, device, peaks, tc_peak):
     o8, l8 = jfa.jfa_fwd_fp8(q8, k8, v8, w["offsets"], w["max_seqlen"], 0.01, 0.01, 0.01)
     t8 = time_events(lambda: jfa.jfa_fwd_fp8(q8, k8, v8, w["offsets"], w["max_seqlen"], 0.01, 0.01, 0.01, o=o8,
                                              lse=l8), 10, 3)
-    out["fp8_fwd_gem"] = {"fwd_tflops": attn_flops(w["lengths"], 4, 128, False, "fwd") / (t8 * 1e-3) / 1e12,
-                          "fwd_ms": t8, "workload": "GEM-like s=0.5 forward, e4m3 Q/K/V (V transposed per tile in "
-                                                    "the call), bf16 O"}
-    del w, q8, k8, v8, o8, l8
+    # the same with V quantized by the caller straight into the blocks the forward reads
+    # (jfa_fp8_quantize_v, outside the timed calls like the caller's quantization of Q, K, V)
+    vt = jfa.jfa_fp8_quantize_v(w["v"], w["offsets"], w["max_seqlen"], 0.01)
+    t8v = time_events(lambda: jfa.jfa_fwd_fp8(q8, k8, None, w["offsets"], w["max_seqlen"], 0.01, 0.01, 0.01, o=o8,
+                                              lse=l8, vt=vt), 10, 3)
+    tq = time_events(lambda: jfa.jfa_fp8_quantize_v(w["v"], w["offsets"], w["max_seqlen"], 0.01, vt=vt), 10, 3)
+    fl8 = attn_flops(w["lengths"], 4, 128, False, "fwd")
+    out["fp8_fwd_gem"] = {"fwd_tflops": fl8 / (t8 * 1e-3) / 1e12, "fwd_ms": t8,
+                          "fwd_tflops_vt": fl8 / (t8v * 1e-3) / 1e12, "fwd_ms_vt": t8v, "quantize_v_ms": tq,
+                          "workload": "GEM-like s=0.5 forward, e4m3 Q/K/V (fwd_ms: V transposed per tile in the "
+                                      "call; fwd_ms_vt: V given as the blocks jfa_fp8_quantize_v writes from bf16 V, "
+                                      "quantize_v_ms), bf16 O"}
+    del w, q8, k8, v8, o8, l8, vt
     for sp in (0.1, 0.9):
         w = gem_workload(0, device, sparsity=sp)
         bufs = alloc_bufs(jfa, w, device)

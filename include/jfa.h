@@ -295,7 +295,31 @@ typedef struct {
   void* o;                   /* out: bf16 [total, heads, 128] */
   float* lse;                /* out: fp32 [heads, total] */
   void* main_kernel_events;  /* optional cudaEvent_t[2] */
+  const void* vt;            /* optional: V already in the forward's key-contiguous layout, as
+                                jfa_fp8_quantize_v writes it for the same offsets and heads (v is
+                                then not read and may be NULL, and the call makes no pass over V) */
 } jfa_fwd_fp8_args;
+
+/* V for the FP8 forward, quantized straight into the layout the forward reads
+ * ([INF] PR 2109; the layout is this library's). P V takes V as a K-major
+ * operand (keys contiguous), so jfa_fwd_fp8 rewrites an e4m3 [total, heads,
+ * 128] V on every call as one [128 dims x 128 keys] block per 128-key tile of
+ * each sequence and head. A caller that quantizes V from bf16 anyway can write
+ * those blocks instead: this call reads bf16 V and writes
+ *   block (tile_base[b] + t) * heads + h, byte [d][k] = e4m3(V[s_b + 128 t + k, h, d] * inv)
+ * with inv = 1 / v_descale rounded to fp32, e4m3 rounding to nearest even and
+ * saturating at +-448, tile_base[b] = sum over b' < b of ceil(L_b' / 128), and
+ * zero bytes for keys past the end of the sequence; jfa_fwd_fp8 with vt set
+ * (and the same v_descale) then reads them. vt must hold
+ * jfa_fp8_vt_bytes(batch, heads, total) bytes (16-byte aligned); head_dim must
+ * be 128. */
+typedef struct {
+  const void* v;             /* bf16 [total, heads, 128] */
+  const int32_t* offsets;    /* int32 [batch+1], device */
+  int32_t batch, heads, head_dim, max_seqlen, total;
+  float v_descale;           /* > 0 */
+  void* vt;                  /* out: e4m3 blocks */
+} jfa_fp8_quantize_v_args;
 
 /* ------------------------------------------------------------------ small-query paged decode
  * Paged split-KV GQA decode with q_len >= 1 query tokens per sequence ([INF]
@@ -342,6 +366,9 @@ JFA_API size_t jfa_varlen_fwd_workspace_size(const jfa_varlen_fwd_args* args);
 JFA_API size_t jfa_varlen_bwd_workspace_size(const jfa_varlen_bwd_args* args);
 JFA_API size_t jfa_decode_smallq_workspace_size(const jfa_decode_smallq_args* args);
 JFA_API size_t jfa_fwd_fp8_workspace_size(const jfa_fwd_fp8_args* args);
+JFA_API size_t jfa_fp8_quantize_v_workspace_size(const jfa_fp8_quantize_v_args* args);
+/* Bytes of the V blocks for a batch (an upper bound: (ceil(total/128) + batch) x heads x 16384). */
+JFA_API size_t jfa_fp8_vt_bytes(int32_t batch, int32_t heads, int32_t total);
 
 /* Entry points. `workspace` is device memory of at least the size above,
  * 256-byte aligned; its contents on entry do not matter. */
@@ -361,6 +388,8 @@ JFA_API jfa_status jfa_decode_smallq(const jfa_decode_smallq_args* args, void* w
                              cudaStream_t stream);
 JFA_API jfa_status jfa_fwd_fp8(const jfa_fwd_fp8_args* args, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream);
+JFA_API jfa_status jfa_fp8_quantize_v(const jfa_fp8_quantize_v_args* args, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
 
 /* Paged split-KV decode that allocates nothing. The pages have no
  * counterpart for this entry point; it exists for callers that cannot

@@ -27,6 +27,7 @@ STRUCTS = {
     "jfa_varlen_bwd_args": _abi.VarlenBwdArgs,
     "jfa_decode_smallq_args": _abi.DecodeSmallqArgs,
     "jfa_fwd_fp8_args": _abi.FwdFp8Args,
+    "jfa_fp8_quantize_v_args": _abi.Fp8QuantizeVArgs,
 }
 
 
@@ -263,3 +264,18 @@ def test_debugging_builds_compile_and_export_the_abi(variant):
         assert (compiled, off, bad) == (1, _abi.JFA_OK, _abi.JFA_ERR_INVALID_ARG)
     else:
         assert (compiled, off, bad) == (0, _abi.JFA_ERR_UNSUPPORTED, _abi.JFA_ERR_UNSUPPORTED)
+
+
+def test_fp8_quantize_v_validation(lib):
+    """jfa_fp8_quantize_v checks its arguments on the host; jfa_fp8_vt_bytes sizes the blocks."""
+    assert lib.jfa_fp8_vt_bytes(3, 2, 300) == (3 + 3) * 2 * 16384  # ceil(300/128) + batch tiles per head
+    assert lib.jfa_fp8_vt_bytes(-1, 2, 300) == 0 and lib.jfa_fp8_vt_bytes(3, 0, 300) == 0
+    ok = dict(v=None, offsets=None, batch=0, heads=2, head_dim=128, max_seqlen=0, total=0, v_descale=1.0, vt=None)
+    ws = ctypes.c_void_p(256)
+    assert lib.jfa_fp8_quantize_v(ctypes.byref(_abi.Fp8QuantizeVArgs(**{**ok, "head_dim": 64})), ws, 4096,
+                                  None) == _abi.JFA_ERR_UNSUPPORTED
+    for bad in ({"v_descale": 0.0}, {"v_descale": float("inf")}, {"v_descale": 1e-45}, {"batch": -1},
+                {"heads": 0}, {"total": -1}):
+        a = _abi.Fp8QuantizeVArgs(**{**ok, **bad})
+        assert lib.jfa_fp8_quantize_v(ctypes.byref(a), ws, 4096, None) == _abi.JFA_ERR_INVALID_ARG, bad
+    assert lib.jfa_fp8_quantize_v(None, ws, 4096, None) == _abi.JFA_ERR_INVALID_ARG

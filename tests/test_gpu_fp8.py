@@ -75,3 +75,57 @@ def test_fp8_descales_scale_the_output():
     o3, l3 = jfa.jfa_fwd_fp8(q, k, v, off, 200, 1.0, 2.0, 1.0, 0.025, check=True)
     assert torch.equal(o2, (2 * o1.float()).to(torch.bfloat16)) and torch.equal(l1, l2)
     assert torch.equal(o3, o1) and torch.equal(l3, l1)
+
+
+def _vt_reference(v_bf16, offsets, heads, inv):
+    """The V blocks jfa_fp8_quantize_v writes, built on the CPU: e4m3(v * inv) with torch's
+    round-to-nearest conversion, block (tile_base[b] + t) * H + h holding [d][key] of key tile t."""
+    codes = (v_bf16.float() * torch.tensor(inv, dtype=torch.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
+    off = [int(x) for x in offsets]
+    blocks = []
+    for b in range(len(off) - 1):
+        L = off[b + 1] - off[b]
+        for t in range((L + 127) // 128):
+            rows = min(128, L - 128 * t)
+            for h in range(heads):
+                blk = torch.zeros((128, 128), dtype=torch.uint8)
+                blk[:, :rows] = codes[off[b] + 128 * t:off[b] + 128 * t + rows, h, :].T
+                blocks.append(blk)
+    return torch.stack(blocks).reshape(-1) if blocks else torch.zeros(0, dtype=torch.uint8)
+
+
+def test_fp8_quantize_v_layout_bit_exact():
+    """jfa_fp8_quantize_v: every byte of every block equals the CPU quantization placed by the
+    documented layout (zeros past the end of a sequence)."""
+    g = torch.Generator().manual_seed(64)
+    lengths = torch.tensor(EDGE, dtype=torch.int32)
+    d = inputs.jagged_from_lengths(lengths, 2, 128, g)
+    v = d["v"]
+    descale = float(v.float().abs().max()) / 440.0
+    inv = float(np.float32(1.0) / np.float32(descale))
+    vt = jfa.jfa_fp8_quantize_v(v.cuda(), d["offsets"].cuda(), d["max_seqlen"], descale, check=True)
+    ref = _vt_reference(v, d["offsets"], 2, inv)
+    got = vt.cpu()[:ref.numel()]
+    assert torch.equal(got, ref), f"{int((got != ref).sum())} of {ref.numel()} bytes differ"
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_from_quantized_v_blocks(causal):
+    """jfa_fwd_fp8 reading the blocks of jfa_fp8_quantize_v (no pass over V in the call) gives
+    bit for bit the outputs of the call that takes the same e4m3 V and transposes it itself."""
+    g = torch.Generator().manual_seed(65)
+    lengths = inputs.uniform_lengths(24, 1, 1024, g)
+    d = inputs.jagged_from_lengths(lengths, 4, 128, g)
+    qd = kd = 0.02
+    vd = float(d["v"].float().abs().max()) / 440.0
+    q8 = (d["q"].float() / qd).clamp(-440, 440).to(torch.float8_e4m3fn).view(torch.uint8).cuda()
+    k8 = (d["k"].float() / kd).clamp(-440, 440).to(torch.float8_e4m3fn).view(torch.uint8).cuda()
+    inv = torch.tensor(float(np.float32(1.0) / np.float32(vd)), dtype=torch.float32)
+    v8 = (d["v"].float() * inv).to(torch.float8_e4m3fn).view(torch.uint8).cuda()
+    off = d["offsets"].cuda()
+    o1, l1 = jfa.jfa_fwd_fp8(q8, k8, v8, off, d["max_seqlen"], qd, kd, vd, d["scale"], causal, check=True)
+    vt = jfa.jfa_fp8_quantize_v(d["v"].cuda(), off, d["max_seqlen"], vd, check=True)
+    o2, l2 = jfa.jfa_fwd_fp8(q8, k8, None, off, d["max_seqlen"], qd, kd, vd, d["scale"], causal, check=True, vt=vt)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)

@@ -15,6 +15,7 @@ kernels; there is no CPU or PyTorch fallback.
     jfa_bwd_varlen        its backward -> (dQ, dK, dV)
     jfa_decode_smallq     paged split-KV decode of a few query tokens per sequence -> (O, LSE)
     jfa_fwd_fp8           jagged forward over FP8 (e4m3) inputs with per-tensor descales -> (O, LSE)
+    jfa_fp8_quantize_v    bf16 V -> e4m3 V in the layout jfa_fwd_fp8 reads (its vt argument)
     jfa_trace_enable      registers a per-role event trace buffer (JFA_TRACE builds; see trace.py)
     jfa_trace_compiled    1 if the loaded library records traces
     jagged_attention      autograd wrapper of jfa_fwd / jfa_bwd
@@ -34,7 +35,7 @@ __all__ = [
     "JfaError", "jfa_fwd", "jfa_bwd", "jfa_fwd_broadcast_q", "jfa_bwd_broadcast_q", "jfa_decode_splitkv",
     "jfa_read_device_status", "jagged_attention", "library", "jfa_fwd_varlen", "jfa_bwd_varlen",
     "varlen_attention", "jfa_decode_smallq", "jfa_selftest_wait_timeout", "jfa_fwd_fp8",
-    "jfa_trace_enable", "jfa_trace_compiled",
+    "jfa_trace_enable", "jfa_trace_compiled", "jfa_fp8_quantize_v",
 ]
 
 
@@ -299,12 +300,17 @@ def jfa_bwd_broadcast_q(q, k, v, o, dout, lse, kv_offsets, max_seqlen_k, scale=N
 
 
 def jfa_fwd_fp8(q, k, v, offsets, max_seqlen, q_descale, k_descale, v_descale, scale=None, causal=False, o=None,
-                lse=None, workspace=None, stream=None, events=None, check=False):
+                lse=None, workspace=None, stream=None, events=None, check=False, vt=None):
     """Jagged forward over FP8 inputs. q, k, v: e4m3 codes [total, H, 128] (torch.uint8 or
     torch.float8_e4m3fn); byte x of q stands for e4m3(x) * q_descale (likewise k, v).
+    vt (optional): V as jfa_fp8_quantize_v wrote it for these offsets and heads; v is then
+    not read (it may be None) and the call makes no pass over V.
     Returns O bf16 [total, H, 128] and LSE fp32 [H, total]."""
     qkv = []
     for n, t in (("q", q), ("k", k), ("v", v)):
+        if n == "v" and t is None and vt is not None:
+            qkv.append(None)
+            continue
         if isinstance(t, torch.Tensor) and t.dtype == torch.float8_e4m3fn:
             t = t.view(torch.uint8)
         _need(t, n, torch.uint8, 3)
@@ -312,23 +318,44 @@ def jfa_fwd_fp8(q, k, v, offsets, max_seqlen, q_descale, k_descale, v_descale, s
     q, k, v = qkv
     total, H, d = q.shape
     _need(k, "k", torch.uint8, q.shape)
-    _need(v, "v", torch.uint8, q.shape)
+    if v is not None:
+        _need(v, "v", torch.uint8, q.shape)
     _need_offsets(offsets, "offsets")
+    if vt is not None:
+        _need(vt, "vt", torch.uint8, (int(library().jfa_fp8_vt_bytes(offsets.numel() - 1, H, total)),))
     if o is not None:
         _need(o, "o", torch.bfloat16, q.shape)
     if lse is not None:
         _need(lse, "lse", torch.float32, (H, total))
-    dev = _device(q=q, k=k, v=v, offsets=offsets, o=o, lse=lse)
+    dev = _device(q=q, k=k, v=v, offsets=offsets, o=o, lse=lse, vt=vt)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty((total, H, d), dtype=torch.bfloat16, device=dev) if o is None else o
     lse = torch.empty((H, total), dtype=torch.float32, device=dev) if lse is None else lse
     a = _abi.FwdFp8Args(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), offsets.numel() - 1, H, d, int(max_seqlen), total,
                         scale, int(bool(causal)), float(q_descale), float(k_descale), float(v_descale), _ptr(o),
-                        _ptr(lse), None)
+                        _ptr(lse), None, _ptr(vt))
     ev, _keep = _events(events)
     a.main_kernel_events = ev
     _run("jfa_fwd_fp8", "jfa_fwd_fp8_workspace_size", a, dev, workspace, stream, check)
     return o, lse
+
+
+def jfa_fp8_quantize_v(v, offsets, max_seqlen, v_descale, vt=None, workspace=None, stream=None, check=False):
+    """bf16 V [total, H, 128] -> e4m3(v / v_descale) in the blocks jfa_fwd_fp8 reads (see
+    include/jfa.h): returns the uint8 tensor of jfa_fp8_vt_bytes(batch, H, total) bytes, to
+    pass as jfa_fwd_fp8(..., vt=...)."""
+    _need(v, "v", torch.bfloat16, 3)
+    total, H, d = v.shape
+    _need_offsets(offsets, "offsets")
+    nbytes = int(library().jfa_fp8_vt_bytes(offsets.numel() - 1, H, total))
+    if vt is not None:
+        _need(vt, "vt", torch.uint8, (nbytes,))
+    dev = _device(v=v, offsets=offsets, vt=vt)
+    vt = torch.empty(nbytes, dtype=torch.uint8, device=dev) if vt is None else vt
+    a = _abi.Fp8QuantizeVArgs(_ptr(v), _ptr(offsets), offsets.numel() - 1, H, d, int(max_seqlen), total,
+                              float(v_descale), _ptr(vt))
+    _run("jfa_fp8_quantize_v", "jfa_fp8_quantize_v_workspace_size", a, dev, workspace, stream, check)
+    return vt
 
 
 # ---------------------------------------------------------------- varlen / GQA

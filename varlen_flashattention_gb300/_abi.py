@@ -99,7 +99,13 @@ class FwdFp8Args(ctypes.Structure):
     _fields_ = [("q", c_void_p), ("k", c_void_p), ("v", c_void_p), ("offsets", c_void_p),
                 ("batch", c_i32), ("heads", c_i32), ("head_dim", c_i32), ("max_seqlen", c_i32), ("total", c_i32),
                 ("scale", c_f32), ("causal", c_i32), ("q_descale", c_f32), ("k_descale", c_f32),
-                ("v_descale", c_f32), ("o", c_void_p), ("lse", c_void_p), ("main_kernel_events", c_void_p)]
+                ("v_descale", c_f32), ("o", c_void_p), ("lse", c_void_p), ("main_kernel_events", c_void_p),
+                ("vt", c_void_p)]
+
+
+class Fp8QuantizeVArgs(ctypes.Structure):
+    _fields_ = [("v", c_void_p), ("offsets", c_void_p), ("batch", c_i32), ("heads", c_i32), ("head_dim", c_i32),
+                ("max_seqlen", c_i32), ("total", c_i32), ("v_descale", c_f32), ("vt", c_void_p)]
 
 
 # (name, argtypes, restype) of every exported symbol declared in include/jfa.h
@@ -113,6 +119,8 @@ SIGNATURES = [
     ("jfa_varlen_bwd_workspace_size", [ctypes.POINTER(VarlenBwdArgs)], ctypes.c_size_t),
     ("jfa_decode_smallq_workspace_size", [ctypes.POINTER(DecodeSmallqArgs)], ctypes.c_size_t),
     ("jfa_fwd_fp8_workspace_size", [ctypes.POINTER(FwdFp8Args)], ctypes.c_size_t),
+    ("jfa_fp8_quantize_v_workspace_size", [ctypes.POINTER(Fp8QuantizeVArgs)], ctypes.c_size_t),
+    ("jfa_fp8_vt_bytes", [c_i32, c_i32, c_i32], ctypes.c_size_t),
     ("jfa_fwd", [ctypes.POINTER(FwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_bwd", [ctypes.POINTER(BwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_fwd_broadcast_q", [ctypes.POINTER(BcastFwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
@@ -122,6 +130,7 @@ SIGNATURES = [
     ("jfa_bwd_varlen", [ctypes.POINTER(VarlenBwdArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_decode_smallq", [ctypes.POINTER(DecodeSmallqArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_fwd_fp8", [ctypes.POINTER(FwdFp8Args), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
+    ("jfa_fp8_quantize_v", [ctypes.POINTER(Fp8QuantizeVArgs), c_void_p, ctypes.c_size_t, c_void_p], c_i32),
     ("jfa_decode_splitkv_noalloc", [ctypes.POINTER(DecodeArgs), c_void_p], c_i32),
     ("jfa_decode_noalloc_status", [c_void_p, ctypes.POINTER(c_i32)], c_i32),
     ("jfa_read_device_status", [c_void_p, c_void_p, ctypes.POINTER(c_i32)], c_i32),

@@ -216,11 +216,11 @@ Layout var_layout(int64_t batch, int64_t q_heads, int64_t kv_heads, int64_t tota
 }
 
 // FP8 forward: the self-attention forward layout plus the transposed V blocks
-// (one [128 x 128] byte block per key tile and head).
-Layout fp8_layout(int64_t batch, int64_t heads, int64_t total, size_t* vt_off) {
+// (one [128 x 128] byte block per key tile and head) unless the caller brings them.
+Layout fp8_layout(int64_t batch, int64_t heads, int64_t total, size_t* vt_off, bool own_vt = true) {
   Layout L = self_layout(batch, heads, total, 128, false);
   *vt_off = L.bytes;
-  L.bytes = align_up(L.bytes + static_cast<size_t>(L.pad_tiles) * heads * 128 * 128, 256);
+  if (own_vt) L.bytes = align_up(L.bytes + static_cast<size_t>(L.pad_tiles) * heads * 128 * 128, 256);
   return L;
 }
 
@@ -932,7 +932,53 @@ jfa_status jfa_selftest_wait_timeout(int32_t budget_us, void* ws, cudaStream_t s
 size_t jfa_fwd_fp8_workspace_size(const jfa_fwd_fp8_args* a) {
   if (!a) return 0;
   size_t vt_off = 0;
-  return fp8_layout(a->batch, a->heads, a->total, &vt_off).bytes;
+  return fp8_layout(a->batch, a->heads, a->total, &vt_off, a->vt == nullptr).bytes;
+}
+
+size_t jfa_fp8_vt_bytes(int32_t batch, int32_t heads, int32_t total) {
+  if (batch < 0 || heads < 1 || total < 0) return 0;
+  return static_cast<size_t>(max_tiles(total, batch)) * heads * 128 * 128;
+}
+
+size_t jfa_fp8_quantize_v_workspace_size(const jfa_fp8_quantize_v_args* a) {
+  if (!a) return 0;
+  return self_layout(a->batch, a->heads, a->total, 128, false).bytes;
+}
+
+jfa_status jfa_fp8_quantize_v(const jfa_fp8_quantize_v_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!a) return JFA_ERR_INVALID_ARG;
+  if (a->batch < 0 || a->heads < 1 || a->total < 0 || a->max_seqlen < 0) return JFA_ERR_INVALID_ARG;
+  if (a->head_dim != 128) return JFA_ERR_UNSUPPORTED;
+  if (!(a->v_descale > 0.f) || !std::isfinite(a->v_descale)) return JFA_ERR_INVALID_ARG;
+  const float inv = 1.0f / a->v_descale;
+  if (!std::isfinite(inv) || !(inv > 0.f)) return JFA_ERR_INVALID_ARG;
+  if (!aligned(a->offsets, 4)) return JFA_ERR_INVALID_ARG;
+  if (a->total > 0 && (!aligned(a->v, 16) || !aligned(a->vt, 16))) return JFA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(a->total) * a->heads * 128 >= (int64_t(1) << 40)) return JFA_ERR_INVALID_ARG;
+  const Layout L = self_layout(a->batch, a->heads, a->total, 128, false);
+  if (!aligned(ws, 256)) return JFA_ERR_INVALID_ARG;
+  if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(w);
+  if (launch_status_clear(status, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (a->batch == 0 || a->total == 0) return JFA_OK;
+  QueueParams qp{};  // every 128-key tile of every sequence and head, as the forward numbers them
+  qp.offsets = a->offsets;
+  qp.batch = a->batch;
+  qp.heads = a->heads;
+  qp.total = a->total;
+  qp.max_seqlen = a->max_seqlen;
+  qp.causal = 0;
+  qp.mode = kQueueSelfFwd;
+  qp.status = status;
+  qp.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base);
+  qp.items = reinterpret_cast<int4*>(w + L.items);
+  qp.item_seq = reinterpret_cast<int4*>(w + L.item_seq);
+  qp.max_items = static_cast<int32_t>(L.max_items);
+  qp.count_index = 2;
+  if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  return cuda_status(launch_vt_transpose(a->v, qp.items, qp.item_seq, status, a->heads, static_cast<int>(L.max_items),
+                                         a->vt, stream, &inv));
 }
 
 jfa_status jfa_fwd_fp8(const jfa_fwd_fp8_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
@@ -943,12 +989,13 @@ jfa_status jfa_fwd_fp8(const jfa_fwd_fp8_args* a, void* ws, size_t ws_bytes, cud
   for (float f : {a->q_descale, a->k_descale, a->v_descale})
     if (!(f > 0.f) || !std::isfinite(f)) return JFA_ERR_INVALID_ARG;
   if (!aligned(a->offsets, 4)) return JFA_ERR_INVALID_ARG;
-  if (a->total > 0 && (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->o, 16) ||
-                       !aligned(a->lse, 4)))
+  const bool own_vt = a->vt == nullptr;  // else the caller's blocks from jfa_fp8_quantize_v
+  if (a->total > 0 && (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(own_vt ? a->v : a->vt, 16) ||
+                       !aligned(a->o, 16) || !aligned(a->lse, 4)))
     return JFA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(a->total) * a->heads * 128 >= (int64_t(1) << 40)) return JFA_ERR_INVALID_ARG;
   size_t vt_off = 0;
-  const Layout L = fp8_layout(a->batch, a->heads, a->total, &vt_off);
+  const Layout L = fp8_layout(a->batch, a->heads, a->total, &vt_off, own_vt);
   if (!aligned(ws, 256) || !events_ok(a->main_kernel_events)) return JFA_ERR_INVALID_ARG;
   if (ws_bytes < L.bytes) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -972,9 +1019,9 @@ jfa_status jfa_fwd_fp8(const jfa_fwd_fp8_args* a, void* ws, size_t ws_bytes, cud
   qp.max_items = static_cast<int32_t>(L.max_items);
   qp.count_index = 2;
   if (launch_queue(qp, stream) != cudaSuccess) return JFA_ERR_CUDA;
-  uint8_t* vt = w + vt_off;
-  if (launch_vt_transpose(a->v, qp.items, qp.item_seq, status, a->heads, static_cast<int>(L.max_items), vt,
-                          stream) != cudaSuccess)
+  const void* vt = own_vt ? static_cast<const void*>(w + vt_off) : a->vt;
+  if (own_vt && launch_vt_transpose(a->v, qp.items, qp.item_seq, status, a->heads, static_cast<int>(L.max_items),
+                                    w + vt_off, stream) != cudaSuccess)
     return JFA_ERR_CUDA;
   CUtensorMap tq, tk, tvt;
   const uint64_t cols = static_cast<uint64_t>(a->heads) * 128;

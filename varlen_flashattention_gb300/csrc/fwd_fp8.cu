@@ -610,9 +610,11 @@ __device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t c,
   w[3] = __byte_perm(t2, t3, 0x7632);
 }
 
-// V (e4m3 [total, H, 128]) -> one [128 head-dim rows x 128 keys] block per key
-// tile and head: block (g * H + h) holds key tile g (tile_base numbering) of
-// head h, keys past the end of the sequence zero. In self-attention every
+// V (e4m3 [total, H, 128]; with QUANT, bf16 values quantized on the way to
+// e4m3(v * inv_descale), round to nearest even, saturating at +-448) -> one
+// [128 head-dim rows x 128 keys] block per key tile and head: block (g * H + h)
+// holds key tile g (tile_base numbering) of head h, keys past the end of the
+// sequence zero. In self-attention every
 // query tile is also a key tile, so the forward queue's items (head, tile,
 // sequence start and tile base) name the blocks; a few CTAs per SM walk them.
 // Per item: the 16 KB tile is read from global memory whole rows at a time
@@ -621,11 +623,14 @@ __device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t c,
 // of warp w takes keys 4 l .. 4 l + 3 at head-dim columns 16 w .. 16 w + 15
 // (one 16-byte read per key, conflict-free under that swizzle), transposes
 // 4 x 4 byte blocks in registers and writes 4 keys of 16 head-dim rows, so
-// every warp store is one contiguous 128-byte row of the block.
+// every warp store is one contiguous 128-byte row of the block. With QUANT a
+// lane reads the 32 bf16 bytes behind its 16 output bytes and converts them.
 constexpr int kVtThreads = 256;
+template <bool QUANT>
 __global__ void __launch_bounds__(kVtThreads) vt_transpose_kernel(const uint8_t* __restrict__ v, const int4* items,
                                                                   const int4* item_seq, const int32_t* status,
-                                                                  int heads, uint8_t* __restrict__ vt) {
+                                                                  int heads, float inv_descale,
+                                                                  uint8_t* __restrict__ vt) {
   __shared__ __align__(16) uint8_t tile[kTile * kF8D];
   wait_prior_grid();
   allow_next_grid();
@@ -643,7 +648,29 @@ __global__ void __launch_bounds__(kVtThreads) vt_transpose_kernel(const uint8_t*
     for (int m = 0; m < 4; ++m) {
       const int k = (lane >> 3) + 4 * w + 32 * m;
       g[m] = make_uint4(0, 0, 0, 0);
-      if (k < rows) g[m] = ptx::ld_nc_v4(v + ((static_cast<int64_t>(s0) + kTile * j + k) * heads + h) * kF8D + 16 * c);
+      if (k < rows) {
+        const int64_t e0 = ((static_cast<int64_t>(s0) + kTile * j + k) * heads + h) * kF8D + 16 * c;  // element
+        if constexpr (!QUANT) {
+          g[m] = ptx::ld_nc_v4(v + e0);
+        } else {
+          const uint4 lo = ptx::ld_nc_v4(v + 2 * e0), hi = ptx::ld_nc_v4(v + 2 * e0 + 16);  // 16 bf16 values
+          const uint32_t in[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+          uint32_t out[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t b[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const uint32_t x = in[2 * q + u];  // two bf16: element 2 (2q + u) in the low half
+              const float2 f = make_float2(__uint_as_float(x << 16) * inv_descale,
+                                           __uint_as_float(x & 0xffff0000u) * inv_descale);
+              b[u] = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);  // low byte: f.x
+            }
+            out[q] = b[0] | (b[1] << 16);
+          }
+          g[m] = make_uint4(out[0], out[1], out[2], out[3]);
+        }
+      }
     }
     __syncthreads();  // the previous item's reads of the tile are done
 #pragma unroll
@@ -688,13 +715,18 @@ cudaError_t launch_fp8_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }  // namespace
 
 cudaError_t launch_vt_transpose(const void* v, const int4* items, const int4* item_seq, const int32_t* status,
-                                int heads, int max_items, void* vt, cudaStream_t stream) {
+                                int heads, int max_items, void* vt, cudaStream_t stream, const float* inv_descale) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return cudaErrorInvalidValue;
   const int grid = std::max(1, std::min(max_items, 8 * sms));  // a few blocks per SM walk the items
-  return launch_after(vt_transpose_kernel, dim3(grid), dim3(kVtThreads), 0, stream, static_cast<const uint8_t*>(v),
-                      items, item_seq, static_cast<const int32_t*>(status), heads, static_cast<uint8_t*>(vt));
+  if (inv_descale)
+    return launch_after(vt_transpose_kernel<true>, dim3(grid), dim3(kVtThreads), 0, stream,
+                        static_cast<const uint8_t*>(v), items, item_seq, static_cast<const int32_t*>(status), heads,
+                        *inv_descale, static_cast<uint8_t*>(vt));
+  return launch_after(vt_transpose_kernel<false>, dim3(grid), dim3(kVtThreads), 0, stream,
+                      static_cast<const uint8_t*>(v), items, item_seq, static_cast<const int32_t*>(status), heads, 1.0f,
+                      static_cast<uint8_t*>(vt));
 }
 
 cudaError_t launch_fwd_fp8(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,

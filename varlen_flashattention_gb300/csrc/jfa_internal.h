@@ -193,8 +193,10 @@ cudaError_t launch_bwd_post(const float* acc, void* dq, int64_t n, float scale, 
 // [128 head-dim rows x 128 keys] blocks (block g * H + h = key tile g, head h;
 // tiles numbered by tile_base), one CTA per item of the self-attention forward
 // queue, then the forward over that queue.
+// inv_descale non-null: v is bf16, quantized on the way to e4m3(v * *inv_descale).
 cudaError_t launch_vt_transpose(const void* v, const int4* items, const int4* item_seq, const int32_t* status,
-                                int heads, int max_items, void* vt, cudaStream_t stream);
+                                int heads, int max_items, void* vt, cudaStream_t stream,
+                                const float* inv_descale = nullptr);
 cudaError_t launch_fwd_fp8(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
                            const CUtensorMap& to, const int4* items, const int4* item_seq, int32_t* status, void* o, float* lse, int heads,
                            int total, float s_log2, float v_descale, uint64_t budget_ns, int grid,
