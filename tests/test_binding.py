@@ -173,3 +173,18 @@ def test_well_formed_host_buffers_reach_the_device_check():
     for call in calls:
         with pytest.raises(ValueError, match="must be on a CUDA device"):
             call()
+
+
+def test_fp8_vt_and_quantize_v_reject_mismatched_shapes():
+    u8 = torch.uint8
+    q = torch.zeros(10, 2, 128, dtype=u8)
+    off = torch.tensor([0, 4, 10], dtype=i32)
+    with pytest.raises(ValueError, match="vt must have shape"):  # the blocks of 2 sequences x 2 heads
+        jfa.jfa_fwd_fp8(q, q, None, off, 8, 1.0, 1.0, 1.0, vt=torch.zeros(100, dtype=u8))
+    with pytest.raises(TypeError, match="v must be torch.bfloat16"):
+        jfa.jfa_fp8_quantize_v(q, off, 8, 1.0)
+    v = torch.zeros(10, 2, 128, dtype=bf16)
+    with pytest.raises(ValueError, match="vt must have shape"):
+        jfa.jfa_fp8_quantize_v(v, off, 8, 1.0, vt=torch.zeros(7, dtype=u8))
+    with pytest.raises(ValueError, match="must be on a CUDA device"):
+        jfa.jfa_fp8_quantize_v(v, off, 8, 1.0)
