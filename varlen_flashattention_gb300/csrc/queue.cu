@@ -293,8 +293,8 @@ __global__ void __launch_bounds__(kQThreads) build_queue_kernel(const QueueParam
 
   // 4. place the items: within a bucket ascending (b, tile, h). When all tiles
   // of a sequence share one cost, the bucket pass only records where each
-  // sequence starts and every thread then writes its own sequences' items,
-  // so that one large bucket is not written by one warp.
+  // sequence starts, and the records are then written by every warp for its
+  // own sequences (below), so that one large bucket is not written by one warp.
   const bool one_cost = !p.causal;  // the broadcast modes are never causal
   // The items fit the queue (checked once here; every write below is in range).
   const bool fits = static_cast<int64_t>(total_tiles) * p.heads <= p.max_items;
